@@ -1,0 +1,111 @@
+"""Seeded synthetic inputs for the affine group-quantized matmul.
+
+This module only draws random inputs; it holds none of the method's arithmetic
+(no unpacking, no dequantization, no dot products).  Both the CUDA path and the
+CPU oracle consume what it returns, so the two sides always see identical bytes.
+
+Recipe (one case = one weight matrix W[N,K] plus an activation x[M,K]):
+
+* packed codes: ``N * K * bits / 32`` uint32 words, each word uniform over
+  [0, 2^32).  For 4-bit codes this is exactly "every code uniform in [0, 15]"
+  (eight independent nibbles per word); for 8-bit codes, every code uniform in
+  [0, 255].
+* scales: bf16(U(0.004, 0.02)), one per group of ``group_size`` along K.
+* biases: bf16(-7.5 * scale + N(0, 0.002)), with ``scale`` the bf16 value, so
+  that the dequantized weights are centred near zero.
+* x: bf16(N(0, 1)).
+
+bf16 values are returned as their uint16 bit patterns.  The bf16 rounding here
+is round-to-nearest-even from float32 (numpy rounds float64 -> float32 first);
+this double rounding only shapes the input distribution, never a result.
+
+Random streams: ``numpy.random.Philox`` keyed through
+``SeedSequence([seed, stream])``; stream 0 draws the weights (codes, then
+scales, then bias noise), stream 1 draws x.  The seed of matrix j of layer l of
+workload c is ``1000*c + 16*l + j``; the tiny correctness case uses seed 0.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+STREAM_WEIGHTS = 0
+STREAM_X = 1
+
+
+def _rng(seed: int, stream: int) -> np.random.Generator:
+    return np.random.Generator(np.random.Philox(np.random.SeedSequence([int(seed), int(stream)])))
+
+
+def f32_to_bf16_bits(a) -> np.ndarray:
+    """Round float32 values to bf16 (nearest, ties to even); return uint16 bit patterns."""
+    f = np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+    u = f.view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return r.astype(np.uint16)
+
+
+def bf16_bits_to_f32(h) -> np.ndarray:
+    """Widen bf16 bit patterns (uint16) to float32 exactly."""
+    h = np.ascontiguousarray(np.asarray(h, dtype=np.uint16))
+    return (h.astype(np.uint32) << 16).view(np.float32)
+
+
+@dataclasses.dataclass
+class QuantWeights:
+    """A packed weight matrix: ``w_packed`` uint32[N, K*bits/32], ``scales``/``biases``
+    bf16 bit patterns uint16[N, K/group_size]."""
+
+    w_packed: np.ndarray
+    scales: np.ndarray
+    biases: np.ndarray
+    N: int
+    K: int
+    group_size: int
+    bits: int
+
+    @property
+    def nbytes(self) -> int:
+        return self.w_packed.nbytes + self.scales.nbytes + self.biases.nbytes
+
+
+def make_weights(N: int, K: int, seed: int, group_size: int = 64, bits: int = 4) -> QuantWeights:
+    """Draw a packed weight matrix W[N,K] with the recipe in the module docstring."""
+    if K % group_size or (K * bits) % 32:
+        raise ValueError("K must be a multiple of group_size and of 32/bits")
+    rng = _rng(seed, STREAM_WEIGHTS)
+    words = K * bits // 32
+    w_packed = rng.integers(0, 1 << 32, size=(N, words), dtype=np.uint32)
+    G = K // group_size
+    s = f32_to_bf16_bits(rng.uniform(0.004, 0.02, size=(N, G)))
+    noise = rng.normal(0.0, 0.002, size=(N, G))
+    b = f32_to_bf16_bits(-7.5 * bf16_bits_to_f32(s).astype(np.float64) + noise)
+    return QuantWeights(w_packed, s, b, N, K, group_size, bits)
+
+
+def make_x(M: int, K: int, seed: int) -> np.ndarray:
+    """Draw activations x[M,K] = bf16(N(0,1)) as uint16 bit patterns."""
+    rng = _rng(seed, STREAM_X)
+    return f32_to_bf16_bits(rng.standard_normal((M, K)))
+
+
+def seed_for(config: int, layer: int = 0, matrix: int = 0) -> int:
+    """Seed of matrix ``matrix`` of layer ``layer`` in workload ``config`` (1-based)."""
+    if config == 1:
+        return 0
+    return 1000 * config + 16 * layer + matrix
+
+
+# Llama-3.1-8B-shaped decode layer, (name, N, K): q, k, v, o, gate, up, down.
+LLAMA8B_LAYER = (
+    ("q_proj", 4096, 4096),
+    ("k_proj", 1024, 4096),
+    ("v_proj", 1024, 4096),
+    ("o_proj", 4096, 4096),
+    ("gate_proj", 14336, 4096),
+    ("up_proj", 14336, 4096),
+    ("down_proj", 4096, 14336),
+)
+LLAMA8B_LM_HEAD = ("lm_head", 128256, 4096)
+LLAMA8B_LAYERS = 32
