@@ -1,0 +1,168 @@
+"""ctypes binding of libaq.so: the same names as the C ABI, argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; there is no
+Python or CPU fallback.  If the library has not been built this module raises
+on first use.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+from ._build import INCLUDE, LIB
+
+AQ_OK = 0
+AQ_ERR_INVALID_ARG = 1
+AQ_ERR_UNSUPPORTED = 2
+AQ_ERR_ALIGNMENT = 3
+AQ_ERR_CUDA = 4
+AQ_ERR_TIMEOUT = 5
+
+AQ_KERNEL_AUTO = 0
+AQ_KERNEL_QMV = 1
+AQ_KERNEL_QMM = 2
+
+AQ_FLAG_PDL = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AqError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = f"{where} failed: {status_string(status)}"
+        if status == AQ_ERR_CUDA:
+            msg += f" ({last_cuda_error()})"
+        super().__init__(msg)
+
+
+def library_path() -> str:
+    return LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load libaq.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB):
+                raise RuntimeError(f"libaq.so is not built ({LIB}); run __graft_entry__.build()")
+            lib = ctypes.CDLL(LIB)
+            P, I64, I, U = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint
+            lib.aq_matmul_bf16.argtypes = [P, P, P, P, P, I64, I64, I64, I, I, P]
+            lib.aq_matmul_bf16.restype = I
+            lib.aq_matmul_bf16_ex.argtypes = [P, P, P, P, P, I64, I64, I64, I, I, I, U, P]
+            lib.aq_matmul_bf16_ex.restype = I
+            lib.aq_quantize_ref.argtypes = [P, I64, I64, I, I, P, P, P]
+            lib.aq_quantize_ref.restype = I
+            lib.aq_pack_ref.argtypes = [P, I64, I64, I, P]
+            lib.aq_pack_ref.restype = I
+            lib.aq_status_string.argtypes = [I]
+            lib.aq_status_string.restype = ctypes.c_char_p
+            lib.aq_last_cuda_error.argtypes = []
+            lib.aq_last_cuda_error.restype = ctypes.c_char_p
+            lib.aq_version.argtypes = []
+            lib.aq_version.restype = I
+            _lib = lib
+    return _lib
+
+
+def declared_functions() -> list[str]:
+    """Names of the functions include/aq.h declares."""
+    names = []
+    for path in sorted(os.listdir(INCLUDE)):
+        if path.endswith(".h"):
+            text = open(os.path.join(INCLUDE, path)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"\b(aq_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+# ---------------------------------------------------------------- raw C-ABI names
+
+def aq_matmul_bf16(x, w_packed, scales, biases, y, M, N, K, group_size, bits, stream) -> int:
+    return load().aq_matmul_bf16(x, w_packed, scales, biases, y, M, N, K, group_size, bits, stream)
+
+
+def aq_matmul_bf16_ex(x, w_packed, scales, biases, y, M, N, K, group_size, bits, kernel, flags, stream) -> int:
+    return load().aq_matmul_bf16_ex(x, w_packed, scales, biases, y, M, N, K, group_size, bits, kernel, flags,
+                                    stream)
+
+
+def aq_quantize_ref(w, N, K, group_size, bits, w_packed, scales_bf16, biases_bf16) -> int:
+    return load().aq_quantize_ref(w, N, K, group_size, bits, w_packed, scales_bf16, biases_bf16)
+
+
+def aq_pack_ref(codes, N, K, bits, w_packed) -> int:
+    return load().aq_pack_ref(codes, N, K, bits, w_packed)
+
+
+def status_string(status: int) -> str:
+    return load().aq_status_string(status).decode()
+
+
+def last_cuda_error() -> str:
+    return load().aq_last_cuda_error().decode()
+
+
+def version() -> int:
+    return load().aq_version()
+
+
+# ---------------------------------------------------------------- torch / numpy helpers
+
+_KERNELS = {"auto": AQ_KERNEL_AUTO, "qmv": AQ_KERNEL_QMV, "qmm": AQ_KERNEL_QMM}
+
+
+def matmul(x, w_packed, scales, biases, out=None, *, group_size: int = 64, bits: int = 4,
+           kernel: str = "auto", pdl: bool = False, stream=None):
+    """y = x . dequant(W)^T for torch CUDA tensors (x bf16 [M,K]; w_packed int32/uint32
+    [N, K*bits/32]; scales/biases bf16 [N, K/group_size]).  Returns y bf16 [M, N]."""
+    import torch
+
+    M, K = x.shape
+    N = w_packed.shape[0]
+    for name, t in (("x", x), ("w_packed", w_packed), ("scales", scales), ("biases", biases)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    st = aq_matmul_bf16_ex(x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(), biases.data_ptr(),
+                           out.data_ptr(), M, N, K, group_size, bits, _KERNELS[kernel],
+                           AQ_FLAG_PDL if pdl else 0, stream.cuda_stream)
+    if st != AQ_OK:
+        raise AqError(st, "aq_matmul_bf16_ex")
+    return out
+
+
+def quantize_ref(w, group_size: int = 64, bits: int = 4):
+    """Host min-max quantization of a float32 numpy array [N, K] (library's aq_quantize_ref)."""
+    import numpy as np
+
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    N, K = w.shape
+    wp = np.empty((N, K * bits // 32), np.uint32)
+    s = np.empty((N, K // group_size), np.uint16)
+    b = np.empty((N, K // group_size), np.uint16)
+    st = aq_quantize_ref(w.ctypes.data, N, K, group_size, bits, wp.ctypes.data, s.ctypes.data, b.ctypes.data)
+    if st != AQ_OK:
+        raise AqError(st, "aq_quantize_ref")
+    return wp, s, b
+
+
+def pack_ref(codes, bits: int = 4):
+    """Host packing of uint8 codes [N, K] (library's aq_pack_ref)."""
+    import numpy as np
+
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    N, K = codes.shape
+    wp = np.empty((N, K * bits // 32), np.uint32)
+    st = aq_pack_ref(codes.ctypes.data, N, K, bits, wp.ctypes.data)
+    if st != AQ_OK:
+        raise AqError(st, "aq_pack_ref")
+    return wp

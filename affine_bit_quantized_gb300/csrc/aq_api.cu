@@ -1,0 +1,201 @@
+// C ABI of libaq: argument validation, kernel choice and the host utilities.
+//
+// Validation happens before any CUDA runtime call, so a rejected call never
+// touches the device (the boundary behaviour asked for by the "MLX CUDA
+// Cleanup Plan" page: small wrappers for status handling, no hidden
+// fallbacks, no extra copies or synchronization).
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "../../include/aq.h"
+#include "aq_internal.h"
+
+namespace {
+
+thread_local char g_last_cuda_error[256] = "";
+
+aq_status record_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return AQ_OK;
+    std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s", cudaGetErrorName(e),
+                  cudaGetErrorString(e));
+    return AQ_ERR_CUDA;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+constexpr int64_t kMaxDim = (int64_t)1 << 30;  // keeps every per-row index inside 32 bits
+constexpr int kQmvMaxRows = 16;                // rows of x per weight-streaming pass
+
+aq_status validate(const void *x, const uint32_t *w, const void *s, const void *b, void *y,
+                   int64_t M, int64_t N, int64_t K, int group_size, int bits) {
+    if (M < 0 || N < 0 || K < 0) return AQ_ERR_INVALID_ARG;
+    if (bits != 4 || group_size != 64) return AQ_ERR_UNSUPPORTED;
+    if (K % group_size) return AQ_ERR_INVALID_ARG;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return AQ_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return AQ_OK;
+    if (!y) return AQ_ERR_INVALID_ARG;
+    if (K == 0) return AQ_OK;
+    if (!x || !w || !s || !b) return AQ_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(w, 16) || !aligned(s, 2) || !aligned(b, 2) || !aligned(y, 2))
+        return AQ_ERR_ALIGNMENT;
+    return AQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+aq_status aq_matmul_bf16_ex(const void *x, const uint32_t *w_packed, const void *scales,
+                            const void *biases, void *y, int64_t M, int64_t N, int64_t K,
+                            int group_size, int bits, int kernel, unsigned flags, void *stream) {
+    if (kernel != AQ_KERNEL_AUTO && kernel != AQ_KERNEL_QMV && kernel != AQ_KERNEL_QMM)
+        return AQ_ERR_INVALID_ARG;
+    if (flags & ~(unsigned)AQ_FLAG_PDL) return AQ_ERR_INVALID_ARG;
+    aq_status st = validate(x, w_packed, scales, biases, y, M, N, K, group_size, bits);
+    if (st != AQ_OK || M == 0 || N == 0) return st;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (K == 0) return record_cuda(cudaMemsetAsync(y, 0, (size_t)(M * N) * 2, cs));
+
+    if (kernel == AQ_KERNEL_QMM) return AQ_ERR_UNSUPPORTED;
+
+    aq::MatmulArgs a;
+    a.w = w_packed;
+    a.scales = static_cast<const uint16_t *>(scales);
+    a.biases = static_cast<const uint16_t *>(biases);
+    a.N = N;
+    a.K = K;
+    a.pdl = (flags & AQ_FLAG_PDL) != 0;
+    a.stream = cs;
+    // Weight-streaming passes over at most 16 rows of x each.
+    for (int64_t m0 = 0; m0 < M; m0 += kQmvMaxRows) {
+        a.x = static_cast<const uint16_t *>(x) + m0 * K;
+        a.y = static_cast<uint16_t *>(y) + m0 * N;
+        a.M = (M - m0) < kQmvMaxRows ? (M - m0) : kQmvMaxRows;
+        st = record_cuda(aq::launch_qmv(a));
+        if (st != AQ_OK) return st;
+    }
+    return AQ_OK;
+}
+
+aq_status aq_matmul_bf16(const void *x, const uint32_t *w_packed, const void *scales,
+                         const void *biases, void *y, int64_t M, int64_t N, int64_t K,
+                         int group_size, int bits, void *stream) {
+    return aq_matmul_bf16_ex(x, w_packed, scales, biases, y, M, N, K, group_size, bits,
+                             AQ_KERNEL_AUTO, 0u, stream);
+}
+
+// ---------------------------------------------------------------- host utilities
+
+namespace {
+
+// Nearest-even rounding of a double to bf16 by integer arithmetic on its
+// significand: keep 8 significant bits (fewer below 2^-126, where bf16 has
+// a fixed spacing of 2^-133), round on the dropped bits.
+uint16_t bf16_from_double(double v) {
+    uint64_t u;
+    std::memcpy(&u, &v, sizeof u);
+    const uint16_t sign = (uint16_t)((u >> 48) & 0x8000u);
+    const uint64_t mag = u & 0x7FFFFFFFFFFFFFFFull;
+    const int biased = (int)(mag >> 52);
+    if (biased == 0x7FF) return (mag & 0xFFFFFFFFFFFFFull) ? (uint16_t)(sign | 0x7FC0u) : (uint16_t)(sign | 0x7F80u);
+    if (biased == 0) return sign;  // zero or a double subnormal, far below half the least bf16
+    const int e = biased - 1023;   // |v| = sig * 2^(e - 52), sig in [2^52, 2^53)
+    const uint64_t sig = (mag & 0xFFFFFFFFFFFFFull) | (1ull << 52);
+    const int unit = e >= -126 ? e - 7 : -133;  // exponent of the bf16 spacing at |v|
+    const int drop = 52 + unit - e;             // significand bits below that spacing
+    if (drop > 54) return sign;                 // below a quarter of the least spacing
+    uint64_t kept = sig >> drop;
+    const uint64_t rest = sig & ((1ull << drop) - 1);
+    const uint64_t half = 1ull << (drop - 1);
+    if (rest > half || (rest == half && (kept & 1))) ++kept;
+    const float f = std::ldexp((float)kept, unit);  // exact, or inf on overflow
+    uint32_t fb;
+    std::memcpy(&fb, &f, sizeof fb);
+    return (uint16_t)(sign | (fb >> 16));
+}
+
+double double_from_bf16(uint16_t h) {
+    const uint32_t fb = (uint32_t)h << 16;
+    float f;
+    std::memcpy(&f, &fb, sizeof f);
+    return f;
+}
+
+}  // namespace
+
+aq_status aq_pack_ref(const uint8_t *codes, int64_t N, int64_t K, int bits, uint32_t *w_packed) {
+    if (bits != 4 && bits != 8) return AQ_ERR_UNSUPPORTED;
+    if (N < 0 || K < 0 || K % (32 / bits)) return AQ_ERR_INVALID_ARG;
+    if (N * K == 0) return AQ_OK;
+    if (!codes || !w_packed) return AQ_ERR_INVALID_ARG;
+    const int per = 32 / bits;
+    const unsigned limit = 1u << bits;
+    for (int64_t i = 0; i < N * K; ++i)
+        if (codes[i] >= limit) return AQ_ERR_INVALID_ARG;
+    const int64_t nwords = N * K / per;
+    for (int64_t wi = 0; wi < nwords; ++wi) {
+        uint32_t word = 0;
+        const uint8_t *c = codes + wi * per;  // rows are whole words, so words never straddle rows
+        for (int p = per - 1; p >= 0; --p) word = (word << bits) | c[p];
+        w_packed[wi] = word;
+    }
+    return AQ_OK;
+}
+
+aq_status aq_quantize_ref(const float *w, int64_t N, int64_t K, int group_size, int bits,
+                          uint32_t *w_packed, uint16_t *scales_bf16, uint16_t *biases_bf16) {
+    if (bits != 4 && bits != 8) return AQ_ERR_UNSUPPORTED;
+    if (group_size <= 0 || N < 0 || K <= 0 || K % group_size || K % (32 / bits))
+        return AQ_ERR_INVALID_ARG;
+    if (N == 0) return AQ_OK;
+    if (!w || !w_packed || !scales_bf16 || !biases_bf16) return AQ_ERR_INVALID_ARG;
+    const int top = (1 << bits) - 1;
+    const int64_t G = K / group_size;
+    std::vector<uint8_t> codes((size_t)K);
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t g = 0; g < G; ++g) {
+            const float *seg = w + n * K + g * group_size;
+            float lo = seg[0], hi = seg[0];
+            for (int i = 1; i < group_size; ++i) {
+                lo = seg[i] < lo ? seg[i] : lo;
+                hi = seg[i] > hi ? seg[i] : hi;
+            }
+            const uint16_t s16 = bf16_from_double(((double)hi - (double)lo) / (double)top);
+            const uint16_t b16 = bf16_from_double((double)lo);
+            scales_bf16[n * G + g] = s16;
+            biases_bf16[n * G + g] = b16;
+            const double s = double_from_bf16(s16), b = double_from_bf16(b16);
+            for (int i = 0; i < group_size; ++i) {
+                int q = 0;
+                if (s != 0.0) {
+                    const double t = std::nearbyint(((double)seg[i] - b) / s);
+                    q = t < 0.0 ? 0 : (t > (double)top ? top : (int)t);
+                }
+                codes[(size_t)(g * group_size + i)] = (uint8_t)q;
+            }
+        }
+        aq_status st = aq_pack_ref(codes.data(), 1, K, bits, w_packed + n * (K * bits / 32));
+        if (st != AQ_OK) return st;
+    }
+    return AQ_OK;
+}
+
+const char *aq_status_string(aq_status status) {
+    switch (status) {
+    case AQ_OK: return "AQ_OK";
+    case AQ_ERR_INVALID_ARG: return "AQ_ERR_INVALID_ARG";
+    case AQ_ERR_UNSUPPORTED: return "AQ_ERR_UNSUPPORTED";
+    case AQ_ERR_ALIGNMENT: return "AQ_ERR_ALIGNMENT";
+    case AQ_ERR_CUDA: return "AQ_ERR_CUDA";
+    case AQ_ERR_TIMEOUT: return "AQ_ERR_TIMEOUT";
+    }
+    return "AQ_ERR_UNKNOWN";
+}
+
+const char *aq_last_cuda_error(void) { return g_last_cuda_error; }
+
+int aq_version(void) { return 100; }
+
+}  // extern "C"

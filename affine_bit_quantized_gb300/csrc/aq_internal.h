@@ -1,0 +1,28 @@
+// Internal declarations shared by the libaq translation units (not installed).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace aq {
+
+// Arguments of one y = x . dequant(W)^T launch, already validated.
+struct MatmulArgs {
+    const void *x;           // bf16 [M, K]
+    const uint32_t *w;       // uint32 [N, K/8]
+    const uint16_t *scales;  // bf16 bits [N, K/64]
+    const uint16_t *biases;  // bf16 bits [N, K/64]
+    void *y;                 // bf16 [M, N]
+    int64_t M, N, K;
+    bool pdl;                // launch with programmatic stream serialization
+    cudaStream_t stream;
+};
+
+// Weight-streaming kernel for up to 16 rows of x (qmv.cu).  Requires
+// 1 <= M <= 16, N >= 1, K >= 64.
+cudaError_t launch_qmv(const MatmulArgs &a);
+
+// Tensor-core kernel (qmm.cu).  Requires M >= 1, N >= 1, K >= 64.
+cudaError_t launch_qmm(const MatmulArgs &a);
+
+}  // namespace aq

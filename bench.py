@@ -1,0 +1,439 @@
+#!/usr/bin/env python
+"""Benchmark: a Llama-3.1-8B-shaped decode step of the affine group-quantized matmul.
+
+One step = every weight matrix of 32 decoder layers (q, k, v, o, gate, up,
+down; 4-bit codes, group 64, bf16 scales and biases, each layer drawn from its
+own seed) plus lm_head, each multiplied by one bf16 activation row (M = 1).
+That is 4.22 GB of weights streamed per step, far larger than the 129 MB L2,
+so consecutive steps never hit in L2.  The step is captured once into a CUDA
+graph (kernels chained with programmatic dependent launch) and replayed.
+
+Prints one JSON line.  `value` is the achieved algorithmic HBM bandwidth of
+the step in GB/s (bytes the definition must read and write: packed codes,
+scales, biases, x and y), summed over ranks; `tok_s` is the equivalent decode
+rate; the `qmm` object gives the prefill-sized tensor-core GEMM's TFLOPS on
+the 4096x14336 / 14336x4096 shapes at M = 256 and 2048.
+
+--impl reference times the CPU oracle (the plain fp64 definition) on a bounded
+sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from affine_bit_quantized_gb300 import synth  # noqa: E402
+
+METRIC = "qmv achieved HBM GB/s (% of GB300 peak) and 8B-shape equiv decode tok/s; qmm TFLOPS"
+WORKLOAD = ("llama-3.1-8b-shaped decode step: 32 layers x (q,k,v,o,gate,up,down) + lm_head, "
+            "M=1, 4-bit affine codes, group 64, bf16 scales/biases")
+CONFIG_ID = 4          # seeds of the full decode step
+N_ROLES = 4            # activations per layer: attention in, attention out, MLP in, MLP activation
+ROLE_OF = {"q_proj": 0, "k_proj": 0, "v_proj": 0, "o_proj": 1, "gate_proj": 2, "up_proj": 2, "down_proj": 3}
+QMM_SHAPES = ((4096, 14336, "gate/up"), (14336, 4096, "down"))   # (K, N)
+QMM_M = (256, 2048)
+
+
+def alg_bytes(M: int, N: int, K: int) -> int:
+    """Bytes the definition must move: codes (K/2 per row), scales and biases
+    (2 x 2 bytes per group of 64), x and y."""
+    return N * K // 2 + N * (K // 64) * 4 + 2 * M * K + 2 * M * N
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        sm, smax, power, reasons = [], [], [], set()
+        for line in self.file.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        os.unlink(self.file.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workload
+
+def step_matrices(layers: int):
+    """(layer, j, name, N, K, seed) for every matrix of the step, in launch order."""
+    out = []
+    for layer in range(layers):
+        for j, (name, N, K) in enumerate(synth.LLAMA8B_LAYER):
+            out.append((layer, j, name, N, K, synth.seed_for(CONFIG_ID, layer, j)))
+    name, N, K = synth.LLAMA8B_LM_HEAD
+    out.append((layers, 0, name, N, K, synth.seed_for(CONFIG_ID, layers, 0)))
+    return out
+
+
+def x_layout(layers: int):
+    """Offsets (in elements) of each activation row inside one contiguous x buffer."""
+    offs, pos = {}, 0
+    for layer in range(layers):
+        for role, K in enumerate((4096, 4096, 4096, 14336)):
+            offs[(layer, role)] = (pos, K, synth.seed_for(CONFIG_ID, layer, 8 + role))
+            pos += K
+    offs[(layers, 0)] = (pos, 4096, synth.seed_for(CONFIG_ID, layers, 8))
+    pos += 4096
+    return offs, pos
+
+
+def run_reference(args, target_seconds: float = 150.0):
+    """CPU oracle on a bounded sample of the decode step: the first R rows of
+    each of the 7 matrices of one layer per step, R sized so that warm-up plus
+    timed steps take about `target_seconds` on this host's cores."""
+    import oracle
+
+    mats = [m for m in step_matrices(1) if m[2] != "lm_head"]
+    offs, _ = x_layout(1)
+    full = []
+    for (layer, j, name, N, K, seed) in mats:
+        w = synth.make_weights(N, K, seed)
+        full.append((synth.make_x(1, K, offs[(layer, ROLE_OF[name])][2]), w, N, K))
+    threads = oracle.default_threads()
+
+    def run_rows(R):
+        for x, w, N, K in full:
+            r = min(R, N)
+            oracle.matmul(x, w.w_packed[:r], w.scales[:r], w.biases[:r], 1, r, K, nthreads=threads)
+
+    t0 = time.perf_counter()
+    run_rows(64)
+    per_row = (time.perf_counter() - t0) / 64
+    budget = target_seconds / (args.steps + args.warmup)
+    R = int(max(8, min(1024, budget / max(per_row, 1e-9))))
+    step_bytes = sum(alg_bytes(1, min(R, N), K) for (_, _, N, K) in full)
+    for _ in range(args.warmup):
+        run_rows(R)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run_rows(R)
+    dt = (time.perf_counter() - t0) / args.steps
+    gbs = step_bytes / dt / 1e9
+    sample = (f"first {R} rows of each of the 7 matrices of one 8B-shaped decode layer per step "
+              f"({sum(min(R, N) * K for (_, _, N, K) in full) / 1e6:.1f} M weights), M=1, fp64")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": sample, "M": 1},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("qmv.cu",):
+        with open(os.path.join(ROOT, "affine_bit_quantized_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic():
+    """Per-step DRAM bytes from the committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "qmv_decode_step_dram_traffic.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha256_16") != kernel_source_hash():
+            return None
+        return float(kv["dram_bytes_per_step"])
+    except Exception:
+        return None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--layers", type=int, default=32, help="decoder layers in the step (32 = the workload)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import affine_bit_quantized_gb300 as aq
+    from affine_bit_quantized_gb300 import _build
+
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    _build.build_library()
+    lib = aq.load()
+
+    hbm_peak, bf16_peak, bf16_sus, peak_src = load_peaks()
+
+    # ---- workload (generated on the host from the seeded recipe, uploaded once)
+    mats = step_matrices(args.layers)
+    offs, x_elems = x_layout(args.layers)
+    pool = ThreadPoolExecutor(max(1, min(16, os.cpu_count() or 1)))
+    weights = {}
+    host_keep = {}
+    cpu_layers = {0, 1} if (rank == 0 and world == 1 and not args.no_cpu_baseline) else set()
+
+    def gen(m):
+        layer, j, name, N, K, seed = m
+        return m, synth.make_weights(N, K, seed)
+
+    for m, w in pool.map(gen, mats):
+        layer, j, name, N, K, seed = m
+        weights[(layer, j)] = (torch.from_numpy(w.w_packed.view(np.int32)).to(dev),
+                               torch.from_numpy(w.scales.view(np.int16)).to(dev),
+                               torch.from_numpy(w.biases.view(np.int16)).to(dev))
+        if layer in cpu_layers:
+            host_keep[(layer, j)] = w
+    x_host = np.empty(x_elems, np.uint16)
+    for (layer, role), (pos, K, seed) in offs.items():
+        x_host[pos:pos + K] = synth.make_x(1, K, seed)[0]
+    x_pinned = torch.from_numpy(x_host.view(np.int16)).pin_memory()
+    x_dev = x_pinned.to(dev)
+    y_offs, pos = [], 0
+    for m in mats:
+        y_offs.append(pos)
+        pos += m[3]
+    y_dev = torch.empty(pos, dtype=torch.int16, device=dev)
+    logits_pinned = torch.empty(mats[-1][3], dtype=torch.int16).pin_memory()
+    step_bytes = sum(alg_bytes(1, N, K) for (_, _, _, N, K, _) in mats)
+    launches = []
+    for i, (layer, j, name, N, K, seed) in enumerate(mats):
+        role = 0 if name == "lm_head" else ROLE_OF[name]
+        xo = offs[(layer, role)][0]
+        wt, st, bt = weights[(layer, j)]
+        launches.append((x_dev.data_ptr() + 2 * xo, wt.data_ptr(), st.data_ptr(), bt.data_ptr(),
+                         y_dev.data_ptr() + 2 * y_offs[i], 1, N, K))
+
+    def enqueue(stream_handle, sel=None):
+        for i, (xp, wp, sp, bp, yp, M, N, K) in enumerate(launches):
+            if sel is not None and i not in sel:
+                continue
+            st = lib.aq_matmul_bf16_ex(xp, wp, sp, bp, yp, M, N, K, 64, 4, aq.AQ_KERNEL_AUTO, aq.AQ_FLAG_PDL,
+                                       stream_handle)
+            if st != aq.AQ_OK:
+                raise aq.AqError(st, "aq_matmul_bf16_ex")
+
+    # ---- capture the step
+    cap_stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(cap_stream):
+        enqueue(cap_stream.cuda_stream)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap_stream):
+        enqueue(cap_stream.cuda_stream)
+    torch.cuda.synchronize(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def max_over_ranks(v: float) -> float:
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    gpu_id = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+    clocks = ClockSampler(gpu_id)
+
+    # ---- device-resident timing (value)
+    cur = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        graph.replay()
+    barrier()
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cur)
+    for _ in range(args.steps):
+        graph.replay()
+    e1.record(cur)
+    e1.synchronize()
+    clk = clocks.stop()
+    barrier()
+    ms_step = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+
+    # ---- end to end: inputs copied in from pinned host memory, logits read back, every step
+    h2d = x_pinned.numel() * 2
+    d2h = logits_pinned.numel() * 2
+    logits_dev = y_dev[y_offs[-1]:y_offs[-1] + mats[-1][3]]
+
+    def e2e_step():
+        x_dev.copy_(x_pinned, non_blocking=True)
+        graph.replay()
+        logits_pinned.copy_(logits_dev, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier()
+    e0.record(cur)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(cur)
+    e1.synchronize()
+    barrier()
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+
+    # ---- per-matrix kernel times (the 32 layer copies of each shape back to back)
+    per_matrix = {}
+    reps = 5
+    for j, (name, N, K) in enumerate(synth.LLAMA8B_LAYER + (synth.LLAMA8B_LM_HEAD,)):
+        sel = {i for i, m in enumerate(mats) if (m[2] == name)}
+        for _ in range(2):
+            enqueue(cur.cuda_stream, sel)
+        torch.cuda.synchronize(dev)
+        e0.record(cur)
+        for _ in range(reps):
+            enqueue(cur.cuda_stream, sel)
+        e1.record(cur)
+        e1.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (reps * len(sel))
+        per_matrix[name] = {"N": N, "K": K, "us_per_call": round(us, 3),
+                            "gbs": round(alg_bytes(1, N, K) / (us * 1e-6) / 1e9, 1)}
+
+    # ---- CPU baseline: the oracle on two layers of the same workload, host cores
+    cpu = None
+    if cpu_layers:
+        import oracle
+        threads = oracle.default_threads()
+        done_bytes, t0 = 0, time.perf_counter()
+        for (layer, j), w in sorted(host_keep.items()):
+            name = synth.LLAMA8B_LAYER[j][0]
+            xo, K, xseed = offs[(layer, ROLE_OF[name])]
+            x = x_host[xo:xo + K].reshape(1, K)
+            oracle.matmul(x, w.w_packed, w.scales, w.biases, 1, w.N, w.K, nthreads=threads)
+            done_bytes += alg_bytes(1, w.N, w.K)
+        dt = time.perf_counter() - t0
+        cpu = {"value": round(done_bytes / dt / 1e9, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"layers 0-1 of the step ({len(host_keep)} matrices, "
+                         f"{sum(w.N * w.K for w in host_keep.values()) / 1e6:.0f} M weights), M=1, fp64",
+               "seconds": round(dt, 2)}
+
+    gbs = world * step_bytes / (ms_step * 1e-3) / 1e9
+    gbs_e2e = world * step_bytes / (ms_e2e * 1e-3) / 1e9
+    traffic = committed_traffic()
+    line = {
+        "metric": METRIC,
+        "value": round(gbs, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "layers": args.layers, "M": 1, "bytes_per_step": step_bytes,
+                   "launches_per_step": len(launches), "graph": "CUDA graph, programmatic dependent launch",
+                   "l2": "inputs larger than L2 (4.22 GB of weights per step vs 129 MB L2)",
+                   "parallelism": f"replicas x{world}"},
+        "tok_s": round(world * 1e3 / ms_step, 1),
+        "pct_of_hbm_peak": round(100 * gbs / world / hbm_peak, 1),
+        "roofline": {"bound": "hbm", "achieved": round(step_bytes / (ms_step * 1e-3) / 1e9, 1), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(step_bytes / (ms_step * 1e-3) / 1e9 / hbm_peak, 4),
+                     "traffic": traffic, "kernel": "qmv_kernel (every launch of the step)",
+                     "peak_source": f"{peak_src} hbm_gbs (copy)"},
+        "e2e": {"value": round(gbs_e2e, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(ms_e2e, 5)},
+        "gpu_launches": args.steps * len(launches),
+        "clocks": clk,
+        "per_matrix": per_matrix,
+    }
+    if cpu:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

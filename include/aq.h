@@ -1,0 +1,138 @@
+/*
+ * aq.h -- C ABI of libaq, the affine group-quantized matmul for NVIDIA GB300
+ * (sm_103a).
+ *
+ * The operation is the one the "MLX CUDA Cleanup Plan" page (makepad
+ * libs/mlx/mlx.md) asks a backend-neutral accelerator to provide, "affine
+ * packed BF16 input x U32 packed weights x BF16 scales/biases" (Target
+ * Architecture, sections 1-2), in the 4-bit, group-size-64 affine packed form
+ * of its Refactor Plan, Phase 3:
+ *
+ *     y[m,n] = sum_k x[m,k] * w[n,k],   w[n,k] = scale[n,k/64] * q[n,k] + bias[n,k/64]
+ *
+ *   x        bf16 [M, K], row-major.
+ *   w_packed uint32 [N, K/8]: the 4-bit unsigned codes q[n, 0..K), eight per
+ *            word, the lowest nibble holding the lowest k.
+ *   scales   bf16 [N, K/64], row-major; biases likewise.
+ *   y        bf16 [M, N], row-major; each element is the fp32-accumulated sum
+ *            rounded to nearest-even bf16.
+ *
+ * Decode on the pages is bound by streaming these weights ("epic: CUDA (MLX
+ * backend) prefill and decode acceleration program", Diagnosis; "gemma-4
+ * decode carries ~44 ms/token ...", re-scope paragraph), so M = 1..16 runs a
+ * weight-streaming kernel and larger M a tensor-core GEMM.
+ *
+ * Conventions shared by every entry point below:
+ *  - Ownership: the caller owns every buffer and the stream.  No entry point
+ *    allocates, frees or keeps device memory, and none synchronizes the host
+ *    (the Hard Constraints section of the cleanup plan: no extra copies,
+ *    staging buffers or synchronization points on the hot path).
+ *  - Device pointers are plain CUDA device addresses of the current device.
+ *    `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *  - Work is enqueued asynchronously on `stream`; an AQ_OK return means the
+ *    arguments were valid and the launch was accepted, not that it finished.
+ *  - Arguments are validated before anything is enqueued; on any error
+ *    nothing is launched and the output is left untouched.
+ *  - Thread safety: every entry point may be called from several host threads
+ *    at once.  aq_last_cuda_error() is per host thread.
+ */
+#ifndef AQ_H
+#define AQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum aq_status {
+    AQ_OK = 0,
+    AQ_ERR_INVALID_ARG = 1, /* negative size, null pointer, K not a multiple of the group size */
+    AQ_ERR_UNSUPPORTED = 2, /* bits or group_size outside what this build implements */
+    AQ_ERR_ALIGNMENT = 3,   /* a pointer without the alignment stated below */
+    AQ_ERR_CUDA = 4,        /* the CUDA runtime refused the launch: see aq_last_cuda_error() */
+    AQ_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (see aq_read_device_status) */
+} aq_status;
+
+/* Kernel choice for aq_matmul_bf16_ex.  AUTO picks by M exactly as
+ * aq_matmul_bf16 does. */
+typedef enum aq_kernel {
+    AQ_KERNEL_AUTO = 0,
+    AQ_KERNEL_QMV = 1, /* weight-streaming decode kernel; any M (runs 16 rows of x per pass) */
+    AQ_KERNEL_QMM = 2  /* tensor-core GEMM kernel (tcgen05); any M >= 1 */
+} aq_kernel;
+
+/* Flags for aq_matmul_bf16_ex. */
+enum {
+    /* Launch with programmatic dependent launch: the kernel may start while
+     * the previous kernel on the stream is still running and begins streaming
+     * w_packed/scales/biases before it waits for that kernel to finish.  It
+     * reads x and writes y only after the wait.  PRECONDITION: the weights
+     * were not written by the kernel immediately before on the stream. */
+    AQ_FLAG_PDL = 1u << 0
+};
+
+/*
+ * y = x . dequant(W)^T as defined above.
+ *
+ *   M, N, K     M >= 0, N >= 0, K >= 0; K a multiple of group_size.  M == 0 or
+ *               N == 0 launches nothing and returns AQ_OK; K == 0 writes y = 0.
+ *   group_size  64.  Other values return AQ_ERR_UNSUPPORTED.
+ *   bits        4.  Other values return AQ_ERR_UNSUPPORTED.
+ *   Alignment   x and w_packed 16-byte aligned; scales, biases and y 2-byte
+ *               aligned; otherwise AQ_ERR_ALIGNMENT.
+ *   Aliasing    y must not overlap any input.
+ *   Numerics    fp32 accumulation, one rounding to bf16 per output.  Inputs
+ *               with NaN or Inf propagate them.  The tensor-core path
+ *               (M > 16) converts x to fp16 on chip: it needs |x| <= 65504,
+ *               and |x| below 2^-14 loses relative precision (not its
+ *               contribution to y, which stays far below one bf16 ulp for
+ *               weights of unit scale or less).
+ *   Result is deterministic: the same inputs give the same bits on every
+ *   call (fixed reduction order, no floating-point atomics).
+ */
+aq_status aq_matmul_bf16(const void *x, const uint32_t *w_packed, const void *scales,
+                         const void *biases, void *y, int64_t M, int64_t N, int64_t K,
+                         int group_size, int bits, void *stream);
+
+/* As aq_matmul_bf16, with an explicit kernel choice (aq_kernel) and flags
+ * (AQ_FLAG_*).  Unknown kernel values or flag bits return AQ_ERR_INVALID_ARG. */
+aq_status aq_matmul_bf16_ex(const void *x, const uint32_t *w_packed, const void *scales,
+                            const void *biases, void *y, int64_t M, int64_t N, int64_t K,
+                            int group_size, int bits, int kernel, unsigned flags, void *stream);
+
+/*
+ * Host utility (test data): min-max affine quantization of float weights
+ * w[N, K] (host memory) into the packed format above.  The pages give no
+ * quantization procedure; this one takes, per group, scale = (max - min) /
+ * (2^bits - 1) and bias = min, each rounded to nearest-even bf16, then
+ * q = clamp(round_half_even((w - bias) / scale), 0, 2^bits - 1) with the
+ * rounded scale and bias (a constant group gets scale 0 and q = 0).
+ * Outputs are host buffers of N*K*bits/32 words and N*K/group_size bf16 bit
+ * patterns each.  bits 4 or 8; K a multiple of group_size (> 0).  Runs
+ * synchronously on the calling thread.
+ */
+aq_status aq_quantize_ref(const float *w, int64_t N, int64_t K, int group_size, int bits,
+                          uint32_t *w_packed, uint16_t *scales_bf16, uint16_t *biases_bf16);
+
+/* Host utility: pack codes[N, K] (host, one code per byte, values below
+ * 2^bits) into words as described above.  bits 4 or 8; K a multiple of
+ * 32/bits.  A code >= 2^bits returns AQ_ERR_INVALID_ARG. */
+aq_status aq_pack_ref(const uint8_t *codes, int64_t N, int64_t K, int bits, uint32_t *w_packed);
+
+/* Static, NUL-terminated name of a status code. */
+const char *aq_status_string(aq_status status);
+
+/* Text of the last CUDA runtime error seen by an entry point on this host
+ * thread ("" if none).  Valid until the next call on this thread. */
+const char *aq_last_cuda_error(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int aq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AQ_H */

@@ -1,0 +1,99 @@
+"""CPU tests of the C ABI: the library loads, exports what include/aq.h
+declares, rejects bad arguments before touching a device, and its host
+utilities agree bit for bit with the oracle's."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import affine_bit_quantized_gb300 as aq
+import oracle
+from affine_bit_quantized_gb300 import _build
+
+A = 0x10000  # a 64 KiB-aligned fake address: validation never dereferences it
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    _build.build_library()
+
+
+def test_exports_every_declared_symbol():
+    names = aq.declared_functions()
+    assert {"aq_matmul_bf16", "aq_matmul_bf16_ex", "aq_quantize_ref", "aq_pack_ref", "aq_status_string",
+            "aq_last_cuda_error"} <= set(names)
+    lib = ctypes.CDLL(aq.library_path())
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings():
+    for code, name in ((0, "AQ_OK"), (1, "AQ_ERR_INVALID_ARG"), (2, "AQ_ERR_UNSUPPORTED"), (3, "AQ_ERR_ALIGNMENT"),
+                       (4, "AQ_ERR_CUDA"), (5, "AQ_ERR_TIMEOUT")):
+        assert aq.status_string(code) == name
+    assert aq.last_cuda_error() == ""
+
+
+@pytest.mark.parametrize("args,expect", [
+    (dict(bits=3), aq.AQ_ERR_UNSUPPORTED),
+    (dict(bits=8), aq.AQ_ERR_UNSUPPORTED),
+    (dict(group_size=32), aq.AQ_ERR_UNSUPPORTED),
+    (dict(group_size=128), aq.AQ_ERR_UNSUPPORTED),
+    (dict(K=96), aq.AQ_ERR_INVALID_ARG),
+    (dict(M=-1), aq.AQ_ERR_INVALID_ARG),
+    (dict(N=-5), aq.AQ_ERR_INVALID_ARG),
+    (dict(K=-64), aq.AQ_ERR_INVALID_ARG),
+    (dict(x=None), aq.AQ_ERR_INVALID_ARG),
+    (dict(w=None), aq.AQ_ERR_INVALID_ARG),
+    (dict(s=None), aq.AQ_ERR_INVALID_ARG),
+    (dict(b=None), aq.AQ_ERR_INVALID_ARG),
+    (dict(y=None), aq.AQ_ERR_INVALID_ARG),
+    (dict(x=A + 8), aq.AQ_ERR_ALIGNMENT),
+    (dict(w=A + 4), aq.AQ_ERR_ALIGNMENT),
+    (dict(s=A + 1), aq.AQ_ERR_ALIGNMENT),
+    (dict(b=A + 1), aq.AQ_ERR_ALIGNMENT),
+    (dict(y=A + 1), aq.AQ_ERR_ALIGNMENT),
+    (dict(M=0), aq.AQ_OK),          # empty: nothing launched
+    (dict(N=0), aq.AQ_OK),
+    (dict(M=0, x=None, y=None), aq.AQ_OK),
+    (dict(M=1 << 31), aq.AQ_ERR_INVALID_ARG),
+])
+def test_validation_before_launch(args, expect):
+    p = dict(x=A, w=A, s=A, b=A, y=A, M=1, N=64, K=128, group_size=64, bits=4)
+    p.update(args)
+    st = aq.aq_matmul_bf16(p["x"], p["w"], p["s"], p["b"], p["y"], p["M"], p["N"], p["K"], p["group_size"],
+                           p["bits"], None)
+    assert st == expect, aq.status_string(st)
+
+
+def test_ex_rejects_unknown_kernel_and_flags():
+    assert aq.aq_matmul_bf16_ex(A, A, A, A, A, 1, 64, 128, 64, 4, 7, 0, None) == aq.AQ_ERR_INVALID_ARG
+    assert aq.aq_matmul_bf16_ex(A, A, A, A, A, 1, 64, 128, 64, 4, 0, 1 << 5, None) == aq.AQ_ERR_INVALID_ARG
+    assert aq.aq_matmul_bf16_ex(A, A, A, A, A, 0, 64, 128, 64, 4, 2, 1, None) == aq.AQ_OK
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_pack_ref_matches_oracle(bits):
+    rng = np.random.default_rng(7)
+    codes = rng.integers(0, 1 << bits, size=(9, 256), dtype=np.uint8)
+    assert np.array_equal(aq.pack_ref(codes, bits), oracle.pack(codes, bits))
+
+
+def test_pack_ref_rejects_out_of_range_code():
+    codes = np.zeros((1, 8), np.uint8)
+    codes[0, 3] = 16
+    out = np.zeros((1, 1), np.uint32)
+    assert aq.aq_pack_ref(codes.ctypes.data, 1, 8, 4, out.ctypes.data) == aq.AQ_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_quantize_ref_matches_oracle(bits):
+    rng = np.random.default_rng(8)
+    w = rng.normal(0, 0.03, size=(17, 512)).astype(np.float32)
+    w[3, :64] = -0.5                                  # constant group
+    w[4, 64:128] = rng.normal(0, 1e-30, 64)           # tiny values: subnormal-range rounding
+    w[5, 128:192] *= 1e4
+    got = aq.quantize_ref(w, bits=bits)
+    want = oracle.quantize(w, bits=bits)
+    for g, o in zip(got, want):
+        assert np.array_equal(g, o)

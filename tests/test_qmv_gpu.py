@@ -1,0 +1,128 @@
+"""GPU parity of the weight-streaming path (M = 1..16 and chunked larger M)
+against the oracle, element by element, through the C ABI."""
+import numpy as np
+import pytest
+
+import affine_bit_quantized_gb300 as aq
+import oracle
+from affine_bit_quantized_gb300 import _build, synth
+
+from ._helpers import assert_parity, from_dev_bf16, upload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import torch
+    _build.build_library()
+    return torch.device("cuda:0")
+
+
+def run(dev, x, w, kernel="qmv", pdl=False):
+    import torch
+    xt, wt, st, bt = upload(x, w, dev)
+    y = aq.matmul(xt, wt, st, bt, kernel=kernel, pdl=pdl)
+    torch.cuda.synchronize()
+    return from_dev_bf16(y)
+
+
+def check(dev, M, N, K, seed, kernel="qmv", pdl=False):
+    w = synth.make_weights(N, K, seed)
+    x = synth.make_x(M, K, seed)
+    got = run(dev, x, w, kernel, pdl)
+    _, ref = oracle.matmul(x, w.w_packed, w.scales, w.biases, M, N, K)
+    return assert_parity(got, ref, what=f"M={M} N={N} K={K}")
+
+
+def test_tiny_correctness_config(dev):
+    # 256 x 512 weights, M = 1, seed 0
+    check(dev, 1, 256, 512, synth.seed_for(1))
+
+
+@pytest.mark.parametrize("name,N,K", synth.LLAMA8B_LAYER + (synth.LLAMA8B_LM_HEAD,))
+def test_llama8b_layer_m1(dev, name, N, K):
+    j = [n for n, _, _ in synth.LLAMA8B_LAYER + (synth.LLAMA8B_LM_HEAD,)].index(name)
+    check(dev, 1, N, K, synth.seed_for(2, 0, j))
+
+
+@pytest.mark.parametrize("M", [2, 4, 8, 16])
+@pytest.mark.parametrize("name,N,K", [s for s in synth.LLAMA8B_LAYER if s[0] in ("q_proj", "k_proj", "down_proj")])
+def test_small_batch_sweep(dev, M, name, N, K):
+    j = [n for n, _, _ in synth.LLAMA8B_LAYER].index(name)
+    check(dev, M, N, K, synth.seed_for(3, M, j))
+
+
+@pytest.mark.parametrize("M", [2, 16])
+def test_small_batch_lm_head_sampled(dev, M):
+    import torch
+    _, N, K = synth.LLAMA8B_LM_HEAD
+    w = synth.make_weights(N, K, synth.seed_for(3, M, 7))
+    x = synth.make_x(M, K, synth.seed_for(3, M, 7))
+    got = run(dev, x, w)
+    rng = np.random.default_rng(M)
+    im = rng.integers(0, M, 4000)
+    inn = rng.integers(0, N, 4000)
+    ye, yb = oracle.matmul_sampled(x, w.w_packed, w.scales, w.biases, M, N, K, im, inn)
+    rms = float(np.sqrt(np.mean(ye * ye)))
+    assert_parity(got[im, inn], yb, rms=rms, what="lm_head sampled")
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (1, 1, 64), (1, 14, 64), (1, 15, 64), (1, 16, 64), (1, 31, 128), (3, 45, 576), (5, 7, 1088),
+    (8, 33, 4160), (9, 100, 192), (13, 256, 1024), (16, 15, 64), (1, 1000, 8192), (2, 77, 16384),
+    (17, 50, 256), (33, 40, 512), (70, 31, 320),
+])
+def test_ragged_shapes(dev, M, N, K):
+    check(dev, M, N, K, 100 + M + N + K)
+
+
+def test_pdl_flag_same_bits(dev):
+    M, N, K = 4, 300, 1024
+    w = synth.make_weights(N, K, 5)
+    x = synth.make_x(M, K, 5)
+    a = run(dev, x, w, pdl=False)
+    b = run(dev, x, w, pdl=True)
+    assert np.array_equal(a, b)
+
+
+def test_deterministic(dev):
+    import torch
+    M, N, K = 3, 4096, 4096
+    w = synth.make_weights(N, K, 6)
+    x = synth.make_x(M, K, 6)
+    xt, wt, st, bt = upload(x, w, dev)
+    y1 = aq.matmul(xt, wt, st, bt)
+    y2 = aq.matmul(xt, wt, st, bt)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+
+
+def test_k_zero_writes_zeros_and_m_zero_is_noop(dev):
+    import torch
+    y = torch.full((2, 5), 3.0, dtype=torch.bfloat16, device=dev)
+    p = y.data_ptr()
+    st = aq.aq_matmul_bf16(p, p, p, p, p, 2, 5, 0, 64, 4, None)
+    torch.cuda.synchronize()
+    assert st == aq.AQ_OK and not y.float().any()
+    y.fill_(3.0)
+    st = aq.aq_matmul_bf16(p, p, p, p, p, 0, 5, 64, 64, 4, None)
+    torch.cuda.synchronize()
+    assert st == aq.AQ_OK and bool((y.float() == 3.0).all())
+
+
+def test_special_inputs(dev):
+    """Zero x gives exact zeros; a one-hot x returns one dequantized column
+    (q = 0 gives the bias); NaN in x propagates to every output of its row."""
+    N, K = 40, 256
+    w = synth.make_weights(N, K, 9)
+    codes = oracle.unpack(w.w_packed, N, K)
+    codes[:, 5] = 0
+    w.w_packed = oracle.pack(codes)
+    x = np.zeros((3, K), np.uint16)
+    x[1, 5] = 0x3F80
+    x[2, 7] = 0x7FC0  # NaN
+    got = run(dev, x, w)
+    assert not got[0].any()
+    assert np.array_equal(got[1], w.biases[:, 0])
+    assert np.all((got[2] & 0x7F80) == 0x7F80) and np.all(got[2] & 0x007F)
