@@ -25,6 +25,7 @@ AQ_KERNEL_QMV = 1
 AQ_KERNEL_QMM = 2
 
 AQ_FLAG_PDL = 1
+AQ_FLAG_DEBUG_SKIP_X = 1 << 31
 
 _lock = threading.Lock()
 _lib = None
@@ -64,6 +65,8 @@ def load() -> ctypes.CDLL:
             lib.aq_status_string.restype = ctypes.c_char_p
             lib.aq_last_cuda_error.argtypes = []
             lib.aq_last_cuda_error.restype = ctypes.c_char_p
+            lib.aq_read_device_status.argtypes = [P]
+            lib.aq_read_device_status.restype = I
             lib.aq_version.argtypes = []
             lib.aq_version.restype = I
             _lib = lib
@@ -100,6 +103,10 @@ def aq_pack_ref(codes, N, K, bits, w_packed) -> int:
     return load().aq_pack_ref(codes, N, K, bits, w_packed)
 
 
+def aq_read_device_status(stream) -> int:
+    return load().aq_read_device_status(stream)
+
+
 def status_string(status: int) -> str:
     return load().aq_status_string(status).decode()
 
@@ -118,7 +125,7 @@ _KERNELS = {"auto": AQ_KERNEL_AUTO, "qmv": AQ_KERNEL_QMV, "qmm": AQ_KERNEL_QMM}
 
 
 def matmul(x, w_packed, scales, biases, out=None, *, group_size: int = 64, bits: int = 4,
-           kernel: str = "auto", pdl: bool = False, stream=None):
+           kernel: str = "auto", pdl: bool = False, stream=None, flags: int = 0):
     """y = x . dequant(W)^T for torch CUDA tensors (x bf16 [M,K]; w_packed int32/uint32
     [N, K*bits/32]; scales/biases bf16 [N, K/group_size]).  Returns y bf16 [M, N]."""
     import torch
@@ -134,7 +141,7 @@ def matmul(x, w_packed, scales, biases, out=None, *, group_size: int = 64, bits:
         stream = torch.cuda.current_stream(x.device)
     st = aq_matmul_bf16_ex(x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(), biases.data_ptr(),
                            out.data_ptr(), M, N, K, group_size, bits, _KERNELS[kernel],
-                           AQ_FLAG_PDL if pdl else 0, stream.cuda_stream)
+                           (AQ_FLAG_PDL if pdl else 0) | flags, stream.cuda_stream)
     if st != AQ_OK:
         raise AqError(st, "aq_matmul_bf16_ex")
     return out

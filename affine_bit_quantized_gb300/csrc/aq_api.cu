@@ -4,6 +4,7 @@
 // touches the device (the boundary behaviour asked for by the "MLX CUDA
 // Cleanup Plan" page: small wrappers for status handling, no hidden
 // fallbacks, no extra copies or synchronization).
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -12,9 +13,34 @@
 #include "../../include/aq.h"
 #include "aq_internal.h"
 
+// Device status word: bounded device-side waits that expire record
+// AQ_DEVICE_STATUS_TIMEOUT here; aq_read_device_status() reads and clears it.
+__device__ int g_aq_device_status;
+
 namespace {
 
 thread_local char g_last_cuda_error[256] = "";
+constexpr int kMaxDevices = 64;
+std::atomic<int *> g_status_ptr[kMaxDevices];
+constexpr uint64_t kTimeoutNs = 2000000000ull;      // 2 s: far beyond any legitimate wait
+constexpr uint64_t kDebugTimeoutNs = 20000000ull;   // 20 ms for the timeout test hook
+
+// Device address of g_aq_device_status on the current device (looked up once
+// per device; the first call on a device must not be inside stream capture).
+cudaError_t status_ptr(int **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    int *p = g_status_ptr[dev].load(std::memory_order_acquire);
+    if (!p) {
+        e = cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_aq_device_status);
+        if (e != cudaSuccess) return e;
+        g_status_ptr[dev].store(p, std::memory_order_release);
+    }
+    *out = p;
+    return cudaSuccess;
+}
 
 aq_status record_cuda(cudaError_t e) {
     if (e == cudaSuccess) return AQ_OK;
@@ -52,7 +78,7 @@ aq_status aq_matmul_bf16_ex(const void *x, const uint32_t *w_packed, const void 
                             int group_size, int bits, int kernel, unsigned flags, void *stream) {
     if (kernel != AQ_KERNEL_AUTO && kernel != AQ_KERNEL_QMV && kernel != AQ_KERNEL_QMM)
         return AQ_ERR_INVALID_ARG;
-    if (flags & ~(unsigned)AQ_FLAG_PDL) return AQ_ERR_INVALID_ARG;
+    if (flags & ~(unsigned)(AQ_FLAG_PDL | AQ_FLAG_DEBUG_SKIP_X)) return AQ_ERR_INVALID_ARG;
     aq_status st = validate(x, w_packed, scales, biases, y, M, N, K, group_size, bits);
     if (st != AQ_OK || M == 0 || N == 0) return st;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -68,6 +94,17 @@ aq_status aq_matmul_bf16_ex(const void *x, const uint32_t *w_packed, const void 
     a.K = K;
     a.pdl = (flags & AQ_FLAG_PDL) != 0;
     a.stream = cs;
+    a.debug_skip_x = (flags & AQ_FLAG_DEBUG_SKIP_X) != 0;
+    a.timeout_ns = a.debug_skip_x ? kDebugTimeoutNs : kTimeoutNs;
+    st = record_cuda(status_ptr(&a.status));
+    if (st != AQ_OK) return st;
+    if (M <= 8) {
+        a.x = x;
+        a.y = y;
+        a.M = M;
+        if (aq::qmv_tma_supported(a)) return record_cuda(aq::launch_qmv_tma(a));
+    }
+    if (a.debug_skip_x) return AQ_ERR_UNSUPPORTED;  // the hook exists only in the TMA kernel
     // Weight-streaming passes over at most 16 rows of x each.
     for (int64_t m0 = 0; m0 < M; m0 += kQmvMaxRows) {
         a.x = static_cast<const uint16_t *>(x) + m0 * K;
@@ -195,6 +232,24 @@ const char *aq_status_string(aq_status status) {
 }
 
 const char *aq_last_cuda_error(void) { return g_last_cuda_error; }
+
+aq_status aq_read_device_status(void *stream) {
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    aq_status st = record_cuda(cudaStreamSynchronize(cs));
+    if (st != AQ_OK) return st;
+    int *p = nullptr;
+    st = record_cuda(status_ptr(&p));
+    if (st != AQ_OK) return st;
+    int v = 0;
+    st = record_cuda(cudaMemcpyFromSymbolAsync(&v, g_aq_device_status, sizeof v, 0, cudaMemcpyDeviceToHost, cs));
+    if (st != AQ_OK) return st;
+    const int zero = 0;
+    st = record_cuda(cudaMemcpyToSymbolAsync(g_aq_device_status, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, cs));
+    if (st != AQ_OK) return st;
+    st = record_cuda(cudaStreamSynchronize(cs));
+    if (st != AQ_OK) return st;
+    return v == aq::AQ_DEVICE_STATUS_TIMEOUT ? AQ_ERR_TIMEOUT : AQ_OK;
+}
 
 int aq_version(void) { return 100; }
 

@@ -16,11 +16,23 @@ struct MatmulArgs {
     int64_t M, N, K;
     bool pdl;                // launch with programmatic stream serialization
     cudaStream_t stream;
+    int *status;             // device status word (bounded waits record timeouts here)
+    uint64_t timeout_ns;     // deadline of every bounded device-side wait
+    bool debug_skip_x;       // test hook: the TMA kernel omits the copy of x
 };
+
+// Values of the device status word.
+constexpr int AQ_DEVICE_STATUS_OK = 0;
+constexpr int AQ_DEVICE_STATUS_TIMEOUT = 5;
 
 // Weight-streaming kernel for up to 16 rows of x (qmv.cu).  Requires
 // 1 <= M <= 16, N >= 1, K >= 64.
 cudaError_t launch_qmv(const MatmulArgs &a);
+
+// TMA-fed weight-streaming kernel (qmv_tma.cu) for 1 <= M <= 8,
+// K % 512 == 0, M*K <= 16384 and 16-byte aligned scales/biases.
+bool qmv_tma_supported(const MatmulArgs &a);
+cudaError_t launch_qmv_tma(const MatmulArgs &a);
 
 // Tensor-core kernel (qmm.cu).  Requires M >= 1, N >= 1, K >= 64.
 cudaError_t launch_qmm(const MatmulArgs &a);

@@ -1,0 +1,475 @@
+// Weight-streaming kernel for y = x . dequant(W)^T with 1..8 rows of x,
+// fed by the Tensor Memory Accelerator.
+//
+// Decode time is the time to stream the packed weights ("epic: CUDA (MLX
+// backend) prefill and decode acceleration program", Diagnosis; "gemma-4
+// decode carries ~44 ms/token ...", re-scope paragraph).  This kernel keeps
+// the weight stream going independently of the arithmetic:
+//
+//  * one producer warp per CTA copies 16-row x 2048-code tiles of the packed
+//    codes, plus the matching scales and biases, into a ring of shared-memory
+//    stages with cp.async.bulk.tensor (TMA), completion tracked by mbarriers;
+//  * eight consumer warps each take one 256-code column block of a stage
+//    (16 rows x 4 groups) and run the dequantization-free dot product of
+//    the folded form on mma.sync m16n8k16 (bf16 in, fp32 out):
+//        D[n,m,g] = sum_{k in g} (128 + q[n,k]) * x[m,k]
+//        y[m,n]  += scale[n,g] * D[n,m,g] + (bias[n,g] - 128*scale[n,g]) * X[m,g]
+//    with X[m,g] = sum_{k in g} x[m,k] computed once per CTA;
+//  * CTAs are persistent: each walks its 16-row tiles across the whole K,
+//    the eight warps' partial sums are combined in shared memory in a fixed
+//    order, and every output is written exactly once (deterministic).
+//
+// A code q is turned into the exact bf16 value 128 + q by OR-ing its nibble
+// into the mantissa of 128.0: one LOP3 makes the pair (q[p], q[p+4]) of a
+// word; x is stored in shared memory with each 8-element word permuted to
+// (x0,x4,x1,x5,x2,x6,x3,x7) so that the MMA's B fragment matches those pairs
+// (a dot product is indifferent to the order of k).
+//
+// The code tiles use the TMA 128-byte swizzle, so the consumers' 8-byte
+// shared-memory reads of 8 rows at once are free of bank conflicts.
+//
+// Every mbarrier wait is bounded by a global-timer deadline; on expiry the
+// thread records AQ_ERR_TIMEOUT in the library's device status word, the CTA
+// stops, and the producer first waits (also bounded) for the copies it
+// issued.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+
+#include "aq_internal.h"
+
+namespace aq {
+namespace {
+
+constexpr int kRows = 16;                    // rows of W per tile (MMA M)
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kBlockCodes = 256;             // codes per column block (one 128-byte swizzle row)
+constexpr int kStageCodes = kBlockCodes * kConsumerWarps;  // 2048 codes per stage
+constexpr int kStageGroups = kStageCodes / 64;             // 32
+constexpr int kStages = 4;
+constexpr int kCodeBlockBytes = kRows * 128;               // 2048
+constexpr int kCodesBytes = kCodeBlockBytes * kConsumerWarps;  // 16384
+constexpr int kSBBytes = kRows * kStageGroups * 2;         // 1024 (scales, and again biases)
+constexpr int kStageBytes = kCodesBytes + 2 * kSBBytes;    // 18432
+constexpr int kMaxXBytes = 32768;                          // M*K*2 limit for staging x once per CTA
+constexpr int kRedBytes = 2 * kConsumerWarps * kRows * 8 * 4;  // double-buffered cross-warp sums
+constexpr uint32_t kMagic = 0x43004300u;   // bf16x2 (128.0, 128.0)
+// largest layout: x of 32 KB, X sums of M*K/16 bytes, barriers, alignment slack
+constexpr int kMaxSmem = kStages * kStageBytes + kMaxXBytes + kMaxXBytes / 16 + 16 + kRedBytes +
+                         (2 * kStages + 1) * 8 + 16 + 1024;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t global_timer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait; false if the deadline passed or the CTA is aborting.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t deadline,
+                                          const volatile int *abort_flag) {
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (global_timer() > deadline) return false;
+    }
+    return true;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(map), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+// (128 + q[p], 128 + q[p+4]) as bf16x2, from a word already shifted right by 4p.
+__device__ __forceinline__ uint32_t code_pair(uint32_t v) { return (v & 0x000F000Fu) | kMagic; }
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+struct Layout {
+    int x_bytes;     // M*K*2 rounded up to 16
+    int xsum_off;    // float [M][G]
+    int red_off;     // float [2][8][16][8]
+    int bar_off;     // uint64 [2*kStages + 1] + abort flag
+    int total;       // bytes (excluding the 1024 alignment slack)
+};
+__host__ __device__ inline Layout make_layout(int M, int K) {
+    Layout L;
+    L.x_bytes = (M * K * 2 + 15) & ~15;
+    const int x_off = kStages * kStageBytes;
+    L.xsum_off = x_off + L.x_bytes;
+    L.red_off = (L.xsum_off + M * (K / 64) * 4 + 15) & ~15;
+    L.bar_off = L.red_off + kRedBytes;
+    L.total = L.bar_off + (2 * kStages + 1) * 8 + 16;
+    return L;
+}
+
+// ONE_ROW: M == 1 (only column 0 of the MMA output is used).
+template <bool ONE_ROW>
+__global__ void __launch_bounds__(kThreads, 1)
+qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
+               const __grid_constant__ CUtensorMap tm_b, const __nv_bfloat16 *__restrict__ x,
+               __nv_bfloat16 *__restrict__ y, int M, int N, int K, unsigned long long timeout_ns,
+               int *status, int skip_x) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const Layout L = make_layout(M, K);
+    const uint32_t s_base = smem_addr(smem);
+    const uint32_t x_s = s_base + kStages * kStageBytes;
+    float *xsum = reinterpret_cast<float *>(smem + L.xsum_off);
+    float *red = reinterpret_cast<float *>(smem + L.red_off);
+    const uint32_t bar_full = s_base + L.bar_off;          // kStages barriers
+    const uint32_t bar_empty = bar_full + kStages * 8;     // kStages barriers
+    const uint32_t bar_x = bar_empty + kStages * 8;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.bar_off + (2 * kStages + 1) * 8);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = K >> 6;
+    const int nblk = K / kBlockCodes;                       // column blocks in K
+    const int KB = (K + kStageCodes - 1) / kStageCodes;     // stages per tile
+    const int T = (N + kRows - 1) / kRows;
+    const int my_tiles = blockIdx.x < T ? (T - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int L_items = my_tiles * KB;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, kConsumerWarps);
+        }
+        mbar_init(bar_x, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    griddep_launch();
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        if (lane != 0) return;
+        const uint64_t pol = policy_evict_first();
+        auto issue = [&](int it) {
+            const int slot = it % kStages;
+            const int tile = (int)blockIdx.x + (it / KB) * (int)gridDim.x;
+            const int kb = it % KB;
+            const uint32_t dst = s_base + slot * kStageBytes;
+            const uint32_t fb = bar_full + 8 * slot;
+            int nvalid = nblk - kb * kConsumerWarps;
+            nvalid = nvalid < kConsumerWarps ? nvalid : kConsumerWarps;
+            mbar_expect_tx(fb, (uint32_t)(nvalid * kCodeBlockBytes + 2 * kSBBytes));
+            for (int b = 0; b < nvalid; ++b)
+                tma_load_2d(dst + b * kCodeBlockBytes, &tm_w, (kb * kConsumerWarps + b) * 32, tile * kRows, fb, pol);
+            tma_load_2d(dst + kCodesBytes, &tm_s, kb * kStageGroups, tile * kRows, fb, pol);
+            tma_load_2d(dst + kCodesBytes + kSBBytes, &tm_b, kb * kStageGroups, tile * kRows, fb, pol);
+        };
+        int issued = 0;
+        bool ok = true;
+        // the weights do not depend on the preceding kernel: prefetch them first
+        for (; issued < L_items && issued < kStages; ++issued) issue(issued);
+        griddep_wait();
+        const uint64_t deadline = global_timer() + timeout_ns;
+        if (!skip_x) {  // skip_x: test hook that leaves the x barrier incomplete
+            mbar_expect_tx(bar_x, (uint32_t)(M * K * 2));
+            for (int m = 0; m < M; ++m) bulk_load(x_s + m * K * 2, x + (int64_t)m * K, (uint32_t)(K * 2), bar_x);
+        }
+        for (; issued < L_items; ++issued) {
+            const int slot = issued % kStages;
+            if (!mbar_wait(bar_empty + 8 * slot, ((issued / kStages) - 1) & 1, deadline, abort_flag)) {
+                ok = false;
+                break;
+            }
+            issue(issued);
+        }
+        if (!ok) {
+            if (!*abort_flag) {
+                atomicExch(status, (int)AQ_DEVICE_STATUS_TIMEOUT);
+                *abort_flag = 1;
+            }
+            // let the copies already issued land before the CTA can exit
+            const uint64_t drain = global_timer() + timeout_ns;
+            for (int it = (issued > kStages ? issued - kStages : 0); it < issued; ++it)
+                while (!mbar_try_wait(bar_full + 8 * (it % kStages), (it / kStages) & 1) && global_timer() < drain) {
+                }
+            while (!mbar_try_wait(bar_x, 0) && global_timer() < drain) {
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    // Every consumer warp runs the whole loop, even after a timeout, because
+    // the named barriers below need all of them; after an abort the waits
+    // return at once and the work is skipped.
+    const int gid = lane >> 2;
+    const int j = lane & 3;
+    const int r0 = gid, r1 = gid + 8;
+    griddep_wait();  // x comes from the preceding kernel; the deadline starts after it
+    const uint64_t deadline = global_timer() + timeout_ns;
+    bool alive = true;
+    auto fail = [&]() {
+        if (alive && !*abort_flag) {
+            atomicExch(status, (int)AQ_DEVICE_STATUS_TIMEOUT);
+            *abort_flag = 1;
+        }
+        alive = false;
+    };
+
+    if (!mbar_wait(bar_x, 0, deadline, abort_flag)) fail();
+    // permute each 8-element word of x to (x0,x4,x1,x5,x2,x6,x3,x7) and form
+    // the per-group sums X[m,g] (8 lanes per group, fixed order)
+    if (alive) {
+        const int words = M * K / 8;
+        for (int base = 0; base < words; base += 256) {
+            const int wi = base + threadIdx.x;
+            float part = 0.f;
+            if (wi < words) {
+                const uint32_t a = x_s + wi * 16;
+                const uint4 v = lds128(a);
+                part = ((bf16lo(v.x) + bf16hi(v.x)) + (bf16lo(v.y) + bf16hi(v.y))) +
+                       ((bf16lo(v.z) + bf16hi(v.z)) + (bf16lo(v.w) + bf16hi(v.w)));
+                uint4 p;
+                p.x = __byte_perm(v.x, v.z, 0x5410);
+                p.y = __byte_perm(v.x, v.z, 0x7632);
+                p.z = __byte_perm(v.y, v.w, 0x5410);
+                p.w = __byte_perm(v.y, v.w, 0x7632);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(p.x), "r"(p.y), "r"(p.z),
+                             "r"(p.w)
+                             : "memory");
+            }
+            part += __shfl_xor_sync(0xFFFFFFFFu, part, 1);
+            part += __shfl_xor_sync(0xFFFFFFFFu, part, 2);
+            part += __shfl_xor_sync(0xFFFFFFFFu, part, 4);
+            // word wi of the x buffer belongs to row m = wi / (K/8), group (wi mod K/8) / 8,
+            // i.e. to X[m*G + g] with index wi / 8
+            if (wi < words && (wi & 7) == 0) xsum[wi >> 3] = part;
+        }
+    }
+    consumer_sync();
+
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    int par = 0;
+    for (int it = 0; it < L_items; ++it) {
+        const int slot = it % kStages;
+        const int kb = it % KB;
+        if (alive && !mbar_wait(bar_full + 8 * slot, (it / kStages) & 1, deadline, abort_flag)) fail();
+        const int blk = kb * kConsumerWarps + warp;
+        if (alive && blk < nblk) {
+            const uint8_t *st = smem + slot * kStageBytes;
+            const uint8_t *cb = st + warp * kCodeBlockBytes;
+            const uint8_t *sb = st + kCodesBytes;
+            const uint8_t *bb = sb + kSBBytes;
+            const uint2 s0 = *reinterpret_cast<const uint2 *>(sb + r0 * 64 + 8 * warp);
+            const uint2 s1 = *reinterpret_cast<const uint2 *>(sb + r1 * 64 + 8 * warp);
+            const uint2 b0 = *reinterpret_cast<const uint2 *>(bb + r0 * 64 + 8 * warp);
+            const uint2 b1 = *reinterpret_cast<const uint2 *>(bb + r1 * 64 + 8 * warp);
+            const uint8_t *xrow = smem + kStages * kStageBytes + (size_t)gid * K * 2;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const int c = 2 * g + (j >> 1);
+                const int off = ((c ^ gid) << 4) | ((j & 1) << 3);
+                const uint2 w0 = *reinterpret_cast<const uint2 *>(cb + r0 * 128 + off);
+                const uint2 w1 = *reinterpret_cast<const uint2 *>(cb + r1 * 128 + off);
+                const int gg = blk * 4 + g;                    // group index in K
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const uint32_t wa = i ? w0.y : w0.x;
+                    const uint32_t wb = i ? w1.y : w1.x;
+                    uint4 X = make_uint4(0u, 0u, 0u, 0u);
+                    if (gid < M) X = *reinterpret_cast<const uint4 *>(xrow + (gg * 8 + 2 * j + i) * 16);
+                    const uint32_t wa4 = wa >> 4, wb4 = wb >> 4, wa8 = wa >> 8, wb8 = wb >> 8;
+                    mma_bf16_16816(d, code_pair(wa), code_pair(wb), code_pair(wa4), code_pair(wb4), X.x, X.y);
+                    mma_bf16_16816(d, code_pair(wa8), code_pair(wb8), code_pair(wa8 >> 4), code_pair(wb8 >> 4), X.z,
+                                   X.w);
+                }
+                const uint32_t sw0 = (g < 2) ? s0.x : s0.y, sw1 = (g < 2) ? s1.x : s1.y;
+                const uint32_t bw0 = (g < 2) ? b0.x : b0.y, bw1 = (g < 2) ? b1.x : b1.y;
+                const float sc0 = (g & 1) ? bf16hi(sw0) : bf16lo(sw0);
+                const float sc1 = (g & 1) ? bf16hi(sw1) : bf16lo(sw1);
+                const float p0 = fmaf(-128.f, sc0, (g & 1) ? bf16hi(bw0) : bf16lo(bw0));
+                const float p1 = fmaf(-128.f, sc1, (g & 1) ? bf16hi(bw1) : bf16lo(bw1));
+                if (ONE_ROW) {
+                    const float xs = xsum[gg];
+                    acc[0] = fmaf(sc0, d[0], fmaf(p0, xs, acc[0]));
+                    acc[2] = fmaf(sc1, d[2], fmaf(p1, xs, acc[2]));
+                } else {
+                    const float xs0 = (2 * j < M) ? xsum[(2 * j) * G + gg] : 0.f;
+                    const float xs1 = (2 * j + 1 < M) ? xsum[(2 * j + 1) * G + gg] : 0.f;
+                    acc[0] = fmaf(sc0, d[0], fmaf(p0, xs0, acc[0]));
+                    acc[1] = fmaf(sc0, d[1], fmaf(p0, xs1, acc[1]));
+                    acc[2] = fmaf(sc1, d[2], fmaf(p1, xs0, acc[2]));
+                    acc[3] = fmaf(sc1, d[3], fmaf(p1, xs1, acc[3]));
+                }
+            }
+        }
+        __syncwarp();
+        // a CTA that is aborting stops releasing stages, so its producer stops
+        // issuing copies and drains the ones in flight
+        if (alive && lane == 0) mbar_arrive(bar_empty + 8 * slot);
+
+        if (kb == KB - 1) {
+            // tile finished: combine the eight warps' partial sums in order
+            const int tile = (int)blockIdx.x + (it / KB) * (int)gridDim.x;
+            float *rb = red + par * (kConsumerWarps * kRows * 8);
+            float *rw = rb + warp * (kRows * 8);
+            rw[r0 * 8 + 2 * j] = acc[0];
+            rw[r0 * 8 + 2 * j + 1] = acc[1];
+            rw[r1 * 8 + 2 * j] = acc[2];
+            rw[r1 * 8 + 2 * j + 1] = acc[3];
+            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+            consumer_sync();
+            const int t = threadIdx.x;
+            if (alive && !*abort_flag && t < kRows * M) {
+                const int m = t / kRows, row = t % kRows;
+                const int n = tile * kRows + row;
+                if (n < N) {
+                    float v = rb[row * 8 + m];
+#pragma unroll
+                    for (int w = 1; w < kConsumerWarps; ++w) v += rb[w * (kRows * 8) + row * 8 + m];
+                    y[(int64_t)m * N + n] = __float2bfloat16_rn(v);
+                }
+            }
+            par ^= 1;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sms[kMaxDevices];
+std::atomic<int> g_attr_done[2][kMaxDevices];
+
+}  // namespace
+
+bool qmv_tma_supported(const MatmulArgs &a) {
+    return a.M >= 1 && a.M <= 8 && a.K % 512 == 0 && a.M * a.K * 2 <= kMaxXBytes && encode_fn() != nullptr &&
+           (reinterpret_cast<uintptr_t>(a.scales) & 15) == 0 && (reinterpret_cast<uintptr_t>(a.biases) & 15) == 0;
+}
+
+cudaError_t launch_qmv_tma(const MatmulArgs &a) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    int sms = g_sms[dev].load(std::memory_order_relaxed);
+    if (sms == 0) {
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        g_sms[dev].store(sms, std::memory_order_relaxed);
+    }
+    const int M = (int)a.M, N = (int)a.N, K = (int)a.K;
+    const Layout L = make_layout(M, K);
+    const int smem = L.total + 1024;
+    const bool one = (M == 1);
+    auto kern = one ? qmv_tma_kernel<true> : qmv_tma_kernel<false>;
+    if (!g_attr_done[one][dev].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+        if (e != cudaSuccess) return e;
+        g_attr_done[one][dev].store(1, std::memory_order_release);
+    }
+    CUtensorMap tw, ts, tb;
+    const int G = K / 64;
+    if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.w, (uint64_t)K / 8, (uint64_t)N, (uint64_t)K / 2, 32, kRows,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.scales, (uint64_t)G, (uint64_t)N, (uint64_t)G * 2,
+                   kStageGroups, kRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.biases, (uint64_t)G, (uint64_t)N, (uint64_t)G * 2,
+                   kStageGroups, kRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    const int T = (N + kRows - 1) / kRows;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)std::min(T, sms));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, tw, ts, tb, static_cast<const __nv_bfloat16 *>(a.x),
+                              static_cast<__nv_bfloat16 *>(a.y), M, N, K, (unsigned long long)a.timeout_ns,
+                              a.status, a.debug_skip_x ? 1 : 0);
+}
+
+}  // namespace aq

@@ -70,7 +70,14 @@ enum {
      * w_packed/scales/biases before it waits for that kernel to finish.  It
      * reads x and writes y only after the wait.  PRECONDITION: the weights
      * were not written by the kernel immediately before on the stream. */
-    AQ_FLAG_PDL = 1u << 0
+    AQ_FLAG_PDL = 1u << 0,
+    /* Test hook for the failure path of the bounded device-side waits: the
+     * weight-streaming kernel's producer omits the copy of x, so its
+     * consumers' wait expires (after 20 ms instead of the normal 2 s), the
+     * kernel records a timeout in the device status word and returns without
+     * writing y.  Only for 1 <= M <= 8 with K a multiple of 512 (otherwise
+     * AQ_ERR_UNSUPPORTED).  Read the outcome with aq_read_device_status(). */
+    AQ_FLAG_DEBUG_SKIP_X = 1u << 31
 };
 
 /*
@@ -127,6 +134,13 @@ const char *aq_status_string(aq_status status);
 /* Text of the last CUDA runtime error seen by an entry point on this host
  * thread ("" if none).  Valid until the next call on this thread. */
 const char *aq_last_cuda_error(void);
+
+/* Waits for `stream` to finish, then reads and clears the library's device
+ * status word on the current device: AQ_ERR_TIMEOUT if a bounded wait inside
+ * a kernel expired since the last read (that kernel's output is then not
+ * valid), else AQ_OK; AQ_ERR_CUDA if the synchronization or copy failed.
+ * A debugging call: it synchronizes the host with the stream. */
+aq_status aq_read_device_status(void *stream);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int aq_version(void);

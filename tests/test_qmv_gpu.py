@@ -126,3 +126,38 @@ def test_special_inputs(dev):
     assert not got[0].any()
     assert np.array_equal(got[1], w.biases[:, 0])
     assert np.all((got[2] & 0x7F80) == 0x7F80) and np.all(got[2] & 0x007F)
+
+
+# ---------------------------------------------------------------- TMA-fed kernel (M <= 8, K % 512 == 0)
+
+@pytest.mark.parametrize("M,N,K", [
+    (1, 1, 512), (1, 16, 512), (1, 17, 1024), (1, 33, 2560), (1, 100, 4096), (1, 257, 14336), (1, 64, 16384),
+    (2, 45, 1536), (2, 300, 8192), (3, 31, 3072), (4, 200, 4096), (5, 15, 2048), (8, 77, 2048), (7, 129, 512),
+    (2, 50, 8704), (8, 40, 2560),   # M*K beyond the TMA kernel's x budget: generic kernel
+])
+def test_tma_kernel_shapes(dev, M, N, K):
+    check(dev, M, N, K, 7 * M + N + K)
+
+
+def test_tma_kernel_many_tiles_per_cta(dev):
+    # more 16-row tiles than SMs: every CTA walks several tiles and stages wrap the ring
+    check(dev, 1, 16 * 152 * 3 + 5, 1024, 77)
+
+
+def test_bounded_wait_timeout_reports_status(dev):
+    """The test hook leaves the x barrier incomplete: the kernel's bounded wait
+    expires, it records a timeout, the host reads AQ_ERR_TIMEOUT, and the
+    context stays usable (a normal call right after is correct)."""
+    import torch
+    M, N, K = 1, 64, 1024
+    w = synth.make_weights(N, K, 8)
+    x = synth.make_x(M, K, 8)
+    xt, wt, st, bt = upload(x, w, dev)
+    assert aq.aq_read_device_status(None) == aq.AQ_OK
+    aq.matmul(xt, wt, st, bt, flags=aq.AQ_FLAG_DEBUG_SKIP_X)
+    assert aq.aq_read_device_status(torch.cuda.current_stream().cuda_stream) == aq.AQ_ERR_TIMEOUT
+    assert aq.aq_read_device_status(None) == aq.AQ_OK          # cleared by the read
+    check(dev, M, N, K, 8)
+    with pytest.raises(aq.AqError):
+        aq.matmul(xt[:, :64].contiguous(), wt[:, :8].contiguous(), st[:, :1].contiguous(), bt[:, :1].contiguous(),
+                  flags=aq.AQ_FLAG_DEBUG_SKIP_X)                # K = 64: no TMA kernel, hook unsupported
