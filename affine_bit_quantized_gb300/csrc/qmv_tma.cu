@@ -125,10 +125,25 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
     return v;
 }
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+    return v;
+}
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
-// (128 + q[p], 128 + q[p+4]) as bf16x2, from a word already shifted right by 4p.
-__device__ __forceinline__ uint32_t code_pair(uint32_t v) { return (v & 0x000F000Fu) | kMagic; }
+// (128 + q[p], 128 + q[p+4]) as bf16x2, from a word already shifted right by
+// 4p: (v & 0x000F000F) | magic in one LOP3 (truth table 0xEA = (a & b) | c).
+__device__ __forceinline__ uint32_t code_pair(uint32_t v, uint32_t magic) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;" : "=r"(r) : "r"(v), "r"(magic));
+    return r;
+}
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -159,7 +174,7 @@ __host__ __device__ inline Layout make_layout(int M, int K) {
 
 // ONE_ROW: M == 1 (only column 0 of the MMA output is used).
 template <bool ONE_ROW>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
                const __grid_constant__ CUtensorMap tm_b, const __nv_bfloat16 *__restrict__ x,
                __nv_bfloat16 *__restrict__ y, int M, int N, int K, unsigned long long timeout_ns,
@@ -299,41 +314,51 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
     }
     consumer_sync();
 
+    // Per-thread shared-memory offsets, fixed for the whole kernel.  Codes:
+    // rows r0 / r1 of this warp's 256-code block, word pair 2j..2j+1 of group
+    // g, undone 128-byte swizzle (16-byte chunk index XOR row % 8).
+    uint32_t coff[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+        coff[g] = (uint32_t)(warp * kCodeBlockBytes + r0 * 128 + ((((2 * g + (j >> 1)) ^ gid) << 4) | ((j & 1) << 3)));
+    const uint32_t soff = (uint32_t)(kCodesBytes + r0 * 64 + 8 * warp);      // scales of row r0; row r1 at +512
+    const uint32_t xs_thread = x_s + (uint32_t)(gid * K * 2 + warp * 512 + 2 * j * 16);
+    const uint32_t xsum_s = smem_addr(xsum);
+    const uint32_t xsum_thread = ONE_ROW ? xsum_s + warp * 16 : xsum_s + (uint32_t)(2 * j * G * 4 + warp * 16);
+    const uint32_t magic = kMagic;
+    const bool has_x = gid < M;
+    const bool xs0_ok = 2 * j < M, xs1_ok = 2 * j + 1 < M;
+
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     int par = 0;
+    int slot = 0, kb = 0, tile = (int)blockIdx.x;
+    uint32_t phase = 0;
     for (int it = 0; it < L_items; ++it) {
-        const int slot = it % kStages;
-        const int kb = it % KB;
-        if (alive && !mbar_wait(bar_full + 8 * slot, (it / kStages) & 1, deadline, abort_flag)) fail();
+        if (alive && !mbar_wait(bar_full + 8 * slot, phase, deadline, abort_flag)) fail();
         const int blk = kb * kConsumerWarps + warp;
         if (alive && blk < nblk) {
-            const uint8_t *st = smem + slot * kStageBytes;
-            const uint8_t *cb = st + warp * kCodeBlockBytes;
-            const uint8_t *sb = st + kCodesBytes;
-            const uint8_t *bb = sb + kSBBytes;
-            const uint2 s0 = *reinterpret_cast<const uint2 *>(sb + r0 * 64 + 8 * warp);
-            const uint2 s1 = *reinterpret_cast<const uint2 *>(sb + r1 * 64 + 8 * warp);
-            const uint2 b0 = *reinterpret_cast<const uint2 *>(bb + r0 * 64 + 8 * warp);
-            const uint2 b1 = *reinterpret_cast<const uint2 *>(bb + r1 * 64 + 8 * warp);
-            const uint8_t *xrow = smem + kStages * kStageBytes + (size_t)gid * K * 2;
+            const uint32_t st = s_base + slot * kStageBytes;
+            const uint2 s0 = lds64(st + soff), s1 = lds64(st + soff + 512);
+            const uint2 b0 = lds64(st + soff + kSBBytes), b1 = lds64(st + soff + kSBBytes + 512);
+            const uint32_t xb = xs_thread + kb * (kConsumerWarps * 512);
+            const uint32_t xsb = xsum_thread + kb * (kConsumerWarps * 16);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
-                const int c = 2 * g + (j >> 1);
-                const int off = ((c ^ gid) << 4) | ((j & 1) << 3);
-                const uint2 w0 = *reinterpret_cast<const uint2 *>(cb + r0 * 128 + off);
-                const uint2 w1 = *reinterpret_cast<const uint2 *>(cb + r1 * 128 + off);
-                const int gg = blk * 4 + g;                    // group index in K
+                const uint2 w0 = lds64(st + coff[g]);
+                const uint2 w1 = lds64(st + coff[g] + 1024);
                 float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
                     const uint32_t wa = i ? w0.y : w0.x;
                     const uint32_t wb = i ? w1.y : w1.x;
                     uint4 X = make_uint4(0u, 0u, 0u, 0u);
-                    if (gid < M) X = *reinterpret_cast<const uint4 *>(xrow + (gg * 8 + 2 * j + i) * 16);
+                    if (has_x) X = lds128(xb + g * 128 + i * 16);
                     const uint32_t wa4 = wa >> 4, wb4 = wb >> 4, wa8 = wa >> 8, wb8 = wb >> 8;
-                    mma_bf16_16816(d, code_pair(wa), code_pair(wb), code_pair(wa4), code_pair(wb4), X.x, X.y);
-                    mma_bf16_16816(d, code_pair(wa8), code_pair(wb8), code_pair(wa8 >> 4), code_pair(wb8 >> 4), X.z,
-                                   X.w);
+                    const uint32_t wa12 = wa >> 12, wb12 = wb >> 12;
+                    mma_bf16_16816(d, code_pair(wa, magic), code_pair(wb, magic), code_pair(wa4, magic),
+                                   code_pair(wb4, magic), X.x, X.y);
+                    mma_bf16_16816(d, code_pair(wa8, magic), code_pair(wb8, magic), code_pair(wa12, magic),
+                                   code_pair(wb12, magic), X.z, X.w);
                 }
                 const uint32_t sw0 = (g < 2) ? s0.x : s0.y, sw1 = (g < 2) ? s1.x : s1.y;
                 const uint32_t bw0 = (g < 2) ? b0.x : b0.y, bw1 = (g < 2) ? b1.x : b1.y;
@@ -342,12 +367,12 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                 const float p0 = fmaf(-128.f, sc0, (g & 1) ? bf16hi(bw0) : bf16lo(bw0));
                 const float p1 = fmaf(-128.f, sc1, (g & 1) ? bf16hi(bw1) : bf16lo(bw1));
                 if (ONE_ROW) {
-                    const float xs = xsum[gg];
+                    const float xs = lds_f32(xsb + g * 4);
                     acc[0] = fmaf(sc0, d[0], fmaf(p0, xs, acc[0]));
                     acc[2] = fmaf(sc1, d[2], fmaf(p1, xs, acc[2]));
                 } else {
-                    const float xs0 = (2 * j < M) ? xsum[(2 * j) * G + gg] : 0.f;
-                    const float xs1 = (2 * j + 1 < M) ? xsum[(2 * j + 1) * G + gg] : 0.f;
+                    const float xs0 = xs0_ok ? lds_f32(xsb + g * 4) : 0.f;
+                    const float xs1 = xs1_ok ? lds_f32(xsb + G * 4 + g * 4) : 0.f;
                     acc[0] = fmaf(sc0, d[0], fmaf(p0, xs0, acc[0]));
                     acc[1] = fmaf(sc0, d[1], fmaf(p0, xs1, acc[1]));
                     acc[2] = fmaf(sc1, d[2], fmaf(p1, xs0, acc[2]));
@@ -362,7 +387,6 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
 
         if (kb == KB - 1) {
             // tile finished: combine the eight warps' partial sums in order
-            const int tile = (int)blockIdx.x + (it / KB) * (int)gridDim.x;
             float *rb = red + par * (kConsumerWarps * kRows * 8);
             float *rw = rb + warp * (kRows * 8);
             rw[r0 * 8 + 2 * j] = acc[0];
@@ -383,6 +407,14 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                 }
             }
             par ^= 1;
+            kb = 0;
+            tile += (int)gridDim.x;
+        } else {
+            ++kb;
+        }
+        if (++slot == kStages) {
+            slot = 0;
+            phase ^= 1u;
         }
     }
 }
@@ -416,7 +448,9 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint6
 }
 
 constexpr int kMaxDevices = 64;
+constexpr int kMaxCtasPerSm = 2;
 std::atomic<int> g_sms[kMaxDevices];
+std::atomic<int> g_smem_per_sm[kMaxDevices];
 std::atomic<int> g_attr_done[2][kMaxDevices];
 
 }  // namespace
@@ -436,6 +470,12 @@ cudaError_t launch_qmv_tma(const MatmulArgs &a) {
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         g_sms[dev].store(sms, std::memory_order_relaxed);
+    }
+    int smem_sm = g_smem_per_sm[dev].load(std::memory_order_relaxed);
+    if (smem_sm == 0) {
+        e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        if (e != cudaSuccess) return e;
+        g_smem_per_sm[dev].store(smem_sm, std::memory_order_relaxed);
     }
     const int M = (int)a.M, N = (int)a.N, K = (int)a.K;
     const Layout L = make_layout(M, K);
@@ -457,8 +497,10 @@ cudaError_t launch_qmv_tma(const MatmulArgs &a) {
                    kStageGroups, kRows, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     const int T = (N + kRows - 1) / kRows;
+    // CTAs per SM that fit in shared memory (1 KB per CTA is reserved by the system)
+    const int per_sm = std::max(1, std::min(kMaxCtasPerSm, smem_sm / (smem + 1024)));
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)std::min(T, sms));
+    cfg.gridDim = dim3((unsigned)std::min(T, sms * per_sm));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = a.stream;

@@ -186,6 +186,58 @@ def run_reference(args, target_seconds: float = 150.0):
     print(json.dumps(line), flush=True)
 
 
+def run_case(args):
+    """Time y = x . dequant(W)^T for one (M, N, K) through the C ABI: enough
+    distinct weight copies to exceed 3x L2 are cycled so that no launch finds
+    its weights in L2; CUDA events around `steps` launches."""
+    import torch
+
+    import affine_bit_quantized_gb300 as aq
+    from affine_bit_quantized_gb300 import _build
+
+    M, N, K = (int(v) for v in args.case.split(","))
+    dev = torch.device("cuda", 0)
+    _build.build_library()
+    lib = aq.load()
+    w = synth.make_weights(N, K, 1)
+    x = synth.make_x(M, K, 1)
+    wbytes = w.nbytes
+    copies = max(1, min(64, -(-3 * 129 * 2**20 // wbytes)))
+    ws = []
+    for c in range(copies):
+        ws.append((torch.from_numpy(w.w_packed.view(np.int32)).to(dev),
+                   torch.from_numpy(w.scales.view(np.int16)).to(dev),
+                   torch.from_numpy(w.biases.view(np.int16)).to(dev)))
+    xt = torch.from_numpy(x.view(np.int16)).to(dev)
+    yt = torch.empty((M, N), dtype=torch.int16, device=dev)
+    kernel = {"auto": aq.AQ_KERNEL_AUTO, "qmv": aq.AQ_KERNEL_QMV, "qmm": aq.AQ_KERNEL_QMM}[args.kernel]
+    stream = torch.cuda.current_stream(dev)
+
+    def launch(i):
+        wt, st, bt = ws[i % copies]
+        rc = lib.aq_matmul_bf16_ex(xt.data_ptr(), wt.data_ptr(), st.data_ptr(), bt.data_ptr(), yt.data_ptr(), M, N,
+                                   K, 64, 4, kernel, 0, stream.cuda_stream)
+        if rc != aq.AQ_OK:
+            raise aq.AqError(rc, "aq_matmul_bf16_ex")
+
+    for i in range(args.warmup):
+        launch(i)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        launch(args.warmup + i)
+    e1.record(stream)
+    e1.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    hbm_peak, bf16_peak, _, _ = load_peaks()
+    gbs = alg_bytes(M, N, K) / (us * 1e-6) / 1e9
+    tflops = 2.0 * M * N * K / (us * 1e-6) / 1e12
+    print(json.dumps({"case": [M, N, K], "kernel": args.kernel, "us_per_call": round(us, 3), "gbs": round(gbs, 1),
+                      "hbm_frac": round(gbs / hbm_peak, 4), "tflops": round(tflops, 2),
+                      "bf16_frac": round(tflops / bf16_peak, 4), "weight_copies": copies}), flush=True)
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for name in ("qmv.cu",):
@@ -220,6 +272,9 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--layers", type=int, default=32, help="decoder layers in the step (32 = the workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default=None,
+                    help="M,N,K: time one matrix shape instead of the decode step (also the ncu target)")
+    ap.add_argument("--kernel", choices=("auto", "qmv", "qmm"), default="auto", help="kernel for --case")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -231,6 +286,9 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             run_reference(args)
+        return
+    if args.case:
+        run_case(args)
         return
 
     import torch
