@@ -497,7 +497,9 @@ cudaError_t launch_qmv_tma(const MatmulArgs &a) {
                    kStageGroups, kRows, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     const int T = (N + kRows - 1) / kRows;
-    // CTAs per SM that fit in shared memory (1 KB per CTA is reserved by the system)
+    // CTAs per SM that fit in shared memory (1 KB per CTA is reserved by the
+    // system).  Two CTAs per SM measured faster than one, also in a chain of
+    // launches with programmatic dependent launch.
     const int per_sm = std::max(1, std::min(kMaxCtasPerSm, smem_sm / (smem + 1024)));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)std::min(T, sms * per_sm));
