@@ -240,7 +240,7 @@ def run_case(args):
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for name in ("qmv.cu",):
+    for name in ("qmv.cu", "qmv_tma.cu"):
         with open(os.path.join(ROOT, "affine_bit_quantized_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
