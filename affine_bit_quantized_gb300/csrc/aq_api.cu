@@ -84,8 +84,6 @@ aq_status aq_matmul_bf16_ex(const void *x, const uint32_t *w_packed, const void 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (K == 0) return record_cuda(cudaMemsetAsync(y, 0, (size_t)(M * N) * 2, cs));
 
-    if (kernel == AQ_KERNEL_QMM) return AQ_ERR_UNSUPPORTED;
-
     aq::MatmulArgs a;
     a.w = w_packed;
     a.scales = static_cast<const uint16_t *>(scales);
@@ -98,7 +96,15 @@ aq_status aq_matmul_bf16_ex(const void *x, const uint32_t *w_packed, const void 
     a.timeout_ns = a.debug_skip_x ? kDebugTimeoutNs : kTimeoutNs;
     st = record_cuda(status_ptr(&a.status));
     if (st != AQ_OK) return st;
-    if (M <= 8) {
+    a.x = x;
+    a.y = y;
+    a.M = M;
+    if (kernel == AQ_KERNEL_QMM || (kernel == AQ_KERNEL_AUTO && M > kQmvMaxRows)) {
+        if (a.debug_skip_x) return AQ_ERR_UNSUPPORTED;
+        if (aq::qmm_supported(a)) return record_cuda(aq::launch_qmm(a));
+        if (kernel == AQ_KERNEL_QMM) return AQ_ERR_UNSUPPORTED;
+    }
+    if (M <= 8 && kernel != AQ_KERNEL_QMM) {
         a.x = x;
         a.y = y;
         a.M = M;

@@ -34,7 +34,9 @@ cudaError_t launch_qmv(const MatmulArgs &a);
 bool qmv_tma_supported(const MatmulArgs &a);
 cudaError_t launch_qmv_tma(const MatmulArgs &a);
 
-// Tensor-core kernel (qmm.cu).  Requires M >= 1, N >= 1, K >= 64.
+// Tensor-core kernel (qmm.cu) for any M >= 1 with K % 512 == 0 and 16-byte
+// aligned scales/biases.
+bool qmm_supported(const MatmulArgs &a);
 cudaError_t launch_qmm(const MatmulArgs &a);
 
 }  // namespace aq

@@ -1,0 +1,529 @@
+// Tensor-core kernel for y = x . dequant(W)^T at prefill sizes (M > 16),
+// on the 5th-generation tensor cores (tcgen05) of sm_103a.
+//
+// The pages name a quantized GEMM for Blackwell prefill as the large-M
+// counterpart of the decode matvec ("epic: CUDA (MLX backend) prefill and
+// decode acceleration program", code-audit findings and Phase 6).  At M in
+// the hundreds to thousands the work is a real dense contraction, so here it
+// runs on tcgen05.mma with fp32 accumulators in tensor memory (TMEM):
+//
+//   * CTA tile 256 (rows of x) x 256 (rows of W), K walked one group of 64 at
+//     a time; two 128 x 256 fp32 accumulators fill the 512 TMEM columns.
+//   * warp 0 (one thread) streams raw tiles with TMA: x (bf16, 128-byte
+//     swizzle), the packed codes of the 256 W rows, and every 8 groups the
+//     rows' bf16 scales and biases;
+//   * warps 2..9 turn a raw stage into the MMA operands, in the canonical
+//     K-major 128-byte-swizzled layout: W is dequantized to fp16 as
+//     fp16(scale * q + bias) (q made exact with the 1024 + q exponent trick,
+//     then one HFMA2, so one rounding per weight), and x is converted from
+//     bf16 to fp16.  fp16 rather than bf16 because a bf16 weight (8-bit
+//     significand) perturbs y by about twice the tolerance on these shapes,
+//     while fp16 (11 bits) stays about 6 sigma inside it.  Inside every
+//     8-element chunk both operands use the k order (0,4,1,5,2,6,3,7), which
+//     lets one LOP3 build a pair of codes; the dot product is unchanged;
+//   * warp 1 allocates TMEM and one of its threads issues the MMAs
+//     (M=128, N=256, K=16, both operands from shared memory), committing each
+//     consumed stage back to the converters through an mbarrier;
+//   * after the last group, warps 2..9 read the accumulators with tcgen05.ld,
+//     round to bf16 and store y.
+//
+// Every mbarrier wait is bounded by a global-timer deadline; on expiry the
+// kernel records a timeout in the device status word, stops issuing work,
+// waits (bounded) for what it already issued, frees its TMEM and returns.
+//
+// Numerics precondition of this path: x, scales and biases inside the fp16
+// normal range (|v| < 65504; magnitudes below 2^-14 lose relative precision).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+
+#include "aq_internal.h"
+
+namespace aq {
+namespace {
+
+constexpr int kTileM = 256;            // rows of x per CTA (two UMMA M=128 halves)
+constexpr int kTileN = 256;            // rows of W per CTA (UMMA N)
+constexpr int kGroup = 64;             // K per pipeline step (one quantization group)
+constexpr int kConvWarps = 8;
+constexpr int kThreads = (2 + kConvWarps) * 32;
+constexpr int kConvThreads = kConvWarps * 32;
+constexpr int kSBGroups = 8;           // groups of scales/biases per TMA box (16 bytes per row)
+
+// shared memory layout (offsets from a 1024-aligned base)
+constexpr int kATileBytes = kTileM * 128;          // 32768: fp16 x, 256 rows x 64 k
+constexpr int kBTileBytes = kTileN * 128;          // 32768: fp16 W, 256 rows x 64 k
+constexpr int kConvStageBytes = kATileBytes + kBTileBytes;
+constexpr int kConvStages = 2;
+constexpr int kRawXBytes = kTileM * 128;           // 32768: bf16 x, same swizzled geometry
+constexpr int kRawCodeBytes = kTileN * 32;         // 8192: 8 words per row
+constexpr int kRawStageBytes = kRawXBytes + kRawCodeBytes;
+constexpr int kRawStages = 2;
+constexpr int kSBBytes = kTileN * kSBGroups * 2;   // 4096 (scales, and again biases)
+constexpr int kSBStages = 2;
+constexpr int kOffConv = 0;
+constexpr int kOffRaw = kOffConv + kConvStages * kConvStageBytes;       // 131072
+constexpr int kOffSB = kOffRaw + kRawStages * kRawStageBytes;           // 212992
+constexpr int kOffBar = kOffSB + kSBStages * 2 * kSBBytes;              // 229376
+// barriers: raw_full[2], raw_empty[2], sb_full[2], sb_empty[2], conv_full[2], conv_empty[2], acc_done
+constexpr int kNumBars = 2 * kRawStages + 2 * kSBStages + 2 * kConvStages + 1;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;                        // tmem address, abort flag
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;                        // + alignment slack
+
+constexpr uint32_t kTmemCols = 512;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t global_timer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t deadline,
+                                          const volatile int *abort_flag) {
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (global_timer() > deadline) return false;
+    }
+    return true;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(dst),
+        "l"(map), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint16_t lds16(uint32_t a) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// fp16x2 (1024 + q[p], 1024 + q[p+4]) from a word shifted right by 4p.
+__device__ __forceinline__ uint32_t code_pair_f16(uint32_t v, uint32_t magic) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;" : "=r"(r) : "r"(v), "r"(magic));
+    return r;
+}
+// fp16x2: (pair - 1024) * s + b, with the subtraction exact and one rounding in the FMA
+__device__ __forceinline__ uint32_t dequant_pair(uint32_t pair, uint32_t s2, uint32_t b2, uint32_t off2) {
+    uint32_t q, w;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(q) : "r"(pair), "r"(off2));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(w) : "r"(q), "r"(s2), "r"(b2));
+    return w;
+}
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(uint32_t lo, uint32_t hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(__uint_as_float(hi)), "f"(__uint_as_float(lo)));
+    return r;
+}
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// tcgen05 shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row
+// groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);  // start address
+    d |= (uint64_t)1 << 16;                   // leading-dimension offset (unused with this swizzle)
+    d |= (uint64_t)(1024 >> 4) << 32;         // stride-dimension offset: next 8-row group
+    d |= (uint64_t)1 << 46;                   // descriptor version
+    d |= (uint64_t)2 << 61;                   // 128-byte swizzle
+    return d;
+}
+// instruction descriptor: D f32, A f16, B f16, both K-major, M=128, N=256
+constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(kTileN >> 3) << 17) |
+                            ((uint32_t)(128 >> 4) << 24);
+
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+           const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_b,
+           __nv_bfloat16 *__restrict__ y, int M, int N, int K, unsigned long long timeout_ns, int *status) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_base = smem_addr(smem_raw);
+    const uint32_t base = (raw_base + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw_base);
+
+    const uint32_t bar0 = base + kOffBar;
+    auto raw_full = [&](int s) { return bar0 + 8 * s; };
+    auto raw_empty = [&](int s) { return bar0 + 8 * (kRawStages + s); };
+    auto sb_full = [&](int s) { return bar0 + 8 * (2 * kRawStages + s); };
+    auto sb_empty = [&](int s) { return bar0 + 8 * (2 * kRawStages + kSBStages + s); };
+    auto conv_full = [&](int s) { return bar0 + 8 * (2 * kRawStages + 2 * kSBStages + s); };
+    auto conv_empty = [&](int s) { return bar0 + 8 * (2 * kRawStages + 2 * kSBStages + kConvStages + s); };
+    const uint32_t acc_done = bar0 + 8 * (kNumBars - 1);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * kTileN;
+    const int m0 = blockIdx.y * kTileM;
+    const int steps = K / kGroup;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kRawStages; ++s) {
+            mbar_init(raw_full(s), 1);
+            mbar_init(raw_empty(s), kConvWarps);
+        }
+        for (int s = 0; s < kSBStages; ++s) {
+            mbar_init(sb_full(s), 1);
+            mbar_init(sb_empty(s), kConvWarps);
+        }
+        for (int s = 0; s < kConvStages; ++s) {
+            mbar_init(conv_full(s), kConvWarps);
+            mbar_init(conv_empty(s), 1);
+        }
+        mbar_init(acc_done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    griddep_launch();
+    griddep_wait();  // x (and y) may belong to the preceding kernel
+    const uint64_t deadline = global_timer() + timeout_ns;
+
+    auto fail = [&]() {
+        if (!*abort_flag) {
+            atomicExch(status, (int)AQ_DEVICE_STATUS_TIMEOUT);
+            *abort_flag = 1;
+        }
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int issued_raw = 0, issued_sb = 0;
+            bool ok = true;
+            for (int i = 0; i < steps && ok; ++i) {
+                const int rs = i % kRawStages;
+                if (i % kSBGroups == 0) {
+                    const int j = i / kSBGroups, ss = j % kSBStages;
+                    if (j >= kSBStages && !mbar_wait(sb_empty(ss), ((j / kSBStages) - 1) & 1, deadline, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst = base + kOffSB + ss * 2 * kSBBytes;
+                    mbar_expect_tx(sb_full(ss), 2 * kSBBytes);
+                    tma_load_2d(dst, &tm_s, j * kSBGroups, n0, sb_full(ss));
+                    tma_load_2d(dst + kSBBytes, &tm_b, j * kSBGroups, n0, sb_full(ss));
+                    issued_sb = j + 1;
+                }
+                if (i >= kRawStages && !mbar_wait(raw_empty(rs), ((i / kRawStages) - 1) & 1, deadline, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t dst = base + kOffRaw + rs * kRawStageBytes;
+                mbar_expect_tx(raw_full(rs), kRawStageBytes);
+                tma_load_2d(dst, &tm_x, i * kGroup, m0, raw_full(rs));
+                tma_load_2d(dst + kRawXBytes, &tm_w, i * (kGroup / 8), n0, raw_full(rs));
+                issued_raw = i + 1;
+            }
+            if (!ok) {
+                fail();
+                // let the copies already issued land before the CTA may exit
+                const uint64_t drain = global_timer() + timeout_ns;
+                for (int i = (issued_raw > kRawStages ? issued_raw - kRawStages : 0); i < issued_raw; ++i)
+                    while (!mbar_try_wait(raw_full(i % kRawStages), (i / kRawStages) & 1) && global_timer() < drain) {
+                    }
+                for (int j = (issued_sb > kSBStages ? issued_sb - kSBStages : 0); j < issued_sb; ++j)
+                    while (!mbar_try_wait(sb_full(j % kSBStages), (j / kSBStages) & 1) && global_timer() < drain) {
+                    }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            for (int i = 0; i < steps; ++i) {
+                const int cs = i % kConvStages;
+                if (!mbar_wait(conv_full(cs), (i / kConvStages) & 1, deadline, abort_flag)) {
+                    fail();
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a0 = base + kOffConv + cs * kConvStageBytes;
+                const uint32_t b0 = a0 + kATileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kGroup / 16; ++kk) {
+                    const uint64_t bd = sw128_desc(b0 + kk * 32);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        umma_f16(tmem + h * kTileN, sw128_desc(a0 + h * (kATileBytes / 2) + kk * 32), bd,
+                                 (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                umma_commit(conv_empty(cs));
+            }
+            // acc_done fires when every MMA issued so far has completed (also on abort)
+            umma_commit(acc_done);
+        }
+    } else {
+        // ------------------------------------------------------------ converters
+        const int t = threadIdx.x - 64;  // 0..255
+        const uint32_t magic = 0x64006400u;   // fp16x2 (1024, 1024)
+        const uint32_t off2 = 0x64006400u;
+        bool alive = true;
+        for (int i = 0; i < steps; ++i) {
+            const int rs = i % kRawStages, cs = i % kConvStages, ss = (i / kSBGroups) % kSBStages;
+            if (alive && !mbar_wait(raw_full(rs), (i / kRawStages) & 1, deadline, abort_flag)) alive = false;
+            if (alive && !mbar_wait(sb_full(ss), (i / (kSBGroups * kSBStages)) & 1, deadline, abort_flag))
+                alive = false;
+            if (alive && i >= kConvStages &&
+                !mbar_wait(conv_empty(cs), ((i / kConvStages) - 1) & 1, deadline, abort_flag))
+                alive = false;
+            alive = __all_sync(0xFFFFFFFFu, alive);  // keep the warp's decisions uniform
+            if (!alive) {
+                fail();
+                break;
+            }
+            const uint32_t raw = base + kOffRaw + rs * kRawStageBytes;
+            const uint32_t conv = base + kOffConv + cs * kConvStageBytes;
+            // x: bf16 -> fp16, chunk by chunk at the same (swizzled) offsets,
+            // each chunk's k order becoming (0,4,1,5,2,6,3,7)
+#pragma unroll 4
+            for (int c = 0; c < kRawXBytes / 16 / kConvThreads; ++c) {
+                const uint32_t off = (uint32_t)((c * kConvThreads + t) * 16);
+                const uint4 v = lds128(raw + off);
+                uint4 o;
+                o.x = f32x2_to_f16x2(bf16lo(v.x), bf16lo(v.z));
+                o.y = f32x2_to_f16x2(bf16hi(v.x), bf16hi(v.z));
+                o.z = f32x2_to_f16x2(bf16lo(v.y), bf16lo(v.w));
+                o.w = f32x2_to_f16x2(bf16hi(v.y), bf16hi(v.w));
+                sts128(conv + off, o);
+            }
+            // W: word (row r, chunk c) -> 8 fp16 weights at row r, chunk c ^ (r & 7)
+            const uint32_t sb = base + kOffSB + ss * 2 * kSBBytes;
+            const int g8 = i % kSBGroups;
+#pragma unroll 2
+            for (int e = 0; e < kRawCodeBytes / 4 / kConvThreads; ++e) {
+                const int wi = e * kConvThreads + t;
+                const int r = wi >> 3, c = wi & 7;
+                const uint32_t w = lds32(raw + kRawXBytes + wi * 4);
+                const __half sh = __float2half_rn(__uint_as_float((uint32_t)lds16(sb + (r * kSBGroups + g8) * 2) << 16));
+                const __half bh =
+                    __float2half_rn(__uint_as_float((uint32_t)lds16(sb + kSBBytes + (r * kSBGroups + g8) * 2) << 16));
+                const uint32_t s2 = (uint32_t)__half_as_ushort(sh) * 0x00010001u;
+                const uint32_t b2 = (uint32_t)__half_as_ushort(bh) * 0x00010001u;
+                uint4 o;
+                o.x = dequant_pair(code_pair_f16(w, magic), s2, b2, off2);
+                o.y = dequant_pair(code_pair_f16(w >> 4, magic), s2, b2, off2);
+                o.z = dequant_pair(code_pair_f16(w >> 8, magic), s2, b2, off2);
+                o.w = dequant_pair(code_pair_f16(w >> 12, magic), s2, b2, off2);
+                sts128(conv + kATileBytes + r * 128 + ((c ^ (r & 7)) << 4), o);
+            }
+            fence_proxy_async();  // make the generic-proxy stores visible to the MMA (async proxy)
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(conv_full(cs));
+                mbar_arrive(raw_empty(rs));
+                if (g8 == kSBGroups - 1 || i == steps - 1) mbar_arrive(sb_empty(ss));
+            }
+        }
+        // ------------------------------------------------------------ epilogue
+        bool go = alive && mbar_wait(acc_done, 0, deadline, abort_flag) && !*abort_flag;
+        go = __all_sync(0xFFFFFFFFu, go);   // tcgen05.ld below is warp-collective
+        if (go) {
+            tc_fence_after();
+            const int q = warp & 3;                 // TMEM lane quarter this warp may access
+            const int h = (warp - 2) >> 2;          // accumulator half: x rows 128h..128h+127
+            const int m = m0 + h * 128 + q * 32 + lane;
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * kTileN);
+#pragma unroll 1
+            for (int j = 0; j < kTileN / 32; ++j) {
+                uint32_t r[32];
+                tmem_ld32(tbase + j * 32, r);
+                const int n = n0 + j * 32;
+                if (m < M) {
+                    __nv_bfloat16 *yp = y + (int64_t)m * N + n;
+                    if (n + 32 <= N && (((uintptr_t)yp) & 15) == 0) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 o;
+                            o.x = f32x2_to_bf16x2(r[8 * v + 0], r[8 * v + 1]);
+                            o.y = f32x2_to_bf16x2(r[8 * v + 2], r[8 * v + 3]);
+                            o.z = f32x2_to_bf16x2(r[8 * v + 4], r[8 * v + 5]);
+                            o.w = f32x2_to_bf16x2(r[8 * v + 6], r[8 * v + 7]);
+                            *reinterpret_cast<uint4 *>(yp + 8 * v) = o;
+                        }
+                    } else {
+#pragma unroll
+                        for (int v = 0; v < 32; ++v)
+                            if (n + v < N) yp[v] = __float2bfloat16_rn(__uint_as_float(r[v]));
+                    }
+                }
+            }
+        } else if (alive) {
+            fail();
+        }
+    }
+
+    // every role ends here; wait (bounded) for the MMAs before freeing TMEM
+    if (warp == 1 && lane == 0 && *abort_flag) {
+        const uint64_t drain = global_timer() + timeout_ns;
+        while (!mbar_try_wait(acc_done, 0) && global_timer() < drain) {
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *gaddr, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, dt, 2, const_cast<void *>(gaddr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_attr_done[kMaxDevices];
+
+}  // namespace
+
+bool qmm_supported(const MatmulArgs &a) {
+    return a.K % 512 == 0 && a.M >= 1 && a.N >= 1 && encode_fn() != nullptr &&
+           (reinterpret_cast<uintptr_t>(a.scales) & 15) == 0 && (reinterpret_cast<uintptr_t>(a.biases) & 15) == 0;
+}
+
+cudaError_t launch_qmm(const MatmulArgs &a) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!g_attr_done[dev].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(qmm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        g_attr_done[dev].store(1, std::memory_order_release);
+    }
+    const int M = (int)a.M, N = (int)a.N, K = (int)a.K, G = K / 64;
+    CUtensorMap tx, tw, ts, tb;
+    if (!encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, kGroup, kTileM,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.w, (uint64_t)K / 8, (uint64_t)N, (uint64_t)K / 2, kGroup / 8,
+                   kTileN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.scales, (uint64_t)G, (uint64_t)N, (uint64_t)G * 2, kSBGroups,
+                   kTileN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.biases, (uint64_t)G, (uint64_t)N, (uint64_t)G * 2, kSBGroups,
+                   kTileN, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + kTileM - 1) / kTileM));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, qmm_kernel, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(a.y), M, N, K,
+                              (unsigned long long)a.timeout_ns, a.status);
+}
+
+}  // namespace aq
