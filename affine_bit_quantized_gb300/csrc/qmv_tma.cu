@@ -60,8 +60,9 @@ constexpr int kMaxXBytes = 32768;                          // M*K*2 limit for st
 constexpr int kRedBytes = 2 * kConsumerWarps * kRows * 8 * 4;  // double-buffered cross-warp sums
 constexpr uint32_t kMagic = 0x43004300u;   // bf16x2 (128.0, 128.0)
 // largest layout: x of 32 KB, X sums of M*K/16 bytes, barriers, alignment slack
-constexpr int kMaxSmem = kStages * kStageBytes + kMaxXBytes + kMaxXBytes / 16 + 16 + kRedBytes +
-                         (2 * kStages + 1) * 8 + 16 + 1024;
+constexpr int kNumBars = 2 * kStages + 1 + 4;   // full[S], empty[S], x, red_full[2], red_empty[2]
+constexpr int kMaxSmem = kStages * kStageBytes + kMaxXBytes + kMaxXBytes / 16 + 16 + kRedBytes + kNumBars * 8 +
+                         16 + 1024;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -135,6 +136,15 @@ __device__ __forceinline__ float lds_f32(uint32_t a) {
     asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
     return v;
 }
+// two IEEE fused multiply-adds in one instruction: (a.x*b.x + c.x, a.y*b.y + c.y)
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
+        " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 // (128 + q[p], 128 + q[p+4]) as bf16x2, from a word already shifted right by
@@ -158,7 +168,7 @@ struct Layout {
     int x_bytes;     // M*K*2 rounded up to 16
     int xsum_off;    // float [M][G]
     int red_off;     // float [2][8][16][8]
-    int bar_off;     // uint64 [2*kStages + 1] + abort flag
+    int bar_off;     // uint64 [kNumBars] + abort flag
     int total;       // bytes (excluding the 1024 alignment slack)
 };
 __host__ __device__ inline Layout make_layout(int M, int K) {
@@ -168,7 +178,7 @@ __host__ __device__ inline Layout make_layout(int M, int K) {
     L.xsum_off = x_off + L.x_bytes;
     L.red_off = (L.xsum_off + M * (K / 64) * 4 + 15) & ~15;
     L.bar_off = L.red_off + kRedBytes;
-    L.total = L.bar_off + (2 * kStages + 1) * 8 + 16;
+    L.total = L.bar_off + kNumBars * 8 + 16;
     return L;
 }
 
@@ -189,7 +199,9 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
     const uint32_t bar_full = s_base + L.bar_off;          // kStages barriers
     const uint32_t bar_empty = bar_full + kStages * 8;     // kStages barriers
     const uint32_t bar_x = bar_empty + kStages * 8;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.bar_off + (2 * kStages + 1) * 8);
+    const uint32_t bar_red_full = bar_x + 8;               // 2 barriers: partial sums written
+    const uint32_t bar_red_empty = bar_red_full + 16;      // 2 barriers: partial sums consumed
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.bar_off + kNumBars * 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -206,6 +218,10 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
             mbar_init(bar_empty + 8 * s, kConsumerWarps);
         }
         mbar_init(bar_x, 1);
+        for (int p = 0; p < 2; ++p) {
+            mbar_init(bar_red_full + 8 * p, kConsumerWarps);
+            mbar_init(bar_red_empty + 8 * p, 1);
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -330,7 +346,7 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
     const bool xs0_ok = 2 * j < M, xs1_ok = 2 * j + 1 < M;
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    int par = 0;
+    int par = 0, tcount = 0;
     int slot = 0, kb = 0, tile = (int)blockIdx.x;
     uint32_t phase = 0;
     for (int it = 0; it < L_items; ++it) {
@@ -353,8 +369,10 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                     const uint32_t wb = i ? w1.y : w1.x;
                     uint4 X = make_uint4(0u, 0u, 0u, 0u);
                     if (has_x) X = lds128(xb + g * 128 + i * 16);
-                    const uint32_t wa4 = wa >> 4, wb4 = wb >> 4, wa8 = wa >> 8, wb8 = wb >> 8;
-                    const uint32_t wa12 = wa >> 12, wb12 = wb >> 12;
+                    // w >> 4 and w >> 12 as high halves of products (FMA pipe), w >> 8 on the ALU
+                    const uint32_t wa4 = __umulhi(wa, 1u << 28), wb4 = __umulhi(wb, 1u << 28);
+                    const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
+                    const uint32_t wa12 = __umulhi(wa, 1u << 20), wb12 = __umulhi(wb, 1u << 20);
                     mma_bf16_16816(d, code_pair(wa, magic), code_pair(wb, magic), code_pair(wa4, magic),
                                    code_pair(wb4, magic), X.x, X.y);
                     mma_bf16_16816(d, code_pair(wa8, magic), code_pair(wb8, magic), code_pair(wa12, magic),
@@ -364,19 +382,28 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                 const uint32_t bw0 = (g < 2) ? b0.x : b0.y, bw1 = (g < 2) ? b1.x : b1.y;
                 const float sc0 = (g & 1) ? bf16hi(sw0) : bf16lo(sw0);
                 const float sc1 = (g & 1) ? bf16hi(sw1) : bf16lo(sw1);
-                const float p0 = fmaf(-128.f, sc0, (g & 1) ? bf16hi(bw0) : bf16lo(bw0));
-                const float p1 = fmaf(-128.f, sc1, (g & 1) ? bf16hi(bw1) : bf16lo(bw1));
+                const float2 sc = make_float2(sc0, sc1);
+                const float2 p = fma2(make_float2(-128.f, -128.f), sc,
+                                      make_float2((g & 1) ? bf16hi(bw0) : bf16lo(bw0),
+                                                  (g & 1) ? bf16hi(bw1) : bf16lo(bw1)));
                 if (ONE_ROW) {
                     const float xs = lds_f32(xsb + g * 4);
-                    acc[0] = fmaf(sc0, d[0], fmaf(p0, xs, acc[0]));
-                    acc[2] = fmaf(sc1, d[2], fmaf(p1, xs, acc[2]));
+                    const float2 a02 = fma2(sc, make_float2(d[0], d[2]),
+                                            fma2(p, make_float2(xs, xs), make_float2(acc[0], acc[2])));
+                    acc[0] = a02.x;
+                    acc[2] = a02.y;
                 } else {
                     const float xs0 = xs0_ok ? lds_f32(xsb + g * 4) : 0.f;
                     const float xs1 = xs1_ok ? lds_f32(xsb + G * 4 + g * 4) : 0.f;
-                    acc[0] = fmaf(sc0, d[0], fmaf(p0, xs0, acc[0]));
-                    acc[1] = fmaf(sc0, d[1], fmaf(p0, xs1, acc[1]));
-                    acc[2] = fmaf(sc1, d[2], fmaf(p1, xs0, acc[2]));
-                    acc[3] = fmaf(sc1, d[3], fmaf(p1, xs1, acc[3]));
+                    const float2 xs = make_float2(xs0, xs1);
+                    const float2 a01 = fma2(make_float2(sc.x, sc.x), make_float2(d[0], d[1]),
+                                            fma2(make_float2(p.x, p.x), xs, make_float2(acc[0], acc[1])));
+                    const float2 a23 = fma2(make_float2(sc.y, sc.y), make_float2(d[2], d[3]),
+                                            fma2(make_float2(p.y, p.y), xs, make_float2(acc[2], acc[3])));
+                    acc[0] = a01.x;
+                    acc[1] = a01.y;
+                    acc[2] = a23.x;
+                    acc[3] = a23.y;
                 }
             }
         }
@@ -386,26 +413,42 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
         if (alive && lane == 0) mbar_arrive(bar_empty + 8 * slot);
 
         if (kb == KB - 1) {
-            // tile finished: combine the eight warps' partial sums in order
+            // Tile finished.  Every warp deposits its partial sums and moves on;
+            // one warp per tile (rotating) adds the eight partials in a fixed
+            // order and stores y.  Two buffers, guarded by mbarriers, so no
+            // CTA-wide barrier stalls the pipeline.
+            const uint32_t rf = bar_red_full + 8 * par, re = bar_red_empty + 8 * par;
             float *rb = red + par * (kConsumerWarps * kRows * 8);
-            float *rw = rb + warp * (kRows * 8);
-            rw[r0 * 8 + 2 * j] = acc[0];
-            rw[r0 * 8 + 2 * j + 1] = acc[1];
-            rw[r1 * 8 + 2 * j] = acc[2];
-            rw[r1 * 8 + 2 * j + 1] = acc[3];
+            if (alive && tcount >= 2 && !mbar_wait(re, ((tcount >> 1) - 1) & 1, deadline, abort_flag)) fail();
+            if (alive) {
+                float *rw = rb + warp * (kRows * 8);
+                rw[r0 * 8 + 2 * j] = acc[0];
+                rw[r0 * 8 + 2 * j + 1] = acc[1];
+                rw[r1 * 8 + 2 * j] = acc[2];
+                rw[r1 * 8 + 2 * j + 1] = acc[3];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(rf);
+            }
             acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-            consumer_sync();
-            const int t = threadIdx.x;
-            if (alive && !*abort_flag && t < kRows * M) {
-                const int m = t / kRows, row = t % kRows;
-                const int n = tile * kRows + row;
-                if (n < N) {
-                    float v = rb[row * 8 + m];
+            if (alive && warp == (tcount & (kConsumerWarps - 1))) {
+                if (!mbar_wait(rf, (tcount >> 1) & 1, deadline, abort_flag)) {
+                    fail();
+                } else {
+                    for (int idx = lane; idx < kRows * M; idx += 32) {
+                        const int m = idx / kRows, row = idx % kRows;
+                        const int n = tile * kRows + row;
+                        if (n < N) {
+                            float v = rb[row * 8 + m];
 #pragma unroll
-                    for (int w = 1; w < kConsumerWarps; ++w) v += rb[w * (kRows * 8) + row * 8 + m];
-                    y[(int64_t)m * N + n] = __float2bfloat16_rn(v);
+                            for (int w = 1; w < kConsumerWarps; ++w) v += rb[w * (kRows * 8) + row * 8 + m];
+                            y[(int64_t)m * N + n] = __float2bfloat16_rn(v);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(re);
                 }
             }
+            ++tcount;
             par ^= 1;
             kb = 0;
             tile += (int)gridDim.x;
