@@ -10,7 +10,7 @@
 #include <cstring>
 #include <vector>
 
-#include "../../include/aq.h"
+#include "aq.h"
 #include "aq_internal.h"
 
 // Device status word: bounded device-side waits that expire record

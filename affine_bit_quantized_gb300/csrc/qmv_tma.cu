@@ -369,10 +369,8 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                     const uint32_t wb = i ? w1.y : w1.x;
                     uint4 X = make_uint4(0u, 0u, 0u, 0u);
                     if (has_x) X = lds128(xb + g * 128 + i * 16);
-                    // w >> 4 and w >> 12 as high halves of products (FMA pipe), w >> 8 on the ALU
-                    const uint32_t wa4 = __umulhi(wa, 1u << 28), wb4 = __umulhi(wb, 1u << 28);
-                    const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
-                    const uint32_t wa12 = __umulhi(wa, 1u << 20), wb12 = __umulhi(wb, 1u << 20);
+                    const uint32_t wa4 = wa >> 4, wb4 = wb >> 4, wa8 = wa >> 8, wb8 = wb >> 8;
+                    const uint32_t wa12 = wa >> 12, wb12 = wb >> 12;
                     mma_bf16_16816(d, code_pair(wa, magic), code_pair(wb, magic), code_pair(wa4, magic),
                                    code_pair(wb4, magic), X.x, X.y);
                     mma_bf16_16816(d, code_pair(wa8, magic), code_pair(wb8, magic), code_pair(wa12, magic),
