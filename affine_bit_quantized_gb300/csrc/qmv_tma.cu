@@ -99,6 +99,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     }
     return true;
 }
+// Fast path of a bounded wait: one try_wait; the retry loop lives out of line.
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, uint64_t deadline,
+                                            const volatile int *abort_flag) {
+    return mbar_wait(bar, parity, deadline, abort_flag);
+}
+__device__ __forceinline__ bool mbar_wait_fast(uint32_t bar, uint32_t parity, uint64_t deadline,
+                                               const volatile int *abort_flag) {
+    return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, deadline, abort_flag);
+}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar,
                                             uint64_t policy) {
     asm volatile(
@@ -162,6 +171,15 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The same MMA with a zero accumulator input (first MMA of a group).
+__device__ __forceinline__ void mma_bf16_16816_zc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                                  uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
 
 struct Layout {
@@ -330,14 +348,16 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
     }
     consumer_sync();
 
-    // Per-thread shared-memory offsets, fixed for the whole kernel.  Codes:
-    // rows r0 / r1 of this warp's 256-code block, word pair 2j..2j+1 of group
-    // g, undone 128-byte swizzle (16-byte chunk index XOR row % 8).
-    uint32_t coff[4];
+    // Per-thread shared-memory addresses, fixed for the whole kernel (stage
+    // slot offsets are added as immediates).  Codes: row r0 of this warp's
+    // 256-code block (row r1 = +1024), word pair 2j..2j+1 of group g, with the
+    // 128-byte swizzle undone (16-byte chunk index XOR row % 8).
+    uint32_t caddr[4];
 #pragma unroll
     for (int g = 0; g < 4; ++g)
-        coff[g] = (uint32_t)(warp * kCodeBlockBytes + r0 * 128 + ((((2 * g + (j >> 1)) ^ gid) << 4) | ((j & 1) << 3)));
-    const uint32_t soff = (uint32_t)(kCodesBytes + r0 * 64 + 8 * warp);      // scales of row r0; row r1 at +512
+        caddr[g] = s_base + (uint32_t)(warp * kCodeBlockBytes + r0 * 128 +
+                                       ((((2 * g + (j >> 1)) ^ gid) << 4) | ((j & 1) << 3)));
+    const uint32_t saddr = s_base + (uint32_t)(kCodesBytes + r0 * 64 + 8 * warp);  // scales row r0; r1 +512
     const uint32_t xs_thread = x_s + (uint32_t)(gid * K * 2 + warp * 512 + 2 * j * 16);
     const uint32_t xsum_s = smem_addr(xsum);
     const uint32_t xsum_thread = ONE_ROW ? xsum_s + warp * 16 : xsum_s + (uint32_t)(2 * j * G * 4 + warp * 16);
@@ -347,78 +367,88 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     int par = 0, tcount = 0;
-    int slot = 0, kb = 0, tile = (int)blockIdx.x;
+    int kb = 0, tile = (int)blockIdx.x;
     uint32_t phase = 0;
-    for (int it = 0; it < L_items; ++it) {
-        if (alive && !mbar_wait(bar_full + 8 * slot, phase, deadline, abort_flag)) fail();
-        const int blk = kb * kConsumerWarps + warp;
-        if (alive && blk < nblk) {
-            const uint32_t st = s_base + slot * kStageBytes;
-            const uint2 s0 = lds64(st + soff), s1 = lds64(st + soff + 512);
-            const uint2 b0 = lds64(st + soff + kSBBytes), b1 = lds64(st + soff + kSBBytes + 512);
-            const uint32_t xb = xs_thread + kb * (kConsumerWarps * 512);
-            const uint32_t xsb = xsum_thread + kb * (kConsumerWarps * 16);
+    bool ok = alive;
+    for (int it0 = 0; ok && it0 < L_items; it0 += kStages, phase ^= 1u) {
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                const uint2 w0 = lds64(st + coff[g]);
-                const uint2 w1 = lds64(st + coff[g] + 1024);
-                float d[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int slot = 0; slot < kStages; ++slot) {
+            if (it0 + slot >= L_items) break;
+            if (!mbar_wait_fast(bar_full + 8 * slot, phase, deadline, abort_flag)) {
+                ok = false;
+                break;
+            }
+            const int blk = kb * kConsumerWarps + warp;
+            if (blk < nblk) {
+                const uint32_t stage_off = (uint32_t)(slot * kStageBytes);
+                const uint2 s0 = lds64(saddr + stage_off), s1 = lds64(saddr + stage_off + 512);
+                const uint2 b0 = lds64(saddr + stage_off + kSBBytes), b1 = lds64(saddr + stage_off + kSBBytes + 512);
+                const uint32_t xb = xs_thread + (uint32_t)kb * (kConsumerWarps * 512);
+                const uint32_t xsb = xsum_thread + (uint32_t)kb * (kConsumerWarps * 16);
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const uint32_t wa = i ? w0.y : w0.x;
-                    const uint32_t wb = i ? w1.y : w1.x;
-                    uint4 X = make_uint4(0u, 0u, 0u, 0u);
-                    if (has_x) X = lds128(xb + g * 128 + i * 16);
-                    const uint32_t wa4 = wa >> 4, wb4 = wb >> 4, wa8 = wa >> 8, wb8 = wb >> 8;
-                    const uint32_t wa12 = wa >> 12, wb12 = wb >> 12;
-                    mma_bf16_16816(d, code_pair(wa, magic), code_pair(wb, magic), code_pair(wa4, magic),
-                                   code_pair(wb4, magic), X.x, X.y);
-                    mma_bf16_16816(d, code_pair(wa8, magic), code_pair(wb8, magic), code_pair(wa12, magic),
-                                   code_pair(wb12, magic), X.z, X.w);
-                }
-                const uint32_t sw0 = (g < 2) ? s0.x : s0.y, sw1 = (g < 2) ? s1.x : s1.y;
-                const uint32_t bw0 = (g < 2) ? b0.x : b0.y, bw1 = (g < 2) ? b1.x : b1.y;
-                const float sc0 = (g & 1) ? bf16hi(sw0) : bf16lo(sw0);
-                const float sc1 = (g & 1) ? bf16hi(sw1) : bf16lo(sw1);
-                const float2 sc = make_float2(sc0, sc1);
-                const float2 p = fma2(make_float2(-128.f, -128.f), sc,
-                                      make_float2((g & 1) ? bf16hi(bw0) : bf16lo(bw0),
-                                                  (g & 1) ? bf16hi(bw1) : bf16lo(bw1)));
-                if (ONE_ROW) {
-                    const float xs = lds_f32(xsb + g * 4);
-                    const float2 a02 = fma2(sc, make_float2(d[0], d[2]),
-                                            fma2(p, make_float2(xs, xs), make_float2(acc[0], acc[2])));
-                    acc[0] = a02.x;
-                    acc[2] = a02.y;
-                } else {
-                    const float xs0 = xs0_ok ? lds_f32(xsb + g * 4) : 0.f;
-                    const float xs1 = xs1_ok ? lds_f32(xsb + G * 4 + g * 4) : 0.f;
-                    const float2 xs = make_float2(xs0, xs1);
-                    const float2 a01 = fma2(make_float2(sc.x, sc.x), make_float2(d[0], d[1]),
-                                            fma2(make_float2(p.x, p.x), xs, make_float2(acc[0], acc[1])));
-                    const float2 a23 = fma2(make_float2(sc.y, sc.y), make_float2(d[2], d[3]),
-                                            fma2(make_float2(p.y, p.y), xs, make_float2(acc[2], acc[3])));
-                    acc[0] = a01.x;
-                    acc[1] = a01.y;
-                    acc[2] = a23.x;
-                    acc[3] = a23.y;
+                for (int g = 0; g < 4; ++g) {
+                    const uint2 w0 = lds64(caddr[g] + stage_off);
+                    const uint2 w1 = lds64(caddr[g] + stage_off + 1024);
+                    float d[4];
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const uint32_t wa = i ? w0.y : w0.x;
+                        const uint32_t wb = i ? w1.y : w1.x;
+                        uint4 X = make_uint4(0u, 0u, 0u, 0u);
+                        if (has_x) X = lds128(xb + g * 128 + i * 16);
+                        const uint32_t wa4 = wa >> 4, wb4 = wb >> 4, wa8 = wa >> 8, wb8 = wb >> 8;
+                        const uint32_t wa12 = wa >> 12, wb12 = wb >> 12;
+                        if (i == 0)
+                            mma_bf16_16816_zc(d, code_pair(wa, magic), code_pair(wb, magic), code_pair(wa4, magic),
+                                              code_pair(wb4, magic), X.x, X.y);
+                        else
+                            mma_bf16_16816(d, code_pair(wa, magic), code_pair(wb, magic), code_pair(wa4, magic),
+                                           code_pair(wb4, magic), X.x, X.y);
+                        mma_bf16_16816(d, code_pair(wa8, magic), code_pair(wb8, magic), code_pair(wa12, magic),
+                                       code_pair(wb12, magic), X.z, X.w);
+                    }
+                    const uint32_t sw0 = (g < 2) ? s0.x : s0.y, sw1 = (g < 2) ? s1.x : s1.y;
+                    const uint32_t bw0 = (g < 2) ? b0.x : b0.y, bw1 = (g < 2) ? b1.x : b1.y;
+                    const float2 sc = make_float2((g & 1) ? bf16hi(sw0) : bf16lo(sw0),
+                                                  (g & 1) ? bf16hi(sw1) : bf16lo(sw1));
+                    const float2 p = fma2(make_float2(-128.f, -128.f), sc,
+                                          make_float2((g & 1) ? bf16hi(bw0) : bf16lo(bw0),
+                                                      (g & 1) ? bf16hi(bw1) : bf16lo(bw1)));
+                    if (ONE_ROW) {
+                        const float xs = lds_f32(xsb + g * 4);
+                        const float2 a02 = fma2(sc, make_float2(d[0], d[2]),
+                                                fma2(p, make_float2(xs, xs), make_float2(acc[0], acc[2])));
+                        acc[0] = a02.x;
+                        acc[2] = a02.y;
+                    } else {
+                        const float xs0 = xs0_ok ? lds_f32(xsb + g * 4) : 0.f;
+                        const float xs1 = xs1_ok ? lds_f32(xsb + G * 4 + g * 4) : 0.f;
+                        const float2 xs = make_float2(xs0, xs1);
+                        const float2 a01 = fma2(make_float2(sc.x, sc.x), make_float2(d[0], d[1]),
+                                                fma2(make_float2(p.x, p.x), xs, make_float2(acc[0], acc[1])));
+                        const float2 a23 = fma2(make_float2(sc.y, sc.y), make_float2(d[2], d[3]),
+                                                fma2(make_float2(p.y, p.y), xs, make_float2(acc[2], acc[3])));
+                        acc[0] = a01.x;
+                        acc[1] = a01.y;
+                        acc[2] = a23.x;
+                        acc[3] = a23.y;
+                    }
                 }
             }
-        }
-        __syncwarp();
-        // a CTA that is aborting stops releasing stages, so its producer stops
-        // issuing copies and drains the ones in flight
-        if (alive && lane == 0) mbar_arrive(bar_empty + 8 * slot);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
 
-        if (kb == KB - 1) {
-            // Tile finished.  Every warp deposits its partial sums and moves on;
-            // one warp per tile (rotating) adds the eight partials in a fixed
-            // order and stores y.  Two buffers, guarded by mbarriers, so no
-            // CTA-wide barrier stalls the pipeline.
-            const uint32_t rf = bar_red_full + 8 * par, re = bar_red_empty + 8 * par;
-            float *rb = red + par * (kConsumerWarps * kRows * 8);
-            if (alive && tcount >= 2 && !mbar_wait(re, ((tcount >> 1) - 1) & 1, deadline, abort_flag)) fail();
-            if (alive) {
+            if (kb == KB - 1) {
+                // Tile finished.  Every warp deposits its partial sums and moves
+                // on; one warp per tile (rotating) adds the eight partials in a
+                // fixed order and stores y.  Two buffers guarded by mbarriers,
+                // so no CTA-wide barrier stalls the pipeline.
+                const uint32_t rf = bar_red_full + 8 * par, re = bar_red_empty + 8 * par;
+                float *rb = red + par * (kConsumerWarps * kRows * 8);
+                if (tcount >= 2 && !mbar_wait_fast(re, ((tcount >> 1) - 1) & 1, deadline, abort_flag)) {
+                    ok = false;
+                    break;
+                }
                 float *rw = rb + warp * (kRows * 8);
                 rw[r0 * 8 + 2 * j] = acc[0];
                 rw[r0 * 8 + 2 * j + 1] = acc[1];
@@ -426,12 +456,12 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                 rw[r1 * 8 + 2 * j + 1] = acc[3];
                 __syncwarp();
                 if (lane == 0) mbar_arrive(rf);
-            }
-            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-            if (alive && warp == (tcount & (kConsumerWarps - 1))) {
-                if (!mbar_wait(rf, (tcount >> 1) & 1, deadline, abort_flag)) {
-                    fail();
-                } else {
+                acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+                if (warp == (tcount & (kConsumerWarps - 1))) {
+                    if (!mbar_wait_fast(rf, (tcount >> 1) & 1, deadline, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
                     for (int idx = lane; idx < kRows * M; idx += 32) {
                         const int m = idx / kRows, row = idx % kRows;
                         const int n = tile * kRows + row;
@@ -445,19 +475,16 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                     __syncwarp();
                     if (lane == 0) mbar_arrive(re);
                 }
+                ++tcount;
+                par ^= 1;
+                kb = 0;
+                tile += (int)gridDim.x;
+            } else {
+                ++kb;
             }
-            ++tcount;
-            par ^= 1;
-            kb = 0;
-            tile += (int)gridDim.x;
-        } else {
-            ++kb;
-        }
-        if (++slot == kStages) {
-            slot = 0;
-            phase ^= 1u;
         }
     }
+    if (!ok) fail();
 }
 
 // ---------------------------------------------------------------- host side
