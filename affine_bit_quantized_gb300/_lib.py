@@ -31,6 +31,19 @@ _lock = threading.Lock()
 _lib = None
 
 
+class MatmulDesc(ctypes.Structure):
+    """aq_matmul_desc: one matmul of a chain (device pointers as integers)."""
+    _fields_ = [("x", ctypes.c_void_p), ("w_packed", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("biases", ctypes.c_void_p), ("y", ctypes.c_void_p), ("M", ctypes.c_int64), ("N", ctypes.c_int64),
+                ("K", ctypes.c_int64)]
+
+
+class ChainPlan(ctypes.Structure):
+    """aq_chain_plan: filled by aq_chain_prepare, read by aq_chain_run."""
+    _fields_ = [("workspace", ctypes.c_void_p), ("count", ctypes.c_int), ("x_bytes", ctypes.c_int),
+                ("one_row", ctypes.c_int), ("reserved", ctypes.c_int * 5)]
+
+
 class AqError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -65,6 +78,13 @@ def load() -> ctypes.CDLL:
             lib.aq_status_string.restype = ctypes.c_char_p
             lib.aq_last_cuda_error.argtypes = []
             lib.aq_last_cuda_error.restype = ctypes.c_char_p
+            lib.aq_chain_workspace_bytes.argtypes = [I]
+            lib.aq_chain_workspace_bytes.restype = ctypes.c_size_t
+            lib.aq_chain_prepare.argtypes = [ctypes.POINTER(MatmulDesc), I, I, I, P, ctypes.c_size_t,
+                                             ctypes.POINTER(ChainPlan)]
+            lib.aq_chain_prepare.restype = I
+            lib.aq_chain_run.argtypes = [ctypes.POINTER(ChainPlan), P]
+            lib.aq_chain_run.restype = I
             lib.aq_read_device_status.argtypes = [P]
             lib.aq_read_device_status.restype = I
             lib.aq_version.argtypes = []
@@ -101,6 +121,51 @@ def aq_quantize_ref(w, N, K, group_size, bits, w_packed, scales_bf16, biases_bf1
 
 def aq_pack_ref(codes, N, K, bits, w_packed) -> int:
     return load().aq_pack_ref(codes, N, K, bits, w_packed)
+
+
+def aq_chain_workspace_bytes(count) -> int:
+    return load().aq_chain_workspace_bytes(count)
+
+
+def aq_chain_prepare(descs, count, group_size, bits, workspace, workspace_bytes, plan) -> int:
+    return load().aq_chain_prepare(descs, count, group_size, bits, workspace, workspace_bytes, ctypes.byref(plan))
+
+
+def aq_chain_run(plan, stream) -> int:
+    return load().aq_chain_run(ctypes.byref(plan), stream)
+
+
+class Chain:
+    """A prepared chain of matmuls over torch CUDA tensors: Chain([(x, w, s, b, y), ...]).run().
+
+    Each y_j is written before matmul j+1 reads its x, so an x may be an
+    earlier y.  Holds the device workspace (a torch tensor) and the plan."""
+
+    def __init__(self, items, group_size: int = 64, bits: int = 4):
+        import torch
+
+        n = len(items)
+        arr = (MatmulDesc * max(n, 1))()
+        for i, (x, w, s, b, y) in enumerate(items):
+            arr[i] = MatmulDesc(x.data_ptr(), w.data_ptr(), s.data_ptr(), b.data_ptr(), y.data_ptr(), x.shape[0],
+                                w.shape[0], x.shape[1])
+        self.items = items
+        nbytes = aq_chain_workspace_bytes(n)
+        dev = items[0][0].device if n else torch.device("cuda")
+        self.workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+        self.plan = ChainPlan()
+        st = aq_chain_prepare(arr, n, group_size, bits, self.workspace.data_ptr(), nbytes, self.plan)
+        if st != AQ_OK:
+            raise AqError(st, "aq_chain_prepare")
+
+    def run(self, stream=None):
+        import torch
+
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        st = aq_chain_run(self.plan, stream.cuda_stream)
+        if st != AQ_OK:
+            raise AqError(st, "aq_chain_run")
 
 
 def aq_read_device_status(stream) -> int:

@@ -225,6 +225,26 @@ aq_status aq_quantize_ref(const float *w, int64_t N, int64_t K, int group_size, 
     return AQ_OK;
 }
 
+size_t aq_chain_workspace_bytes(int count) { return aq::chain_workspace_bytes(count); }
+
+aq_status aq_chain_prepare(const aq_matmul_desc *descs, int count, int group_size, int bits, void *workspace,
+                           size_t workspace_bytes, aq_chain_plan *plan) {
+    cudaError_t e = cudaSuccess;
+    aq_status st = aq::chain_prepare(descs, count, group_size, bits, workspace, workspace_bytes, plan, &e);
+    if (st == AQ_ERR_CUDA) record_cuda(e);
+    return st;
+}
+
+aq_status aq_chain_run(const aq_chain_plan *plan, void *stream) {
+    if (!plan || plan->count < 0) return AQ_ERR_INVALID_ARG;
+    if (plan->count == 0) return AQ_OK;
+    if (!plan->workspace) return AQ_ERR_INVALID_ARG;
+    int *status = nullptr;
+    aq_status st = record_cuda(status_ptr(&status));
+    if (st != AQ_OK) return st;
+    return record_cuda(aq::chain_run(plan, kTimeoutNs, status, static_cast<cudaStream_t>(stream)));
+}
+
 const char *aq_status_string(aq_status status) {
     switch (status) {
     case AQ_OK: return "AQ_OK";

@@ -1,8 +1,11 @@
 // Internal declarations shared by the libaq translation units (not installed).
 #pragma once
 
+#include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
+
+#include "aq.h"
 
 namespace aq {
 
@@ -38,5 +41,11 @@ cudaError_t launch_qmv_tma(const MatmulArgs &a);
 // aligned scales/biases.
 bool qmm_supported(const MatmulArgs &a);
 cudaError_t launch_qmm(const MatmulArgs &a);
+
+// Chains of decode matmuls in one persistent launch (qmv_chain.cu).
+size_t chain_workspace_bytes(int count);
+aq_status chain_prepare(const aq_matmul_desc *descs, int count, int group_size, int bits, void *workspace,
+                        size_t workspace_bytes, aq_chain_plan *plan, cudaError_t *err);
+cudaError_t chain_run(const aq_chain_plan *plan, uint64_t timeout_ns, int *status, cudaStream_t stream);
 
 }  // namespace aq

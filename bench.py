@@ -275,6 +275,9 @@ def main():
     ap.add_argument("--case", default=None,
                     help="M,N,K: time one matrix shape instead of the decode step (also the ncu target)")
     ap.add_argument("--kernel", choices=("auto", "qmv", "qmm"), default="auto", help="kernel for --case")
+    ap.add_argument("--step-impl", choices=("chain", "graph"), default="chain",
+                    help="decode step as one persistent chained launch (aq_chain_run) or as a CUDA graph of "
+                         "one aq_matmul_bf16_ex launch per matrix; the other is reported as 'alt'")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -381,21 +384,50 @@ def main():
     gpu_id = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
     clocks = ClockSampler(gpu_id)
 
-    # ---- device-resident timing (value)
+    # ---- the same step as one chained launch over the same buffers
+    arr = (aq.MatmulDesc * len(launches))(*[aq.MatmulDesc(xp, wp, sp, bp, yp, M, N, K)
+                                            for (xp, wp, sp, bp, yp, M, N, K) in launches])
+    ws_bytes = aq.aq_chain_workspace_bytes(len(launches))
+    chain_ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    plan = aq.ChainPlan()
+    st = aq.aq_chain_prepare(arr, len(launches), 64, 4, chain_ws.data_ptr(), ws_bytes, plan)
+    if st != aq.AQ_OK:
+        raise aq.AqError(st, "aq_chain_prepare")
     cur = torch.cuda.current_stream(dev)
+
+    def chain_step():
+        rc = aq.aq_chain_run(plan, cur.cuda_stream)
+        if rc != aq.AQ_OK:
+            raise aq.AqError(rc, "aq_chain_run")
+
+    step_fns = {"chain": chain_step, "graph": graph.replay}
+    step = step_fns[args.step_impl]
+    alt_impl = "graph" if args.step_impl == "chain" else "chain"
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def time_steps(fn, n):
+        barrier()
+        e0.record(cur)
+        for _ in range(n):
+            fn()
+        e1.record(cur)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    # ---- device-resident timing (value)
     for _ in range(args.warmup):
-        graph.replay()
+        step()
     barrier()
     clocks.start()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(cur)
-    for _ in range(args.steps):
-        graph.replay()
-    e1.record(cur)
-    e1.synchronize()
+    ms_step = time_steps(step, args.steps)
     clk = clocks.stop()
     barrier()
-    ms_step = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+    ms_step = max_over_ranks(ms_step)
+    for _ in range(args.warmup):
+        step_fns[alt_impl]()
+    ms_alt = max_over_ranks(time_steps(step_fns[alt_impl], max(3, min(args.steps, 500))))
+    if aq.aq_read_device_status(cur.cuda_stream) != aq.AQ_OK:
+        raise RuntimeError("a bounded device-side wait expired during the timed steps")
 
     # ---- end to end: inputs copied in from pinned host memory, logits read back, every step
     h2d = x_pinned.numel() * 2
@@ -404,19 +436,12 @@ def main():
 
     def e2e_step():
         x_dev.copy_(x_pinned, non_blocking=True)
-        graph.replay()
+        step()
         logits_pinned.copy_(logits_dev, non_blocking=True)
 
     for _ in range(args.warmup):
         e2e_step()
-    barrier()
-    e0.record(cur)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(cur)
-    e1.synchronize()
-    barrier()
-    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+    ms_e2e = max_over_ranks(time_steps(e2e_step, args.steps))
 
     # ---- per-matrix kernel times (the 32 layer copies of each shape back to back)
     per_matrix = {}
@@ -504,18 +529,26 @@ def main():
         "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "layers": args.layers, "M": 1, "bytes_per_step": step_bytes,
-                   "launches_per_step": len(launches), "graph": "CUDA graph, programmatic dependent launch",
+                   "matmuls_per_step": len(launches), "step_impl": args.step_impl,
+                   "step_impl_desc": {"chain": "one cooperative persistent launch (aq_chain_run); matmul j reads x "
+                                               "only after matmul j-1 is complete",
+                                      "graph": "CUDA graph of one launch per matmul, programmatic dependent launch"
+                                      }[args.step_impl],
                    "l2": "inputs larger than L2 (4.22 GB of weights per step vs 129 MB L2)",
                    "parallelism": f"replicas x{world}"},
         "tok_s": round(world * 1e3 / ms_step, 1),
         "pct_of_hbm_peak": round(100 * gbs / world / hbm_peak, 1),
         "roofline": {"bound": "hbm", "achieved": round(step_bytes / (ms_step * 1e-3) / 1e9, 1), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(step_bytes / (ms_step * 1e-3) / 1e9 / hbm_peak, 4),
-                     "traffic": traffic, "kernel": "qmv_kernel (every launch of the step)",
+                     "traffic": traffic if args.step_impl == "graph" else None,
+                     "kernel": {"chain": "qmv_chain_kernel (the one launch of the step)",
+                                "graph": "qmv_tma_kernel (every launch of the step)"}[args.step_impl],
                      "peak_source": f"{peak_src} hbm_gbs (copy)"},
         "e2e": {"value": round(gbs_e2e, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(ms_e2e, 5)},
-        "gpu_launches": args.steps * len(launches),
+        "gpu_launches": args.steps * (1 if args.step_impl == "chain" else len(launches)),
+        "alt": {"step_impl": alt_impl, "ms_per_step": round(ms_alt, 5),
+                "value": round(world * step_bytes / (ms_alt * 1e-3) / 1e9, 1)},
         "clocks": clk,
         "per_matrix": per_matrix,
         "qmm": qmm,

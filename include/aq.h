@@ -128,6 +128,64 @@ aq_status aq_quantize_ref(const float *w, int64_t N, int64_t K, int group_size, 
  * 32/bits.  A code >= 2^bits returns AQ_ERR_INVALID_ARG. */
 aq_status aq_pack_ref(const uint8_t *codes, int64_t N, int64_t K, int bits, uint32_t *w_packed);
 
+/*
+ * Chains of decode matmuls in one launch.
+ *
+ * A decode step is a sequence of matmuls, each reading an x produced by
+ * earlier work; its cost is streaming the weights ("gemma-4 decode carries
+ * ~44 ms/token ...", re-scope paragraph), and the "MLX CUDA Cleanup Plan"
+ * page (Refactor Plan, Phase 5) asks for a device-resident step with
+ * persistent work buffers.  aq_chain_run executes count matmuls in order in a
+ * single persistent kernel: matmul j reads its x only after every earlier
+ * matmul of the chain has written all of its y (so x_j may be an earlier
+ * y_i), while the weights of the next matmuls keep streaming.
+ *
+ * Each descriptor follows aq_matmul_bf16's definition, with the limits of the
+ * weight-streaming kernel: 1 <= M <= 8, K a multiple of 512, M*K <= 16384,
+ * x, w_packed, scales and biases 16-byte aligned, y 2-byte aligned.
+ */
+typedef struct aq_matmul_desc {
+    const void *x;            /* bf16 [M, K], device */
+    const uint32_t *w_packed; /* uint32 [N, K/8], device */
+    const void *scales;       /* bf16 [N, K/64], device */
+    const void *biases;       /* bf16 [N, K/64], device */
+    void *y;                  /* bf16 [M, N], device, written */
+    int64_t M, N, K;
+} aq_matmul_desc;
+
+/* Filled by aq_chain_prepare; owned by the caller, read by aq_chain_run. */
+typedef struct aq_chain_plan {
+    void *workspace; /* the caller's device workspace (plan records + counters) */
+    int count;       /* number of matmuls */
+    int x_bytes;     /* largest M*K*2 of the chain */
+    int one_row;     /* 1 if every matmul has M == 1 */
+    int reserved[5];
+} aq_chain_plan;
+
+/* Device workspace bytes a chain of `count` matmuls needs (one 512-byte
+ * record per matmul plus 4 bytes of completion counter per matmul, rounded
+ * up to 128). */
+size_t aq_chain_workspace_bytes(int count);
+
+/* Set-up call: validates the descriptors, encodes one record per matmul
+ * (TMA descriptors, pointers, sizes) and copies them into `workspace`
+ * (device memory, 128-byte aligned, at least aq_chain_workspace_bytes(count)
+ * bytes, owned by the caller and left untouched by anything else until the
+ * last aq_chain_run with this plan has finished).  This call synchronizes (it
+ * copies the records with cudaMemcpy); the pointers it records are used by
+ * every later run.  Errors: AQ_ERR_INVALID_ARG (bad sizes, null pointers,
+ * small workspace), AQ_ERR_UNSUPPORTED (outside the limits above or bits/group
+ * size), AQ_ERR_ALIGNMENT, AQ_ERR_CUDA.  count == 0 gives an empty plan. */
+aq_status aq_chain_prepare(const aq_matmul_desc *descs, int count, int group_size, int bits,
+                           void *workspace, size_t workspace_bytes, aq_chain_plan *plan);
+
+/* Enqueues the chain on `stream`: a reset of the completion counters
+ * (cudaMemsetAsync on the workspace) and one cooperative launch of the
+ * persistent kernel.  Asynchronous; allocates nothing.  Runs that overlap on
+ * the GPU must use different workspaces.  A bounded wait that expires inside
+ * the kernel is reported by aq_read_device_status(). */
+aq_status aq_chain_run(const aq_chain_plan *plan, void *stream);
+
 /* Static, NUL-terminated name of a status code. */
 const char *aq_status_string(aq_status status);
 

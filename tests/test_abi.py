@@ -97,3 +97,38 @@ def test_quantize_ref_matches_oracle(bits):
     want = oracle.quantize(w, bits=bits)
     for g, o in zip(got, want):
         assert np.array_equal(g, o)
+
+
+def _desc(**kw):
+    d = dict(x=A, w_packed=A, scales=A, biases=A, y=A, M=1, N=64, K=512)
+    d.update(kw)
+    return aq.MatmulDesc(d["x"], d["w_packed"], d["scales"], d["biases"], d["y"], d["M"], d["N"], d["K"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(M=9), aq.AQ_ERR_UNSUPPORTED),
+    (dict(K=576), aq.AQ_ERR_UNSUPPORTED),        # not a multiple of 512
+    (dict(K=96), aq.AQ_ERR_INVALID_ARG),
+    (dict(M=2, K=16384), aq.AQ_ERR_UNSUPPORTED), # M*K beyond the staged-x limit
+    (dict(N=0), aq.AQ_ERR_INVALID_ARG),
+    (dict(x=None), aq.AQ_ERR_INVALID_ARG),
+    (dict(x=A + 8), aq.AQ_ERR_ALIGNMENT),
+    (dict(scales=A + 2), aq.AQ_ERR_ALIGNMENT),
+])
+def test_chain_prepare_validation(kw, expect):
+    arr = (aq.MatmulDesc * 2)(_desc(), _desc(**kw))
+    plan = aq.ChainPlan()
+    nbytes = aq.aq_chain_workspace_bytes(2)
+    assert aq.aq_chain_prepare(arr, 2, 64, 4, A, nbytes, plan) == expect
+
+
+def test_chain_workspace_and_plan_checks():
+    assert aq.aq_chain_workspace_bytes(0) == 0
+    assert aq.aq_chain_workspace_bytes(225) == 225 * 512 + 1024
+    arr = (aq.MatmulDesc * 1)(_desc())
+    plan = aq.ChainPlan()
+    assert aq.aq_chain_prepare(arr, 1, 64, 4, A, 100, plan) == aq.AQ_ERR_INVALID_ARG      # workspace too small
+    assert aq.aq_chain_prepare(arr, 1, 64, 4, A + 64, 4096, plan) == aq.AQ_ERR_ALIGNMENT   # not 128-aligned
+    assert aq.aq_chain_prepare(arr, 1, 64, 8, A, 4096, plan) == aq.AQ_ERR_UNSUPPORTED
+    assert aq.aq_chain_prepare(arr, 0, 64, 4, None, 0, plan) == aq.AQ_OK and plan.count == 0
+    assert aq.aq_chain_run(plan, None) == aq.AQ_OK                                          # empty chain

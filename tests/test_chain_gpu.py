@@ -1,0 +1,94 @@
+"""GPU tests of aq_chain_run: every matmul of a chain against the oracle, and
+the ordering guarantee (a matmul that reads an earlier matmul's output sees
+it completely written)."""
+import numpy as np
+import pytest
+
+import affine_bit_quantized_gb300 as aq
+import oracle
+from affine_bit_quantized_gb300 import _build, synth
+
+from ._helpers import assert_parity, from_dev_bf16, to_dev_bf16, upload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import torch
+    _build.build_library()
+    return torch.device("cuda:0")
+
+
+def _mat(dev, M, N, K, seed):
+    import torch
+    w = synth.make_weights(N, K, seed)
+    x = synth.make_x(M, K, seed)
+    xt, wt, st, bt = upload(x, w, dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    return x, w, (xt, wt, st, bt, y)
+
+
+@pytest.mark.parametrize("shapes", [
+    [(1, 64, 512)],
+    [(1, 4096, 4096), (1, 1024, 4096), (1, 1024, 4096), (1, 4096, 4096), (1, 14336, 4096), (1, 4096, 14336)],
+    [(1, 17, 1024), (1, 300, 2560), (1, 1, 512), (1, 1000, 8192), (1, 33, 16384)],
+    [(2, 100, 1024), (8, 77, 2048), (3, 15, 512), (1, 260, 1536)],      # M > 1 in the chain: general path
+])
+def test_chain_parity(dev, shapes):
+    import torch
+    mats = [_mat(dev, M, N, K, 40 + i) for i, (M, N, K) in enumerate(shapes)]
+    chain = aq.Chain([m[2] for m in mats])
+    chain.run()
+    torch.cuda.synchronize()
+    assert aq.aq_read_device_status(None) == aq.AQ_OK
+    for (x, w, t), (M, N, K) in zip(mats, shapes):
+        _, ref = oracle.matmul(x, w.w_packed, w.scales, w.biases, M, N, K)
+        assert_parity(from_dev_bf16(t[4]), ref, what=f"chain M={M} N={N} K={K}")
+
+
+def test_chain_same_bits_as_single_calls_and_repeatable(dev):
+    import torch
+    shapes = [(1, 4096, 4096), (1, 1024, 4096), (1, 14336, 4096)]
+    mats = [_mat(dev, M, N, K, 60 + i) for i, (M, N, K) in enumerate(shapes)]
+    chain = aq.Chain([m[2] for m in mats])
+    chain.run()
+    torch.cuda.synchronize()
+    first = [m[2][4].clone() for m in mats]
+    chain.run()
+    chain.run()
+    torch.cuda.synchronize()
+    for m, f in zip(mats, first):
+        xt, wt, st, bt, y = m[2]
+        assert torch.equal(y, f)
+        assert torch.equal(y, aq.matmul(xt, wt, st, bt))
+
+
+def test_chain_dependency_reads_earlier_output(dev):
+    """x of matmul j+1 IS the output buffer of matmul j.  The chain must give
+    exactly what a sequence of separate calls gives (each call sees the
+    previous output completely written)."""
+    import torch
+    Ks = [512, 1024, 2048, 1024, 4096]   # N of matmul j = K of matmul j+1
+    Ns = Ks[1:] + [3000]
+    ws = [synth.make_weights(N, K, 70 + i) for i, (N, K) in enumerate(zip(Ns, Ks))]
+    x0 = to_dev_bf16(synth.make_x(1, Ks[0], 70), dev)
+    wdev = [upload(np.zeros((1, w.K), np.uint16), w, dev)[1:] for w in ws]
+    ys = [torch.empty((1, N), dtype=torch.bfloat16, device=dev) for N in Ns]
+    items = []
+    for i in range(len(ws)):
+        xin = x0 if i == 0 else ys[i - 1]
+        items.append((xin, *wdev[i], ys[i]))
+    chain = aq.Chain(items)
+    for _ in range(3):
+        for y in ys:
+            y.fill_(float("nan"))
+        chain.run()
+        torch.cuda.synchronize()
+        # reference: separate calls, in order
+        cur = x0
+        for i in range(len(ws)):
+            ref = aq.matmul(cur, *wdev[i])
+            torch.cuda.synchronize()
+            assert torch.equal(ys[i], ref), f"matmul {i}"
+            cur = ref
