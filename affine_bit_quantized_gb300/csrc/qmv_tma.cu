@@ -42,23 +42,16 @@
 
 #include "aq_internal.h"
 #include "aq_ptx.cuh"
+#include "qmv_consumer.cuh"
 
 namespace aq {
 namespace {
 
 using namespace dev;
+using namespace qmv;
 
-constexpr int kRows = 16;                    // rows of W per tile (MMA M)
-constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kBlockCodes = 256;             // codes per column block (one 128-byte swizzle row)
-constexpr int kStageCodes = kBlockCodes * kConsumerWarps;  // 2048 codes per stage
-constexpr int kStageGroups = kStageCodes / 64;             // 32
 constexpr int kStages = 4;
-constexpr int kCodeBlockBytes = kRows * 128;               // 2048
-constexpr int kCodesBytes = kCodeBlockBytes * kConsumerWarps;  // 16384
-constexpr int kSBBytes = kRows * kStageGroups * 2;         // 1024 (scales, and again biases)
-constexpr int kStageBytes = kCodesBytes + 2 * kSBBytes;    // 18432
 constexpr int kMaxXBytes = 32768;                          // M*K*2 limit for staging x once per CTA
 constexpr int kRedBytes = 2 * kConsumerWarps * kRows * 8 * 4;  // double-buffered cross-warp sums
 // largest layout: x of 32 KB, X sums of M*K/16 bytes, barriers, alignment slack
@@ -107,7 +100,6 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int G = K >> 6;
     const int nblk = K / kBlockCodes;                       // column blocks in K
     const int KB = (K + kStageCodes - 1) / kStageCodes;     // stages per tile
     const int T = (N + kRows - 1) / kRows;
@@ -232,22 +224,8 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
     }
     consumer_sync();
 
-    // Per-thread shared-memory addresses, fixed for the whole kernel (stage
-    // slot offsets are added as immediates).  Codes: row r0 of this warp's
-    // 256-code block (row r1 = +1024), word pair 2j..2j+1 of group g, with the
-    // 128-byte swizzle undone (16-byte chunk index XOR row % 8).
-    uint32_t caddr[4];
-#pragma unroll
-    for (int g = 0; g < 4; ++g)
-        caddr[g] = s_base + (uint32_t)(warp * kCodeBlockBytes + r0 * 128 +
-                                       ((((2 * g + (j >> 1)) ^ gid) << 4) | ((j & 1) << 3)));
-    const uint32_t saddr = s_base + (uint32_t)(kCodesBytes + r0 * 64 + 8 * warp);  // scales row r0; r1 +512
-    const uint32_t xs_thread = x_s + (uint32_t)(gid * K * 2 + warp * 512 + 2 * j * 16);
-    const uint32_t xsum_s = smem_addr(xsum);
-    const uint32_t xsum_thread = ONE_ROW ? xsum_s + warp * 16 : xsum_s + (uint32_t)(2 * j * G * 4 + warp * 16);
-    const uint32_t magic = kMagic;
-    const bool has_x = gid < M;
-    const bool xs0_ok = 2 * j < M, xs1_ok = 2 * j + 1 < M;
+    ConsumerThread ct;
+    consumer_init(ct, warp, lane, x_s, smem_addr(xsum), M, K);
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     int par = 0, tcount = 0;
@@ -263,62 +241,7 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                 break;
             }
             const int blk = kb * kConsumerWarps + warp;
-            if (blk < nblk) {
-                const uint32_t stage_off = (uint32_t)(slot * kStageBytes);
-                const uint2 s0 = lds64(saddr + stage_off), s1 = lds64(saddr + stage_off + 512);
-                const uint2 b0 = lds64(saddr + stage_off + kSBBytes), b1 = lds64(saddr + stage_off + kSBBytes + 512);
-                const uint32_t xb = xs_thread + (uint32_t)kb * (kConsumerWarps * 512);
-                const uint32_t xsb = xsum_thread + (uint32_t)kb * (kConsumerWarps * 16);
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const uint2 w0 = lds64(caddr[g] + stage_off);
-                    const uint2 w1 = lds64(caddr[g] + stage_off + 1024);
-                    float d[4];
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        const uint32_t wa = i ? w0.y : w0.x;
-                        const uint32_t wb = i ? w1.y : w1.x;
-                        uint4 X = make_uint4(0u, 0u, 0u, 0u);
-                        if (has_x) X = lds128(xb + g * 128 + i * 16);
-                        const uint32_t wa4 = wa >> 4, wb4 = wb >> 4, wa8 = wa >> 8, wb8 = wb >> 8;
-                        const uint32_t wa12 = wa >> 12, wb12 = wb >> 12;
-                        if (i == 0)
-                            mma_bf16_16816_zc(d, code_pair(wa, magic), code_pair(wb, magic), code_pair(wa4, magic),
-                                              code_pair(wb4, magic), X.x, X.y);
-                        else
-                            mma_bf16_16816(d, code_pair(wa, magic), code_pair(wb, magic), code_pair(wa4, magic),
-                                           code_pair(wb4, magic), X.x, X.y);
-                        mma_bf16_16816(d, code_pair(wa8, magic), code_pair(wb8, magic), code_pair(wa12, magic),
-                                       code_pair(wb12, magic), X.z, X.w);
-                    }
-                    const uint32_t sw0 = (g < 2) ? s0.x : s0.y, sw1 = (g < 2) ? s1.x : s1.y;
-                    const uint32_t bw0 = (g < 2) ? b0.x : b0.y, bw1 = (g < 2) ? b1.x : b1.y;
-                    const float2 sc = make_float2((g & 1) ? bf16hi(sw0) : bf16lo(sw0),
-                                                  (g & 1) ? bf16hi(sw1) : bf16lo(sw1));
-                    const float2 p = fma2(make_float2(-128.f, -128.f), sc,
-                                          make_float2((g & 1) ? bf16hi(bw0) : bf16lo(bw0),
-                                                      (g & 1) ? bf16hi(bw1) : bf16lo(bw1)));
-                    if (ONE_ROW) {
-                        const float xs = lds_f32(xsb + g * 4);
-                        const float2 a02 = fma2(sc, make_float2(d[0], d[2]),
-                                                fma2(p, make_float2(xs, xs), make_float2(acc[0], acc[2])));
-                        acc[0] = a02.x;
-                        acc[2] = a02.y;
-                    } else {
-                        const float xs0 = xs0_ok ? lds_f32(xsb + g * 4) : 0.f;
-                        const float xs1 = xs1_ok ? lds_f32(xsb + G * 4 + g * 4) : 0.f;
-                        const float2 xs = make_float2(xs0, xs1);
-                        const float2 a01 = fma2(make_float2(sc.x, sc.x), make_float2(d[0], d[1]),
-                                                fma2(make_float2(p.x, p.x), xs, make_float2(acc[0], acc[1])));
-                        const float2 a23 = fma2(make_float2(sc.y, sc.y), make_float2(d[2], d[3]),
-                                                fma2(make_float2(p.y, p.y), xs, make_float2(acc[2], acc[3])));
-                        acc[0] = a01.x;
-                        acc[1] = a01.y;
-                        acc[2] = a23.x;
-                        acc[3] = a23.y;
-                    }
-                }
-            }
+            if (blk < nblk) consume_block<ONE_ROW>(s_base + (uint32_t)(slot * kStageBytes), kb, ct, acc);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
 
