@@ -252,7 +252,7 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
                     break;
                 }
                 const int blk = kb * kConsumerWarps + warp;
-                if (blk < nblk) consume_block<ONE_ROW>(s_base + (uint32_t)(slot * kStageBytes), kb, ct, acc);
+                if (blk < nblk) consume_shared_stage<ONE_ROW>(s_base + (uint32_t)(slot * kStageBytes), warp, lane, kb, ct, acc);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
             }

@@ -30,8 +30,7 @@ constexpr int kStageBytes = kCodesBytes + 2 * kSBBytes;    // 18432
 
 // Per-thread shared-memory addresses, fixed while one matrix is processed.
 struct ConsumerThread {
-    uint32_t caddr[4];  // codes of row r0, group g, word pair 2j..2j+1 (stage-relative, swizzle undone)
-    uint32_t soff;      // scales of row r0 for this warp's 4 groups (stage-relative); row r1 at +512
+    uint32_t caddr[4];  // codes of row r0, group g, word pair 2j..2j+1, relative to the block base (swizzle undone)
     uint32_t x_row;     // permuted x, row min(lane/4, M-1), this warp's block and word pair (absolute)
     uint32_t xsum;      // per-group sums of x for column 2j (absolute); column 2j+1 at +G*4
     int G;
@@ -43,8 +42,7 @@ __device__ __forceinline__ void consumer_init(ConsumerThread &c, int warp, int l
     const int gid = lane >> 2, j = lane & 3;
 #pragma unroll
     for (int g = 0; g < 4; ++g)
-        c.caddr[g] = (uint32_t)(warp * kCodeBlockBytes + gid * 128 + ((((2 * g + (j >> 1)) ^ gid) << 4) | ((j & 1) << 3)));
-    c.soff = (uint32_t)(kCodesBytes + gid * 64 + 8 * warp);
+        c.caddr[g] = (uint32_t)(gid * 128 + ((((2 * g + (j >> 1)) ^ gid) << 4) | ((j & 1) << 3)));
     // B columns beyond M read a real row: those accumulator columns are never used
     const int xr = gid < M ? gid : M - 1;
     c.x_row = x_s + (uint32_t)(xr * K * 2 + warp * 512 + 2 * j * 16);
@@ -54,19 +52,22 @@ __device__ __forceinline__ void consumer_init(ConsumerThread &c, int warp, int l
     c.xs1_ok = 2 * j + 1 < M;
 }
 
-// Adds the warp's 16 x 256-code block of the stage at shared address `st`
-// (column block kb*8 + warp of the matrix) to acc.
-template <bool ONE_ROW>
-__device__ __forceinline__ void consume_block(uint32_t st, int kb, const ConsumerThread &c, float (&acc)[4]) {
+// Adds one 16-row x 256-code column block (column block kb*8 + warp of the
+// matrix) to acc.  `codes` is the block's 128-byte-swizzled code tile (16
+// rows of 128 bytes); `sc` points at the scales of row lane/4 for the block's
+// 4 groups, row lane/4 + 8 at +S_R1 bytes, and the biases at +B_OFF.
+template <bool ONE_ROW, int S_R1, int B_OFF>
+__device__ __forceinline__ void consume_block(uint32_t codes, uint32_t sc, int kb, const ConsumerThread &c,
+                                              float (&acc)[4]) {
     const uint32_t magic = kMagic;
-    const uint2 s0 = lds64(st + c.soff), s1 = lds64(st + c.soff + 512);
-    const uint2 b0 = lds64(st + c.soff + kSBBytes), b1 = lds64(st + c.soff + kSBBytes + 512);
+    const uint2 s0 = lds64(sc), s1 = lds64(sc + S_R1);
+    const uint2 b0 = lds64(sc + B_OFF), b1 = lds64(sc + B_OFF + S_R1);
     const uint32_t xb = c.x_row + (uint32_t)kb * (kConsumerWarps * 512);
     const uint32_t xsb = c.xsum + (uint32_t)kb * (kConsumerWarps * 16);
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
-        const uint2 w0 = lds64(st + c.caddr[g]);
-        const uint2 w1 = lds64(st + c.caddr[g] + 1024);
+        const uint2 w0 = lds64(codes + c.caddr[g]);
+        const uint2 w1 = lds64(codes + c.caddr[g] + 1024);
         float d[4];
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
@@ -86,21 +87,21 @@ __device__ __forceinline__ void consume_block(uint32_t st, int kb, const Consume
         }
         const uint32_t sw0 = (g < 2) ? s0.x : s0.y, sw1 = (g < 2) ? s1.x : s1.y;
         const uint32_t bw0 = (g < 2) ? b0.x : b0.y, bw1 = (g < 2) ? b1.x : b1.y;
-        const float2 sc = make_float2((g & 1) ? bf16hi(sw0) : bf16lo(sw0), (g & 1) ? bf16hi(sw1) : bf16lo(sw1));
-        const float2 p = fma2(make_float2(-128.f, -128.f), sc,
+        const float2 sc2 = make_float2((g & 1) ? bf16hi(sw0) : bf16lo(sw0), (g & 1) ? bf16hi(sw1) : bf16lo(sw1));
+        const float2 p = fma2(make_float2(-128.f, -128.f), sc2,
                               make_float2((g & 1) ? bf16hi(bw0) : bf16lo(bw0), (g & 1) ? bf16hi(bw1) : bf16lo(bw1)));
         if (ONE_ROW) {
             const float xs = lds_f32(xsb + g * 4);
-            const float2 a02 = fma2(sc, make_float2(d[0], d[2]), fma2(p, make_float2(xs, xs), make_float2(acc[0], acc[2])));
+            const float2 a02 = fma2(sc2, make_float2(d[0], d[2]), fma2(p, make_float2(xs, xs), make_float2(acc[0], acc[2])));
             acc[0] = a02.x;
             acc[2] = a02.y;
         } else {
             const float xs0 = c.xs0_ok ? lds_f32(xsb + g * 4) : 0.f;
             const float xs1 = c.xs1_ok ? lds_f32(xsb + c.G * 4 + g * 4) : 0.f;
             const float2 xs = make_float2(xs0, xs1);
-            const float2 a01 = fma2(make_float2(sc.x, sc.x), make_float2(d[0], d[1]),
+            const float2 a01 = fma2(make_float2(sc2.x, sc2.x), make_float2(d[0], d[1]),
                                     fma2(make_float2(p.x, p.x), xs, make_float2(acc[0], acc[1])));
-            const float2 a23 = fma2(make_float2(sc.y, sc.y), make_float2(d[2], d[3]),
+            const float2 a23 = fma2(make_float2(sc2.y, sc2.y), make_float2(d[2], d[3]),
                                     fma2(make_float2(p.y, p.y), xs, make_float2(acc[2], acc[3])));
             acc[0] = a01.x;
             acc[1] = a01.y;
@@ -108,6 +109,15 @@ __device__ __forceinline__ void consume_block(uint32_t st, int kb, const Consume
             acc[3] = a23.y;
         }
     }
+}
+
+// Layout of a shared stage (16 rows x 2048 codes + scales/biases of 32 groups):
+// warp w's block codes at +w*2048, scales row r at +16384 + r*64 + 8*w.
+template <bool ONE_ROW>
+__device__ __forceinline__ void consume_shared_stage(uint32_t st, int warp, int lane, int kb, const ConsumerThread &c,
+                                                     float (&acc)[4]) {
+    consume_block<ONE_ROW, 512, kSBBytes>(st + (uint32_t)(warp * kCodeBlockBytes),
+                                          st + (uint32_t)(kCodesBytes + (lane >> 2) * 64 + 8 * warp), kb, c, acc);
 }
 
 }  // namespace
