@@ -26,6 +26,7 @@ AQ_KERNEL_QMM = 2
 
 AQ_FLAG_PDL = 1
 AQ_FLAG_DEBUG_SKIP_X = 1 << 31
+AQ_CHAIN_INDEPENDENT = 1
 
 _lock = threading.Lock()
 _lib = None
@@ -35,7 +36,7 @@ class MatmulDesc(ctypes.Structure):
     """aq_matmul_desc: one matmul of a chain (device pointers as integers)."""
     _fields_ = [("x", ctypes.c_void_p), ("w_packed", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("biases", ctypes.c_void_p), ("y", ctypes.c_void_p), ("M", ctypes.c_int64), ("N", ctypes.c_int64),
-                ("K", ctypes.c_int64)]
+                ("K", ctypes.c_int64), ("flags", ctypes.c_int64)]
 
 
 class ChainPlan(ctypes.Structure):
@@ -141,14 +142,15 @@ class Chain:
     Each y_j is written before matmul j+1 reads its x, so an x may be an
     earlier y.  Holds the device workspace (a torch tensor) and the plan."""
 
-    def __init__(self, items, group_size: int = 64, bits: int = 4):
+    def __init__(self, items, group_size: int = 64, bits: int = 4, independent=None):
         import torch
 
         n = len(items)
         arr = (MatmulDesc * max(n, 1))()
         for i, (x, w, s, b, y) in enumerate(items):
+            flags = AQ_CHAIN_INDEPENDENT if (independent and independent[i]) else 0
             arr[i] = MatmulDesc(x.data_ptr(), w.data_ptr(), s.data_ptr(), b.data_ptr(), y.data_ptr(), x.shape[0],
-                                w.shape[0], x.shape[1])
+                                w.shape[0], x.shape[1], flags)
         self.items = items
         nbytes = aq_chain_workspace_bytes(n)
         dev = items[0][0].device if n else torch.device("cuda")

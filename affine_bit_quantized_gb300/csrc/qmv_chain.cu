@@ -44,7 +44,8 @@ struct ChainRec {                // 128-byte aligned, as CUtensorMap is
     const __nv_bfloat16 *x;
     __nv_bfloat16 *y;
     int M, N, K, tiles;           // tiles = ceil(N / 16)
-    int pad[8];
+    int flags;                    // AQ_CHAIN_INDEPENDENT
+    int pad[7];
 };
 static_assert(sizeof(ChainRec) % 128 == 0, "records must stay 128-byte aligned");
 
@@ -180,39 +181,50 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
     bool ok = true;
 
     volatile int *go = abort_flag + 1;  // CTA-wide decision, written by thread 0 between two barriers
+    const __nv_bfloat16 *prev_x = nullptr;
+    int prev_M = 0, prev_K = 0;
     for (int jm = 0; jm < count; ++jm) {
-        // ---- dependency: every CTA has stored all its tiles of matmul jm-1.
-        // Warps that stopped early (abort) still arrive here, so every warp
-        // passes the same sequence of named barriers.
-        consumer_sync();
-        if (threadIdx.x == 0) {
-            if (jm > 0 && !*abort_flag) {
-                __threadfence();
-                atomicAdd(done + (jm - 1), prev_tiles_mine);
-                const uint64_t dl = global_timer() + timeout_ns;
-                while (ld_acquire_gpu(done + (jm - 1)) < prev_tiles_total) {
-                    if (*abort_flag || global_timer() > dl) {
-                        set_abort();
-                        break;
-                    }
-                }
-            }
-            *go = *abort_flag ? 0 : 1;
-        }
-        consumer_sync();
-        if (!*go) {
-            ok = false;
-            break;
-        }
         const ChainRec *rec = recs + jm;
         const int M = rec->M, N = rec->N, K = rec->K, T = rec->tiles;
         const __nv_bfloat16 *x = rec->x;
         __nv_bfloat16 *y = rec->y;
         const int nblk = K / kBlockCodes;
         const int KB = (K + kStageCodes - 1) / kStageCodes;
+        // A matmul flagged independent does not read the previous one's
+        // output: it neither waits for it nor, when its x is the same buffer,
+        // reloads x.  These decisions depend only on the plan, so every warp
+        // passes the same sequence of named barriers.
+        const bool dep = jm > 0 && !(rec->flags & AQ_CHAIN_INDEPENDENT);
+        const bool new_x = jm == 0 || x != prev_x || M != prev_M || K != prev_K;
+        if (jm > 0 && (dep || new_x)) {
+            consumer_sync();  // every warp is done with the previous matmuls (tiles, y stores, x reads)
+            if (threadIdx.x == 0) {
+                if (dep && !*abort_flag) {
+                    // every CTA has stored all its tiles of matmul jm-1
+                    __threadfence();
+                    atomicAdd(done + (jm - 1), prev_tiles_mine);
+                    const uint64_t dl = global_timer() + timeout_ns;
+                    while (ld_acquire_gpu(done + (jm - 1)) < prev_tiles_total) {
+                        if (*abort_flag || global_timer() > dl) {
+                            set_abort();
+                            break;
+                        }
+                    }
+                }
+                *go = *abort_flag ? 0 : 1;
+            }
+            consumer_sync();
+            if (!*go) {
+                ok = false;
+                break;
+            }
+        }
+        prev_x = x;
+        prev_M = M;
+        prev_K = K;
 
         // ---- x of this matmul: L2 loads, word permutation, per-group sums
-        {
+        if (new_x) {
             const int words = M * K / 8;
             for (int base = 0; base < words; base += 256) {
                 const int wi = base + threadIdx.x;
@@ -235,8 +247,8 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
                 part += __shfl_xor_sync(0xFFFFFFFFu, part, 4);
                 if (wi < words && (wi & 7) == 0) xsum[wi >> 3] = part;
             }
+            consumer_sync();
         }
-        consumer_sync();
 
         ConsumerThread ct;
         consumer_init(ct, warp, lane, x_s, xsum_s, M, K);
@@ -367,6 +379,7 @@ aq_status chain_prepare(const aq_matmul_desc *descs, int count, int group_size, 
     for (int i = 0; i < count; ++i) {
         const aq_matmul_desc &d = descs[i];
         if (d.M < 1 || d.N < 1 || d.K < 1 || d.K % 64) return AQ_ERR_INVALID_ARG;
+        if (d.flags & ~(int64_t)AQ_CHAIN_INDEPENDENT) return AQ_ERR_INVALID_ARG;
         if (!d.x || !d.w_packed || !d.scales || !d.biases || !d.y) return AQ_ERR_INVALID_ARG;
         if (d.M > 8 || d.K % 512 || d.M * d.K * 2 > kMaxXBytes || d.N > (int64_t)1 << 30) return AQ_ERR_UNSUPPORTED;
         if (!aligned(d.x, 16) || !aligned(d.w_packed, 16) || !aligned(d.scales, 16) || !aligned(d.biases, 16) ||
@@ -395,6 +408,7 @@ aq_status chain_prepare(const aq_matmul_desc *descs, int count, int group_size, 
         r.N = (int)d.N;
         r.K = (int)d.K;
         r.tiles = (int)((d.N + kRows - 1) / kRows);
+        r.flags = (int)d.flags;
         x_bytes = std::max(x_bytes, (int)(d.M * d.K * 2));
         one_row = one_row && d.M == 1;
     }

@@ -138,7 +138,8 @@ aq_status aq_pack_ref(const uint8_t *codes, int64_t N, int64_t K, int bits, uint
  * persistent work buffers.  aq_chain_run executes count matmuls in order in a
  * single persistent kernel: matmul j reads its x only after every earlier
  * matmul of the chain has written all of its y (so x_j may be an earlier
- * y_i), while the weights of the next matmuls keep streaming.
+ * y_i), unless it is flagged AQ_CHAIN_INDEPENDENT, while the weights of the
+ * next matmuls keep streaming.
  *
  * Each descriptor follows aq_matmul_bf16's definition, with the limits of the
  * weight-streaming kernel: 1 <= M <= 8, K a multiple of 512, M*K <= 16384,
@@ -151,7 +152,17 @@ typedef struct aq_matmul_desc {
     const void *biases;       /* bf16 [N, K/64], device */
     void *y;                  /* bf16 [M, N], device, written */
     int64_t M, N, K;
+    int64_t flags;            /* 0 or AQ_CHAIN_INDEPENDENT */
 } aq_matmul_desc;
+
+enum {
+    /* This matmul does not read the output of the matmul before it in the
+     * chain (e.g. k and v after q, or up after gate: same input, no mutual
+     * dependency).  It is ordered after whatever the previous matmul waited
+     * for, but not after the previous matmul itself, so the two overlap.  A
+     * run of matmuls on the same x buffer with this flag loads x once. */
+    AQ_CHAIN_INDEPENDENT = 1
+};
 
 /* Filled by aq_chain_prepare; owned by the caller, read by aq_chain_run. */
 typedef struct aq_chain_plan {

@@ -100,9 +100,9 @@ def test_quantize_ref_matches_oracle(bits):
 
 
 def _desc(**kw):
-    d = dict(x=A, w_packed=A, scales=A, biases=A, y=A, M=1, N=64, K=512)
+    d = dict(x=A, w_packed=A, scales=A, biases=A, y=A, M=1, N=64, K=512, flags=0)
     d.update(kw)
-    return aq.MatmulDesc(d["x"], d["w_packed"], d["scales"], d["biases"], d["y"], d["M"], d["N"], d["K"])
+    return aq.MatmulDesc(d["x"], d["w_packed"], d["scales"], d["biases"], d["y"], d["M"], d["N"], d["K"], d["flags"])
 
 
 @pytest.mark.parametrize("kw,expect", [
@@ -132,3 +132,9 @@ def test_chain_workspace_and_plan_checks():
     assert aq.aq_chain_prepare(arr, 1, 64, 8, A, 4096, plan) == aq.AQ_ERR_UNSUPPORTED
     assert aq.aq_chain_prepare(arr, 0, 64, 4, None, 0, plan) == aq.AQ_OK and plan.count == 0
     assert aq.aq_chain_run(plan, None) == aq.AQ_OK                                          # empty chain
+
+
+def test_chain_prepare_rejects_unknown_flags():
+    arr = (aq.MatmulDesc * 1)(_desc(flags=2))
+    plan = aq.ChainPlan()
+    assert aq.aq_chain_prepare(arr, 1, 64, 4, A, aq.aq_chain_workspace_bytes(1), plan) == aq.AQ_ERR_INVALID_ARG
