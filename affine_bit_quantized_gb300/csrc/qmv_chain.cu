@@ -45,7 +45,8 @@ struct ChainRec {                // 128-byte aligned, as CUtensorMap is
     __nv_bfloat16 *y;
     int M, N, K, tiles;           // tiles = ceil(N / 16)
     int flags;                    // AQ_CHAIN_INDEPENDENT
-    int pad[7];
+    int tile_base;                // tiles of the preceding matmuls since the last dependent one
+    int pad[6];
 };
 static_assert(sizeof(ChainRec) % 128 == 0, "records must stay 128-byte aligned");
 
@@ -136,7 +137,10 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
             const int K = rec->K, T = rec->tiles;
             const int nblk = K / kBlockCodes;
             const int KB = (K + kStageCodes - 1) / kStageCodes;
-            for (int tile = blockIdx.x; tile < T && ok; tile += gridDim.x) {
+            // tiles are dealt round-robin, continuing from the previous matmul
+            // of the same dependency group so that the group stays balanced
+            const int first = ((int)blockIdx.x - rec->tile_base % (int)gridDim.x + (int)gridDim.x) % (int)gridDim.x;
+            for (int tile = first; tile < T && ok; tile += gridDim.x) {
                 for (int kb = 0; kb < KB; ++kb) {
                     const int slot = issued % kStages;
                     if (issued >= kStages &&
@@ -254,7 +258,8 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
         consumer_init(ct, warp, lane, x_s, xsum_s, M, K);
         int mine = 0;
 
-        for (int tile = blockIdx.x; tile < T && ok; tile += gridDim.x) {  // on failure: abort, then barrier A
+        const int first = ((int)blockIdx.x - rec->tile_base % (int)gridDim.x + (int)gridDim.x) % (int)gridDim.x;
+        for (int tile = first; tile < T && ok; tile += gridDim.x) {  // on failure: abort, then barrier A
             ++mine;
             for (int kb = 0; kb < KB; ++kb, ++item) {
                 const int slot = item % kStages;
@@ -409,6 +414,7 @@ aq_status chain_prepare(const aq_matmul_desc *descs, int count, int group_size, 
         r.K = (int)d.K;
         r.tiles = (int)((d.N + kRows - 1) / kRows);
         r.flags = (int)d.flags;
+        r.tile_base = (i > 0 && (d.flags & AQ_CHAIN_INDEPENDENT)) ? recs[(size_t)i - 1].tile_base + recs[(size_t)i - 1].tiles : 0;
         x_bytes = std::max(x_bytes, (int)(d.M * d.K * 2));
         one_row = one_row && d.M == 1;
     }
