@@ -370,17 +370,11 @@ size_t chain_workspace_bytes(int count) {
     return records_bytes(count) + counters_bytes(count);
 }
 
-aq_status chain_prepare(const aq_matmul_desc *descs, int count, int group_size, int bits, void *workspace,
-                        size_t workspace_bytes, aq_chain_plan *plan, cudaError_t *err) {
-    *err = cudaSuccess;
-    if (!plan || count < 0) return AQ_ERR_INVALID_ARG;
-    std::memset(plan, 0, sizeof *plan);
-    if (count == 0) return AQ_OK;
-    if (!descs || !workspace) return AQ_ERR_INVALID_ARG;
+namespace {
+
+// Validates the descriptors (host only, no CUDA call).
+aq_status chain_validate(const aq_matmul_desc *descs, int count, int group_size, int bits) {
     if (bits != 4 || group_size != 64) return AQ_ERR_UNSUPPORTED;
-    if (workspace_bytes < chain_workspace_bytes(count)) return AQ_ERR_INVALID_ARG;
-    if (!aligned(workspace, 128)) return AQ_ERR_ALIGNMENT;
-    // validate everything on the host before any CUDA call
     for (int i = 0; i < count; ++i) {
         const aq_matmul_desc &d = descs[i];
         if (d.M < 1 || d.N < 1 || d.K < 1 || d.K % 64) return AQ_ERR_INVALID_ARG;
@@ -391,13 +385,17 @@ aq_status chain_prepare(const aq_matmul_desc *descs, int count, int group_size, 
             !aligned(d.y, 2))
             return AQ_ERR_ALIGNMENT;
     }
+    return AQ_OK;
+}
+
+// Encodes validated descriptors into host records and fills the plan's sizes.
+aq_status chain_encode(const aq_matmul_desc *descs, int count, ChainRec *recs, aq_chain_plan *plan) {
     if (!encode_fn()) return AQ_ERR_UNSUPPORTED;
-    std::vector<ChainRec> recs((size_t)count);
     int x_bytes = 16;
     bool one_row = true;
     for (int i = 0; i < count; ++i) {
         const aq_matmul_desc &d = descs[i];
-        ChainRec &r = recs[(size_t)i];
+        ChainRec &r = recs[i];
         std::memset(&r, 0, sizeof r);
         const uint64_t K = (uint64_t)d.K, N = (uint64_t)d.N, G = K / 64;
         if (!encode_2d(&r.tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, d.w_packed, K / 8, N, K / 2, 32, kRows,
@@ -414,16 +412,39 @@ aq_status chain_prepare(const aq_matmul_desc *descs, int count, int group_size, 
         r.K = (int)d.K;
         r.tiles = (int)((d.N + kRows - 1) / kRows);
         r.flags = (int)d.flags;
-        r.tile_base = (i > 0 && (d.flags & AQ_CHAIN_INDEPENDENT)) ? recs[(size_t)i - 1].tile_base + recs[(size_t)i - 1].tiles : 0;
+        r.tile_base = (i > 0 && (d.flags & AQ_CHAIN_INDEPENDENT)) ? recs[i - 1].tile_base + recs[i - 1].tiles : 0;
         x_bytes = std::max(x_bytes, (int)(d.M * d.K * 2));
         one_row = one_row && d.M == 1;
     }
-    *err = cudaMemcpy(workspace, recs.data(), records_bytes(count), cudaMemcpyHostToDevice);
-    if (*err != cudaSuccess) return AQ_ERR_CUDA;
-    plan->workspace = workspace;
     plan->count = count;
     plan->x_bytes = (x_bytes + 15) & ~15;
     plan->one_row = one_row ? 1 : 0;
+    return AQ_OK;
+}
+
+}  // namespace
+
+aq_status chain_prepare(const aq_matmul_desc *descs, int count, int group_size, int bits, void *workspace,
+                        size_t workspace_bytes, aq_chain_plan *plan, cudaError_t *err) {
+    *err = cudaSuccess;
+    if (!plan || count < 0) return AQ_ERR_INVALID_ARG;
+    std::memset(plan, 0, sizeof *plan);
+    if (count == 0) return AQ_OK;
+    if (!descs || !workspace) return AQ_ERR_INVALID_ARG;
+    if (bits != 4 || group_size != 64) return AQ_ERR_UNSUPPORTED;
+    if (workspace_bytes < chain_workspace_bytes(count)) return AQ_ERR_INVALID_ARG;
+    if (!aligned(workspace, 128)) return AQ_ERR_ALIGNMENT;
+    aq_status st = chain_validate(descs, count, group_size, bits);  // before any CUDA call
+    if (st != AQ_OK) return st;
+    std::vector<ChainRec> recs((size_t)count);
+    st = chain_encode(descs, count, recs.data(), plan);
+    if (st != AQ_OK) return st;
+    *err = cudaMemcpy(workspace, recs.data(), records_bytes(count), cudaMemcpyHostToDevice);
+    if (*err != cudaSuccess) {
+        std::memset(plan, 0, sizeof *plan);
+        return AQ_ERR_CUDA;
+    }
+    plan->workspace = workspace;
     return AQ_OK;
 }
 
