@@ -86,6 +86,8 @@ def load() -> ctypes.CDLL:
             lib.aq_chain_prepare.restype = I
             lib.aq_chain_run.argtypes = [ctypes.POINTER(ChainPlan), P]
             lib.aq_chain_run.restype = I
+            lib.aq_chain_run_static.argtypes = [ctypes.POINTER(MatmulDesc), I, I, I, P]
+            lib.aq_chain_run_static.restype = I
             lib.aq_read_device_status.argtypes = [P]
             lib.aq_read_device_status.restype = I
             lib.aq_version.argtypes = []
@@ -168,6 +170,10 @@ class Chain:
         st = aq_chain_run(self.plan, stream.cuda_stream)
         if st != AQ_OK:
             raise AqError(st, "aq_chain_run")
+
+
+def aq_chain_run_static(descs, count, group_size, bits, stream) -> int:
+    return load().aq_chain_run_static(descs, count, group_size, bits, stream)
 
 
 def aq_read_device_status(stream) -> int:

@@ -245,6 +245,20 @@ aq_status aq_chain_run(const aq_chain_plan *plan, void *stream) {
     return record_cuda(aq::chain_run(plan, kTimeoutNs, status, static_cast<cudaStream_t>(stream)));
 }
 
+aq_status aq_chain_run_static(const aq_matmul_desc *descs, int count, int group_size, int bits, void *stream) {
+    if (count > aq::chain_static_max()) return AQ_ERR_INVALID_ARG;
+    int *status = nullptr;
+    if (count > 0) {
+        aq_status st = record_cuda(status_ptr(&status));
+        if (st != AQ_OK) return st;
+    }
+    cudaError_t e = cudaSuccess;
+    aq_status st = aq::chain_run_static(descs, count, group_size, bits, kTimeoutNs, status,
+                                        static_cast<cudaStream_t>(stream), &e);
+    if (st == AQ_ERR_CUDA) record_cuda(e);
+    return st;
+}
+
 const char *aq_status_string(aq_status status) {
     switch (status) {
     case AQ_OK: return "AQ_OK";

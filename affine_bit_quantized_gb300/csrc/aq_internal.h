@@ -47,5 +47,9 @@ size_t chain_workspace_bytes(int count);
 aq_status chain_prepare(const aq_matmul_desc *descs, int count, int group_size, int bits, void *workspace,
                         size_t workspace_bytes, aq_chain_plan *plan, cudaError_t *err);
 cudaError_t chain_run(const aq_chain_plan *plan, uint64_t timeout_ns, int *status, cudaStream_t stream);
+// The allocation-free variant: plan and counters in a static device array.
+int chain_static_max();
+aq_status chain_run_static(const aq_matmul_desc *descs, int count, int group_size, int bits, uint64_t timeout_ns,
+                           int *status, cudaStream_t stream, cudaError_t *err);
 
 }  // namespace aq

@@ -494,4 +494,66 @@ cudaError_t chain_run(const aq_chain_plan *plan, uint64_t timeout_ns, int *statu
                               (unsigned long long)timeout_ns, status);
 }
 
+// ---------------------------------------------------------------- allocation-free variant
+//
+// aq_chain_run_static runs the same kernel with its plan records and
+// completion counters in the file-scope array below instead of a
+// caller-provided workspace, for callers that cannot hand the library any
+// device memory.  The array is fixed at kStaticChainMax matmuls (132 KB) and
+// is held by every GPU that loads the library until the process exits.  Its
+// device address is looked up once per device with cudaGetSymbolAddress (in
+// host code the array's name is only a host-side stand-in).  Every call shares
+// the array: calls that overlap on the GPU race, and the counters are cleared
+// by every call before its launch.
+
+constexpr int kStaticChainMax = 256;
+static __device__ __align__(256) uint8_t g_static_chain_scratch[kStaticChainMax * sizeof(ChainRec) + 1024];
+
+namespace {
+std::atomic<void *> g_static_scratch_ptr[kMaxDevices];
+std::mutex g_static_host_mutex;
+ChainRec g_static_host_recs[kStaticChainMax];  // host staging of the records (no heap allocation)
+}  // namespace
+
+int chain_static_max() { return kStaticChainMax; }
+
+aq_status chain_run_static(const aq_matmul_desc *descs, int count, int group_size, int bits, uint64_t timeout_ns,
+                           int *status, cudaStream_t stream, cudaError_t *err) {
+    *err = cudaSuccess;
+    if (count < 0) return AQ_ERR_INVALID_ARG;
+    if (count == 0) return AQ_OK;
+    if (count > kStaticChainMax) return AQ_ERR_INVALID_ARG;  // beyond the static scratch
+    if (!descs) return AQ_ERR_INVALID_ARG;
+    aq_status st = chain_validate(descs, count, group_size, bits);  // before any CUDA call
+    if (st != AQ_OK) return st;
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess) return AQ_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) {
+        *err = cudaErrorInvalidDevice;
+        return AQ_ERR_CUDA;
+    }
+    // set-up, once per device, with that device current
+    void *scratch = g_static_scratch_ptr[dev].load(std::memory_order_acquire);
+    if (!scratch) {
+        *err = cudaGetSymbolAddress(&scratch, g_static_chain_scratch);
+        if (*err != cudaSuccess) return AQ_ERR_CUDA;
+        g_static_scratch_ptr[dev].store(scratch, std::memory_order_release);
+    }
+    aq_chain_plan plan;
+    std::memset(&plan, 0, sizeof plan);
+    {
+        std::lock_guard<std::mutex> lock(g_static_host_mutex);
+        st = chain_encode(descs, count, g_static_host_recs, &plan);
+        if (st != AQ_OK) return st;
+        // from pageable memory: returns once the records are staged, so the
+        // host buffer may be reused by the next call
+        *err = cudaMemcpyAsync(scratch, g_static_host_recs, records_bytes(count), cudaMemcpyHostToDevice, stream);
+        if (*err != cudaSuccess) return AQ_ERR_CUDA;
+    }
+    plan.workspace = scratch;
+    *err = chain_run(&plan, timeout_ns, status, stream);  // clears the counters, then launches
+    return *err == cudaSuccess ? AQ_OK : AQ_ERR_CUDA;
+}
+
 }  // namespace aq

@@ -197,6 +197,30 @@ aq_status aq_chain_prepare(const aq_matmul_desc *descs, int count, int group_siz
  * the kernel is reported by aq_read_device_status(). */
 aq_status aq_chain_run(const aq_chain_plan *plan, void *stream);
 
+/*
+ * aq_chain_run as a single call that allocates nothing, for callers that
+ * cannot hand this library any device memory: a plugin inside a host
+ * framework that owns the whole device memory pool and gives plugins no
+ * workspace, or a serving loop that must not reach an allocator after
+ * start-up (an allocation can synchronize the device, and can fail once
+ * memory is fragmented).  No counterpart in the paper.
+ *
+ * Same descriptors, semantics and limits as aq_chain_prepare + aq_chain_run,
+ * at most 256 matmuls per call (a longer chain returns AQ_ERR_INVALID_ARG and
+ * launches nothing).  The plan records and completion counters live in a
+ * static device array of 132 KB that every GPU loading this library holds
+ * until the process exits; the caller still owns every input and output
+ * buffer.  Each call encodes the descriptors again, copies them into that
+ * array on `stream` (cudaMemcpyAsync from host memory) and clears the
+ * counters before its launch.  All calls share the array: calls whose work
+ * overlaps on the GPU (other streams, or another device-side user of the
+ * same array) race, so serialize them.  The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress) and should come before
+ * any stream capture.  Calls no cudaMalloc or cudaFree.
+ */
+aq_status aq_chain_run_static(const aq_matmul_desc *descs, int count, int group_size, int bits,
+                              void *stream);
+
 /* Static, NUL-terminated name of a status code. */
 const char *aq_status_string(aq_status status);
 
