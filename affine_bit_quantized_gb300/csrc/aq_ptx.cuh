@@ -1,7 +1,7 @@
 // Device-side helpers shared by the libaq kernels: mbarriers with bounded
 // waits, TMA and bulk copies, programmatic dependent launch, shared-memory
-// loads, the mma.sync wrapper and the bf16 bit tricks of the weight-streaming
-// kernels.  Internal header (not installed).
+// loads, the mma.sync wrappers and the code-to-fp16 bit tricks of the
+// weight-streaming kernels.  Internal header (not installed).
 #pragma once
 
 #include <cuda.h>
@@ -10,8 +10,6 @@
 namespace aq {
 namespace dev {
 namespace {
-
-constexpr uint32_t kMagic = 0x43004300u;   // bf16x2 (128.0, 128.0)
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -87,7 +85,6 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
     uint4 v;
@@ -113,30 +110,59 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
     return d;
 }
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ void sts32(uint32_t a, uint32_t v) {
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ void sts64(uint32_t a, float x, float y) {
+    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(x), "f"(y) : "memory");
+}
+// Four 8x8 matrices of 16-bit elements; lanes 8p..8p+7 give the row addresses
+// of matrix p, and lane (g, t) = (lane / 4, lane % 4) receives the 32-bit word t
+// of row g of every matrix.
+__device__ __forceinline__ uint4 ldsm_x4(uint32_t a) {
+    uint4 v;
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(a));
+    return v;
+}
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
-// (128 + q[p], 128 + q[p+4]) as bf16x2, from a word already shifted right by
-// 4p: (v & 0x000F000F) | magic in one LOP3 (truth table 0xEA = (a & b) | c).
-__device__ __forceinline__ uint32_t code_pair(uint32_t v, uint32_t magic) {
+
+// Code pairs as exact fp16 values, one LOP3 each (truth table 0xEA = (a & b) | c
+// with c = fp16x2 (1024, 1024)):
+//   lo_pair(v) = (1024 + v[3:0],        1024 + v[19:16])
+//   hi_pair(v) = (1024 + 16 * v[7:4],   1024 + 16 * v[23:20])
+// For a packed word w, lo_pair(w) and hi_pair(w) hold codes (0,4) and (1,5),
+// lo_pair(w >> 8) and hi_pair(w >> 8) codes (2,6) and (3,7).
+__device__ __forceinline__ uint32_t lo_pair(uint32_t v) {
     uint32_t r;
-    asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;" : "=r"(r) : "r"(v), "r"(magic));
+    asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;" : "=r"(r) : "r"(v));
+    return r;
+}
+__device__ __forceinline__ uint32_t hi_pair(uint32_t v) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, 0x00F000F0, 0x64006400, 0xEA;" : "=r"(r) : "r"(v));
     return r;
 }
 
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+// D += A(16x16, fp16) * B(16x8, fp16), fp32 accumulation
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-
-
 // The same MMA with a zero accumulator input (first MMA of a group).
-__device__ __forceinline__ void mma_bf16_16816_zc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                                  uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+__device__ __forceinline__ void mma_f16_16816_zc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                 uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%10,%10,%10,%10};"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));

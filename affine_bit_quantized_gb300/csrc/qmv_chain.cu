@@ -10,8 +10,9 @@
 //
 //  * CTAs are persistent and co-resident (cooperative launch), with the same
 //    producer / consumer structure and arithmetic as the single-matmul
-//    TMA kernel (qmv_tma.cu): 16-row x 2048-code stages through a 4-stage
-//    shared-memory ring, mma.sync on exact 128 + q bf16 codes, per-group fold;
+//    TMA kernel (qmv_tma.cu): 32-row x 2048-code stages through a 4-stage
+//    shared-memory ring, mma.sync on exact fp16 codes 1024 + q, per-group fold
+//    (qmv_consumer.cuh);
 //  * the producer walks the matmuls in order and keeps streaming the NEXT
 //    matmuls' weights while the consumers wait for a dependency, because
 //    weights never depend on earlier outputs;
@@ -27,6 +28,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstddef>
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -40,37 +42,46 @@
 namespace aq {
 
 struct ChainRec {                // 128-byte aligned, as CUtensorMap is
-    CUtensorMap tw, ts, tb;       // codes (128-byte swizzle), scales, biases
+    CUtensorMap tw, ts, tb;       // codes (128-byte swizzle), scales and biases (32-byte swizzle)
     const __nv_bfloat16 *x;
     __nv_bfloat16 *y;
-    int M, N, K, tiles;           // tiles = ceil(N / 16)
+    int M, N, K, tiles;           // tiles = ceil(N / 32)
     int flags;                    // AQ_CHAIN_INDEPENDENT
     int tile_base;                // tiles of the preceding matmuls since the last dependent one
     int pad[6];
 };
 static_assert(sizeof(ChainRec) % 128 == 0, "records must stay 128-byte aligned");
+static_assert(offsetof(ChainRec, x) % 16 == 0 && offsetof(ChainRec, M) == offsetof(ChainRec, x) + 16 &&
+                  offsetof(ChainRec, flags) == offsetof(ChainRec, x) + 32,
+              "the scalar part of a record is read as three 16-byte vectors");
 
 namespace {
 
 using namespace dev;
 using namespace qmv;
 
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 4;
-constexpr int kMaxXBytes = 32768;
-constexpr int kRedBytes = 2 * kConsumerWarps * kRows * 8 * 4;
-constexpr int kNumBars = 2 * kStages + 4;                  // full[S], empty[S], red_full[2], red_empty[2]
+constexpr int kThreads = (kConsumerWarps + 2) * 32;   // consumers, TMA producer, signaller
+constexpr int kMaxStages = 4;   // ring depth (36 KB stages); 5 measured no faster
+constexpr int kNumBars = 2 * kMaxStages + 5;   // full[S], empty[S], red_full[2], red_empty[2], dep
+constexpr int kSmemLimit = 232448;           // dynamic shared memory a CTA may use
+
+constexpr int kInfoCap = 256;   // records whose scalar part is kept in shared memory (48 bytes each)
 
 struct ChainLayout {
-    int x_off, xsum_off, red_off, bar_off, total;
+    int stages;  // ring depth (kMaxStages)
+    int x_off, xsum_off, xinfo_off, red_off, info_off, bar_off, total;
 };
-__host__ __device__ inline ChainLayout chain_layout(int x_bytes) {
+// x_bytes: the largest M*K*2 of the chain; max_m: its largest M
+__host__ __device__ inline ChainLayout chain_layout(int x_bytes, int max_m) {
     ChainLayout L;
-    L.x_off = kStages * kStageBytes;
+    L.stages = kMaxStages;   // fits beside the largest rest (M*K*2 = 32 KB, M = 8)
+    L.x_off = L.stages * kStageBytes;
     L.xsum_off = L.x_off + x_bytes;
-    L.red_off = (L.xsum_off + x_bytes / 32 + 15) & ~15;  // M*K/64 floats = x_bytes/32 bytes
-    L.bar_off = L.red_off + kRedBytes;
-    L.total = L.bar_off + kNumBars * 8 + 16;   // + abort flag and the CTA-wide "go" word
+    L.xinfo_off = L.xsum_off + ((x_bytes / 16 + 15) & ~15);  // float2 per (row, group): M*K/8 bytes
+    L.red_off = L.xinfo_off + kXInfoBytes;
+    L.info_off = L.red_off + red_bytes(max_m);
+    L.bar_off = L.info_off + kInfoCap * 48;
+    L.total = L.bar_off + kNumBars * 8 + 16;   // + abort flag and the stored-tile count
     return L;
 }
 
@@ -79,43 +90,85 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
-__device__ __forceinline__ uint4 ldg_cg_v4(const void *p) {
-    uint4 v;
-    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+__device__ __forceinline__ int ld_acquire_cta_shared(const int *p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
     return v;
+}
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *m) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
+}
+
+// The scalar part of a record (three 16-byte vectors).
+struct RecInfo {
+    const __nv_bfloat16 *x;
+    __nv_bfloat16 *y;
+    int M, N, K, T, flags, tile_base;
+};
+__device__ __forceinline__ RecInfo unpack_info(uint4 a, uint4 b, uint4 c) {
+    RecInfo i;
+    i.x = reinterpret_cast<const __nv_bfloat16 *>((uint64_t)a.x | ((uint64_t)a.y << 32));
+    i.y = reinterpret_cast<__nv_bfloat16 *>((uint64_t)a.z | ((uint64_t)a.w << 32));
+    i.M = (int)b.x;
+    i.N = (int)b.y;
+    i.K = (int)b.z;
+    i.T = (int)b.w;
+    i.flags = (int)c.x;
+    i.tile_base = (int)c.y;
+    return i;
+}
+// Record jm's scalars: the first kInfoCap come from the copy every CTA makes in
+// shared memory at start (walking matmuls in which a CTA has no tile then costs
+// no global-memory round trip), the rest from global memory.
+__device__ __forceinline__ RecInfo load_info(const ChainRec *recs, const uint4 *info, int jm) {
+    if (jm < kInfoCap) return unpack_info(info[3 * jm], info[3 * jm + 1], info[3 * jm + 2]);
+    const uint4 *p = reinterpret_cast<const uint4 *>(&recs[jm].x);
+    return unpack_info(__ldg(p), __ldg(p + 1), __ldg(p + 2));
 }
 
 template <bool ONE_ROW>
-__global__ void __launch_bounds__(kThreads, 2)
-qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_bytes,
+__global__ void __launch_bounds__(kThreads, 1)
+qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_bytes, int max_m,
                  unsigned long long timeout_ns, int *status) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_addr(smem_raw);
     const uint32_t s_base = (raw_base + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (s_base - raw_base);
-    const ChainLayout L = chain_layout(x_bytes);
-    const uint32_t x_s = s_base + L.x_off;
-    float *xsum = reinterpret_cast<float *>(smem + L.xsum_off);
-    float *red = reinterpret_cast<float *>(smem + L.red_off);
+    const ChainLayout L = chain_layout(x_bytes, max_m);
+    const XStage xs = {s_base + (uint32_t)L.x_off, s_base + (uint32_t)L.xsum_off, s_base + (uint32_t)L.xinfo_off};
+    const float *inv_scale = reinterpret_cast<const float *>(smem + L.xinfo_off + 64);
     const uint32_t bar_full = s_base + L.bar_off;
-    const uint32_t bar_empty = bar_full + kStages * 8;
-    const uint32_t bar_red_full = bar_empty + kStages * 8;
-    const uint32_t bar_red_empty = bar_red_full + 16;
+    const uint32_t bar_empty = bar_full + kMaxStages * 8;
+    const uint32_t bar_red = bar_empty + kMaxStages * 8;   // red_full[2], red_empty[2]
+    constexpr int NS = kMaxStages;   // compile time: a runtime ring modulus measured 8% slower
+    const uint32_t bar_dep = bar_red + 32;              // the previous matmul is complete (thread 0 -> all)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.bar_off + kNumBars * 8);
+    int *stored = reinterpret_cast<int *>(smem + L.bar_off + kNumBars * 8 + 4);   // this CTA's stored tiles
+    const int cta = (int)blockIdx.x, ncta = (int)gridDim.x;
+    uint4 *info = reinterpret_cast<uint4 *>(smem + L.info_off);
+    TileCtx tc;
+    tc.red = reinterpret_cast<float *>(smem + L.red_off);
+    tc.red_full = bar_red;
+    tc.red_empty = bar_red + 16;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    for (int i = threadIdx.x; i < 3 * (count < kInfoCap ? count : kInfoCap); i += blockDim.x)
+        info[i] = __ldg(reinterpret_cast<const uint4 *>(&recs[i / 3].x) + i % 3);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, kConsumerWarps);
         }
         for (int p = 0; p < 2; ++p) {
-            mbar_init(bar_red_full + 8 * p, kConsumerWarps);
-            mbar_init(bar_red_empty + 8 * p, 1);
+            mbar_init(tc.red_full + 8 * p, kConsumerWarps);
+            mbar_init(tc.red_empty + 8 * p, 1);
         }
+        mbar_init(bar_dep, 1);
+        for (int m = 0; m < 2 * kMaxM; ++m) reinterpret_cast<int *>(smem + L.xinfo_off)[m] = 0;
         *abort_flag = 0;
+        *stored = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -128,200 +181,164 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
-        if (lane != 0) return;
-        const uint64_t pol = policy_evict_first();
-        int issued = 0;
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            int issued = 0;
+            bool ok = true;
+            RecInfo cur = load_info(recs, info, 0);
+            for (int jm = 0; jm < count && ok; ++jm) {
+                const ChainRec *rec = recs + jm;
+                // the next record's scalars and descriptors travel while this matmul streams
+                RecInfo nxt = cur;
+                if (jm + 1 < count) {
+                    nxt = load_info(recs, info, jm + 1);
+                    prefetch_tensormap(&rec[1].tw);
+                    prefetch_tensormap(&rec[1].ts);
+                    prefetch_tensormap(&rec[1].tb);
+                }
+                const int K = cur.K, T = cur.T;
+                const int nbox = K / kBoxCodes;
+                const int KB = (K + kStageCodes - 1) / kStageCodes;
+                // tiles are dealt round-robin, continuing from the previous
+                // matmul of the same dependency group so that the group stays
+                // balanced
+                const int first = (cta - cur.tile_base % ncta + ncta) % ncta;
+                for (int tile = first; tile < T && ok; tile += ncta) {
+                    for (int kb = 0; kb < KB; ++kb) {
+                        const int slot = issued % NS;
+                        if (issued >= NS &&
+                            !mbar_wait_for(bar_empty + 8 * slot, ((issued / NS) - 1) & 1, timeout_ns, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t dst = s_base + slot * kStageBytes;
+                        const uint32_t fb = bar_full + 8 * slot;
+                        int nvalid = nbox - kb * kBoxes;
+                        nvalid = nvalid < kBoxes ? nvalid : kBoxes;
+                        mbar_expect_tx(fb, (uint32_t)(nvalid * kBoxBytes + 2 * kSBBytes));
+                        for (int b = 0; b < nvalid; ++b)
+                            tma_load_2d(dst + b * kBoxBytes, &rec->tw, (kb * kBoxes + b) * 32, tile * kRows, fb, pol);
+                        tma_load_2d(dst + kCodesBytes, &rec->ts, kb * kStageGroups, tile * kRows, fb, pol);
+                        tma_load_2d(dst + kCodesBytes + kSBBytes, &rec->tb, kb * kStageGroups, tile * kRows, fb, pol);
+                        ++issued;
+                    }
+                }
+                cur = nxt;
+            }
+            if (!ok) {
+                set_abort();
+                const uint64_t drain = global_timer() + timeout_ns;
+                for (int it = (issued > NS ? issued - NS : 0); it < issued; ++it)
+                    while (!mbar_try_wait(bar_full + 8 * (it % NS), (it / NS) & 1) && global_timer() < drain) {
+                    }
+            }
+        }
+        __syncwarp();
+    } else if (warp == kConsumerWarps + 1) {
+        // ------------------------------------------------------------ signaller
+        // Publishes this CTA's stored tiles to the per-matmul counters (one
+        // GPU-scope fence per batch, off the consumers' path) and, before a
+        // dependent matmul, waits until every CTA has stored all tiles of the
+        // previous one, then releases the consumers.
+        if (lane == 0) {
+            int signaled = 0, prev_T = 0;
+            bool ok = true;
+            RecInfo cur = load_info(recs, info, 0);
+            for (int jm = 0; jm < count; ++jm) {
+                RecInfo nxt = cur;
+                if (jm + 1 < count) nxt = load_info(recs, info, jm + 1);
+                if (jm > 0 && !(cur.flags & AQ_CHAIN_INDEPENDENT)) {
+                    const uint64_t dl = global_timer() + timeout_ns;
+                    while (ok && ld_acquire_gpu(done + (jm - 1)) < prev_T) {
+                        if (*abort_flag || global_timer() > dl) {
+                            set_abort();
+                            ok = false;
+                        }
+                    }
+                    mbar_arrive(bar_dep);
+                }
+                const int first = (cta - cur.tile_base % ncta + ncta) % ncta;
+                const int target = signaled + (first < cur.T ? (cur.T - 1 - first) / ncta + 1 : 0);
+                const uint64_t dl = global_timer() + timeout_ns;
+                while (ok && signaled < target) {
+                    const int n = ld_acquire_cta_shared(stored);
+                    if (n > signaled) {
+                        const int upto = n < target ? n : target;
+                        __threadfence();   // those tiles' y stores, seen through `stored`, reach GPU scope first
+                        atomicAdd(done + jm, upto - signaled);
+                        signaled = upto;
+                    } else if (*abort_flag || global_timer() > dl) {
+                        set_abort();
+                        ok = false;
+                    } else {
+                        __nanosleep(64);
+                    }
+                }
+                prev_T = cur.T;
+                cur = nxt;
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------------- consumers
+        // The only named barriers are inside stage_x, whose calls depend on
+        // the plan alone, so every consumer warp passes the same sequence of
+        // them, also after an abort (the waits then return at once and the
+        // work is skipped).
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        int tcount = 0, item = 0, ndep = 0, nstaged = 0;
         bool ok = true;
-        for (int jm = 0; jm < count && ok; ++jm) {
-            const ChainRec *rec = recs + jm;
-            const int K = rec->K, T = rec->tiles;
-            const int nblk = K / kBlockCodes;
+        const __nv_bfloat16 *prev_x = nullptr;
+        int prev_M = 0, prev_K = 0;
+        RecInfo cur = load_info(recs, info, 0);
+        for (int jm = 0; jm < count; ++jm) {
+            RecInfo nxt = cur;
+            if (jm + 1 < count) nxt = load_info(recs, info, jm + 1);
+            const int M = cur.M, N = cur.N, K = cur.K, T = cur.T;
+            const int nblk = K / kWarpCodes;
             const int KB = (K + kStageCodes - 1) / kStageCodes;
-            // tiles are dealt round-robin, continuing from the previous matmul
-            // of the same dependency group so that the group stays balanced
-            const int first = ((int)blockIdx.x - rec->tile_base % (int)gridDim.x + (int)gridDim.x) % (int)gridDim.x;
-            for (int tile = first; tile < T && ok; tile += gridDim.x) {
-                for (int kb = 0; kb < KB; ++kb) {
-                    const int slot = issued % kStages;
-                    if (issued >= kStages &&
-                        !mbar_wait_for(bar_empty + 8 * slot, ((issued / kStages) - 1) & 1, timeout_ns, abort_flag)) {
+            // A matmul flagged independent does not read the previous one's
+            // output: it neither waits for it nor, when its x is the same
+            // buffer, reloads x.
+            const bool dep = jm > 0 && !(cur.flags & AQ_CHAIN_INDEPENDENT);
+            const bool new_x = jm == 0 || cur.x != prev_x || M != prev_M || K != prev_K;
+            if (dep) {
+                // the signaller saw every tile of matmul jm-1 stored
+                if (!mbar_wait_for(bar_dep, (uint32_t)(ndep & 1), timeout_ns, abort_flag)) ok = false;
+                ++ndep;
+            }
+            prev_x = cur.x;
+            prev_M = M;
+            prev_K = K;
+
+            // ---- x of this matmul: L2 loads, fp16 fragments, group sums and scales
+            if (new_x) stage_x<true>(xs, cur.x, 0, M, K, nstaged++);
+
+            ConsumerThread ct;
+            consumer_init(ct, warp, lane, xs, M, K);
+
+            const int first = (cta - cur.tile_base % ncta + ncta) % ncta;
+            for (int tile = first; tile < T && ok; tile += ncta) {
+                for (int kb = 0; kb < KB; ++kb, ++item) {
+                    const int slot = item % NS;
+                    const uint32_t phase = (uint32_t)(item / NS) & 1u;
+                    if (!mbar_wait_for(bar_full + 8 * slot, phase, timeout_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t dst = s_base + slot * kStageBytes;
-                    const uint32_t fb = bar_full + 8 * slot;
-                    int nvalid = nblk - kb * kConsumerWarps;
-                    nvalid = nvalid < kConsumerWarps ? nvalid : kConsumerWarps;
-                    mbar_expect_tx(fb, (uint32_t)(nvalid * kCodeBlockBytes + 2 * kSBBytes));
-                    for (int b = 0; b < nvalid; ++b)
-                        tma_load_2d(dst + b * kCodeBlockBytes, &rec->tw, (kb * kConsumerWarps + b) * 32, tile * kRows,
-                                    fb, pol);
-                    tma_load_2d(dst + kCodesBytes, &rec->ts, kb * kStageGroups, tile * kRows, fb, pol);
-                    tma_load_2d(dst + kCodesBytes + kSBBytes, &rec->tb, kb * kStageGroups, tile * kRows, fb, pol);
-                    ++issued;
+                    if (kb * kConsumerWarps + warp < nblk)
+                        consume_stage<ONE_ROW>(s_base + (uint32_t)(slot * kStageBytes), kb, ct, acc);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
                 }
+                if (!ok) break;
+                ok = finish_tile<ONE_ROW>(tc, acc, tcount, tile, M, N, cur.y, inv_scale, warp, lane, timeout_ns,
+                                          abort_flag, stored);
+                ++tcount;
             }
+            if (!ok) set_abort();   // the remaining matmuls are walked through without work
+            cur = nxt;
         }
-        if (!ok) {
-            set_abort();
-            const uint64_t drain = global_timer() + timeout_ns;
-            for (int it = (issued > kStages ? issued - kStages : 0); it < issued; ++it)
-                while (!mbar_try_wait(bar_full + 8 * (it % kStages), (it / kStages) & 1) && global_timer() < drain) {
-                }
-        }
-        return;
-    }
-
-    // ---------------------------------------------------------------- consumers
-    // All eight consumer warps run every step below (named barriers need all
-    // of them); after an abort the waits return at once and work is skipped.
-    const int gid = lane >> 2;
-    const int j = lane & 3;
-    const int r0 = gid, r1 = gid + 8;
-    const uint32_t xsum_s = smem_addr(xsum);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    int par = 0, tcount = 0, item = 0;
-    int prev_tiles_mine = 0, prev_tiles_total = 0;
-    bool ok = true;
-
-    volatile int *go = abort_flag + 1;  // CTA-wide decision, written by thread 0 between two barriers
-    const __nv_bfloat16 *prev_x = nullptr;
-    int prev_M = 0, prev_K = 0;
-    for (int jm = 0; jm < count; ++jm) {
-        const ChainRec *rec = recs + jm;
-        const int M = rec->M, N = rec->N, K = rec->K, T = rec->tiles;
-        const __nv_bfloat16 *x = rec->x;
-        __nv_bfloat16 *y = rec->y;
-        const int nblk = K / kBlockCodes;
-        const int KB = (K + kStageCodes - 1) / kStageCodes;
-        // A matmul flagged independent does not read the previous one's
-        // output: it neither waits for it nor, when its x is the same buffer,
-        // reloads x.  These decisions depend only on the plan, so every warp
-        // passes the same sequence of named barriers.
-        const bool dep = jm > 0 && !(rec->flags & AQ_CHAIN_INDEPENDENT);
-        const bool new_x = jm == 0 || x != prev_x || M != prev_M || K != prev_K;
-        if (jm > 0 && (dep || new_x)) {
-            consumer_sync();  // every warp is done with the previous matmuls (tiles, y stores, x reads)
-            if (threadIdx.x == 0) {
-                if (dep && !*abort_flag) {
-                    // every CTA has stored all its tiles of matmul jm-1
-                    __threadfence();
-                    atomicAdd(done + (jm - 1), prev_tiles_mine);
-                    const uint64_t dl = global_timer() + timeout_ns;
-                    while (ld_acquire_gpu(done + (jm - 1)) < prev_tiles_total) {
-                        if (*abort_flag || global_timer() > dl) {
-                            set_abort();
-                            break;
-                        }
-                    }
-                }
-                *go = *abort_flag ? 0 : 1;
-            }
-            consumer_sync();
-            if (!*go) {
-                ok = false;
-                break;
-            }
-        }
-        prev_x = x;
-        prev_M = M;
-        prev_K = K;
-
-        // ---- x of this matmul: L2 loads, word permutation, per-group sums
-        if (new_x) {
-            const int words = M * K / 8;
-            for (int base = 0; base < words; base += 256) {
-                const int wi = base + threadIdx.x;
-                float part = 0.f;
-                if (wi < words) {
-                    const uint4 v = ldg_cg_v4(x + (size_t)wi * 8);
-                    part = ((bf16lo(v.x) + bf16hi(v.x)) + (bf16lo(v.y) + bf16hi(v.y))) +
-                           ((bf16lo(v.z) + bf16hi(v.z)) + (bf16lo(v.w) + bf16hi(v.w)));
-                    uint4 p;
-                    p.x = __byte_perm(v.x, v.z, 0x5410);
-                    p.y = __byte_perm(v.x, v.z, 0x7632);
-                    p.z = __byte_perm(v.y, v.w, 0x5410);
-                    p.w = __byte_perm(v.y, v.w, 0x7632);
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(x_s + wi * 16), "r"(p.x),
-                                 "r"(p.y), "r"(p.z), "r"(p.w)
-                                 : "memory");
-                }
-                part += __shfl_xor_sync(0xFFFFFFFFu, part, 1);
-                part += __shfl_xor_sync(0xFFFFFFFFu, part, 2);
-                part += __shfl_xor_sync(0xFFFFFFFFu, part, 4);
-                if (wi < words && (wi & 7) == 0) xsum[wi >> 3] = part;
-            }
-            consumer_sync();
-        }
-
-        ConsumerThread ct;
-        consumer_init(ct, warp, lane, x_s, xsum_s, M, K);
-        int mine = 0;
-
-        const int first = ((int)blockIdx.x - rec->tile_base % (int)gridDim.x + (int)gridDim.x) % (int)gridDim.x;
-        for (int tile = first; tile < T && ok; tile += gridDim.x) {  // on failure: abort, then barrier A
-            ++mine;
-            for (int kb = 0; kb < KB; ++kb, ++item) {
-                const int slot = item % kStages;
-                const uint32_t phase = (uint32_t)(item / kStages) & 1u;
-                if (!mbar_wait_for(bar_full + 8 * slot, phase, timeout_ns, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const int blk = kb * kConsumerWarps + warp;
-                if (blk < nblk) consume_shared_stage<ONE_ROW>(s_base + (uint32_t)(slot * kStageBytes), warp, lane, kb, ct, acc);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
-            }
-            if (!ok) break;
-            // ---- tile finished: rotating reducer adds the eight partials in order
-            const uint32_t rf = bar_red_full + 8 * par, re = bar_red_empty + 8 * par;
-            float *rb = red + par * (kConsumerWarps * kRows * 8);
-            if (tcount >= 2 && !mbar_wait_for(re, ((tcount >> 1) - 1) & 1, timeout_ns, abort_flag)) {
-                ok = false;
-                break;
-            }
-            float *rw = rb + warp * (kRows * 8);
-            rw[r0 * 8 + 2 * j] = acc[0];
-            rw[r0 * 8 + 2 * j + 1] = acc[1];
-            rw[r1 * 8 + 2 * j] = acc[2];
-            rw[r1 * 8 + 2 * j + 1] = acc[3];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(rf);
-            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-            if (warp == (tcount & (kConsumerWarps - 1))) {
-                if (!mbar_wait_for(rf, (tcount >> 1) & 1, timeout_ns, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                for (int idx = lane; idx < kRows * M; idx += 32) {
-                    const int m = idx / kRows, row = idx % kRows;
-                    const int n = tile * kRows + row;
-                    if (n < N) {
-                        float v = rb[row * 8 + m];
-#pragma unroll
-                        for (int w = 1; w < kConsumerWarps; ++w) v += rb[w * (kRows * 8) + row * 8 + m];
-                        y[(int64_t)m * N + n] = __float2bfloat16_rn(v);
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(re);
-            }
-            ++tcount;
-            par ^= 1;
-        }
-        if (!ok) {
-            set_abort();   // the next barrier pair turns this into a CTA-wide stop
-            ok = true;     // keep walking to barrier A with the other warps
-        }
-        prev_tiles_mine = mine;
-        prev_tiles_total = T;
-    }
-    // the last matmul's counter, for completeness (nothing waits on it)
-    consumer_sync();
-    if (threadIdx.x == 0 && count > 0 && !*abort_flag) {
-        __threadfence();
-        atomicAdd(done + (count - 1), prev_tiles_mine);
     }
 }
 
@@ -358,7 +375,6 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_attr_done[2][kMaxDevices];
 std::atomic<int> g_sms[kMaxDevices];
-std::atomic<int> g_smem_per_sm[kMaxDevices];
 
 size_t records_bytes(int count) { return (size_t)count * sizeof(ChainRec); }
 size_t counters_bytes(int count) { return ((size_t)count * sizeof(int) + 127) & ~(size_t)127; }
@@ -401,9 +417,9 @@ aq_status chain_encode(const aq_matmul_desc *descs, int count, ChainRec *recs, a
         if (!encode_2d(&r.tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, d.w_packed, K / 8, N, K / 2, 32, kRows,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
             !encode_2d(&r.ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, d.scales, G, N, G * 2, kStageGroups, kRows,
-                       CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                       CU_TENSOR_MAP_SWIZZLE_64B) ||
             !encode_2d(&r.tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, d.biases, G, N, G * 2, kStageGroups, kRows,
-                       CU_TENSOR_MAP_SWIZZLE_NONE))
+                       CU_TENSOR_MAP_SWIZZLE_64B))
             return AQ_ERR_INVALID_ARG;
         r.x = static_cast<const __nv_bfloat16 *>(d.x);
         r.y = static_cast<__nv_bfloat16 *>(d.y);
@@ -459,29 +475,23 @@ cudaError_t chain_run(const aq_chain_plan *plan, uint64_t timeout_ns, int *statu
         if (e != cudaSuccess) return e;
         g_sms[dev].store(sms, std::memory_order_relaxed);
     }
-    int smem_sm = g_smem_per_sm[dev].load(std::memory_order_relaxed);
-    if (!smem_sm) {
-        e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
-        if (e != cudaSuccess) return e;
-        g_smem_per_sm[dev].store(smem_sm, std::memory_order_relaxed);
-    }
     const int count = plan->count;
-    const ChainLayout L = chain_layout(plan->x_bytes);
+    const int max_m = plan->one_row ? 1 : kMaxM;
+    const ChainLayout L = chain_layout(plan->x_bytes, max_m);
     const int smem = L.total + 1024;
     const bool one = plan->one_row != 0;
     auto kern = one ? qmv_chain_kernel<true> : qmv_chain_kernel<false>;
     if (!g_attr_done[one][dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 chain_layout(kMaxXBytes).total + 1024);
+                                 kSmemLimit);
         if (e != cudaSuccess) return e;
         g_attr_done[one][dev].store(1, std::memory_order_release);
     }
-    const int per_sm = std::max(1, std::min(2, smem_sm / (smem + 1024)));
     int *done = reinterpret_cast<int *>(static_cast<uint8_t *>(plan->workspace) + records_bytes(count));
     e = cudaMemsetAsync(done, 0, (size_t)count * sizeof(int), stream);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(sms * per_sm));
+    cfg.gridDim = dim3((unsigned)sms);   // one CTA per SM, all resident (they wait on one another)
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = stream;
@@ -491,7 +501,7 @@ cudaError_t chain_run(const aq_chain_plan *plan, uint64_t timeout_ns, int *statu
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, static_cast<const ChainRec *>(plan->workspace), count, done, plan->x_bytes,
-                              (unsigned long long)timeout_ns, status);
+                              max_m, (unsigned long long)timeout_ns, status);
 }
 
 // ---------------------------------------------------------------- allocation-free variant

@@ -1,14 +1,33 @@
 // The consumer side of the weight-streaming kernels (qmv_tma.cu and
-// qmv_chain.cu): one warp's share of a shared-memory stage, i.e. 16 rows of W
-// times one 256-code column block (4 groups of 64), folded into the warp's
-// fp32 accumulators.  Internal header (not installed).
+// qmv_chain.cu): staging of x in shared memory, one warp's share of a
+// shared-memory stage (32 rows of W x one 128-code column block, i.e. two
+// groups of 64; sixteen warps cover a 2048-code stage), and the per-tile
+// cross-warp reduction.  Internal header (not installed).
 //
-// Arithmetic per group g and row n (fp32 accumulation):
-//   D[n,m,g] = sum_{k in g} (128 + q[n,k]) * x[m,k]      (mma.sync, exact bf16 operands)
-//   acc     += scale[n,g] * D + (bias[n,g] - 128*scale[n,g]) * X[m,g],   X = sum_{k in g} x
-// MMA A rows are W rows (r0 = lane/4 and r1 = r0 + 8); B columns are rows of x
-// (column lane/4 for B, columns 2*(lane%4) and +1 for the accumulators).
+// Arithmetic per group g, row n and row m of x (fp32 accumulation):
+//   x'[m,k]  = fp16(2^e[m] * x[m,k] / c[k]),  c[k] = 1 or 16 by position in its
+//              8-element word (see below); e[m] puts max|x[m,:]| in [2^14, 2^15)
+//   D[n,m,g] = sum_{k in g} (1024 + c[k] * q[n,k]) * x'[m,k]     (mma.sync, exact fp16 operands)
+//            = 1024 * X'[m,g] + 2^e[m] * sum_{k in g} q[n,k] * x[m,k]
+//   acc     += scale[n,g] * (D - 1024 * X'[m,g]) + bias[n,g] * Xs[m,g]
+//   y[m,n]   = 2^-e[m] * acc
+// with X'[m,g] = sum_{k in g} x'[m,k] and Xs[m,g] = 2^e[m] * sum_{k in g} x[m,k].
+//
+// Codes become exact fp16 values with one LOP3 per pair: within a packed word
+// the nibbles at bits 0-3 and 16-19 go into the mantissa as 1024 + q, those at
+// bits 4-7 and 20-23 as 1024 + 16q (hence c = 16 there), and the word shifted
+// right by 8 gives the other four codes the same way.  A bf16 value has an
+// 8-bit significand, so with the power-of-two scale every element of x whose
+// magnitude is within 2^-29 of the row maximum is exact in fp16; smaller ones
+// round to the fp16 subnormal grid, an absolute error below 2^-39 of the row
+// maximum.
+//
+// MMA A rows are W rows: row block h (0, 1) of the 32-row tile holds rows
+// 16h + lane/4 and 16h + lane/4 + 8.  B columns are rows of x (column lane/4
+// reads row min(lane/4, M-1); columns beyond M are never used).
 #pragma once
+
+#include <cuda_bf16.h>
 
 #include "aq_ptx.cuh"
 
@@ -18,106 +37,318 @@ namespace {
 
 using namespace dev;
 
-constexpr int kRows = 16;                                  // rows of W per tile (MMA M)
-constexpr int kConsumerWarps = 8;
-constexpr int kBlockCodes = 256;                           // codes per column block (one 128-byte swizzle row)
-constexpr int kStageCodes = kBlockCodes * kConsumerWarps;  // 2048 codes per stage
+constexpr int kRows = 32;                                  // rows of W per tile
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kWarpCodes = 128;                            // codes of a warp's column block (2 groups)
+constexpr int kStageCodes = kWarpCodes * kConsumerWarps;   // 2048 codes per stage
 constexpr int kStageGroups = kStageCodes / 64;             // 32
-constexpr int kCodeBlockBytes = kRows * 128;               // 2048
-constexpr int kCodesBytes = kCodeBlockBytes * kConsumerWarps;  // 16384
-constexpr int kSBBytes = kRows * kStageGroups * 2;         // 1024 (scales, and again biases)
-constexpr int kStageBytes = kCodesBytes + 2 * kSBBytes;    // 18432
+constexpr int kBoxCodes = 256;                             // codes per TMA box row (128 bytes)
+constexpr int kBoxes = kStageCodes / kBoxCodes;            // 8 code boxes per stage
+constexpr int kBoxBytes = kRows * 128;                     // 4096
+constexpr int kCodesBytes = kBoxes * kBoxBytes;            // 32768
+constexpr int kSBBytes = kRows * kStageGroups * 2;         // 2048 (scales, and again biases)
+constexpr int kStageBytes = kCodesBytes + 2 * kSBBytes;    // 36864
+constexpr int kMaxM = 8;                                   // rows of x these kernels take
+constexpr int kMaxXBytes = 32768;                          // M*K*2 limit for staging x once per CTA
+constexpr int kXInfoBytes = 96;                            // int row_max[2][8], float inv_scale[8]
 
-// Per-thread shared-memory addresses, fixed while one matrix is processed.
-struct ConsumerThread {
-    uint32_t caddr[4];  // codes of row r0, group g, word pair 2j..2j+1, relative to the block base (swizzle undone)
-    uint32_t x_row;     // permuted x, row min(lane/4, M-1), this warp's block and word pair (absolute)
-    uint32_t xsum;      // per-group sums of x for column 2j (absolute); column 2j+1 at +G*4
-    int G;
-    bool xs0_ok, xs1_ok;
-};
-
-__device__ __forceinline__ void consumer_init(ConsumerThread &c, int warp, int lane, uint32_t x_s, uint32_t xsum_s,
-                                              int M, int K) {
-    const int gid = lane >> 2, j = lane & 3;
-#pragma unroll
-    for (int g = 0; g < 4; ++g)
-        c.caddr[g] = (uint32_t)(gid * 128 + ((((2 * g + (j >> 1)) ^ gid) << 4) | ((j & 1) << 3)));
-    // B columns beyond M read a real row: those accumulator columns are never used
-    const int xr = gid < M ? gid : M - 1;
-    c.x_row = x_s + (uint32_t)(xr * K * 2 + warp * 512 + 2 * j * 16);
-    c.G = K >> 6;
-    c.xsum = xsum_s + (uint32_t)((2 * j < M ? 2 * j : 0) * c.G * 4 + warp * 16);
-    c.xs0_ok = 2 * j < M;
-    c.xs1_ok = 2 * j + 1 < M;
+// named barrier 1: the consumer warps only (the producer warp runs on)
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
 }
 
-// Adds one 16-row x 256-code column block (column block kb*8 + warp of the
-// matrix) to acc.  `codes` is the block's 128-byte-swizzled code tile (16
-// rows of 128 bytes); `sc` points at the scales of row lane/4 for the block's
-// 4 groups, row lane/4 + 8 at +S_R1 bytes, and the biases at +B_OFF.
-template <bool ONE_ROW, int S_R1, int B_OFF>
-__device__ __forceinline__ void consume_block(uint32_t codes, uint32_t sc, int kb, const ConsumerThread &c,
-                                              float (&acc)[4]) {
-    const uint32_t magic = kMagic;
-    const uint2 s0 = lds64(sc), s1 = lds64(sc + S_R1);
-    const uint2 b0 = lds64(sc + B_OFF), b1 = lds64(sc + B_OFF + S_R1);
-    const uint32_t xb = c.x_row + (uint32_t)kb * (kConsumerWarps * 512);
-    const uint32_t xsb = c.xsum + (uint32_t)kb * (kConsumerWarps * 16);
+// Shared-memory addresses of the staged x of the current matmul.
+//   xq    : fp16 MMA fragments of x', M rows of 2K bytes.  For row m, group g
+//           and word half i (words 2t+i of the group, t = 0..3) a 64-byte
+//           "quad" at (2g + i) * 64 holds four 16-byte rows (fragment
+//           register p = 0..3), each the registers of threads t = 0..3, so one
+//           ldmatrix.x4 per quad serves all 32 lanes;
+//   xsum  : float2 [M][K/64] = (Xs, X');
+//   xinfo : int row_max[2][8] (|x| bits, for the scale), float inv_scale[8] = 2^-e.
+struct XStage {
+    uint32_t xq, xsum, xinfo;
+};
+
+__device__ __forceinline__ int x_scale_exponent(int max_bits) {
+    // e with max|x| * 2^e in [2^14, 2^15); 0 for an all-zero row and for a row
+    // holding inf or nan (propagated unchanged)
+    if (max_bits == 0 || max_bits >= 0x7F80) return 0;
+    const int e = 14 - ((max_bits >> 7) - 127);
+    return e < -126 ? -126 : (e > 126 ? 126 : e);
+}
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }  // e in [-126, 127]
+
+__device__ __forceinline__ int bf16x2_abs_max(uint32_t v) {
+    const int a = (int)(v & 0x7FFFu), b = (int)((v >> 16) & 0x7FFFu);
+    return a > b ? a : b;
+}
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ float f16x2_sum(uint32_t v) {
+    float lo, hi;
+    asm("{\n .reg .f16 l, h;\n mov.b32 {l, h}, %2;\n cvt.f32.f16 %0, l;\n cvt.f32.f16 %1, h;\n}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(v));
+    return lo + hi;
+}
+__device__ __forceinline__ uint4 ldg_cg_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+// Stages x [M][K] (bf16, from global memory through L2, or from a raw copy
+// already in shared memory at `raw`, which may alias xs.xq) for the consumers:
+// fragments, group sums and scales.  Called by all consumer threads, which
+// meet at a barrier before the first shared-memory write (so the previous x
+// may still be in use on entry).  `n` counts the stagings of this CTA: staging
+// n takes its row maxima in buffer n % 2, which is zero on entry and is
+// cleared again for staging n + 2.  M*K <= 16384, K % 512 == 0.
+template <bool FROM_GLOBAL>
+__device__ __forceinline__ void stage_x(const XStage &xs, const __nv_bfloat16 *xg, uint32_t raw, int M, int K, int n) {
+    const int tid = threadIdx.x;
+    const int words = M * K / 8;
+    const int wpr = K / 8;  // words per row (a multiple of 64: a warp's 32 words share a row)
+    int *row_max = reinterpret_cast<int *>(__cvta_shared_to_generic(xs.xinfo)) + (n & 1) * kMaxM;
+    float *inv_scale = reinterpret_cast<float *>(__cvta_shared_to_generic(xs.xinfo + 64));
+    uint4 v[kMaxXBytes / 16 / kConsumerThreads];  // 4 words per thread at most
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        const uint2 w0 = lds64(codes + c.caddr[g]);
-        const uint2 w1 = lds64(codes + c.caddr[g] + 1024);
-        float d[4];
+    for (int u = 0; u < kMaxXBytes / 16 / kConsumerThreads; ++u) {
+        if (u * kConsumerThreads >= words) break;  // uniform over the CTA
+        const int wi = u * kConsumerThreads + tid;
+        int mx = 0;
+        if (wi < words) {
+            v[u] = FROM_GLOBAL ? ldg_cg_v4(xg + (size_t)wi * 8) : lds128(raw + (uint32_t)wi * 16);
+            mx = bf16x2_abs_max(v[u].x);
+            mx = max(mx, bf16x2_abs_max(v[u].y));
+            mx = max(mx, bf16x2_abs_max(v[u].z));
+            mx = max(mx, bf16x2_abs_max(v[u].w));
+        }
+        mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+        if ((tid & 31) == 0 && wi < words) atomicMax(row_max + wi / wpr, mx);
+    }
+    consumer_sync();
+#pragma unroll
+    for (int u = 0; u < kMaxXBytes / 16 / kConsumerThreads; ++u) {
+        if (u * kConsumerThreads >= words) break;  // uniform over the CTA
+        const int wi = u * kConsumerThreads + tid;
+        float s_part = 0.f, p_part = 0.f;
+        if (wi < words) {
+            const int m = wi / wpr, wr = wi - m * wpr;
+            const float sc = pow2f(x_scale_exponent(row_max[m]));
+            const float sc16 = sc * 0.0625f;
+            const uint4 a = v[u];
+            const float x0 = bf16lo(a.x) * sc, x1 = bf16hi(a.x) * sc, x2 = bf16lo(a.y) * sc, x3 = bf16hi(a.y) * sc;
+            const float x4 = bf16lo(a.z) * sc, x5 = bf16hi(a.z) * sc, x6 = bf16lo(a.w) * sc, x7 = bf16hi(a.w) * sc;
+            // fragment registers: (x0, x4), (x1, x5)/16, (x2, x6), (x3, x7)/16
+            const uint32_t p0 = f32x2_to_f16x2(x0, x4);
+            const uint32_t p1 = f32x2_to_f16x2(bf16hi(a.x) * sc16, bf16hi(a.z) * sc16);
+            const uint32_t p2 = f32x2_to_f16x2(x2, x6);
+            const uint32_t p3 = f32x2_to_f16x2(bf16hi(a.y) * sc16, bf16hi(a.w) * sc16);
+            s_part = ((x0 + x1) + (x2 + x3)) + ((x4 + x5) + (x6 + x7));
+            p_part = (f16x2_sum(p0) + f16x2_sum(p1)) + (f16x2_sum(p2) + f16x2_sum(p3));
+            const int g = wr >> 3, w8 = wr & 7;
+            const uint32_t q = xs.xq + (uint32_t)(m * 2 * K + (2 * g + (w8 & 1)) * 64 + (w8 >> 1) * 4);
+            sts32(q, p0);
+            sts32(q + 16, p1);
+            sts32(q + 32, p2);
+            sts32(q + 48, p3);
+        }
+        // the 8 words of a group sit in 8 consecutive lanes: fixed-order sums
+        s_part += __shfl_xor_sync(0xFFFFFFFFu, s_part, 1);
+        p_part += __shfl_xor_sync(0xFFFFFFFFu, p_part, 1);
+        s_part += __shfl_xor_sync(0xFFFFFFFFu, s_part, 2);
+        p_part += __shfl_xor_sync(0xFFFFFFFFu, p_part, 2);
+        s_part += __shfl_xor_sync(0xFFFFFFFFu, s_part, 4);
+        p_part += __shfl_xor_sync(0xFFFFFFFFu, p_part, 4);
+        if (wi < words && (wi & 7) == 0) sts64(xs.xsum + (uint32_t)(wi >> 3) * 8, s_part, p_part);
+    }
+    if (tid < M) inv_scale[tid] = pow2f(-x_scale_exponent(row_max[tid]));
+    consumer_sync();
+    if (tid < kMaxM) row_max[tid] = 0;  // for staging n + 2 (staging n + 1 has barriers in between)
+}
+
+// Per-thread shared-memory offsets, fixed while one matrix is processed.
+struct ConsumerThread {
+    uint32_t code[2];   // stage offsets of the code words of row lane/4, groups 2w and 2w+1 (rows +8 at +1024)
+    uint32_t sb;        // offset in a scale box of row lane/4's scales of groups 2w, 2w+1 (rows +8 at +512)
+    uint32_t xq;        // ldmatrix row address of this warp's first quad in stage 0
+    uint32_t xs0, xs1;  // (Xs, X') of this warp's first group in stage 0, x rows of columns 2j and 2j+1
+};
+
+__device__ __forceinline__ void consumer_init(ConsumerThread &c, int warp, int lane, const XStage &xs, int M, int K) {
+    const int gid = lane >> 2, j = lane & 3;
+    // code boxes use the 128-byte swizzle: 16-byte chunk c of box row r sits at chunk c ^ (r % 8)
+    const int c0 = (4 * (warp & 1)) | (j >> 1);
+#pragma unroll
+    for (int gl = 0; gl < 2; ++gl)
+        c.code[gl] = (uint32_t)((warp >> 1) * kBoxBytes + gid * 128 + (((c0 ^ gid) ^ (2 * gl)) << 4) + ((j & 1) << 3));
+    // scale boxes (64-byte rows) use the 64-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ ((r / 2) % 4)
+    c.sb = (uint32_t)(gid * 64 + (((warp >> 2) ^ ((gid >> 1) & 3)) << 4) + ((warp & 3) << 2));
+    const int xr = (lane & 7) < M ? (lane & 7) : M - 1;
+    c.xq = xs.xq + (uint32_t)(xr * 2 * K + (lane >> 3) * 16 + warp * 256);
+    const int G = K / 64;
+    const int m0 = 2 * j < M ? 2 * j : M - 1, m1 = 2 * j + 1 < M ? 2 * j + 1 : M - 1;
+    c.xs0 = xs.xsum + (uint32_t)((m0 * G + 2 * warp) * 8);
+    c.xs1 = xs.xsum + (uint32_t)((m1 * G + 2 * warp) * 8);
+}
+
+// Adds the warp's 32-row x 128-code block of stage `st` (stage index kb of
+// the tile) to acc.  acc[h][*] are the MMA accumulator registers of row block
+// h: (row, column) = (gid, 2j), (gid, 2j+1), (gid+8, 2j), (gid+8, 2j+1).
+template <bool ONE_ROW>
+__device__ __forceinline__ void consume_stage(uint32_t st, int kb, const ConsumerThread &c, float (&acc)[2][4]) {
+    uint32_t sw[4], bw[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        sw[r] = lds32(st + kCodesBytes + c.sb + 512 * r);
+        bw[r] = lds32(st + kCodesBytes + kSBBytes + c.sb + 512 * r);
+    }
+    const uint32_t xq = c.xq + (uint32_t)kb * (kStageGroups * 128);
+    const uint32_t xo = (uint32_t)kb * (kStageGroups * 8);
+#pragma unroll
+    for (int gl = 0; gl < 2; ++gl) {
+        uint2 wr[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) wr[r] = lds64(st + c.code[gl] + 1024 * r);
+        float d[2][4];
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-            const uint32_t wa = i ? w0.y : w0.x;
-            const uint32_t wb = i ? w1.y : w1.x;
-            const uint4 X = lds128(xb + g * 128 + i * 16);
-            const uint32_t wa4 = wa >> 4, wb4 = wb >> 4, wa8 = wa >> 8, wb8 = wb >> 8;
-            const uint32_t wa12 = wa >> 12, wb12 = wb >> 12;
-            if (i == 0)
-                mma_bf16_16816_zc(d, code_pair(wa, magic), code_pair(wb, magic), code_pair(wa4, magic),
-                                  code_pair(wb4, magic), X.x, X.y);
-            else
-                mma_bf16_16816(d, code_pair(wa, magic), code_pair(wb, magic), code_pair(wa4, magic),
-                               code_pair(wb4, magic), X.x, X.y);
-            mma_bf16_16816(d, code_pair(wa8, magic), code_pair(wb8, magic), code_pair(wa12, magic),
-                           code_pair(wb12, magic), X.z, X.w);
+            const uint4 X = ldsm_x4(xq + gl * 128 + i * 64);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t wa = i ? wr[2 * h].y : wr[2 * h].x;
+                const uint32_t wb = i ? wr[2 * h + 1].y : wr[2 * h + 1].x;
+                const uint32_t ta = wa >> 8, tb = wb >> 8;
+                if (i == 0)
+                    mma_f16_16816_zc(d[h], lo_pair(wa), lo_pair(wb), hi_pair(wa), hi_pair(wb), X.x, X.y);
+                else
+                    mma_f16_16816(d[h], lo_pair(wa), lo_pair(wb), hi_pair(wa), hi_pair(wb), X.x, X.y);
+                mma_f16_16816(d[h], lo_pair(ta), lo_pair(tb), hi_pair(ta), hi_pair(tb), X.z, X.w);
+            }
         }
-        const uint32_t sw0 = (g < 2) ? s0.x : s0.y, sw1 = (g < 2) ? s1.x : s1.y;
-        const uint32_t bw0 = (g < 2) ? b0.x : b0.y, bw1 = (g < 2) ? b1.x : b1.y;
-        const float2 sc2 = make_float2((g & 1) ? bf16hi(sw0) : bf16lo(sw0), (g & 1) ? bf16hi(sw1) : bf16lo(sw1));
-        const float2 p = fma2(make_float2(-128.f, -128.f), sc2,
-                              make_float2((g & 1) ? bf16hi(bw0) : bf16lo(bw0), (g & 1) ? bf16hi(bw1) : bf16lo(bw1)));
         if (ONE_ROW) {
-            const float xs = lds_f32(xsb + g * 4);
-            const float2 a02 = fma2(sc2, make_float2(d[0], d[2]), fma2(p, make_float2(xs, xs), make_float2(acc[0], acc[2])));
-            acc[0] = a02.x;
-            acc[2] = a02.y;
+            const uint2 xv = lds64(c.xs0 + xo + gl * 8);
+            const float xsum = __uint_as_float(xv.x), xpr = __uint_as_float(xv.y);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float2 s2 = make_float2(gl ? bf16hi(sw[2 * h]) : bf16lo(sw[2 * h]),
+                                              gl ? bf16hi(sw[2 * h + 1]) : bf16lo(sw[2 * h + 1]));
+                const float2 b2 = make_float2(gl ? bf16hi(bw[2 * h]) : bf16lo(bw[2 * h]),
+                                              gl ? bf16hi(bw[2 * h + 1]) : bf16lo(bw[2 * h + 1]));
+                const float2 t = fma2(make_float2(-1024.f, -1024.f), make_float2(xpr, xpr), make_float2(d[h][0], d[h][2]));
+                const float2 a = fma2(s2, t, fma2(b2, make_float2(xsum, xsum), make_float2(acc[h][0], acc[h][2])));
+                acc[h][0] = a.x;
+                acc[h][2] = a.y;
+            }
         } else {
-            const float xs0 = c.xs0_ok ? lds_f32(xsb + g * 4) : 0.f;
-            const float xs1 = c.xs1_ok ? lds_f32(xsb + c.G * 4 + g * 4) : 0.f;
-            const float2 xs = make_float2(xs0, xs1);
-            const float2 a01 = fma2(make_float2(sc2.x, sc2.x), make_float2(d[0], d[1]),
-                                    fma2(make_float2(p.x, p.x), xs, make_float2(acc[0], acc[1])));
-            const float2 a23 = fma2(make_float2(sc2.y, sc2.y), make_float2(d[2], d[3]),
-                                    fma2(make_float2(p.y, p.y), xs, make_float2(acc[2], acc[3])));
-            acc[0] = a01.x;
-            acc[1] = a01.y;
-            acc[2] = a23.x;
-            acc[3] = a23.y;
+            const uint2 xa = lds64(c.xs0 + xo + gl * 8), xb = lds64(c.xs1 + xo + gl * 8);
+            const float2 xsum = make_float2(__uint_as_float(xa.x), __uint_as_float(xb.x));
+            const float2 xpr = make_float2(__uint_as_float(xa.y), __uint_as_float(xb.y));
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const float s = gl ? bf16hi(sw[2 * h + rr]) : bf16lo(sw[2 * h + rr]);
+                    const float b = gl ? bf16hi(bw[2 * h + rr]) : bf16lo(bw[2 * h + rr]);
+                    const float2 t = fma2(make_float2(-1024.f, -1024.f), xpr,
+                                          make_float2(d[h][2 * rr], d[h][2 * rr + 1]));
+                    const float2 a = fma2(make_float2(s, s), t,
+                                          fma2(make_float2(b, b), xsum, make_float2(acc[h][2 * rr], acc[h][2 * rr + 1])));
+                    acc[h][2 * rr] = a.x;
+                    acc[h][2 * rr + 1] = a.y;
+                }
+            }
         }
     }
 }
 
-// Layout of a shared stage (16 rows x 2048 codes + scales/biases of 32 groups):
-// warp w's block codes at +w*2048, scales row r at +16384 + r*64 + 8*w.
+// Tile reduction buffers: float [2][kConsumerWarps][kRows][M].
+__host__ __device__ constexpr int red_bytes(int max_m) { return 2 * kConsumerWarps * kRows * max_m * 4; }
+
+// This warp's partial sums of a tile into rw = its [kRows][M] slice; acc is
+// cleared.
 template <bool ONE_ROW>
-__device__ __forceinline__ void consume_shared_stage(uint32_t st, int warp, int lane, int kb, const ConsumerThread &c,
-                                                     float (&acc)[4]) {
-    consume_block<ONE_ROW, 512, kSBBytes>(st + (uint32_t)(warp * kCodeBlockBytes),
-                                          st + (uint32_t)(kCodesBytes + (lane >> 2) * 64 + 8 * warp), kb, c, acc);
+__device__ __forceinline__ void write_partials(float *rw, int M, int lane, float (&acc)[2][4]) {
+    const int gid = lane >> 2, j = lane & 3;
+    if (ONE_ROW) {
+        if (j == 0) {  // every column holds x row 0: lanes j > 0 carry copies
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                rw[16 * h + gid] = acc[h][0];
+                rw[16 * h + gid + 8] = acc[h][2];
+            }
+        }
+    } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int m = 2 * j + cc;
+                    if (m < M) rw[(16 * h + gid + 8 * rr) * M + m] = acc[h][2 * rr + cc];
+                }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) acc[h][0] = acc[h][1] = acc[h][2] = acc[h][3] = 0.f;
+}
+
+// ---------------------------------------------------------------- end of a tile
+//
+// Every warp deposits its partial sums of the tile and moves on; one warp per
+// tile (rotating) adds the partials in a fixed order and stores y.  Two
+// buffers guarded by mbarriers, so no CTA-wide barrier stalls the pipeline,
+// and every sum has a fixed order, so results do not depend on timing.
+struct TileCtx {
+    float *red;            // float [2][kConsumerWarps][kRows][M]
+    uint32_t red_full;     // 2 mbarriers: every warp's sums are in red[par] (count kConsumerWarps)
+    uint32_t red_empty;    // 2 mbarriers: red[par] is free again (count 1)
+};
+
+// Called by every consumer warp after the last stage of a tile (the
+// tcount-th tile of this CTA).  False on a timeout.
+// `stored`, if not null, is a shared-memory count of this CTA's stored tiles:
+// the warp that stores a tile adds 1 after its stores (release at CTA scope).
+// Tiles are counted in order: tile t's reducer stores y before its warp takes
+// part in tile t+1, and tile t+1 is reduced only after every warp did.
+template <bool ONE_ROW>
+__device__ __forceinline__ bool finish_tile(const TileCtx &t, float (&acc)[2][4], int tcount, int tile, int M, int N,
+                                            __nv_bfloat16 *y, const float *inv_scale, int warp, int lane,
+                                            uint64_t timeout_ns, const volatile int *abort_flag, int *stored) {
+    const int par = tcount & 1;
+    const uint32_t rf = t.red_full + 8 * par, re = t.red_empty + 8 * par;
+    const int n_out = kRows * M;
+    float *rb = t.red + par * (kConsumerWarps * n_out);
+    if (tcount >= 2 && !mbar_wait_for(re, ((tcount >> 1) - 1) & 1, timeout_ns, abort_flag)) return false;
+    write_partials<ONE_ROW>(rb + warp * n_out, M, lane, acc);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(rf);
+    if (warp != (tcount & (kConsumerWarps - 1))) return true;
+    if (!mbar_wait_for(rf, (tcount >> 1) & 1, timeout_ns, abort_flag)) return false;
+    for (int idx = lane; idx < n_out; idx += 32) {
+        const int row = idx / M, m = idx - row * M;
+        const int n = tile * kRows + row;
+        if (n < N) {
+            float v = rb[idx];
+#pragma unroll
+            for (int w = 1; w < kConsumerWarps; ++w) v += rb[w * n_out + idx];
+            y[(int64_t)m * N + n] = __float2bfloat16_rn(v * inv_scale[m]);
+        }
+    }
+    __syncwarp();
+    if (lane == 0) {
+        mbar_arrive(re);
+        if (stored) {
+            __threadfence_block();
+            atomicAdd(stored, 1);
+        }
+    }
+    return true;
 }
 
 }  // namespace

@@ -7,7 +7,7 @@ import affine_bit_quantized_gb300 as aq
 import oracle
 from affine_bit_quantized_gb300 import _build, synth
 
-from ._helpers import assert_parity, from_dev_bf16, upload
+from ._helpers import assert_parity, bf16_to_f64, from_dev_bf16, upload
 
 pytestmark = pytest.mark.gpu
 
@@ -111,10 +111,11 @@ def test_k_zero_writes_zeros_and_m_zero_is_noop(dev):
     assert st == aq.AQ_OK and bool((y.float() == 3.0).all())
 
 
-def test_special_inputs(dev):
+@pytest.mark.parametrize("K", [256, 1024])   # generic kernel, TMA-fed kernel
+def test_special_inputs(dev, K):
     """Zero x gives exact zeros; a one-hot x returns one dequantized column
     (q = 0 gives the bias); NaN in x propagates to every output of its row."""
-    N, K = 40, 256
+    N = 40
     w = synth.make_weights(N, K, 9)
     codes = oracle.unpack(w.w_packed, N, K)
     codes[:, 5] = 0
@@ -140,8 +141,31 @@ def test_tma_kernel_shapes(dev, M, N, K):
 
 
 def test_tma_kernel_many_tiles_per_cta(dev):
-    # more 16-row tiles than SMs: every CTA walks several tiles and stages wrap the ring
-    check(dev, 1, 16 * 152 * 3 + 5, 1024, 77)
+    # more 32-row tiles than CTAs (two per SM): every CTA walks several tiles and stages wrap the ring
+    check(dev, 1, 32 * 304 * 3 + 5, 1024, 77)
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_tma_kernel_x_dynamic_range(dev, M):
+    """Rows of x scaled by 2^-100, 2^100 and into the bf16 subnormal range, and a
+    row mixing magnitudes 2^20 apart: the kernel stages each row of x in fp16
+    with its own power-of-two scale, which keeps every element exact.  Each
+    output row is checked against the oracle with that row's own RMS."""
+    import torch
+    N, K = 96, 2048
+    w = synth.make_weights(N, K, 31)
+    base = bf16_to_f64(synth.make_x(4, K, 31))
+    base[0] *= 2.0 ** -100
+    base[1] *= 2.0 ** 100
+    base[2, ::3] *= 2.0 ** -20
+    base[3] *= 2.0 ** -128
+    x = synth.f32_to_bf16_bits(base.astype(np.float32))
+    rows = [x[i:i + 1] for i in range(4)] if M == 1 else [x]
+    for xr in rows:
+        got = run(dev, xr, w)
+        _, ref = oracle.matmul(xr, w.w_packed, w.scales, w.biases, xr.shape[0], N, K)
+        for m in range(xr.shape[0]):
+            assert_parity(got[m], ref[m], what=f"row {m} of {xr.shape[0]}")
 
 
 def test_bounded_wait_timeout_reports_status(dev):
