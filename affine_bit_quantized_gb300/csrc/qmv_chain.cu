@@ -60,9 +60,9 @@ namespace {
 using namespace dev;
 using namespace qmv;
 
-constexpr int kThreads = (kConsumerWarps + 2) * 32;   // consumers, TMA producer, signaller
+constexpr int kThreads = (kConsumerWarps + 2) * 32;   // consumers, TMA producer, reducer/signaller
 constexpr int kMaxStages = 4;   // ring depth (36 KB stages); 5 measured no faster
-constexpr int kNumBars = 2 * kMaxStages + 5;   // full[S], empty[S], red_full[2], red_empty[2], dep
+constexpr int kNumBars = 2 * kMaxStages + 9;   // full[S], empty[S], red_full[4], red_empty[4], dep
 constexpr int kSmemLimit = 232448;           // dynamic shared memory a CTA may use
 
 constexpr int kInfoCap = 256;   // records whose scalar part is kept in shared memory (48 bytes each)
@@ -81,18 +81,13 @@ __host__ __device__ inline ChainLayout chain_layout(int x_bytes, int max_m) {
     L.red_off = L.xinfo_off + kXInfoBytes;
     L.info_off = L.red_off + red_bytes(max_m);
     L.bar_off = L.info_off + kInfoCap * 48;
-    L.total = L.bar_off + kNumBars * 8 + 16;   // + abort flag and the stored-tile count
+    L.total = L.bar_off + kNumBars * 8 + 16;   // + abort flag
     return L;
 }
 
 __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ int ld_acquire_cta_shared(const int *p) {
-    int v;
-    asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
     return v;
 }
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *m) {
@@ -139,17 +134,16 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
     const float *inv_scale = reinterpret_cast<const float *>(smem + L.xinfo_off + 64);
     const uint32_t bar_full = s_base + L.bar_off;
     const uint32_t bar_empty = bar_full + kMaxStages * 8;
-    const uint32_t bar_red = bar_empty + kMaxStages * 8;   // red_full[2], red_empty[2]
+    const uint32_t bar_red = bar_empty + kMaxStages * 8;   // red_full[4], red_empty[4]
     constexpr int NS = kMaxStages;   // compile time: a runtime ring modulus measured 8% slower
-    const uint32_t bar_dep = bar_red + 32;              // the previous matmul is complete (thread 0 -> all)
+    const uint32_t bar_dep = bar_red + 64;              // the previous matmul is complete (signaller -> consumers)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.bar_off + kNumBars * 8);
-    int *stored = reinterpret_cast<int *>(smem + L.bar_off + kNumBars * 8 + 4);   // this CTA's stored tiles
     const int cta = (int)blockIdx.x, ncta = (int)gridDim.x;
     uint4 *info = reinterpret_cast<uint4 *>(smem + L.info_off);
     TileCtx tc;
     tc.red = reinterpret_cast<float *>(smem + L.red_off);
     tc.red_full = bar_red;
-    tc.red_empty = bar_red + 16;
+    tc.red_empty = bar_red + 32;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -161,14 +155,13 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, kConsumerWarps);
         }
-        for (int p = 0; p < 2; ++p) {
+        for (int p = 0; p < red_bufs<ONE_ROW>(); ++p) {
             mbar_init(tc.red_full + 8 * p, kConsumerWarps);
             mbar_init(tc.red_empty + 8 * p, 1);
         }
         mbar_init(bar_dep, 1);
         for (int m = 0; m < 2 * kMaxM; ++m) reinterpret_cast<int *>(smem + L.xinfo_off)[m] = 0;
         *abort_flag = 0;
-        *stored = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -235,19 +228,21 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
         }
         __syncwarp();
     } else if (warp == kConsumerWarps + 1) {
-        // ------------------------------------------------------------ signaller
-        // Publishes this CTA's stored tiles to the per-matmul counters (one
-        // GPU-scope fence per batch, off the consumers' path) and, before a
-        // dependent matmul, waits until every CTA has stored all tiles of the
-        // previous one, then releases the consumers.
-        if (lane == 0) {
-            int signaled = 0, prev_T = 0;
-            bool ok = true;
-            RecInfo cur = load_info(recs, info, 0);
-            for (int jm = 0; jm < count; ++jm) {
-                RecInfo nxt = cur;
-                if (jm + 1 < count) nxt = load_info(recs, info, jm + 1);
-                if (jm > 0 && !(cur.flags & AQ_CHAIN_INDEPENDENT)) {
+        // ------------------------------------------------------------ reducer / signaller
+        // Adds the sixteen warps' partials of each of this CTA's tiles in order
+        // and stores y.  After the CTA's last tile of a matmul it publishes
+        // the count to the matmul's counter (one GPU-scope fence per CTA and
+        // matmul, off the consumers' path); before a dependent matmul it waits
+        // until every CTA has stored all tiles of the previous one, then
+        // releases the consumers.
+        int tcount = 0, prev_T = 0;
+        bool ok = true;
+        RecInfo cur = load_info(recs, info, 0);
+        for (int jm = 0; jm < count; ++jm) {
+            RecInfo nxt = cur;
+            if (jm + 1 < count) nxt = load_info(recs, info, jm + 1);
+            if (jm > 0 && !(cur.flags & AQ_CHAIN_INDEPENDENT)) {
+                if (lane == 0) {
                     const uint64_t dl = global_timer() + timeout_ns;
                     while (ok && ld_acquire_gpu(done + (jm - 1)) < prev_T) {
                         if (*abort_flag || global_timer() > dl) {
@@ -257,26 +252,19 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
                     }
                     mbar_arrive(bar_dep);
                 }
-                const int first = (cta - cur.tile_base % ncta + ncta) % ncta;
-                const int target = signaled + (first < cur.T ? (cur.T - 1 - first) / ncta + 1 : 0);
-                const uint64_t dl = global_timer() + timeout_ns;
-                while (ok && signaled < target) {
-                    const int n = ld_acquire_cta_shared(stored);
-                    if (n > signaled) {
-                        const int upto = n < target ? n : target;
-                        __threadfence();   // those tiles' y stores, seen through `stored`, reach GPU scope first
-                        atomicAdd(done + jm, upto - signaled);
-                        signaled = upto;
-                    } else if (*abort_flag || global_timer() > dl) {
-                        set_abort();
-                        ok = false;
-                    } else {
-                        __nanosleep(64);
-                    }
-                }
-                prev_T = cur.T;
-                cur = nxt;
+                ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
             }
+            const int first = (cta - cur.tile_base % ncta + ncta) % ncta;
+            int mine = 0;
+            for (int tile = first; tile < cur.T && ok; tile += ncta, ++mine, ++tcount)
+                ok = reduce_tile<ONE_ROW>(tc, tcount, tile, cur.M, cur.N, cur.y, lane, timeout_ns, abort_flag);
+            if (ok && mine > 0 && lane == 0) {
+                __threadfence();   // this warp's y stores of the matmul reach GPU scope before the count
+                atomicAdd(done + jm, mine);
+            }
+            if (!ok && lane == 0) set_abort();
+            prev_T = cur.T;
+            cur = nxt;
         }
         __syncwarp();
     } else {
@@ -294,7 +282,7 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
         for (int jm = 0; jm < count; ++jm) {
             RecInfo nxt = cur;
             if (jm + 1 < count) nxt = load_info(recs, info, jm + 1);
-            const int M = cur.M, N = cur.N, K = cur.K, T = cur.T;
+            const int M = cur.M, K = cur.K, T = cur.T;
             const int nblk = K / kWarpCodes;
             const int KB = (K + kStageCodes - 1) / kStageCodes;
             // A matmul flagged independent does not read the previous one's
@@ -332,8 +320,7 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
                     if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
                 }
                 if (!ok) break;
-                ok = finish_tile<ONE_ROW>(tc, acc, tcount, tile, M, N, cur.y, inv_scale, warp, lane, timeout_ns,
-                                          abort_flag, stored);
+                ok = deposit_tile<ONE_ROW>(tc, acc, tcount, M, warp, lane, inv_scale, timeout_ns, abort_flag);
                 ++tcount;
             }
             if (!ok) set_abort();   // the remaining matmuls are walked through without work

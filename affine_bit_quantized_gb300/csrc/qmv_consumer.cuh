@@ -10,7 +10,7 @@
 //   D[n,m,g] = sum_{k in g} (1024 + c[k] * q[n,k]) * x'[m,k]     (mma.sync, exact fp16 operands)
 //            = 1024 * X'[m,g] + 2^e[m] * sum_{k in g} q[n,k] * x[m,k]
 //   acc     += scale[n,g] * (D - 1024 * X'[m,g]) + bias[n,g] * Xs[m,g]
-//   y[m,n]   = 2^-e[m] * acc
+//   y[m,n]   = sum over warps of (2^-e[m] * acc)   (power-of-two scaling: exact)
 // with X'[m,g] = sum_{k in g} x'[m,k] and Xs[m,g] = 2^e[m] * sum_{k in g} x[m,k].
 //
 // Codes become exact fp16 values with one LOP3 per pair: within a packed word
@@ -267,32 +267,32 @@ __device__ __forceinline__ void consume_stage(uint32_t st, int kb, const Consume
     }
 }
 
-// Tile reduction buffers: float [2][kConsumerWarps][kRows][M].
-__host__ __device__ constexpr int red_bytes(int max_m) { return 2 * kConsumerWarps * kRows * max_m * 4; }
-
-// This warp's partial sums of a tile into rw = its [kRows][M] slice; acc is
-// cleared.
+// This warp's partial sums of a tile, times the x scale 2^-e[m] of their column
+// (exact: a power of two), into rw = its [kRows][M] slice; acc is cleared.
 template <bool ONE_ROW>
-__device__ __forceinline__ void write_partials(float *rw, int M, int lane, float (&acc)[2][4]) {
+__device__ __forceinline__ void write_partials(float *rw, int M, int lane, float (&acc)[2][4], const float *inv_scale) {
     const int gid = lane >> 2, j = lane & 3;
     if (ONE_ROW) {
         if (j == 0) {  // every column holds x row 0: lanes j > 0 carry copies
+            const float sc = inv_scale[0];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                rw[16 * h + gid] = acc[h][0];
-                rw[16 * h + gid + 8] = acc[h][2];
+                rw[16 * h + gid] = acc[h][0] * sc;
+                rw[16 * h + gid + 8] = acc[h][2] * sc;
             }
         }
     } else {
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int cc = 0; cc < 2; ++cc) {
+            const int m = 2 * j + cc;
+            if (m < M) {
+                const float sc = inv_scale[m];
 #pragma unroll
-            for (int rr = 0; rr < 2; ++rr)
+                for (int h = 0; h < 2; ++h)
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    const int m = 2 * j + cc;
-                    if (m < M) rw[(16 * h + gid + 8 * rr) * M + m] = acc[h][2 * rr + cc];
-                }
+                    for (int rr = 0; rr < 2; ++rr) rw[(16 * h + gid + 8 * rr) * M + m] = acc[h][2 * rr + cc] * sc;
+            }
+        }
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h) acc[h][0] = acc[h][1] = acc[h][2] = acc[h][3] = 0.f;
@@ -300,36 +300,52 @@ __device__ __forceinline__ void write_partials(float *rw, int M, int lane, float
 
 // ---------------------------------------------------------------- end of a tile
 //
-// Every warp deposits its partial sums of the tile and moves on; one warp per
-// tile (rotating) adds the partials in a fixed order and stores y.  Two
-// buffers guarded by mbarriers, so no CTA-wide barrier stalls the pipeline,
-// and every sum has a fixed order, so results do not depend on timing.
+// Every consumer warp deposits its partial sums of a tile in one of
+// red_bufs<ONE_ROW> rotating buffers and moves on to the next tile; a
+// dedicated reducer warp adds the sixteen partials of each tile in a fixed
+// order and stores y.  The consumers never wait for one another here (a
+// buffer is reused only after the reducer has emptied it), and every sum has
+// a fixed order, so results do not depend on timing.
+template <bool ONE_ROW>
+__host__ __device__ constexpr int red_bufs() { return ONE_ROW ? 4 : 2; }
+// bytes of the partial-sum buffers: float [bufs][kConsumerWarps][kRows][M]
+__host__ __device__ constexpr int red_bytes(int m) { return (m == 1 ? 4 : 2) * kConsumerWarps * kRows * m * 4; }
+
 struct TileCtx {
-    float *red;            // float [2][kConsumerWarps][kRows][M]
-    uint32_t red_full;     // 2 mbarriers: every warp's sums are in red[par] (count kConsumerWarps)
-    uint32_t red_empty;    // 2 mbarriers: red[par] is free again (count 1)
+    float *red;            // float [bufs][kConsumerWarps][kRows][M]
+    uint32_t red_full;     // bufs mbarriers: every warp's sums are in red[b] (count kConsumerWarps)
+    uint32_t red_empty;    // bufs mbarriers: red[b] is free again (count 1)
 };
 
-// Called by every consumer warp after the last stage of a tile (the
-// tcount-th tile of this CTA).  False on a timeout.
-// `stored`, if not null, is a shared-memory count of this CTA's stored tiles:
-// the warp that stores a tile adds 1 after its stores (release at CTA scope).
-// Tiles are counted in order: tile t's reducer stores y before its warp takes
-// part in tile t+1, and tile t+1 is reduced only after every warp did.
+// Consumer side, after the last stage of the tcount-th tile of this CTA.
+// False on a timeout.
 template <bool ONE_ROW>
-__device__ __forceinline__ bool finish_tile(const TileCtx &t, float (&acc)[2][4], int tcount, int tile, int M, int N,
-                                            __nv_bfloat16 *y, const float *inv_scale, int warp, int lane,
-                                            uint64_t timeout_ns, const volatile int *abort_flag, int *stored) {
-    const int par = tcount & 1;
-    const uint32_t rf = t.red_full + 8 * par, re = t.red_empty + 8 * par;
+__device__ __forceinline__ bool deposit_tile(const TileCtx &t, float (&acc)[2][4], int tcount, int M, int warp,
+                                             int lane, const float *inv_scale, uint64_t timeout_ns,
+                                             const volatile int *abort_flag) {
+    constexpr int B = red_bufs<ONE_ROW>();
+    const int b = tcount % B;
     const int n_out = kRows * M;
-    float *rb = t.red + par * (kConsumerWarps * n_out);
-    if (tcount >= 2 && !mbar_wait_for(re, ((tcount >> 1) - 1) & 1, timeout_ns, abort_flag)) return false;
-    write_partials<ONE_ROW>(rb + warp * n_out, M, lane, acc);
+    if (tcount >= B && !mbar_wait_for(t.red_empty + 8 * b, (uint32_t)((tcount / B) - 1) & 1u, timeout_ns, abort_flag))
+        return false;
+    write_partials<ONE_ROW>(t.red + (b * kConsumerWarps + warp) * n_out, M, lane, acc, inv_scale);
     __syncwarp();
-    if (lane == 0) mbar_arrive(rf);
-    if (warp != (tcount & (kConsumerWarps - 1))) return true;
-    if (!mbar_wait_for(rf, (tcount >> 1) & 1, timeout_ns, abort_flag)) return false;
+    if (lane == 0) mbar_arrive(t.red_full + 8 * b);
+    return true;
+}
+
+// Reducer warp, for the tcount-th tile of this CTA (tile index `tile` of a
+// matrix with N rows): adds the (already unscaled) partials in warp order and
+// stores y rows tile*kRows .. (bf16, round to nearest even).
+template <bool ONE_ROW>
+__device__ __forceinline__ bool reduce_tile(const TileCtx &t, int tcount, int tile, int M, int N,
+                                            __nv_bfloat16 *y, int lane, uint64_t timeout_ns,
+                                            const volatile int *abort_flag) {
+    constexpr int B = red_bufs<ONE_ROW>();
+    const int b = tcount % B;
+    const int n_out = kRows * M;
+    if (!mbar_wait_for(t.red_full + 8 * b, (uint32_t)(tcount / B) & 1u, timeout_ns, abort_flag)) return false;
+    const float *rb = t.red + b * kConsumerWarps * n_out;
     for (int idx = lane; idx < n_out; idx += 32) {
         const int row = idx / M, m = idx - row * M;
         const int n = tile * kRows + row;
@@ -337,17 +353,11 @@ __device__ __forceinline__ bool finish_tile(const TileCtx &t, float (&acc)[2][4]
             float v = rb[idx];
 #pragma unroll
             for (int w = 1; w < kConsumerWarps; ++w) v += rb[w * n_out + idx];
-            y[(int64_t)m * N + n] = __float2bfloat16_rn(v * inv_scale[m]);
+            y[(int64_t)m * N + n] = __float2bfloat16_rn(v);
         }
     }
     __syncwarp();
-    if (lane == 0) {
-        mbar_arrive(re);
-        if (stored) {
-            __threadfence_block();
-            atomicAdd(stored, 1);
-        }
-    }
+    if (lane == 0) mbar_arrive(t.red_empty + 8 * b);
     return true;
 }
 

@@ -49,9 +49,9 @@ namespace {
 using namespace dev;
 using namespace qmv;
 
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kThreads = (kConsumerWarps + 2) * 32;   // consumers, TMA producer, reducer
 constexpr int kMaxStages = 4;   // ring depth (36 KB stages); 5 measured no faster
-constexpr int kNumBars = 2 * kMaxStages + 1 + 4;   // full[S], empty[S], x, red_full[2], red_empty[2]
+constexpr int kNumBars = 2 * kMaxStages + 1 + 8;   // full[S], empty[S], x, red_full[4], red_empty[4]
 constexpr int kSmemLimit = 232448;               // dynamic shared memory a CTA may use
 
 struct Layout {
@@ -59,7 +59,7 @@ struct Layout {
     int x_bytes;     // M*K*2 rounded up to 16
     int xsum_off;    // float2 [M][G]
     int xinfo_off;   // int row_max[8], float inv_scale[8]
-    int red_off;     // float [2][16][32][M]
+    int red_off;     // float [bufs][16][32][M]
     int bar_off;     // uint64 [kNumBars] + abort flag
     int total;       // bytes (excluding the 1024 alignment slack)
 };
@@ -95,12 +95,12 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
     const uint32_t bar_full = s_base + L.bar_off;          // NS barriers (room for kMaxStages)
     const uint32_t bar_empty = bar_full + kMaxStages * 8;  // NS barriers
     const uint32_t bar_x = bar_empty + kMaxStages * 8;
-    const uint32_t bar_red = bar_x + 8;                    // red_full[2], red_empty[2]
+    const uint32_t bar_red = bar_x + 8;                    // red_full[4], red_empty[4]
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.bar_off + kNumBars * 8);
     TileCtx tc;
     tc.red = reinterpret_cast<float *>(smem + L.red_off);
     tc.red_full = bar_red;
-    tc.red_empty = bar_red + 16;
+    tc.red_empty = bar_red + 32;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -117,7 +117,7 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
             mbar_init(bar_empty + 8 * s, kConsumerWarps);
         }
         mbar_init(bar_x, 1);
-        for (int p = 0; p < 2; ++p) {
+        for (int p = 0; p < red_bufs<ONE_ROW>(); ++p) {
             mbar_init(tc.red_full + 8 * p, kConsumerWarps);
             mbar_init(tc.red_empty + 8 * p, 1);
         }
@@ -179,6 +179,21 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
             }
         }
         __syncwarp();
+    } else if (warp == kConsumerWarps + 1) {
+        // ------------------------------------------------------------ reducer
+        // Adds the sixteen warps' partials of each tile and stores y (the
+        // consumers deposit a tile only after their griddepcontrol.wait, so y
+        // is written after the preceding kernel).
+        for (int t = 0; t < my_tiles; ++t) {
+            const int tile = (int)blockIdx.x + t * (int)gridDim.x;
+            if (!reduce_tile<ONE_ROW>(tc, t, tile, M, N, y, lane, timeout_ns, abort_flag)) {
+                if (lane == 0 && !*abort_flag) {
+                    atomicExch(status, (int)AQ_DEVICE_STATUS_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+        }
     } else {
         // ---------------------------------------------------------------- consumers
         // Every consumer warp runs the whole loop, even after a timeout, because
@@ -207,7 +222,6 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
         bool ok = alive && !*abort_flag;
         int item = 0;
         for (int t = 0; ok && t < my_tiles; ++t) {
-            const int tile = (int)blockIdx.x + t * (int)gridDim.x;
             for (int kb = 0; kb < KB; ++kb, ++item) {
                 const int slot = item % NS;
                 if (!mbar_wait_fast(bar_full + 8 * slot, (uint32_t)(item / NS) & 1u, deadline, abort_flag)) {
@@ -220,7 +234,7 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                 if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
             }
             if (!ok) break;
-            ok = finish_tile<ONE_ROW>(tc, acc, t, tile, M, N, y, inv_scale, warp, lane, timeout_ns, abort_flag, nullptr);
+            ok = deposit_tile<ONE_ROW>(tc, acc, t, M, warp, lane, inv_scale, timeout_ns, abort_flag);
         }
         if (!ok) fail();
     }
