@@ -240,7 +240,7 @@ def run_case(args):
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for name in ("qmv.cu", "qmv_tma.cu"):
+    for name in ("qmv_chain.cu", "qmv_tma.cu", "qmv_consumer.cuh", "aq_ptx.cuh"):
         with open(os.path.join(ROOT, "affine_bit_quantized_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -249,7 +249,7 @@ def kernel_source_hash() -> str:
 def committed_traffic():
     """Per-step DRAM bytes from the committed ncu summary, if it was taken on
     the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "qmv_decode_step_dram_traffic.txt")
+    path = os.path.join(ROOT, "profiles", "qmv_chain_decode_step_dram_traffic.txt")
     try:
         kv = {}
         with open(path) as f:
@@ -573,7 +573,7 @@ def main():
         "pct_of_hbm_peak": round(100 * gbs / world / hbm_peak, 1),
         "roofline": {"bound": "hbm", "achieved": round(step_bytes / (ms_step * 1e-3) / 1e9, 1), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(step_bytes / (ms_step * 1e-3) / 1e9 / hbm_peak, 4),
-                     "traffic": traffic if args.step_impl == "graph" else None,
+                     "traffic": traffic if args.step_impl == "chain" else None,
                      "kernel": {"chain": "qmv_chain_kernel (the one launch of the step)",
                                 "graph": "qmv_tma_kernel (every launch of the step)"}[args.step_impl],
                      "peak_source": f"{peak_src} hbm_gbs (copy)"},
