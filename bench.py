@@ -531,17 +531,21 @@ def main():
     if cpu_layers:
         import oracle
         threads = oracle.default_threads()
-        done_bytes, t0 = 0, time.perf_counter()
-        for (layer, j), w in sorted(host_keep.items()):
-            name = synth.LLAMA8B_LAYER[j][0]
-            xo, K, xseed = offs[(layer, ROLE_OF[name])]
-            x = x_host[xo:xo + K].reshape(1, K)
-            oracle.matmul(x, w.w_packed, w.scales, w.biases, 1, w.N, w.K, nthreads=threads)
-            done_bytes += alg_bytes(1, w.N, w.K)
+        done_bytes, passes, t0 = 0, 0, time.perf_counter()
+        # layers 0-1 of the step, repeated until at least 10 s of CPU work (at most 50 passes)
+        while passes < 50 and (passes == 0 or time.perf_counter() - t0 < 10.0):
+            for (layer, j), w in sorted(host_keep.items()):
+                name = synth.LLAMA8B_LAYER[j][0]
+                xo, K, xseed = offs[(layer, ROLE_OF[name])]
+                x = x_host[xo:xo + K].reshape(1, K)
+                oracle.matmul(x, w.w_packed, w.scales, w.biases, 1, w.N, w.K, nthreads=threads)
+                done_bytes += alg_bytes(1, w.N, w.K)
+            passes += 1
         dt = time.perf_counter() - t0
         cpu = {"value": round(done_bytes / dt / 1e9, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": f"layers 0-1 of the step ({len(host_keep)} matrices, "
-                         f"{sum(w.N * w.K for w in host_keep.values()) / 1e6:.0f} M weights), M=1, fp64",
+                         f"{sum(w.N * w.K for w in host_keep.values()) / 1e6:.0f} M weights), M=1, fp64, "
+                         f"{passes} passes",
                "seconds": round(dt, 2)}
 
     gbs = world * step_bytes / (ms_step * 1e-3) / 1e9
