@@ -12,7 +12,7 @@
 //   * warp 0 (one thread) streams raw tiles with TMA: x (bf16, 128-byte
 //     swizzle), the packed codes of the 256 W rows, and every 8 groups the
 //     rows' bf16 scales and biases;
-//   * warps 2..9 turn a raw stage into the MMA operands, in the canonical
+//   * warps 2..17 turn a raw stage into the MMA operands, in the canonical
 //     K-major 128-byte-swizzled layout: W is dequantized to fp16 as
 //     fp16(scale * q + bias) (q made exact with the 1024 + q exponent trick,
 //     then one HFMA2, so one rounding per weight), and x is converted from
@@ -50,7 +50,7 @@ namespace {
 constexpr int kTileM = 256;            // rows of x per CTA (two UMMA M=128 halves)
 constexpr int kTileN = 256;            // rows of W per CTA (UMMA N)
 constexpr int kGroup = 64;             // K per pipeline step (one quantization group)
-constexpr int kConvWarps = 8;
+constexpr int kConvWarps = 16;
 constexpr int kThreads = (2 + kConvWarps) * 32;
 constexpr int kConvThreads = kConvWarps * 32;
 constexpr int kSBGroups = 8;           // groups of scales/biases per TMA box (16 bytes per row)
@@ -341,7 +341,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         }
     } else {
         // ------------------------------------------------------------ converters
-        const int t = threadIdx.x - 64;  // 0..255
+        const int t = threadIdx.x - 64;  // 0..kConvThreads-1
         const uint32_t magic = 0x64006400u;   // fp16x2 (1024, 1024)
         const uint32_t off2 = 0x64006400u;
         bool alive = true;
@@ -373,25 +373,31 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 o.w = f32x2_to_f16x2(bf16hi(v.y), bf16hi(v.w));
                 sts128(conv + off, o);
             }
-            // W: word (row r, chunk c) -> 8 fp16 weights at row r, chunk c ^ (r & 7)
+            // W: thread t takes half of row r = t / 2 (words 4h..4h+3, h = t % 2) and
+            // converts the row's scale and bias once; word c becomes 8 fp16
+            // weights at row r, chunk c ^ (r & 7)
             const uint32_t sb = base + kOffSB + ss * 2 * kSBBytes;
             const int g8 = i % kSBGroups;
-#pragma unroll 2
-            for (int e = 0; e < kRawCodeBytes / 4 / kConvThreads; ++e) {
-                const int wi = e * kConvThreads + t;
-                const int r = wi >> 3, c = wi & 7;
-                const uint32_t w = lds32(raw + kRawXBytes + wi * 4);
+            {
+                static_assert(kConvThreads == 2 * kTileN, "two converter threads per W row");
+                const int r = t >> 1, hw = t & 1;
+                const uint4 wv = lds128(raw + kRawXBytes + r * 32 + hw * 16);
                 const __half sh = __float2half_rn(__uint_as_float((uint32_t)lds16(sb + (r * kSBGroups + g8) * 2) << 16));
                 const __half bh =
                     __float2half_rn(__uint_as_float((uint32_t)lds16(sb + kSBBytes + (r * kSBGroups + g8) * 2) << 16));
                 const uint32_t s2 = (uint32_t)__half_as_ushort(sh) * 0x00010001u;
                 const uint32_t b2 = (uint32_t)__half_as_ushort(bh) * 0x00010001u;
-                uint4 o;
-                o.x = dequant_pair(code_pair_f16(w, magic), s2, b2, off2);
-                o.y = dequant_pair(code_pair_f16(w >> 4, magic), s2, b2, off2);
-                o.z = dequant_pair(code_pair_f16(w >> 8, magic), s2, b2, off2);
-                o.w = dequant_pair(code_pair_f16(w >> 12, magic), s2, b2, off2);
-                sts128(conv + kATileBytes + r * 128 + ((c ^ (r & 7)) << 4), o);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t w = e == 0 ? wv.x : e == 1 ? wv.y : e == 2 ? wv.z : wv.w;
+                    const int c = 4 * hw + e;
+                    uint4 o;
+                    o.x = dequant_pair(code_pair_f16(w, magic), s2, b2, off2);
+                    o.y = dequant_pair(code_pair_f16(w >> 4, magic), s2, b2, off2);
+                    o.z = dequant_pair(code_pair_f16(w >> 8, magic), s2, b2, off2);
+                    o.w = dequant_pair(code_pair_f16(w >> 12, magic), s2, b2, off2);
+                    sts128(conv + kATileBytes + r * 128 + ((c ^ (r & 7)) << 4), o);
+                }
             }
             fence_proxy_async();  // make the generic-proxy stores visible to the MMA (async proxy)
             __syncwarp();
@@ -402,7 +408,8 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             }
         }
         // ------------------------------------------------------------ epilogue
-        bool go = alive && mbar_wait(acc_done, 0, deadline, abort_flag) && !*abort_flag;
+        // warps 2..9 read the accumulators (two per TMEM lane quarter); the rest are done
+        bool go = warp < 10 && alive && mbar_wait(acc_done, 0, deadline, abort_flag) && !*abort_flag;
         go = __all_sync(0xFFFFFFFFu, go);   // tcgen05.ld below is warp-collective
         if (go) {
             tc_fence_after();
@@ -434,7 +441,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                     }
                 }
             }
-        } else if (alive) {
+        } else if (alive && warp < 10) {
             fail();
         }
     }
