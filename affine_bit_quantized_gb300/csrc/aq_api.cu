@@ -57,7 +57,7 @@ constexpr int kQmvMaxRows = 16;                // rows of x per weight-streaming
 aq_status validate(const void *x, const uint32_t *w, const void *s, const void *b, void *y,
                    int64_t M, int64_t N, int64_t K, int group_size, int bits) {
     if (M < 0 || N < 0 || K < 0) return AQ_ERR_INVALID_ARG;
-    if (bits != 4 || group_size != 64) return AQ_ERR_UNSUPPORTED;
+    if ((bits != 4 && bits != 8) || group_size != 64) return AQ_ERR_UNSUPPORTED;
     if (K % group_size) return AQ_ERR_INVALID_ARG;
     if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return AQ_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return AQ_OK;
@@ -66,6 +66,12 @@ aq_status validate(const void *x, const uint32_t *w, const void *s, const void *
     if (!x || !w || !s || !b) return AQ_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(w, 16) || !aligned(s, 2) || !aligned(b, 2) || !aligned(y, 2))
         return AQ_ERR_ALIGNMENT;
+    if (bits == 8) {
+        // 8-bit codes run on the TMA-fed decode kernel only (one row of x per
+        // pass at the largest K)
+        if (K % 512 || K > 16384) return AQ_ERR_UNSUPPORTED;
+        if (!aligned(s, 16) || !aligned(b, 16)) return AQ_ERR_ALIGNMENT;
+    }
     return AQ_OK;
 }
 
@@ -81,6 +87,7 @@ aq_status aq_matmul_bf16_ex(const void *x, const uint32_t *w_packed, const void 
     if (flags & ~(unsigned)(AQ_FLAG_PDL | AQ_FLAG_DEBUG_SKIP_X)) return AQ_ERR_INVALID_ARG;
     aq_status st = validate(x, w_packed, scales, biases, y, M, N, K, group_size, bits);
     if (st != AQ_OK || M == 0 || N == 0) return st;
+    if (bits == 8 && kernel == AQ_KERNEL_QMM) return AQ_ERR_UNSUPPORTED;   // no tensor-core path for 8-bit yet
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (K == 0) return record_cuda(cudaMemsetAsync(y, 0, (size_t)(M * N) * 2, cs));
 
@@ -99,6 +106,21 @@ aq_status aq_matmul_bf16_ex(const void *x, const uint32_t *w_packed, const void 
     a.x = x;
     a.y = y;
     a.M = M;
+    a.bits = bits;
+    if (bits == 8) {
+        // 8-bit codes run on the TMA-fed decode kernel only, in passes of as many
+        // rows of x as it stages at once (no tensor-core path for them yet)
+        const int64_t rows = K <= 2048 ? 8 : (K >= 16384 ? 1 : 16384 / K);
+        for (int64_t m0 = 0; m0 < M; m0 += rows) {
+            a.x = static_cast<const uint16_t *>(x) + m0 * K;
+            a.y = static_cast<uint16_t *>(y) + m0 * N;
+            a.M = (M - m0) < rows ? (M - m0) : rows;
+            if (!aq::qmv_tma_supported(a)) return AQ_ERR_UNSUPPORTED;
+            st = record_cuda(aq::launch_qmv_tma(a));
+            if (st != AQ_OK) return st;
+        }
+        return AQ_OK;
+    }
     if (kernel == AQ_KERNEL_QMM || (kernel == AQ_KERNEL_AUTO && M > kQmvMaxRows)) {
         if (a.debug_skip_x) return AQ_ERR_UNSUPPORTED;
         if (aq::qmm_supported(a)) return record_cuda(aq::launch_qmm(a));

@@ -12,7 +12,7 @@ namespace aq {
 // Arguments of one y = x . dequant(W)^T launch, already validated.
 struct MatmulArgs {
     const void *x;           // bf16 [M, K]
-    const uint32_t *w;       // uint32 [N, K/8]
+    const uint32_t *w;       // uint32 [N, K*bits/32]
     const uint16_t *scales;  // bf16 bits [N, K/64]
     const uint16_t *biases;  // bf16 bits [N, K/64]
     void *y;                 // bf16 [M, N]
@@ -22,6 +22,7 @@ struct MatmulArgs {
     int *status;             // device status word (bounded waits record timeouts here)
     uint64_t timeout_ns;     // deadline of every bounded device-side wait
     bool debug_skip_x;       // test hook: the TMA kernel omits the copy of x
+    int bits = 4;            // code width: 4 or 8 (8: the TMA-fed decode kernel only)
 };
 
 // Values of the device status word.

@@ -151,6 +151,14 @@ __device__ __forceinline__ uint32_t hi_pair(uint32_t v) {
     return r;
 }
 
+// 8-bit codes: fp16x2 (1024 + v[7:0], 1024 + v[23:16]); for a packed word w,
+// byte_pair(w) holds codes (0,2) and byte_pair(w >> 8) codes (1,3)
+__device__ __forceinline__ uint32_t byte_pair(uint32_t v) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, 0x00FF00FF, 0x64006400, 0xEA;" : "=r"(r) : "r"(v));
+    return r;
+}
+
 // D += A(16x16, fp16) * B(16x8, fp16), fp32 accumulation
 __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                               uint32_t b0, uint32_t b1) {

@@ -32,6 +32,7 @@
 #include <atomic>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 #include <vector>
 
 #include "aq.h"
@@ -48,11 +49,13 @@ struct ChainRec {                // 128-byte aligned, as CUtensorMap is
     int M, N, K, tiles;           // tiles = ceil(N / 32)
     int flags;                    // AQ_CHAIN_INDEPENDENT
     int tile_base;                // tiles of the preceding matmuls since the last dependent one
-    int pad[6];
+    int bits;                     // code width: 4 or 8
+    int pad[5];
 };
 static_assert(sizeof(ChainRec) % 128 == 0, "records must stay 128-byte aligned");
 static_assert(offsetof(ChainRec, x) % 16 == 0 && offsetof(ChainRec, M) == offsetof(ChainRec, x) + 16 &&
-                  offsetof(ChainRec, flags) == offsetof(ChainRec, x) + 32,
+                  offsetof(ChainRec, flags) == offsetof(ChainRec, x) + 32 &&
+                  offsetof(ChainRec, bits) == offsetof(ChainRec, x) + 40,
               "the scalar part of a record is read as three 16-byte vectors");
 
 namespace {
@@ -98,7 +101,7 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *m) {
 struct RecInfo {
     const __nv_bfloat16 *x;
     __nv_bfloat16 *y;
-    int M, N, K, T, flags, tile_base;
+    int M, N, K, T, flags, tile_base, bits;
 };
 __device__ __forceinline__ RecInfo unpack_info(uint4 a, uint4 b, uint4 c) {
     RecInfo i;
@@ -110,6 +113,7 @@ __device__ __forceinline__ RecInfo unpack_info(uint4 a, uint4 b, uint4 c) {
     i.T = (int)b.w;
     i.flags = (int)c.x;
     i.tile_base = (int)c.y;
+    i.bits = (int)c.z;
     return i;
 }
 // Record jm's scalars: the first kInfoCap come from the copy every CTA makes in
@@ -121,7 +125,8 @@ __device__ __forceinline__ RecInfo load_info(const ChainRec *recs, const uint4 *
     return unpack_info(__ldg(p), __ldg(p + 1), __ldg(p + 2));
 }
 
-template <bool ONE_ROW>
+// BITS: code width of every matmul of the chain (4 or 8).
+template <int BITS, bool ONE_ROW>
 __global__ void __launch_bounds__(kThreads, 1)
 qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_bytes, int max_m,
                  unsigned long long timeout_ns, int *status) {
@@ -190,8 +195,9 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
                     prefetch_tensormap(&rec[1].tb);
                 }
                 const int K = cur.K, T = cur.T;
-                const int nbox = K / kBoxCodes;
-                const int KB = (K + kStageCodes - 1) / kStageCodes;
+                constexpr int SC = Geo<BITS>::kStageCodes, SG = Geo<BITS>::kStageGroups;
+                const int nbox = K / Geo<BITS>::kBoxCodes;             // 128-byte code boxes per row
+                const int KB = (K + SC - 1) / SC;
                 // tiles are dealt round-robin, continuing from the previous
                 // matmul of the same dependency group so that the group stays
                 // balanced
@@ -208,11 +214,11 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
                         const uint32_t fb = bar_full + 8 * slot;
                         int nvalid = nbox - kb * kBoxes;
                         nvalid = nvalid < kBoxes ? nvalid : kBoxes;
-                        mbar_expect_tx(fb, (uint32_t)(nvalid * kBoxBytes + 2 * kSBBytes));
+                        mbar_expect_tx(fb, (uint32_t)(nvalid * kBoxBytes + 2 * kRows * SG * 2));
                         for (int b = 0; b < nvalid; ++b)
                             tma_load_2d(dst + b * kBoxBytes, &rec->tw, (kb * kBoxes + b) * 32, tile * kRows, fb, pol);
-                        tma_load_2d(dst + kCodesBytes, &rec->ts, kb * kStageGroups, tile * kRows, fb, pol);
-                        tma_load_2d(dst + kCodesBytes + kSBBytes, &rec->tb, kb * kStageGroups, tile * kRows, fb, pol);
+                        tma_load_2d(dst + kCodesBytes, &rec->ts, kb * SG, tile * kRows, fb, pol);
+                        tma_load_2d(dst + kCodesBytes + kSBRegion, &rec->tb, kb * SG, tile * kRows, fb, pol);
                         ++issued;
                     }
                 }
@@ -277,19 +283,17 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
         int tcount = 0, item = 0, ndep = 0, nstaged = 0;
         bool ok = true;
         const __nv_bfloat16 *prev_x = nullptr;
-        int prev_M = 0, prev_K = 0;
+        int prev_M = 0, prev_K = 0, prev_bits = 0;
         RecInfo cur = load_info(recs, info, 0);
         for (int jm = 0; jm < count; ++jm) {
             RecInfo nxt = cur;
             if (jm + 1 < count) nxt = load_info(recs, info, jm + 1);
             const int M = cur.M, K = cur.K, T = cur.T;
-            const int nblk = K / kWarpCodes;
-            const int KB = (K + kStageCodes - 1) / kStageCodes;
             // A matmul flagged independent does not read the previous one's
             // output: it neither waits for it nor, when its x is the same
-            // buffer, reloads x.
+            // buffer (staged for the same code width), reloads x.
             const bool dep = jm > 0 && !(cur.flags & AQ_CHAIN_INDEPENDENT);
-            const bool new_x = jm == 0 || cur.x != prev_x || M != prev_M || K != prev_K;
+            const bool new_x = jm == 0 || cur.x != prev_x || M != prev_M || K != prev_K || cur.bits != prev_bits;
             if (dep) {
                 // the signaller saw every tile of matmul jm-1 stored
                 if (!mbar_wait_for(bar_dep, (uint32_t)(ndep & 1), timeout_ns, abort_flag)) ok = false;
@@ -298,31 +302,39 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
             prev_x = cur.x;
             prev_M = M;
             prev_K = K;
+            prev_bits = cur.bits;
 
-            // ---- x of this matmul: L2 loads, fp16 fragments, group sums and scales
-            if (new_x) stage_x<true>(xs, cur.x, 0, M, K, nstaged++);
+            auto run = [&](auto width) {
+                constexpr int BITS = decltype(width)::value;
+                using Gm = Geo<BITS>;
+                const int nblk = K / Gm::kWarpCodes;
+                const int KB = (K + Gm::kStageCodes - 1) / Gm::kStageCodes;
+                // ---- x of this matmul: L2 loads, fp16 fragments, group sums and scales
+                if (new_x) stage_x<true, BITS>(xs, cur.x, 0, M, K, nstaged++);
 
-            ConsumerThread ct;
-            consumer_init(ct, warp, lane, xs, M, K);
+                ConsumerThread ct;
+                consumer_init<BITS>(ct, warp, lane, xs, M, K);
 
-            const int first = (cta - cur.tile_base % ncta + ncta) % ncta;
-            for (int tile = first; tile < T && ok; tile += ncta) {
-                for (int kb = 0; kb < KB; ++kb, ++item) {
-                    const int slot = item % NS;
-                    const uint32_t phase = (uint32_t)(item / NS) & 1u;
-                    if (!mbar_wait_for(bar_full + 8 * slot, phase, timeout_ns, abort_flag)) {
-                        ok = false;
-                        break;
+                const int first = (cta - cur.tile_base % ncta + ncta) % ncta;
+                for (int tile = first; tile < T && ok; tile += ncta) {
+                    for (int kb = 0; kb < KB; ++kb, ++item) {
+                        const int slot = item % NS;
+                        const uint32_t phase = (uint32_t)(item / NS) & 1u;
+                        if (!mbar_wait_for(bar_full + 8 * slot, phase, timeout_ns, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        if (kb * kConsumerWarps + warp < nblk)
+                            consume_stage<BITS, ONE_ROW>(s_base + (uint32_t)(slot * kStageBytes), kb, ct, acc);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
                     }
-                    if (kb * kConsumerWarps + warp < nblk)
-                        consume_stage<ONE_ROW>(s_base + (uint32_t)(slot * kStageBytes), kb, ct, acc);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+                    if (!ok) break;
+                    ok = deposit_tile<ONE_ROW>(tc, acc, tcount, M, warp, lane, inv_scale, timeout_ns, abort_flag);
+                    ++tcount;
                 }
-                if (!ok) break;
-                ok = deposit_tile<ONE_ROW>(tc, acc, tcount, M, warp, lane, inv_scale, timeout_ns, abort_flag);
-                ++tcount;
-            }
+            };
+            run(std::integral_constant<int, BITS>());
             if (!ok) set_abort();   // the remaining matmuls are walked through without work
             cur = nxt;
         }
@@ -360,7 +372,7 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint6
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 constexpr int kMaxDevices = 64;
-std::atomic<int> g_attr_done[2][kMaxDevices];
+std::atomic<int> g_attr_done[4][kMaxDevices];
 std::atomic<int> g_sms[kMaxDevices];
 
 size_t records_bytes(int count) { return (size_t)count * sizeof(ChainRec); }
@@ -377,7 +389,7 @@ namespace {
 
 // Validates the descriptors (host only, no CUDA call).
 aq_status chain_validate(const aq_matmul_desc *descs, int count, int group_size, int bits) {
-    if (bits != 4 || group_size != 64) return AQ_ERR_UNSUPPORTED;
+    if ((bits != 4 && bits != 8) || group_size != 64) return AQ_ERR_UNSUPPORTED;
     for (int i = 0; i < count; ++i) {
         const aq_matmul_desc &d = descs[i];
         if (d.M < 1 || d.N < 1 || d.K < 1 || d.K % 64) return AQ_ERR_INVALID_ARG;
@@ -392,7 +404,7 @@ aq_status chain_validate(const aq_matmul_desc *descs, int count, int group_size,
 }
 
 // Encodes validated descriptors into host records and fills the plan's sizes.
-aq_status chain_encode(const aq_matmul_desc *descs, int count, ChainRec *recs, aq_chain_plan *plan) {
+aq_status chain_encode(const aq_matmul_desc *descs, int count, int bits, ChainRec *recs, aq_chain_plan *plan) {
     if (!encode_fn()) return AQ_ERR_UNSUPPORTED;
     int x_bytes = 16;
     bool one_row = true;
@@ -401,12 +413,14 @@ aq_status chain_encode(const aq_matmul_desc *descs, int count, ChainRec *recs, a
         ChainRec &r = recs[i];
         std::memset(&r, 0, sizeof r);
         const uint64_t K = (uint64_t)d.K, N = (uint64_t)d.N, G = K / 64;
-        if (!encode_2d(&r.tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, d.w_packed, K / 8, N, K / 2, 32, kRows,
+        // codes: 32-word x 32-row boxes, 128-byte swizzle; scales and biases: one
+        // stage's groups x 32 rows (64-byte rows and swizzle for 4-bit codes, 32 for 8-bit)
+        const uint32_t sg = (uint32_t)stage_groups(bits);
+        const CUtensorMapSwizzle sbs = bits == 8 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
+        if (!encode_2d(&r.tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, d.w_packed, K * bits / 32, N, K * bits / 8, 32, kRows,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_2d(&r.ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, d.scales, G, N, G * 2, kStageGroups, kRows,
-                       CU_TENSOR_MAP_SWIZZLE_64B) ||
-            !encode_2d(&r.tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, d.biases, G, N, G * 2, kStageGroups, kRows,
-                       CU_TENSOR_MAP_SWIZZLE_64B))
+            !encode_2d(&r.ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, d.scales, G, N, G * 2, sg, kRows, sbs) ||
+            !encode_2d(&r.tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, d.biases, G, N, G * 2, sg, kRows, sbs))
             return AQ_ERR_INVALID_ARG;
         r.x = static_cast<const __nv_bfloat16 *>(d.x);
         r.y = static_cast<__nv_bfloat16 *>(d.y);
@@ -415,6 +429,7 @@ aq_status chain_encode(const aq_matmul_desc *descs, int count, ChainRec *recs, a
         r.K = (int)d.K;
         r.tiles = (int)((d.N + kRows - 1) / kRows);
         r.flags = (int)d.flags;
+        r.bits = bits;
         r.tile_base = (i > 0 && (d.flags & AQ_CHAIN_INDEPENDENT)) ? recs[i - 1].tile_base + recs[i - 1].tiles : 0;
         x_bytes = std::max(x_bytes, (int)(d.M * d.K * 2));
         one_row = one_row && d.M == 1;
@@ -422,6 +437,7 @@ aq_status chain_encode(const aq_matmul_desc *descs, int count, ChainRec *recs, a
     plan->count = count;
     plan->x_bytes = (x_bytes + 15) & ~15;
     plan->one_row = one_row ? 1 : 0;
+    plan->reserved[0] = bits;   // code width of the chain (selects the kernel)
     return AQ_OK;
 }
 
@@ -434,13 +450,13 @@ aq_status chain_prepare(const aq_matmul_desc *descs, int count, int group_size, 
     std::memset(plan, 0, sizeof *plan);
     if (count == 0) return AQ_OK;
     if (!descs || !workspace) return AQ_ERR_INVALID_ARG;
-    if (bits != 4 || group_size != 64) return AQ_ERR_UNSUPPORTED;
+    if ((bits != 4 && bits != 8) || group_size != 64) return AQ_ERR_UNSUPPORTED;
     if (workspace_bytes < chain_workspace_bytes(count)) return AQ_ERR_INVALID_ARG;
     if (!aligned(workspace, 128)) return AQ_ERR_ALIGNMENT;
     aq_status st = chain_validate(descs, count, group_size, bits);  // before any CUDA call
     if (st != AQ_OK) return st;
     std::vector<ChainRec> recs((size_t)count);
-    st = chain_encode(descs, count, recs.data(), plan);
+    st = chain_encode(descs, count, bits, recs.data(), plan);
     if (st != AQ_OK) return st;
     *err = cudaMemcpy(workspace, recs.data(), records_bytes(count), cudaMemcpyHostToDevice);
     if (*err != cudaSuccess) {
@@ -467,12 +483,15 @@ cudaError_t chain_run(const aq_chain_plan *plan, uint64_t timeout_ns, int *statu
     const ChainLayout L = chain_layout(plan->x_bytes, max_m);
     const int smem = L.total + 1024;
     const bool one = plan->one_row != 0;
-    auto kern = one ? qmv_chain_kernel<true> : qmv_chain_kernel<false>;
-    if (!g_attr_done[one][dev].load(std::memory_order_acquire)) {
+    const bool eight = plan->reserved[0] == 8;
+    auto kern = eight ? (one ? qmv_chain_kernel<8, true> : qmv_chain_kernel<8, false>)
+                      : (one ? qmv_chain_kernel<4, true> : qmv_chain_kernel<4, false>);
+    const int ki = 2 * (int)eight + (int)one;
+    if (!g_attr_done[ki][dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemLimit);
         if (e != cudaSuccess) return e;
-        g_attr_done[one][dev].store(1, std::memory_order_release);
+        g_attr_done[ki][dev].store(1, std::memory_order_release);
     }
     int *done = reinterpret_cast<int *>(static_cast<uint8_t *>(plan->workspace) + records_bytes(count));
     e = cudaMemsetAsync(done, 0, (size_t)count * sizeof(int), stream);
@@ -541,7 +560,7 @@ aq_status chain_run_static(const aq_matmul_desc *descs, int count, int group_siz
     std::memset(&plan, 0, sizeof plan);
     {
         std::lock_guard<std::mutex> lock(g_static_host_mutex);
-        st = chain_encode(descs, count, g_static_host_recs, &plan);
+        st = chain_encode(descs, count, bits, g_static_host_recs, &plan);
         if (st != AQ_OK) return st;
         // from pageable memory: returns once the records are staged, so the
         // host buffer may be reused by the next call

@@ -40,15 +40,28 @@ using namespace dev;
 constexpr int kRows = 32;                                  // rows of W per tile
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kWarpCodes = 128;                            // codes of a warp's column block (2 groups)
-constexpr int kStageCodes = kWarpCodes * kConsumerWarps;   // 2048 codes per stage
-constexpr int kStageGroups = kStageCodes / 64;             // 32
-constexpr int kBoxCodes = 256;                             // codes per TMA box row (128 bytes)
-constexpr int kBoxes = kStageCodes / kBoxCodes;            // 8 code boxes per stage
+constexpr int kBoxes = 8;                                  // code boxes per stage ({32 words, 32 rows})
 constexpr int kBoxBytes = kRows * 128;                     // 4096
 constexpr int kCodesBytes = kBoxes * kBoxBytes;            // 32768
-constexpr int kSBBytes = kRows * kStageGroups * 2;         // 2048 (scales, and again biases)
-constexpr int kStageBytes = kCodesBytes + 2 * kSBBytes;    // 36864
+constexpr int kSBRegion = 2048;                            // room for one scale (or bias) box per stage
+constexpr int kStageBytes = kCodesBytes + 2 * kSBRegion;   // 36864
+
+// Geometry by code width.  A stage is 32 rows x 1024 bytes of codes, i.e.
+// 2048 4-bit or 1024 8-bit codes; each of the sixteen warps takes 128 bytes
+// of every row (two groups of 4-bit codes, one group of 8-bit codes).
+template <int BITS>
+struct Geo {
+    static_assert(BITS == 4 || BITS == 8, "4-bit and 8-bit codes");
+    static constexpr int kGroupsPerWarp = BITS == 4 ? 2 : 1;
+    static constexpr int kWarpCodes = 64 * kGroupsPerWarp;              // codes of a warp's column block
+    static constexpr int kStageCodes = kWarpCodes * kConsumerWarps;     // 2048 or 1024
+    static constexpr int kStageGroups = kStageCodes / 64;               // 32 or 16
+    static constexpr int kBoxCodes = 1024 / BITS;                       // codes per 128-byte box row
+    static constexpr int kSBRowBytes = kStageGroups * 2;                // 64 or 32 bytes: scale-box row
+};
+// the same numbers at run time (host and device)
+__host__ __device__ constexpr int stage_codes(int bits) { return bits == 4 ? 2048 : 1024; }
+__host__ __device__ constexpr int stage_groups(int bits) { return stage_codes(bits) / 64; }
 constexpr int kMaxM = 8;                                   // rows of x these kernels take
 constexpr int kMaxXBytes = 32768;                          // M*K*2 limit for staging x once per CTA
 constexpr int kXInfoBytes = 96;                            // int row_max[2][8], float inv_scale[8]
@@ -108,7 +121,7 @@ __device__ __forceinline__ uint4 ldg_cg_v4(const void *p) {
 // may still be in use on entry).  `n` counts the stagings of this CTA: staging
 // n takes its row maxima in buffer n % 2, which is zero on entry and is
 // cleared again for staging n + 2.  M*K <= 16384, K % 512 == 0.
-template <bool FROM_GLOBAL>
+template <bool FROM_GLOBAL, int BITS>
 __device__ __forceinline__ void stage_x(const XStage &xs, const __nv_bfloat16 *xg, uint32_t raw, int M, int K, int n) {
     const int tid = threadIdx.x;
     const int words = M * K / 8;
@@ -140,15 +153,24 @@ __device__ __forceinline__ void stage_x(const XStage &xs, const __nv_bfloat16 *x
         if (wi < words) {
             const int m = wi / wpr, wr = wi - m * wpr;
             const float sc = pow2f(x_scale_exponent(row_max[m]));
-            const float sc16 = sc * 0.0625f;
+            const float sc16 = sc * 0.0625f;   // 4-bit: codes at bits 4-7 of a byte weigh 16x
             const uint4 a = v[u];
             const float x0 = bf16lo(a.x) * sc, x1 = bf16hi(a.x) * sc, x2 = bf16lo(a.y) * sc, x3 = bf16hi(a.y) * sc;
             const float x4 = bf16lo(a.z) * sc, x5 = bf16hi(a.z) * sc, x6 = bf16lo(a.w) * sc, x7 = bf16hi(a.w) * sc;
-            // fragment registers: (x0, x4), (x1, x5)/16, (x2, x6), (x3, x7)/16
-            const uint32_t p0 = f32x2_to_f16x2(x0, x4);
-            const uint32_t p1 = f32x2_to_f16x2(bf16hi(a.x) * sc16, bf16hi(a.z) * sc16);
-            const uint32_t p2 = f32x2_to_f16x2(x2, x6);
-            const uint32_t p3 = f32x2_to_f16x2(bf16hi(a.y) * sc16, bf16hi(a.w) * sc16);
+            uint32_t p0, p1, p2, p3;
+            if (BITS == 4) {
+                // fragment registers: (x0, x4), (x1, x5)/16, (x2, x6), (x3, x7)/16
+                p0 = f32x2_to_f16x2(x0, x4);
+                p1 = f32x2_to_f16x2(bf16hi(a.x) * sc16, bf16hi(a.z) * sc16);
+                p2 = f32x2_to_f16x2(x2, x6);
+                p3 = f32x2_to_f16x2(bf16hi(a.y) * sc16, bf16hi(a.w) * sc16);
+            } else {
+                // the chunk is code words 2c, 2c+1 of 8-bit codes: (x0, x2), (x1, x3), (x4, x6), (x5, x7)
+                p0 = f32x2_to_f16x2(x0, x2);
+                p1 = f32x2_to_f16x2(x1, x3);
+                p2 = f32x2_to_f16x2(x4, x6);
+                p3 = f32x2_to_f16x2(x5, x7);
+            }
             s_part = ((x0 + x1) + (x2 + x3)) + ((x4 + x5) + (x6 + x7));
             p_part = (f16x2_sum(p0) + f16x2_sum(p1)) + (f16x2_sum(p2) + f16x2_sum(p3));
             const int g = wr >> 3, w8 = wr & 7;
@@ -180,90 +202,151 @@ struct ConsumerThread {
     uint32_t xs0, xs1;  // (Xs, X') of this warp's first group in stage 0, x rows of columns 2j and 2j+1
 };
 
+template <int BITS>
 __device__ __forceinline__ void consumer_init(ConsumerThread &c, int warp, int lane, const XStage &xs, int M, int K) {
+    using Gm = Geo<BITS>;
     const int gid = lane >> 2, j = lane & 3;
     // code boxes use the 128-byte swizzle: 16-byte chunk c of box row r sits at chunk c ^ (r % 8)
-    const int c0 = (4 * (warp & 1)) | (j >> 1);
+    if (BITS == 4) {
+        // words 2j, 2j+1 of groups 2w, 2w+1: 8 bytes per group
+        const int c0 = (4 * (warp & 1)) | (j >> 1);
 #pragma unroll
-    for (int gl = 0; gl < 2; ++gl)
-        c.code[gl] = (uint32_t)((warp >> 1) * kBoxBytes + gid * 128 + (((c0 ^ gid) ^ (2 * gl)) << 4) + ((j & 1) << 3));
-    // scale boxes (64-byte rows) use the 64-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ ((r / 2) % 4)
-    c.sb = (uint32_t)(gid * 64 + (((warp >> 2) ^ ((gid >> 1) & 3)) << 4) + ((warp & 3) << 2));
+        for (int gl = 0; gl < 2; ++gl)
+            c.code[gl] = (uint32_t)((warp >> 1) * kBoxBytes + gid * 128 + (((c0 ^ gid) ^ (2 * gl)) << 4) + ((j & 1) << 3));
+        // scale boxes (64-byte rows), 64-byte swizzle: chunk c of row r sits at chunk c ^ ((r / 2) % 4)
+        c.sb = (uint32_t)(gid * 64 + (((warp >> 2) ^ ((gid >> 1) & 3)) << 4) + ((warp & 3) << 2));
+    } else {
+        // words 4j..4j+3 of group w: 16 bytes
+        const int c0 = 4 * (warp & 1) + j;
+        c.code[0] = c.code[1] = (uint32_t)((warp >> 1) * kBoxBytes + gid * 128 + ((c0 ^ gid) << 4));
+        // scale boxes (32-byte rows), 32-byte swizzle: chunk bit 0 ^= row bit 2; the word of groups
+        // w & ~1 and w | 1
+        c.sb = (uint32_t)(gid * 32 + ((((warp >> 3) ^ (gid >> 2)) & 1) << 4) + (((warp >> 1) & 3) << 2));
+    }
     const int xr = (lane & 7) < M ? (lane & 7) : M - 1;
-    c.xq = xs.xq + (uint32_t)(xr * 2 * K + (lane >> 3) * 16 + warp * 256);
+    c.xq = xs.xq + (uint32_t)(xr * 2 * K + (lane >> 3) * 16 + warp * Gm::kGroupsPerWarp * 128);
     const int G = K / 64;
     const int m0 = 2 * j < M ? 2 * j : M - 1, m1 = 2 * j + 1 < M ? 2 * j + 1 : M - 1;
-    c.xs0 = xs.xsum + (uint32_t)((m0 * G + 2 * warp) * 8);
-    c.xs1 = xs.xsum + (uint32_t)((m1 * G + 2 * warp) * 8);
+    c.xs0 = xs.xsum + (uint32_t)((m0 * G + Gm::kGroupsPerWarp * warp) * 8);
+    c.xs1 = xs.xsum + (uint32_t)((m1 * G + Gm::kGroupsPerWarp * warp) * 8);
 }
 
-// Adds the warp's 32-row x 128-code block of stage `st` (stage index kb of
-// the tile) to acc.  acc[h][*] are the MMA accumulator registers of row block
-// h: (row, column) = (gid, 2j), (gid, 2j+1), (gid+8, 2j), (gid+8, 2j+1).
+// acc += scale * (D - 1024 X') + bias * Xs for one group: D = d[h] (the MMA
+// accumulators of row block h), scale/bias of rows gid + 8r in s[r], b[r],
+// (Xs, X') of the group at xs0 (column 2j) and xs1 (column 2j+1).
 template <bool ONE_ROW>
+__device__ __forceinline__ void fold_group(const float (&d)[2][4], const float (&sc)[4], const float (&bi)[4],
+                                           uint32_t xs0, uint32_t xs1, float (&acc)[2][4]) {
+    if (ONE_ROW) {
+        const uint2 xv = lds64(xs0);
+        const float xsum = __uint_as_float(xv.x), xpr = __uint_as_float(xv.y);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float2 s2 = make_float2(sc[2 * h], sc[2 * h + 1]);
+            const float2 b2 = make_float2(bi[2 * h], bi[2 * h + 1]);
+            const float2 t = fma2(make_float2(-1024.f, -1024.f), make_float2(xpr, xpr), make_float2(d[h][0], d[h][2]));
+            const float2 a = fma2(s2, t, fma2(b2, make_float2(xsum, xsum), make_float2(acc[h][0], acc[h][2])));
+            acc[h][0] = a.x;
+            acc[h][2] = a.y;
+        }
+    } else {
+        const uint2 xa = lds64(xs0), xb = lds64(xs1);
+        const float2 xsum = make_float2(__uint_as_float(xa.x), __uint_as_float(xb.x));
+        const float2 xpr = make_float2(__uint_as_float(xa.y), __uint_as_float(xb.y));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const float s = sc[2 * h + rr], b = bi[2 * h + rr];
+                const float2 t = fma2(make_float2(-1024.f, -1024.f), xpr, make_float2(d[h][2 * rr], d[h][2 * rr + 1]));
+                const float2 a = fma2(make_float2(s, s), t,
+                                      fma2(make_float2(b, b), xsum, make_float2(acc[h][2 * rr], acc[h][2 * rr + 1])));
+                acc[h][2 * rr] = a.x;
+                acc[h][2 * rr + 1] = a.y;
+            }
+        }
+    }
+}
+
+// Adds the warp's block of stage `st` (32 rows x 128 bytes of codes; stage
+// index kb of the tile) to acc.  acc[h][*] are the MMA accumulator registers
+// of row block h: (row, column) = (gid, 2j), (gid, 2j+1), (gid+8, 2j),
+// (gid+8, 2j+1).
+template <int BITS, bool ONE_ROW>
 __device__ __forceinline__ void consume_stage(uint32_t st, int kb, const ConsumerThread &c, float (&acc)[2][4]) {
+    using Gm = Geo<BITS>;
     uint32_t sw[4], bw[4];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-        sw[r] = lds32(st + kCodesBytes + c.sb + 512 * r);
-        bw[r] = lds32(st + kCodesBytes + kSBBytes + c.sb + 512 * r);
+        sw[r] = lds32(st + kCodesBytes + c.sb + 8 * Gm::kSBRowBytes * r);
+        bw[r] = lds32(st + kCodesBytes + kSBRegion + c.sb + 8 * Gm::kSBRowBytes * r);
     }
-    const uint32_t xq = c.xq + (uint32_t)kb * (kStageGroups * 128);
-    const uint32_t xo = (uint32_t)kb * (kStageGroups * 8);
+    const uint32_t xq = c.xq + (uint32_t)kb * (Gm::kStageGroups * 128);
+    const uint32_t xo = (uint32_t)kb * (Gm::kStageGroups * 8);
+    if (BITS == 4) {
 #pragma unroll
-    for (int gl = 0; gl < 2; ++gl) {
-        uint2 wr[4];
+        for (int gl = 0; gl < 2; ++gl) {
+            uint2 wr[4];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) wr[r] = lds64(st + c.code[gl] + 1024 * r);
+            for (int r = 0; r < 4; ++r) wr[r] = lds64(st + c.code[gl] + 1024 * r);
+            float d[2][4];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const uint4 X = ldsm_x4(xq + gl * 128 + i * 64);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t wa = i ? wr[2 * h].y : wr[2 * h].x;
+                    const uint32_t wb = i ? wr[2 * h + 1].y : wr[2 * h + 1].x;
+                    const uint32_t ta = wa >> 8, tb = wb >> 8;
+                    if (i == 0)
+                        mma_f16_16816_zc(d[h], lo_pair(wa), lo_pair(wb), hi_pair(wa), hi_pair(wb), X.x, X.y);
+                    else
+                        mma_f16_16816(d[h], lo_pair(wa), lo_pair(wb), hi_pair(wa), hi_pair(wb), X.x, X.y);
+                    mma_f16_16816(d[h], lo_pair(ta), lo_pair(tb), hi_pair(ta), hi_pair(tb), X.z, X.w);
+                }
+            }
+            float sc[4], bi[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                sc[r] = gl ? bf16hi(sw[r]) : bf16lo(sw[r]);
+                bi[r] = gl ? bf16hi(bw[r]) : bf16lo(bw[r]);
+            }
+            fold_group<ONE_ROW>(d, sc, bi, c.xs0 + xo + gl * 8, c.xs1 + xo + gl * 8, acc);
+        }
+    } else {
+        // 8-bit: thread j holds words 4j..4j+3 of its rows' group; k-step s of
+        // the MMA takes word 4j + s, bytes (0, 2) and (1, 3) as two code pairs
+        uint4 wr[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) wr[r] = lds128(st + c.code[0] + 1024 * r);
         float d[2][4];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const uint4 X = ldsm_x4(xq + gl * 128 + i * 64);
+        for (int sp = 0; sp < 2; ++sp) {
+            const uint4 X = ldsm_x4(xq + sp * 64);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint32_t wa = i ? wr[2 * h].y : wr[2 * h].x;
-                const uint32_t wb = i ? wr[2 * h + 1].y : wr[2 * h + 1].x;
-                const uint32_t ta = wa >> 8, tb = wb >> 8;
-                if (i == 0)
-                    mma_f16_16816_zc(d[h], lo_pair(wa), lo_pair(wb), hi_pair(wa), hi_pair(wb), X.x, X.y);
-                else
-                    mma_f16_16816(d[h], lo_pair(wa), lo_pair(wb), hi_pair(wa), hi_pair(wb), X.x, X.y);
-                mma_f16_16816(d[h], lo_pair(ta), lo_pair(tb), hi_pair(ta), hi_pair(tb), X.z, X.w);
-            }
-        }
-        if (ONE_ROW) {
-            const uint2 xv = lds64(c.xs0 + xo + gl * 8);
-            const float xsum = __uint_as_float(xv.x), xpr = __uint_as_float(xv.y);
+            for (int ss = 0; ss < 2; ++ss) {
+                const int s = 2 * sp + ss;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const float2 s2 = make_float2(gl ? bf16hi(sw[2 * h]) : bf16lo(sw[2 * h]),
-                                              gl ? bf16hi(sw[2 * h + 1]) : bf16lo(sw[2 * h + 1]));
-                const float2 b2 = make_float2(gl ? bf16hi(bw[2 * h]) : bf16lo(bw[2 * h]),
-                                              gl ? bf16hi(bw[2 * h + 1]) : bf16lo(bw[2 * h + 1]));
-                const float2 t = fma2(make_float2(-1024.f, -1024.f), make_float2(xpr, xpr), make_float2(d[h][0], d[h][2]));
-                const float2 a = fma2(s2, t, fma2(b2, make_float2(xsum, xsum), make_float2(acc[h][0], acc[h][2])));
-                acc[h][0] = a.x;
-                acc[h][2] = a.y;
-            }
-        } else {
-            const uint2 xa = lds64(c.xs0 + xo + gl * 8), xb = lds64(c.xs1 + xo + gl * 8);
-            const float2 xsum = make_float2(__uint_as_float(xa.x), __uint_as_float(xb.x));
-            const float2 xpr = make_float2(__uint_as_float(xa.y), __uint_as_float(xb.y));
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
-                    const float s = gl ? bf16hi(sw[2 * h + rr]) : bf16lo(sw[2 * h + rr]);
-                    const float b = gl ? bf16hi(bw[2 * h + rr]) : bf16lo(bw[2 * h + rr]);
-                    const float2 t = fma2(make_float2(-1024.f, -1024.f), xpr,
-                                          make_float2(d[h][2 * rr], d[h][2 * rr + 1]));
-                    const float2 a = fma2(make_float2(s, s), t,
-                                          fma2(make_float2(b, b), xsum, make_float2(acc[h][2 * rr], acc[h][2 * rr + 1])));
-                    acc[h][2 * rr] = a.x;
-                    acc[h][2 * rr + 1] = a.y;
+                for (int h = 0; h < 2; ++h) {
+                    const uint4 &A = wr[2 * h], &B = wr[2 * h + 1];
+                    const uint32_t wa = s == 0 ? A.x : s == 1 ? A.y : s == 2 ? A.z : A.w;
+                    const uint32_t wb = s == 0 ? B.x : s == 1 ? B.y : s == 2 ? B.z : B.w;
+                    const uint32_t b0 = ss ? X.z : X.x, b1 = ss ? X.w : X.y;
+                    if (s == 0)
+                        mma_f16_16816_zc(d[h], byte_pair(wa), byte_pair(wb), byte_pair(wa >> 8), byte_pair(wb >> 8), b0, b1);
+                    else
+                        mma_f16_16816(d[h], byte_pair(wa), byte_pair(wb), byte_pair(wa >> 8), byte_pair(wb >> 8), b0, b1);
                 }
             }
         }
+        const int odd = threadIdx.x >> 5 & 1;   // the warp's group is the high half of its scale word
+        float sc[4], bi[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            sc[r] = odd ? bf16hi(sw[r]) : bf16lo(sw[r]);
+            bi[r] = odd ? bf16hi(bw[r]) : bf16lo(bw[r]);
+        }
+        fold_group<ONE_ROW>(d, sc, bi, c.xs0 + xo, c.xs1 + xo, acc);
     }
 }
 

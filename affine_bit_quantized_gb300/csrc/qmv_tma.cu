@@ -77,8 +77,9 @@ __host__ __device__ inline Layout make_layout(int M, int K) {
 }
 constexpr int kMaxSmem = kSmemLimit;
 
-// ONE_ROW: M == 1 (every MMA column holds x row 0).  One CTA per SM.
-template <bool ONE_ROW>
+// BITS: code width (4 or 8).  ONE_ROW: M == 1 (every MMA column holds x row 0).
+// One CTA per SM.
+template <int BITS, bool ONE_ROW>
 __global__ void __launch_bounds__(kThreads, 1)
 qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
                const __grid_constant__ CUtensorMap tm_b, const __nv_bfloat16 *__restrict__ x,
@@ -104,9 +105,10 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int nblk = K / kWarpCodes;                        // warp column blocks in K
-    const int nbox = K / kBoxCodes;                         // code boxes in K
-    const int KB = (K + kStageCodes - 1) / kStageCodes;     // stages per tile
+    using Gm = Geo<BITS>;
+    const int nblk = K / Gm::kWarpCodes;                           // warp column blocks in K
+    const int nbox = K / Gm::kBoxCodes;                            // code boxes in K
+    const int KB = (K + Gm::kStageCodes - 1) / Gm::kStageCodes;    // stages per tile
     const int T = (N + kRows - 1) / kRows;
     const int my_tiles = (int)blockIdx.x < T ? (T - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int L_items = my_tiles * KB;
@@ -140,11 +142,11 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                 const uint32_t fb = bar_full + 8 * slot;
                 int nvalid = nbox - kb * kBoxes;
                 nvalid = nvalid < kBoxes ? nvalid : kBoxes;
-                mbar_expect_tx(fb, (uint32_t)(nvalid * kBoxBytes + 2 * kSBBytes));
+                mbar_expect_tx(fb, (uint32_t)(nvalid * kBoxBytes + 2 * kRows * Gm::kSBRowBytes));
                 for (int b = 0; b < nvalid; ++b)
                     tma_load_2d(dst + b * kBoxBytes, &tm_w, (kb * kBoxes + b) * 32, tile * kRows, fb, pol);
-                tma_load_2d(dst + kCodesBytes, &tm_s, kb * kStageGroups, tile * kRows, fb, pol);
-                tma_load_2d(dst + kCodesBytes + kSBBytes, &tm_b, kb * kStageGroups, tile * kRows, fb, pol);
+                tma_load_2d(dst + kCodesBytes, &tm_s, kb * Gm::kStageGroups, tile * kRows, fb, pol);
+                tma_load_2d(dst + kCodesBytes + kSBRegion, &tm_b, kb * Gm::kStageGroups, tile * kRows, fb, pol);
             };
             int issued = 0;
             bool ok = true;
@@ -213,10 +215,10 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
         if (!mbar_wait(bar_x, 0, deadline, abort_flag)) fail();
         // in place: raw bf16 rows -> fp16 fragments, group sums and scales (after a
         // timeout this only shuffles shared memory; the loop below then stops)
-        stage_x<false>(xs, nullptr, x_s, M, K, 0);
+        stage_x<false, BITS>(xs, nullptr, x_s, M, K, 0);
 
         ConsumerThread ct;
-        consumer_init(ct, warp, lane, xs, M, K);
+        consumer_init<BITS>(ct, warp, lane, xs, M, K);
 
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         bool ok = alive && !*abort_flag;
@@ -229,7 +231,7 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                     break;
                 }
                 if (kb * kConsumerWarps + warp < nblk)
-                    consume_stage<ONE_ROW>(s_base + (uint32_t)(slot * kStageBytes), kb, ct, acc);
+                    consume_stage<BITS, ONE_ROW>(s_base + (uint32_t)(slot * kStageBytes), kb, ct, acc);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
             }
@@ -270,12 +272,13 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint6
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sms[kMaxDevices];
-std::atomic<int> g_attr_done[2][kMaxDevices];
+std::atomic<int> g_attr_done[4][kMaxDevices];
 
 }  // namespace
 
 bool qmv_tma_supported(const MatmulArgs &a) {
-    return a.M >= 1 && a.M <= 8 && a.K % 512 == 0 && a.M * a.K * 2 <= kMaxXBytes && encode_fn() != nullptr &&
+    return (a.bits == 4 || a.bits == 8) && a.M >= 1 && a.M <= 8 && a.K % 512 == 0 && a.M * a.K * 2 <= kMaxXBytes &&
+           encode_fn() != nullptr &&
            (reinterpret_cast<uintptr_t>(a.scales) & 15) == 0 && (reinterpret_cast<uintptr_t>(a.biases) & 15) == 0;
 }
 
@@ -293,21 +296,28 @@ cudaError_t launch_qmv_tma(const MatmulArgs &a) {
     const int M = (int)a.M, N = (int)a.N, K = (int)a.K;
     const Layout L = make_layout(M, K);
     const int smem = L.total + 1024;
-    const bool one = (M == 1);
-    auto kern = one ? qmv_tma_kernel<true> : qmv_tma_kernel<false>;
-    if (!g_attr_done[one][dev].load(std::memory_order_acquire)) {
+    const bool one = (M == 1), eight = (a.bits == 8);
+    auto kern = eight ? (one ? qmv_tma_kernel<8, true> : qmv_tma_kernel<8, false>)
+                      : (one ? qmv_tma_kernel<4, true> : qmv_tma_kernel<4, false>);
+    const int ki = 2 * (int)eight + (int)one;
+    if (!g_attr_done[ki][dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
         if (e != cudaSuccess) return e;
-        g_attr_done[one][dev].store(1, std::memory_order_release);
+        g_attr_done[ki][dev].store(1, std::memory_order_release);
     }
     CUtensorMap tw, ts, tb;
     const int G = K / 64;
-    if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.w, (uint64_t)K / 8, (uint64_t)N, (uint64_t)K / 2, 32, kRows,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.scales, (uint64_t)G, (uint64_t)N, (uint64_t)G * 2,
-                   kStageGroups, kRows, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.biases, (uint64_t)G, (uint64_t)N, (uint64_t)G * 2,
-                   kStageGroups, kRows, CU_TENSOR_MAP_SWIZZLE_64B))
+    // codes: 32-word x 32-row boxes, 128-byte swizzle; scales and biases: one
+    // stage's groups x 32 rows (64 bytes and 64-byte swizzle for 4-bit codes,
+    // 32 bytes and 32-byte swizzle for 8-bit)
+    const uint32_t sg = (uint32_t)stage_groups(a.bits);
+    const CUtensorMapSwizzle sbs = eight ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.w, (uint64_t)K * a.bits / 32, (uint64_t)N,
+                   (uint64_t)K * a.bits / 8, 32, kRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.scales, (uint64_t)G, (uint64_t)N, (uint64_t)G * 2, sg, kRows,
+                   sbs) ||
+        !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.biases, (uint64_t)G, (uint64_t)N, (uint64_t)G * 2, sg, kRows,
+                   sbs))
         return cudaErrorInvalidValue;
     const int T = (N + kRows - 1) / kRows;
     cudaLaunchConfig_t cfg = {};

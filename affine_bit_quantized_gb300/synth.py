@@ -10,8 +10,9 @@ Recipe (one case = one weight matrix W[N,K] plus an activation x[M,K]):
   [0, 2^32).  For 4-bit codes this is exactly "every code uniform in [0, 15]"
   (eight independent nibbles per word); for 8-bit codes, every code uniform in
   [0, 255].
-* scales: bf16(U(0.004, 0.02)), one per group of ``group_size`` along K.
-* biases: bf16(-7.5 * scale + N(0, 0.002)), with ``scale`` the bf16 value, so
+* scales: bf16(U(0.004, 0.02) * 15 / (2^bits - 1)), one per group of ``group_size``
+  along K (the 4-bit range; 8-bit codes cover the same weight range in finer steps).
+* biases: bf16(-(2^bits - 1)/2 * scale + N(0, 0.002)), with ``scale`` the bf16 value, so
   that the dequantized weights are centred near zero.
 * x: bf16(N(0, 1)).
 
@@ -78,9 +79,10 @@ def make_weights(N: int, K: int, seed: int, group_size: int = 64, bits: int = 4)
     words = K * bits // 32
     w_packed = rng.integers(0, 1 << 32, size=(N, words), dtype=np.uint32)
     G = K // group_size
-    s = f32_to_bf16_bits(rng.uniform(0.004, 0.02, size=(N, G)))
+    top = (1 << bits) - 1          # 15 for 4-bit codes, 255 for 8-bit
+    s = f32_to_bf16_bits(rng.uniform(0.004, 0.02, size=(N, G)) * (15.0 / top))
     noise = rng.normal(0.0, 0.002, size=(N, G))
-    b = f32_to_bf16_bits(-7.5 * bf16_bits_to_f32(s).astype(np.float64) + noise)
+    b = f32_to_bf16_bits(-(top / 2.0) * bf16_bits_to_f32(s).astype(np.float64) + noise)
     return QuantWeights(w_packed, s, b, N, K, group_size, bits)
 
 

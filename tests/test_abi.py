@@ -36,7 +36,8 @@ def test_status_strings():
 
 @pytest.mark.parametrize("args,expect", [
     (dict(bits=3), aq.AQ_ERR_UNSUPPORTED),
-    (dict(bits=8), aq.AQ_ERR_UNSUPPORTED),
+    (dict(bits=8), aq.AQ_ERR_UNSUPPORTED),           # 8-bit codes need K % 512 == 0 (here K = 128)
+    (dict(bits=8, K=1024, s=A + 2), aq.AQ_ERR_ALIGNMENT),  # ... and 16-byte aligned scales
     (dict(group_size=32), aq.AQ_ERR_UNSUPPORTED),
     (dict(group_size=128), aq.AQ_ERR_UNSUPPORTED),
     (dict(K=96), aq.AQ_ERR_INVALID_ARG),
@@ -68,6 +69,8 @@ def test_validation_before_launch(args, expect):
 
 def test_ex_rejects_unknown_kernel_and_flags():
     assert aq.aq_matmul_bf16_ex(A, A, A, A, A, 1, 64, 128, 64, 4, 7, 0, None) == aq.AQ_ERR_INVALID_ARG
+    # no tensor-core kernel for 8-bit codes: an explicit request is refused before any launch
+    assert aq.aq_matmul_bf16_ex(A, A, A, A, A, 64, 64, 512, 64, 8, aq.AQ_KERNEL_QMM, 0, None) == aq.AQ_ERR_UNSUPPORTED
     assert aq.aq_matmul_bf16_ex(A, A, A, A, A, 1, 64, 128, 64, 4, 0, 1 << 5, None) == aq.AQ_ERR_INVALID_ARG
     assert aq.aq_matmul_bf16_ex(A, A, A, A, A, 0, 64, 128, 64, 4, 2, 1, None) == aq.AQ_OK
 
@@ -129,7 +132,7 @@ def test_chain_workspace_and_plan_checks():
     plan = aq.ChainPlan()
     assert aq.aq_chain_prepare(arr, 1, 64, 4, A, 100, plan) == aq.AQ_ERR_INVALID_ARG      # workspace too small
     assert aq.aq_chain_prepare(arr, 1, 64, 4, A + 64, 4096, plan) == aq.AQ_ERR_ALIGNMENT   # not 128-aligned
-    assert aq.aq_chain_prepare(arr, 1, 64, 8, A, 4096, plan) == aq.AQ_ERR_UNSUPPORTED
+    assert aq.aq_chain_prepare(arr, 1, 64, 2, A, 4096, plan) == aq.AQ_ERR_UNSUPPORTED
     assert aq.aq_chain_prepare(arr, 0, 64, 4, None, 0, plan) == aq.AQ_OK and plan.count == 0
     assert aq.aq_chain_run(plan, None) == aq.AQ_OK                                          # empty chain
 

@@ -20,9 +20,9 @@ def dev():
     return torch.device("cuda:0")
 
 
-def _mat(dev, M, N, K, seed):
+def _mat(dev, M, N, K, seed, bits=4):
     import torch
-    w = synth.make_weights(N, K, seed)
+    w = synth.make_weights(N, K, seed, bits=bits)
     x = synth.make_x(M, K, seed)
     xt, wt, st, bt = upload(x, w, dev)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
@@ -137,3 +137,23 @@ def test_chain_independent_matmuls_share_x(dev):
             xh = x_attn if src == "xa" else x_mlp
             _, ref = oracle.matmul(xh, w.w_packed, w.scales, w.biases, 1, N, Kin)
             assert_parity(from_dev_bf16(got[name]), ref, what=name)
+
+
+@pytest.mark.parametrize("shapes", [
+    [(1, 4096, 4096), (1, 1024, 4096), (1, 14336, 4096), (1, 4096, 14336)],
+    [(1, 17, 1024), (2, 300, 2048), (1, 33, 16384), (4, 50, 1536)],
+])
+def test_chain_eight_bit(dev, shapes):
+    """A chain of 8-bit matmuls: every output against the oracle, and the same
+    bits as single calls."""
+    import torch
+    mats = [_mat(dev, M, N, K, 500 + i, bits=8) for i, (M, N, K) in enumerate(shapes)]
+    chain = aq.Chain([m[2] for m in mats], bits=8)
+    chain.run()
+    torch.cuda.synchronize()
+    assert aq.aq_read_device_status(None) == aq.AQ_OK
+    for (x, w, t), (M, N, K) in zip(mats, shapes):
+        _, ref = oracle.matmul(x, w.w_packed, w.scales, w.biases, M, N, K, bits=8)
+        assert_parity(from_dev_bf16(t[4]), ref, what=f"chain 8-bit M={M} N={N} K={K}")
+        xt, wt, st, bt, y = t
+        assert torch.equal(y, aq.matmul(xt, wt, st, bt, bits=8))

@@ -220,6 +220,28 @@ def test_one_hot_x_returns_dequantized_column_and_endpoints():
             assert y_exact[0].tolist() == [float(v) for v in want15]
 
 
+def test_one_hot_x_eight_bit_endpoints():
+    """8-bit codes: a one-hot x returns q=0 -> bias, q=255 -> 255*scale + bias,
+    and a middle code exactly (byte order: lowest byte = lowest k)."""
+    N, K = 4, 128
+    w = synth.make_weights(N, K, 12, bits=8)
+    codes = oracle.unpack(w.w_packed, N, K, 8)
+    codes[:, 5] = 0
+    codes[:, 66] = 255
+    codes[:, 99] = 128
+    wp = oracle.pack(codes, 8)
+    assert (int(wp[0, 66 // 4]) >> (8 * (66 % 4))) & 0xFF == 255       # byte 2 of word 16
+    for k, q in ((5, 0), (66, 255), (99, 128)):
+        x = np.zeros((1, K), np.uint16)
+        x[0, k] = 0x3F80
+        y_exact, y_bf16 = oracle.matmul(x, wp, w.scales, w.biases, 1, N, K, bits=8)
+        g = k // 64
+        for n in range(N):
+            want = bf16_bits_to_fraction(w.scales[n, g]) * q + bf16_bits_to_fraction(w.biases[n, g])
+            assert Fraction(y_exact[0, n]) == want
+            assert y_bf16[0, n] == fraction_to_bf16_bits(want)
+
+
 def test_zero_x_gives_zero():
     x = np.zeros((3, 192), np.uint16)
     w = synth.make_weights(9, 192, 12)

@@ -22,17 +22,17 @@ def dev():
 def run(dev, x, w, kernel="qmv", pdl=False):
     import torch
     xt, wt, st, bt = upload(x, w, dev)
-    y = aq.matmul(xt, wt, st, bt, kernel=kernel, pdl=pdl)
+    y = aq.matmul(xt, wt, st, bt, kernel=kernel, pdl=pdl, bits=w.bits)
     torch.cuda.synchronize()
     return from_dev_bf16(y)
 
 
-def check(dev, M, N, K, seed, kernel="qmv", pdl=False):
-    w = synth.make_weights(N, K, seed)
+def check(dev, M, N, K, seed, kernel="qmv", pdl=False, bits=4):
+    w = synth.make_weights(N, K, seed, bits=bits)
     x = synth.make_x(M, K, seed)
     got = run(dev, x, w, kernel, pdl)
-    _, ref = oracle.matmul(x, w.w_packed, w.scales, w.biases, M, N, K)
-    return assert_parity(got, ref, what=f"M={M} N={N} K={K}")
+    _, ref = oracle.matmul(x, w.w_packed, w.scales, w.biases, M, N, K, bits=bits)
+    return assert_parity(got, ref, what=f"M={M} N={N} K={K} bits={bits}")
 
 
 def test_tiny_correctness_config(dev):
@@ -185,3 +185,50 @@ def test_bounded_wait_timeout_reports_status(dev):
     with pytest.raises(aq.AqError):
         aq.matmul(xt[:, :64].contiguous(), wt[:, :8].contiguous(), st[:, :1].contiguous(), bt[:, :1].contiguous(),
                   flags=aq.AQ_FLAG_DEBUG_SKIP_X)                # K = 64: no TMA kernel, hook unsupported
+
+
+# ---------------------------------------------------------------- 8-bit codes (TMA-fed kernel)
+
+@pytest.mark.parametrize("M,N,K", [
+    (1, 1, 512), (1, 33, 1024), (1, 100, 4096), (1, 4096, 4096), (1, 14336, 4096), (1, 4096, 14336),
+    (1, 64, 16384), (2, 300, 2048), (3, 31, 3072), (8, 77, 2048), (5, 129, 1024), (7, 40, 1536),
+    (16, 64, 1024), (4, 50, 8704), (20, 96, 512),   # rows beyond one staged pass: several launches
+])
+def test_eight_bit_shapes(dev, M, N, K):
+    check(dev, M, N, K, 300 + M + N + K, bits=8)
+
+
+def test_eight_bit_special_inputs(dev):
+    """8-bit: zero x gives exact zeros, a one-hot x on a q = 0 column gives the
+    bias, q = 255 gives 255*scale + bias, NaN propagates to its row."""
+    N, K = 40, 1024
+    w = synth.make_weights(N, K, 19, bits=8)
+    codes = oracle.unpack(w.w_packed, N, K, 8)
+    codes[:, 5] = 0
+    codes[:, 700] = 255
+    w.w_packed = oracle.pack(codes, 8)
+    x = np.zeros((4, K), np.uint16)
+    x[1, 5] = 0x3F80
+    x[2, 700] = 0x3F80
+    x[3, 7] = 0x7FC0  # NaN
+    got = run(dev, x, w)
+    _, ref = oracle.matmul(x, w.w_packed, w.scales, w.biases, 4, N, K, bits=8)
+    assert not got[0].any()
+    assert np.array_equal(got[1], w.biases[:, 0])
+    assert np.array_equal(got[2], ref[2])
+    assert np.all((got[3] & 0x7F80) == 0x7F80) and np.all(got[3] & 0x007F)
+
+
+def test_eight_bit_rejected_where_unsupported(dev):
+    import torch
+    w = synth.make_weights(8, 576, 1, bits=8)
+    x = synth.make_x(1, 576, 1)
+    xt, wt, st, bt = upload(x, w, dev)
+    with pytest.raises(aq.AqError):
+        aq.matmul(xt, wt, st, bt, bits=8)            # K % 512 != 0: no 8-bit kernel
+    w = synth.make_weights(8, 512, 1, bits=8)
+    x = synth.make_x(32, 512, 1)
+    xt, wt, st, bt = upload(x, w, dev)
+    with pytest.raises(aq.AqError):
+        aq.matmul(xt, wt, st, bt, bits=8, kernel="qmm")   # no tensor-core kernel for 8-bit
+    torch.cuda.synchronize()
