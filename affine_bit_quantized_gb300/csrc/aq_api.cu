@@ -67,9 +67,8 @@ aq_status validate(const void *x, const uint32_t *w, const void *s, const void *
     if (!aligned(x, 16) || !aligned(w, 16) || !aligned(s, 2) || !aligned(b, 2) || !aligned(y, 2))
         return AQ_ERR_ALIGNMENT;
     if (bits == 8) {
-        // 8-bit codes run on the TMA-fed decode kernel only (one row of x per
-        // pass at the largest K)
-        if (K % 512 || K > 16384) return AQ_ERR_UNSUPPORTED;
+        // 8-bit codes run on the TMA-fed decode kernel only
+        if (K % 512) return AQ_ERR_UNSUPPORTED;
         if (!aligned(s, 16) || !aligned(b, 16)) return AQ_ERR_ALIGNMENT;
     }
     return AQ_OK;
@@ -107,19 +106,26 @@ aq_status aq_matmul_bf16_ex(const void *x, const uint32_t *w_packed, const void 
     a.y = y;
     a.M = M;
     a.bits = bits;
-    if (bits == 8) {
-        // 8-bit codes run on the TMA-fed decode kernel only, in passes of as many
-        // rows of x as it stages at once (no tensor-core path for them yet)
-        const int64_t rows = K <= 2048 ? 8 : (K >= 16384 ? 1 : 16384 / K);
+    // TMA-fed decode kernel over launches of at most `rows` rows of x (W is
+    // streamed once per launch); false when it cannot take this matrix
+    auto tma_rows = [&](int64_t rows, aq_status *out) -> bool {
+        a.M = rows < M ? rows : M;
+        if (!aq::qmv_tma_supported(a)) return false;   // depends on M only through M <= 8
+        if (a.debug_skip_x && (M > rows || aq::qmv_tma_passes(a) != 1)) return false;   // hook: x in one piece
         for (int64_t m0 = 0; m0 < M; m0 += rows) {
             a.x = static_cast<const uint16_t *>(x) + m0 * K;
             a.y = static_cast<uint16_t *>(y) + m0 * N;
             a.M = (M - m0) < rows ? (M - m0) : rows;
-            if (!aq::qmv_tma_supported(a)) return AQ_ERR_UNSUPPORTED;
-            st = record_cuda(aq::launch_qmv_tma(a));
-            if (st != AQ_OK) return st;
+            *out = record_cuda(aq::launch_qmv_tma(a));
+            if (*out != AQ_OK) break;
         }
-        return AQ_OK;
+        return true;
+    };
+    if (bits == 8) {
+        // 8-bit codes run on the TMA-fed decode kernel only (no tensor-core path
+        // for them yet), in launches of 8 rows of x
+        st = AQ_OK;
+        return tma_rows(8, &st) ? st : AQ_ERR_UNSUPPORTED;
     }
     if (kernel == AQ_KERNEL_QMM || (kernel == AQ_KERNEL_AUTO && M > kQmvMaxRows)) {
         if (a.debug_skip_x) return AQ_ERR_UNSUPPORTED;
@@ -127,10 +133,13 @@ aq_status aq_matmul_bf16_ex(const void *x, const uint32_t *w_packed, const void 
         if (kernel == AQ_KERNEL_QMM) return AQ_ERR_UNSUPPORTED;
     }
     if (M <= 8 && kernel != AQ_KERNEL_QMM) {
-        a.x = x;
-        a.y = y;
         a.M = M;
-        if (aq::qmv_tma_supported(a)) return record_cuda(aq::launch_qmv_tma(a));
+        // an explicit AQ_KERNEL_QMV takes the TMA-fed kernel wherever it applies
+        if (aq::qmv_tma_supported(a) &&
+            (kernel == AQ_KERNEL_QMV || a.debug_skip_x || aq::qmv_tma_preferred(a))) {
+            st = AQ_OK;
+            if (tma_rows(M, &st)) return st;
+        }
     }
     if (a.debug_skip_x) return AQ_ERR_UNSUPPORTED;  // the hook exists only in the TMA kernel
     // Weight-streaming passes over at most 16 rows of x each.

@@ -36,6 +36,8 @@ cudaError_t launch_qmv(const MatmulArgs &a);
 // TMA-fed weight-streaming kernel (qmv_tma.cu) for 1 <= M <= 8,
 // K % 512 == 0, M*K <= 16384 and 16-byte aligned scales/biases.
 bool qmv_tma_supported(const MatmulArgs &a);
+int qmv_tma_passes(const MatmulArgs &a);   // K passes the TMA kernel makes (x staged per pass)
+bool qmv_tma_preferred(const MatmulArgs &a);   // faster than the general kernel for this 4-bit shape
 cudaError_t launch_qmv_tma(const MatmulArgs &a);
 
 // Tensor-core kernel (qmm.cu) for any M >= 1 with K % 512 == 0 and 16-byte

@@ -74,13 +74,14 @@ struct ChainLayout {
     int stages;  // ring depth (kMaxStages)
     int x_off, xsum_off, xinfo_off, red_off, info_off, bar_off, total;
 };
-// x_bytes: the largest M*K*2 of the chain; max_m: its largest M
+// x_bytes: the largest M*K*2 of the chain; max_m: its largest M.  The staged
+// rows of x and of (Xs, X') each carry up to 16 bytes of pad (kXPadBytes).
 __host__ __device__ inline ChainLayout chain_layout(int x_bytes, int max_m) {
     ChainLayout L;
     L.stages = kMaxStages;   // fits beside the largest rest (M*K*2 = 32 KB, M = 8)
     L.x_off = L.stages * kStageBytes;
-    L.xsum_off = L.x_off + x_bytes;
-    L.xinfo_off = L.xsum_off + ((x_bytes / 16 + 15) & ~15);  // float2 per (row, group): M*K/8 bytes
+    L.xsum_off = L.x_off + x_bytes + kXPadBytes;
+    L.xinfo_off = L.xsum_off + ((x_bytes / 16 + kXPadBytes + 15) & ~15);  // float2 per (row, group): M*K/8 bytes
     L.red_off = L.xinfo_off + kXInfoBytes;
     L.info_off = L.red_off + red_bytes(max_m);
     L.bar_off = L.info_off + kInfoCap * 48;
@@ -310,10 +311,10 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
                 const int nblk = K / Gm::kWarpCodes;
                 const int KB = (K + Gm::kStageCodes - 1) / Gm::kStageCodes;
                 // ---- x of this matmul: L2 loads, fp16 fragments, group sums and scales
-                if (new_x) stage_x<true, BITS>(xs, cur.x, 0, M, K, nstaged++);
+                if (new_x) stage_x<true, BITS, false>(xs, cur.x, 0, M, K, nstaged++, K);
 
                 ConsumerThread ct;
-                consumer_init<BITS>(ct, warp, lane, xs, M, K);
+                consumer_init<BITS, ONE_ROW>(ct, warp, lane, xs, M, K);
 
                 const int first = (cta - cur.tile_base % ncta + ncta) % ncta;
                 for (int tile = first; tile < T && ok; tile += ncta) {

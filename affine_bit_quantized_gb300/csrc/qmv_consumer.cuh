@@ -65,6 +65,14 @@ __host__ __device__ constexpr int stage_groups(int bits) { return stage_codes(bi
 constexpr int kMaxM = 8;                                   // rows of x these kernels take
 constexpr int kMaxXBytes = 32768;                          // M*K*2 limit for staging x once per CTA
 constexpr int kXInfoBytes = 96;                            // int row_max[2][8], float inv_scale[8]
+// Row strides of the staged x.  A row is 2K bytes of fragments and K/8 bytes of
+// (Xs, X'), both multiples of 128 bytes: with several rows, the eight row
+// addresses of an ldmatrix (rows 0..7 of x) and the four (Xs, X') rows a warp
+// reads at once would share banks.  One 16-byte pad per row shifts row m by m
+// 16-byte bank groups.  One row needs no pad.
+__host__ __device__ constexpr int x_row_bytes(int M, int K) { return M == 1 ? 2 * K : 2 * K + 16; }
+__host__ __device__ constexpr int xsum_row_bytes(int M, int K) { return M == 1 ? K / 8 : K / 8 + 16; }
+constexpr int kXPadBytes = kMaxM * 16;                     // the pads of x rows (and of (Xs, X') rows)
 
 // named barrier 1: the consumer warps only (the producer warp runs on)
 __device__ __forceinline__ void consumer_sync() {
@@ -72,12 +80,12 @@ __device__ __forceinline__ void consumer_sync() {
 }
 
 // Shared-memory addresses of the staged x of the current matmul.
-//   xq    : fp16 MMA fragments of x', M rows of 2K bytes.  For row m, group g
+//   xq    : fp16 MMA fragments of x', M rows x_row_bytes(M, K) apart.  For row m, group g
 //           and word half i (words 2t+i of the group, t = 0..3) a 64-byte
 //           "quad" at (2g + i) * 64 holds four 16-byte rows (fragment
 //           register p = 0..3), each the registers of threads t = 0..3, so one
 //           ldmatrix.x4 per quad serves all 32 lanes;
-//   xsum  : float2 [M][K/64] = (Xs, X');
+//   xsum  : float2 (Xs, X') per row and group, rows xsum_row_bytes(M, K) apart;
 //   xinfo : int row_max[2][8] (|x| bits, for the scale), float inv_scale[8] = 2^-e.
 struct XStage {
     uint32_t xq, xsum, xinfo;
@@ -114,18 +122,23 @@ __device__ __forceinline__ uint4 ldg_cg_v4(const void *p) {
     return v;
 }
 
-// Stages x [M][K] (bf16, from global memory through L2, or from a raw copy
-// already in shared memory at `raw`, which may alias xs.xq) for the consumers:
+// Stages x [M][K] (bf16, from global memory through L2 with rows ldx elements
+// apart, or from a raw copy already in shared memory at `raw`, rows
+// x_row_bytes(M, K) apart, which may alias xs.xq) for the consumers:
 // fragments, group sums and scales.  Called by all consumer threads, which
 // meet at a barrier before the first shared-memory write (so the previous x
 // may still be in use on entry).  `n` counts the stagings of this CTA: staging
 // n takes its row maxima in buffer n % 2, which is zero on entry and is
-// cleared again for staging n + 2.  M*K <= 16384, K % 512 == 0.
-template <bool FROM_GLOBAL, int BITS>
-__device__ __forceinline__ void stage_x(const XStage &xs, const __nv_bfloat16 *xg, uint32_t raw, int M, int K, int n) {
+// cleared again for staging n + 2.  M*K <= 16384, K % 512 == 0.  ONE_ROW:
+// M == 1, known at compile time (no row arithmetic).
+template <bool FROM_GLOBAL, int BITS, bool ONE_ROW>
+__device__ __forceinline__ void stage_x(const XStage &xs, const __nv_bfloat16 *xg, uint32_t raw, int M_, int K, int n,
+                                        int ldx) {
+    const int M = ONE_ROW ? 1 : M_;
     const int tid = threadIdx.x;
     const int words = M * K / 8;
     const int wpr = K / 8;  // words per row (a multiple of 64: a warp's 32 words share a row)
+    const int xrb = x_row_bytes(M, K), xsrb = xsum_row_bytes(M, K);
     int *row_max = reinterpret_cast<int *>(__cvta_shared_to_generic(xs.xinfo)) + (n & 1) * kMaxM;
     float *inv_scale = reinterpret_cast<float *>(__cvta_shared_to_generic(xs.xinfo + 64));
     uint4 v[kMaxXBytes / 16 / kConsumerThreads];  // 4 words per thread at most
@@ -135,14 +148,16 @@ __device__ __forceinline__ void stage_x(const XStage &xs, const __nv_bfloat16 *x
         const int wi = u * kConsumerThreads + tid;
         int mx = 0;
         if (wi < words) {
-            v[u] = FROM_GLOBAL ? ldg_cg_v4(xg + (size_t)wi * 8) : lds128(raw + (uint32_t)wi * 16);
+            const int m = ONE_ROW ? 0 : wi / wpr, wr = wi - m * wpr;
+            v[u] = FROM_GLOBAL ? ldg_cg_v4(xg + (size_t)m * ldx + (size_t)wr * 8)
+                               : lds128(raw + (uint32_t)(m * xrb + wr * 16));
             mx = bf16x2_abs_max(v[u].x);
             mx = max(mx, bf16x2_abs_max(v[u].y));
             mx = max(mx, bf16x2_abs_max(v[u].z));
             mx = max(mx, bf16x2_abs_max(v[u].w));
         }
         mx = __reduce_max_sync(0xFFFFFFFFu, mx);
-        if ((tid & 31) == 0 && wi < words) atomicMax(row_max + wi / wpr, mx);
+        if ((tid & 31) == 0 && wi < words) atomicMax(row_max + (ONE_ROW ? 0 : wi / wpr), mx);
     }
     consumer_sync();
 #pragma unroll
@@ -150,8 +165,8 @@ __device__ __forceinline__ void stage_x(const XStage &xs, const __nv_bfloat16 *x
         if (u * kConsumerThreads >= words) break;  // uniform over the CTA
         const int wi = u * kConsumerThreads + tid;
         float s_part = 0.f, p_part = 0.f;
+        const int m = ONE_ROW ? 0 : wi / wpr, wr = wi - m * wpr;
         if (wi < words) {
-            const int m = wi / wpr, wr = wi - m * wpr;
             const float sc = pow2f(x_scale_exponent(row_max[m]));
             const float sc16 = sc * 0.0625f;   // 4-bit: codes at bits 4-7 of a byte weigh 16x
             const uint4 a = v[u];
@@ -174,7 +189,7 @@ __device__ __forceinline__ void stage_x(const XStage &xs, const __nv_bfloat16 *x
             s_part = ((x0 + x1) + (x2 + x3)) + ((x4 + x5) + (x6 + x7));
             p_part = (f16x2_sum(p0) + f16x2_sum(p1)) + (f16x2_sum(p2) + f16x2_sum(p3));
             const int g = wr >> 3, w8 = wr & 7;
-            const uint32_t q = xs.xq + (uint32_t)(m * 2 * K + (2 * g + (w8 & 1)) * 64 + (w8 >> 1) * 4);
+            const uint32_t q = xs.xq + (uint32_t)(m * xrb + (2 * g + (w8 & 1)) * 64 + (w8 >> 1) * 4);
             sts32(q, p0);
             sts32(q + 16, p1);
             sts32(q + 32, p2);
@@ -187,7 +202,7 @@ __device__ __forceinline__ void stage_x(const XStage &xs, const __nv_bfloat16 *x
         p_part += __shfl_xor_sync(0xFFFFFFFFu, p_part, 2);
         s_part += __shfl_xor_sync(0xFFFFFFFFu, s_part, 4);
         p_part += __shfl_xor_sync(0xFFFFFFFFu, p_part, 4);
-        if (wi < words && (wi & 7) == 0) sts64(xs.xsum + (uint32_t)(wi >> 3) * 8, s_part, p_part);
+        if (wi < words && (wi & 7) == 0) sts64(xs.xsum + (uint32_t)(m * xsrb + (wr >> 3) * 8), s_part, p_part);
     }
     if (tid < M) inv_scale[tid] = pow2f(-x_scale_exponent(row_max[tid]));
     consumer_sync();
@@ -202,8 +217,9 @@ struct ConsumerThread {
     uint32_t xs0, xs1;  // (Xs, X') of this warp's first group in stage 0, x rows of columns 2j and 2j+1
 };
 
-template <int BITS>
-__device__ __forceinline__ void consumer_init(ConsumerThread &c, int warp, int lane, const XStage &xs, int M, int K) {
+template <int BITS, bool ONE_ROW>
+__device__ __forceinline__ void consumer_init(ConsumerThread &c, int warp, int lane, const XStage &xs, int M_, int K) {
+    const int M = ONE_ROW ? 1 : M_;
     using Gm = Geo<BITS>;
     const int gid = lane >> 2, j = lane & 3;
     // code boxes use the 128-byte swizzle: 16-byte chunk c of box row r sits at chunk c ^ (r % 8)
@@ -224,11 +240,11 @@ __device__ __forceinline__ void consumer_init(ConsumerThread &c, int warp, int l
         c.sb = (uint32_t)(gid * 32 + ((((warp >> 3) ^ (gid >> 2)) & 1) << 4) + (((warp >> 1) & 3) << 2));
     }
     const int xr = (lane & 7) < M ? (lane & 7) : M - 1;
-    c.xq = xs.xq + (uint32_t)(xr * 2 * K + (lane >> 3) * 16 + warp * Gm::kGroupsPerWarp * 128);
-    const int G = K / 64;
+    c.xq = xs.xq + (uint32_t)(xr * x_row_bytes(M, K) + (lane >> 3) * 16 + warp * Gm::kGroupsPerWarp * 128);
+    const int xsrb = xsum_row_bytes(M, K);
     const int m0 = 2 * j < M ? 2 * j : M - 1, m1 = 2 * j + 1 < M ? 2 * j + 1 : M - 1;
-    c.xs0 = xs.xsum + (uint32_t)((m0 * G + Gm::kGroupsPerWarp * warp) * 8);
-    c.xs1 = xs.xsum + (uint32_t)((m1 * G + Gm::kGroupsPerWarp * warp) * 8);
+    c.xs0 = xs.xsum + (uint32_t)(m0 * xsrb + Gm::kGroupsPerWarp * warp * 8);
+    c.xs1 = xs.xsum + (uint32_t)(m1 * xsrb + Gm::kGroupsPerWarp * warp * 8);
 }
 
 // acc += scale * (D - 1024 X') + bias * Xs for one group: D = d[h] (the MMA
@@ -420,10 +436,15 @@ __device__ __forceinline__ bool deposit_tile(const TileCtx &t, float (&acc)[2][4
 // Reducer warp, for the tcount-th tile of this CTA (tile index `tile` of a
 // matrix with N rows): adds the (already unscaled) partials in warp order and
 // stores y rows tile*kRows .. (bf16, round to nearest even).
+//
+// When K is walked in several passes (pass `pass` of `passes`), the tile's
+// sums of the passes before the last are kept in yacc (float [kRows][M]):
+// assigned by the first pass, added to by the next ones, in pass order.
 template <bool ONE_ROW>
 __device__ __forceinline__ bool reduce_tile(const TileCtx &t, int tcount, int tile, int M, int N,
                                             __nv_bfloat16 *y, int lane, uint64_t timeout_ns,
-                                            const volatile int *abort_flag) {
+                                            const volatile int *abort_flag, float *yacc = nullptr, int pass = 0,
+                                            int passes = 1) {
     constexpr int B = red_bufs<ONE_ROW>();
     const int b = tcount % B;
     const int n_out = kRows * M;
@@ -432,12 +453,14 @@ __device__ __forceinline__ bool reduce_tile(const TileCtx &t, int tcount, int ti
     for (int idx = lane; idx < n_out; idx += 32) {
         const int row = idx / M, m = idx - row * M;
         const int n = tile * kRows + row;
-        if (n < N) {
-            float v = rb[idx];
+        float v = rb[idx];
 #pragma unroll
-            for (int w = 1; w < kConsumerWarps; ++w) v += rb[w * n_out + idx];
+        for (int w = 1; w < kConsumerWarps; ++w) v += rb[w * n_out + idx];
+        if (pass > 0) v = yacc[idx] + v;
+        if (pass + 1 < passes)
+            yacc[idx] = v;
+        else if (n < N)
             y[(int64_t)m * N + n] = __float2bfloat16_rn(v);
-        }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(t.red_empty + 8 * b);

@@ -47,10 +47,10 @@ QMM_SHAPES = ((4096, 14336, "gate/up"), (14336, 4096, "down"))   # (K, N)
 QMM_M = (256, 2048)
 
 
-def alg_bytes(M: int, N: int, K: int) -> int:
-    """Bytes the definition must move: codes (K/2 per row), scales and biases
-    (2 x 2 bytes per group of 64), x and y."""
-    return N * K // 2 + N * (K // 64) * 4 + 2 * M * K + 2 * M * N
+def alg_bytes(M: int, N: int, K: int, bits: int = 4) -> int:
+    """Bytes the definition must move: codes (K*bits/8 per row), scales and
+    biases (2 x 2 bytes per group of 64), x and y."""
+    return N * K * bits // 8 + N * (K // 64) * 4 + 2 * M * K + 2 * M * N
 
 
 def load_peaks():
@@ -492,6 +492,61 @@ def main():
         per_matrix[name] = {"N": N, "K": K, "us_per_call": round(us, 3),
                             "gbs": round(alg_bytes(1, N, K) / (us * 1e-6) / 1e9, 1)}
 
+    def time_calls(launch, n_calls, reps=5):
+        for i in range(2 * n_calls):
+            launch(i)
+        torch.cuda.synchronize(dev)
+        e0.record(cur)
+        for i in range(reps * n_calls):
+            launch(i)
+        e1.record(cur)
+        e1.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / (reps * n_calls)
+
+    # ---- small batches (the multi-row decode path): M in {2, 4, 8, 16} over the layer shapes
+    # and lm_head, on the step's copies (32 distinct weights per layer shape: no L2 reuse; the
+    # one lm_head, 296 MB, is larger than L2)
+    small_batch = {}
+    for M in (2, 4, 8, 16):
+        for j, (name, N, K) in enumerate(synth.LLAMA8B_LAYER + (synth.LLAMA8B_LM_HEAD,)):
+            lm = name == "lm_head"
+            xb = torch.from_numpy(synth.make_x(M, K, synth.seed_for(3, M, j)).view(np.int16)).to(dev)
+            yb = torch.empty((M, N), dtype=torch.int16, device=dev)
+            ws = [weights[(args.layers, 0)]] if lm else [weights[(layer, j)] for layer in range(args.layers)]
+
+            def launch_sb(i, ws=ws, xb=xb, yb=yb, M=M, N=N, K=K):
+                wt, st_, bt = ws[i % len(ws)]
+                rc = lib.aq_matmul_bf16_ex(xb.data_ptr(), wt.data_ptr(), st_.data_ptr(), bt.data_ptr(), yb.data_ptr(),
+                                           M, N, K, 64, 4, aq.AQ_KERNEL_AUTO, aq.AQ_FLAG_PDL, cur.cuda_stream)
+                if rc != aq.AQ_OK:
+                    raise aq.AqError(rc, "aq_matmul_bf16_ex")
+
+            us = time_calls(launch_sb, 4 if lm else len(ws))
+            small_batch[f"M{M}_{name}"] = {"M": M, "N": N, "K": K, "us_per_call": round(us, 3),
+                                           "gbs": round(alg_bytes(M, N, K) / (us * 1e-6) / 1e9, 1)}
+
+    # ---- 8-bit codes (same shapes, M = 1): 4 device copies of each weight matrix cycled
+    eight_bit = {}
+    for j, (name, N, K) in enumerate(synth.LLAMA8B_LAYER + (synth.LLAMA8B_LM_HEAD,)):
+        w8 = synth.make_weights(N, K, synth.seed_for(6, 0, j), bits=8)
+        base = (torch.from_numpy(w8.w_packed.view(np.int32)).to(dev), torch.from_numpy(w8.scales.view(np.int16)).to(dev),
+                torch.from_numpy(w8.biases.view(np.int16)).to(dev))
+        ws8 = [base] + [tuple(t.clone() for t in base) for _ in range(3)]
+        x8 = torch.from_numpy(synth.make_x(1, K, synth.seed_for(6, 1, j)).view(np.int16)).to(dev)
+        y8 = torch.empty((1, N), dtype=torch.int16, device=dev)
+
+        def launch8(i, ws8=ws8, x8=x8, y8=y8, N=N, K=K):
+            wt, st_, bt = ws8[i % len(ws8)]
+            rc = lib.aq_matmul_bf16_ex(x8.data_ptr(), wt.data_ptr(), st_.data_ptr(), bt.data_ptr(), y8.data_ptr(),
+                                       1, N, K, 64, 8, aq.AQ_KERNEL_AUTO, aq.AQ_FLAG_PDL, cur.cuda_stream)
+            if rc != aq.AQ_OK:
+                raise aq.AqError(rc, "aq_matmul_bf16_ex")
+
+        us = time_calls(launch8, 8)
+        eight_bit[name] = {"N": N, "K": K, "us_per_call": round(us, 3),
+                           "gbs": round(alg_bytes(1, N, K, 8) / (us * 1e-6) / 1e9, 1)}
+        del ws8, base
+
     # ---- prefill-sized tensor-core GEMM (qmm): M in {256, 2048}, (K, N) in {(4096, 14336), (14336, 4096)}
     qmm = {}
     for (K, N, label) in QMM_SHAPES:
@@ -588,6 +643,8 @@ def main():
                 "value": round(world * step_bytes / (ms_alt * 1e-3) / 1e9, 1)},
         "clocks": clk,
         "per_matrix": per_matrix,
+        "small_batch": small_batch,
+        "eight_bit": eight_bit,
         "qmm": qmm,
     }
     if cpu:

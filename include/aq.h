@@ -59,7 +59,11 @@ typedef enum aq_status {
  * aq_matmul_bf16 does. */
 typedef enum aq_kernel {
     AQ_KERNEL_AUTO = 0,
-    AQ_KERNEL_QMV = 1, /* weight-streaming decode kernel; any M (runs 16 rows of x per pass) */
+    AQ_KERNEL_QMV = 1, /* weight-streaming decode kernels; any M: the TMA-fed kernel wherever
+                          it applies (M <= 8, K % 512 == 0, 16-byte aligned scales and biases),
+                          else the general one in launches of 16 rows of x.  AQ_KERNEL_AUTO
+                          chooses between the two (and the GEMM kernel above 16 rows) by
+                          measured speed. */
     AQ_KERNEL_QMM = 2  /* tensor-core GEMM kernel (tcgen05); any M >= 1 */
 } aq_kernel;
 
@@ -75,8 +79,10 @@ enum {
      * weight-streaming kernel's producer omits the copy of x, so its
      * consumers' wait expires (after 20 ms instead of the normal 2 s), the
      * kernel records a timeout in the device status word and returns without
-     * writing y.  Only for 1 <= M <= 8 with K a multiple of 512 (otherwise
-     * AQ_ERR_UNSUPPORTED).  Read the outcome with aq_read_device_status(). */
+     * writing y.  Only where that kernel stages x in one piece: 1 <= M <= 8,
+     * K a multiple of 512, and x within 32 KB rounded up to whole 2048-code
+     * stages (4-bit) or 1024-code stages (8-bit); otherwise AQ_ERR_UNSUPPORTED.
+     * Read the outcome with aq_read_device_status(). */
     AQ_FLAG_DEBUG_SKIP_X = 1u << 31
 };
 
@@ -86,7 +92,11 @@ enum {
  *   M, N, K     M >= 0, N >= 0, K >= 0; K a multiple of group_size.  M == 0 or
  *               N == 0 launches nothing and returns AQ_OK; K == 0 writes y = 0.
  *   group_size  64.  Other values return AQ_ERR_UNSUPPORTED.
- *   bits        4.  Other values return AQ_ERR_UNSUPPORTED.
+ *   bits        4 or 8.  Other values return AQ_ERR_UNSUPPORTED.  8-bit codes
+ *               run on the weight-streaming kernel only: they need K a multiple
+ *               of 512 and 16-byte aligned scales and biases
+ *               (AQ_ERR_UNSUPPORTED / AQ_ERR_ALIGNMENT otherwise), and
+ *               kernel AQ_KERNEL_QMM returns AQ_ERR_UNSUPPORTED.
  *   Alignment   x and w_packed 16-byte aligned; scales, biases and y 2-byte
  *               aligned; otherwise AQ_ERR_ALIGNMENT.
  *   Aliasing    y must not overlap any input.

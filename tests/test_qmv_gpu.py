@@ -77,6 +77,43 @@ def test_ragged_shapes(dev, M, N, K):
     check(dev, M, N, K, 100 + M + N + K)
 
 
+@pytest.mark.parametrize("M,N,K,bits", [
+    (2, 300, 16384, 4),    # x of 64 KB: two passes of 8192 codes
+    (8, 77, 4096, 4),      # one 2048-code stage per pass
+    (3, 1000, 14336, 4),   # four passes, the last of one stage
+    (1, 100, 28672, 4),    # one row beyond 16384 codes: 8 stages, then 6
+    (5, 4100, 6144, 4),    # three passes over 129 tiles
+    (7, 33, 2560, 4),      # second pass of 512 codes (a partial stage)
+    (4, 64, 33280, 4),     # nine passes, the last of 512 codes
+    (8, 200, 4096, 8),
+    (1, 64, 32768, 8),
+    (3, 50, 7680, 8),      # second pass of 2560 codes
+])
+@pytest.mark.parametrize("kernel", ["qmv", "auto"])
+def test_tma_kernel_k_passes(dev, M, N, K, bits, kernel):
+    """x larger than one staging (M*K*2 > 32 KB): the TMA-fed kernel walks K
+    in passes and keeps each tile's sums in shared memory across them ("qmv"
+    forces it; "auto" may pick the general kernel for these shapes)."""
+    check(dev, M, N, K, 600 + M + N + K, kernel=kernel, bits=bits)
+
+
+def test_tma_kernel_tile_batches_sampled(dev):
+    """8 rows of x over the 128256 x 4096 lm_head matrix with 8-bit codes: two
+    K passes, and more tiles per CTA than the shared-memory tile sums hold, so
+    the tiles go in batches.  Sampled outputs against the oracle."""
+    _, N, K = synth.LLAMA8B_LM_HEAD
+    M = 8
+    w = synth.make_weights(N, K, 777, bits=8)
+    x = synth.make_x(M, K, 777)
+    got = run(dev, x, w)
+    rng = np.random.default_rng(7)
+    im = rng.integers(0, M, 4000)
+    inn = np.concatenate([rng.integers(0, N, 3990), np.arange(N - 10, N)])
+    ye, yb = oracle.matmul_sampled(x, w.w_packed, w.scales, w.biases, M, N, K, im, inn, bits=8)
+    rms = float(np.sqrt(np.mean(ye * ye)))
+    assert_parity(got[im, inn], yb, rms=rms, what="lm_head 8-bit M=8 sampled")
+
+
 def test_pdl_flag_same_bits(dev):
     M, N, K = 4, 300, 1024
     w = synth.make_weights(N, K, 5)
