@@ -67,7 +67,7 @@ aq_status validate(const void *x, const uint32_t *w, const void *s, const void *
     if (!aligned(x, 16) || !aligned(w, 16) || !aligned(s, 2) || !aligned(b, 2) || !aligned(y, 2))
         return AQ_ERR_ALIGNMENT;
     if (bits == 8) {
-        // 8-bit codes run on the TMA-fed decode kernel only
+        // 8-bit codes run on the TMA-fed kernels only (decode and tensor-core)
         if (K % 512) return AQ_ERR_UNSUPPORTED;
         if (!aligned(s, 16) || !aligned(b, 16)) return AQ_ERR_ALIGNMENT;
     }
@@ -86,7 +86,6 @@ aq_status aq_matmul_bf16_ex(const void *x, const uint32_t *w_packed, const void 
     if (flags & ~(unsigned)(AQ_FLAG_PDL | AQ_FLAG_DEBUG_SKIP_X)) return AQ_ERR_INVALID_ARG;
     aq_status st = validate(x, w_packed, scales, biases, y, M, N, K, group_size, bits);
     if (st != AQ_OK || M == 0 || N == 0) return st;
-    if (bits == 8 && kernel == AQ_KERNEL_QMM) return AQ_ERR_UNSUPPORTED;   // no tensor-core path for 8-bit yet
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (K == 0) return record_cuda(cudaMemsetAsync(y, 0, (size_t)(M * N) * 2, cs));
 
@@ -121,16 +120,16 @@ aq_status aq_matmul_bf16_ex(const void *x, const uint32_t *w_packed, const void 
         }
         return true;
     };
-    if (bits == 8) {
-        // 8-bit codes run on the TMA-fed decode kernel only (no tensor-core path
-        // for them yet), in launches of 8 rows of x
-        st = AQ_OK;
-        return tma_rows(8, &st) ? st : AQ_ERR_UNSUPPORTED;
-    }
     if (kernel == AQ_KERNEL_QMM || (kernel == AQ_KERNEL_AUTO && M > kQmvMaxRows)) {
         if (a.debug_skip_x) return AQ_ERR_UNSUPPORTED;
         if (aq::qmm_supported(a)) return record_cuda(aq::launch_qmm(a));
         if (kernel == AQ_KERNEL_QMM) return AQ_ERR_UNSUPPORTED;
+    }
+    if (bits == 8) {
+        // 8-bit codes have no general decode kernel: the TMA-fed one, in launches
+        // of 8 rows of x
+        st = AQ_OK;
+        return tma_rows(8, &st) ? st : AQ_ERR_UNSUPPORTED;
     }
     if (M <= 8 && kernel != AQ_KERNEL_QMM) {
         a.M = M;

@@ -47,33 +47,42 @@
 namespace aq {
 namespace {
 
-constexpr int kTileM = 256;            // rows of x per CTA (two UMMA M=128 halves)
 constexpr int kTileN = 256;            // rows of W per CTA (UMMA N)
 constexpr int kGroup = 64;             // K per pipeline step (one quantization group)
 constexpr int kConvWarps = 16;
 constexpr int kThreads = (2 + kConvWarps) * 32;
 constexpr int kConvThreads = kConvWarps * 32;
 constexpr int kSBGroups = 8;           // groups of scales/biases per TMA box (16 bytes per row)
-
-// shared memory layout (offsets from a 1024-aligned base)
-constexpr int kATileBytes = kTileM * 128;          // 32768: fp16 x, 256 rows x 64 k
-constexpr int kBTileBytes = kTileN * 128;          // 32768: fp16 W, 256 rows x 64 k
-constexpr int kConvStageBytes = kATileBytes + kBTileBytes;
 constexpr int kConvStages = 2;
-constexpr int kRawXBytes = kTileM * 128;           // 32768: bf16 x, same swizzled geometry
-constexpr int kRawCodeBytes = kTileN * 32;         // 8192: 8 words per row
-constexpr int kRawStageBytes = kRawXBytes + kRawCodeBytes;
 constexpr int kRawStages = 2;
-constexpr int kSBBytes = kTileN * kSBGroups * 2;   // 4096 (scales, and again biases)
 constexpr int kSBStages = 2;
-constexpr int kOffConv = 0;
-constexpr int kOffRaw = kOffConv + kConvStages * kConvStageBytes;       // 131072
-constexpr int kOffSB = kOffRaw + kRawStages * kRawStageBytes;           // 212992
-constexpr int kOffBar = kOffSB + kSBStages * 2 * kSBBytes;              // 229376
+constexpr int kBTileBytes = kTileN * 128;          // 32768: fp16 W, 256 rows x 64 k
+constexpr int kSBBytes = kTileN * kSBGroups * 2;   // 4096 (scales, and again biases)
 // barriers: raw_full[2], raw_empty[2], sb_full[2], sb_empty[2], conv_full[2], conv_empty[2], acc_done
 constexpr int kNumBars = 2 * kRawStages + 2 * kSBStages + 2 * kConvStages + 1;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;                        // tmem address, abort flag
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;                        // + alignment slack
+
+// Shared-memory layout for a code width (offsets from a 1024-aligned base).
+// 4-bit codes: 256 rows of x per CTA (two UMMA M=128 halves); 8-bit codes
+// carry twice the raw bytes per W row, and 128 rows of x keep the stages
+// within the 227 KB a CTA may use.
+template <int BITS>
+struct Cfg {
+    static constexpr int kTileM = BITS == 4 ? 256 : 128;        // rows of x per CTA
+    static constexpr int kHalves = kTileM / 128;                 // UMMA M=128 accumulators
+    static constexpr int kATileBytes = kTileM * 128;             // fp16 x, kTileM rows x 64 k
+    static constexpr int kConvStageBytes = kATileBytes + kBTileBytes;
+    static constexpr int kRawXBytes = kTileM * 128;              // bf16 x, same swizzled geometry
+    static constexpr int kRowWords = kGroup * BITS / 32;         // code words per W row and group
+    static constexpr int kRawCodeBytes = kTileN * kRowWords * 4; // 8192 or 16384
+    static constexpr int kRawStageBytes = kRawXBytes + kRawCodeBytes;
+    static constexpr int kOffConv = 0;
+    static constexpr int kOffRaw = kOffConv + kConvStages * kConvStageBytes;
+    static constexpr int kOffSB = kOffRaw + kRawStages * kRawStageBytes;
+    static constexpr int kOffBar = kOffSB + kSBStages * 2 * kSBBytes;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;     // tmem address, abort flag
+    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;     // + alignment slack
+};
+static_assert(Cfg<4>::kSmemBytes <= 232448 && Cfg<8>::kSmemBytes <= 232448, "shared memory per CTA");
 
 constexpr uint32_t kTmemCols = 512;
 
@@ -150,6 +159,12 @@ __device__ __forceinline__ uint32_t code_pair_f16(uint32_t v, uint32_t magic) {
     asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;" : "=r"(r) : "r"(v), "r"(magic));
     return r;
 }
+// fp16x2 (1024 + byte 0, 1024 + byte 2) of a word: exact for bytes up to 255.
+__device__ __forceinline__ uint32_t byte_pair_f16(uint32_t v, uint32_t magic) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, 0x00FF00FF, %2, 0xEA;" : "=r"(r) : "r"(v), "r"(magic));
+    return r;
+}
 // fp16x2: (pair - 1024) * s + b, with the subtraction exact and one rounding in the FMA
 __device__ __forceinline__ uint32_t dequant_pair(uint32_t pair, uint32_t s2, uint32_t b2, uint32_t off2) {
     uint32_t q, w;
@@ -209,16 +224,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+template <int BITS>
 __global__ void __launch_bounds__(kThreads, 1)
 qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
            const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_b,
            __nv_bfloat16 *__restrict__ y, int M, int N, int K, unsigned long long timeout_ns, int *status) {
+    using C = Cfg<BITS>;
+    constexpr int kTileM = C::kTileM, kATileBytes = C::kATileBytes, kConvStageBytes = C::kConvStageBytes;
+    constexpr int kRawXBytes = C::kRawXBytes, kRawStageBytes = C::kRawStageBytes;
+    constexpr int kOffConv = C::kOffConv, kOffRaw = C::kOffRaw, kOffSB = C::kOffSB, kOffMisc = C::kOffMisc;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_addr(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (base - raw_base);
 
-    const uint32_t bar0 = base + kOffBar;
+    const uint32_t bar0 = base + C::kOffBar;
     auto raw_full = [&](int s) { return bar0 + 8 * s; };
     auto raw_empty = [&](int s) { return bar0 + 8 * (kRawStages + s); };
     auto sb_full = [&](int s) { return bar0 + 8 * (2 * kRawStages + s); };
@@ -299,7 +319,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 const uint32_t dst = base + kOffRaw + rs * kRawStageBytes;
                 mbar_expect_tx(raw_full(rs), kRawStageBytes);
                 tma_load_2d(dst, &tm_x, i * kGroup, m0, raw_full(rs));
-                tma_load_2d(dst + kRawXBytes, &tm_w, i * (kGroup / 8), n0, raw_full(rs));
+                tma_load_2d(dst + kRawXBytes, &tm_w, i * C::kRowWords, n0, raw_full(rs));
                 issued_raw = i + 1;
             }
             if (!ok) {
@@ -330,8 +350,8 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 for (int kk = 0; kk < kGroup / 16; ++kk) {
                     const uint64_t bd = sw128_desc(b0 + kk * 32);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h)
-                        umma_f16(tmem + h * kTileN, sw128_desc(a0 + h * (kATileBytes / 2) + kk * 32), bd,
+                    for (int h = 0; h < C::kHalves; ++h)
+                        umma_f16(tmem + h * kTileN, sw128_desc(a0 + h * (128 * 128) + kk * 32), bd,
                                  (i > 0 || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(conv_empty(cs));
@@ -361,42 +381,71 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             const uint32_t raw = base + kOffRaw + rs * kRawStageBytes;
             const uint32_t conv = base + kOffConv + cs * kConvStageBytes;
             // x: bf16 -> fp16, chunk by chunk at the same (swizzled) offsets,
-            // each chunk's k order becoming (0,4,1,5,2,6,3,7)
+            // each chunk's k order becoming (0,4,1,5,2,6,3,7) for 4-bit codes
+            // and (0,2,1,3,4,6,5,7) for 8-bit codes (the order the W pairs come in)
 #pragma unroll 4
             for (int c = 0; c < kRawXBytes / 16 / kConvThreads; ++c) {
                 const uint32_t off = (uint32_t)((c * kConvThreads + t) * 16);
                 const uint4 v = lds128(raw + off);
                 uint4 o;
-                o.x = f32x2_to_f16x2(bf16lo(v.x), bf16lo(v.z));
-                o.y = f32x2_to_f16x2(bf16hi(v.x), bf16hi(v.z));
-                o.z = f32x2_to_f16x2(bf16lo(v.y), bf16lo(v.w));
-                o.w = f32x2_to_f16x2(bf16hi(v.y), bf16hi(v.w));
+                if (BITS == 4) {
+                    o.x = f32x2_to_f16x2(bf16lo(v.x), bf16lo(v.z));
+                    o.y = f32x2_to_f16x2(bf16hi(v.x), bf16hi(v.z));
+                    o.z = f32x2_to_f16x2(bf16lo(v.y), bf16lo(v.w));
+                    o.w = f32x2_to_f16x2(bf16hi(v.y), bf16hi(v.w));
+                } else {
+                    o.x = f32x2_to_f16x2(bf16lo(v.x), bf16lo(v.y));
+                    o.y = f32x2_to_f16x2(bf16hi(v.x), bf16hi(v.y));
+                    o.z = f32x2_to_f16x2(bf16lo(v.z), bf16lo(v.w));
+                    o.w = f32x2_to_f16x2(bf16hi(v.z), bf16hi(v.w));
+                }
                 sts128(conv + off, o);
             }
-            // W: thread t takes half of row r = t / 2 (words 4h..4h+3, h = t % 2) and
-            // converts the row's scale and bias once; word c becomes 8 fp16
-            // weights at row r, chunk c ^ (r & 7)
+            // W: thread t takes half of row r = t / 2 (chunks 4h..4h+3, h = t % 2) and
+            // converts the row's scale and bias once; each chunk of 8 codes
+            // becomes 8 fp16 weights at row r, chunk c ^ (r & 7)
             const uint32_t sb = base + kOffSB + ss * 2 * kSBBytes;
             const int g8 = i % kSBGroups;
             {
                 static_assert(kConvThreads == 2 * kTileN, "two converter threads per W row");
                 const int r = t >> 1, hw = t & 1;
-                const uint4 wv = lds128(raw + kRawXBytes + r * 32 + hw * 16);
                 const __half sh = __float2half_rn(__uint_as_float((uint32_t)lds16(sb + (r * kSBGroups + g8) * 2) << 16));
                 const __half bh =
                     __float2half_rn(__uint_as_float((uint32_t)lds16(sb + kSBBytes + (r * kSBGroups + g8) * 2) << 16));
                 const uint32_t s2 = (uint32_t)__half_as_ushort(sh) * 0x00010001u;
                 const uint32_t b2 = (uint32_t)__half_as_ushort(bh) * 0x00010001u;
+                const uint32_t wrow = raw + kRawXBytes + r * (C::kRowWords * 4) + hw * (C::kRowWords * 2);
+                if (BITS == 4) {
+                    // word c of the row holds chunk c: pairs (p, p+4) from the word shifted by 4p
+                    const uint4 wv = lds128(wrow);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const uint32_t w = e == 0 ? wv.x : e == 1 ? wv.y : e == 2 ? wv.z : wv.w;
-                    const int c = 4 * hw + e;
-                    uint4 o;
-                    o.x = dequant_pair(code_pair_f16(w, magic), s2, b2, off2);
-                    o.y = dequant_pair(code_pair_f16(w >> 4, magic), s2, b2, off2);
-                    o.z = dequant_pair(code_pair_f16(w >> 8, magic), s2, b2, off2);
-                    o.w = dequant_pair(code_pair_f16(w >> 12, magic), s2, b2, off2);
-                    sts128(conv + kATileBytes + r * 128 + ((c ^ (r & 7)) << 4), o);
+                    for (int e = 0; e < 4; ++e) {
+                        const uint32_t w = e == 0 ? wv.x : e == 1 ? wv.y : e == 2 ? wv.z : wv.w;
+                        const int c = 4 * hw + e;
+                        uint4 o;
+                        o.x = dequant_pair(code_pair_f16(w, magic), s2, b2, off2);
+                        o.y = dequant_pair(code_pair_f16(w >> 4, magic), s2, b2, off2);
+                        o.z = dequant_pair(code_pair_f16(w >> 8, magic), s2, b2, off2);
+                        o.w = dequant_pair(code_pair_f16(w >> 12, magic), s2, b2, off2);
+                        sts128(conv + kATileBytes + r * 128 + ((c ^ (r & 7)) << 4), o);
+                    }
+                } else {
+                    // words 2c, 2c+1 hold chunk c: bytes (0,2) and (1,3) of each word pair up
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const uint4 wv = lds128(wrow + hh * 16);
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const uint32_t wa = e == 0 ? wv.x : wv.z, wb = e == 0 ? wv.y : wv.w;
+                            const int c = 4 * hw + 2 * hh + e;
+                            uint4 o;
+                            o.x = dequant_pair(byte_pair_f16(wa, magic), s2, b2, off2);
+                            o.y = dequant_pair(byte_pair_f16(wa >> 8, magic), s2, b2, off2);
+                            o.z = dequant_pair(byte_pair_f16(wb, magic), s2, b2, off2);
+                            o.w = dequant_pair(byte_pair_f16(wb >> 8, magic), s2, b2, off2);
+                            sts128(conv + kATileBytes + r * 128 + ((c ^ (r & 7)) << 4), o);
+                        }
+                    }
                 }
             }
             fence_proxy_async();  // make the generic-proxy stores visible to the MMA (async proxy)
@@ -408,8 +457,9 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             }
         }
         // ------------------------------------------------------------ epilogue
-        // warps 2..9 read the accumulators (two per TMEM lane quarter); the rest are done
-        bool go = warp < 10 && alive && mbar_wait(acc_done, 0, deadline, abort_flag) && !*abort_flag;
+        // warps 2..(1 + 4 x halves) read the accumulators (one per TMEM lane quarter and half)
+        constexpr int kEpiEnd = 2 + 4 * C::kHalves;
+        bool go = warp < kEpiEnd && alive && mbar_wait(acc_done, 0, deadline, abort_flag) && !*abort_flag;
         go = __all_sync(0xFFFFFFFFu, go);   // tcgen05.ld below is warp-collective
         if (go) {
             tc_fence_after();
@@ -441,7 +491,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                     }
                 }
             }
-        } else if (alive && warp < 10) {
+        } else if (alive && warp < kEpiEnd) {
             fail();
         }
     }
@@ -489,48 +539,58 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *gaddr, uint
 }
 
 constexpr int kMaxDevices = 64;
-std::atomic<int> g_attr_done[kMaxDevices];
+std::atomic<int> g_attr_done[2][kMaxDevices];
 
 }  // namespace
 
 bool qmm_supported(const MatmulArgs &a) {
-    return a.K % 512 == 0 && a.M >= 1 && a.N >= 1 && encode_fn() != nullptr &&
+    return (a.bits == 4 || a.bits == 8) && a.K % 512 == 0 && a.M >= 1 && a.N >= 1 && encode_fn() != nullptr &&
            (reinterpret_cast<uintptr_t>(a.scales) & 15) == 0 && (reinterpret_cast<uintptr_t>(a.biases) & 15) == 0;
 }
 
-cudaError_t launch_qmm(const MatmulArgs &a) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if (!g_attr_done[dev].load(std::memory_order_acquire)) {
-        e = cudaFuncSetAttribute(qmm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+namespace {
+template <int BITS>
+cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev) {
+    using C = Cfg<BITS>;
+    const int bi = BITS == 8 ? 1 : 0;
+    if (!g_attr_done[bi][dev].load(std::memory_order_acquire)) {
+        cudaError_t e = cudaFuncSetAttribute(qmm_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::kSmemBytes);
         if (e != cudaSuccess) return e;
-        g_attr_done[dev].store(1, std::memory_order_release);
+        g_attr_done[bi][dev].store(1, std::memory_order_release);
     }
     const int M = (int)a.M, N = (int)a.N, K = (int)a.K, G = K / 64;
     CUtensorMap tx, tw, ts, tb;
-    if (!encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, kGroup, kTileM,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.w, (uint64_t)K / 8, (uint64_t)N, (uint64_t)K / 2, kGroup / 8,
-                   kTileN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+    if (!encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, kGroup,
+                   C::kTileM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.w, (uint64_t)K * BITS / 32, (uint64_t)N,
+                   (uint64_t)K * BITS / 8, C::kRowWords, kTileN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.scales, (uint64_t)G, (uint64_t)N, (uint64_t)G * 2, kSBGroups,
                    kTileN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.biases, (uint64_t)G, (uint64_t)N, (uint64_t)G * 2, kSBGroups,
                    kTileN, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + kTileM - 1) / kTileM));
+    cfg.gridDim = dim3((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + C::kTileM - 1) / C::kTileM));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = a.stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, qmm_kernel, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(a.y), M, N, K,
+    return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(a.y), M, N, K,
                               (unsigned long long)a.timeout_ns, a.status);
+}
+}  // namespace
+
+cudaError_t launch_qmm(const MatmulArgs &a) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    return a.bits == 8 ? launch_qmm_bits<8>(a, dev) : launch_qmm_bits<4>(a, dev);
 }
 
 }  // namespace aq

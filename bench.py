@@ -547,39 +547,42 @@ def main():
                            "gbs": round(alg_bytes(1, N, K, 8) / (us * 1e-6) / 1e9, 1)}
         del ws8, base
 
-    # ---- prefill-sized tensor-core GEMM (qmm): M in {256, 2048}, (K, N) in {(4096, 14336), (14336, 4096)}
+    # ---- prefill-sized tensor-core GEMM (qmm): M in {256, 2048}, (K, N) in {(4096, 14336), (14336, 4096)},
+    # 4-bit codes (the workload) and 8-bit codes
     qmm = {}
-    for (K, N, label) in QMM_SHAPES:
-        w = synth.make_weights(N, K, synth.seed_for(5, 0, 0 if N == 14336 else 1))
-        copies = 4   # 4 x 33 MB of distinct weights > L2 between consecutive launches
-        ws = [(torch.from_numpy(w.w_packed.view(np.int32)).to(dev), torch.from_numpy(w.scales.view(np.int16)).to(dev),
-               torch.from_numpy(w.biases.view(np.int16)).to(dev)) for _ in range(copies)]
-        for M in QMM_M:
-            xq = torch.from_numpy(synth.make_x(M, K, synth.seed_for(5, M, 9)).view(np.int16)).to(dev)
-            yq = torch.empty((M, N), dtype=torch.int16, device=dev)
+    for bits in (4, 8):
+        for (K, N, label) in QMM_SHAPES:
+            w = synth.make_weights(N, K, synth.seed_for(5, 0, 0 if N == 14336 else 1), bits=bits)
+            copies = 4   # 4 x 33 MB (4-bit) of distinct weights > L2 between consecutive launches
+            ws = [(torch.from_numpy(w.w_packed.view(np.int32)).to(dev), torch.from_numpy(w.scales.view(np.int16)).to(dev),
+                   torch.from_numpy(w.biases.view(np.int16)).to(dev)) for _ in range(copies)]
+            for M in QMM_M:
+                xq = torch.from_numpy(synth.make_x(M, K, synth.seed_for(5, M, 9)).view(np.int16)).to(dev)
+                yq = torch.empty((M, N), dtype=torch.int16, device=dev)
 
-            def qlaunch(i):
-                wt, st, bt = ws[i % copies]
-                rc = lib.aq_matmul_bf16_ex(xq.data_ptr(), wt.data_ptr(), st.data_ptr(), bt.data_ptr(), yq.data_ptr(),
-                                           M, N, K, 64, 4, aq.AQ_KERNEL_AUTO, 0, cur.cuda_stream)
-                if rc != aq.AQ_OK:
-                    raise aq.AqError(rc, "aq_matmul_bf16_ex")
+                def qlaunch(i, ws=ws, xq=xq, yq=yq, M=M, N=N, K=K, bits=bits):
+                    wt, st, bt = ws[i % copies]
+                    rc = lib.aq_matmul_bf16_ex(xq.data_ptr(), wt.data_ptr(), st.data_ptr(), bt.data_ptr(),
+                                               yq.data_ptr(), M, N, K, 64, bits, aq.AQ_KERNEL_AUTO, 0, cur.cuda_stream)
+                    if rc != aq.AQ_OK:
+                        raise aq.AqError(rc, "aq_matmul_bf16_ex")
 
-            for i in range(3):
-                qlaunch(i)
-            torch.cuda.synchronize(dev)
-            reps = 10
-            e0.record(cur)
-            for i in range(reps):
-                qlaunch(i)
-            e1.record(cur)
-            e1.synchronize()
-            us = e0.elapsed_time(e1) * 1e3 / reps
-            tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
-            qmm[f"M{M}_K{K}_N{N}"] = {"us_per_call": round(us, 2), "tflops": round(tf, 1),
-                                      "frac_of_bf16_burst": round(tf / bf16_peak, 4),
-                                      "frac_of_bf16_sustained": round(tf / bf16_sus, 4)}
-        del ws
+                for i in range(3):
+                    qlaunch(i)
+                torch.cuda.synchronize(dev)
+                reps = 10
+                e0.record(cur)
+                for i in range(reps):
+                    qlaunch(i)
+                e1.record(cur)
+                e1.synchronize()
+                us = e0.elapsed_time(e1) * 1e3 / reps
+                tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
+                key = f"M{M}_K{K}_N{N}" + ("" if bits == 4 else "_8bit")
+                qmm[key] = {"us_per_call": round(us, 2), "tflops": round(tf, 1),
+                            "frac_of_bf16_burst": round(tf / bf16_peak, 4),
+                            "frac_of_bf16_sustained": round(tf / bf16_sus, 4)}
+            del ws
 
     # ---- CPU baseline: the oracle on two layers of the same workload, host cores
     cpu = None

@@ -93,10 +93,10 @@ enum {
  *               N == 0 launches nothing and returns AQ_OK; K == 0 writes y = 0.
  *   group_size  64.  Other values return AQ_ERR_UNSUPPORTED.
  *   bits        4 or 8.  Other values return AQ_ERR_UNSUPPORTED.  8-bit codes
- *               run on the weight-streaming kernel only: they need K a multiple
- *               of 512 and 16-byte aligned scales and biases
- *               (AQ_ERR_UNSUPPORTED / AQ_ERR_ALIGNMENT otherwise), and
- *               kernel AQ_KERNEL_QMM returns AQ_ERR_UNSUPPORTED.
+ *               run on the TMA-fed kernels only (the decode kernel up to 16
+ *               rows of x, the tensor-core kernel above): they need K a
+ *               multiple of 512 and 16-byte aligned scales and biases
+ *               (AQ_ERR_UNSUPPORTED / AQ_ERR_ALIGNMENT otherwise).
  *   Alignment   x and w_packed 16-byte aligned; scales, biases and y 2-byte
  *               aligned; otherwise AQ_ERR_ALIGNMENT.
  *   Aliasing    y must not overlap any input.

@@ -69,8 +69,8 @@ def test_validation_before_launch(args, expect):
 
 def test_ex_rejects_unknown_kernel_and_flags():
     assert aq.aq_matmul_bf16_ex(A, A, A, A, A, 1, 64, 128, 64, 4, 7, 0, None) == aq.AQ_ERR_INVALID_ARG
-    # no tensor-core kernel for 8-bit codes: an explicit request is refused before any launch
-    assert aq.aq_matmul_bf16_ex(A, A, A, A, A, 64, 64, 512, 64, 8, aq.AQ_KERNEL_QMM, 0, None) == aq.AQ_ERR_UNSUPPORTED
+    # 8-bit codes on the tensor-core kernel need K % 512 == 0: refused before any launch
+    assert aq.aq_matmul_bf16_ex(A, A, A, A, A, 64, 64, 576, 64, 8, aq.AQ_KERNEL_QMM, 0, None) == aq.AQ_ERR_UNSUPPORTED
     assert aq.aq_matmul_bf16_ex(A, A, A, A, A, 1, 64, 128, 64, 4, 0, 1 << 5, None) == aq.AQ_ERR_INVALID_ARG
     assert aq.aq_matmul_bf16_ex(A, A, A, A, A, 0, 64, 128, 64, 4, 2, 1, None) == aq.AQ_OK
 

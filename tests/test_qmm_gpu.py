@@ -22,21 +22,21 @@ def dev():
 def run(dev, x, w, kernel="qmm"):
     import torch
     xt, wt, st, bt = upload(x, w, dev)
-    y = aq.matmul(xt, wt, st, bt, kernel=kernel)
+    y = aq.matmul(xt, wt, st, bt, kernel=kernel, bits=w.bits)
     torch.cuda.synchronize()
     return from_dev_bf16(y)
 
 
-def check_full(dev, M, N, K, seed, kernel="qmm"):
-    w = synth.make_weights(N, K, seed)
+def check_full(dev, M, N, K, seed, kernel="qmm", bits=4):
+    w = synth.make_weights(N, K, seed, bits=bits)
     x = synth.make_x(M, K, seed)
     got = run(dev, x, w, kernel)
-    _, ref = oracle.matmul(x, w.w_packed, w.scales, w.biases, M, N, K)
-    return assert_parity(got, ref, what=f"qmm M={M} N={N} K={K}")
+    _, ref = oracle.matmul(x, w.w_packed, w.scales, w.biases, M, N, K, bits=bits)
+    return assert_parity(got, ref, what=f"qmm M={M} N={N} K={K} bits={bits}")
 
 
-def check_sampled(dev, M, N, K, seed, samples=3000, kernel="qmm"):
-    w = synth.make_weights(N, K, seed)
+def check_sampled(dev, M, N, K, seed, samples=3000, kernel="qmm", bits=4):
+    w = synth.make_weights(N, K, seed, bits=bits)
     x = synth.make_x(M, K, seed)
     got = run(dev, x, w, kernel)
     rng = np.random.default_rng(seed)
@@ -45,9 +45,9 @@ def check_sampled(dev, M, N, K, seed, samples=3000, kernel="qmm"):
     # always include the tile corners and the last row/column
     im = np.concatenate([im, [0, M - 1, M - 1, 0, min(255, M - 1), min(256, M - 1)]])
     inn = np.concatenate([inn, [0, N - 1, 0, N - 1, min(255, N - 1), min(256, N - 1)]])
-    ye, yb = oracle.matmul_sampled(x, w.w_packed, w.scales, w.biases, M, N, K, im, inn)
+    ye, yb = oracle.matmul_sampled(x, w.w_packed, w.scales, w.biases, M, N, K, im, inn, bits=bits)
     rms = float(np.sqrt(np.mean(ye * ye)))
-    return assert_parity(got[im, inn], yb, rms=rms, what=f"qmm sampled M={M} N={N} K={K}")
+    return assert_parity(got[im, inn], yb, rms=rms, what=f"qmm sampled M={M} N={N} K={K} bits={bits}")
 
 
 def test_qmm_single_tile(dev):
@@ -84,3 +84,41 @@ def test_qmm_deterministic(dev):
     torch.cuda.synchronize()
     assert torch.equal(a, b)
     assert aq.aq_read_device_status(None) == aq.AQ_OK
+
+
+# ---------------------------------------------------------------- 8-bit codes (128-row x tiles)
+
+@pytest.mark.parametrize("M,N,K", [
+    (128, 256, 512), (17, 64, 512), (129, 300, 1024), (255, 513, 1536), (300, 700, 2048), (1, 100, 512),
+    (1000, 257, 4096),
+])
+def test_qmm_eight_bit(dev, M, N, K):
+    check_full(dev, M, N, K, 900 + M + N + K, bits=8)
+
+
+@pytest.mark.parametrize("M", [256, 2048])
+@pytest.mark.parametrize("K,N", [(4096, 14336), (14336, 4096)])
+def test_qmm_eight_bit_prefill_shapes(dev, M, K, N):
+    check_sampled(dev, M, N, K, 950 + M + K, bits=8)
+
+
+def test_qmm_eight_bit_endpoints(dev):
+    """8-bit codes on the tensor-core path: a one-hot x over a q = 0 column gives
+    the bias and over a q = 255 column gives 255*scale + bias (each rounded to
+    fp16 on chip, then to bf16: compared with the oracle under the usual bound);
+    auto selects this path above 16 rows."""
+    N, K, M = 300, 1024, 40
+    w = synth.make_weights(N, K, 23, bits=8)
+    codes = oracle.unpack(w.w_packed, N, K, 8)
+    codes[:, 3] = 0
+    codes[:, 900] = 255
+    w.w_packed = oracle.pack(codes, 8)
+    x = synth.make_x(M, K, 23)
+    x[0] = 0
+    x[0, 3] = 0x3F80
+    x[1] = 0
+    x[1, 900] = 0x3F80
+    got = run(dev, x, w, kernel="auto")
+    _, ref = oracle.matmul(x, w.w_packed, w.scales, w.biases, M, N, K, bits=8)
+    assert_parity(got, ref, what="8-bit endpoints")
+    assert np.array_equal(got[0], w.biases[:, 0])

@@ -266,6 +266,12 @@ def test_eight_bit_rejected_where_unsupported(dev):
     w = synth.make_weights(8, 512, 1, bits=8)
     x = synth.make_x(32, 512, 1)
     xt, wt, st, bt = upload(x, w, dev)
+    # scales 2 bytes past a 16-byte boundary: neither 8-bit kernel can load them
+    flat = torch.empty(st.numel() + 1, dtype=st.dtype, device=st.device)
+    st_off = flat[1:].view(st.shape)
+    st_off.copy_(st)
     with pytest.raises(aq.AqError):
-        aq.matmul(xt, wt, st, bt, bits=8, kernel="qmm")   # no tensor-core kernel for 8-bit
+        aq.matmul(xt, wt, st_off, bt, bits=8, kernel="qmm")
+    with pytest.raises(aq.AqError):
+        aq.matmul(xt[:1].contiguous(), wt, st_off, bt, bits=8)
     torch.cuda.synchronize()
