@@ -83,6 +83,12 @@ struct Cfg {
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;     // + alignment slack
 };
 static_assert(Cfg<4>::kSmemBytes <= 232448 && Cfg<8>::kSmemBytes <= 232448, "shared memory per CTA");
+// split-K partials received by a CTA (at most 7 sources x its 32 columns x the tile's rows) fit in
+// the stage memory in front of the barriers
+constexpr int kMaxSplit = 8;
+static_assert((kMaxSplit - 1) * Cfg<4>::kTileM * (kTileN / kMaxSplit) * 4 <= Cfg<4>::kOffBar &&
+                  (kMaxSplit - 1) * Cfg<8>::kTileM * (kTileN / kMaxSplit) * 4 <= Cfg<8>::kOffBar,
+              "split-K receive slots");
 
 constexpr uint32_t kTmemCols = 512;
 
@@ -212,6 +218,34 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
                  : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// all threads of every CTA of the cluster; release/acquire orders shared::cluster memory
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// the same shared-memory offset in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t map_cta(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -253,7 +287,14 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     const int lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * kTileN;
     const int m0 = blockIdx.y * kTileM;
-    const int steps = K / kGroup;
+    // split K: the gridDim.z CTAs of a cluster each take a contiguous share of
+    // the K/512 blocks of 8 groups and add their partial tiles through
+    // distributed shared memory at the end
+    const int nsplit = (int)gridDim.z, split = (int)blockIdx.z;
+    const int blocks = K / (kGroup * kSBGroups);
+    const int blk0 = split * blocks / nsplit, blk1 = (split + 1) * blocks / nsplit;
+    const int g0 = blk0 * kSBGroups;                // first group of this CTA
+    const int steps = (blk1 - blk0) * kSBGroups;    // groups of this CTA
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRawStages; ++s) {
@@ -292,6 +333,54 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             *abort_flag = 1;
         }
     };
+    // epilogue geometry of warps 2..kEpiEnd-1: TMEM lane quarter q, accumulator half h
+    // (x rows 128h..128h+127), this lane's row m of y
+    constexpr int kEpiEnd = 2 + 4 * C::kHalves;
+    const int q = warp & 3;
+    const int h = warp >= 2 ? (warp - 2) >> 2 : 0;
+    const int m = m0 + h * 128 + q * 32 + lane;
+    const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * kTileN);
+    bool go = false;   // this warp holds final accumulators to write out
+    // 16 fp32 values of row m, columns n..n+15 -> bf16 y
+    auto store_row16 = [&](const float (&a)[16], int m_, int n) {
+        if (m_ >= M) return;
+        __nv_bfloat16 *yp = y + (int64_t)m_ * N + n;
+        if (n + 16 <= N && (((uintptr_t)yp) & 15) == 0) {
+#pragma unroll
+            for (int v = 0; v < 2; ++v) {
+                uint4 o;
+                o.x = f32x2_to_bf16x2(__float_as_uint(a[8 * v + 0]), __float_as_uint(a[8 * v + 1]));
+                o.y = f32x2_to_bf16x2(__float_as_uint(a[8 * v + 2]), __float_as_uint(a[8 * v + 3]));
+                o.z = f32x2_to_bf16x2(__float_as_uint(a[8 * v + 4]), __float_as_uint(a[8 * v + 5]));
+                o.w = f32x2_to_bf16x2(__float_as_uint(a[8 * v + 6]), __float_as_uint(a[8 * v + 7]));
+                *reinterpret_cast<uint4 *>(yp + 8 * v) = o;
+            }
+        } else {
+#pragma unroll
+            for (int v = 0; v < 16; ++v)
+                if (n + v < N) yp[v] = __float2bfloat16_rn(a[v]);
+        }
+    };
+    // 32 fp32 values of row m, columns n..n+31 -> bf16 y
+    auto store_row32 = [&](const uint32_t (&r)[32], int m_, int n) {
+        if (m_ >= M) return;
+        __nv_bfloat16 *yp = y + (int64_t)m_ * N + n;
+        if (n + 32 <= N && (((uintptr_t)yp) & 15) == 0) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                uint4 o;
+                o.x = f32x2_to_bf16x2(r[8 * v + 0], r[8 * v + 1]);
+                o.y = f32x2_to_bf16x2(r[8 * v + 2], r[8 * v + 3]);
+                o.z = f32x2_to_bf16x2(r[8 * v + 4], r[8 * v + 5]);
+                o.w = f32x2_to_bf16x2(r[8 * v + 6], r[8 * v + 7]);
+                *reinterpret_cast<uint4 *>(yp + 8 * v) = o;
+            }
+        } else {
+#pragma unroll
+            for (int v = 0; v < 32; ++v)
+                if (n + v < N) yp[v] = __float2bfloat16_rn(__uint_as_float(r[v]));
+        }
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -308,8 +397,8 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                     }
                     const uint32_t dst = base + kOffSB + ss * 2 * kSBBytes;
                     mbar_expect_tx(sb_full(ss), 2 * kSBBytes);
-                    tma_load_2d(dst, &tm_s, j * kSBGroups, n0, sb_full(ss));
-                    tma_load_2d(dst + kSBBytes, &tm_b, j * kSBGroups, n0, sb_full(ss));
+                    tma_load_2d(dst, &tm_s, g0 + j * kSBGroups, n0, sb_full(ss));
+                    tma_load_2d(dst + kSBBytes, &tm_b, g0 + j * kSBGroups, n0, sb_full(ss));
                     issued_sb = j + 1;
                 }
                 if (i >= kRawStages && !mbar_wait(raw_empty(rs), ((i / kRawStages) - 1) & 1, deadline, abort_flag)) {
@@ -318,8 +407,8 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 }
                 const uint32_t dst = base + kOffRaw + rs * kRawStageBytes;
                 mbar_expect_tx(raw_full(rs), kRawStageBytes);
-                tma_load_2d(dst, &tm_x, i * kGroup, m0, raw_full(rs));
-                tma_load_2d(dst + kRawXBytes, &tm_w, i * C::kRowWords, n0, raw_full(rs));
+                tma_load_2d(dst, &tm_x, (g0 + i) * kGroup, m0, raw_full(rs));
+                tma_load_2d(dst + kRawXBytes, &tm_w, (g0 + i) * C::kRowWords, n0, raw_full(rs));
                 issued_raw = i + 1;
             }
             if (!ok) {
@@ -458,41 +547,81 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         }
         // ------------------------------------------------------------ epilogue
         // warps 2..(1 + 4 x halves) read the accumulators (one per TMEM lane quarter and half)
-        constexpr int kEpiEnd = 2 + 4 * C::kHalves;
-        bool go = warp < kEpiEnd && alive && mbar_wait(acc_done, 0, deadline, abort_flag) && !*abort_flag;
+        go = warp < kEpiEnd && alive && mbar_wait(acc_done, 0, deadline, abort_flag) && !*abort_flag;
         go = __all_sync(0xFFFFFFFFu, go);   // tcgen05.ld below is warp-collective
         if (go) {
             tc_fence_after();
-            const int q = warp & 3;                 // TMEM lane quarter this warp may access
-            const int h = (warp - 2) >> 2;          // accumulator half: x rows 128h..128h+127
-            const int m = m0 + h * 128 + q * 32 + lane;
-            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * kTileN);
+            if (nsplit == 1) {
 #pragma unroll 1
-            for (int j = 0; j < kTileN / 32; ++j) {
-                uint32_t r[32];
-                tmem_ld32(tbase + j * 32, r);
-                const int n = n0 + j * 32;
-                if (m < M) {
-                    __nv_bfloat16 *yp = y + (int64_t)m * N + n;
-                    if (n + 32 <= N && (((uintptr_t)yp) & 15) == 0) {
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint4 o;
-                            o.x = f32x2_to_bf16x2(r[8 * v + 0], r[8 * v + 1]);
-                            o.y = f32x2_to_bf16x2(r[8 * v + 2], r[8 * v + 3]);
-                            o.z = f32x2_to_bf16x2(r[8 * v + 4], r[8 * v + 5]);
-                            o.w = f32x2_to_bf16x2(r[8 * v + 6], r[8 * v + 7]);
-                            *reinterpret_cast<uint4 *>(yp + 8 * v) = o;
-                        }
-                    } else {
-#pragma unroll
-                        for (int v = 0; v < 32; ++v)
-                            if (n + v < N) yp[v] = __float2bfloat16_rn(__uint_as_float(r[v]));
-                    }
+                for (int j = 0; j < kTileN / 32; ++j) {
+                    uint32_t r[32];
+                    tmem_ld32(tbase + j * 32, r);
+                    store_row32(r, m, n0 + j * 32);
                 }
             }
         } else if (alive && warp < kEpiEnd) {
             fail();
+        }
+    }
+
+    if (nsplit > 1) {
+        // Split-K sum.  CTA o of the cluster owns columns [o W, (o + 1) W) of the
+        // tile (W = 256 / nsplit); every other CTA writes its partial of those
+        // columns into o's (now idle) stage memory, and o adds the partials in
+        // cluster-rank order (deterministic) and stores y.  Receive slot of
+        // source z at owner o: z - (z > o); rows of W floats, 16-byte units
+        // XOR-swizzled by row so the stores spread over the banks.
+        const int W = kTileN / nsplit;
+        const uint32_t me = cluster_rank();
+        const uint32_t recv = base + kOffConv;
+        auto unit_addr = [&](int slot, int row, int col, int v) {   // col: first column of a 32-column chunk
+            return recv + (uint32_t)(((slot * kTileM + row) * W + col) * 4 + (((v ^ (row & 7)) & 7) << 4));
+        };
+        cluster_sync();   // every partial final, every CTA's stage memory free
+        const int row = m - m0;
+        if (go) {
+#pragma unroll 1
+            for (int j = 0; j < kTileN / 32; ++j) {
+                const int o = j * 32 / W;
+                if (o == (int)me) continue;
+                uint32_t r[32];
+                tmem_ld32(tbase + j * 32, r);
+                const int slot = (int)me - ((int)me > o ? 1 : 0);
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    st_cluster128(map_cta(unit_addr(slot, row, j * 32 - o * W, v), (uint32_t)o), r[4 * v],
+                                  r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+            }
+        }
+        cluster_sync();   // every partial delivered
+        if (go) {
+            // 16 columns at a time: the own partial from TMEM, the others from the receive slots
+#pragma unroll 1
+            for (int c = (int)me * W; c < ((int)me + 1) * W; c += 16) {
+                const int col = (c & ~31) - (int)me * W, v0 = (c & 16) >> 2;   // chunk start, first 16-byte unit
+                float acc[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+                for (int z = 0; z < nsplit; ++z) {
+                    if (z == (int)me) {
+                        uint32_t r[16];
+                        tmem_ld16(tbase + c, r);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) acc[e] += __uint_as_float(r[e]);
+                    } else {
+                        const int slot = z - (z > (int)me ? 1 : 0);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const uint4 u = lds128(unit_addr(slot, row, col, v0 + v));
+                            acc[4 * v] += __uint_as_float(u.x);
+                            acc[4 * v + 1] += __uint_as_float(u.y);
+                            acc[4 * v + 2] += __uint_as_float(u.z);
+                            acc[4 * v + 3] += __uint_as_float(u.w);
+                        }
+                    }
+                }
+                store_row16(acc, m, n0 + c);
+            }
         }
     }
 
@@ -540,6 +669,9 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *gaddr, uint
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_attr_done[2][kMaxDevices];
+std::atomic<int> g_sms[kMaxDevices];
+// clusters of 2, 4, 8 CTAs that can be resident at once, per code width (0: not yet asked; -1: none)
+std::atomic<int> g_max_clusters[2][3][kMaxDevices];
 
 }  // namespace
 
@@ -570,16 +702,62 @@ cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev) {
         !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.biases, (uint64_t)G, (uint64_t)N, (uint64_t)G * 2, kSBGroups,
                    kTileN, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
+    int sms = g_sms[dev].load(std::memory_order_relaxed);
+    if (sms == 0) {
+        cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        g_sms[dev].store(sms, std::memory_order_relaxed);
+    }
+    const int tiles = ((N + kTileN - 1) / kTileN) * ((M + C::kTileM - 1) / C::kTileM);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + C::kTileM - 1) / C::kTileM));
+    cfg.gridDim = dim3((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + C::kTileM - 1) / C::kTileM), 1);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = a.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (a.pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    // Too few output tiles to occupy half the SMs (prefill at M = 256): split K
+    // across a cluster of 2, 4 or 8 CTAs, as many as still fit in one wave.
+    int split = 1;
+    if (2 * tiles <= sms) {
+        for (int si = 2; si >= 0 && split == 1; --si) {
+            const int S = 2 << si;
+            if (S > K / (kGroup * kSBGroups) || tiles * S > sms) continue;
+            int n = g_max_clusters[bi][si][dev].load(std::memory_order_relaxed);
+            if (n == 0) {
+                cudaLaunchConfig_t q = cfg;
+                q.gridDim = dim3(1, 1, (unsigned)S);
+                cudaLaunchAttribute ca;
+                ca.id = cudaLaunchAttributeClusterDimension;
+                ca.val.clusterDim.x = 1;
+                ca.val.clusterDim.y = 1;
+                ca.val.clusterDim.z = (unsigned)S;
+                q.attrs = &ca;
+                q.numAttrs = 1;
+                if (cudaOccupancyMaxActiveClusters(&n, qmm_kernel<BITS>, &q) != cudaSuccess || n < 1) {
+                    cudaGetLastError();   // the query's error is not the caller's
+                    n = -1;
+                }
+                g_max_clusters[bi][si][dev].store(n, std::memory_order_relaxed);
+            }
+            if (n >= tiles) split = S;
+        }
+    }
+    if (split > 1) {
+        cfg.gridDim.z = (unsigned)split;
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = (unsigned)split;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = a.pdl ? 1 : 0;
+    cfg.numAttrs = (unsigned)na;
     return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(a.y), M, N, K,
                               (unsigned long long)a.timeout_ns, a.status);
 }

@@ -122,3 +122,19 @@ def test_qmm_eight_bit_endpoints(dev):
     _, ref = oracle.matmul(x, w.w_packed, w.scales, w.biases, M, N, K, bits=8)
     assert_parity(got, ref, what="8-bit endpoints")
     assert np.array_equal(got[0], w.biases[:, 0])
+
+
+@pytest.mark.parametrize("M,N,K,bits", [(256, 512, 4096, 4), (64, 256, 8192, 4), (128, 300, 4096, 8)])
+def test_qmm_split_k(dev, M, N, K, bits):
+    """Few output tiles: K is split across a cluster of CTAs whose partial tiles
+    are added in shared memory in a fixed order.  Against the oracle, and the
+    same bits on every call."""
+    import torch
+    check_full(dev, M, N, K, 1300 + M + K, bits=bits)
+    w = synth.make_weights(N, K, 7, bits=bits)
+    x = synth.make_x(M, K, 7)
+    xt, wt, st, bt = upload(x, w, dev)
+    y1 = aq.matmul(xt, wt, st, bt, kernel="qmm", bits=bits)
+    y2 = aq.matmul(xt, wt, st, bt, kernel="qmm", bits=bits)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
