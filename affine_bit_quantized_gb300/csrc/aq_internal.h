@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "aq.h"
@@ -35,6 +36,8 @@ cudaError_t launch_qmv(const MatmulArgs &a);
 
 // TMA-fed weight-streaming kernel (qmv_tma.cu) for 1 <= M <= 8,
 // K % 512 == 0, M*K <= 16384 and 16-byte aligned scales/biases.
+// tensor map of packed codes for the decode kernels: a stage (32 rows x 1024 bytes) per copy
+bool encode_codes_3d(CUtensorMap *map, const void *base, uint64_t row_bytes, uint64_t rows);
 bool qmv_tma_supported(const MatmulArgs &a);
 int qmv_tma_passes(const MatmulArgs &a);   // K passes the TMA kernel makes (x staged per pass)
 bool qmv_tma_preferred(const MatmulArgs &a);   // faster than the general kernel for this 4-bit shape

@@ -197,7 +197,6 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
                 }
                 const int K = cur.K, T = cur.T;
                 constexpr int SC = Geo<BITS>::kStageCodes, SG = Geo<BITS>::kStageGroups;
-                const int nbox = K / Geo<BITS>::kBoxCodes;             // 128-byte code boxes per row
                 const int KB = (K + SC - 1) / SC;
                 // tiles are dealt round-robin, continuing from the previous
                 // matmul of the same dependency group so that the group stays
@@ -213,11 +212,9 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
                         }
                         const uint32_t dst = s_base + slot * kStageBytes;
                         const uint32_t fb = bar_full + 8 * slot;
-                        int nvalid = nbox - kb * kBoxes;
-                        nvalid = nvalid < kBoxes ? nvalid : kBoxes;
-                        mbar_expect_tx(fb, (uint32_t)(nvalid * kBoxBytes + 2 * kRows * SG * 2));
-                        for (int b = 0; b < nvalid; ++b)
-                            tma_load_2d(dst + b * kBoxBytes, &rec->tw, (kb * kBoxes + b) * 32, tile * kRows, fb, pol);
+                        // one copy of the stage's codes (chunks past the row's end read as zeros)
+                        mbar_expect_tx(fb, (uint32_t)(kCodesBytes + 2 * kRows * SG * 2));
+                        tma_load_3d(dst, &rec->tw, 0, tile * kRows, kb * kBoxes, fb, pol);
                         tma_load_2d(dst + kCodesBytes, &rec->ts, kb * SG, tile * kRows, fb, pol);
                         tma_load_2d(dst + kCodesBytes + kSBRegion, &rec->tb, kb * SG, tile * kRows, fb, pol);
                         ++issued;
@@ -414,12 +411,12 @@ aq_status chain_encode(const aq_matmul_desc *descs, int count, int bits, ChainRe
         ChainRec &r = recs[i];
         std::memset(&r, 0, sizeof r);
         const uint64_t K = (uint64_t)d.K, N = (uint64_t)d.N, G = K / 64;
-        // codes: 32-word x 32-row boxes, 128-byte swizzle; scales and biases: one
-        // stage's groups x 32 rows (64-byte rows and swizzle for 4-bit codes, 32 for 8-bit)
+        // codes: one stage (8 chunks x 32 rows x 128 bytes, 128-byte swizzle) per box; scales
+        // and biases: one stage's groups x 32 rows (64-byte rows and swizzle for 4-bit codes,
+        // 32 for 8-bit)
         const uint32_t sg = (uint32_t)stage_groups(bits);
         const CUtensorMapSwizzle sbs = bits == 8 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
-        if (!encode_2d(&r.tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, d.w_packed, K * bits / 32, N, K * bits / 8, 32, kRows,
-                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+        if (!encode_codes_3d(&r.tw, d.w_packed, K * bits / 8, N) ||
             !encode_2d(&r.ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, d.scales, G, N, G * 2, sg, kRows, sbs) ||
             !encode_2d(&r.tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, d.biases, G, N, G * 2, sg, kRows, sbs))
             return AQ_ERR_INVALID_ARG;

@@ -119,7 +119,6 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int nbox = K / Gm::kBoxCodes;                            // code boxes in K
     const int T = (N + kRows - 1) / kRows;
     const int my_tiles = (int)blockIdx.x < T ? (T - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int L_items = my_tiles * KB;
@@ -169,11 +168,10 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                 const int tile = (int)blockIdx.x + t * (int)gridDim.x;
                 const uint32_t dst = s_base + slot * kStageBytes;
                 const uint32_t fb = bar_full + 8 * slot;
-                int nvalid = nbox - kb * kBoxes;
-                nvalid = nvalid < kBoxes ? nvalid : kBoxes;
-                mbar_expect_tx(fb, (uint32_t)(nvalid * kBoxBytes + 2 * kRows * Gm::kSBRowBytes));
-                for (int b = 0; b < nvalid; ++b)
-                    tma_load_2d(dst + b * kBoxBytes, &tm_w, (kb * kBoxes + b) * 32, tile * kRows, fb, pol);
+                // one box of 8 chunks x 32 rows x 128 bytes (chunks past the row's end read as
+                // zeros and still count toward the transaction)
+                mbar_expect_tx(fb, (uint32_t)(kCodesBytes + 2 * kRows * Gm::kSBRowBytes));
+                tma_load_3d(dst, &tm_w, 0, tile * kRows, kb * kBoxes, fb, pol);
                 tma_load_2d(dst + kCodesBytes, &tm_s, kb * Gm::kStageGroups, tile * kRows, fb, pol);
                 tma_load_2d(dst + kCodesBytes + kSBRegion, &tm_b, kb * Gm::kStageGroups, tile * kRows, fb, pol);
                 advance();
@@ -332,6 +330,22 @@ std::atomic<int> g_attr_done[8][kMaxDevices];
 
 }  // namespace
 
+// The packed codes as a 3-D tensor {32 words, N rows, row bytes / 128 chunks} (the
+// chunks 128 bytes apart, rows row_bytes apart), read in boxes of {32, 32, 8}:
+// one copy brings a whole stage, laid out as 8 chunk planes of 32 rows x 128
+// bytes with the 128-byte swizzle.
+bool encode_codes_3d(CUtensorMap *map, const void *base, uint64_t row_bytes, uint64_t rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {32, rows, row_bytes / 128};
+    cuuint64_t strides[2] = {row_bytes, 128};
+    cuuint32_t box[3] = {32, (cuuint32_t)kRows, (cuuint32_t)kBoxes};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool qmv_tma_supported(const MatmulArgs &a) {
     return (a.bits == 4 || a.bits == 8) && a.M >= 1 && a.M <= kMaxM && a.K % 512 == 0 && encode_fn() != nullptr &&
            (reinterpret_cast<uintptr_t>(a.scales) & 15) == 0 && (reinterpret_cast<uintptr_t>(a.biases) & 15) == 0;
@@ -411,13 +425,12 @@ cudaError_t launch_qmv_tma(const MatmulArgs &a) {
     }
     CUtensorMap tw, ts, tb;
     const int G = K / 64;
-    // codes: 32-word x 32-row boxes, 128-byte swizzle; scales and biases: one
+    // codes: one stage (8 chunks x 32 rows x 128 bytes, 128-byte swizzle) per box; scales and biases: one
     // stage's groups x 32 rows (64 bytes and 64-byte swizzle for 4-bit codes,
     // 32 bytes and 32-byte swizzle for 8-bit)
     const uint32_t sg = (uint32_t)stage_groups(a.bits);
     const CUtensorMapSwizzle sbs = eight ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
-    if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.w, (uint64_t)K * a.bits / 32, (uint64_t)N,
-                   (uint64_t)K * a.bits / 8, 32, kRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+    if (!encode_codes_3d(&tw, a.w, (uint64_t)K * a.bits / 8, (uint64_t)N) ||
         !encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.scales, (uint64_t)G, (uint64_t)N, (uint64_t)G * 2, sg, kRows,
                    sbs) ||
         !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.biases, (uint64_t)G, (uint64_t)N, (uint64_t)G * 2, sg, kRows,
