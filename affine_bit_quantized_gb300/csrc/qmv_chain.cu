@@ -50,12 +50,14 @@ struct ChainRec {                // 128-byte aligned, as CUtensorMap is
     int flags;                    // AQ_CHAIN_INDEPENDENT
     int tile_base;                // tiles of the preceding matmuls since the last dependent one
     int bits;                     // code width: 4 or 8
-    int pad[5];
+    int group;                    // first matmul of this one's dependency group (its counter)
+    int pad[4];
 };
 static_assert(sizeof(ChainRec) % 128 == 0, "records must stay 128-byte aligned");
 static_assert(offsetof(ChainRec, x) % 16 == 0 && offsetof(ChainRec, M) == offsetof(ChainRec, x) + 16 &&
                   offsetof(ChainRec, flags) == offsetof(ChainRec, x) + 32 &&
-                  offsetof(ChainRec, bits) == offsetof(ChainRec, x) + 40,
+                  offsetof(ChainRec, bits) == offsetof(ChainRec, x) + 40 &&
+                  offsetof(ChainRec, group) == offsetof(ChainRec, x) + 44,
               "the scalar part of a record is read as three 16-byte vectors");
 
 namespace {
@@ -89,6 +91,9 @@ __host__ __device__ inline ChainLayout chain_layout(int x_bytes, int max_m) {
     return L;
 }
 
+__device__ __forceinline__ void red_release_gpu_add(int *p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -102,7 +107,7 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *m) {
 struct RecInfo {
     const __nv_bfloat16 *x;
     __nv_bfloat16 *y;
-    int M, N, K, T, flags, tile_base, bits;
+    int M, N, K, T, flags, tile_base, bits, group;
 };
 __device__ __forceinline__ RecInfo unpack_info(uint4 a, uint4 b, uint4 c) {
     RecInfo i;
@@ -115,6 +120,7 @@ __device__ __forceinline__ RecInfo unpack_info(uint4 a, uint4 b, uint4 c) {
     i.flags = (int)c.x;
     i.tile_base = (int)c.y;
     i.bits = (int)c.z;
+    i.group = (int)c.w;
     return i;
 }
 // Record jm's scalars: the first kInfoCap come from the copy every CTA makes in
@@ -234,21 +240,25 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
     } else if (warp == kConsumerWarps + 1) {
         // ------------------------------------------------------------ reducer / signaller
         // Adds the sixteen warps' partials of each of this CTA's tiles in order
-        // and stores y.  After the CTA's last tile of a matmul it publishes
-        // the count to the matmul's counter (one GPU-scope fence per CTA and
-        // matmul, off the consumers' path); before a dependent matmul it waits
-        // until every CTA has stored all tiles of the previous one, then
-        // releases the consumers.
-        int tcount = 0, prev_T = 0;
+        // and stores y.  A dependency group is a dependent matmul and the
+        // independent ones after it; each has one completion counter.  After
+        // the CTA's last tile of a group the warp publishes its tile count of
+        // the group (one GPU-scope release per CTA and group, off the
+        // consumers' path); before a dependent matmul it waits until every CTA
+        // has stored all tiles of the previous group, then releases the
+        // consumers.
+        int tcount = 0, pending = 0;
         bool ok = true;
-        RecInfo cur = load_info(recs, info, 0);
+        RecInfo prev = load_info(recs, info, 0), cur = prev;
         for (int jm = 0; jm < count; ++jm) {
             RecInfo nxt = cur;
             if (jm + 1 < count) nxt = load_info(recs, info, jm + 1);
             if (jm > 0 && !(cur.flags & AQ_CHAIN_INDEPENDENT)) {
                 if (lane == 0) {
+                    // the previous group's tiles: its last matmul's tile_base counts the ones before it
+                    const int want = prev.tile_base + prev.T;
                     const uint64_t dl = global_timer() + timeout_ns;
-                    while (ok && ld_acquire_gpu(done + (jm - 1)) < prev_T) {
+                    while (ok && ld_acquire_gpu(done + prev.group) < want) {
                         if (*abort_flag || global_timer() > dl) {
                             set_abort();
                             ok = false;
@@ -259,15 +269,17 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
                 ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
             }
             const int first = (cta - cur.tile_base % ncta + ncta) % ncta;
-            int mine = 0;
-            for (int tile = first; tile < cur.T && ok; tile += ncta, ++mine, ++tcount)
+            for (int tile = first; tile < cur.T && ok; tile += ncta, ++pending, ++tcount)
                 ok = reduce_tile<ONE_ROW>(tc, tcount, tile, cur.M, cur.N, cur.y, lane, timeout_ns, abort_flag);
-            if (ok && mine > 0 && lane == 0) {
-                __threadfence();   // this warp's y stores of the matmul reach GPU scope before the count
-                atomicAdd(done + jm, mine);
+            const bool group_ends = jm + 1 == count || !(nxt.flags & AQ_CHAIN_INDEPENDENT);
+            if (ok && group_ends && pending > 0 && lane == 0) {
+                // every lane's y stores precede this (reduce_tile ends with __syncwarp);
+                // the release makes them visible at GPU scope before the count
+                red_release_gpu_add(done + cur.group, pending);
             }
+            if (group_ends) pending = 0;
             if (!ok && lane == 0) set_abort();
-            prev_T = cur.T;
+            prev = cur;
             cur = nxt;
         }
         __syncwarp();
@@ -428,7 +440,9 @@ aq_status chain_encode(const aq_matmul_desc *descs, int count, int bits, ChainRe
         r.tiles = (int)((d.N + kRows - 1) / kRows);
         r.flags = (int)d.flags;
         r.bits = bits;
-        r.tile_base = (i > 0 && (d.flags & AQ_CHAIN_INDEPENDENT)) ? recs[i - 1].tile_base + recs[i - 1].tiles : 0;
+        const bool indep = i > 0 && (d.flags & AQ_CHAIN_INDEPENDENT);
+        r.tile_base = indep ? recs[i - 1].tile_base + recs[i - 1].tiles : 0;
+        r.group = indep ? recs[i - 1].group : i;
         x_bytes = std::max(x_bytes, (int)(d.M * d.K * 2));
         one_row = one_row && d.M == 1;
     }
