@@ -22,8 +22,14 @@ this double rounding only shapes the input distribution, never a result.
 
 Random streams: ``numpy.random.Philox`` keyed through
 ``SeedSequence([seed, stream])``; stream 0 draws the weights (codes, then
-scales, then bias noise), stream 1 draws x.  The seed of matrix j of layer l of
-workload c is ``1000*c + 16*l + j``; the tiny correctness case uses seed 0.
+scales, then bias noise), stream 1 draws x, stream 2 draws the MoE routing.
+The seed of matrix j of layer l of workload c is ``1000*c + 16*l + j``; the tiny
+correctness case uses seed 0.
+
+MoE (expert-indexed) cases: E expert matrices of one shape stacked (expert e
+from seed + e), T tokens of x, and a synthetic top-k routing: each token picks
+k distinct experts uniformly at random; the rows (token, expert) are sorted by
+expert, as a grouped prefill kernel consumes them.
 """
 from __future__ import annotations
 
@@ -33,6 +39,7 @@ import numpy as np
 
 STREAM_WEIGHTS = 0
 STREAM_X = 1
+STREAM_ROUTING = 2
 
 
 def _rng(seed: int, stream: int) -> np.random.Generator:
@@ -98,6 +105,42 @@ def seed_for(config: int, layer: int = 0, matrix: int = 0) -> int:
         return 0
     return 1000 * config + 16 * layer + matrix
 
+
+class ExpertWeights:
+    """E packed weight matrices stacked: ``w_packed`` uint32[E, N, K*bits/32],
+    ``scales``/``biases`` uint16[E, N, K/group_size] (expert e drawn with
+    ``make_weights(N, K, seed + e)``)."""
+
+    def __init__(self, E: int, N: int, K: int, seed: int, group_size: int = 64, bits: int = 4):
+        ws = [make_weights(N, K, seed + e, group_size, bits) for e in range(E)]
+        self.w_packed = np.stack([w.w_packed for w in ws])
+        self.scales = np.stack([w.scales for w in ws])
+        self.biases = np.stack([w.biases for w in ws])
+        self.E, self.N, self.K, self.group_size, self.bits = E, N, K, group_size, bits
+
+
+def make_routing(T: int, E: int, top_k: int, seed: int):
+    """Synthetic top-k routing of T tokens over E experts: every token picks
+    top_k distinct experts uniformly at random.  Returns int32 arrays
+    (lhs, rhs) of T*top_k rows sorted by expert (stable, so by token within an
+    expert): row r multiplies token lhs[r] by expert rhs[r]."""
+    rng = _rng(seed, STREAM_ROUTING)
+    picks = np.argsort(rng.random((T, E)), axis=1)[:, :top_k]      # top_k distinct experts per token
+    tok = np.repeat(np.arange(T, dtype=np.int64), top_k)
+    exp = picks.reshape(-1).astype(np.int64)
+    order = np.lexsort((tok, exp))
+    return tok[order].astype(np.int32), exp[order].astype(np.int32)
+
+
+# Mixtral-8x7B-shaped MoE feed-forward (the pages' MoE prefill case): 8 experts,
+# top-2 routing, (name, N, K) of each expert's matrices.
+MIXTRAL_EXPERTS = 8
+MIXTRAL_TOP_K = 2
+MIXTRAL_EXPERT_MATS = (
+    ("w1_gate", 14336, 4096),
+    ("w3_up", 14336, 4096),
+    ("w2_down", 4096, 14336),
+)
 
 # Llama-3.1-8B-shaped decode layer, (name, N, K): q, k, v, o, gate, up, down.
 LLAMA8B_LAYER = (

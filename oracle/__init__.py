@@ -147,6 +147,55 @@ def matmul_sampled(x, w_packed, scales, biases, M: int, N: int, K: int, idx_m, i
     return y_exact, y_bf16
 
 
+def gather_matmul(x, w_packed, scales, biases, lhs_indices, rhs_indices, N: int, K: int,
+                  group_size: int = 64, bits: int = 4, nthreads: int = 0):
+    """Expert-indexed matmul (MLX gather_qmm with the weights transposed, as in
+    the MoE prefill path of "epic: CUDA (MLX backend) prefill and decode
+    acceleration program", Diagnosis table and Phase 3): output row r is token
+    row x[lhs_indices[r]] times dequant(W[rhs_indices[r]])^T.
+
+    x uint16[T, K]; w_packed uint32[E, N, K*bits/32]; scales, biases
+    uint16[E, N, K/group_size].  Written out plainly: the rows that share an
+    expert are gathered and multiplied by that expert with ``matmul`` (the
+    pinned definition), then scattered back to their row positions.
+    Returns (y_exact float64[R, N], y_bf16 uint16[R, N])."""
+    x = _c(x, np.uint16)
+    lhs = np.asarray(lhs_indices, dtype=np.int64)
+    rhs = np.asarray(rhs_indices, dtype=np.int64)
+    R = lhs.size
+    y_exact = np.zeros((R, N), np.float64)
+    y_bf16 = np.zeros((R, N), np.uint16)
+    for e in np.unique(rhs):
+        rows = np.nonzero(rhs == e)[0]
+        xe = x[lhs[rows]]
+        ye, yb = matmul(xe, w_packed[e], scales[e], biases[e], rows.size, N, K, group_size, bits, nthreads)
+        y_exact[rows] = ye
+        y_bf16[rows] = yb
+    return y_exact, y_bf16
+
+
+def gather_matmul_sampled(x, w_packed, scales, biases, lhs_indices, rhs_indices, N: int, K: int, idx_r, idx_n,
+                          group_size: int = 64, bits: int = 4, nthreads: int = 0):
+    """``gather_matmul`` evaluated at the (idx_r[i], idx_n[i]) pairs only (for
+    full-size checks): each sampled row is its token times its expert, through
+    ``matmul_sampled``.  Returns (y_exact float64[S], y_bf16 uint16[S])."""
+    x = _c(x, np.uint16)
+    lhs = np.asarray(lhs_indices, dtype=np.int64)
+    rhs = np.asarray(rhs_indices, dtype=np.int64)
+    idx_r = np.asarray(idx_r, dtype=np.int64)
+    idx_n = np.asarray(idx_n, dtype=np.int64)
+    y_exact = np.zeros(idx_r.size, np.float64)
+    y_bf16 = np.zeros(idx_r.size, np.uint16)
+    for e in np.unique(rhs[idx_r]):
+        sel = np.nonzero(rhs[idx_r] == e)[0]
+        xe = x[lhs[idx_r[sel]]]                        # one x row per sample
+        ye, yb = matmul_sampled(xe, w_packed[e], scales[e], biases[e], sel.size, N, K,
+                                np.arange(sel.size), idx_n[sel], group_size, bits, nthreads)
+        y_exact[sel] = ye
+        y_bf16[sel] = yb
+    return y_exact, y_bf16
+
+
 def quantize(w, group_size: int = 64, bits: int = 4):
     """Min-max affine quantization; returns (w_packed, scales_bf16, biases_bf16)."""
     w = _c(w, np.float32)

@@ -338,3 +338,64 @@ def test_quantize_invariants(bits):
             assert np.all(err[inside] <= step / 2 * (1 + 1e-12))
     # the dequantized matrix is within a step of the original everywhere
     assert np.all(np.abs(deq - w) <= sd * 1.01 + 1e-6)
+
+
+# ---------------------------------------------------------------- expert-indexed (gather) pins
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_gather_brute_force_rational(bits):
+    """Every output row of the gather oracle equals the exact rational value of
+    its token row times its expert (brute force), rounded once to bf16."""
+    T, E, N, K = 3, 3, 3, 64
+    ew = synth.ExpertWeights(E, N, K, 70, bits=bits)
+    x = synth.make_x(T, K, 71)
+    lhs, rhs = synth.make_routing(T, E, 2, 72)
+    y_exact, y_bf16 = oracle.gather_matmul(x, ew.w_packed, ew.scales, ew.biases, lhs, rhs, N, K, bits=bits)
+    for r in range(lhs.size):
+        w = synth.QuantWeights(ew.w_packed[rhs[r]], ew.scales[rhs[r]], ew.biases[rhs[r]], N, K, 64, bits)
+        exact, ref_bits = brute_force(x[lhs[r]:lhs[r] + 1], w)
+        assert np.array_equal(y_bf16[r], ref_bits[0]), r
+        for n in range(N):
+            assert abs(Fraction(y_exact[r, n]) - exact[0][n]) <= abs(exact[0][n]) * Fraction(1, 2 ** 45)
+
+
+def test_gather_rows_follow_their_indices():
+    """Output rows depend only on their own (token, expert) pair: reordering the
+    index pairs reorders the rows, and a repeated pair repeats its row."""
+    T, E, N, K = 5, 4, 6, 128
+    ew = synth.ExpertWeights(E, N, K, 80)
+    x = synth.make_x(T, K, 81)
+    lhs, rhs = synth.make_routing(T, E, 2, 82)
+    _, y = oracle.gather_matmul(x, ew.w_packed, ew.scales, ew.biases, lhs, rhs, N, K)
+    perm = np.random.default_rng(0).permutation(lhs.size)
+    _, yp = oracle.gather_matmul(x, ew.w_packed, ew.scales, ew.biases, lhs[perm], rhs[perm], N, K)
+    assert np.array_equal(yp, y[perm])
+    lhs2, rhs2 = np.concatenate([lhs, lhs[:1]]), np.concatenate([rhs, rhs[:1]])
+    _, y2 = oracle.gather_matmul(x, ew.w_packed, ew.scales, ew.biases, lhs2, rhs2, N, K)
+    assert np.array_equal(y2[-1], y[0])
+
+
+def test_gather_sampled_matches_full():
+    T, E, N, K = 6, 3, 40, 256
+    ew = synth.ExpertWeights(E, N, K, 90)
+    x = synth.make_x(T, K, 91)
+    lhs, rhs = synth.make_routing(T, E, 2, 92)
+    ye, yb = oracle.gather_matmul(x, ew.w_packed, ew.scales, ew.biases, lhs, rhs, N, K)
+    rng = np.random.default_rng(1)
+    ir, inn = rng.integers(0, lhs.size, 200), rng.integers(0, N, 200)
+    se, sb = oracle.gather_matmul_sampled(x, ew.w_packed, ew.scales, ew.biases, lhs, rhs, N, K, ir, inn)
+    assert np.array_equal(sb, yb[ir, inn])
+    assert np.array_equal(se, ye[ir, inn])
+
+
+def test_routing_recipe():
+    T, E, k = 1000, 8, 2
+    lhs, rhs = synth.make_routing(T, E, k, 5)
+    assert lhs.dtype == np.int32 and rhs.dtype == np.int32 and lhs.size == T * k
+    assert np.all(np.diff(rhs) >= 0)                              # sorted by expert
+    for e in range(E):
+        toks = lhs[rhs == e]
+        assert np.all(np.diff(toks) > 0)                          # by token within an expert, no repeats
+    assert np.array_equal(np.bincount(lhs, minlength=T), np.full(T, k))   # every token k times
+    counts = np.bincount(rhs, minlength=E)
+    assert counts.min() > 0.8 * T * k / E and counts.max() < 1.2 * T * k / E   # roughly uniform
