@@ -19,6 +19,7 @@ AQ_ERR_UNSUPPORTED = 2
 AQ_ERR_ALIGNMENT = 3
 AQ_ERR_CUDA = 4
 AQ_ERR_TIMEOUT = 5
+AQ_ERR_BAD_INDEX = 6
 
 AQ_KERNEL_AUTO = 0
 AQ_KERNEL_QMV = 1
@@ -90,6 +91,11 @@ def load() -> ctypes.CDLL:
             lib.aq_chain_run_static.restype = I
             lib.aq_read_device_status.argtypes = [P]
             lib.aq_read_device_status.restype = I
+            lib.aq_gather_qmm_workspace_bytes.argtypes = [I64, I64, I64]
+            lib.aq_gather_qmm_workspace_bytes.restype = ctypes.c_size_t
+            lib.aq_gather_qmm_bf16.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I, I, P,
+                                               ctypes.c_size_t, P]
+            lib.aq_gather_qmm_bf16.restype = I
             lib.aq_version.argtypes = []
             lib.aq_version.restype = I
             _lib = lib
@@ -176,6 +182,16 @@ def aq_chain_run_static(descs, count, group_size, bits, stream) -> int:
     return load().aq_chain_run_static(descs, count, group_size, bits, stream)
 
 
+def aq_gather_qmm_workspace_bytes(R, K, E) -> int:
+    return load().aq_gather_qmm_workspace_bytes(R, K, E)
+
+
+def aq_gather_qmm_bf16(x, w_packed, scales, biases, lhs_indices, rhs_indices, y, R, T, N, K, E, group_size, bits,
+                       workspace, workspace_bytes, stream) -> int:
+    return load().aq_gather_qmm_bf16(x, w_packed, scales, biases, lhs_indices, rhs_indices, y, R, T, N, K, E,
+                                     group_size, bits, workspace, workspace_bytes, stream)
+
+
 def aq_read_device_status(stream) -> int:
     return load().aq_read_device_status(stream)
 
@@ -246,3 +262,33 @@ def pack_ref(codes, bits: int = 4):
     if st != AQ_OK:
         raise AqError(st, "aq_pack_ref")
     return wp
+
+
+def gather_qmm(x, w_packed, scales, biases, lhs_indices, rhs_indices, out=None, workspace=None, *,
+               group_size: int = 64, bits: int = 4, stream=None):
+    """Expert-indexed matmul for torch CUDA tensors: x bf16 [T, K]; w_packed int32
+    [E, N, K*bits/32]; scales/biases bf16 [E, N, K/group_size]; lhs/rhs int32 [R]
+    (rhs non-decreasing).  Returns y bf16 [R, N]; allocates the workspace if none
+    is given (a uint8 CUDA tensor of aq_gather_qmm_workspace_bytes)."""
+    import torch
+
+    T, K = x.shape
+    E, N = w_packed.shape[0], w_packed.shape[1]
+    R = lhs_indices.shape[0]
+    for name, t in (("x", x), ("w_packed", w_packed), ("scales", scales), ("biases", biases),
+                    ("lhs_indices", lhs_indices), ("rhs_indices", rhs_indices)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if out is None:
+        out = torch.empty((R, N), dtype=torch.bfloat16, device=x.device)
+    need = aq_gather_qmm_workspace_bytes(R, K, E)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    st = aq_gather_qmm_bf16(x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(), biases.data_ptr(),
+                            lhs_indices.data_ptr(), rhs_indices.data_ptr(), out.data_ptr(), R, T, N, K, E,
+                            group_size, bits, workspace.data_ptr(), workspace.numel(), stream.cuda_stream)
+    if st != AQ_OK:
+        raise AqError(st, "aq_gather_qmm_bf16")
+    return out

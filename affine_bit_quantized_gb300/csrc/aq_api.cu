@@ -297,6 +297,7 @@ const char *aq_status_string(aq_status status) {
     case AQ_ERR_ALIGNMENT: return "AQ_ERR_ALIGNMENT";
     case AQ_ERR_CUDA: return "AQ_ERR_CUDA";
     case AQ_ERR_TIMEOUT: return "AQ_ERR_TIMEOUT";
+    case AQ_ERR_BAD_INDEX: return "AQ_ERR_BAD_INDEX";
     }
     return "AQ_ERR_UNKNOWN";
 }
@@ -318,7 +319,52 @@ aq_status aq_read_device_status(void *stream) {
     if (st != AQ_OK) return st;
     st = record_cuda(cudaStreamSynchronize(cs));
     if (st != AQ_OK) return st;
-    return v == aq::AQ_DEVICE_STATUS_TIMEOUT ? AQ_ERR_TIMEOUT : AQ_OK;
+    if (v == aq::AQ_DEVICE_STATUS_TIMEOUT) return AQ_ERR_TIMEOUT;
+    if (v == aq::AQ_DEVICE_STATUS_BAD_INDEX) return AQ_ERR_BAD_INDEX;
+    return AQ_OK;
+}
+
+size_t aq_gather_qmm_workspace_bytes(int64_t R, int64_t K, int64_t E) {
+    if (R < 0 || K < 0 || E < 0 || R > kMaxDim || K > kMaxDim || E > aq::kMaxExperts) return 0;
+    return aq::gather_workspace_bytes(R, K, E);
+}
+
+aq_status aq_gather_qmm_bf16(const void *x, const uint32_t *w_packed, const void *scales, const void *biases,
+                             const int32_t *lhs_indices, const int32_t *rhs_indices, void *y, int64_t R, int64_t T,
+                             int64_t N, int64_t K, int64_t E, int group_size, int bits, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+    if ((bits != 4 && bits != 8) || group_size != 64) return AQ_ERR_UNSUPPORTED;
+    if (R < 0 || T < 1 || N < 1 || K < 1 || E < 1 || E > aq::kMaxExperts) return AQ_ERR_INVALID_ARG;
+    if (R > kMaxDim || T > kMaxDim || N > kMaxDim || K > kMaxDim || E * N > kMaxDim) return AQ_ERR_INVALID_ARG;
+    if (K % group_size) return AQ_ERR_INVALID_ARG;
+    if (K % 512) return AQ_ERR_UNSUPPORTED;   // the tensor-core kernel's K step
+    if (R == 0) return AQ_OK;
+    if (!x || !w_packed || !scales || !biases || !lhs_indices || !rhs_indices || !y || !workspace)
+        return AQ_ERR_INVALID_ARG;
+    if (workspace_bytes < aq::gather_workspace_bytes(R, K, E)) return AQ_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(w_packed, 16) || !aligned(scales, 16) || !aligned(biases, 16) ||
+        !aligned(lhs_indices, 4) || !aligned(rhs_indices, 4) || !aligned(y, 2) || !aligned(workspace, 128))
+        return AQ_ERR_ALIGNMENT;
+    aq::GatherArgs g;
+    g.x = x;
+    g.w = w_packed;
+    g.scales = static_cast<const uint16_t *>(scales);
+    g.biases = static_cast<const uint16_t *>(biases);
+    g.lhs = lhs_indices;
+    g.rhs = rhs_indices;
+    g.y = y;
+    g.R = R;
+    g.T = T;
+    g.N = N;
+    g.K = K;
+    g.E = E;
+    g.bits = bits;
+    g.workspace = workspace;
+    g.stream = static_cast<cudaStream_t>(stream);
+    g.timeout_ns = kTimeoutNs;
+    aq_status st = record_cuda(status_ptr(&g.status));
+    if (st != AQ_OK) return st;
+    return record_cuda(aq::launch_gather_qmm(g));
 }
 
 int aq_version(void) { return 100; }

@@ -29,6 +29,7 @@ struct MatmulArgs {
 // Values of the device status word.
 constexpr int AQ_DEVICE_STATUS_OK = 0;
 constexpr int AQ_DEVICE_STATUS_TIMEOUT = 5;
+constexpr int AQ_DEVICE_STATUS_BAD_INDEX = 6;
 
 // Weight-streaming kernel for up to 16 rows of x (qmv.cu).  Requires
 // 1 <= M <= 16, N >= 1, K >= 64.
@@ -47,6 +48,27 @@ cudaError_t launch_qmv_tma(const MatmulArgs &a);
 // aligned scales/biases.
 bool qmm_supported(const MatmulArgs &a);
 cudaError_t launch_qmm(const MatmulArgs &a);
+
+// Expert-indexed matmul (qmm.cu): row r of y = x[lhs[r]] . dequant(W[rhs[r]])^T,
+// rows grouped by expert (rhs non-decreasing), through a plan and a gathered
+// copy of x in the caller's workspace and the tensor-core kernel.
+constexpr int kMaxExperts = 1024;
+struct GatherArgs {
+    const void *x;           // bf16 [T, K]
+    const uint32_t *w;       // uint32 [E, N, K*bits/32]
+    const uint16_t *scales;  // bf16 bits [E, N, K/64]
+    const uint16_t *biases;  // bf16 bits [E, N, K/64]
+    const int *lhs, *rhs;    // int32 [R]
+    void *y;                 // bf16 [R, N]
+    int64_t R, T, N, K, E;
+    int bits;
+    void *workspace;         // gather_workspace_bytes(R, K, E), 128-byte aligned
+    cudaStream_t stream;
+    int *status;
+    uint64_t timeout_ns;
+};
+size_t gather_workspace_bytes(int64_t R, int64_t K, int64_t E);
+cudaError_t launch_gather_qmm(const GatherArgs &g);
 
 // Chains of decode matmuls in one persistent launch (qmv_chain.cu).
 size_t chain_workspace_bytes(int count);

@@ -91,6 +91,7 @@ static_assert((kMaxSplit - 1) * Cfg<4>::kTileM * (kTileN / kMaxSplit) * 4 <= Cfg
               "split-K receive slots");
 
 constexpr uint32_t kTmemCols = 512;
+constexpr int kPlanHeaderInts = 32;    // tile count, then the tiles (int4 each) from byte 128
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -258,11 +259,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-template <int BITS>
+// GROUPED (expert-indexed matmul): x holds the rows gathered in expert order,
+// W, scales and biases are E matrices stacked along N, and `plan` lists the
+// work tiles {expert, first row, rows} (see gather_plan_kernel); CTA row
+// blockIdx.y takes tile blockIdx.y and exits at once if there is none.
+template <int BITS, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1)
 qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
            const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_b,
-           __nv_bfloat16 *__restrict__ y, int M, int N, int K, unsigned long long timeout_ns, int *status) {
+           __nv_bfloat16 *__restrict__ y, int M, int N, int K, unsigned long long timeout_ns, int *status,
+           const int *__restrict__ plan) {
     using C = Cfg<BITS>;
     constexpr int kTileM = C::kTileM, kATileBytes = C::kATileBytes, kConvStageBytes = C::kConvStageBytes;
     constexpr int kRawXBytes = C::kRawXBytes, kRawStageBytes = C::kRawStageBytes;
@@ -286,7 +292,16 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * kTileN;
-    const int m0 = blockIdx.y * kTileM;
+    int m0 = blockIdx.y * kTileM;   // first row of x (and of y) of the tile
+    int m_end = M;                  // rows from m_end on are not this tile's
+    int wrow0 = n0;                 // first row of W (in the stacked experts: expert * N + n0)
+    if (GROUPED) {
+        if ((int)blockIdx.y >= __ldg(plan)) return;   // no tile: nothing set up yet
+        const int4 t = __ldg(reinterpret_cast<const int4 *>(plan + kPlanHeaderInts) + blockIdx.y);
+        m0 = t.y;
+        m_end = t.y + t.z;
+        wrow0 = t.x * N + n0;
+    }
     // split K: the gridDim.z CTAs of a cluster each take a contiguous share of
     // the K/512 blocks of 8 groups and add their partial tiles through
     // distributed shared memory at the end
@@ -343,7 +358,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     bool go = false;   // this warp holds final accumulators to write out
     // 16 fp32 values of row m, columns n..n+15 -> bf16 y
     auto store_row16 = [&](const float (&a)[16], int m_, int n) {
-        if (m_ >= M) return;
+        if (m_ >= m_end) return;
         __nv_bfloat16 *yp = y + (int64_t)m_ * N + n;
         if (n + 16 <= N && (((uintptr_t)yp) & 15) == 0) {
 #pragma unroll
@@ -363,7 +378,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     };
     // 32 fp32 values of row m, columns n..n+31 -> bf16 y
     auto store_row32 = [&](const uint32_t (&r)[32], int m_, int n) {
-        if (m_ >= M) return;
+        if (m_ >= m_end) return;
         __nv_bfloat16 *yp = y + (int64_t)m_ * N + n;
         if (n + 32 <= N && (((uintptr_t)yp) & 15) == 0) {
 #pragma unroll
@@ -397,8 +412,8 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                     }
                     const uint32_t dst = base + kOffSB + ss * 2 * kSBBytes;
                     mbar_expect_tx(sb_full(ss), 2 * kSBBytes);
-                    tma_load_2d(dst, &tm_s, g0 + j * kSBGroups, n0, sb_full(ss));
-                    tma_load_2d(dst + kSBBytes, &tm_b, g0 + j * kSBGroups, n0, sb_full(ss));
+                    tma_load_2d(dst, &tm_s, g0 + j * kSBGroups, wrow0, sb_full(ss));
+                    tma_load_2d(dst + kSBBytes, &tm_b, g0 + j * kSBGroups, wrow0, sb_full(ss));
                     issued_sb = j + 1;
                 }
                 if (i >= kRawStages && !mbar_wait(raw_empty(rs), ((i / kRawStages) - 1) & 1, deadline, abort_flag)) {
@@ -408,7 +423,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 const uint32_t dst = base + kOffRaw + rs * kRawStageBytes;
                 mbar_expect_tx(raw_full(rs), kRawStageBytes);
                 tma_load_2d(dst, &tm_x, (g0 + i) * kGroup, m0, raw_full(rs));
-                tma_load_2d(dst + kRawXBytes, &tm_w, (g0 + i) * C::kRowWords, n0, raw_full(rs));
+                tma_load_2d(dst + kRawXBytes, &tm_w, (g0 + i) * C::kRowWords, wrow0, raw_full(rs));
                 issued_raw = i + 1;
             }
             if (!ok) {
@@ -669,6 +684,7 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *gaddr, uint
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_attr_done[2][kMaxDevices];
+std::atomic<int> g_attr_done_grouped[2][kMaxDevices];
 std::atomic<int> g_sms[kMaxDevices];
 // clusters of 2, 4, 8 CTAs that can be resident at once, per code width (0: not yet asked; -1: none)
 std::atomic<int> g_max_clusters[2][3][kMaxDevices];
@@ -686,7 +702,7 @@ cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev) {
     using C = Cfg<BITS>;
     const int bi = BITS == 8 ? 1 : 0;
     if (!g_attr_done[bi][dev].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(qmm_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(qmm_kernel<BITS, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
         if (e != cudaSuccess) return e;
         g_attr_done[bi][dev].store(1, std::memory_order_release);
@@ -739,7 +755,7 @@ cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev) {
                 ca.val.clusterDim.z = (unsigned)S;
                 q.attrs = &ca;
                 q.numAttrs = 1;
-                if (cudaOccupancyMaxActiveClusters(&n, qmm_kernel<BITS>, &q) != cudaSuccess || n < 1) {
+                if (cudaOccupancyMaxActiveClusters(&n, qmm_kernel<BITS, false>, &q) != cudaSuccess || n < 1) {
                     cudaGetLastError();   // the query's error is not the caller's
                     n = -1;
                 }
@@ -758,8 +774,8 @@ cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev) {
     }
     cfg.attrs = attr;
     cfg.numAttrs = (unsigned)na;
-    return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(a.y), M, N, K,
-                              (unsigned long long)a.timeout_ns, a.status);
+    return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS, false>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(a.y), M,
+                              N, K, (unsigned long long)a.timeout_ns, a.status, (const int *)nullptr);
 }
 }  // namespace
 
@@ -769,6 +785,136 @@ cudaError_t launch_qmm(const MatmulArgs &a) {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     return a.bits == 8 ? launch_qmm_bits<8>(a, dev) : launch_qmm_bits<4>(a, dev);
+}
+
+// ---------------------------------------------------------------- expert-indexed matmul
+
+namespace {
+
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanMinTileM = 128;   // the smaller x tile of the two code widths (bounds the plan)
+
+// One CTA: checks the indices (token in [0, T), expert in [0, E), experts
+// non-decreasing), counts the rows of every expert and writes the work tiles
+// {expert, first row, rows, 0} of at most tile_m rows each, in expert order,
+// after the tile count.  Bad indices: a count of 0 (the matmul then does
+// nothing) and AQ_DEVICE_STATUS_BAD_INDEX in the status word.
+__global__ void __launch_bounds__(kPlanThreads, 1)
+gather_plan_kernel(const int *__restrict__ lhs, const int *__restrict__ rhs, int R, int T, int E, int tile_m,
+                   int *__restrict__ plan, int *status) {
+    __shared__ int cnt[kMaxExperts];
+    __shared__ int bad;
+    const int tid = threadIdx.x;
+    for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
+    if (tid == 0) bad = 0;
+    __syncthreads();
+    for (int r = tid; r < R; r += blockDim.x) {
+        const int l = __ldg(lhs + r), e = __ldg(rhs + r);
+        if (l < 0 || l >= T || e < 0 || e >= E || (r > 0 && __ldg(rhs + r - 1) > e))
+            bad = 1;
+        else
+            atomicAdd(&cnt[e], 1);
+    }
+    __syncthreads();
+    if (bad) {
+        if (tid == 0) {
+            plan[0] = 0;
+            atomicExch(status, AQ_DEVICE_STATUS_BAD_INDEX);
+        }
+        return;
+    }
+    __shared__ int tile_off[kMaxExperts], row_off[kMaxExperts];
+    if (tid == 0) {
+        int tiles = 0, rows = 0;
+        for (int e = 0; e < E; ++e) {
+            tile_off[e] = tiles;
+            row_off[e] = rows;
+            tiles += (cnt[e] + tile_m - 1) / tile_m;
+            rows += cnt[e];
+        }
+        plan[0] = tiles;
+    }
+    __syncthreads();
+    int4 *tiles = reinterpret_cast<int4 *>(plan + kPlanHeaderInts);
+    for (int e = tid; e < E; e += blockDim.x)
+        for (int i = 0; i * tile_m < cnt[e]; ++i)
+            tiles[tile_off[e] + i] = make_int4(e, row_off[e] + i * tile_m, min(tile_m, cnt[e] - i * tile_m), 0);
+}
+
+// x rows in row order of the matmul: xg[r] = x[lhs[r]] (zeros for an index out
+// of range, which the plan kernel reports), 16 bytes per thread and step.
+__global__ void gather_rows_kernel(const uint4 *__restrict__ x, const int *__restrict__ lhs, uint4 *__restrict__ xg,
+                                   int R, int T, int row_vecs) {
+    const int64_t total = (int64_t)R * row_vecs;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / row_vecs, c = i - r * row_vecs;
+        const int l = __ldg(lhs + r);
+        xg[i] = (l >= 0 && l < T) ? __ldg(x + (int64_t)l * row_vecs + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+int64_t plan_max_tiles(int64_t R, int64_t E) { return (R + kPlanMinTileM - 1) / kPlanMinTileM + E; }
+int64_t plan_bytes(int64_t R, int64_t E) { return (kPlanHeaderInts * 4 + 16 * plan_max_tiles(R, E) + 127) & ~int64_t(127); }
+
+template <int BITS>
+cudaError_t launch_gather_bits(const GatherArgs &g, int dev, int sms) {
+    using C = Cfg<BITS>;
+    const int bi = BITS == 8 ? 1 : 0;
+    if (!g_attr_done_grouped[bi][dev].load(std::memory_order_acquire)) {
+        cudaError_t e = cudaFuncSetAttribute(qmm_kernel<BITS, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        g_attr_done_grouped[bi][dev].store(1, std::memory_order_release);
+    }
+    const int R = (int)g.R, N = (int)g.N, K = (int)g.K, E = (int)g.E, G = K / 64;
+    int *plan = static_cast<int *>(g.workspace);
+    void *xg = static_cast<uint8_t *>(g.workspace) + plan_bytes(g.R, g.E);
+    gather_plan_kernel<<<1, kPlanThreads, 0, g.stream>>>(g.lhs, g.rhs, R, (int)g.T, E, C::kTileM, plan, g.status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    gather_rows_kernel<<<sms * 4, 256, 0, g.stream>>>(static_cast<const uint4 *>(g.x), g.lhs, static_cast<uint4 *>(xg),
+                                                       R, (int)g.T, K / 8);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    CUtensorMap tx, tw, ts, tb;
+    if (!encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xg, (uint64_t)K, (uint64_t)R, (uint64_t)K * 2, kGroup,
+                   C::kTileM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, g.w, (uint64_t)K * BITS / 32, (uint64_t)E * N,
+                   (uint64_t)K * BITS / 8, C::kRowWords, kTileN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, g.scales, (uint64_t)G, (uint64_t)E * N, (uint64_t)G * 2,
+                   kSBGroups, kTileN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, g.biases, (uint64_t)G, (uint64_t)E * N, (uint64_t)G * 2,
+                   kSBGroups, kTileN, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    const int64_t max_tiles = (g.R + C::kTileM - 1) / C::kTileM + g.E;
+    cfg.gridDim = dim3((unsigned)((N + kTileN - 1) / kTileN), (unsigned)max_tiles, 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = g.stream;
+    return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS, true>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(g.y), R, N,
+                              K, (unsigned long long)g.timeout_ns, g.status, (const int *)plan);
+}
+
+}  // namespace
+
+size_t gather_workspace_bytes(int64_t R, int64_t K, int64_t E) {
+    return (size_t)(plan_bytes(R, E) + R * K * 2);
+}
+
+cudaError_t launch_gather_qmm(const GatherArgs &g) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    int sms = g_sms[dev].load(std::memory_order_relaxed);
+    if (sms == 0) {
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        g_sms[dev].store(sms, std::memory_order_relaxed);
+    }
+    if (!encode_fn()) return cudaErrorNotSupported;
+    return g.bits == 8 ? launch_gather_bits<8>(g, dev, sms) : launch_gather_bits<4>(g, dev, sms);
 }
 
 }  // namespace aq

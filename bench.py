@@ -584,6 +584,38 @@ def main():
                             "frac_of_bf16_sustained": round(tf / bf16_sus, 4)}
             del ws
 
+    # ---- MoE prefill (expert-indexed matmul): Mixtral-8x7B-shaped experts, 2048 tokens routed
+    # top-2 over 8 experts (4096 rows), one call = plan + row gather + tensor-core matmul
+    moe = {}
+    T_moe = 2048
+    lhs, rhs = synth.make_routing(T_moe, synth.MIXTRAL_EXPERTS, synth.MIXTRAL_TOP_K, synth.seed_for(6, 0, 9))
+    lt = torch.from_numpy(lhs).to(dev)
+    rt = torch.from_numpy(rhs).to(dev)
+    R_moe = int(lhs.size)
+    for j, (name, N, K) in enumerate(synth.MIXTRAL_EXPERT_MATS):
+        ew = synth.ExpertWeights(synth.MIXTRAL_EXPERTS, N, K, synth.seed_for(6, 0, 16 * j))
+        wt = torch.from_numpy(ew.w_packed.view(np.int32)).to(dev)
+        st = torch.from_numpy(ew.scales.view(np.int16)).to(dev)
+        bt = torch.from_numpy(ew.biases.view(np.int16)).to(dev)
+        xm = torch.from_numpy(synth.make_x(T_moe, K, synth.seed_for(6, 0, 8)).view(np.int16)).to(dev)
+        ym = torch.empty((R_moe, N), dtype=torch.int16, device=dev)
+        nws = aq.aq_gather_qmm_workspace_bytes(R_moe, K, synth.MIXTRAL_EXPERTS)
+        wsm = torch.empty(nws, dtype=torch.uint8, device=dev)
+
+        def mlaunch(i, wt=wt, st=st, bt=bt, xm=xm, ym=ym, wsm=wsm, N=N, K=K):
+            rc = lib.aq_gather_qmm_bf16(xm.data_ptr(), wt.data_ptr(), st.data_ptr(), bt.data_ptr(), lt.data_ptr(),
+                                        rt.data_ptr(), ym.data_ptr(), R_moe, T_moe, N, K, synth.MIXTRAL_EXPERTS, 64,
+                                        4, wsm.data_ptr(), wsm.numel(), cur.cuda_stream)
+            if rc != aq.AQ_OK:
+                raise aq.AqError(rc, "aq_gather_qmm_bf16")
+
+        us = time_calls(mlaunch, 4)
+        tf = 2.0 * R_moe * N * K / (us * 1e-6) / 1e12
+        moe[name] = {"tokens": T_moe, "experts": synth.MIXTRAL_EXPERTS, "top_k": synth.MIXTRAL_TOP_K, "rows": R_moe,
+                     "N": N, "K": K, "us_per_call": round(us, 2), "tflops": round(tf, 1),
+                     "frac_of_bf16_burst": round(tf / bf16_peak, 4)}
+        del wt, st, bt, ew, wsm
+
     # ---- CPU baseline: the oracle on two layers of the same workload, host cores
     cpu = None
     if cpu_layers:
@@ -648,6 +680,7 @@ def main():
         "per_matrix": per_matrix,
         "small_batch": small_batch,
         "eight_bit": eight_bit,
+        "moe_prefill": moe,
         "qmm": qmm,
     }
     if cpu:

@@ -52,7 +52,9 @@ typedef enum aq_status {
     AQ_ERR_UNSUPPORTED = 2, /* bits or group_size outside what this build implements */
     AQ_ERR_ALIGNMENT = 3,   /* a pointer without the alignment stated below */
     AQ_ERR_CUDA = 4,        /* the CUDA runtime refused the launch: see aq_last_cuda_error() */
-    AQ_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (see aq_read_device_status) */
+    AQ_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up (see aq_read_device_status) */
+    AQ_ERR_BAD_INDEX = 6    /* aq_gather_qmm_bf16 met an index out of range or experts out of
+                               order (see aq_read_device_status) */
 } aq_status;
 
 /* Kernel choice for aq_matmul_bf16_ex.  AUTO picks by M exactly as
@@ -213,7 +215,8 @@ aq_status aq_chain_run(const aq_chain_plan *plan, void *stream);
  * framework that owns the whole device memory pool and gives plugins no
  * workspace, or a serving loop that must not reach an allocator after
  * start-up (an allocation can synchronize the device, and can fail once
- * memory is fragmented).  No counterpart in the paper.
+ * memory is fragmented).  An addition of this library, not a call the pages
+ * describe.
  *
  * Same descriptors, semantics and limits as aq_chain_prepare + aq_chain_run,
  * at most 256 matmuls per call (a longer chain returns AQ_ERR_INVALID_ARG and
@@ -234,6 +237,44 @@ aq_status aq_chain_run_static(const aq_matmul_desc *descs, int count, int group_
 /* Static, NUL-terminated name of a status code. */
 const char *aq_status_string(aq_status status);
 
+/*
+ * Expert-indexed matmul for mixture-of-experts prefill: MLX's gather_qmm with
+ * transposed weights, the grouped-GEMM path behind the MoE prefill gap of
+ * "epic: CUDA (MLX backend) prefill and decode acceleration program"
+ * (Diagnosis table, MoE prefill row; Phase 3).  For r in [0, R):
+ *
+ *     y[r, :] = x[lhs_indices[r], :] . dequant(W_e)^T,   e = rhs_indices[r]
+ *
+ * with W_e, its scales and biases the e-th of E matrices stacked in
+ * w_packed [E, N, K*bits/32], scales and biases [E, N, K/group_size], each as
+ * in aq_matmul_bf16.
+ *
+ *   x            bf16 [T, K], device; lhs_indices int32 [R], device, in [0, T)
+ *   rhs_indices  int32 [R], device, in [0, E) and non-decreasing: the rows of
+ *                an expert are contiguous (sort the (token, expert) pairs by
+ *                expert first, as a MoE layer does before its experts)
+ *   y            bf16 [R, N], device, written
+ *   R >= 0 (0 launches nothing), T >= 1, N >= 1, 1 <= E <= 1024,
+ *   K a multiple of 512; group_size 64; bits 4 or 8.
+ *   workspace    device, 128-byte aligned, at least
+ *                aq_gather_qmm_workspace_bytes(R, K, E) bytes, owned by the
+ *                caller (the work plan and x's rows in row order, R*K*2 bytes)
+ *   Alignment    x, w_packed, scales, biases 16-byte aligned; indices 4-byte;
+ *                y 2-byte (AQ_ERR_ALIGNMENT otherwise).
+ * Runs as three launches on `stream`: a plan of the work tiles per expert
+ * (which also checks the indices), the gather of x's rows, and the
+ * tensor-core kernel over the tiles.  Indices out of range or out of order
+ * are reported by aq_read_device_status() as AQ_ERR_BAD_INDEX and y is not
+ * written.  Numerics as aq_matmul_bf16's tensor-core path (|x| < 65504).
+ * Asynchronous; allocates nothing; deterministic.
+ */
+size_t aq_gather_qmm_workspace_bytes(int64_t R, int64_t K, int64_t E);
+aq_status aq_gather_qmm_bf16(const void *x, const uint32_t *w_packed, const void *scales,
+                             const void *biases, const int32_t *lhs_indices,
+                             const int32_t *rhs_indices, void *y, int64_t R, int64_t T,
+                             int64_t N, int64_t K, int64_t E, int group_size, int bits,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
 /* Text of the last CUDA runtime error seen by an entry point on this host
  * thread ("" if none).  Valid until the next call on this thread. */
 const char *aq_last_cuda_error(void);
@@ -241,7 +282,9 @@ const char *aq_last_cuda_error(void);
 /* Waits for `stream` to finish, then reads and clears the library's device
  * status word on the current device: AQ_ERR_TIMEOUT if a bounded wait inside
  * a kernel expired since the last read (that kernel's output is then not
- * valid), else AQ_OK; AQ_ERR_CUDA if the synchronization or copy failed.
+ * valid), AQ_ERR_BAD_INDEX if an aq_gather_qmm_bf16 call found invalid
+ * indices (it then wrote nothing to y), else AQ_OK; AQ_ERR_CUDA if the
+ * synchronization or copy failed.
  * A debugging call: it synchronizes the host with the stream. */
 aq_status aq_read_device_status(void *stream);
 

@@ -29,7 +29,7 @@ def test_exports_every_declared_symbol():
 
 def test_status_strings():
     for code, name in ((0, "AQ_OK"), (1, "AQ_ERR_INVALID_ARG"), (2, "AQ_ERR_UNSUPPORTED"), (3, "AQ_ERR_ALIGNMENT"),
-                       (4, "AQ_ERR_CUDA"), (5, "AQ_ERR_TIMEOUT")):
+                       (4, "AQ_ERR_CUDA"), (5, "AQ_ERR_TIMEOUT"), (6, "AQ_ERR_BAD_INDEX")):
         assert aq.status_string(code) == name
     assert aq.last_cuda_error() == ""
 
@@ -141,3 +141,44 @@ def test_chain_prepare_rejects_unknown_flags():
     arr = (aq.MatmulDesc * 1)(_desc(flags=2))
     plan = aq.ChainPlan()
     assert aq.aq_chain_prepare(arr, 1, 64, 4, A, aq.aq_chain_workspace_bytes(1), plan) == aq.AQ_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------- expert-indexed matmul: validation
+
+def _gather_call(**kw):
+    d = dict(x=A, w=A, s=A, b=A, lhs=A, rhs=A, y=A, R=64, T=32, N=256, K=512, E=4, group_size=64, bits=4,
+             ws=A, ws_bytes=None)
+    d.update(kw)
+    if d["ws_bytes"] is None:
+        d["ws_bytes"] = aq.aq_gather_qmm_workspace_bytes(d["R"], d["K"], d["E"])
+    return aq.aq_gather_qmm_bf16(d["x"], d["w"], d["s"], d["b"], d["lhs"], d["rhs"], d["y"], d["R"], d["T"], d["N"],
+                                 d["K"], d["E"], d["group_size"], d["bits"], d["ws"], d["ws_bytes"], None)
+
+
+def test_gather_workspace_bytes():
+    # plan header (128) + one 16-byte tile per 128 rows plus one per expert, rounded to 128, then R*K*2
+    assert aq.aq_gather_qmm_workspace_bytes(4096, 4096, 8) == 128 * ((128 + 16 * (32 + 8) + 127) // 128) + 4096 * 4096 * 2
+    assert aq.aq_gather_qmm_workspace_bytes(0, 4096, 8) == 128 * ((128 + 16 * 8 + 127) // 128)
+    assert aq.aq_gather_qmm_workspace_bytes(1, 512, 2000) == 0          # more experts than supported
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(bits=3), aq.AQ_ERR_UNSUPPORTED),
+    (dict(group_size=32), aq.AQ_ERR_UNSUPPORTED),
+    (dict(K=576), aq.AQ_ERR_UNSUPPORTED),          # not a multiple of 512 (the tensor-core K step)
+    (dict(K=100), aq.AQ_ERR_INVALID_ARG),          # not a multiple of the group size
+    (dict(E=0), aq.AQ_ERR_INVALID_ARG),
+    (dict(E=1025), aq.AQ_ERR_INVALID_ARG),
+    (dict(T=0), aq.AQ_ERR_INVALID_ARG),
+    (dict(R=-1), aq.AQ_ERR_INVALID_ARG),
+    (dict(lhs=None), aq.AQ_ERR_INVALID_ARG),
+    (dict(ws=None), aq.AQ_ERR_INVALID_ARG),
+    (dict(ws_bytes=1000), aq.AQ_ERR_INVALID_ARG),  # workspace too small
+    (dict(x=A + 8), aq.AQ_ERR_ALIGNMENT),
+    (dict(s=A + 2), aq.AQ_ERR_ALIGNMENT),
+    (dict(rhs=A + 2), aq.AQ_ERR_ALIGNMENT),
+    (dict(ws=A + 64), aq.AQ_ERR_ALIGNMENT),
+    (dict(R=0, x=None, y=None), aq.AQ_OK),         # no rows: nothing launched
+])
+def test_gather_validation(kw, expect):
+    assert _gather_call(**kw) == expect
