@@ -119,6 +119,31 @@ class ExpertWeights:
         self.E, self.N, self.K, self.group_size, self.bits = E, N, K, group_size, bits
 
 
+@dataclasses.dataclass
+class NVFP4Weights:
+    """NVFP4 weights: ``w_packed`` uint32[N, K/8] of FP4 E2M1 codes (lowest nibble
+    = lowest k), ``scales`` uint8[N, K/16] of FP8 E4M3 block scales, and one fp32
+    ``global_scale``."""
+
+    w_packed: np.ndarray
+    scales: np.ndarray
+    global_scale: float
+    N: int
+    K: int
+
+
+def make_nvfp4_weights(N: int, K: int, seed: int) -> NVFP4Weights:
+    """Synthetic NVFP4 weights: every E2M1 code uniform over its 16 encodings,
+    block scales uniform over the E4M3 encodings 0x48..0x7E (4 to 448, all
+    finite and normal), global scale 2^-13 (weights of magnitude ~0.01-0.3)."""
+    if K % 16:
+        raise ValueError("K must be a multiple of 16")
+    rng = _rng(seed, STREAM_WEIGHTS)
+    w_packed = rng.integers(0, 1 << 32, size=(N, K // 8), dtype=np.uint32)
+    scales = rng.integers(0x48, 0x7F, size=(N, K // 16), dtype=np.uint8)
+    return NVFP4Weights(w_packed, scales, 2.0 ** -13, N, K)
+
+
 def make_routing(T: int, E: int, top_k: int, seed: int):
     """Synthetic top-k routing of T tokens over E experts: every token picks
     top_k distinct experts uniformly at random.  Returns int32 arrays

@@ -19,6 +19,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "aq_oracle.c")
+_SRCS = (_SRC, os.path.join(_HERE, "nvfp4_oracle.c"))
 _LIB = os.path.join(_HERE, "liboracle_aq.so")
 _lock = threading.Lock()
 _lib = None
@@ -26,11 +27,11 @@ _lib = None
 
 def build(force: bool = False) -> str:
     """Compile the oracle into ``liboracle_aq.so`` (gcc, -O2, no fast-math)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    if force or not os.path.exists(_LIB) or any(os.path.getmtime(_LIB) < os.path.getmtime(s) for s in _SRCS):
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.run(
             ["gcc", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fPIC", "-shared",
-             "-std=c11", "-o", tmp, _SRC, "-lm", "-lpthread"],
+             "-std=c11", "-o", tmp, *_SRCS, "-lm", "-lpthread"],
             check=True,
         )
         os.replace(tmp, _LIB)
@@ -57,6 +58,15 @@ def _load():
             lib.aqo_matmul.argtypes = [P, P, P, P, I64, I64, I64, I, I, P, P, I]
             lib.aqo_matmul_sampled.argtypes = [P, P, P, P, I64, I64, I64, I, I, P, P, I64, P, P, I]
             lib.aqo_quantize.argtypes = [P, I64, I64, I, I, P, P, P]
+            D = ctypes.c_double
+            F = ctypes.c_float
+            lib.aqo_e2m1_to_double.argtypes = [ctypes.c_uint]
+            lib.aqo_e2m1_to_double.restype = D
+            lib.aqo_e4m3_to_double.argtypes = [ctypes.c_uint]
+            lib.aqo_e4m3_to_double.restype = D
+            lib.aqo_nvfp4_dequant.argtypes = [P, P, F, I64, I64, P]
+            lib.aqo_nvfp4_matmul.argtypes = [P, P, P, F, I64, I64, I64, P, P]
+            lib.aqo_nvfp4_matmul_sampled.argtypes = [P, P, P, F, I64, I64, I64, P, P, I64, P, P]
             lib.aqo_default_threads.argtypes = []
             for f in ("aqo_unpack", "aqo_pack", "aqo_dequant", "aqo_matmul", "aqo_matmul_sampled",
                       "aqo_quantize", "aqo_default_threads"):
@@ -193,6 +203,53 @@ def gather_matmul_sampled(x, w_packed, scales, biases, lhs_indices, rhs_indices,
                                 np.arange(sel.size), idx_n[sel], group_size, bits, nthreads)
         y_exact[sel] = ye
         y_bf16[sel] = yb
+    return y_exact, y_bf16
+
+
+# ---------------------------------------------------------------- NVFP4 (nvfp4_oracle.c)
+
+def e2m1_to_double(code: int) -> float:
+    """Value of one FP4 E2M1 code (0..15)."""
+    return _load().aqo_e2m1_to_double(int(code))
+
+
+def e4m3_to_double(byte: int) -> float:
+    """Value of one FP8 E4M3 byte (NaN for S.1111.111)."""
+    return _load().aqo_e4m3_to_double(int(byte))
+
+
+def nvfp4_dequant(w_packed, scales, global_scale: float, N: int, K: int) -> np.ndarray:
+    """w[n,k] = global * e4m3(scales[n, k/16]) * e2m1(q[n,k]) as float64[N, K]."""
+    w_packed, scales = _c(w_packed, np.uint32), _c(scales, np.uint8)
+    out = np.empty((N, K), np.float64)
+    if _load().aqo_nvfp4_dequant(_ptr(w_packed), _ptr(scales), float(global_scale), N, K, _ptr(out)):
+        raise ValueError("oracle nvfp4 dequant failed")
+    return out
+
+
+def nvfp4_matmul(x, w_packed, scales, global_scale: float, M: int, N: int, K: int):
+    """y = x . w^T for NVFP4 weights (group 16, e4m3 scales, fp32 tensor scale).
+    Returns (y_exact float64[M,N], y_bf16 uint16[M,N])."""
+    x = _c(x, np.uint16)
+    w_packed, scales = _c(w_packed, np.uint32), _c(scales, np.uint8)
+    y_exact = np.empty((M, N), np.float64)
+    y_bf16 = np.empty((M, N), np.uint16)
+    if _load().aqo_nvfp4_matmul(_ptr(x), _ptr(w_packed), _ptr(scales), float(global_scale), M, N, K,
+                                _ptr(y_exact), _ptr(y_bf16)):
+        raise ValueError("oracle nvfp4 matmul failed")
+    return y_exact, y_bf16
+
+
+def nvfp4_matmul_sampled(x, w_packed, scales, global_scale: float, M: int, N: int, K: int, idx_m, idx_n):
+    """``nvfp4_matmul`` at the (idx_m[i], idx_n[i]) pairs only."""
+    x = _c(x, np.uint16)
+    w_packed, scales = _c(w_packed, np.uint32), _c(scales, np.uint8)
+    idx_m, idx_n = _c(idx_m, np.int64), _c(idx_n, np.int64)
+    y_exact = np.empty(idx_m.size, np.float64)
+    y_bf16 = np.empty(idx_m.size, np.uint16)
+    if _load().aqo_nvfp4_matmul_sampled(_ptr(x), _ptr(w_packed), _ptr(scales), float(global_scale), M, N, K,
+                                        _ptr(idx_m), _ptr(idx_n), idx_m.size, _ptr(y_exact), _ptr(y_bf16)):
+        raise ValueError("oracle nvfp4 sampled matmul failed")
     return y_exact, y_bf16
 
 

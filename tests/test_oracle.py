@@ -399,3 +399,81 @@ def test_routing_recipe():
     assert np.array_equal(np.bincount(lhs, minlength=T), np.full(T, k))   # every token k times
     counts = np.bincount(rhs, minlength=E)
     assert counts.min() > 0.8 * T * k / E and counts.max() < 1.2 * T * k / E   # roughly uniform
+
+
+# ---------------------------------------------------------------- NVFP4 pins
+
+def test_e2m1_values_fixture():
+    rows = [l.split() for l in open(os.path.join(GOLDEN, "e2m1_values.txt")) if l.strip() and not l.startswith("#")]
+    assert len(rows) == 16
+    for code, value in rows:
+        got = oracle.e2m1_to_double(int(code, 16))
+        want = float(value)
+        assert got == want and np.signbit(got) == np.signbit(want), (code, got, want)
+
+
+def test_e4m3_matches_torch_float8():
+    """Every FP8 E4M3 byte decodes as torch's float8_e4m3fn does (an independent
+    implementation of the same format), NaN included."""
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_to_double(b) for b in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert oracle.e4m3_to_double(0x38) == 1.0 and oracle.e4m3_to_double(0x7E) == 448.0
+    assert oracle.e4m3_to_double(0x01) == 2.0 ** -9 and oracle.e4m3_to_double(0x08) == 2.0 ** -6
+
+
+def brute_force_nvfp4(x, w):
+    """Exact rational value of every output (Fraction), rounded once to bf16."""
+    M, K = x.shape
+    e2m1 = {c: Fraction(v) for c, v in ((0, 0), (1, Fraction(1, 2)), (2, 1), (3, Fraction(3, 2)), (4, 2), (5, 3),
+                                          (6, 4), (7, 6))}
+    glob = Fraction(w.global_scale)
+    exact = [[Fraction(0)] * w.N for _ in range(M)]
+    for n in range(w.N):
+        for k in range(K):
+            c = (int(w.w_packed[n, k // 8]) >> (4 * (k % 8))) & 15
+            mag = e2m1[c & 7]
+            sb = int(w.scales[n, k // 16])
+            e, m = (sb >> 3) & 15, sb & 7
+            s = Fraction(m, 8) * Fraction(2) ** -6 if e == 0 else (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7)
+            wk = glob * s * (-mag if c & 8 else mag)
+            for mm in range(M):
+                exact[mm][n] += bf16_bits_to_fraction(x[mm, k]) * wk
+    bits = np.array([[fraction_to_bf16_bits(v) for v in row] for row in exact], np.uint16)
+    return exact, bits
+
+
+@pytest.mark.parametrize("M,N,K,seed", [(1, 4, 32, 1), (2, 3, 64, 2), (1, 2, 128, 3)])
+def test_nvfp4_brute_force_rational(M, N, K, seed):
+    w = synth.make_nvfp4_weights(N, K, seed)
+    x = synth.make_x(M, K, seed)
+    exact, ref_bits = brute_force_nvfp4(x, w)
+    y_exact, y_bf16 = oracle.nvfp4_matmul(x, w.w_packed, w.scales, w.global_scale, M, N, K)
+    assert np.array_equal(y_bf16, ref_bits)
+    for m in range(M):
+        for n in range(N):
+            assert abs(Fraction(y_exact[m, n]) - exact[m][n]) <= abs(exact[m][n]) * Fraction(1, 2 ** 45)
+
+
+def test_nvfp4_one_hot_column_and_sampled():
+    N, K = 20, 64
+    w = synth.make_nvfp4_weights(N, K, 9)
+    wd = oracle.nvfp4_dequant(w.w_packed, w.scales, w.global_scale, N, K)
+    for k in (0, 15, 16, 63):
+        x = np.zeros((1, K), np.uint16)
+        x[0, k] = 0x3F80                                        # 1.0
+        ye, _ = oracle.nvfp4_matmul(x, w.w_packed, w.scales, w.global_scale, 1, N, K)
+        for n in range(N):
+            c = (int(w.w_packed[n, k // 8]) >> (4 * (k % 8))) & 15
+            want = w.global_scale * oracle.e4m3_to_double(int(w.scales[n, k // 16])) * oracle.e2m1_to_double(c)
+            assert ye[0, n] == want == wd[n, k]
+    x = synth.make_x(3, K, 9)
+    ye, yb = oracle.nvfp4_matmul(x, w.w_packed, w.scales, w.global_scale, 3, N, K)
+    im, inn = np.array([0, 2, 1, 2]), np.array([0, 19, 7, 3])
+    se, sb = oracle.nvfp4_matmul_sampled(x, w.w_packed, w.scales, w.global_scale, 3, N, K, im, inn)
+    assert np.array_equal(se, ye[im, inn]) and np.array_equal(sb, yb[im, inn])
