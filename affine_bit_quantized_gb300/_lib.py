@@ -96,6 +96,8 @@ def load() -> ctypes.CDLL:
             lib.aq_gather_qmm_bf16.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I, I, P,
                                                ctypes.c_size_t, P]
             lib.aq_gather_qmm_bf16.restype = I
+            lib.aq_matmul_nvfp4_bf16.argtypes = [P, P, P, ctypes.c_float, P, I64, I64, I64, U, P]
+            lib.aq_matmul_nvfp4_bf16.restype = I
             lib.aq_version.argtypes = []
             lib.aq_version.restype = I
             _lib = lib
@@ -190,6 +192,10 @@ def aq_gather_qmm_bf16(x, w_packed, scales, biases, lhs_indices, rhs_indices, y,
                        workspace, workspace_bytes, stream) -> int:
     return load().aq_gather_qmm_bf16(x, w_packed, scales, biases, lhs_indices, rhs_indices, y, R, T, N, K, E,
                                      group_size, bits, workspace, workspace_bytes, stream)
+
+
+def aq_matmul_nvfp4_bf16(x, w_packed, scales_e4m3, global_scale, y, M, N, K, flags, stream) -> int:
+    return load().aq_matmul_nvfp4_bf16(x, w_packed, scales_e4m3, global_scale, y, M, N, K, flags, stream)
 
 
 def aq_read_device_status(stream) -> int:
@@ -291,4 +297,25 @@ def gather_qmm(x, w_packed, scales, biases, lhs_indices, rhs_indices, out=None, 
                             group_size, bits, workspace.data_ptr(), workspace.numel(), stream.cuda_stream)
     if st != AQ_OK:
         raise AqError(st, "aq_gather_qmm_bf16")
+    return out
+
+
+def matmul_nvfp4(x, w_packed, scales_e4m3, global_scale: float = 1.0, out=None, *, pdl: bool = False, stream=None):
+    """NVFP4 decode matmul for torch CUDA tensors: x bf16 [M, K]; w_packed int32
+    [N, K/8] (E2M1 codes); scales_e4m3 uint8 [N, K/16].  Returns y bf16 [M, N]."""
+    import torch
+
+    M, K = x.shape
+    N = w_packed.shape[0]
+    for name, t in (("x", x), ("w_packed", w_packed), ("scales_e4m3", scales_e4m3)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    st = aq_matmul_nvfp4_bf16(x.data_ptr(), w_packed.data_ptr(), scales_e4m3.data_ptr(), float(global_scale),
+                              out.data_ptr(), M, N, K, AQ_FLAG_PDL if pdl else 0, stream.cuda_stream)
+    if st != AQ_OK:
+        raise AqError(st, "aq_matmul_nvfp4_bf16")
     return out

@@ -367,6 +367,33 @@ aq_status aq_gather_qmm_bf16(const void *x, const uint32_t *w_packed, const void
     return record_cuda(aq::launch_gather_qmm(g));
 }
 
+aq_status aq_matmul_nvfp4_bf16(const void *x, const uint32_t *w_packed, const uint8_t *scales_e4m3,
+                               float global_scale, void *y, int64_t M, int64_t N, int64_t K, unsigned flags,
+                               void *stream) {
+    if (flags & ~(unsigned)AQ_FLAG_PDL) return AQ_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim || K % 16) return AQ_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return AQ_OK;
+    if (M > 8 || K == 0 || K % 256 || M * K > 16384) return AQ_ERR_UNSUPPORTED;
+    if (!x || !w_packed || !scales_e4m3 || !y) return AQ_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(w_packed, 16) || !aligned(scales_e4m3, 16) || !aligned(y, 2))
+        return AQ_ERR_ALIGNMENT;
+    aq::Nvfp4Args a;
+    a.x = x;
+    a.w = w_packed;
+    a.scales = scales_e4m3;
+    a.global_scale = global_scale;
+    a.y = y;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.pdl = (flags & AQ_FLAG_PDL) != 0;
+    a.stream = static_cast<cudaStream_t>(stream);
+    a.timeout_ns = kTimeoutNs;
+    aq_status st = record_cuda(status_ptr(&a.status));
+    if (st != AQ_OK) return st;
+    return record_cuda(aq::launch_nvfp4_qmv(a));
+}
+
 int aq_version(void) { return 100; }
 
 }  // extern "C"

@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "aq.h"
@@ -37,6 +38,8 @@ cudaError_t launch_qmv(const MatmulArgs &a);
 
 // TMA-fed weight-streaming kernel (qmv_tma.cu) for 1 <= M <= 8,
 // K % 512 == 0, M*K <= 16384 and 16-byte aligned scales/biases.
+// the driver's tensor-map encoder (null if the driver does not offer it)
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 // tensor map of packed codes for the decode kernels: a stage (32 rows x 1024 bytes) per copy
 bool encode_codes_3d(CUtensorMap *map, const void *base, uint64_t row_bytes, uint64_t rows);
 bool qmv_tma_supported(const MatmulArgs &a);
@@ -69,6 +72,22 @@ struct GatherArgs {
 };
 size_t gather_workspace_bytes(int64_t R, int64_t K, int64_t E);
 cudaError_t launch_gather_qmm(const GatherArgs &g);
+
+// NVFP4 weight-streaming kernel (nvfp4_qmv.cu): 1 <= M <= 8, K % 256 == 0,
+// M*K <= 16384, 16-byte aligned x, codes and scales.
+struct Nvfp4Args {
+    const void *x;            // bf16 [M, K]
+    const uint32_t *w;        // FP4 E2M1 codes [N, K/8]
+    const uint8_t *scales;    // FP8 E4M3 [N, K/16]
+    float global_scale;
+    void *y;                  // bf16 [M, N]
+    int64_t M, N, K;
+    bool pdl;
+    cudaStream_t stream;
+    int *status;
+    uint64_t timeout_ns;
+};
+cudaError_t launch_nvfp4_qmv(const Nvfp4Args &a);
 
 // Chains of decode matmuls in one persistent launch (qmv_chain.cu).
 size_t chain_workspace_bytes(int count);

@@ -1,0 +1,394 @@
+// Weight-streaming kernel for y = x . W^T with NVFP4 weights and 1..8 rows of x.
+//
+// The "MLX CUDA Cleanup Plan" page (Refactor Plan, Phase 3b) asks for a CUDA
+// NVFP4 qmv for its mode=nvfp4, group_size=16 checkpoint, kept structurally
+// separate from the affine path.  Format (the NVFP4 layout of NVIDIA's model
+// optimizer): FP4 E2M1 codes packed eight per uint32 (lowest nibble = lowest
+// k), one FP8 E4M3 scale per 16 codes along K, one fp32 scale per tensor:
+//
+//     w[n,k] = global * e4m3(scale[n, k/16]) * e2m1(q[n,k])
+//
+// The stream and the tile bookkeeping are those of the affine decode kernel
+// (a TMA producer warp filling a ring of 36 KB stages, sixteen consumer warps,
+// a reducer warp adding their partials in a fixed order); the arithmetic is
+// this format's own:
+//
+//  * e2m1 * e4m3 has at most six significant bits and lies in [2^-10, 2688],
+//    so a code pair converted to fp16 (cvt.rn.f16x2.e2m1x2) times its block
+//    scale (fp16, exact for every finite E4M3 value) is the exact weight in
+//    fp16: no per-group fold, the MMA accumulates across all groups;
+//  * x is staged once per CTA in fp16, each row scaled by a power of two so
+//    that its bf16 values stay exact (the partial sums are scaled back, then
+//    the reducer multiplies by the tensor scale before the one bf16 rounding);
+//  * lane t of a warp holds 32 consecutive codes of each of its four rows (one
+//    16-byte load), i.e. two whole scale groups; MMA step s takes bytes 2s and
+//    2s+1 of those 16, and the x fragment of step s is the four x values at
+//    the same code positions (one 8-byte load), so A and B agree on which k
+//    sits in each MMA slot.
+//
+// Every mbarrier wait is bounded (global-timer deadline, device status word),
+// as in the affine kernels.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+
+#include "aq_internal.h"
+#include "aq_ptx.cuh"
+#include "qmv_consumer.cuh"
+
+namespace aq {
+namespace {
+
+using namespace dev;
+using namespace qmv;
+
+constexpr int kThreads = (kConsumerWarps + 2) * 32;   // consumers, TMA producer, reducer
+constexpr int kNS = 4;                                 // ring depth
+constexpr int kCodes = 2048;                           // codes per row and stage (1024 bytes)
+constexpr int kScaleBytes = kRows * (kCodes / 16);     // 4096: one E4M3 byte per 16 codes, 32 rows
+constexpr int kStage = kCodesBytes + kScaleBytes;      // 36864
+constexpr int kNumBars = 2 * kNS + 1 + 8;              // full[4], empty[4], x, red_full[4], red_empty[4]
+constexpr int kSmemLimit = 232448;
+
+struct Layout {
+    int x_off, xinfo_off, red_off, bar_off, total;
+};
+__host__ __device__ inline Layout make_layout(int M, int K) {
+    Layout L;
+    L.x_off = kNS * kStage;
+    L.xinfo_off = L.x_off + M * x_row_bytes(M, K);
+    L.red_off = L.xinfo_off + kXInfoBytes;
+    L.bar_off = L.red_off + red_bytes(M);
+    L.total = L.bar_off + kNumBars * 8 + 16;
+    return L;
+}
+
+// fp16x2 of the two E2M1 codes of byte `b` of v (low nibble in the low half)
+template <int B>
+__device__ __forceinline__ uint32_t e2m1_pair(uint32_t v) {
+    uint32_t r;
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n cvt.rn.f16x2.e2m1x2 %0, b%2;\n}"
+        : "=r"(r)
+        : "r"(v), "n"(B));
+    return r;
+}
+// fp16x2 of the two E4M3 bytes in the low 16 bits of v (low byte in the low half)
+__device__ __forceinline__ uint32_t e4m3_pair(uint32_t v) {
+    uint32_t r;
+    asm("{\n .reg .b16 h;\n cvt.u16.u32 h, %1;\n cvt.rn.f16x2.e4m3x2 %0, h;\n}" : "=r"(r) : "r"(v));
+    return r;
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+__device__ __forceinline__ uint32_t lds16u(uint32_t a) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+
+// x [M][K] bf16, bulk-copied to `raw` (rows x_row_bytes apart) -> fp16 in
+// natural k order in place, each row times 2^e (e from its max |x|, as in the
+// affine staging), and inv_scale[m] = 2^-e.
+template <bool ONE_ROW>
+__device__ __forceinline__ void stage_x_fp16(uint32_t raw, uint32_t xinfo, int M_, int K) {
+    const int M = ONE_ROW ? 1 : M_;
+    const int tid = threadIdx.x;
+    const int wpr = K / 8, words = M * wpr, xrb = x_row_bytes(M, K);
+    int *row_max = reinterpret_cast<int *>(__cvta_shared_to_generic(xinfo));
+    float *inv_scale = reinterpret_cast<float *>(__cvta_shared_to_generic(xinfo + 64));
+    uint4 v[kMaxXBytes / 16 / kConsumerThreads];
+#pragma unroll
+    for (int u = 0; u < kMaxXBytes / 16 / kConsumerThreads; ++u) {
+        if (u * kConsumerThreads >= words) break;   // uniform over the CTA
+        const int wi = u * kConsumerThreads + tid;
+        int mx = 0;
+        if (wi < words) {
+            const int m = ONE_ROW ? 0 : wi / wpr, wr = wi - m * wpr;
+            v[u] = lds128(raw + (uint32_t)(m * xrb + wr * 16));
+            mx = max(max(bf16x2_abs_max(v[u].x), bf16x2_abs_max(v[u].y)),
+                     max(bf16x2_abs_max(v[u].z), bf16x2_abs_max(v[u].w)));
+        }
+        mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+        if ((tid & 31) == 0 && wi < words) atomicMax(row_max + (ONE_ROW ? 0 : wi / wpr), mx);
+    }
+    consumer_sync();
+#pragma unroll
+    for (int u = 0; u < kMaxXBytes / 16 / kConsumerThreads; ++u) {
+        if (u * kConsumerThreads >= words) break;
+        const int wi = u * kConsumerThreads + tid;
+        if (wi < words) {
+            const int m = ONE_ROW ? 0 : wi / wpr, wr = wi - m * wpr;
+            const float sc = pow2f(x_scale_exponent(row_max[m]));
+            const uint4 a = v[u];
+            uint4 o;
+            o.x = f32x2_to_f16x2(bf16lo(a.x) * sc, bf16hi(a.x) * sc);
+            o.y = f32x2_to_f16x2(bf16lo(a.y) * sc, bf16hi(a.y) * sc);
+            o.z = f32x2_to_f16x2(bf16lo(a.z) * sc, bf16hi(a.z) * sc);
+            o.w = f32x2_to_f16x2(bf16lo(a.w) * sc, bf16hi(a.w) * sc);
+            sts128(raw + (uint32_t)(m * xrb + wr * 16), o);
+        }
+    }
+    if (tid < M) inv_scale[tid] = pow2f(-x_scale_exponent(row_max[tid]));
+    consumer_sync();
+}
+
+// Adds warp `warp`'s block of a stage (32 rows x 128 codes: codes
+// [warp*128, warp*128 + 128) of the stage) to acc.  code: the lane's row
+// offsets; xq: byte address of x[row][stage_k + warp*128 + lane%4 * 32].
+__device__ __forceinline__ void consume_stage_nvfp4(uint32_t st, const uint32_t (&code)[4], uint32_t sb,
+                                                    uint32_t xq, float (&acc)[2][4]) {
+    uint4 cw[4];
+    uint32_t sa2[4], sb2[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        cw[r] = lds128(st + code[r]);
+        // the block scales of the lane's two groups in row gid + 8r, each in both halves
+        const uint32_t s2 = e4m3_pair(lds16u(st + kCodesBytes + sb + 8 * 128 * r));
+        sa2[r] = prmt(s2, s2, 0x1010u);
+        sb2[r] = prmt(s2, s2, 0x3232u);
+    }
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+        const uint2 X = lds64(xq + s * 8);   // x at the lane's codes 4s .. 4s+3
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint4 &R0 = cw[2 * h], &R1 = cw[2 * h + 1];   // rows gid + 16h, gid + 8 + 16h
+            const uint32_t w0 = s < 2 ? R0.x : s < 4 ? R0.y : s < 6 ? R0.z : R0.w;
+            const uint32_t w1 = s < 2 ? R1.x : s < 4 ? R1.y : s < 6 ? R1.z : R1.w;
+            const uint32_t g0 = s < 4 ? sa2[2 * h] : sb2[2 * h];
+            const uint32_t g1 = s < 4 ? sa2[2 * h + 1] : sb2[2 * h + 1];
+            uint32_t a0, a1, a2, a3;
+            if (s & 1) {
+                a0 = hmul2(e2m1_pair<2>(w0), g0);
+                a1 = hmul2(e2m1_pair<2>(w1), g1);
+                a2 = hmul2(e2m1_pair<3>(w0), g0);
+                a3 = hmul2(e2m1_pair<3>(w1), g1);
+            } else {
+                a0 = hmul2(e2m1_pair<0>(w0), g0);
+                a1 = hmul2(e2m1_pair<0>(w1), g1);
+                a2 = hmul2(e2m1_pair<1>(w0), g0);
+                a3 = hmul2(e2m1_pair<1>(w1), g1);
+            }
+            mma_f16_16816(acc[h], a0, a1, a2, a3, X.x, X.y);
+        }
+    }
+}
+
+template <bool ONE_ROW>
+__global__ void __launch_bounds__(kThreads, 1)
+nvfp4_qmv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
+                 const __nv_bfloat16 *__restrict__ x, __nv_bfloat16 *__restrict__ y, int M, int N, int K,
+                 float global_scale, unsigned long long timeout_ns, int *status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const Layout L = make_layout(M, K);
+    const uint32_t s_base = smem_addr(smem);
+    const uint32_t x_s = s_base + (uint32_t)L.x_off;
+    const uint32_t xinfo = s_base + (uint32_t)L.xinfo_off;
+    const float *inv_scale = reinterpret_cast<const float *>(smem + L.xinfo_off + 64);
+    const uint32_t bar_full = s_base + L.bar_off;
+    const uint32_t bar_empty = bar_full + kNS * 8;
+    const uint32_t bar_x = bar_empty + kNS * 8;
+    const uint32_t bar_red = bar_x + 8;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.bar_off + kNumBars * 8);
+    TileCtx tc;
+    tc.red = reinterpret_cast<float *>(smem + L.red_off);
+    tc.red_full = bar_red;
+    tc.red_empty = bar_red + 32;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int KB = (K + kCodes - 1) / kCodes;   // stages per tile
+    const int T = (N + kRows - 1) / kRows;
+    const int my_tiles = (int)blockIdx.x < T ? (T - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int items = my_tiles * KB;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kNS; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, kConsumerWarps);
+        }
+        mbar_init(bar_x, 1);
+        for (int p = 0; p < red_bufs<ONE_ROW>(); ++p) {
+            mbar_init(tc.red_full + 8 * p, kConsumerWarps);
+            mbar_init(tc.red_empty + 8 * p, 1);
+        }
+        for (int m = 0; m < 2 * kMaxM; ++m) reinterpret_cast<int *>(smem + L.xinfo_off)[m] = 0;
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    griddep_launch();
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            auto issue = [&](int it) {
+                const int slot = it % kNS, tile = (int)blockIdx.x + (it / KB) * (int)gridDim.x, kb = it % KB;
+                const uint32_t dst = s_base + slot * kStage, fb = bar_full + 8 * slot;
+                // codes: one box of 8 chunks x 32 rows x 128 bytes; scales: 128 bytes x 32 rows
+                // (parts past the row's end read as zeros and still count)
+                mbar_expect_tx(fb, (uint32_t)kStage);
+                tma_load_3d(dst, &tm_w, 0, tile * kRows, kb * kBoxes, fb, pol);
+                tma_load_2d(dst + kCodesBytes, &tm_s, kb * (kCodes / 16), tile * kRows, fb, pol);
+            };
+            int issued = 0;
+            bool ok = true;
+            for (; issued < items && issued < kNS; ++issued) issue(issued);   // weights first
+            griddep_wait();
+            const uint64_t deadline = global_timer() + timeout_ns;
+            mbar_expect_tx(bar_x, (uint32_t)(M * K * 2));
+            for (int m = 0; m < M; ++m)
+                bulk_load(x_s + m * x_row_bytes(M, K), x + (int64_t)m * K, (uint32_t)(K * 2), bar_x);
+            for (; issued < items; ++issued) {
+                const int slot = issued % kNS;
+                if (!mbar_wait(bar_empty + 8 * slot, ((issued / kNS) - 1) & 1, deadline, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                issue(issued);
+            }
+            if (!ok) {
+                if (!*abort_flag) {
+                    atomicExch(status, (int)AQ_DEVICE_STATUS_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                const uint64_t drain = global_timer() + timeout_ns;
+                for (int it = (issued > kNS ? issued - kNS : 0); it < issued; ++it)
+                    while (!mbar_try_wait(bar_full + 8 * (it % kNS), (it / kNS) & 1) && global_timer() < drain) {
+                    }
+                while (!mbar_try_wait(bar_x, 0) && global_timer() < drain) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == kConsumerWarps + 1) {
+        // ------------------------------------------------------------ reducer
+        bool ok = true;
+        for (int t = 0; ok && t < my_tiles; ++t)
+            ok = reduce_tile<ONE_ROW>(tc, t, (int)blockIdx.x + t * (int)gridDim.x, M, N, y, lane, timeout_ns,
+                                      abort_flag, nullptr, 0, 1, global_scale);
+        if (!ok && lane == 0 && !*abort_flag) {
+            atomicExch(status, (int)AQ_DEVICE_STATUS_TIMEOUT);
+            *abort_flag = 1;
+        }
+    } else {
+        // ------------------------------------------------------------ consumers
+        griddep_wait();
+        const uint64_t deadline = global_timer() + timeout_ns;
+        bool alive = true;
+        auto fail = [&]() {
+            if (alive && !*abort_flag) {
+                atomicExch(status, (int)AQ_DEVICE_STATUS_TIMEOUT);
+                *abort_flag = 1;
+            }
+            alive = false;
+        };
+        if (!mbar_wait(bar_x, 0, deadline, abort_flag)) fail();
+        stage_x_fp16<ONE_ROW>(x_s, xinfo, M, K);
+        const int gid = lane >> 2, t = lane & 3;
+        // the lane's 16 bytes of codes in row gid + 8r (128-byte swizzle: unit u of row r at u ^ (r % 8))
+        uint32_t code[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            code[r] = (uint32_t)((warp >> 1) * kBoxBytes + (gid + 8 * r) * 128 + (((4 * (warp & 1) + t) ^ gid) << 4));
+        // the lane's two scale bytes (groups warp*8 + 2t, +1) of row gid (128-byte swizzle)
+        const uint32_t sb = (uint32_t)(gid * 128 + (((warp >> 1) ^ gid) << 4) + 8 * (warp & 1) + 2 * t);
+        const int M1 = ONE_ROW ? 1 : M;
+        const int xrow = ONE_ROW ? 0 : (gid < M1 ? gid : M1 - 1);    // B column gid holds x row gid
+        const uint32_t xq0 = x_s + (uint32_t)(xrow * x_row_bytes(M1, K) + (warp * 128 + t * 32) * 2);
+        const int nblk = K / 128;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        bool ok = alive && !*abort_flag;
+        int item = 0;
+        for (int tl = 0; tl < my_tiles; ++tl) {
+            for (int kb = 0; ok && kb < KB; ++kb, ++item) {
+                const int slot = item % kNS;
+                if (!mbar_wait_fast(bar_full + 8 * slot, (uint32_t)(item / kNS) & 1u, deadline, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (kb * kConsumerWarps + warp < nblk)
+                    consume_stage_nvfp4(s_base + (uint32_t)(slot * kStage), code, sb, xq0 + (uint32_t)(kb * kCodes * 2),
+                                        acc);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+            }
+            if (ok) ok = deposit_tile<ONE_ROW>(tc, acc, tl, M, warp, lane, inv_scale, timeout_ns, abort_flag);
+        }
+        if (!ok) fail();
+    }
+}
+
+bool encode_scales_2d(CUtensorMap *map, const void *base, uint64_t row_bytes, uint64_t rows) {
+    auto fn = tensor_map_encoder();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {row_bytes, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)(kCodes / 16), (cuuint32_t)kRows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sms[kMaxDevices];
+std::atomic<int> g_attr_done[2][kMaxDevices];
+
+}  // namespace
+
+cudaError_t launch_nvfp4_qmv(const Nvfp4Args &a) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    int sms = g_sms[dev].load(std::memory_order_relaxed);
+    if (sms == 0) {
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        g_sms[dev].store(sms, std::memory_order_relaxed);
+    }
+    const int M = (int)a.M, N = (int)a.N, K = (int)a.K;
+    const bool one = M == 1;
+    auto kern = one ? nvfp4_qmv_kernel<true> : nvfp4_qmv_kernel<false>;
+    if (!g_attr_done[one][dev].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+        if (e != cudaSuccess) return e;
+        g_attr_done[one][dev].store(1, std::memory_order_release);
+    }
+    const Layout L = make_layout(M, K);
+    const int smem = L.total + 1024;
+    if (smem > kSmemLimit) return cudaErrorInvalidConfiguration;
+    CUtensorMap tw, ts;
+    if (!tensor_map_encoder() || !encode_codes_3d(&tw, a.w, (uint64_t)K / 2, (uint64_t)N) ||
+        !encode_scales_2d(&ts, a.scales, (uint64_t)K / 16, (uint64_t)N))
+        return cudaErrorInvalidValue;
+    const int T = (N + kRows - 1) / kRows;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)std::min(T, sms));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, tw, ts, static_cast<const __nv_bfloat16 *>(a.x),
+                              static_cast<__nv_bfloat16 *>(a.y), M, N, K, a.global_scale,
+                              (unsigned long long)a.timeout_ns, a.status);
+}
+
+}  // namespace aq

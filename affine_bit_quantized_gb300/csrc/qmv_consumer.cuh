@@ -444,7 +444,7 @@ template <bool ONE_ROW>
 __device__ __forceinline__ bool reduce_tile(const TileCtx &t, int tcount, int tile, int M, int N,
                                             __nv_bfloat16 *y, int lane, uint64_t timeout_ns,
                                             const volatile int *abort_flag, float *yacc = nullptr, int pass = 0,
-                                            int passes = 1) {
+                                            int passes = 1, float yscale = 1.f) {
     constexpr int B = red_bufs<ONE_ROW>();
     const int b = tcount % B;
     const int n_out = kRows * M;
@@ -460,7 +460,7 @@ __device__ __forceinline__ bool reduce_tile(const TileCtx &t, int tcount, int ti
         if (pass + 1 < passes)
             yacc[idx] = v;
         else if (n < N)
-            y[(int64_t)m * N + n] = __float2bfloat16_rn(v);
+            y[(int64_t)m * N + n] = __float2bfloat16_rn(v * yscale);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(t.red_empty + 8 * b);

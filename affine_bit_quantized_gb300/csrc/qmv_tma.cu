@@ -346,6 +346,8 @@ bool encode_codes_3d(CUtensorMap *map, const void *base, uint64_t row_bytes, uin
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() { return encode_fn(); }
+
 bool qmv_tma_supported(const MatmulArgs &a) {
     return (a.bits == 4 || a.bits == 8) && a.M >= 1 && a.M <= kMaxM && a.K % 512 == 0 && encode_fn() != nullptr &&
            (reinterpret_cast<uintptr_t>(a.scales) & 15) == 0 && (reinterpret_cast<uintptr_t>(a.biases) & 15) == 0;

@@ -584,6 +584,28 @@ def main():
                             "frac_of_bf16_sustained": round(tf / bf16_sus, 4)}
             del ws
 
+    # ---- NVFP4 weights (E2M1 codes, E4M3 scale per 16, fp32 tensor scale), M = 1, the step's shapes:
+    # 4 device copies of each matrix cycled (0.5625 B per weight, as the affine 4-bit format)
+    nvfp4 = {}
+    for j, (name, N, K) in enumerate(synth.LLAMA8B_LAYER + (synth.LLAMA8B_LM_HEAD,)):
+        wn = synth.make_nvfp4_weights(N, K, synth.seed_for(7, 0, j))
+        base = (torch.from_numpy(wn.w_packed.view(np.int32)).to(dev), torch.from_numpy(wn.scales).to(dev))
+        wsn = [base] + [tuple(t.clone() for t in base) for _ in range(3)]
+        xn = torch.from_numpy(synth.make_x(1, K, synth.seed_for(7, 1, j)).view(np.int16)).to(dev)
+        yn = torch.empty((1, N), dtype=torch.int16, device=dev)
+
+        def launchn(i, wsn=wsn, xn=xn, yn=yn, N=N, K=K, g=wn.global_scale):
+            wt, st_ = wsn[i % len(wsn)]
+            rc = lib.aq_matmul_nvfp4_bf16(xn.data_ptr(), wt.data_ptr(), st_.data_ptr(), g, yn.data_ptr(), 1, N, K,
+                                          aq.AQ_FLAG_PDL, cur.cuda_stream)
+            if rc != aq.AQ_OK:
+                raise aq.AqError(rc, "aq_matmul_nvfp4_bf16")
+
+        us = time_calls(launchn, 8)
+        nvfp4[name] = {"N": N, "K": K, "us_per_call": round(us, 3),
+                       "gbs": round(alg_bytes(1, N, K) / (us * 1e-6) / 1e9, 1)}
+        del wsn, base
+
     # ---- MoE prefill (expert-indexed matmul): Mixtral-8x7B-shaped experts, 2048 tokens routed
     # top-2 over 8 experts (4096 rows), one call = plan + row gather + tensor-core matmul
     moe = {}
@@ -680,6 +702,7 @@ def main():
         "per_matrix": per_matrix,
         "small_batch": small_batch,
         "eight_bit": eight_bit,
+        "nvfp4": nvfp4,
         "moe_prefill": moe,
         "qmm": qmm,
     }

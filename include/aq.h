@@ -275,6 +275,31 @@ aq_status aq_gather_qmm_bf16(const void *x, const uint32_t *w_packed, const void
                              int64_t N, int64_t K, int64_t E, int group_size, int bits,
                              void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * NVFP4 decode matmul ("MLX CUDA Cleanup Plan", Refactor Plan, Phase 3b: the
+ * mode=nvfp4, group_size=16 checkpoint and a CUDA NVFP4 qmv kept separate
+ * from the affine path):
+ *
+ *     y[m, n] = sum_k x[m, k] * global_scale * e4m3(scales[n, k/16]) * e2m1(q[n, k])
+ *
+ *   x             bf16 [M, K], device
+ *   w_packed      uint32 [N, K/8], device: FP4 E2M1 codes (bit 3 sign, two
+ *                 exponent bits with bias 1, one mantissa bit), eight per word,
+ *                 lowest nibble = lowest k
+ *   scales_e4m3   uint8 [N, K/16], device: FP8 E4M3 block scales (no
+ *                 infinities; S.1111.111 is NaN and propagates)
+ *   global_scale  the tensor's fp32 scale (1.0f if it has none)
+ *   y             bf16 [M, N], device, written; fp32 accumulation, one rounding
+ *   1 <= M <= 8, N >= 1, K a multiple of 256 with M*K <= 16384 (M == 0 or
+ *   N == 0: nothing launched).  x, w_packed and scales_e4m3 16-byte aligned,
+ *   y 2-byte aligned.  Errors: AQ_ERR_INVALID_ARG, AQ_ERR_UNSUPPORTED (sizes
+ *   outside these limits), AQ_ERR_ALIGNMENT, AQ_ERR_CUDA.  Asynchronous;
+ *   allocates nothing; deterministic.  AQ_FLAG_PDL is accepted in `flags`.
+ */
+aq_status aq_matmul_nvfp4_bf16(const void *x, const uint32_t *w_packed, const uint8_t *scales_e4m3,
+                               float global_scale, void *y, int64_t M, int64_t N, int64_t K,
+                               unsigned flags, void *stream);
+
 /* Text of the last CUDA runtime error seen by an entry point on this host
  * thread ("" if none).  Valid until the next call on this thread. */
 const char *aq_last_cuda_error(void);

@@ -182,3 +182,25 @@ def test_gather_workspace_bytes():
 ])
 def test_gather_validation(kw, expect):
     assert _gather_call(**kw) == expect
+
+
+# ---------------------------------------------------------------- NVFP4 matmul: validation
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(K=100), aq.AQ_ERR_INVALID_ARG),          # not a multiple of 16
+    (dict(K=272), aq.AQ_ERR_UNSUPPORTED),          # not a multiple of 256
+    (dict(M=9), aq.AQ_ERR_UNSUPPORTED),
+    (dict(M=2, K=16384), aq.AQ_ERR_UNSUPPORTED),   # x beyond one staging
+    (dict(M=-1), aq.AQ_ERR_INVALID_ARG),
+    (dict(flags=1 << 3), aq.AQ_ERR_INVALID_ARG),
+    (dict(x=None), aq.AQ_ERR_INVALID_ARG),
+    (dict(x=A + 8), aq.AQ_ERR_ALIGNMENT),
+    (dict(s=A + 4), aq.AQ_ERR_ALIGNMENT),
+    (dict(M=0, x=None), aq.AQ_OK),
+    (dict(N=0), aq.AQ_OK),
+])
+def test_nvfp4_validation(kw, expect):
+    d = dict(x=A, w=A, s=A, g=1.0, y=A, M=1, N=64, K=512, flags=0)
+    d.update(kw)
+    assert aq.aq_matmul_nvfp4_bf16(d["x"], d["w"], d["s"], d["g"], d["y"], d["M"], d["N"], d["K"], d["flags"],
+                                   None) == expect
