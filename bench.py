@@ -141,6 +141,30 @@ def x_layout(layers: int):
     return offs, pos
 
 
+def rank_env():
+    """(world size, rank, local rank) from the launcher's environment (1, 0, 0 alone)."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(v: float, world: int, device) -> float:
+    """The largest of every rank's v (a collective: every rank must call it)."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, units_per_rank: float, seconds_max: float) -> float:
+    """Whole-job throughput of replicas (weak scaling): every rank processed
+    units_per_rank, the slowest in seconds_max."""
+    return world * units_per_rank / seconds_max
+
+
 def run_reference(args, target_seconds: float = 150.0):
     """CPU oracle on a bounded sample of the decode step: the first R rows of
     each of the 7 matrices of one layer per step, R sized so that warm-up plus
@@ -282,9 +306,7 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local_rank = rank_env()
 
     if args.impl == "reference":
         if rank == 0:
@@ -402,12 +424,6 @@ def main():
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    def max_over_ranks(v: float) -> float:
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
 
     uuid = str(torch.cuda.get_device_properties(dev).uuid)
     gpu_id = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
@@ -454,10 +470,10 @@ def main():
     ms_step = time_steps(step, args.steps)
     clk = clocks.stop()
     barrier()
-    ms_step = max_over_ranks(ms_step)
+    ms_step = max_over_ranks(ms_step, world, dev)
     for _ in range(args.warmup):
         step_fns[alt_impl]()
-    ms_alt = max_over_ranks(time_steps(step_fns[alt_impl], max(3, min(args.steps, 500))))
+    ms_alt = max_over_ranks(time_steps(step_fns[alt_impl], max(3, min(args.steps, 500))), world, dev)
     if aq.aq_read_device_status(cur.cuda_stream) != aq.AQ_OK:
         raise RuntimeError("a bounded device-side wait expired during the timed steps")
 
@@ -473,7 +489,7 @@ def main():
 
     for _ in range(args.warmup):
         e2e_step()
-    ms_e2e = max_over_ranks(time_steps(e2e_step, args.steps))
+    ms_e2e = max_over_ranks(time_steps(e2e_step, args.steps), world, dev)
 
     # ---- per-matrix kernel times (the 32 layer copies of each shape back to back)
     per_matrix = {}
@@ -660,8 +676,8 @@ def main():
                          f"{passes} passes",
                "seconds": round(dt, 2)}
 
-    gbs = world * step_bytes / (ms_step * 1e-3) / 1e9
-    gbs_e2e = world * step_bytes / (ms_e2e * 1e-3) / 1e9
+    gbs = job_rate(world, step_bytes, ms_step * 1e-3) / 1e9
+    gbs_e2e = job_rate(world, step_bytes, ms_e2e * 1e-3) / 1e9
     traffic = committed_traffic()
     line = {
         "metric": METRIC,
