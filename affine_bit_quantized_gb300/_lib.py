@@ -91,6 +91,10 @@ def load() -> ctypes.CDLL:
             lib.aq_chain_run_static.restype = I
             lib.aq_read_device_status.argtypes = [P]
             lib.aq_read_device_status.restype = I
+            lib.aq_matmul_workspace_bytes.argtypes = [I64, I64]
+            lib.aq_matmul_workspace_bytes.restype = ctypes.c_size_t
+            lib.aq_matmul_bf16_ws.argtypes = [P, P, P, P, P, I64, I64, I64, I, I, P, ctypes.c_size_t, P]
+            lib.aq_matmul_bf16_ws.restype = I
             lib.aq_gather_qmm_workspace_bytes.argtypes = [I64, I64, I64]
             lib.aq_gather_qmm_workspace_bytes.restype = ctypes.c_size_t
             lib.aq_gather_qmm_bf16.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I, I, P,
@@ -184,6 +188,16 @@ def aq_chain_run_static(descs, count, group_size, bits, stream) -> int:
     return load().aq_chain_run_static(descs, count, group_size, bits, stream)
 
 
+def aq_matmul_workspace_bytes(M, K) -> int:
+    return load().aq_matmul_workspace_bytes(M, K)
+
+
+def aq_matmul_bf16_ws(x, w_packed, scales, biases, y, M, N, K, group_size, bits, workspace, workspace_bytes,
+                      stream) -> int:
+    return load().aq_matmul_bf16_ws(x, w_packed, scales, biases, y, M, N, K, group_size, bits, workspace,
+                                    workspace_bytes, stream)
+
+
 def aq_gather_qmm_workspace_bytes(R, K, E) -> int:
     return load().aq_gather_qmm_workspace_bytes(R, K, E)
 
@@ -220,7 +234,7 @@ _KERNELS = {"auto": AQ_KERNEL_AUTO, "qmv": AQ_KERNEL_QMV, "qmm": AQ_KERNEL_QMM}
 
 
 def matmul(x, w_packed, scales, biases, out=None, *, group_size: int = 64, bits: int = 4,
-           kernel: str = "auto", pdl: bool = False, stream=None, flags: int = 0):
+           kernel: str = "auto", pdl: bool = False, stream=None, flags: int = 0, workspace=None):
     """y = x . dequant(W)^T for torch CUDA tensors (x bf16 [M,K]; w_packed int32/uint32
     [N, K*bits/32]; scales/biases bf16 [N, K/group_size]).  Returns y bf16 [M, N]."""
     import torch
@@ -234,9 +248,16 @@ def matmul(x, w_packed, scales, biases, out=None, *, group_size: int = 64, bits:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     if stream is None:
         stream = torch.cuda.current_stream(x.device)
-    st = aq_matmul_bf16_ex(x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(), biases.data_ptr(),
-                           out.data_ptr(), M, N, K, group_size, bits, _KERNELS[kernel],
-                           (AQ_FLAG_PDL if pdl else 0) | flags, stream.cuda_stream)
+    if workspace is not None:
+        if kernel != "auto" or pdl or flags:
+            raise ValueError("a workspace goes with the default kernel choice and no flags")
+        st = aq_matmul_bf16_ws(x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(), biases.data_ptr(),
+                               out.data_ptr(), M, N, K, group_size, bits, workspace.data_ptr(), workspace.numel(),
+                               stream.cuda_stream)
+    else:
+        st = aq_matmul_bf16_ex(x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(), biases.data_ptr(),
+                               out.data_ptr(), M, N, K, group_size, bits, _KERNELS[kernel],
+                               (AQ_FLAG_PDL if pdl else 0) | flags, stream.cuda_stream)
     if st != AQ_OK:
         raise AqError(st, "aq_matmul_bf16_ex")
     return out

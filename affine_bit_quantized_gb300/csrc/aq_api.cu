@@ -74,13 +74,10 @@ aq_status validate(const void *x, const uint32_t *w, const void *s, const void *
     return AQ_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-aq_status aq_matmul_bf16_ex(const void *x, const uint32_t *w_packed, const void *scales,
-                            const void *biases, void *y, int64_t M, int64_t N, int64_t K,
-                            int group_size, int bits, int kernel, unsigned flags, void *stream) {
+// aq_matmul_bf16_ex, with an optional workspace for x converted once on the tensor-core path
+aq_status matmul_impl(const void *x, const uint32_t *w_packed, const void *scales, const void *biases, void *y,
+                      int64_t M, int64_t N, int64_t K, int group_size, int bits, int kernel, unsigned flags,
+                      void *workspace, size_t workspace_bytes, void *stream) {
     if (kernel != AQ_KERNEL_AUTO && kernel != AQ_KERNEL_QMV && kernel != AQ_KERNEL_QMM)
         return AQ_ERR_INVALID_ARG;
     if (flags & ~(unsigned)(AQ_FLAG_PDL | AQ_FLAG_DEBUG_SKIP_X)) return AQ_ERR_INVALID_ARG;
@@ -122,6 +119,7 @@ aq_status aq_matmul_bf16_ex(const void *x, const uint32_t *w_packed, const void 
     };
     if (kernel == AQ_KERNEL_QMM || (kernel == AQ_KERNEL_AUTO && M > kQmvMaxRows)) {
         if (a.debug_skip_x) return AQ_ERR_UNSUPPORTED;
+        if (workspace && aligned(workspace, 128) && workspace_bytes >= (size_t)(M * K * 2)) a.xf16 = workspace;
         if (aq::qmm_supported(a)) return record_cuda(aq::launch_qmm(a));
         if (kernel == AQ_KERNEL_QMM) return AQ_ERR_UNSUPPORTED;
     }
@@ -150,6 +148,28 @@ aq_status aq_matmul_bf16_ex(const void *x, const uint32_t *w_packed, const void 
         if (st != AQ_OK) return st;
     }
     return AQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+aq_status aq_matmul_bf16_ex(const void *x, const uint32_t *w_packed, const void *scales,
+                            const void *biases, void *y, int64_t M, int64_t N, int64_t K,
+                            int group_size, int bits, int kernel, unsigned flags, void *stream) {
+    return matmul_impl(x, w_packed, scales, biases, y, M, N, K, group_size, bits, kernel, flags, nullptr, 0, stream);
+}
+
+size_t aq_matmul_workspace_bytes(int64_t M, int64_t K) {
+    if (M <= kQmvMaxRows || K <= 0 || M > kMaxDim || K > kMaxDim) return 0;
+    return (size_t)(M * K * 2);
+}
+
+aq_status aq_matmul_bf16_ws(const void *x, const uint32_t *w_packed, const void *scales, const void *biases,
+                            void *y, int64_t M, int64_t N, int64_t K, int group_size, int bits, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+    return matmul_impl(x, w_packed, scales, biases, y, M, N, K, group_size, bits, AQ_KERNEL_AUTO, 0u, workspace,
+                       workspace_bytes, stream);
 }
 
 aq_status aq_matmul_bf16(const void *x, const uint32_t *w_packed, const void *scales,

@@ -53,28 +53,32 @@ constexpr int kConvWarps = 16;
 constexpr int kThreads = (2 + kConvWarps) * 32;
 constexpr int kConvThreads = kConvWarps * 32;
 constexpr int kSBGroups = 8;           // groups of scales/biases per TMA box (16 bytes per row)
-constexpr int kConvStages = 2;
 constexpr int kRawStages = 2;
 constexpr int kSBStages = 2;
 constexpr int kBTileBytes = kTileN * 128;          // 32768: fp16 W, 256 rows x 64 k
 constexpr int kSBBytes = kTileN * kSBGroups * 2;   // 4096 (scales, and again biases)
-// barriers: raw_full[2], raw_empty[2], sb_full[2], sb_empty[2], conv_full[2], conv_empty[2], acc_done
-constexpr int kNumBars = 2 * kRawStages + 2 * kSBStages + 2 * kConvStages + 1;
 
 // Shared-memory layout for a code width (offsets from a 1024-aligned base).
 // 4-bit codes: 256 rows of x per CTA (two UMMA M=128 halves); 8-bit codes
 // carry twice the raw bytes per W row, and 128 rows of x keep the stages
-// within the 227 KB a CTA may use.
-template <int BITS>
+// within the 227 KB a CTA may use.  XPRE: x arrives already in fp16 (in the
+// MMA's k order, from a conversion pass into the caller's workspace), copied
+// by TMA straight into the operand tile: no raw x stage, which leaves room
+// for a third converted stage.
+template <int BITS, bool XPRE = false>
 struct Cfg {
     static constexpr int kTileM = BITS == 4 ? 256 : 128;        // rows of x per CTA
     static constexpr int kHalves = kTileM / 128;                 // UMMA M=128 accumulators
+    static constexpr int kConvStages = XPRE ? 3 : 2;
     static constexpr int kATileBytes = kTileM * 128;             // fp16 x, kTileM rows x 64 k
     static constexpr int kConvStageBytes = kATileBytes + kBTileBytes;
-    static constexpr int kRawXBytes = kTileM * 128;              // bf16 x, same swizzled geometry
+    static constexpr int kRawXBytes = XPRE ? 0 : kTileM * 128;   // bf16 x, same swizzled geometry
     static constexpr int kRowWords = kGroup * BITS / 32;         // code words per W row and group
     static constexpr int kRawCodeBytes = kTileN * kRowWords * 4; // 8192 or 16384
     static constexpr int kRawStageBytes = kRawXBytes + kRawCodeBytes;
+    // barriers: raw_full[2], raw_empty[2], sb_full[2], sb_empty[2], conv_full[S], conv_empty[S], acc_done,
+    // and with XPRE x_full[S] (the x copy of a converted stage has landed)
+    static constexpr int kNumBars = 2 * kRawStages + 2 * kSBStages + 2 * kConvStages + 1 + (XPRE ? kConvStages : 0);
     static constexpr int kOffConv = 0;
     static constexpr int kOffRaw = kOffConv + kConvStages * kConvStageBytes;
     static constexpr int kOffSB = kOffRaw + kRawStages * kRawStageBytes;
@@ -82,7 +86,9 @@ struct Cfg {
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;     // tmem address, abort flag
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;     // + alignment slack
 };
-static_assert(Cfg<4>::kSmemBytes <= 232448 && Cfg<8>::kSmemBytes <= 232448, "shared memory per CTA");
+static_assert(Cfg<4>::kSmemBytes <= 232448 && Cfg<8>::kSmemBytes <= 232448 && Cfg<4, true>::kSmemBytes <= 232448 &&
+                  Cfg<8, true>::kSmemBytes <= 232448,
+              "shared memory per CTA");
 // split-K partials received by a CTA (at most 7 sources x its 32 columns x the tile's rows) fit in
 // the stage memory in front of the barriers
 constexpr int kMaxSplit = 8;
@@ -166,6 +172,12 @@ __device__ __forceinline__ uint32_t code_pair_f16(uint32_t v, uint32_t magic) {
     asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;" : "=r"(r) : "r"(v), "r"(magic));
     return r;
 }
+// Eight bf16 x values (one 16-byte chunk) as fp16 in the MMA's k order within the
+// chunk: (0,4,1,5,2,6,3,7) for 4-bit codes, (0,2,1,3,4,6,5,7) for 8-bit codes --
+// the order the code pairs of W come in.
+template <int BITS>
+__device__ __forceinline__ uint4 x_chunk_f16(uint4 v);
+
 // fp16x2 (1024 + byte 0, 1024 + byte 2) of a word: exact for bytes up to 255.
 __device__ __forceinline__ uint32_t byte_pair_f16(uint32_t v, uint32_t magic) {
     uint32_t r;
@@ -259,17 +271,55 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+template <int BITS>
+__device__ __forceinline__ uint4 x_chunk_f16(uint4 v) {
+    uint4 o;
+    if (BITS == 4) {
+        o.x = f32x2_to_f16x2(bf16lo(v.x), bf16lo(v.z));
+        o.y = f32x2_to_f16x2(bf16hi(v.x), bf16hi(v.z));
+        o.z = f32x2_to_f16x2(bf16lo(v.y), bf16lo(v.w));
+        o.w = f32x2_to_f16x2(bf16hi(v.y), bf16hi(v.w));
+    } else {
+        o.x = f32x2_to_f16x2(bf16lo(v.x), bf16lo(v.y));
+        o.y = f32x2_to_f16x2(bf16hi(v.x), bf16hi(v.y));
+        o.z = f32x2_to_f16x2(bf16lo(v.z), bf16lo(v.w));
+        o.w = f32x2_to_f16x2(bf16hi(v.z), bf16hi(v.w));
+    }
+    return o;
+}
+
+// x [rows][K] bf16 -> fp16 in the MMA's chunk order (x_chunk_f16), 16 bytes per
+// thread and step: the conversion every CTA of the tensor-core kernel would
+// otherwise repeat on its raw x tiles.
+template <int BITS>
+__global__ void x_to_f16_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ xf, int64_t vecs) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < vecs; i += (int64_t)gridDim.x * blockDim.x)
+        xf[i] = x_chunk_f16<BITS>(__ldg(x + i));
+}
+
+// A plain launch whose error comes back from the call itself (not through
+// cudaGetLastError, which would also report an earlier, unrelated failure).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_plain(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // GROUPED (expert-indexed matmul): x holds the rows gathered in expert order,
 // W, scales and biases are E matrices stacked along N, and `plan` lists the
 // work tiles {expert, first row, rows} (see gather_plan_kernel); CTA row
 // blockIdx.y takes tile blockIdx.y and exits at once if there is none.
-template <int BITS, bool GROUPED>
+template <int BITS, bool GROUPED, bool XPRE>
 __global__ void __launch_bounds__(kThreads, 1)
 qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
            const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_b,
            __nv_bfloat16 *__restrict__ y, int M, int N, int K, unsigned long long timeout_ns, int *status,
            const int *__restrict__ plan) {
-    using C = Cfg<BITS>;
+    using C = Cfg<BITS, XPRE>;
+    constexpr int kConvStages = C::kConvStages;
     constexpr int kTileM = C::kTileM, kATileBytes = C::kATileBytes, kConvStageBytes = C::kConvStageBytes;
     constexpr int kRawXBytes = C::kRawXBytes, kRawStageBytes = C::kRawStageBytes;
     constexpr int kOffConv = C::kOffConv, kOffRaw = C::kOffRaw, kOffSB = C::kOffSB, kOffMisc = C::kOffMisc;
@@ -285,7 +335,8 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     auto sb_empty = [&](int s) { return bar0 + 8 * (2 * kRawStages + kSBStages + s); };
     auto conv_full = [&](int s) { return bar0 + 8 * (2 * kRawStages + 2 * kSBStages + s); };
     auto conv_empty = [&](int s) { return bar0 + 8 * (2 * kRawStages + 2 * kSBStages + kConvStages + s); };
-    const uint32_t acc_done = bar0 + 8 * (kNumBars - 1);
+    const uint32_t acc_done = bar0 + 8 * (2 * kRawStages + 2 * kSBStages + 2 * kConvStages);
+    auto x_full = [&](int s) { return acc_done + 8 * (1 + s); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
 
@@ -321,6 +372,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             mbar_init(sb_empty(s), kConvWarps);
         }
         for (int s = 0; s < kConvStages; ++s) {
+            if (XPRE) mbar_init(x_full(s), 1);
             mbar_init(conv_full(s), kConvWarps);
             mbar_init(conv_empty(s), 1);
         }
@@ -400,7 +452,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int issued_raw = 0, issued_sb = 0;
+            int issued_raw = 0, issued_sb = 0, issued_conv = 0;
             bool ok = true;
             for (int i = 0; i < steps && ok; ++i) {
                 const int rs = i % kRawStages;
@@ -422,9 +474,21 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 }
                 const uint32_t dst = base + kOffRaw + rs * kRawStageBytes;
                 mbar_expect_tx(raw_full(rs), kRawStageBytes);
-                tma_load_2d(dst, &tm_x, (g0 + i) * kGroup, m0, raw_full(rs));
+                if (!XPRE) tma_load_2d(dst, &tm_x, (g0 + i) * kGroup, m0, raw_full(rs));
                 tma_load_2d(dst + kRawXBytes, &tm_w, (g0 + i) * C::kRowWords, wrow0, raw_full(rs));
                 issued_raw = i + 1;
+                if (XPRE) {
+                    // fp16 x straight into the converted stage, once the MMAs have released it
+                    const int cs = i % kConvStages;
+                    if (i >= kConvStages &&
+                        !mbar_wait(conv_empty(cs), ((i / kConvStages) - 1) & 1, deadline, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(x_full(cs), kATileBytes);
+                    tma_load_2d(base + kOffConv + cs * kConvStageBytes, &tm_x, (g0 + i) * kGroup, m0, x_full(cs));
+                    issued_conv = i + 1;
+                }
             }
             if (!ok) {
                 fail();
@@ -436,6 +500,11 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 for (int j = (issued_sb > kSBStages ? issued_sb - kSBStages : 0); j < issued_sb; ++j)
                     while (!mbar_try_wait(sb_full(j % kSBStages), (j / kSBStages) & 1) && global_timer() < drain) {
                     }
+                if (XPRE)
+                    for (int i = (issued_conv > kConvStages ? issued_conv - kConvStages : 0); i < issued_conv; ++i)
+                        while (!mbar_try_wait(x_full(i % kConvStages), (i / kConvStages) & 1) &&
+                               global_timer() < drain) {
+                        }
             }
         }
     } else if (warp == 1) {
@@ -443,7 +512,8 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         if (lane == 0) {
             for (int i = 0; i < steps; ++i) {
                 const int cs = i % kConvStages;
-                if (!mbar_wait(conv_full(cs), (i / kConvStages) & 1, deadline, abort_flag)) {
+                if (!mbar_wait(conv_full(cs), (i / kConvStages) & 1, deadline, abort_flag) ||
+                    (XPRE && !mbar_wait(x_full(cs), (i / kConvStages) & 1, deadline, abort_flag))) {
                     fail();
                     break;
                 }
@@ -488,22 +558,9 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             // each chunk's k order becoming (0,4,1,5,2,6,3,7) for 4-bit codes
             // and (0,2,1,3,4,6,5,7) for 8-bit codes (the order the W pairs come in)
 #pragma unroll 4
-            for (int c = 0; c < kRawXBytes / 16 / kConvThreads; ++c) {
+            for (int c = 0; c < (XPRE ? 0 : C::kRawXBytes / 16 / kConvThreads); ++c) {
                 const uint32_t off = (uint32_t)((c * kConvThreads + t) * 16);
-                const uint4 v = lds128(raw + off);
-                uint4 o;
-                if (BITS == 4) {
-                    o.x = f32x2_to_f16x2(bf16lo(v.x), bf16lo(v.z));
-                    o.y = f32x2_to_f16x2(bf16hi(v.x), bf16hi(v.z));
-                    o.z = f32x2_to_f16x2(bf16lo(v.y), bf16lo(v.w));
-                    o.w = f32x2_to_f16x2(bf16hi(v.y), bf16hi(v.w));
-                } else {
-                    o.x = f32x2_to_f16x2(bf16lo(v.x), bf16lo(v.y));
-                    o.y = f32x2_to_f16x2(bf16hi(v.x), bf16hi(v.y));
-                    o.z = f32x2_to_f16x2(bf16lo(v.z), bf16lo(v.w));
-                    o.w = f32x2_to_f16x2(bf16hi(v.z), bf16hi(v.w));
-                }
-                sts128(conv + off, o);
+                sts128(conv + off, x_chunk_f16<BITS>(lds128(raw + off)));
             }
             // W: thread t takes half of row r = t / 2 (chunks 4h..4h+3, h = t % 2) and
             // converts the row's scale and bias once; each chunk of 8 codes
@@ -683,7 +740,7 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *gaddr, uint
 }
 
 constexpr int kMaxDevices = 64;
-std::atomic<int> g_attr_done[2][kMaxDevices];
+std::atomic<int> g_attr_done[4][kMaxDevices];
 std::atomic<int> g_attr_done_grouped[2][kMaxDevices];
 std::atomic<int> g_sms[kMaxDevices];
 // clusters of 2, 4, 8 CTAs that can be resident at once, per code width (0: not yet asked; -1: none)
@@ -697,19 +754,26 @@ bool qmm_supported(const MatmulArgs &a) {
 }
 
 namespace {
-template <int BITS>
+template <int BITS, bool XPRE>
 cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev) {
-    using C = Cfg<BITS>;
-    const int bi = BITS == 8 ? 1 : 0;
+    using C = Cfg<BITS, XPRE>;
+    const int bi = (BITS == 8 ? 1 : 0) + (XPRE ? 2 : 0);
     if (!g_attr_done[bi][dev].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(qmm_kernel<BITS, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(qmm_kernel<BITS, false, XPRE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
         if (e != cudaSuccess) return e;
         g_attr_done[bi][dev].store(1, std::memory_order_release);
     }
     const int M = (int)a.M, N = (int)a.N, K = (int)a.K, G = K / 64;
+    if (XPRE) {
+        const int64_t vecs = (int64_t)M * K / 8;
+        cudaError_t e = launch_plain(x_to_f16_kernel<BITS>, dim3((unsigned)std::min<int64_t>((vecs + 255) / 256, 4096)),
+                                     dim3(256), a.stream, static_cast<const uint4 *>(a.x), static_cast<uint4 *>(a.xf16),
+                                     vecs);
+        if (e != cudaSuccess) return e;
+    }
     CUtensorMap tx, tw, ts, tb;
-    if (!encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, kGroup,
+    if (!encode_2d(&tx, XPRE ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, XPRE ? a.xf16 : a.x, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, kGroup,
                    C::kTileM, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.w, (uint64_t)K * BITS / 32, (uint64_t)N,
                    (uint64_t)K * BITS / 8, C::kRowWords, kTileN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
@@ -744,9 +808,21 @@ cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev) {
         for (int si = 2; si >= 0 && split == 1; --si) {
             const int S = 2 << si;
             if (S > K / (kGroup * kSBGroups) || tiles * S > sms) continue;
-            int n = g_max_clusters[bi][si][dev].load(std::memory_order_relaxed);
+            // decided on the kernel without the workspace, so that both variants split alike
+            // (same summation order, same bits)
+            const int bb = BITS == 8 ? 1 : 0;
+            int n = g_max_clusters[bb][si][dev].load(std::memory_order_relaxed);
             if (n == 0) {
+                using C0 = Cfg<BITS, false>;
+                if (!g_attr_done[bb][dev].load(std::memory_order_acquire)) {
+                    if (cudaFuncSetAttribute(qmm_kernel<BITS, false, false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C0::kSmemBytes) != cudaSuccess)
+                        cudaGetLastError();
+                    else
+                        g_attr_done[bb][dev].store(1, std::memory_order_release);
+                }
                 cudaLaunchConfig_t q = cfg;
+                q.dynamicSmemBytes = C0::kSmemBytes;
                 q.gridDim = dim3(1, 1, (unsigned)S);
                 cudaLaunchAttribute ca;
                 ca.id = cudaLaunchAttributeClusterDimension;
@@ -755,11 +831,11 @@ cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev) {
                 ca.val.clusterDim.z = (unsigned)S;
                 q.attrs = &ca;
                 q.numAttrs = 1;
-                if (cudaOccupancyMaxActiveClusters(&n, qmm_kernel<BITS, false>, &q) != cudaSuccess || n < 1) {
+                if (cudaOccupancyMaxActiveClusters(&n, qmm_kernel<BITS, false, false>, &q) != cudaSuccess || n < 1) {
                     cudaGetLastError();   // the query's error is not the caller's
                     n = -1;
                 }
-                g_max_clusters[bi][si][dev].store(n, std::memory_order_relaxed);
+                g_max_clusters[bb][si][dev].store(n, std::memory_order_relaxed);
             }
             if (n >= tiles) split = S;
         }
@@ -774,7 +850,7 @@ cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev) {
     }
     cfg.attrs = attr;
     cfg.numAttrs = (unsigned)na;
-    return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS, false>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(a.y), M,
+    return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS, false, XPRE>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(a.y), M,
                               N, K, (unsigned long long)a.timeout_ns, a.status, (const int *)nullptr);
 }
 }  // namespace
@@ -784,7 +860,8 @@ cudaError_t launch_qmm(const MatmulArgs &a) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    return a.bits == 8 ? launch_qmm_bits<8>(a, dev) : launch_qmm_bits<4>(a, dev);
+    if (a.xf16) return a.bits == 8 ? launch_qmm_bits<8, true>(a, dev) : launch_qmm_bits<4, true>(a, dev);
+    return a.bits == 8 ? launch_qmm_bits<8, false>(a, dev) : launch_qmm_bits<4, false>(a, dev);
 }
 
 // ---------------------------------------------------------------- expert-indexed matmul
@@ -841,15 +918,17 @@ gather_plan_kernel(const int *__restrict__ lhs, const int *__restrict__ rhs, int
             tiles[tile_off[e] + i] = make_int4(e, row_off[e] + i * tile_m, min(tile_m, cnt[e] - i * tile_m), 0);
 }
 
-// x rows in row order of the matmul: xg[r] = x[lhs[r]] (zeros for an index out
+// x rows in row order of the matmul, converted once to the tensor-core
+// kernel's fp16 chunk order: xg[r] = f16(x[lhs[r]]) (zeros for an index out
 // of range, which the plan kernel reports), 16 bytes per thread and step.
+template <int BITS>
 __global__ void gather_rows_kernel(const uint4 *__restrict__ x, const int *__restrict__ lhs, uint4 *__restrict__ xg,
                                    int R, int T, int row_vecs) {
     const int64_t total = (int64_t)R * row_vecs;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = i / row_vecs, c = i - r * row_vecs;
         const int l = __ldg(lhs + r);
-        xg[i] = (l >= 0 && l < T) ? __ldg(x + (int64_t)l * row_vecs + c) : make_uint4(0u, 0u, 0u, 0u);
+        xg[i] = (l >= 0 && l < T) ? x_chunk_f16<BITS>(__ldg(x + (int64_t)l * row_vecs + c)) : make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
@@ -858,10 +937,10 @@ int64_t plan_bytes(int64_t R, int64_t E) { return (kPlanHeaderInts * 4 + 16 * pl
 
 template <int BITS>
 cudaError_t launch_gather_bits(const GatherArgs &g, int dev, int sms) {
-    using C = Cfg<BITS>;
+    using C = Cfg<BITS, true>;
     const int bi = BITS == 8 ? 1 : 0;
     if (!g_attr_done_grouped[bi][dev].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(qmm_kernel<BITS, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(qmm_kernel<BITS, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
         if (e != cudaSuccess) return e;
         g_attr_done_grouped[bi][dev].store(1, std::memory_order_release);
@@ -869,15 +948,14 @@ cudaError_t launch_gather_bits(const GatherArgs &g, int dev, int sms) {
     const int R = (int)g.R, N = (int)g.N, K = (int)g.K, E = (int)g.E, G = K / 64;
     int *plan = static_cast<int *>(g.workspace);
     void *xg = static_cast<uint8_t *>(g.workspace) + plan_bytes(g.R, g.E);
-    gather_plan_kernel<<<1, kPlanThreads, 0, g.stream>>>(g.lhs, g.rhs, R, (int)g.T, E, C::kTileM, plan, g.status);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_plain(gather_plan_kernel, dim3(1), dim3(kPlanThreads), g.stream, g.lhs, g.rhs, R,
+                                 (int)g.T, E, (int)C::kTileM, plan, g.status);
     if (e != cudaSuccess) return e;
-    gather_rows_kernel<<<sms * 4, 256, 0, g.stream>>>(static_cast<const uint4 *>(g.x), g.lhs, static_cast<uint4 *>(xg),
-                                                       R, (int)g.T, K / 8);
-    e = cudaGetLastError();
+    e = launch_plain(gather_rows_kernel<BITS>, dim3((unsigned)(sms * 4)), dim3(256), g.stream,
+                     static_cast<const uint4 *>(g.x), g.lhs, static_cast<uint4 *>(xg), R, (int)g.T, K / 8);
     if (e != cudaSuccess) return e;
     CUtensorMap tx, tw, ts, tb;
-    if (!encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xg, (uint64_t)K, (uint64_t)R, (uint64_t)K * 2, kGroup,
+    if (!encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xg, (uint64_t)K, (uint64_t)R, (uint64_t)K * 2, kGroup,
                    C::kTileM, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, g.w, (uint64_t)K * BITS / 32, (uint64_t)E * N,
                    (uint64_t)K * BITS / 8, C::kRowWords, kTileN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
@@ -892,7 +970,7 @@ cudaError_t launch_gather_bits(const GatherArgs &g, int dev, int sms) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = g.stream;
-    return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS, true>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(g.y), R, N,
+    return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS, true, true>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(g.y), R, N,
                               K, (unsigned long long)g.timeout_ns, g.status, (const int *)plan);
 }
 

@@ -576,28 +576,42 @@ def main():
                 xq = torch.from_numpy(synth.make_x(M, K, synth.seed_for(5, M, 9)).view(np.int16)).to(dev)
                 yq = torch.empty((M, N), dtype=torch.int16, device=dev)
 
-                def qlaunch(i, ws=ws, xq=xq, yq=yq, M=M, N=N, K=K, bits=bits):
-                    wt, st, bt = ws[i % copies]
-                    rc = lib.aq_matmul_bf16_ex(xq.data_ptr(), wt.data_ptr(), st.data_ptr(), bt.data_ptr(),
-                                               yq.data_ptr(), M, N, K, 64, bits, aq.AQ_KERNEL_AUTO, 0, cur.cuda_stream)
-                    if rc != aq.AQ_OK:
-                        raise aq.AqError(rc, "aq_matmul_bf16_ex")
+                xws = torch.empty(aq.aq_matmul_workspace_bytes(M, K), dtype=torch.uint8, device=dev)
 
-                for i in range(3):
-                    qlaunch(i)
-                torch.cuda.synchronize(dev)
-                reps = 10
-                e0.record(cur)
-                for i in range(reps):
-                    qlaunch(i)
-                e1.record(cur)
-                e1.synchronize()
-                us = e0.elapsed_time(e1) * 1e3 / reps
+                def qlaunch(i, ws=ws, xq=xq, yq=yq, M=M, N=N, K=K, bits=bits, xws=xws, use_ws=True):
+                    wt, st, bt = ws[i % copies]
+                    if use_ws:   # x converted once into the workspace (aq_matmul_bf16_ws)
+                        rc = lib.aq_matmul_bf16_ws(xq.data_ptr(), wt.data_ptr(), st.data_ptr(), bt.data_ptr(),
+                                                   yq.data_ptr(), M, N, K, 64, bits, xws.data_ptr(), xws.numel(),
+                                                   cur.cuda_stream)
+                    else:
+                        rc = lib.aq_matmul_bf16_ex(xq.data_ptr(), wt.data_ptr(), st.data_ptr(), bt.data_ptr(),
+                                                   yq.data_ptr(), M, N, K, 64, bits, aq.AQ_KERNEL_AUTO, 0,
+                                                   cur.cuda_stream)
+                    if rc != aq.AQ_OK:
+                        raise aq.AqError(rc, "qmm call")
+
+                def time_q(use_ws, reps=10):
+                    for i in range(3):
+                        qlaunch(i, use_ws=use_ws)
+                    torch.cuda.synchronize(dev)
+                    e0.record(cur)
+                    for i in range(reps):
+                        qlaunch(i, use_ws=use_ws)
+                    e1.record(cur)
+                    e1.synchronize()
+                    return e0.elapsed_time(e1) * 1e3 / reps
+
+                us = time_q(True)
+                us_plain = time_q(False)
                 tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
                 key = f"M{M}_K{K}_N{N}" + ("" if bits == 4 else "_8bit")
                 qmm[key] = {"us_per_call": round(us, 2), "tflops": round(tf, 1),
                             "frac_of_bf16_burst": round(tf / bf16_peak, 4),
-                            "frac_of_bf16_sustained": round(tf / bf16_sus, 4)}
+                            "frac_of_bf16_sustained": round(tf / bf16_sus, 4),
+                            "without_workspace_us": round(us_plain, 2),
+                            "without_workspace_tflops": round(2.0 * M * N * K / (us_plain * 1e-6) / 1e12, 1)}
+                del xws
             del ws
 
     # ---- NVFP4 weights (E2M1 codes, E4M3 scale per 16, fp32 tensor scale), M = 1, the step's shapes:

@@ -237,6 +237,22 @@ aq_status aq_chain_run_static(const aq_matmul_desc *descs, int count, int group_
 /* Static, NUL-terminated name of a status code. */
 const char *aq_status_string(aq_status status);
 
+/* Workspace with which aq_matmul_bf16_ws converts x once for the tensor-core
+ * kernel: M*K*2 bytes where that kernel is taken (M > 16), else 0. */
+size_t aq_matmul_workspace_bytes(int64_t M, int64_t K);
+
+/* aq_matmul_bf16 with a caller workspace (device, 128-byte aligned, owned by
+ * the caller, at least aq_matmul_workspace_bytes(M, K) bytes): on the
+ * tensor-core path x is converted to fp16 once into the workspace (one extra
+ * launch) and copied by TMA straight into the MMA operand tiles, instead of
+ * every CTA converting its x tiles again; the results are bit-identical to
+ * aq_matmul_bf16's.  A null or smaller workspace gives aq_matmul_bf16's path.
+ * Other arguments, errors and numerics as aq_matmul_bf16. */
+aq_status aq_matmul_bf16_ws(const void *x, const uint32_t *w_packed, const void *scales,
+                            const void *biases, void *y, int64_t M, int64_t N, int64_t K,
+                            int group_size, int bits, void *workspace, size_t workspace_bytes,
+                            void *stream);
+
 /*
  * Expert-indexed matmul for mixture-of-experts prefill: MLX's gather_qmm with
  * transposed weights, the grouped-GEMM path behind the MoE prefill gap of

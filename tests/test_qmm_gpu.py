@@ -138,3 +138,28 @@ def test_qmm_split_k(dev, M, N, K, bits):
     y2 = aq.matmul(xt, wt, st, bt, kernel="qmm", bits=bits)
     torch.cuda.synchronize()
     assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("M,N,K,bits", [
+    (17, 64, 512, 4), (300, 700, 2048, 4), (256, 512, 4096, 4), (2048, 1024, 4096, 4),
+    (129, 300, 1024, 8), (1000, 257, 4096, 8),
+])
+def test_qmm_workspace_path_same_bits(dev, M, N, K, bits):
+    """With a workspace, x is converted to fp16 once and copied straight into
+    the MMA tiles: the same bits as without, and the oracle's result class."""
+    import torch
+    w = synth.make_weights(N, K, 1400 + M, bits=bits)
+    x = synth.make_x(M, K, 1400 + M)
+    xt, wt, st, bt = upload(x, w, dev)
+    ws = torch.empty(aq.aq_matmul_workspace_bytes(M, K), dtype=torch.uint8, device=dev)
+    assert ws.numel() == M * K * 2
+    a = aq.matmul(xt, wt, st, bt, bits=bits)
+    b = aq.matmul(xt, wt, st, bt, bits=bits, workspace=ws)
+    b2 = aq.matmul(xt, wt, st, bt, bits=bits, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(b, b2), "the workspace path is not deterministic"
+    diff = (a.view(torch.int16) != b.view(torch.int16))
+    assert not diff.any(), f"{int(diff.sum())} of {diff.numel()} outputs differ, rows {diff.any(1).nonzero()[:8].flatten().tolist()}"
+    if M * N <= 300 * 700:
+        _, ref = oracle.matmul(x, w.w_packed, w.scales, w.biases, M, N, K, bits=bits)
+        assert_parity(from_dev_bf16(b), ref, what=f"qmm workspace M={M} N={N} K={K}")
