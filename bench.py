@@ -237,12 +237,18 @@ def run_case(args):
     kernel = {"auto": aq.AQ_KERNEL_AUTO, "qmv": aq.AQ_KERNEL_QMV, "qmm": aq.AQ_KERNEL_QMM}[args.kernel]
     stream = torch.cuda.current_stream(dev)
 
+    xws = torch.empty(max(1, aq.aq_matmul_workspace_bytes(M, K)), dtype=torch.uint8, device=dev)
+
     def launch(i):
         wt, st, bt = ws[i % copies]
-        rc = lib.aq_matmul_bf16_ex(xt.data_ptr(), wt.data_ptr(), st.data_ptr(), bt.data_ptr(), yt.data_ptr(), M, N,
-                                   K, 64, 4, kernel, 0, stream.cuda_stream)
+        if args.workspace:
+            rc = lib.aq_matmul_bf16_ws(xt.data_ptr(), wt.data_ptr(), st.data_ptr(), bt.data_ptr(), yt.data_ptr(), M,
+                                       N, K, 64, 4, xws.data_ptr(), xws.numel(), stream.cuda_stream)
+        else:
+            rc = lib.aq_matmul_bf16_ex(xt.data_ptr(), wt.data_ptr(), st.data_ptr(), bt.data_ptr(), yt.data_ptr(), M,
+                                       N, K, 64, 4, kernel, 0, stream.cuda_stream)
         if rc != aq.AQ_OK:
-            raise aq.AqError(rc, "aq_matmul_bf16_ex")
+            raise aq.AqError(rc, "matmul call")
 
     for i in range(args.warmup):
         launch(i)
@@ -299,6 +305,8 @@ def main():
     ap.add_argument("--case", default=None,
                     help="M,N,K: time one matrix shape instead of the decode step (also the ncu target)")
     ap.add_argument("--kernel", choices=("auto", "qmv", "qmm"), default="auto", help="kernel for --case")
+    ap.add_argument("--workspace", action="store_true",
+                    help="--case through aq_matmul_bf16_ws (x converted once for the tensor-core kernel)")
     ap.add_argument("--step-impl", choices=("chain", "graph"), default="chain",
                     help="decode step as one persistent chained launch (aq_chain_run) or as a CUDA graph of "
                          "one aq_matmul_bf16_ex launch per matrix; the other is reported as 'alt'")
