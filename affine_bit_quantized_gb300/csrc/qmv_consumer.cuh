@@ -450,6 +450,39 @@ __device__ __forceinline__ bool reduce_tile(const TileCtx &t, int tcount, int ti
     const int n_out = kRows * M;
     if (!mbar_wait_for(t.red_full + 8 * b, (uint32_t)(tcount / B) & 1u, timeout_ns, abort_flag)) return false;
     const float *rb = t.red + b * kConsumerWarps * n_out;
+    if (!ONE_ROW && (M & 3) == 0) {
+        // four outputs (one row of W, four rows of x) per lane and step: 16-byte
+        // loads and paired adds, the same warp order as below, so the same sums
+        for (int idx = lane * 4; idx < n_out; idx += 128) {
+            const float4 f0 = *reinterpret_cast<const float4 *>(rb + idx);
+            float2 lo = make_float2(f0.x, f0.y), hi = make_float2(f0.z, f0.w);
+#pragma unroll
+            for (int w = 1; w < kConsumerWarps; ++w) {
+                const float4 f = *reinterpret_cast<const float4 *>(rb + w * n_out + idx);
+                lo = add2(lo, make_float2(f.x, f.y));
+                hi = add2(hi, make_float2(f.z, f.w));
+            }
+            if (pass > 0) {
+                const float4 a = *reinterpret_cast<const float4 *>(yacc + idx);
+                lo = add2(make_float2(a.x, a.y), lo);
+                hi = add2(make_float2(a.z, a.w), hi);
+            }
+            const int row = idx / M, m = idx - row * M;
+            const int n = tile * kRows + row;
+            if (pass + 1 < passes) {
+                *reinterpret_cast<float4 *>(yacc + idx) = make_float4(lo.x, lo.y, hi.x, hi.y);
+            } else if (n < N) {
+                __nv_bfloat16 *yp = y + (int64_t)m * N + n;
+                yp[0] = __float2bfloat16_rn(lo.x * yscale);
+                yp[N] = __float2bfloat16_rn(lo.y * yscale);
+                yp[2 * (int64_t)N] = __float2bfloat16_rn(hi.x * yscale);
+                yp[3 * (int64_t)N] = __float2bfloat16_rn(hi.y * yscale);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(t.red_empty + 8 * b);
+        return true;
+    }
     for (int idx = lane; idx < n_out; idx += 32) {
         const int row = idx / M, m = idx - row * M;
         const int n = tile * kRows + row;
