@@ -483,6 +483,27 @@ __device__ __forceinline__ bool reduce_tile(const TileCtx &t, int tcount, int ti
         if (lane == 0) mbar_arrive(t.red_empty + 8 * b);
         return true;
     }
+    if (!ONE_ROW && (M & 1) == 0) {
+        // two outputs per lane and step (8-byte loads, paired adds), same order
+        for (int idx = lane * 2; idx < n_out; idx += 64) {
+            float2 v = *reinterpret_cast<const float2 *>(rb + idx);
+#pragma unroll
+            for (int w = 1; w < kConsumerWarps; ++w) v = add2(v, *reinterpret_cast<const float2 *>(rb + w * n_out + idx));
+            if (pass > 0) v = add2(*reinterpret_cast<const float2 *>(yacc + idx), v);
+            const int row = idx / M, m = idx - row * M;
+            const int n = tile * kRows + row;
+            if (pass + 1 < passes) {
+                *reinterpret_cast<float2 *>(yacc + idx) = v;
+            } else if (n < N) {
+                __nv_bfloat16 *yp = y + (int64_t)m * N + n;
+                yp[0] = __float2bfloat16_rn(v.x * yscale);
+                yp[N] = __float2bfloat16_rn(v.y * yscale);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(t.red_empty + 8 * b);
+        return true;
+    }
     for (int idx = lane; idx < n_out; idx += 32) {
         const int row = idx / M, m = idx - row * M;
         const int n = tile * kRows + row;

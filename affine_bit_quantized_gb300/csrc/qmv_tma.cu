@@ -379,16 +379,19 @@ cudaError_t device_sms(int *dev, int *sms) {
 }
 }  // namespace
 
-// Several K passes pay a staging of x (from L2) and a round of tile sums per
-// pass.  Measured on GB300 against the general kernel: one pass always wins;
-// with one stage per pass (M > 4 at K > 2048) the TMA kernel wins only where
-// every SM has tiles to stream (4096 x 14336 at M = 8: 40 us against 25 us;
-// 14336 x 4096: 23 us against 26 us).
+// Measured on GB300 against the general kernel (graph-replayed calls, weights
+// not in L2): the TMA kernel wins wherever every SM gets a tile (14336 x 4096:
+// 12.7-20 us against 24-25 us at M = 2..8; the 128256-row matrix: 58-91 us
+// against 179-185 us) and, for M <= 3, down to 64 tiles (4096 x 14336 at M = 2:
+// 17 us against 23 us); with fewer tiles or more rows the general kernel's
+// shorter start wins (4096 x 4096 at M = 8: 8.0 us against 12.8 us; 1024 x
+// 4096 at M = 2: 5.7 us against 6.2 us).  One row always takes the TMA kernel.
 bool qmv_tma_preferred(const MatmulArgs &a) {
+    if (a.M == 1) return true;
     int dev = 0, sms = 0;
     if (device_sms(&dev, &sms) != cudaSuccess) return true;
     const int T = (int)((a.N + kRows - 1) / kRows);
-    return qmv_tma_passes(a) == 1 || stages_per_pass((int)a.M, a.bits) >= 2 || T >= sms;
+    return T >= sms || (a.M <= 3 && T >= 64);
 }
 
 cudaError_t launch_qmv_tma(const MatmulArgs &a) {
