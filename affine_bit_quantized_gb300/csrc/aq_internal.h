@@ -37,8 +37,8 @@ constexpr int AQ_DEVICE_STATUS_BAD_INDEX = 6;
 // 1 <= M <= 16, N >= 1, K >= 64.
 cudaError_t launch_qmv(const MatmulArgs &a);
 
-// TMA-fed weight-streaming kernel (qmv_tma.cu) for 1 <= M <= 8,
-// K % 512 == 0, M*K <= 16384 and 16-byte aligned scales/biases.
+// TMA-fed weight-streaming kernel (qmv_tma.cu) for 1 <= M <= 8, K % 512 == 0
+// and 16-byte aligned scales/biases (x beyond 32 KB: K in passes).
 // the driver's tensor-map encoder (null if the driver does not offer it)
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 // tensor map of packed codes for the decode kernels: a stage (32 rows x 1024 bytes) per copy
