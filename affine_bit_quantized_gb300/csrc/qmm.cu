@@ -7,8 +7,9 @@
 // the hundreds to thousands the work is a real dense contraction, so here it
 // runs on tcgen05.mma with fp32 accumulators in tensor memory (TMEM):
 //
-//   * CTA tile 256 (rows of x) x 256 (rows of W), K walked one group of 64 at
-//     a time; two 128 x 256 fp32 accumulators fill the 512 TMEM columns.
+//   * CTA tile 256 (rows of x; 128 for 8-bit codes) x 256 (rows of W), K
+//     walked one group of 64 at a time; two 128 x 256 fp32 accumulators fill
+//     the 512 TMEM columns.
 //   * warp 0 (one thread) streams raw tiles with TMA: x (bf16, 128-byte
 //     swizzle), the packed codes of the 256 W rows, and every 8 groups the
 //     rows' bf16 scales and biases;
@@ -19,13 +20,20 @@
 //     bf16 to fp16.  fp16 rather than bf16 because a bf16 weight (8-bit
 //     significand) perturbs y by about twice the tolerance on these shapes,
 //     while fp16 (11 bits) stays about 6 sigma inside it.  Inside every
-//     8-element chunk both operands use the k order (0,4,1,5,2,6,3,7), which
-//     lets one LOP3 build a pair of codes; the dot product is unchanged;
+//     8-element chunk both operands use the k order (0,4,1,5,2,6,3,7)
+//     ((0,2,1,3,4,6,5,7) for 8-bit codes), which lets one LOP3 build a pair
+//     of codes; the dot product is unchanged;
+//   * with a caller workspace (XPRE) x is converted to fp16 once by a small
+//     kernel and the TMA copies it straight into the operand tile: the
+//     converters only build W, and the freed raw x stage becomes a third
+//     converted stage (the expert-indexed path always works this way);
 //   * warp 1 allocates TMEM and one of its threads issues the MMAs
 //     (M=128, N=256, K=16, both operands from shared memory), committing each
 //     consumed stage back to the converters through an mbarrier;
 //   * after the last group, warps 2..9 read the accumulators with tcgen05.ld,
-//     round to bf16 and store y.
+//     round to bf16 and store y; with few output tiles, K is split across a
+//     cluster and the partial tiles are added through distributed shared
+//     memory first (see the epilogue).
 //
 // Every mbarrier wait is bounded by a global-timer deadline; on expiry the
 // kernel records a timeout in the device status word, stops issuing work,

@@ -274,7 +274,8 @@ aq_status aq_matmul_bf16_ws(const void *x, const uint32_t *w_packed, const void 
  *   K a multiple of 512; group_size 64; bits 4 or 8.
  *   workspace    device, 128-byte aligned, at least
  *                aq_gather_qmm_workspace_bytes(R, K, E) bytes, owned by the
- *                caller (the work plan and x's rows in row order, R*K*2 bytes)
+ *                caller (the work plan, and x's rows in row order converted to
+ *                fp16 for the tensor cores: R*K*2 bytes)
  *   Alignment    x, w_packed, scales, biases 16-byte aligned; indices 4-byte;
  *                y 2-byte (AQ_ERR_ALIGNMENT otherwise).
  * Runs as three launches on `stream`: a plan of the work tiles per expert
