@@ -204,3 +204,24 @@ def test_nvfp4_validation(kw, expect):
     d.update(kw)
     assert aq.aq_matmul_nvfp4_bf16(d["x"], d["w"], d["s"], d["g"], d["y"], d["M"], d["N"], d["K"], d["flags"],
                                    None) == expect
+
+
+# ---------------------------------------------------------------- workspace variant: validation
+
+def test_matmul_workspace_bytes():
+    assert aq.aq_matmul_workspace_bytes(16, 4096) == 0          # decode path: no workspace used
+    assert aq.aq_matmul_workspace_bytes(17, 512) == 17 * 512 * 2
+    assert aq.aq_matmul_workspace_bytes(2048, 4096) == 2048 * 4096 * 2
+    assert aq.aq_matmul_workspace_bytes(-1, 4096) == 0
+
+
+@pytest.mark.parametrize("args", [dict(bits=3), dict(group_size=32), dict(K=96), dict(x=A + 8), dict(M=-1),
+                                  dict(x=None)])
+def test_ws_variant_rejects_like_the_plain_call(args):
+    p = dict(x=A, w=A, s=A, b=A, y=A, M=64, N=64, K=128, group_size=64, bits=4)
+    p.update(args)
+    plain = aq.aq_matmul_bf16(p["x"], p["w"], p["s"], p["b"], p["y"], p["M"], p["N"], p["K"], p["group_size"],
+                              p["bits"], None)
+    ws = aq.aq_matmul_bf16_ws(p["x"], p["w"], p["s"], p["b"], p["y"], p["M"], p["N"], p["K"], p["group_size"],
+                              p["bits"], A, 1 << 20, None)
+    assert plain != aq.AQ_OK and ws == plain

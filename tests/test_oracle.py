@@ -477,3 +477,11 @@ def test_nvfp4_one_hot_column_and_sampled():
     im, inn = np.array([0, 2, 1, 2]), np.array([0, 19, 7, 3])
     se, sb = oracle.nvfp4_matmul_sampled(x, w.w_packed, w.scales, w.global_scale, 3, N, K, im, inn)
     assert np.array_equal(se, ye[im, inn]) and np.array_equal(sb, yb[im, inn])
+
+
+def test_nvfp4_recipe():
+    w = synth.make_nvfp4_weights(64, 1024, 5)
+    codes = (w.w_packed[:, :, None] >> (4 * np.arange(8, dtype=np.uint32))) & 15
+    assert set(np.unique(codes)) == set(range(16))                       # every E2M1 encoding drawn
+    assert w.scales.min() >= 0x48 and w.scales.max() <= 0x7E             # finite, normal E4M3 scales
+    assert w.global_scale == 2.0 ** -13
