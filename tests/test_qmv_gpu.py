@@ -53,13 +53,15 @@ def test_small_batch_sweep(dev, M, name, N, K):
     check(dev, M, N, K, synth.seed_for(3, M, j))
 
 
-@pytest.mark.parametrize("M", [2, 16])
-def test_small_batch_lm_head_sampled(dev, M):
+@pytest.mark.parametrize("M,kernel", [(2, "qmv"), (16, "qmv"), (16, "auto"), (12, "auto")])
+def test_small_batch_lm_head_sampled(dev, M, kernel):
+    """The lm_head shape at small batch; with "auto", 9..16 rows run as two
+    launches of half the rows on the TMA kernel."""
     import torch
     _, N, K = synth.LLAMA8B_LM_HEAD
     w = synth.make_weights(N, K, synth.seed_for(3, M, 7))
     x = synth.make_x(M, K, synth.seed_for(3, M, 7))
-    got = run(dev, x, w)
+    got = run(dev, x, w, kernel=kernel)
     rng = np.random.default_rng(M)
     im = rng.integers(0, M, 4000)
     inn = rng.integers(0, N, 4000)
