@@ -268,6 +268,74 @@ def run_case(args):
                       "bf16_frac": round(tflops / bf16_peak, 4), "weight_copies": copies}), flush=True)
 
 
+def run_case_other(args):
+    """One NVFP4 shape (--nvfp4-case M,N,K) or one Mixtral-shaped MoE prefill
+    matrix (--moe-case w1_gate|w3_up|w2_down: 2048 tokens, top-2 of 8 experts),
+    timed through the C ABI with CUDA events; the ncu targets of those kernels."""
+    import torch
+
+    import affine_bit_quantized_gb300 as aq
+    from affine_bit_quantized_gb300 import _build
+
+    dev = torch.device("cuda", 0)
+    _build.build_library()
+    lib = aq.load()
+    stream = torch.cuda.current_stream(dev)
+    if args.nvfp4_case:
+        M, N, K = (int(v) for v in args.nvfp4_case.split(","))
+        w = synth.make_nvfp4_weights(N, K, 1)
+        copies = max(1, min(64, -(-3 * 129 * 2**20 // (w.w_packed.nbytes + w.scales.nbytes))))
+        ws = [(torch.from_numpy(w.w_packed.view(np.int32)).to(dev), torch.from_numpy(w.scales).to(dev))
+              for _ in range(copies)]
+        xt = torch.from_numpy(synth.make_x(M, K, 1).view(np.int16)).to(dev)
+        yt = torch.empty((M, N), dtype=torch.int16, device=dev)
+
+        def launch(i):
+            wt, st = ws[i % copies]
+            rc = lib.aq_matmul_nvfp4_bf16(xt.data_ptr(), wt.data_ptr(), st.data_ptr(), w.global_scale, yt.data_ptr(),
+                                          M, N, K, 0, stream.cuda_stream)
+            if rc != aq.AQ_OK:
+                raise aq.AqError(rc, "aq_matmul_nvfp4_bf16")
+        work = {"case": ["nvfp4", M, N, K], "bytes": alg_bytes(M, N, K)}
+    else:
+        name, N, K = [m for m in synth.MIXTRAL_EXPERT_MATS if m[0] == args.moe_case][0]
+        T, E, top_k = 2048, synth.MIXTRAL_EXPERTS, synth.MIXTRAL_TOP_K
+        lhs, rhs = synth.make_routing(T, E, top_k, synth.seed_for(6, 0, 9))
+        ew = synth.ExpertWeights(E, N, K, synth.seed_for(6, 0, 0))
+        wt = torch.from_numpy(ew.w_packed.view(np.int32)).to(dev)
+        st = torch.from_numpy(ew.scales.view(np.int16)).to(dev)
+        bt = torch.from_numpy(ew.biases.view(np.int16)).to(dev)
+        xt = torch.from_numpy(synth.make_x(T, K, 1).view(np.int16)).to(dev)
+        lt, rt = torch.from_numpy(lhs).to(dev), torch.from_numpy(rhs).to(dev)
+        R = int(lhs.size)
+        yt = torch.empty((R, N), dtype=torch.int16, device=dev)
+        wsp = torch.empty(aq.aq_gather_qmm_workspace_bytes(R, K, E), dtype=torch.uint8, device=dev)
+
+        def launch(i):
+            rc = lib.aq_gather_qmm_bf16(xt.data_ptr(), wt.data_ptr(), st.data_ptr(), bt.data_ptr(), lt.data_ptr(),
+                                        rt.data_ptr(), yt.data_ptr(), R, T, N, K, E, 64, 4, wsp.data_ptr(), wsp.numel(),
+                                        stream.cuda_stream)
+            if rc != aq.AQ_OK:
+                raise aq.AqError(rc, "aq_gather_qmm_bf16")
+        work = {"case": ["moe", name, T, E, top_k, N, K], "flops": 2.0 * R * N * K}
+    for i in range(args.warmup):
+        launch(i)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        launch(args.warmup + i)
+    e1.record(stream)
+    e1.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    out = {"case": work["case"], "us_per_call": round(us, 3)}
+    if "bytes" in work:
+        out["gbs"] = round(work["bytes"] / (us * 1e-6) / 1e9, 1)
+    else:
+        out["tflops"] = round(work["flops"] / (us * 1e-6) / 1e12, 1)
+    print(json.dumps(out), flush=True)
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for name in ("qmv_chain.cu", "qmv_tma.cu", "qmv_consumer.cuh", "aq_ptx.cuh"):
@@ -305,6 +373,9 @@ def main():
     ap.add_argument("--case", default=None,
                     help="M,N,K: time one matrix shape instead of the decode step (also the ncu target)")
     ap.add_argument("--kernel", choices=("auto", "qmv", "qmm"), default="auto", help="kernel for --case")
+    ap.add_argument("--nvfp4-case", default=None, help="M,N,K: time one NVFP4 shape (an ncu target)")
+    ap.add_argument("--moe-case", default=None, choices=[m[0] for m in synth.MIXTRAL_EXPERT_MATS],
+                    help="time one MoE prefill matrix (2048 tokens, top-2 of 8 experts; an ncu target)")
     ap.add_argument("--workspace", action="store_true",
                     help="--case through aq_matmul_bf16_ws (x converted once for the tensor-core kernel)")
     ap.add_argument("--step-impl", choices=("chain", "graph"), default="chain",
@@ -322,6 +393,9 @@ def main():
         return
     if args.case:
         run_case(args)
+        return
+    if args.nvfp4_case or args.moe_case:
+        run_case_other(args)
         return
 
     import torch
