@@ -56,16 +56,20 @@ constexpr int kQmvMaxRows = 16;                // rows of x per weight-streaming
 
 // At least four 32-row tiles per SM of the current device.
 bool many_tiles(int64_t N) {
-    static std::atomic<int> sms{0};
-    int n = sms.load(std::memory_order_relaxed);
+    constexpr int kDevices = 64;
+    static std::atomic<int> sms[kDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevices) {
+        cudaGetLastError();
+        return false;
+    }
+    int n = sms[dev].load(std::memory_order_relaxed);
     if (n == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
-                                                      cudaSuccess) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
             cudaGetLastError();
             return false;
         }
-        sms.store(n, std::memory_order_relaxed);
+        sms[dev].store(n, std::memory_order_relaxed);
     }
     return (N + 31) / 32 >= 4 * (int64_t)n;
 }
