@@ -161,6 +161,17 @@ class Chain:
 
         n = len(items)
         arr = (MatmulDesc * max(n, 1))()
+        named = []
+        for i, (x, w, s, b, y) in enumerate(items):
+            if x.dim() != 2 or w.dim() != 2:
+                raise ValueError(f"chain item {i}: x and w_packed must be 2-D")
+            at = f"chain item {i}: "
+            _check(at + "x", x, tuple(x.shape), "bf16")
+            _check_weights(w, s, b, (w.shape[0],), x.shape[1], group_size, bits, prefix=at)
+            _check(at + "y", y, (x.shape[0], w.shape[0]), "bf16")
+            named += [(at + "x", x), (at + "w_packed", w), (at + "scales", s), (at + "biases", b), (at + "y", y)]
+        if n:
+            _placed(items[0][0].device, named)
         for i, (x, w, s, b, y) in enumerate(items):
             flags = AQ_CHAIN_INDEPENDENT if (independent and independent[i]) else 0
             arr[i] = MatmulDesc(x.data_ptr(), w.data_ptr(), s.data_ptr(), b.data_ptr(), y.data_ptr(), x.shape[0],
@@ -233,33 +244,98 @@ def version() -> int:
 _KERNELS = {"auto": AQ_KERNEL_AUTO, "qmv": AQ_KERNEL_QMV, "qmm": AQ_KERNEL_QMM}
 
 
+def _kind_ok(t, kind: str) -> bool:
+    import torch
+
+    if kind == "bf16":
+        return t.dtype == torch.bfloat16
+    if kind == "word":   # packed codes: any 32-bit integer type (int32 or uint32)
+        return t.element_size() == 4 and not t.is_floating_point() and not t.is_complex()
+    if kind == "i32":
+        return t.dtype == torch.int32
+    if kind == "u8":
+        return t.dtype == torch.uint8
+    raise AssertionError(kind)
+
+
+def _check(name: str, t, shape, kind: str) -> None:
+    """Raise ValueError unless t has `shape` (None entries are free) and the
+    element type `kind`.  The C ABI sees only pointers, so a tensor smaller than
+    the shapes say would be read or written out of bounds: the sizes are checked
+    here, before any launch."""
+    if t.dim() != len(shape) or any(want is not None and int(got) != int(want) for got, want in zip(t.shape, shape)):
+        want = "[" + ", ".join("*" if w is None else str(int(w)) for w in shape) + "]"
+        raise ValueError(f"{name} has shape {list(t.shape)}, expected {want}")
+    if not _kind_ok(t, kind):
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {kind}")
+
+
+def _placed(device, named) -> None:
+    """Raise ValueError unless every (name, tensor) is a contiguous CUDA tensor on `device`."""
+    for name, t in named:
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+        if t.device != device:
+            raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _weight_cols(K: int, group_size: int, bits: int):
+    """(code words, groups) per weight row, or (None, None) where K, the group
+    size or the code width is one the library itself rejects."""
+    if group_size <= 0 or K % group_size or bits not in (4, 8) or (K * bits) % 32:
+        return None, None
+    return K * bits // 32, K // group_size
+
+
+def _check_weights(w_packed, scales, biases, lead, K: int, group_size: int, bits: int, prefix: str = "") -> None:
+    words, groups = _weight_cols(K, group_size, bits)
+    _check(prefix + "w_packed", w_packed, (*lead, words), "word")
+    _check(prefix + "scales", scales, (*lead, groups), "bf16")
+    _check(prefix + "biases", biases, (*lead, groups), "bf16")
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
 def matmul(x, w_packed, scales, biases, out=None, *, group_size: int = 64, bits: int = 4,
            kernel: str = "auto", pdl: bool = False, stream=None, flags: int = 0, workspace=None):
     """y = x . dequant(W)^T for torch CUDA tensors (x bf16 [M,K]; w_packed int32/uint32
     [N, K*bits/32]; scales/biases bf16 [N, K/group_size]).  Returns y bf16 [M, N]."""
     import torch
 
+    if x.dim() != 2 or w_packed.dim() != 2:
+        raise ValueError("x and w_packed must be 2-D")
     M, K = x.shape
     N = w_packed.shape[0]
-    for name, t in (("x", x), ("w_packed", w_packed), ("scales", scales), ("biases", biases)):
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if kernel not in _KERNELS:
+        raise ValueError(f"kernel must be one of {sorted(_KERNELS)}")
+    _check("x", x, (M, K), "bf16")
+    _check_weights(w_packed, scales, biases, (N,), K, group_size, bits)
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
-    if stream is None:
-        stream = torch.cuda.current_stream(x.device)
+    _check("out", out, (M, N), "bf16")
+    named = [("x", x), ("w_packed", w_packed), ("scales", scales), ("biases", biases), ("out", out)]
     if workspace is not None:
         if kernel != "auto" or pdl or flags:
             raise ValueError("a workspace goes with the default kernel choice and no flags")
+        _check("workspace", workspace, (None,), "u8")
+        named.append(("workspace", workspace))
+    _placed(x.device, named)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    if workspace is not None:
+        where = "aq_matmul_bf16_ws"
         st = aq_matmul_bf16_ws(x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(), biases.data_ptr(),
-                               out.data_ptr(), M, N, K, group_size, bits, workspace.data_ptr(), workspace.numel(),
+                               out.data_ptr(), M, N, K, group_size, bits, workspace.data_ptr(), _nbytes(workspace),
                                stream.cuda_stream)
     else:
+        where = "aq_matmul_bf16_ex"
         st = aq_matmul_bf16_ex(x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(), biases.data_ptr(),
                                out.data_ptr(), M, N, K, group_size, bits, _KERNELS[kernel],
                                (AQ_FLAG_PDL if pdl else 0) | flags, stream.cuda_stream)
     if st != AQ_OK:
-        raise AqError(st, "aq_matmul_bf16_ex")
+        raise AqError(st, where)
     return out
 
 
@@ -299,23 +375,31 @@ def gather_qmm(x, w_packed, scales, biases, lhs_indices, rhs_indices, out=None, 
     is given (a uint8 CUDA tensor of aq_gather_qmm_workspace_bytes)."""
     import torch
 
+    if x.dim() != 2 or w_packed.dim() != 3 or lhs_indices.dim() != 1:
+        raise ValueError("x must be 2-D, w_packed 3-D and lhs_indices 1-D")
     T, K = x.shape
     E, N = w_packed.shape[0], w_packed.shape[1]
     R = lhs_indices.shape[0]
-    for name, t in (("x", x), ("w_packed", w_packed), ("scales", scales), ("biases", biases),
-                    ("lhs_indices", lhs_indices), ("rhs_indices", rhs_indices)):
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    _check("x", x, (T, K), "bf16")
+    _check_weights(w_packed, scales, biases, (E, N), K, group_size, bits)
+    _check("lhs_indices", lhs_indices, (R,), "i32")
+    _check("rhs_indices", rhs_indices, (R,), "i32")
     if out is None:
         out = torch.empty((R, N), dtype=torch.bfloat16, device=x.device)
-    need = aq_gather_qmm_workspace_bytes(R, K, E)
+    _check("out", out, (R, N), "bf16")
+    if workspace is not None:
+        _check("workspace", workspace, (None,), "u8")
+    _placed(x.device, [("x", x), ("w_packed", w_packed), ("scales", scales), ("biases", biases),
+                       ("lhs_indices", lhs_indices), ("rhs_indices", rhs_indices), ("out", out)]
+            + ([("workspace", workspace)] if workspace is not None else []))
     if workspace is None:
+        need = aq_gather_qmm_workspace_bytes(R, K, E)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
     if stream is None:
         stream = torch.cuda.current_stream(x.device)
     st = aq_gather_qmm_bf16(x.data_ptr(), w_packed.data_ptr(), scales.data_ptr(), biases.data_ptr(),
                             lhs_indices.data_ptr(), rhs_indices.data_ptr(), out.data_ptr(), R, T, N, K, E,
-                            group_size, bits, workspace.data_ptr(), workspace.numel(), stream.cuda_stream)
+                            group_size, bits, workspace.data_ptr(), _nbytes(workspace), stream.cuda_stream)
     if st != AQ_OK:
         raise AqError(st, "aq_gather_qmm_bf16")
     return out
@@ -326,13 +410,18 @@ def matmul_nvfp4(x, w_packed, scales_e4m3, global_scale: float = 1.0, out=None, 
     [N, K/8] (E2M1 codes); scales_e4m3 uint8 [N, K/16].  Returns y bf16 [M, N]."""
     import torch
 
+    if x.dim() != 2 or w_packed.dim() != 2:
+        raise ValueError("x and w_packed must be 2-D")
     M, K = x.shape
     N = w_packed.shape[0]
-    for name, t in (("x", x), ("w_packed", w_packed), ("scales_e4m3", scales_e4m3)):
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    _check("x", x, (M, K), "bf16")
+    blocks_ok = K % 16 == 0          # other K the library rejects itself
+    _check("w_packed", w_packed, (N, K // 8 if blocks_ok else None), "word")
+    _check("scales_e4m3", scales_e4m3, (N, K // 16 if blocks_ok else None), "u8")
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check("out", out, (M, N), "bf16")
+    _placed(x.device, [("x", x), ("w_packed", w_packed), ("scales_e4m3", scales_e4m3), ("out", out)])
     if stream is None:
         stream = torch.cuda.current_stream(x.device)
     st = aq_matmul_nvfp4_bf16(x.data_ptr(), w_packed.data_ptr(), scales_e4m3.data_ptr(), float(global_scale),
