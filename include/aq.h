@@ -61,11 +61,14 @@ typedef enum aq_status {
  * aq_matmul_bf16 does. */
 typedef enum aq_kernel {
     AQ_KERNEL_AUTO = 0,
-    AQ_KERNEL_QMV = 1, /* weight-streaming decode kernels; any M: the TMA-fed kernel wherever
-                          it applies (M <= 8, K % 512 == 0, 16-byte aligned scales and biases),
-                          else the general one in launches of 16 rows of x.  AQ_KERNEL_AUTO
-                          chooses between the two (and the GEMM kernel above 16 rows) by
-                          measured speed. */
+    AQ_KERNEL_QMV = 1, /* weight-streaming decode kernels, any M.  4-bit codes: the TMA-fed
+                          kernel wherever it applies (M <= 8, K % 512 == 0, 16-byte aligned
+                          scales and biases), else the general one in launches of 16 rows of
+                          x.  8-bit codes: the TMA-fed kernel in launches of 8 rows.
+                          AQ_KERNEL_AUTO chooses among these (and the GEMM kernel above 16
+                          rows) by measured speed; for 9..16 rows over a matrix of at least
+                          four 32-row tiles per SM it runs the TMA-fed kernel twice, on half
+                          the rows each. */
     AQ_KERNEL_QMM = 2  /* tensor-core GEMM kernel (tcgen05); any M >= 1 */
 } aq_kernel;
 
