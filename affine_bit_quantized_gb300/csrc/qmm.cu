@@ -791,7 +791,7 @@ cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev) {
         if (e != cudaSuccess) return e;
         g_sms[dev].store(sms, std::memory_order_relaxed);
     }
-    const int tiles = ((N + kTileN - 1) / kTileN) * ((M + C::kTileM - 1) / C::kTileM);
+    const int64_t tiles = (int64_t)((N + kTileN - 1) / kTileN) * ((M + C::kTileM - 1) / C::kTileM);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + C::kTileM - 1) / C::kTileM), 1);
     cfg.blockDim = dim3(kThreads);

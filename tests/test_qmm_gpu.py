@@ -163,3 +163,25 @@ def test_qmm_workspace_path_same_bits(dev, M, N, K, bits):
     if M * N <= 300 * 700:
         _, ref = oracle.matmul(x, w.w_packed, w.scales, w.biases, M, N, K, bits=bits)
         assert_parity(from_dev_bf16(b), ref, what=f"qmm workspace M={M} N={N} K={K}")
+
+
+def test_output_beyond_2_31_elements(dev):
+    """A prefill over a vocabulary-sized N: y has 2.7e9 elements (5.4 GB), so
+    the outputs past row 2^31 / N sit at offsets that need 64 bits.  Sampled
+    outputs, half of them past that row, are gathered on the device."""
+    import torch
+    M, N, K = 20480, 131072, 512
+    w = synth.make_weights(N, K, 77)
+    x = synth.make_x(M, K, 77)
+    xt, wt, st, bt = upload(x, w, dev)
+    y = aq.matmul(xt, wt, st, bt)
+    hi = (1 << 31) // N                      # first row whose offset reaches 2^31
+    rng = np.random.default_rng(77)
+    im = np.concatenate([rng.integers(0, hi, 1000), rng.integers(hi, M, 2000), [hi, hi, M - 1, M - 1]])
+    inn = np.concatenate([rng.integers(0, N, 3000), [0, N - 1, 0, N - 1]])
+    got = from_dev_bf16(y[torch.from_numpy(im).to(dev), torch.from_numpy(inn).to(dev)])
+    torch.cuda.synchronize()
+    del y
+    ye, yb = oracle.matmul_sampled(x, w.w_packed, w.scales, w.biases, M, N, K, im, inn)
+    rms = float(np.sqrt(np.mean(ye * ye)))
+    assert_parity(got, yb, rms=rms, what=f"qmm sampled M={M} N={N} K={K} (y beyond 2^31 elements)")
