@@ -2,11 +2,11 @@
  * aq.h -- C ABI of libaq, the affine group-quantized matmul for NVIDIA GB300
  * (sm_103a).
  *
- * The operation is the one the "MLX CUDA Cleanup Plan" page (makepad
- * libs/mlx/mlx.md) asks a backend-neutral accelerator to provide, "affine
- * packed BF16 input x U32 packed weights x BF16 scales/biases" (Target
- * Architecture, sections 1-2), in the 4-bit, group-size-64 affine packed form
- * of its Refactor Plan, Phase 3:
+ * The operation is the one the "MLX CUDA Cleanup Plan" page asks a
+ * backend-neutral accelerator call to provide: bf16 activations times weights
+ * packed into 32-bit words with bf16 scales and biases (Target Architecture,
+ * sections 1-2), in the 4-bit, group-size-64 affine packed form of its
+ * Refactor Plan, Phase 3:
  *
  *     y[m,n] = sum_k x[m,k] * w[n,k],   w[n,k] = scale[n,k/64] * q[n,k] + bias[n,k/64]
  *

@@ -8,18 +8,18 @@
  *
  *   y[m,n] = sum_k x[m,k] * w[n,k],   w[n,k] = scale[n,k/gs] * q[n,k] + bias[n,k/gs]
  *
- * Operand types follow "MLX CUDA Cleanup Plan" (makepad libs/mlx/mlx.md),
- * Target Architecture section 1: BF16 input x U32 packed weights x BF16
- * scales/biases; 4-bit and 8-bit affine packed weights with group size 64 are
- * the variants its Refactor Plan, Phase 3, lists.  The pages do not print the
+ * Operand types follow "MLX CUDA Cleanup Plan", Target Architecture section 1:
+ * bf16 activations, weights packed into 32-bit words, bf16 scales and biases;
+ * 4-bit and 8-bit affine packed weights with group size 64 are the variants its
+ * Refactor Plan, Phase 3, lists.  The pages do not print the
  * bit layout or the dequantization formula; the readings used here are:
  *   - codes are unsigned, (32/bits) per uint32 word, the lowest bits holding
  *     the lowest k ("low nibble first along K" for 4-bit);
  *   - groups run along K, contiguous, never straddling a row;
  *   - dequantization is scale*q + bias.
  * Results are rounded once, from double, to bf16 (nearest, ties to even):
- * the Verification Requirements section of the same page asks for "the exact
- * same BF16-rounded math".
+ * the Verification Requirements section of the same page asks that results
+ * follow bf16 rounding.
  *
  * Precision: every bf16 value widens to double exactly; scale*q + bias is
  * exact in double for the value ranges used (a 12-bit product plus an 8-bit
