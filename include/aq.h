@@ -72,24 +72,23 @@ typedef enum aq_kernel {
     AQ_KERNEL_QMM = 2  /* tensor-core GEMM kernel (tcgen05); any M >= 1 */
 } aq_kernel;
 
-/* Flags for aq_matmul_bf16_ex. */
-enum {
-    /* Launch with programmatic dependent launch: the kernel may start while
-     * the previous kernel on the stream is still running and begins streaming
-     * w_packed/scales/biases before it waits for that kernel to finish.  It
-     * reads x and writes y only after the wait.  PRECONDITION: the weights
-     * were not written by the kernel immediately before on the stream. */
-    AQ_FLAG_PDL = 1u << 0,
-    /* Test hook for the failure path of the bounded device-side waits: the
-     * weight-streaming kernel's producer omits the copy of x, so its
-     * consumers' wait expires (after 20 ms instead of the normal 2 s), the
-     * kernel records a timeout in the device status word and returns without
-     * writing y.  Only where that kernel stages x in one piece: 1 <= M <= 8,
-     * K a multiple of 512, and x within 32 KB rounded up to whole 2048-code
-     * stages (4-bit) or 1024-code stages (8-bit); otherwise AQ_ERR_UNSUPPORTED.
-     * Read the outcome with aq_read_device_status(). */
-    AQ_FLAG_DEBUG_SKIP_X = 1u << 31
-};
+/* Flags for aq_matmul_bf16_ex (bits of its unsigned `flags`; macros, because
+ * bit 31 is outside the range ISO C allows an enumerator). */
+/* Launch with programmatic dependent launch: the kernel may start while
+ * the previous kernel on the stream is still running and begins streaming
+ * w_packed/scales/biases before it waits for that kernel to finish.  It
+ * reads x and writes y only after the wait.  PRECONDITION: the weights
+ * were not written by the kernel immediately before on the stream. */
+#define AQ_FLAG_PDL 0x1u
+/* Test hook for the failure path of the bounded device-side waits: the
+ * weight-streaming kernel's producer omits the copy of x, so its
+ * consumers' wait expires (after 20 ms instead of the normal 2 s), the
+ * kernel records a timeout in the device status word and returns without
+ * writing y.  Only where that kernel stages x in one piece: 1 <= M <= 8,
+ * K a multiple of 512, and x within 32 KB rounded up to whole 2048-code
+ * stages (4-bit) or 1024-code stages (8-bit); otherwise AQ_ERR_UNSUPPORTED.
+ * Read the outcome with aq_read_device_status(). */
+#define AQ_FLAG_DEBUG_SKIP_X 0x80000000u
 
 /*
  * y = x . dequant(W)^T as defined above.
