@@ -160,6 +160,8 @@ class Chain:
         import torch
 
         n = len(items)
+        if independent is not None and len(independent) != n:
+            raise ValueError(f"independent has {len(independent)} flags for {n} matmuls")
         arr = (MatmulDesc * max(n, 1))()
         named = []
         for i, (x, w, s, b, y) in enumerate(items):

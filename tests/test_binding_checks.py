@@ -182,3 +182,10 @@ def test_chain_checks_every_item():
     bad = [good[0], (b["x"], b["w_packed"], b["scales"][:, :1].contiguous(), b["biases"], y1)]
     with pytest.raises(ValueError, match="chain item 1: scales has shape"):
         aq.Chain(bad)
+
+
+def test_chain_independent_flags_match_the_items():
+    a = operands(M=1)
+    item = (a["x"], a["w_packed"], a["scales"], a["biases"], torch.zeros(1, N, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="independent has 1 flags for 2 matmuls"):
+        aq.Chain([item, item], independent=[False])
