@@ -150,6 +150,31 @@ def aq_chain_run(plan, stream) -> int:
     return load().aq_chain_run(ctypes.byref(plan), stream)
 
 
+def _chain_descs(items, group_size: int, bits: int, independent):
+    """Checks (x, w_packed, scales, biases, y) tensors of a chain and returns
+    their aq_matmul_desc array (at least one element)."""
+    n = len(items)
+    if independent is not None and len(independent) != n:
+        raise ValueError(f"independent has {len(independent)} flags for {n} matmuls")
+    arr = (MatmulDesc * max(n, 1))()
+    named = []
+    for i, (x, w, s, b, y) in enumerate(items):
+        if x.dim() != 2 or w.dim() != 2:
+            raise ValueError(f"chain item {i}: x and w_packed must be 2-D")
+        at = f"chain item {i}: "
+        _check(at + "x", x, tuple(x.shape), "bf16")
+        _check_weights(w, s, b, (w.shape[0],), x.shape[1], group_size, bits, prefix=at)
+        _check(at + "y", y, (x.shape[0], w.shape[0]), "bf16")
+        named += [(at + "x", x), (at + "w_packed", w), (at + "scales", s), (at + "biases", b), (at + "y", y)]
+    if n:
+        _placed(items[0][0].device, named)
+    for i, (x, w, s, b, y) in enumerate(items):
+        flags = AQ_CHAIN_INDEPENDENT if (independent and independent[i]) else 0
+        arr[i] = MatmulDesc(x.data_ptr(), w.data_ptr(), s.data_ptr(), b.data_ptr(), y.data_ptr(), x.shape[0],
+                            w.shape[0], x.shape[1], flags)
+    return arr
+
+
 class Chain:
     """A prepared chain of matmuls over torch CUDA tensors: Chain([(x, w, s, b, y), ...]).run().
 
@@ -160,24 +185,7 @@ class Chain:
         import torch
 
         n = len(items)
-        if independent is not None and len(independent) != n:
-            raise ValueError(f"independent has {len(independent)} flags for {n} matmuls")
-        arr = (MatmulDesc * max(n, 1))()
-        named = []
-        for i, (x, w, s, b, y) in enumerate(items):
-            if x.dim() != 2 or w.dim() != 2:
-                raise ValueError(f"chain item {i}: x and w_packed must be 2-D")
-            at = f"chain item {i}: "
-            _check(at + "x", x, tuple(x.shape), "bf16")
-            _check_weights(w, s, b, (w.shape[0],), x.shape[1], group_size, bits, prefix=at)
-            _check(at + "y", y, (x.shape[0], w.shape[0]), "bf16")
-            named += [(at + "x", x), (at + "w_packed", w), (at + "scales", s), (at + "biases", b), (at + "y", y)]
-        if n:
-            _placed(items[0][0].device, named)
-        for i, (x, w, s, b, y) in enumerate(items):
-            flags = AQ_CHAIN_INDEPENDENT if (independent and independent[i]) else 0
-            arr[i] = MatmulDesc(x.data_ptr(), w.data_ptr(), s.data_ptr(), b.data_ptr(), y.data_ptr(), x.shape[0],
-                                w.shape[0], x.shape[1], flags)
+        arr = _chain_descs(items, group_size, bits, independent)
         self.items = items
         nbytes = aq_chain_workspace_bytes(n)
         dev = items[0][0].device if n else torch.device("cuda")
@@ -199,6 +207,20 @@ class Chain:
 
 def aq_chain_run_static(descs, count, group_size, bits, stream) -> int:
     return load().aq_chain_run_static(descs, count, group_size, bits, stream)
+
+
+def chain_run_static(items, group_size: int = 64, bits: int = 4, independent=None, stream=None) -> None:
+    """A chain of matmuls over torch CUDA tensors, as Chain(...).run() gives it,
+    through the entry point that allocates nothing (aq_chain_run_static; at
+    most 256 matmuls).  The tensors are checked as Chain checks them."""
+    import torch
+
+    arr = _chain_descs(items, group_size, bits, independent)
+    if stream is None:
+        stream = torch.cuda.current_stream(items[0][0].device) if items else torch.cuda.current_stream()
+    st = aq_chain_run_static(arr, len(items), group_size, bits, stream.cuda_stream)
+    if st != AQ_OK:
+        raise AqError(st, "aq_chain_run_static")
 
 
 def aq_matmul_workspace_bytes(M, K) -> int:

@@ -102,6 +102,18 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
 }
+// The records are rewritten in global memory between launches (the
+// allocation-free entry point reuses one array for every call), and the TMA
+// unit reads descriptors through the tensor-map proxy: acquire each map
+// before its first use so that no descriptor of an earlier call is used.
+__device__ __forceinline__ void acquire_tensormap(const CUtensorMap *m) {
+    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(m) : "memory");
+}
+__device__ __forceinline__ void acquire_record_maps(const ChainRec *r) {
+    acquire_tensormap(&r->tw);
+    acquire_tensormap(&r->ts);
+    acquire_tensormap(&r->tb);
+}
 
 // The scalar part of a record (three 16-byte vectors).
 struct RecInfo {
@@ -191,12 +203,14 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
             int issued = 0;
             bool ok = true;
             RecInfo cur = load_info(recs, info, 0);
+            acquire_record_maps(recs);
             for (int jm = 0; jm < count && ok; ++jm) {
                 const ChainRec *rec = recs + jm;
                 // the next record's scalars and descriptors travel while this matmul streams
                 RecInfo nxt = cur;
                 if (jm + 1 < count) {
                     nxt = load_info(recs, info, jm + 1);
+                    acquire_record_maps(rec + 1);
                     prefetch_tensormap(&rec[1].tw);
                     prefetch_tensormap(&rec[1].ts);
                     prefetch_tensormap(&rec[1].tb);
@@ -570,15 +584,19 @@ aq_status chain_run_static(const aq_matmul_desc *descs, int count, int group_siz
     }
     aq_chain_plan plan;
     std::memset(&plan, 0, sizeof plan);
-    {
-        std::lock_guard<std::mutex> lock(g_static_host_mutex);
-        st = chain_encode(descs, count, bits, g_static_host_recs, &plan);
-        if (st != AQ_OK) return st;
-        // from pageable memory: returns once the records are staged, so the
-        // host buffer may be reused by the next call
-        *err = cudaMemcpyAsync(scratch, g_static_host_recs, records_bytes(count), cudaMemcpyHostToDevice, stream);
-        if (*err != cudaSuccess) return AQ_ERR_CUDA;
-    }
+    // The host staging array is shared too, and the record copy, the counter
+    // clear and the launch of one call must reach the stream together: two
+    // host threads enqueueing on one stream would otherwise interleave them
+    // (one call's kernel running the other's records).  So the lock covers
+    // all three.
+    std::lock_guard<std::mutex> lock(g_static_host_mutex);
+    st = chain_encode(descs, count, bits, g_static_host_recs, &plan);
+    if (st != AQ_OK) return st;
+    // from pageable memory: returns once the records are staged (which may
+    // mean waiting for the stream's earlier work), so the host array may be
+    // reused by the next call
+    *err = cudaMemcpyAsync(scratch, g_static_host_recs, records_bytes(count), cudaMemcpyHostToDevice, stream);
+    if (*err != cudaSuccess) return AQ_ERR_CUDA;
     plan.workspace = scratch;
     *err = chain_run(&plan, timeout_ns, status, stream);  // clears the counters, then launches
     return *err == cudaSuccess ? AQ_OK : AQ_ERR_CUDA;

@@ -5,8 +5,11 @@ One step = every weight matrix of 32 decoder layers (q, k, v, o, gate, up,
 down; 4-bit codes, group 64, bf16 scales and biases, each layer drawn from its
 own seed) plus lm_head, each multiplied by one bf16 activation row (M = 1).
 That is 4.22 GB of weights streamed per step, far larger than the 129 MB L2,
-so consecutive steps never hit in L2.  The step is captured once into a CUDA
-graph (kernels chained with programmatic dependent launch) and replayed.
+so consecutive steps never hit in L2.  The timed step is one cooperative
+persistent launch of the chained decode kernel (aq_chain_run: matmul j reads
+its x only after matmul j-1 has stored all of its y, except k, v and up, which
+read the same x as the matmul before them); the same step as a CUDA graph of
+one launch per matmul is reported beside it as "alt".
 
 Prints one JSON line.  `value` is the achieved algorithmic HBM bandwidth of
 the step in GB/s (bytes the definition must read and write: packed codes,
@@ -28,7 +31,6 @@ import subprocess
 import sys
 import tempfile
 import time
-from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -40,9 +42,6 @@ from affine_bit_quantized_gb300 import synth  # noqa: E402
 METRIC = "qmv achieved HBM GB/s (% of GB300 peak) and 8B-shape equiv decode tok/s; qmm TFLOPS"
 WORKLOAD = ("llama-3.1-8b-shaped decode step: 32 layers x (q,k,v,o,gate,up,down) + lm_head, "
             "M=1, 4-bit affine codes, group 64, bf16 scales/biases")
-CONFIG_ID = 4          # seeds of the full decode step
-N_ROLES = 4            # activations per layer: attention in, attention out, MLP in, MLP activation
-ROLE_OF = {"q_proj": 0, "k_proj": 0, "v_proj": 0, "o_proj": 1, "gate_proj": 2, "up_proj": 2, "down_proj": 3}
 QMM_SHAPES = ((4096, 14336, "gate/up"), (14336, 4096, "down"))   # (K, N)
 QMM_M = (256, 2048)
 
@@ -117,28 +116,10 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- workload
-
-def step_matrices(layers: int):
-    """(layer, j, name, N, K, seed) for every matrix of the step, in launch order."""
-    out = []
-    for layer in range(layers):
-        for j, (name, N, K) in enumerate(synth.LLAMA8B_LAYER):
-            out.append((layer, j, name, N, K, synth.seed_for(CONFIG_ID, layer, j)))
-    name, N, K = synth.LLAMA8B_LM_HEAD
-    out.append((layers, 0, name, N, K, synth.seed_for(CONFIG_ID, layers, 0)))
-    return out
-
-
-def x_layout(layers: int):
-    """Offsets (in elements) of each activation row inside one contiguous x buffer."""
-    offs, pos = {}, 0
-    for layer in range(layers):
-        for role, K in enumerate((4096, 4096, 4096, 14336)):
-            offs[(layer, role)] = (pos, K, synth.seed_for(CONFIG_ID, layer, 8 + role))
-            pos += K
-    offs[(layers, 0)] = (pos, 4096, synth.seed_for(CONFIG_ID, layers, 8))
-    pos += 4096
-    return offs, pos
+# The step's layout (matrices, seeds, activation rows, independence flags) is
+# shared with the tests that compare this exact launch with the oracle.
+from affine_bit_quantized_gb300.decode_step import (  # noqa: E402
+    CONFIG_ID, ROLE_OF, DecodeStep, step_matrices, x_layout)
 
 
 def rank_env():
@@ -415,120 +396,34 @@ def main():
     hbm_peak, bf16_peak, bf16_sus, peak_src = load_peaks()
 
     # ---- workload (generated on the host from the seeded recipe, uploaded once)
-    mats = step_matrices(args.layers)
-    offs, x_elems = x_layout(args.layers)
-    pool = ThreadPoolExecutor(max(1, min(16, os.cpu_count() or 1)))
-    weights = {}
-    host_keep = {}
     cpu_layers = {0, 1} if (rank == 0 and world == 1 and not args.no_cpu_baseline) else set()
-
-    def gen(m):
-        layer, j, name, N, K, seed = m
-        return m, synth.make_weights(N, K, seed)
-
-    for m, w in pool.map(gen, mats):
-        layer, j, name, N, K, seed = m
-        weights[(layer, j)] = (torch.from_numpy(w.w_packed.view(np.int32)).to(dev),
-                               torch.from_numpy(w.scales.view(np.int16)).to(dev),
-                               torch.from_numpy(w.biases.view(np.int16)).to(dev))
-        if layer in cpu_layers:
-            host_keep[(layer, j)] = w
-    x_host = np.empty(x_elems, np.uint16)
-    for (layer, role), (pos, K, seed) in offs.items():
-        x_host[pos:pos + K] = synth.make_x(1, K, seed)[0]
-    x_pinned = torch.from_numpy(x_host.view(np.int16)).pin_memory()
-    x_dev = x_pinned.to(dev)
-    y_offs, pos = [], 0
-    for m in mats:
-        y_offs.append(pos)
-        pos += m[3]
-    y_dev = torch.empty(pos, dtype=torch.int16, device=dev)
+    ds = DecodeStep(dev, args.layers, keep_host=bool(cpu_layers), host_layers=cpu_layers)
+    mats, launches = ds.mats, ds.launches
+    offs, _ = x_layout(args.layers)
+    x_host, x_pinned, x_dev, y_dev, y_offs = ds.x_host, ds.x_pinned, ds.x, ds.y, ds.y_offsets
+    weights = {(m[0], m[1]): ds.weights[i] for i, m in enumerate(mats)}
+    host_keep = {(mats[i][0], mats[i][1]): w for i, w in ds.host_weights.items()}
     logits_pinned = torch.empty(mats[-1][3], dtype=torch.int16).pin_memory()
     step_bytes = sum(alg_bytes(1, N, K) for (_, _, _, N, K, _) in mats)
-    launches = []
-    for i, (layer, j, name, N, K, seed) in enumerate(mats):
-        role = 0 if name == "lm_head" else ROLE_OF[name]
-        xo = offs[(layer, role)][0]
-        wt, st, bt = weights[(layer, j)]
-        launches.append((x_dev.data_ptr() + 2 * xo, wt.data_ptr(), st.data_ptr(), bt.data_ptr(),
-                         y_dev.data_ptr() + 2 * y_offs[i], 1, N, K))
-
-    def enqueue(stream_handle, sel=None):
-        for i, (xp, wp, sp, bp, yp, M, N, K) in enumerate(launches):
-            if sel is not None and i not in sel:
-                continue
-            st = lib.aq_matmul_bf16_ex(xp, wp, sp, bp, yp, M, N, K, 64, 4, aq.AQ_KERNEL_AUTO, aq.AQ_FLAG_PDL,
-                                       stream_handle)
-            if st != aq.AQ_OK:
-                raise aq.AqError(st, "aq_matmul_bf16_ex")
-
-    # ---- capture the step as a graph: one launch per matmul; k and v run as
-    # branches beside q (same input, no mutual dependency), up beside gate;
-    # along each branch, launches chain with programmatic dependent launch
-    cap_stream = torch.cuda.Stream(dev)
-    side = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
-
-    def enqueue_dag():
-        main = torch.cuda.current_stream(dev)
-        i = 0
-        while i < len(launches):
-            name = mats[i][2]
-            group = [i]
-            while i + len(group) < len(launches) and mats[i + len(group)][2] in ("k_proj", "v_proj", "up_proj"):
-                group.append(i + len(group))
-            if len(group) == 1:
-                enqueue(main.cuda_stream, {i})
-            else:
-                fork = torch.cuda.Event()
-                fork.record(main)
-                joins = []
-                for b, idx in enumerate(group[1:]):
-                    side[b].wait_event(fork)
-                    enqueue(side[b].cuda_stream, {idx})
-                    ev = torch.cuda.Event()
-                    ev.record(side[b])
-                    joins.append(ev)
-                enqueue(main.cuda_stream, {group[0]})
-                for ev in joins:
-                    main.wait_event(ev)
-            i += len(group)
-
-    with torch.cuda.stream(cap_stream):
-        enqueue_dag()
-    torch.cuda.synchronize(dev)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=cap_stream):
-        enqueue_dag()
-    torch.cuda.synchronize(dev)
+    enqueue = ds.enqueue
+    # the step as a CUDA graph of one launch per matmul (k, v beside q and up
+    # beside gate as parallel branches), reported as the alternative
+    graph = ds.capture_graph()
 
     def barrier():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-
     uuid = str(torch.cuda.get_device_properties(dev).uuid)
     gpu_id = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
     clocks = ClockSampler(gpu_id)
 
     # ---- the same step as one chained launch over the same buffers
-    # k and v read q's input and do not depend on q; up likewise after gate
-    independent = [m[2] in ("k_proj", "v_proj", "up_proj") for m in mats]
-    arr = (aq.MatmulDesc * len(launches))(*[aq.MatmulDesc(xp, wp, sp, bp, yp, M, N, K,
-                                                          aq.AQ_CHAIN_INDEPENDENT if ind else 0)
-                                            for (xp, wp, sp, bp, yp, M, N, K), ind in zip(launches, independent)])
-    ws_bytes = aq.aq_chain_workspace_bytes(len(launches))
-    chain_ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    plan = aq.ChainPlan()
-    st = aq.aq_chain_prepare(arr, len(launches), 64, 4, chain_ws.data_ptr(), ws_bytes, plan)
-    if st != aq.AQ_OK:
-        raise aq.AqError(st, "aq_chain_prepare")
     cur = torch.cuda.current_stream(dev)
 
     def chain_step():
-        rc = aq.aq_chain_run(plan, cur.cuda_stream)
-        if rc != aq.AQ_OK:
-            raise aq.AqError(rc, "aq_chain_run")
+        ds.run_chain(cur.cuda_stream)
 
     step_fns = {"chain": chain_step, "graph": graph.replay}
     step = step_fns[args.step_impl]

@@ -24,9 +24,14 @@
  *
  * Conventions shared by every entry point below:
  *  - Ownership: the caller owns every buffer and the stream.  No entry point
- *    allocates, frees or keeps device memory, and none synchronizes the host
- *    (the Hard Constraints section of the cleanup plan: no extra copies,
- *    staging buffers or synchronization points on the hot path).
+ *    allocates or frees device memory, and none synchronizes the host (the
+ *    Hard Constraints section of the cleanup plan: no extra copies, staging
+ *    buffers or synchronization points on the hot path), apart from the
+ *    exceptions stated at aq_chain_prepare, aq_chain_run_static and
+ *    aq_read_device_status.  The library's own device memory is two
+ *    file-scope arrays that every GPU loading it holds until the process
+ *    exits: a 4-byte status word (aq_read_device_status) and the 132 KB
+ *    scratch of aq_chain_run_static.
  *  - Device pointers are plain CUDA device addresses of the current device.
  *    `stream` is a cudaStream_t (NULL = the legacy default stream).
  *  - Work is enqueued asynchronously on `stream`; an AQ_OK return means the
@@ -226,8 +231,12 @@ aq_status aq_chain_run(const aq_chain_plan *plan, void *stream);
  * static device array of 132 KB that every GPU loading this library holds
  * until the process exits; the caller still owns every input and output
  * buffer.  Each call encodes the descriptors again, copies them into that
- * array on `stream` (cudaMemcpyAsync from host memory) and clears the
- * counters before its launch.  All calls share the array: calls whose work
+ * array on `stream` (cudaMemcpyAsync from a static host array in pageable
+ * memory) and clears the counters before its launch.  Because the copy is
+ * from pageable memory, the call may wait, before it returns, until the
+ * stream's earlier work has finished.  Calls from several host threads are
+ * serialized inside the library (copy, clear and launch of one call reach
+ * the stream together).  All calls share the array: calls whose work
  * overlaps on the GPU (other streams, or another device-side user of the
  * same array) race, so serialize them.  The first call on a device looks up
  * the array's device address (cudaGetSymbolAddress) and should come before

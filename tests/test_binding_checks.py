@@ -189,3 +189,17 @@ def test_chain_independent_flags_match_the_items():
     item = (a["x"], a["w_packed"], a["scales"], a["biases"], torch.zeros(1, N, dtype=torch.bfloat16))
     with pytest.raises(ValueError, match="independent has 1 flags for 2 matmuls"):
         aq.Chain([item, item], independent=[False])
+
+
+def test_static_chain_wrapper_checks_like_chain():
+    a, b = operands(M=1), operands(M=1, N=K)
+    y0 = torch.zeros(1, N, dtype=torch.bfloat16)
+    y1 = torch.zeros(1, K, dtype=torch.bfloat16)
+    good = [(a["x"], a["w_packed"], a["scales"], a["biases"], y1[:, :N].contiguous()),
+            (b["x"], b["w_packed"], b["scales"], b["biases"], y1)]
+    with pytest.raises(ValueError, match="chain item 0: x must be a contiguous CUDA tensor"):
+        aq.chain_run_static(good)
+    with pytest.raises(ValueError, match="chain item 1: y has shape"):
+        aq.chain_run_static([good[0], (b["x"], b["w_packed"], b["scales"], b["biases"], y0)])
+    with pytest.raises(ValueError, match="independent has 1 flags for 2 matmuls"):
+        aq.chain_run_static(good, independent=[False])

@@ -157,3 +157,38 @@ def test_chain_eight_bit(dev, shapes):
         assert_parity(from_dev_bf16(t[4]), ref, what=f"chain 8-bit M={M} N={N} K={K}")
         xt, wt, st, bt, y = t
         assert torch.equal(y, aq.matmul(xt, wt, st, bt, bits=8))
+
+
+def test_chain_longer_than_the_shared_memory_record_cache(dev):
+    """300 matmuls (the kernel keeps the first 256 records' scalars in shared
+    memory and reads the rest from global memory): pairs of a dependent matmul
+    that reads the previous pair's output and an independent one on the same
+    input.  Every output is compared with the oracle on the inputs it actually
+    read, and with separate calls bit for bit."""
+    import torch
+    K = 512
+    pairs = 150
+    x0 = to_dev_bf16(synth.make_x(1, K, 700), dev)
+    items, indep, ws = [], [], []
+    prev = x0
+    for p in range(pairs):
+        for half, N in enumerate((K, 77 + p % 5)):
+            w = synth.make_weights(N, K, 1000 + 2 * p + half)
+            wt = upload(np.zeros((1, K), np.uint16), w, dev)[1:]
+            y = torch.empty((1, N), dtype=torch.bfloat16, device=dev)
+            items.append((prev, *wt, y))
+            indep.append(half == 1)
+            ws.append(w)
+        prev = items[-2][4]            # the next pair reads this pair's dependent output
+    assert len(items) == 300
+    chain = aq.Chain(items, independent=indep)
+    for it in items:
+        it[4].fill_(float("nan"))
+    chain.run()
+    torch.cuda.synchronize()
+    assert aq.aq_read_device_status(None) == aq.AQ_OK
+    for i, ((xin, wt, st, bt, y), w) in enumerate(zip(items, ws)):
+        xh = from_dev_bf16(xin).reshape(1, K)
+        _, ref = oracle.matmul(xh, w.w_packed, w.scales, w.biases, 1, w.N, K)
+        assert_parity(from_dev_bf16(y), ref, what=f"matmul {i}")
+        assert torch.equal(y, aq.matmul(xin, wt, st, bt)), f"matmul {i}"
