@@ -26,7 +26,7 @@ AQ_KERNEL_QMV = 1
 AQ_KERNEL_QMM = 2
 
 AQ_FLAG_PDL = 1
-AQ_FLAG_DEBUG_SKIP_X = 1 << 31
+AQ_FLAG_DEBUG_SKIP_COPY = 1 << 31
 AQ_CHAIN_INDEPENDENT = 1
 
 _lock = threading.Lock()

@@ -100,7 +100,7 @@ aq_status matmul_impl(const void *x, const uint32_t *w_packed, const void *scale
                       void *workspace, size_t workspace_bytes, void *stream) {
     if (kernel != AQ_KERNEL_AUTO && kernel != AQ_KERNEL_QMV && kernel != AQ_KERNEL_QMM)
         return AQ_ERR_INVALID_ARG;
-    if (flags & ~(unsigned)(AQ_FLAG_PDL | AQ_FLAG_DEBUG_SKIP_X)) return AQ_ERR_INVALID_ARG;
+    if (flags & ~(unsigned)(AQ_FLAG_PDL | AQ_FLAG_DEBUG_SKIP_COPY)) return AQ_ERR_INVALID_ARG;
     aq_status st = validate(x, w_packed, scales, biases, y, M, N, K, group_size, bits);
     if (st != AQ_OK || M == 0 || N == 0) return st;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -114,8 +114,8 @@ aq_status matmul_impl(const void *x, const uint32_t *w_packed, const void *scale
     a.K = K;
     a.pdl = (flags & AQ_FLAG_PDL) != 0;
     a.stream = cs;
-    a.debug_skip_x = (flags & AQ_FLAG_DEBUG_SKIP_X) != 0;
-    a.timeout_ns = a.debug_skip_x ? kDebugTimeoutNs : kTimeoutNs;
+    a.debug_skip_copy = (flags & AQ_FLAG_DEBUG_SKIP_COPY) != 0;
+    a.timeout_ns = a.debug_skip_copy ? kDebugTimeoutNs : kTimeoutNs;
     st = record_cuda(status_ptr(&a.status));
     if (st != AQ_OK) return st;
     a.x = x;
@@ -127,7 +127,7 @@ aq_status matmul_impl(const void *x, const uint32_t *w_packed, const void *scale
     auto tma_rows = [&](int64_t rows, aq_status *out) -> bool {
         a.M = rows < M ? rows : M;
         if (!aq::qmv_tma_supported(a)) return false;   // depends on M only through M <= 8
-        if (a.debug_skip_x && (M > rows || aq::qmv_tma_passes(a) != 1)) return false;   // hook: x in one piece
+        if (a.debug_skip_copy && M > rows) return false;   // the hook: one launch
         for (int64_t m0 = 0; m0 < M; m0 += rows) {
             a.x = static_cast<const uint16_t *>(x) + m0 * K;
             a.y = static_cast<uint16_t *>(y) + m0 * N;
@@ -138,7 +138,7 @@ aq_status matmul_impl(const void *x, const uint32_t *w_packed, const void *scale
         return true;
     };
     if (kernel == AQ_KERNEL_QMM || (kernel == AQ_KERNEL_AUTO && M > kQmvMaxRows)) {
-        if (a.debug_skip_x) return AQ_ERR_UNSUPPORTED;
+        if (a.debug_skip_copy) return AQ_ERR_UNSUPPORTED;
         if (workspace && aligned(workspace, 128) && workspace_bytes >= (size_t)(M * K * 2)) a.xf16 = workspace;
         if (aq::qmm_supported(a)) return record_cuda(aq::launch_qmm(a));
         if (kernel == AQ_KERNEL_QMM) return AQ_ERR_UNSUPPORTED;
@@ -153,12 +153,12 @@ aq_status matmul_impl(const void *x, const uint32_t *w_packed, const void *scale
         a.M = M;
         // an explicit AQ_KERNEL_QMV takes the TMA-fed kernel wherever it applies
         if (aq::qmv_tma_supported(a) &&
-            (kernel == AQ_KERNEL_QMV || a.debug_skip_x || aq::qmv_tma_preferred(a))) {
+            (kernel == AQ_KERNEL_QMV || a.debug_skip_copy || aq::qmv_tma_preferred(a))) {
             st = AQ_OK;
             if (tma_rows(M, &st)) return st;
         }
     }
-    if (M > 8 && M <= kQmvMaxRows && kernel == AQ_KERNEL_AUTO && !a.debug_skip_x && many_tiles(N)) {
+    if (M > 8 && M <= kQmvMaxRows && kernel == AQ_KERNEL_AUTO && !a.debug_skip_copy && many_tiles(N)) {
         // 9..16 rows over a matrix with many tiles per SM (an lm_head): two launches of
         // half the rows on the TMA kernel stream W twice but still beat one launch of the
         // general kernel (128256 x 4096 at M = 16: 2 x 89 us against 233 us)
@@ -166,7 +166,7 @@ aq_status matmul_impl(const void *x, const uint32_t *w_packed, const void *scale
         st = AQ_OK;
         if (tma_rows(rows, &st)) return st;
     }
-    if (a.debug_skip_x) return AQ_ERR_UNSUPPORTED;  // the hook exists only in the TMA kernel
+    if (a.debug_skip_copy) return AQ_ERR_UNSUPPORTED;  // the hook exists only in the TMA kernel
     // Weight-streaming passes over at most 16 rows of x each.
     for (int64_t m0 = 0; m0 < M; m0 += kQmvMaxRows) {
         a.x = static_cast<const uint16_t *>(x) + m0 * K;

@@ -23,7 +23,7 @@ struct MatmulArgs {
     cudaStream_t stream;
     int *status;             // device status word (bounded waits record timeouts here)
     uint64_t timeout_ns;     // deadline of every bounded device-side wait
-    bool debug_skip_x;       // test hook: the TMA kernel omits the copy of x
+    bool debug_skip_copy;    // test hook: the kernel's producer leaves out one copy
     int bits = 4;            // code width: 4 or 8
     void *xf16 = nullptr;    // tensor-core path: M*K*2 bytes of caller workspace for x converted once
 };

@@ -310,6 +310,8 @@ nvfp4_qmv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         const uint32_t xq0 = x_s + (uint32_t)(xrow * x_row_bytes(M1, K) + (warp * 128 + t * 32) * 2);
         const int nblk = K / 128;
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        // the row scales of this lane's MMA columns 2t and 2t + 1
+        const float inv[2] = {inv_scale[2 * t < M1 ? 2 * t : M1 - 1], inv_scale[2 * t + 1 < M1 ? 2 * t + 1 : M1 - 1]};
         bool ok = alive && !*abort_flag;
         int item = 0;
         for (int tl = 0; tl < my_tiles; ++tl) {
@@ -325,7 +327,7 @@ nvfp4_qmv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
             }
-            if (ok) ok = deposit_tile<ONE_ROW>(tc, acc, tl, M, warp, lane, inv_scale, timeout_ns, abort_flag);
+            if (ok) ok = deposit_tile<ONE_ROW>(tc, acc, tl, M, warp, lane, inv, timeout_ns, abort_flag);
         }
         if (!ok) fail();
     }

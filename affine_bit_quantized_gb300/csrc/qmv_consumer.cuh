@@ -4,22 +4,24 @@
 // groups of 64; sixteen warps cover a 2048-code stage), and the per-tile
 // cross-warp reduction.  Internal header (not installed).
 //
-// Arithmetic per group g, row n and row m of x (fp32 accumulation):
-//   x'[m,k]  = fp16(2^e[m] * x[m,k] / c[k]),  c[k] = 1 or 16 by position in its
-//              8-element word (see below); e[m] puts max|x[m,:]| in [2^14, 2^15)
+// Arithmetic per group g, row n and row m of x (fp32 accumulation), for the
+// warp w whose column blocks hold g:
+//   x'[m,k]  = fp16(2^e[w,m] * x[m,k] / c[k]),  c[k] = 1 or 16 by position in its
+//              8-element word (see below); e[w,m] puts the maximum of |x[m,k]|
+//              over the warp's own slice of k in [2^14, 2^15)
 //   D[n,m,g] = sum_{k in g} (1024 + c[k] * q[n,k]) * x'[m,k]     (mma.sync, exact fp16 operands)
-//            = 1024 * X'[m,g] + 2^e[m] * sum_{k in g} q[n,k] * x[m,k]
-//   acc     += scale[n,g] * (D - 1024 * X'[m,g]) + bias[n,g] * Xs[m,g]
-//   y[m,n]   = sum over warps of (2^-e[m] * acc)   (power-of-two scaling: exact)
-// with X'[m,g] = sum_{k in g} x'[m,k] and Xs[m,g] = 2^e[m] * sum_{k in g} x[m,k].
+//            = 1024 * X'[m,g] + 2^e[w,m] * sum_{k in g} q[n,k] * x[m,k]
+//   acc_w   += scale[n,g] * (D - 1024 * X'[m,g]) + bias[n,g] * Xs[m,g]
+//   y[m,n]   = sum over warps w, in warp order, of (2^-e[w,m] * acc_w)   (power-of-two scaling: exact)
+// with X'[m,g] = sum_{k in g} x'[m,k] and Xs[m,g] = 2^e[w,m] * sum_{k in g} x[m,k].
 //
 // Codes become exact fp16 values with one LOP3 per pair: within a packed word
 // the nibbles at bits 0-3 and 16-19 go into the mantissa as 1024 + q, those at
 // bits 4-7 and 20-23 as 1024 + 16q (hence c = 16 there), and the word shifted
 // right by 8 gives the other four codes the same way.  A bf16 value has an
 // 8-bit significand, so with the power-of-two scale every element of x whose
-// magnitude is within 2^-29 of the row maximum is exact in fp16; smaller ones
-// round to the fp16 subnormal grid, an absolute error below 2^-39 of the row
+// magnitude is within 2^-29 of the slice maximum is exact in fp16; smaller ones
+// round to the fp16 subnormal grid, an absolute error below 2^-39 of the slice
 // maximum.
 //
 // MMA A rows are W rows: row block h (0, 1) of the 32-row tile holds rows
@@ -63,33 +65,59 @@ struct Geo {
 __host__ __device__ constexpr int stage_codes(int bits) { return bits == 4 ? 2048 : 1024; }
 __host__ __device__ constexpr int stage_groups(int bits) { return stage_codes(bits) / 64; }
 constexpr int kMaxM = 8;                                   // rows of x these kernels take
-constexpr int kMaxXBytes = 32768;                          // M*K*2 limit for staging x once per CTA
+constexpr int kMaxXBytes = 32768;                          // staging room for x (M * K * 2, K in whole stages)
 constexpr int kXInfoBytes = 96;                            // int row_max[2][8], float inv_scale[8]
-// Row strides of the staged x.  A row is 2K bytes of fragments and K/8 bytes of
-// (Xs, X'), both multiples of 128 bytes: with several rows, the eight row
-// addresses of an ldmatrix (rows 0..7 of x) and the four (Xs, X') rows a warp
-// reads at once would share banks.  One 16-byte pad per row shifts row m by m
-// 16-byte bank groups.  One row needs no pad.
+// Row stride of x staged in natural order (the NVFP4 kernel): 2K bytes, plus a
+// 16-byte pad per row with several rows (rows 2K bytes apart would put the
+// row addresses a warp reads at once in the same banks).
 __host__ __device__ constexpr int x_row_bytes(int M, int K) { return M == 1 ? 2 * K : 2 * K + 16; }
-__host__ __device__ constexpr int xsum_row_bytes(int M, int K) { return M == 1 ? K / 8 : K / 8 + 16; }
-constexpr int kXPadBytes = kMaxM * 16;                     // the pads of x rows (and of (Xs, X') rows)
 
 // named barrier 1: the consumer warps only (the producer warp runs on)
 __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
 }
 
-// Shared-memory addresses of the staged x of the current matmul.
-//   xq    : fp16 MMA fragments of x', M rows x_row_bytes(M, K) apart.  For row m, group g
-//           and word half i (words 2t+i of the group, t = 0..3) a 64-byte
-//           "quad" at (2g + i) * 64 holds four 16-byte rows (fragment
-//           register p = 0..3), each the registers of threads t = 0..3, so one
-//           ldmatrix.x4 per quad serves all 32 lanes;
-//   xsum  : float2 (Xs, X') per row and group, rows xsum_row_bytes(M, K) apart;
-//   xinfo : int row_max[2][8] (|x| bits, for the scale), float inv_scale[8] = 2^-e.
+// Staged x of the current matmul, one region per consumer warp.  A warp reads
+// only the x of its own column blocks (block kb * 16 + warp of every stage
+// kb), so it stages that slice itself, with no barrier against the other
+// warps: a warp may stage the next matmul's x while the others still work on
+// the previous one, since the regions never overlap.  In the region of warp w
+// (fragments at xq + w * wq, sums at xsum + w * ws):
+//   fragments: row m at m * xw_row_bytes(M, KB); stage kb at kb * (groups per
+//              warp) * 128; group gl at gl * 128; for word half i (words 2t+i
+//              of the group, t = 0..3) a 64-byte "quad" at i * 64 holds four
+//              16-byte rows (fragment register p = 0..3), each the registers
+//              of threads t = 0..3, so one ldmatrix.x4 per quad serves all 32
+//              lanes;
+//   sums:      float2 (Xs, X') per row, stage and group, row m at
+//              m * xsw_row_bytes(M, KB).
+// KB is the matmul's (or K pass's) stage count; the regions are sized for the
+// largest M * KB of the launch.
 struct XStage {
-    uint32_t xq, xsum, xinfo;
+    uint32_t xq, xsum;  // bases of the fragment and sum regions
+    int wq, ws;         // bytes per warp of each
 };
+// Row strides inside a warp's region.  A fragment row is a multiple of 128
+// bytes; with several rows, the eight row addresses of an ldmatrix (rows 0..7
+// of x) would share banks, so one 16-byte pad per row shifts row m by m
+// 16-byte bank groups.  One row needs no pad.  The sums are read once per
+// group, so their rows go unpadded.
+__host__ __device__ constexpr int xw_row_bytes(int M, int KB, int bits) {
+    return KB * (bits == 4 ? 256 : 128) + (M == 1 ? 0 : 16);
+}
+__host__ __device__ constexpr int xsw_row_bytes(int M, int KB, int bits) { return KB * (bits == 4 ? 16 : 8); }
+// Bytes per warp of the fragment and sum regions for x of up to x_bytes =
+// M * KB * (stage codes) * 2 (the rounded-up size of x) and max_m rows.
+__host__ __device__ constexpr int xw_region_bytes(int x_bytes, int max_m) {
+    return x_bytes / kConsumerWarps + (max_m == 1 ? 0 : 16 * max_m);
+}
+__host__ __device__ constexpr int xsw_region_bytes(int x_bytes, int max_m) {
+    return x_bytes / (16 * kConsumerWarps);
+}
+// M * K * 2 with K rounded up to whole stages: the staging room x needs
+__host__ __device__ constexpr int x_stage_bytes(int M, int K, int bits) {
+    return M * ((K + stage_codes(bits) - 1) / stage_codes(bits)) * stage_codes(bits) * 2;
+}
 
 __device__ __forceinline__ int x_scale_exponent(int max_bits) {
     // e with max|x| * 2^e in [2^14, 2^15); 0 for an all-zero row and for a row
@@ -122,52 +150,73 @@ __device__ __forceinline__ uint4 ldg_cg_v4(const void *p) {
     return v;
 }
 
-// Stages x [M][K] (bf16, from global memory through L2 with rows ldx elements
-// apart, or from a raw copy already in shared memory at `raw`, rows
-// x_row_bytes(M, K) apart, which may alias xs.xq) for the consumers:
-// fragments, group sums and scales.  Called by all consumer threads, which
-// meet at a barrier before the first shared-memory write (so the previous x
-// may still be in use on entry).  `n` counts the stagings of this CTA: staging
-// n takes its row maxima in buffer n % 2, which is zero on entry and is
-// cleared again for staging n + 2.  M*K <= 16384, K % 512 == 0.  ONE_ROW:
-// M == 1, known at compile time (no row arithmetic).
-template <bool FROM_GLOBAL, int BITS, bool ONE_ROW>
-__device__ __forceinline__ void stage_x(const XStage &xs, const __nv_bfloat16 *xg, uint32_t raw, int M_, int K, int n,
-                                        int ldx) {
+// Stages this warp's slice of x [M][K] (bf16 in global memory, read through L2,
+// rows ldx elements apart): fragments and (Xs, X') of the column blocks
+// kb * 16 + warp, kb < KB, of every row.  The power-of-two scale 2^e of a row
+// comes from the maximum over the warp's own slice; each warp unscales its
+// own partial sums (write_partials), so warps need not agree on e.  Sets
+// inv[c] = 2^-e of the x row of MMA column 2j + c (j = lane % 4; row 0 when
+// ONE_ROW).  Only the calling warp takes part.  M * KB * (stage codes) * 2
+// <= the region's room, K % 64 == 0.
+template <int BITS, bool ONE_ROW>
+__device__ __forceinline__ void stage_x_warp(const XStage &xs, const __nv_bfloat16 *xg, int M_, int K, int ldx,
+                                             int warp, int lane, float (&inv)[2]) {
+    using Gm = Geo<BITS>;
     const int M = ONE_ROW ? 1 : M_;
-    const int tid = threadIdx.x;
-    const int words = M * K / 8;
-    const int wpr = K / 8;  // words per row (a multiple of 64: a warp's 32 words share a row)
-    const int xrb = x_row_bytes(M, K), xsrb = xsum_row_bytes(M, K);
-    int *row_max = reinterpret_cast<int *>(__cvta_shared_to_generic(xs.xinfo)) + (n & 1) * kMaxM;
-    float *inv_scale = reinterpret_cast<float *>(__cvta_shared_to_generic(xs.xinfo + 64));
-    uint4 v[kMaxXBytes / 16 / kConsumerThreads];  // 4 words per thread at most
+    const int nblk = K / Gm::kWarpCodes;                          // column blocks of K
+    const int KB = (K + Gm::kStageCodes - 1) / Gm::kStageCodes;   // stages
+    const int kbw = warp < nblk ? (nblk - warp + kConsumerWarps - 1) / kConsumerWarps : 0;
+    constexpr int WPS = Gm::kGroupsPerWarp * 8;                   // 16-byte words per stage and row
+    const int wpr = kbw * WPS;                                    // words per row in the slice
+    const int words = M * wpr;
+    const uint32_t xq = xs.xq + (uint32_t)(warp * xs.wq), xsum = xs.xsum + (uint32_t)(warp * xs.ws);
+    const int xrb = xw_row_bytes(M, KB, BITS), xsrb = xsw_row_bytes(M, KB, BITS);
+    constexpr int NW = kMaxXBytes / 16 / kConsumerThreads;         // words per lane at most (4)
+    uint4 v[NW];
+    int row[NW];
+    // all loads first (one L2 round trip), then the row maxima
 #pragma unroll
-    for (int u = 0; u < kMaxXBytes / 16 / kConsumerThreads; ++u) {
-        if (u * kConsumerThreads >= words) break;  // uniform over the CTA
-        const int wi = u * kConsumerThreads + tid;
-        int mx = 0;
+    for (int u = 0; u < NW; ++u) {
+        const int wi = u * 32 + lane;
+        row[u] = 0;
+        v[u] = make_uint4(0u, 0u, 0u, 0u);
         if (wi < words) {
-            const int m = ONE_ROW ? 0 : wi / wpr, wr = wi - m * wpr;
-            v[u] = FROM_GLOBAL ? ldg_cg_v4(xg + (size_t)m * ldx + (size_t)wr * 8)
-                               : lds128(raw + (uint32_t)(m * xrb + wr * 16));
-            mx = bf16x2_abs_max(v[u].x);
-            mx = max(mx, bf16x2_abs_max(v[u].y));
-            mx = max(mx, bf16x2_abs_max(v[u].z));
-            mx = max(mx, bf16x2_abs_max(v[u].w));
+            const int m = ONE_ROW ? 0 : wi / wpr, r = wi - m * wpr;
+            const int kb = r / WPS, iw = r - kb * WPS;
+            row[u] = m;
+            v[u] = ldg_cg_v4(xg + (size_t)m * ldx + (size_t)(kb * kConsumerWarps + warp) * Gm::kWarpCodes + iw * 8);
         }
-        mx = __reduce_max_sync(0xFFFFFFFFu, mx);
-        if ((tid & 31) == 0 && wi < words) atomicMax(row_max + (ONE_ROW ? 0 : wi / wpr), mx);
     }
-    consumer_sync();
+    int e[ONE_ROW ? 1 : kMaxM];
 #pragma unroll
-    for (int u = 0; u < kMaxXBytes / 16 / kConsumerThreads; ++u) {
-        if (u * kConsumerThreads >= words) break;  // uniform over the CTA
-        const int wi = u * kConsumerThreads + tid;
+    for (int m = 0; m < (ONE_ROW ? 1 : kMaxM); ++m) {
+        int mx = 0;
+#pragma unroll
+        for (int u = 0; u < NW; ++u) {
+            if (row[u] == m) {
+                mx = max(mx, bf16x2_abs_max(v[u].x));
+                mx = max(mx, bf16x2_abs_max(v[u].y));
+                mx = max(mx, bf16x2_abs_max(v[u].z));
+                mx = max(mx, bf16x2_abs_max(v[u].w));
+            }
+        }
+        e[m] = x_scale_exponent(__reduce_max_sync(0xFFFFFFFFu, mx));
+    }
+    __syncwarp();   // every lane has finished reading the previous x from the region
+#pragma unroll
+    for (int u = 0; u < NW; ++u) {
+        if (u * 32 >= words) break;   // uniform over the warp
+        const int wi = u * 32 + lane;
         float s_part = 0.f, p_part = 0.f;
-        const int m = ONE_ROW ? 0 : wi / wpr, wr = wi - m * wpr;
+        const int m = row[u];
+        int em = e[0];
+        if (!ONE_ROW) {
+#pragma unroll
+            for (int mm = 1; mm < kMaxM; ++mm) em = m == mm ? e[mm] : em;
+        }
+        const int r = wi - m * wpr, kb = r / WPS, iw = r - kb * WPS;
         if (wi < words) {
-            const float sc = pow2f(x_scale_exponent(row_max[m]));
+            const float sc = pow2f(em);
             const float sc16 = sc * 0.0625f;   // 4-bit: codes at bits 4-7 of a byte weigh 16x
             const uint4 a = v[u];
             const float x0 = bf16lo(a.x) * sc, x1 = bf16hi(a.x) * sc, x2 = bf16lo(a.y) * sc, x3 = bf16hi(a.y) * sc;
@@ -188,8 +237,9 @@ __device__ __forceinline__ void stage_x(const XStage &xs, const __nv_bfloat16 *x
             }
             s_part = ((x0 + x1) + (x2 + x3)) + ((x4 + x5) + (x6 + x7));
             p_part = (f16x2_sum(p0) + f16x2_sum(p1)) + (f16x2_sum(p2) + f16x2_sum(p3));
-            const int g = wr >> 3, w8 = wr & 7;
-            const uint32_t q = xs.xq + (uint32_t)(m * xrb + (2 * g + (w8 & 1)) * 64 + (w8 >> 1) * 4);
+            const int gl = iw >> 3, w8 = iw & 7;
+            const uint32_t q = xq + (uint32_t)(m * xrb + kb * (Gm::kGroupsPerWarp * 128) + gl * 128 + (w8 & 1) * 64 +
+                                               (w8 >> 1) * 4);
             sts32(q, p0);
             sts32(q + 16, p1);
             sts32(q + 32, p2);
@@ -202,11 +252,24 @@ __device__ __forceinline__ void stage_x(const XStage &xs, const __nv_bfloat16 *x
         p_part += __shfl_xor_sync(0xFFFFFFFFu, p_part, 2);
         s_part += __shfl_xor_sync(0xFFFFFFFFu, s_part, 4);
         p_part += __shfl_xor_sync(0xFFFFFFFFu, p_part, 4);
-        if (wi < words && (wi & 7) == 0) sts64(xs.xsum + (uint32_t)(m * xsrb + (wr >> 3) * 8), s_part, p_part);
+        if (wi < words && (wi & 7) == 0)
+            sts64(xsum + (uint32_t)(m * xsrb + (kb * Gm::kGroupsPerWarp + (iw >> 3)) * 8), s_part, p_part);
     }
-    if (tid < M) inv_scale[tid] = pow2f(-x_scale_exponent(row_max[tid]));
-    consumer_sync();
-    if (tid < kMaxM) row_max[tid] = 0;  // for staging n + 2 (staging n + 1 has barriers in between)
+    if (ONE_ROW) {
+        inv[0] = inv[1] = pow2f(-e[0]);
+    } else {
+        const int j = lane & 3;
+        const int r0 = 2 * j < M ? 2 * j : M - 1, r1 = 2 * j + 1 < M ? 2 * j + 1 : M - 1;
+        int e0 = e[0], e1 = e[0];
+#pragma unroll
+        for (int mm = 1; mm < kMaxM; ++mm) {
+            e0 = r0 == mm ? e[mm] : e0;
+            e1 = r1 == mm ? e[mm] : e1;
+        }
+        inv[0] = pow2f(-e0);
+        inv[1] = pow2f(-e1);
+    }
+    __syncwarp();   // the region is written before any lane's ldmatrix reads it
 }
 
 // Per-thread shared-memory offsets, fixed while one matrix is processed.
@@ -217,6 +280,7 @@ struct ConsumerThread {
     uint32_t xs0, xs1;  // (Xs, X') of this warp's first group in stage 0, x rows of columns 2j and 2j+1
 };
 
+// K: the codes of the staged x (the matmul's K, or one K pass).
 template <int BITS, bool ONE_ROW>
 __device__ __forceinline__ void consumer_init(ConsumerThread &c, int warp, int lane, const XStage &xs, int M_, int K) {
     const int M = ONE_ROW ? 1 : M_;
@@ -239,12 +303,13 @@ __device__ __forceinline__ void consumer_init(ConsumerThread &c, int warp, int l
         // w & ~1 and w | 1
         c.sb = (uint32_t)(gid * 32 + ((((warp >> 3) ^ (gid >> 2)) & 1) << 4) + (((warp >> 1) & 3) << 2));
     }
+    const int KB = (K + Gm::kStageCodes - 1) / Gm::kStageCodes;
     const int xr = (lane & 7) < M ? (lane & 7) : M - 1;
-    c.xq = xs.xq + (uint32_t)(xr * x_row_bytes(M, K) + (lane >> 3) * 16 + warp * Gm::kGroupsPerWarp * 128);
-    const int xsrb = xsum_row_bytes(M, K);
+    c.xq = xs.xq + (uint32_t)(warp * xs.wq + xr * xw_row_bytes(M, KB, BITS) + (lane >> 3) * 16);
+    const int xsrb = xsw_row_bytes(M, KB, BITS);
     const int m0 = 2 * j < M ? 2 * j : M - 1, m1 = 2 * j + 1 < M ? 2 * j + 1 : M - 1;
-    c.xs0 = xs.xsum + (uint32_t)(m0 * xsrb + Gm::kGroupsPerWarp * warp * 8);
-    c.xs1 = xs.xsum + (uint32_t)(m1 * xsrb + Gm::kGroupsPerWarp * warp * 8);
+    c.xs0 = xs.xsum + (uint32_t)(warp * xs.ws + m0 * xsrb);
+    c.xs1 = xs.xsum + (uint32_t)(warp * xs.ws + m1 * xsrb);
 }
 
 // acc += scale * (D - 1024 X') + bias * Xs for one group: D = d[h] (the MMA
@@ -297,8 +362,8 @@ __device__ __forceinline__ void consume_stage(uint32_t st, int kb, const Consume
         sw[r] = lds32(st + kCodesBytes + c.sb + 8 * Gm::kSBRowBytes * r);
         bw[r] = lds32(st + kCodesBytes + kSBRegion + c.sb + 8 * Gm::kSBRowBytes * r);
     }
-    const uint32_t xq = c.xq + (uint32_t)kb * (Gm::kStageGroups * 128);
-    const uint32_t xo = (uint32_t)kb * (Gm::kStageGroups * 8);
+    const uint32_t xq = c.xq + (uint32_t)kb * (Gm::kGroupsPerWarp * 128);
+    const uint32_t xo = (uint32_t)kb * (Gm::kGroupsPerWarp * 8);
     if (BITS == 4) {
 #pragma unroll
         for (int gl = 0; gl < 2; ++gl) {
@@ -306,6 +371,9 @@ __device__ __forceinline__ void consume_stage(uint32_t st, int kb, const Consume
 #pragma unroll
             for (int r = 0; r < 4; ++r) wr[r] = lds64(st + c.code[gl] + 1024 * r);
             float d[2][4];
+#ifdef AQ_V_SPLITACC
+            float d2[2][4];
+#endif
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const uint4 X = ldsm_x4(xq + gl * 128 + i * 64);
@@ -314,13 +382,25 @@ __device__ __forceinline__ void consume_stage(uint32_t st, int kb, const Consume
                     const uint32_t wa = i ? wr[2 * h].y : wr[2 * h].x;
                     const uint32_t wb = i ? wr[2 * h + 1].y : wr[2 * h + 1].x;
                     const uint32_t ta = wa >> 8, tb = wb >> 8;
+#ifdef AQ_V_SPLITACC
+                    float (&dd)[4] = i ? d2[h] : d[h];
+                    mma_f16_16816_zc(dd, lo_pair(wa), lo_pair(wb), hi_pair(wa), hi_pair(wb), X.x, X.y);
+                    mma_f16_16816(dd, lo_pair(ta), lo_pair(tb), hi_pair(ta), hi_pair(tb), X.z, X.w);
+#else
                     if (i == 0)
                         mma_f16_16816_zc(d[h], lo_pair(wa), lo_pair(wb), hi_pair(wa), hi_pair(wb), X.x, X.y);
                     else
                         mma_f16_16816(d[h], lo_pair(wa), lo_pair(wb), hi_pair(wa), hi_pair(wb), X.x, X.y);
                     mma_f16_16816(d[h], lo_pair(ta), lo_pair(tb), hi_pair(ta), hi_pair(tb), X.z, X.w);
+#endif
                 }
             }
+#ifdef AQ_V_SPLITACC
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) d[h][r] += d2[h][r];
+#endif
             float sc[4], bi[4];
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
@@ -366,14 +446,15 @@ __device__ __forceinline__ void consume_stage(uint32_t st, int kb, const Consume
     }
 }
 
-// This warp's partial sums of a tile, times the x scale 2^-e[m] of their column
-// (exact: a power of two), into rw = its [kRows][M] slice; acc is cleared.
+// This warp's partial sums of a tile, times the x scale 2^-e of their column
+// (exact: a power of two; inv[c] for column 2j + c, j = lane % 4), into rw =
+// its [kRows][M] slice; acc is cleared.
 template <bool ONE_ROW>
-__device__ __forceinline__ void write_partials(float *rw, int M, int lane, float (&acc)[2][4], const float *inv_scale) {
+__device__ __forceinline__ void write_partials(float *rw, int M, int lane, float (&acc)[2][4], const float (&inv)[2]) {
     const int gid = lane >> 2, j = lane & 3;
     if (ONE_ROW) {
         if (j == 0) {  // every column holds x row 0: lanes j > 0 carry copies
-            const float sc = inv_scale[0];
+            const float sc = inv[0];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 rw[16 * h + gid] = acc[h][0] * sc;
@@ -385,7 +466,7 @@ __device__ __forceinline__ void write_partials(float *rw, int M, int lane, float
         for (int cc = 0; cc < 2; ++cc) {
             const int m = 2 * j + cc;
             if (m < M) {
-                const float sc = inv_scale[m];
+                const float sc = inv[cc];
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -420,14 +501,14 @@ struct TileCtx {
 // False on a timeout.
 template <bool ONE_ROW>
 __device__ __forceinline__ bool deposit_tile(const TileCtx &t, float (&acc)[2][4], int tcount, int M, int warp,
-                                             int lane, const float *inv_scale, uint64_t timeout_ns,
+                                             int lane, const float (&inv)[2], uint64_t timeout_ns,
                                              const volatile int *abort_flag) {
     constexpr int B = red_bufs<ONE_ROW>();
     const int b = tcount % B;
     const int n_out = kRows * M;
     if (tcount >= B && !mbar_wait_for(t.red_empty + 8 * b, (uint32_t)((tcount / B) - 1) & 1u, timeout_ns, abort_flag))
         return false;
-    write_partials<ONE_ROW>(t.red + (b * kConsumerWarps + warp) * n_out, M, lane, acc, inv_scale);
+    write_partials<ONE_ROW>(t.red + (b * kConsumerWarps + warp) * n_out, M, lane, acc, inv);
     __syncwarp();
     if (lane == 0) mbar_arrive(t.red_full + 8 * b);
     return true;

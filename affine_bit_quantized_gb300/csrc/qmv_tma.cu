@@ -12,8 +12,10 @@
 //  * sixteen consumer warps each take one 128-code column block of a stage
 //    (32 rows x 2 groups) and run the dequantization-free dot product of the
 //    folded form on mma.sync m16n8k16 (fp16 in, fp32 out), with the codes as
-//    exact fp16 values 1024 + q and x staged once per CTA as fp16 fragments
-//    (qmv_consumer.cuh has the arithmetic and its exactness argument);
+//    exact fp16 values 1024 + q and x staged as fp16 fragments, each warp
+//    loading and converting only the slice of x its column blocks use, with
+//    no barrier against the other warps (qmv_consumer.cuh has the arithmetic
+//    and its exactness argument);
 //  * CTAs are persistent, one per SM: each walks its 32-row tiles across the
 //    whole K, the sixteen warps' partial sums are combined in shared memory
 //    in a fixed order, and every output is written exactly once
@@ -51,28 +53,30 @@ using namespace qmv;
 
 constexpr int kThreads = (kConsumerWarps + 2) * 32;   // consumers, TMA producer, reducer
 constexpr int kMaxStages = 4;   // ring depth (36 KB stages); 5 measured no faster
-constexpr int kNumBars = 2 * kMaxStages + 1 + 8;   // full[S], empty[S], x, red_full[4], red_empty[4]
+constexpr int kNumBars = 2 * kMaxStages + 8;   // full[S], empty[S], red_full[4], red_empty[4]
 constexpr int kSmemLimit = 232448;               // dynamic shared memory a CTA may use
 
 struct Layout {
     int stages;      // ring depth (kMaxStages)
-    int x_bytes;     // M rows of x_row_bytes(M, Kp) (x of one K pass)
-    int xsum_off;    // float2 (Xs, X') per row and group, M rows of xsum_row_bytes(M, Kp)
-    int xinfo_off;   // int row_max[2][8], float inv_scale[8]
+    int xq_off;      // per-warp fragment regions of the staged x (one K pass), wq bytes each
+    int wq;
+    int xsum_off;    // per-warp (Xs, X') regions, ws bytes each
+    int ws;
     int red_off;     // float [bufs][16][32][M]
     int yacc_off;    // float [cap][32][M]: tile sums across K passes (when there are several)
     int bar_off;     // uint64 [kNumBars] + abort flag
     int total;       // bytes (excluding the 1024 alignment slack)
 };
 // Kp: codes of K per pass; cap: tiles per batch kept in yacc (0 with one pass)
-__host__ __device__ inline Layout make_layout(int M, int Kp, int cap) {
+__host__ __device__ inline Layout make_layout(int M, int Kp, int cap, int bits) {
     Layout L;
-    L.x_bytes = M * x_row_bytes(M, Kp);
-    L.stages = kMaxStages;   // fits beside the largest rest (M*Kp*2 = 32 KB, M = 8)
-    const int x_off = L.stages * kStageBytes;
-    L.xsum_off = x_off + L.x_bytes;
-    L.xinfo_off = L.xsum_off + M * xsum_row_bytes(M, Kp);
-    L.red_off = L.xinfo_off + kXInfoBytes;
+    const int xb = x_stage_bytes(M, Kp, bits);
+    L.stages = kMaxStages;   // fits beside the largest rest (x of 32 KB, M = 8)
+    L.xq_off = L.stages * kStageBytes;
+    L.wq = xw_region_bytes(xb, M);
+    L.xsum_off = L.xq_off + kConsumerWarps * L.wq;
+    L.ws = xsw_region_bytes(xb, M);
+    L.red_off = L.xsum_off + kConsumerWarps * L.ws;
     L.yacc_off = L.red_off + red_bytes(M);
     L.bar_off = L.yacc_off + cap * kRows * M * 4;
     L.total = L.bar_off + kNumBars * 8 + 16;
@@ -86,13 +90,15 @@ constexpr int kMaxSmem = kSmemLimit;
 // go in batches of `cap`, and for each batch every pass stages its slice of x
 // and runs the batch's tiles over the pass's stages; the reducer keeps the
 // tile sums across passes.  Each weight byte is still read once.  Without
-// MULTI, x is copied in once (kbp and cap are unused).
+// MULTI, x is staged once (kbp and cap are unused).
+// skip_copy: test hook; the producer leaves out the first stage's copies, so the
+// consumers' bounded wait on it expires.
 template <int BITS, bool ONE_ROW, bool MULTI>
 __global__ void __launch_bounds__(kThreads, 1)
 qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
                const __grid_constant__ CUtensorMap tm_b, const __nv_bfloat16 *__restrict__ x,
                __nv_bfloat16 *__restrict__ y, int M, int N, int K, int kbp, int cap, unsigned long long timeout_ns,
-               int *status, int skip_x) {
+               int *status, int skip_copy) {
     using Gm = Geo<BITS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -100,17 +106,14 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
     if (!MULTI) kbp = KB;
     const int P = MULTI ? (KB + kbp - 1) / kbp : 1;                // K passes
     const int Kp = MULTI ? kbp * Gm::kStageCodes : K;
-    const Layout L = make_layout(M, Kp, MULTI ? cap : 0);
+    const Layout L = make_layout(M, Kp, MULTI ? cap : 0, BITS);
     const uint32_t s_base = smem_addr(smem);
     constexpr int NS = kMaxStages;   // compile time: a runtime ring modulus measured 8% slower
-    const uint32_t x_s = s_base + NS * kStageBytes;
-    const XStage xs = {x_s, s_base + (uint32_t)L.xsum_off, s_base + (uint32_t)L.xinfo_off};
-    const float *inv_scale = reinterpret_cast<const float *>(smem + L.xinfo_off + 64);
+    const XStage xs = {s_base + (uint32_t)L.xq_off, s_base + (uint32_t)L.xsum_off, L.wq, L.ws};
     float *yacc = reinterpret_cast<float *>(smem + L.yacc_off);
     const uint32_t bar_full = s_base + L.bar_off;          // NS barriers (room for kMaxStages)
     const uint32_t bar_empty = bar_full + kMaxStages * 8;  // NS barriers
-    const uint32_t bar_x = bar_empty + kMaxStages * 8;
-    const uint32_t bar_red = bar_x + 8;                    // red_full[4], red_empty[4]
+    const uint32_t bar_red = bar_empty + kMaxStages * 8;   // red_full[4], red_empty[4]
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.bar_off + kNumBars * 8);
     TileCtx tc;
     tc.red = reinterpret_cast<float *>(smem + L.red_off);
@@ -129,12 +132,10 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, kConsumerWarps);
         }
-        mbar_init(bar_x, 1);
         for (int p = 0; p < red_bufs<ONE_ROW>(); ++p) {
             mbar_init(tc.red_full + 8 * p, kConsumerWarps);
             mbar_init(tc.red_empty + 8 * p, 1);
         }
-        for (int m = 0; m < 2 * kMaxM; ++m) reinterpret_cast<int *>(smem + L.xinfo_off)[m] = 0;
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -168,6 +169,10 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                 const int tile = (int)blockIdx.x + t * (int)gridDim.x;
                 const uint32_t dst = s_base + slot * kStageBytes;
                 const uint32_t fb = bar_full + 8 * slot;
+                if (skip_copy && it == 0) {   // test hook: this stage never arrives
+                    advance();
+                    return;
+                }
                 // one box of 8 chunks x 32 rows x 128 bytes (chunks past the row's end read as
                 // zeros and still count toward the transaction)
                 mbar_expect_tx(fb, (uint32_t)(kCodesBytes + 2 * kRows * Gm::kSBRowBytes));
@@ -180,13 +185,7 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
             bool ok = true;
             // the weights do not depend on the preceding kernel: prefetch them first
             for (; issued < L_items && issued < NS; ++issued) issue(issued);
-            griddep_wait();
             const uint64_t deadline = global_timer() + timeout_ns;
-            if (!MULTI && !skip_x) {  // skip_x: test hook that leaves the x barrier incomplete
-                mbar_expect_tx(bar_x, (uint32_t)(M * K * 2));
-                for (int m = 0; m < M; ++m)
-                    bulk_load(x_s + m * x_row_bytes(M, K), x + (int64_t)m * K, (uint32_t)(K * 2), bar_x);
-            }
             for (; issued < L_items; ++issued) {
                 const int slot = issued % NS;
                 if (!mbar_wait(bar_empty + 8 * slot, ((issued / NS) - 1) & 1, deadline, abort_flag)) {
@@ -204,9 +203,6 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                 const uint64_t drain = global_timer() + timeout_ns;
                 for (int it = (issued > NS ? issued - NS : 0); it < issued; ++it)
                     while (!mbar_try_wait(bar_full + 8 * (it % NS), (it / NS) & 1) && global_timer() < drain) {
-                    }
-                if (!MULTI)
-                    while (!mbar_try_wait(bar_x, 0) && global_timer() < drain) {
                     }
             }
         }
@@ -237,23 +233,14 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
         }
     } else {
         // ---------------------------------------------------------------- consumers
-        // Every consumer warp runs the whole loop, even after a timeout, because
-        // the named barriers in stage_x need all of them; after an abort the
-        // waits return at once and the work is skipped.
+        // Each warp stages its own slice of x (no barrier with the other warps)
+        // and runs every tile over its column blocks; after an abort the waits
+        // return at once and the work is skipped.
         griddep_wait();  // x comes from the preceding kernel; the deadline starts after it
         const uint64_t deadline = global_timer() + timeout_ns;
-        bool alive = true;
-        auto fail = [&]() {
-            if (alive && !*abort_flag) {
-                atomicExch(status, (int)AQ_DEVICE_STATUS_TIMEOUT);
-                *abort_flag = 1;
-            }
-            alive = false;
-        };
-        if (!MULTI && !mbar_wait(bar_x, 0, deadline, abort_flag)) fail();
-
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        bool ok = alive && !*abort_flag;
+        float inv[2];
+        bool ok = !*abort_flag;
         int item = 0, tcount = 0;
         // one tile over stages [kb0, kb1) of the staged slice of x, then its partials to the reducer
         auto run_tile = [&](const ConsumerThread &ct, int kb0, int kb1, int nblk) {
@@ -268,31 +255,32 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
             }
-            if (ok) ok = deposit_tile<ONE_ROW>(tc, acc, tcount, M, warp, lane, inv_scale, timeout_ns, abort_flag);
+            if (ok) ok = deposit_tile<ONE_ROW>(tc, acc, tcount, M, warp, lane, inv, timeout_ns, abort_flag);
             ++tcount;
         };
         if (!MULTI) {
-            // raw bf16 rows -> fp16 fragments, group sums and scales, in place
-            stage_x<false, BITS, ONE_ROW>(xs, nullptr, x_s, M, K, 0, K);
+            stage_x_warp<BITS, ONE_ROW>(xs, x, M, K, K, warp, lane, inv);
             ConsumerThread ct;
             consumer_init<BITS, ONE_ROW>(ct, warp, lane, xs, M, K);
             for (int t = 0; t < my_tiles; ++t) run_tile(ct, 0, KB, K / Gm::kWarpCodes);
         } else {
-            int nstaged = 0;
             for (int tb = 0; tb < my_tiles; tb += cap) {
                 const int tb_end = tb + cap < my_tiles ? tb + cap : my_tiles;
                 for (int p = 0; p < P; ++p) {
                     const int k0 = p * Kp, Kpass = K - k0 < Kp ? K - k0 : Kp;
                     const int kb0 = p * kbp, kb1 = kb0 + kbp < KB ? kb0 + kbp : KB;
                     // the pass's slice of x, from L2
-                    stage_x<true, BITS, ONE_ROW>(xs, x + k0, 0, M, Kpass, nstaged++, K);
+                    stage_x_warp<BITS, ONE_ROW>(xs, x + k0, M, Kpass, K, warp, lane, inv);
                     ConsumerThread ct;
                     consumer_init<BITS, ONE_ROW>(ct, warp, lane, xs, M, Kpass);
                     for (int t = tb; t < tb_end; ++t) run_tile(ct, kb0, kb1, Kpass / Gm::kWarpCodes);
                 }
             }
         }
-        if (!ok) fail();
+        if (!ok && lane == 0 && !*abort_flag) {
+            atomicExch(status, (int)AQ_DEVICE_STATUS_TIMEOUT);
+            *abort_flag = 1;
+        }
     }
 }
 
@@ -407,11 +395,11 @@ cudaError_t launch_qmv_tma(const MatmulArgs &a) {
     const int tpc = (T + grid - 1) / grid;
     int cap = 0;   // tiles per batch whose sums stay in shared memory across the passes
     if (P > 1) {
-        const int free_bytes = kSmemLimit - 1024 - make_layout(M, kbp * SC, 0).total;
+        const int free_bytes = kSmemLimit - 1024 - make_layout(M, kbp * SC, 0, a.bits).total;
         cap = std::min(tpc, free_bytes / (kRows * M * 4));
         if (cap < 1) return cudaErrorInvalidConfiguration;
     }
-    const Layout L = make_layout(M, P > 1 ? kbp * SC : K, cap);
+    const Layout L = make_layout(M, P > 1 ? kbp * SC : K, cap, a.bits);
     const int smem = L.total + 1024;
     if (smem > kSmemLimit) return cudaErrorInvalidConfiguration;
     const bool one = (M == 1), eight = (a.bits == 8), multi = (P > 1);
@@ -454,7 +442,7 @@ cudaError_t launch_qmv_tma(const MatmulArgs &a) {
     return cudaLaunchKernelEx(&cfg, kern, tw, ts, tb, static_cast<const __nv_bfloat16 *>(a.x),
                               static_cast<__nv_bfloat16 *>(a.y), M, N, K, kbp, std::max(cap, 1),
                               (unsigned long long)a.timeout_ns,
-                              a.status, a.debug_skip_x ? 1 : 0);
+                              a.status, a.debug_skip_copy ? 1 : 0);
 }
 
 }  // namespace aq

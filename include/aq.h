@@ -86,14 +86,14 @@ typedef enum aq_kernel {
  * were not written by the kernel immediately before on the stream. */
 #define AQ_FLAG_PDL 0x1u
 /* Test hook for the failure path of the bounded device-side waits: the
- * weight-streaming kernel's producer omits the copy of x, so its
- * consumers' wait expires (after 20 ms instead of the normal 2 s), the
- * kernel records a timeout in the device status word and returns without
- * writing y.  Only where that kernel stages x in one piece: 1 <= M <= 8,
- * K a multiple of 512, and x within 32 KB rounded up to whole 2048-code
- * stages (4-bit) or 1024-code stages (8-bit); otherwise AQ_ERR_UNSUPPORTED.
- * Read the outcome with aq_read_device_status(). */
-#define AQ_FLAG_DEBUG_SKIP_X 0x80000000u
+ * kernel's copy producer leaves out one of its copies, so the consumers'
+ * wait for it expires (after 20 ms instead of the normal 2 s), the kernel
+ * records a timeout in the device status word and returns without a valid y.
+ * Taken by the weight-streaming kernel (1 <= M <= 8, K a multiple of 512,
+ * 16-byte aligned scales and biases) and by the tensor-core kernel
+ * (AQ_KERNEL_QMM); elsewhere AQ_ERR_UNSUPPORTED.  Read the outcome with
+ * aq_read_device_status(). */
+#define AQ_FLAG_DEBUG_SKIP_COPY 0x80000000u
 
 /*
  * y = x . dequant(W)^T as defined above.

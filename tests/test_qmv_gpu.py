@@ -208,22 +208,22 @@ def test_tma_kernel_x_dynamic_range(dev, M):
 
 
 def test_bounded_wait_timeout_reports_status(dev):
-    """The test hook leaves the x barrier incomplete: the kernel's bounded wait
-    expires, it records a timeout, the host reads AQ_ERR_TIMEOUT, and the
-    context stays usable (a normal call right after is correct)."""
+    """The test hook leaves out the first stage's copy: the consumers' bounded
+    wait expires, the kernel records a timeout, the host reads AQ_ERR_TIMEOUT,
+    and the context stays usable (a normal call right after is correct)."""
     import torch
     M, N, K = 1, 64, 1024
     w = synth.make_weights(N, K, 8)
     x = synth.make_x(M, K, 8)
     xt, wt, st, bt = upload(x, w, dev)
     assert aq.aq_read_device_status(None) == aq.AQ_OK
-    aq.matmul(xt, wt, st, bt, flags=aq.AQ_FLAG_DEBUG_SKIP_X)
+    aq.matmul(xt, wt, st, bt, flags=aq.AQ_FLAG_DEBUG_SKIP_COPY)
     assert aq.aq_read_device_status(torch.cuda.current_stream().cuda_stream) == aq.AQ_ERR_TIMEOUT
     assert aq.aq_read_device_status(None) == aq.AQ_OK          # cleared by the read
     check(dev, M, N, K, 8)
     with pytest.raises(aq.AqError):
         aq.matmul(xt[:, :64].contiguous(), wt[:, :8].contiguous(), st[:, :1].contiguous(), bt[:, :1].contiguous(),
-                  flags=aq.AQ_FLAG_DEBUG_SKIP_X)                # K = 64: no TMA kernel, hook unsupported
+                  flags=aq.AQ_FLAG_DEBUG_SKIP_COPY)                # K = 64: no TMA kernel, hook unsupported
 
 
 # ---------------------------------------------------------------- 8-bit codes (TMA-fed kernel)
