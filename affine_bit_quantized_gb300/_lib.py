@@ -28,6 +28,7 @@ AQ_KERNEL_QMM = 2
 AQ_FLAG_PDL = 1
 AQ_FLAG_DEBUG_SKIP_COPY = 1 << 31
 AQ_CHAIN_INDEPENDENT = 1
+AQ_CHAIN_DEBUG_SKIP_COPY = 0x40000000
 
 _lock = threading.Lock()
 _lib = None
@@ -102,6 +103,8 @@ def load() -> ctypes.CDLL:
             lib.aq_gather_qmm_bf16.restype = I
             lib.aq_matmul_nvfp4_bf16.argtypes = [P, P, P, ctypes.c_float, P, I64, I64, I64, U, P]
             lib.aq_matmul_nvfp4_bf16.restype = I
+            lib.aq_read_probe.argtypes = [P, ctypes.c_size_t, P]
+            lib.aq_read_probe.restype = I
             lib.aq_version.argtypes = []
             lib.aq_version.restype = I
             _lib = lib
@@ -245,6 +248,10 @@ def aq_gather_qmm_bf16(x, w_packed, scales, biases, lhs_indices, rhs_indices, y,
 
 def aq_matmul_nvfp4_bf16(x, w_packed, scales_e4m3, global_scale, y, M, N, K, flags, stream) -> int:
     return load().aq_matmul_nvfp4_bf16(x, w_packed, scales_e4m3, global_scale, y, M, N, K, flags, stream)
+
+
+def aq_read_probe(buf, nbytes, stream) -> int:
+    return load().aq_read_probe(buf, nbytes, stream)
 
 
 def aq_read_device_status(stream) -> int:

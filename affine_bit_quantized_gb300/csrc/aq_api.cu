@@ -138,10 +138,9 @@ aq_status matmul_impl(const void *x, const uint32_t *w_packed, const void *scale
         return true;
     };
     if (kernel == AQ_KERNEL_QMM || (kernel == AQ_KERNEL_AUTO && M > kQmvMaxRows)) {
-        if (a.debug_skip_copy) return AQ_ERR_UNSUPPORTED;
         if (workspace && aligned(workspace, 128) && workspace_bytes >= (size_t)(M * K * 2)) a.xf16 = workspace;
         if (aq::qmm_supported(a)) return record_cuda(aq::launch_qmm(a));
-        if (kernel == AQ_KERNEL_QMM) return AQ_ERR_UNSUPPORTED;
+        if (kernel == AQ_KERNEL_QMM || a.debug_skip_copy) return AQ_ERR_UNSUPPORTED;
     }
     if (bits == 8) {
         // 8-bit codes have no general decode kernel: the TMA-fed one, in launches
@@ -166,7 +165,7 @@ aq_status matmul_impl(const void *x, const uint32_t *w_packed, const void *scale
         st = AQ_OK;
         if (tma_rows(rows, &st)) return st;
     }
-    if (a.debug_skip_copy) return AQ_ERR_UNSUPPORTED;  // the hook exists only in the TMA kernel
+    if (a.debug_skip_copy) return AQ_ERR_UNSUPPORTED;  // the general kernel has no copy producer
     // Weight-streaming passes over at most 16 rows of x each.
     for (int64_t m0 = 0; m0 < M; m0 += kQmvMaxRows) {
         a.x = static_cast<const uint16_t *>(x) + m0 * K;
@@ -442,6 +441,15 @@ aq_status aq_matmul_nvfp4_bf16(const void *x, const uint32_t *w_packed, const ui
     return record_cuda(aq::launch_nvfp4_qmv(a));
 }
 
-int aq_version(void) { return 100; }
+aq_status aq_read_probe(const void *buf, size_t bytes, void *stream) {
+    if (!buf || bytes < 16384) return AQ_ERR_INVALID_ARG;
+    if (!aligned(buf, 16)) return AQ_ERR_ALIGNMENT;
+    int *status = nullptr;
+    aq_status st = record_cuda(status_ptr(&status));
+    if (st != AQ_OK) return st;
+    return record_cuda(aq::launch_read_probe(buf, bytes, kTimeoutNs, status, static_cast<cudaStream_t>(stream)));
+}
+
+int aq_version(void) { return 200; }
 
 }  // extern "C"

@@ -100,4 +100,7 @@ int chain_static_max();
 aq_status chain_run_static(const aq_matmul_desc *descs, int count, int group_size, int bits, uint64_t timeout_ns,
                            int *status, cudaStream_t stream, cudaError_t *err);
 
+// Read-only TMA stream over floor(bytes / 16384) chunks of 16 KB (read_probe.cu).
+cudaError_t launch_read_probe(const void *buf, size_t bytes, uint64_t timeout_ns, int *status, cudaStream_t stream);
+
 }  // namespace aq

@@ -327,7 +327,7 @@ nvfp4_qmv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
             }
-            if (ok) ok = deposit_tile<ONE_ROW>(tc, acc, tl, M, warp, lane, inv, timeout_ns, abort_flag);
+            if (ok) ok = deposit_tile<ONE_ROW>(tc, acc, tl, M, warp, lane, lane >> 2, inv, timeout_ns, abort_flag);
         }
         if (!ok) fail();
     }

@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
            const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_b,
            __nv_bfloat16 *__restrict__ y, int M, int N, int K, unsigned long long timeout_ns, int *status,
-           const int *__restrict__ plan) {
+           const int *__restrict__ plan, int skip_copy) {
     using C = Cfg<BITS, XPRE>;
     constexpr int kConvStages = C::kConvStages;
     constexpr int kTileM = C::kTileM, kATileBytes = C::kATileBytes, kConvStageBytes = C::kConvStageBytes;
@@ -452,10 +452,26 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         }
     };
 
+    int issued_raw = 0, issued_sb = 0, issued_conv = 0;   // copies issued (producer thread)
+    // let every copy issued land before the CTA may exit (bounded)
+    auto drain_copies = [&]() {
+        const uint64_t drain = global_timer() + timeout_ns;
+        for (int i = (issued_raw > kRawStages ? issued_raw - kRawStages : 0); i < issued_raw; ++i)
+            while (!mbar_try_wait(raw_full(i % kRawStages), (i / kRawStages) & 1) && global_timer() < drain) {
+            }
+        for (int j = (issued_sb > kSBStages ? issued_sb - kSBStages : 0); j < issued_sb; ++j)
+            while (!mbar_try_wait(sb_full(j % kSBStages), (j / kSBStages) & 1) && global_timer() < drain) {
+            }
+        if (XPRE)
+            for (int i = (issued_conv > kConvStages ? issued_conv - kConvStages : 0); i < issued_conv; ++i)
+                while (!mbar_try_wait(x_full(i % kConvStages), (i / kConvStages) & 1) && global_timer() < drain) {
+                }
+    };
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int issued_raw = 0, issued_sb = 0, issued_conv = 0;
+            // test hook: the first CTA leaves out its first raw copy, so its consumers' wait expires
+            const bool skip_first = skip_copy && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
             bool ok = true;
             for (int i = 0; i < steps && ok; ++i) {
                 const int rs = i % kRawStages;
@@ -476,9 +492,11 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                     break;
                 }
                 const uint32_t dst = base + kOffRaw + rs * kRawStageBytes;
-                mbar_expect_tx(raw_full(rs), kRawStageBytes);
-                if (!XPRE) tma_load_2d(dst, &tm_x, (g0 + i) * kGroup, m0, raw_full(rs));
-                tma_load_2d(dst + kRawXBytes, &tm_w, (g0 + i) * C::kRowWords, wrow0, raw_full(rs));
+                if (!(skip_first && i == 0)) {
+                    mbar_expect_tx(raw_full(rs), kRawStageBytes);
+                    if (!XPRE) tma_load_2d(dst, &tm_x, (g0 + i) * kGroup, m0, raw_full(rs));
+                    tma_load_2d(dst + kRawXBytes, &tm_w, (g0 + i) * C::kRowWords, wrow0, raw_full(rs));
+                }
                 issued_raw = i + 1;
                 if (XPRE) {
                     // fp16 x straight into the converted stage, once the MMAs have released it
@@ -493,22 +511,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                     issued_conv = i + 1;
                 }
             }
-            if (!ok) {
-                fail();
-                // let the copies already issued land before the CTA may exit
-                const uint64_t drain = global_timer() + timeout_ns;
-                for (int i = (issued_raw > kRawStages ? issued_raw - kRawStages : 0); i < issued_raw; ++i)
-                    while (!mbar_try_wait(raw_full(i % kRawStages), (i / kRawStages) & 1) && global_timer() < drain) {
-                    }
-                for (int j = (issued_sb > kSBStages ? issued_sb - kSBStages : 0); j < issued_sb; ++j)
-                    while (!mbar_try_wait(sb_full(j % kSBStages), (j / kSBStages) & 1) && global_timer() < drain) {
-                    }
-                if (XPRE)
-                    for (int i = (issued_conv > kConvStages ? issued_conv - kConvStages : 0); i < issued_conv; ++i)
-                        while (!mbar_try_wait(x_full(i % kConvStages), (i / kConvStages) & 1) &&
-                               global_timer() < drain) {
-                        }
-            }
+            if (!ok) fail();   // the copies issued are drained at the end of the kernel
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -700,7 +703,11 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         }
     }
 
-    // every role ends here; wait (bounded) for the MMAs before freeing TMEM
+    // every role ends here.  After an abort, whichever role gave up: the
+    // producer waits (bounded) for every copy it issued, so that none lands in
+    // this CTA's shared memory after it exits, and the MMA issuer waits
+    // (bounded) for the MMAs before TMEM is freed.
+    if (warp == 0 && lane == 0 && *abort_flag) drain_copies();
     if (warp == 1 && lane == 0 && *abort_flag) {
         const uint64_t drain = global_timer() + timeout_ns;
         while (!mbar_try_wait(acc_done, 0) && global_timer() < drain) {
@@ -854,7 +861,8 @@ cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev) {
     cfg.attrs = attr;
     cfg.numAttrs = (unsigned)na;
     return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS, false, XPRE>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(a.y), M,
-                              N, K, (unsigned long long)a.timeout_ns, a.status, (const int *)nullptr);
+                              N, K, (unsigned long long)a.timeout_ns, a.status, (const int *)nullptr,
+                              a.debug_skip_copy ? 1 : 0);
 }
 }  // namespace
 
@@ -974,7 +982,7 @@ cudaError_t launch_gather_bits(const GatherArgs &g, int dev, int sms) {
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = g.stream;
     return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS, true, true>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(g.y), R, N,
-                              K, (unsigned long long)g.timeout_ns, g.status, (const int *)plan);
+                              K, (unsigned long long)g.timeout_ns, g.status, (const int *)plan, 0);
 }
 
 }  // namespace

@@ -119,6 +119,19 @@ __device__ __forceinline__ void acquire_record_maps(const ChainRec *r) {
     acquire_tensormap(&r->tb);
 }
 
+#ifdef AQ_V_TRACE
+// timing trace of a launch: [cta][matmul][6] global-timer stamps (working instrument)
+__device__ unsigned long long *g_chain_trace;
+#define CHAIN_TRACE(ev, jm)                                                                                  \
+    do {                                                                                                     \
+        if (g_chain_trace) g_chain_trace[((size_t)blockIdx.x * count + (jm)) * 6 + (ev)] = global_timer(); \
+    } while (0)
+#else
+#define CHAIN_TRACE(ev, jm) \
+    do {                    \
+    } while (0)
+#endif
+
 // The scalar part of a record (three 16-byte vectors).
 struct RecInfo {
     const __nv_bfloat16 *x;
@@ -232,6 +245,11 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
                             ok = false;
                             break;
                         }
+                        if (tile == first && kb == 0) CHAIN_TRACE(0, jm);
+                        if ((cur.flags & AQ_CHAIN_DEBUG_SKIP_COPY) && cta == 0 && tile == first && kb == 0) {
+                            ++issued;   // test hook: this stage never arrives
+                            continue;
+                        }
                         const uint32_t dst = s_base + slot * kStageBytes;
                         const uint32_t fb = bar_full + 8 * slot;
                         // one copy of the stage's codes (chunks past the row's end read as zeros)
@@ -280,6 +298,7 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
                             ok = false;
                         }
                     }
+                    CHAIN_TRACE(1, jm);
                     mbar_arrive(bar_dep);
                 }
                 ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
@@ -287,6 +306,7 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
             const int first = (cta - cur.tile_base % ncta + ncta) % ncta;
             for (int tile = first; tile < cur.T && ok; tile += ncta, ++pending, ++tcount)
                 ok = reduce_tile<ONE_ROW>(tc, tcount, tile, cur.M, cur.N, cur.y, lane, timeout_ns, abort_flag);
+            if (lane == 0 && first < cur.T) CHAIN_TRACE(4, jm);
             const bool group_ends = jm + 1 == count || !(nxt.flags & AQ_CHAIN_INDEPENDENT);
             if (ok && group_ends && pending > 0 && lane == 0) {
                 // every lane's y stores precede this (reduce_tile ends with __syncwarp);
@@ -330,13 +350,13 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
             prev_K = K;
             prev_bits = cur.bits;
 
-            auto run = [&](auto width) {
-                constexpr int BITS = decltype(width)::value;
+            {
                 using Gm = Geo<BITS>;
                 const int nblk = K / Gm::kWarpCodes;
                 const int KB = (K + Gm::kStageCodes - 1) / Gm::kStageCodes;
                 // ---- this warp's slice of x: L2 loads, fp16 fragments, group sums and scale
                 if (new_x && ok) stage_x_warp<BITS, ONE_ROW>(xs, cur.x, M, K, K, warp, lane, inv);
+                if (warp == 0 && lane == 0) CHAIN_TRACE(2, jm);
 
                 ConsumerThread ct;
                 consumer_init<BITS, ONE_ROW>(ct, warp, lane, xs, M, K);
@@ -354,13 +374,15 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
                             consume_stage<BITS, ONE_ROW>(s_base + (uint32_t)(slot * kStageBytes), kb, ct, acc);
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+                        if (warp == 0 && lane == 0 && tile == first && kb == 0) CHAIN_TRACE(3, jm);
                     }
                     if (!ok) break;
-                    ok = deposit_tile<ONE_ROW>(tc, acc, tcount, M, warp, lane, inv, timeout_ns, abort_flag);
+                    if (warp == 0 && lane == 0 && tile + ncta >= T) CHAIN_TRACE(5, jm);
+                    ok = deposit_tile<ONE_ROW>(tc, acc, tcount, M, warp, lane, mma_row<BITS>(lane), inv, timeout_ns,
+                                               abort_flag);
                     ++tcount;
                 }
-            };
-            run(std::integral_constant<int, BITS>());
+            }
             if (!ok) set_abort();   // the remaining matmuls are walked through without work
             cur = nxt;
         }
@@ -368,6 +390,15 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
 }
 
 // ---------------------------------------------------------------- host side
+#ifdef AQ_V_TRACE
+}  // namespace
+}  // namespace aq
+extern "C" int aq_chain_trace_set(void *p) {
+    return (int)cudaMemcpyToSymbol(aq::g_chain_trace, &p, sizeof p);
+}
+namespace aq {
+namespace {
+#endif
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -419,7 +450,7 @@ aq_status chain_validate(const aq_matmul_desc *descs, int count, int group_size,
     for (int i = 0; i < count; ++i) {
         const aq_matmul_desc &d = descs[i];
         if (d.M < 1 || d.N < 1 || d.K < 1 || d.K % 64) return AQ_ERR_INVALID_ARG;
-        if (d.flags & ~(int64_t)AQ_CHAIN_INDEPENDENT) return AQ_ERR_INVALID_ARG;
+        if (d.flags & ~(int64_t)(AQ_CHAIN_INDEPENDENT | AQ_CHAIN_DEBUG_SKIP_COPY)) return AQ_ERR_INVALID_ARG;
         if (!d.x || !d.w_packed || !d.scales || !d.biases || !d.y) return AQ_ERR_INVALID_ARG;
         if (d.M > 8 || d.K % 512 || d.K > (int64_t)1 << 20 || d.N > (int64_t)1 << 30) return AQ_ERR_UNSUPPORTED;
         if (x_stage_bytes((int)d.M, (int)d.K, bits) > kMaxXBytes) return AQ_ERR_UNSUPPORTED;
@@ -467,6 +498,8 @@ aq_status chain_encode(const aq_matmul_desc *descs, int count, int bits, ChainRe
     plan->x_bytes = (x_bytes + 15) & ~15;
     plan->one_row = one_row ? 1 : 0;
     plan->reserved[0] = bits;   // code width of the chain (selects the kernel)
+    for (int i = 0; i < count; ++i)
+        if (descs[i].flags & AQ_CHAIN_DEBUG_SKIP_COPY) plan->reserved[1] = 1;   // the test hook: short waits
     return AQ_OK;
 }
 
@@ -497,6 +530,7 @@ aq_status chain_prepare(const aq_matmul_desc *descs, int count, int group_size, 
 }
 
 cudaError_t chain_run(const aq_chain_plan *plan, uint64_t timeout_ns, int *status, cudaStream_t stream) {
+    if (plan->reserved[1]) timeout_ns = 20000000ull;   // the test hook: 20 ms waits
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

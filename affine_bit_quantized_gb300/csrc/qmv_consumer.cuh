@@ -281,11 +281,23 @@ struct ConsumerThread {
 };
 
 // K: the codes of the staged x (the matmul's K, or one K pass).
+// Tile row (within each group of 8 rows) that MMA row lane/4 stands for.
+#ifdef AQ_V_ROWPERM
+template <int BITS>
+__device__ __forceinline__ int mma_row(int lane) {
+    const int g = lane >> 2;
+    return BITS == 4 ? ((g & 3) << 1) | (g >> 2) : (g >> 1) | ((g & 1) << 2);
+}
+#else
+template <int BITS>
+__device__ __forceinline__ int mma_row(int lane) { return lane >> 2; }
+#endif
+
 template <int BITS, bool ONE_ROW>
 __device__ __forceinline__ void consumer_init(ConsumerThread &c, int warp, int lane, const XStage &xs, int M_, int K) {
     const int M = ONE_ROW ? 1 : M_;
     using Gm = Geo<BITS>;
-    const int gid = lane >> 2, j = lane & 3;
+    const int gid = mma_row<BITS>(lane), j = lane & 3;
     // code boxes use the 128-byte swizzle: 16-byte chunk c of box row r sits at chunk c ^ (r % 8)
     if (BITS == 4) {
         // words 2j, 2j+1 of groups 2w, 2w+1: 8 bytes per group
@@ -448,10 +460,12 @@ __device__ __forceinline__ void consume_stage(uint32_t st, int kb, const Consume
 
 // This warp's partial sums of a tile, times the x scale 2^-e of their column
 // (exact: a power of two; inv[c] for column 2j + c, j = lane % 4), into rw =
-// its [kRows][M] slice; acc is cleared.
+// its [kRows][M] slice; gid: the tile row (mod 8) of this lane's MMA rows;
+// acc is cleared.
 template <bool ONE_ROW>
-__device__ __forceinline__ void write_partials(float *rw, int M, int lane, float (&acc)[2][4], const float (&inv)[2]) {
-    const int gid = lane >> 2, j = lane & 3;
+__device__ __forceinline__ void write_partials(float *rw, int M, int lane, int gid, float (&acc)[2][4],
+                                               const float (&inv)[2]) {
+    const int j = lane & 3;
     if (ONE_ROW) {
         if (j == 0) {  // every column holds x row 0: lanes j > 0 carry copies
             const float sc = inv[0];
@@ -501,14 +515,14 @@ struct TileCtx {
 // False on a timeout.
 template <bool ONE_ROW>
 __device__ __forceinline__ bool deposit_tile(const TileCtx &t, float (&acc)[2][4], int tcount, int M, int warp,
-                                             int lane, const float (&inv)[2], uint64_t timeout_ns,
+                                             int lane, int gid, const float (&inv)[2], uint64_t timeout_ns,
                                              const volatile int *abort_flag) {
     constexpr int B = red_bufs<ONE_ROW>();
     const int b = tcount % B;
     const int n_out = kRows * M;
     if (tcount >= B && !mbar_wait_for(t.red_empty + 8 * b, (uint32_t)((tcount / B) - 1) & 1u, timeout_ns, abort_flag))
         return false;
-    write_partials<ONE_ROW>(t.red + (b * kConsumerWarps + warp) * n_out, M, lane, acc, inv);
+    write_partials<ONE_ROW>(t.red + (b * kConsumerWarps + warp) * n_out, M, lane, gid, acc, inv);
     __syncwarp();
     if (lane == 0) mbar_arrive(t.red_full + 8 * b);
     return true;

@@ -255,7 +255,7 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
             }
-            if (ok) ok = deposit_tile<ONE_ROW>(tc, acc, tcount, M, warp, lane, inv, timeout_ns, abort_flag);
+            if (ok) ok = deposit_tile<ONE_ROW>(tc, acc, tcount, M, warp, lane, mma_row<BITS>(lane), inv, timeout_ns, abort_flag);
             ++tcount;
         };
         if (!MULTI) {

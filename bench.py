@@ -351,6 +351,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--layers", type=int, default=32, help="decoder layers in the step (32 = the workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--step-only", action="store_true",
+                    help="time the decode step (and its end-to-end form) only, without the side measurements")
     ap.add_argument("--case", default=None,
                     help="M,N,K: time one matrix shape instead of the decode step (also the ncu target)")
     ap.add_argument("--kernel", choices=("auto", "qmv", "qmm"), default="auto", help="kernel for --case")
@@ -396,7 +398,7 @@ def main():
     hbm_peak, bf16_peak, bf16_sus, peak_src = load_peaks()
 
     # ---- workload (generated on the host from the seeded recipe, uploaded once)
-    cpu_layers = {0, 1} if (rank == 0 and world == 1 and not args.no_cpu_baseline) else set()
+    cpu_layers = {0, 1} if (rank == 0 and world == 1 and not args.no_cpu_baseline and not args.step_only) else set()
     ds = DecodeStep(dev, args.layers, keep_host=bool(cpu_layers), host_layers=cpu_layers)
     mats, launches = ds.mats, ds.launches
     offs, _ = x_layout(args.layers)
@@ -454,6 +456,22 @@ def main():
     if aq.aq_read_device_status(cur.cuda_stream) != aq.AQ_OK:
         raise RuntimeError("a bounded device-side wait expired during the timed steps")
 
+    # ---- read-only streaming ceiling of this device: TMA bulk reads of a 4 GiB
+    # buffer with no arithmetic (aq_read_probe), best of 5 runs of 10 launches
+    probe_buf = torch.empty(4 << 30, dtype=torch.uint8, device=dev)
+
+    def probe_once():
+        rc = aq.aq_read_probe(probe_buf.data_ptr(), probe_buf.numel(), cur.cuda_stream)
+        if rc != aq.AQ_OK:
+            raise aq.AqError(rc, "aq_read_probe")
+
+    for _ in range(3):
+        probe_once()
+    read_peak = max(probe_buf.numel() / (time_steps(probe_once, 10) * 1e-3) / 1e9 for _ in range(5))
+    del probe_buf
+    if aq.aq_read_device_status(cur.cuda_stream) != aq.AQ_OK:
+        raise RuntimeError("a bounded device-side wait expired in the read probe")
+
     # ---- end to end: inputs copied in from pinned host memory, logits read back, every step
     h2d = x_pinned.numel() * 2
     d2h = logits_pinned.numel() * 2
@@ -468,182 +486,190 @@ def main():
         e2e_step()
     ms_e2e = max_over_ranks(time_steps(e2e_step, args.steps), world, dev)
 
-    # ---- per-matrix kernel times (the 32 layer copies of each shape back to back)
-    per_matrix = {}
-    reps = 5
-    for j, (name, N, K) in enumerate(synth.LLAMA8B_LAYER + (synth.LLAMA8B_LM_HEAD,)):
-        sel = {i for i, m in enumerate(mats) if (m[2] == name)}
-        for _ in range(2):
-            enqueue(cur.cuda_stream, sel)
-        torch.cuda.synchronize(dev)
-        e0.record(cur)
-        for _ in range(reps):
-            enqueue(cur.cuda_stream, sel)
-        e1.record(cur)
-        e1.synchronize()
-        us = e0.elapsed_time(e1) * 1e3 / (reps * len(sel))
-        per_matrix[name] = {"N": N, "K": K, "us_per_call": round(us, 3),
-                            "gbs": round(alg_bytes(1, N, K) / (us * 1e-6) / 1e9, 1)}
-
-    def time_calls(launch, n_calls, reps=5):
-        for i in range(2 * n_calls):
-            launch(i)
-        torch.cuda.synchronize(dev)
-        e0.record(cur)
-        for i in range(reps * n_calls):
-            launch(i)
-        e1.record(cur)
-        e1.synchronize()
-        return e0.elapsed_time(e1) * 1e3 / (reps * n_calls)
-
-    # ---- small batches (the multi-row decode path): M in {2, 4, 8, 16} over the layer shapes
-    # and lm_head, on the step's copies (32 distinct weights per layer shape: no L2 reuse; the
-    # one lm_head, 296 MB, is larger than L2)
-    small_batch = {}
-    for M in (2, 4, 8, 16):
+    def side_sections():
+        """Per-matrix, small-batch, 8-bit, tensor-core, NVFP4 and MoE measurements beside the step."""
+        # ---- per-matrix kernel times (the 32 layer copies of each shape back to back)
+        per_matrix = {}
+        reps = 5
         for j, (name, N, K) in enumerate(synth.LLAMA8B_LAYER + (synth.LLAMA8B_LM_HEAD,)):
-            lm = name == "lm_head"
-            xb = torch.from_numpy(synth.make_x(M, K, synth.seed_for(3, M, j)).view(np.int16)).to(dev)
-            yb = torch.empty((M, N), dtype=torch.int16, device=dev)
-            ws = [weights[(args.layers, 0)]] if lm else [weights[(layer, j)] for layer in range(args.layers)]
+            sel = {i for i, m in enumerate(mats) if (m[2] == name)}
+            for _ in range(2):
+                enqueue(cur.cuda_stream, sel)
+            torch.cuda.synchronize(dev)
+            e0.record(cur)
+            for _ in range(reps):
+                enqueue(cur.cuda_stream, sel)
+            e1.record(cur)
+            e1.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / (reps * len(sel))
+            per_matrix[name] = {"N": N, "K": K, "us_per_call": round(us, 3),
+                                "gbs": round(alg_bytes(1, N, K) / (us * 1e-6) / 1e9, 1)}
 
-            def launch_sb(i, ws=ws, xb=xb, yb=yb, M=M, N=N, K=K):
-                wt, st_, bt = ws[i % len(ws)]
-                rc = lib.aq_matmul_bf16_ex(xb.data_ptr(), wt.data_ptr(), st_.data_ptr(), bt.data_ptr(), yb.data_ptr(),
-                                           M, N, K, 64, 4, aq.AQ_KERNEL_AUTO, aq.AQ_FLAG_PDL, cur.cuda_stream)
+        def time_calls(launch, n_calls, reps=5):
+            for i in range(2 * n_calls):
+                launch(i)
+            torch.cuda.synchronize(dev)
+            e0.record(cur)
+            for i in range(reps * n_calls):
+                launch(i)
+            e1.record(cur)
+            e1.synchronize()
+            return e0.elapsed_time(e1) * 1e3 / (reps * n_calls)
+
+        # ---- small batches (the multi-row decode path): M in {2, 4, 8, 16} over the layer shapes
+        # and lm_head, on the step's copies (32 distinct weights per layer shape: no L2 reuse; the
+        # one lm_head, 296 MB, is larger than L2)
+        small_batch = {}
+        for M in (2, 4, 8, 16):
+            for j, (name, N, K) in enumerate(synth.LLAMA8B_LAYER + (synth.LLAMA8B_LM_HEAD,)):
+                lm = name == "lm_head"
+                xb = torch.from_numpy(synth.make_x(M, K, synth.seed_for(3, M, j)).view(np.int16)).to(dev)
+                yb = torch.empty((M, N), dtype=torch.int16, device=dev)
+                ws = [weights[(args.layers, 0)]] if lm else [weights[(layer, j)] for layer in range(args.layers)]
+
+                def launch_sb(i, ws=ws, xb=xb, yb=yb, M=M, N=N, K=K):
+                    wt, st_, bt = ws[i % len(ws)]
+                    rc = lib.aq_matmul_bf16_ex(xb.data_ptr(), wt.data_ptr(), st_.data_ptr(), bt.data_ptr(), yb.data_ptr(),
+                                               M, N, K, 64, 4, aq.AQ_KERNEL_AUTO, aq.AQ_FLAG_PDL, cur.cuda_stream)
+                    if rc != aq.AQ_OK:
+                        raise aq.AqError(rc, "aq_matmul_bf16_ex")
+
+                us = time_calls(launch_sb, 4 if lm else len(ws))
+                small_batch[f"M{M}_{name}"] = {"M": M, "N": N, "K": K, "us_per_call": round(us, 3),
+                                               "gbs": round(alg_bytes(M, N, K) / (us * 1e-6) / 1e9, 1)}
+
+        # ---- 8-bit codes (same shapes, M = 1): 4 device copies of each weight matrix cycled
+        eight_bit = {}
+        for j, (name, N, K) in enumerate(synth.LLAMA8B_LAYER + (synth.LLAMA8B_LM_HEAD,)):
+            w8 = synth.make_weights(N, K, synth.seed_for(6, 0, j), bits=8)
+            base = (torch.from_numpy(w8.w_packed.view(np.int32)).to(dev), torch.from_numpy(w8.scales.view(np.int16)).to(dev),
+                    torch.from_numpy(w8.biases.view(np.int16)).to(dev))
+            ws8 = [base] + [tuple(t.clone() for t in base) for _ in range(3)]
+            x8 = torch.from_numpy(synth.make_x(1, K, synth.seed_for(6, 1, j)).view(np.int16)).to(dev)
+            y8 = torch.empty((1, N), dtype=torch.int16, device=dev)
+
+            def launch8(i, ws8=ws8, x8=x8, y8=y8, N=N, K=K):
+                wt, st_, bt = ws8[i % len(ws8)]
+                rc = lib.aq_matmul_bf16_ex(x8.data_ptr(), wt.data_ptr(), st_.data_ptr(), bt.data_ptr(), y8.data_ptr(),
+                                           1, N, K, 64, 8, aq.AQ_KERNEL_AUTO, aq.AQ_FLAG_PDL, cur.cuda_stream)
                 if rc != aq.AQ_OK:
                     raise aq.AqError(rc, "aq_matmul_bf16_ex")
 
-            us = time_calls(launch_sb, 4 if lm else len(ws))
-            small_batch[f"M{M}_{name}"] = {"M": M, "N": N, "K": K, "us_per_call": round(us, 3),
-                                           "gbs": round(alg_bytes(M, N, K) / (us * 1e-6) / 1e9, 1)}
+            us = time_calls(launch8, 8)
+            eight_bit[name] = {"N": N, "K": K, "us_per_call": round(us, 3),
+                               "gbs": round(alg_bytes(1, N, K, 8) / (us * 1e-6) / 1e9, 1)}
+            del ws8, base
 
-    # ---- 8-bit codes (same shapes, M = 1): 4 device copies of each weight matrix cycled
-    eight_bit = {}
-    for j, (name, N, K) in enumerate(synth.LLAMA8B_LAYER + (synth.LLAMA8B_LM_HEAD,)):
-        w8 = synth.make_weights(N, K, synth.seed_for(6, 0, j), bits=8)
-        base = (torch.from_numpy(w8.w_packed.view(np.int32)).to(dev), torch.from_numpy(w8.scales.view(np.int16)).to(dev),
-                torch.from_numpy(w8.biases.view(np.int16)).to(dev))
-        ws8 = [base] + [tuple(t.clone() for t in base) for _ in range(3)]
-        x8 = torch.from_numpy(synth.make_x(1, K, synth.seed_for(6, 1, j)).view(np.int16)).to(dev)
-        y8 = torch.empty((1, N), dtype=torch.int16, device=dev)
+        # ---- prefill-sized tensor-core GEMM (qmm): M in {256, 2048}, (K, N) in {(4096, 14336), (14336, 4096)},
+        # 4-bit codes (the workload) and 8-bit codes
+        qmm = {}
+        for bits in (4, 8):
+            for (K, N, label) in QMM_SHAPES:
+                w = synth.make_weights(N, K, synth.seed_for(5, 0, 0 if N == 14336 else 1), bits=bits)
+                copies = 4   # 4 x 33 MB (4-bit) of distinct weights > L2 between consecutive launches
+                ws = [(torch.from_numpy(w.w_packed.view(np.int32)).to(dev), torch.from_numpy(w.scales.view(np.int16)).to(dev),
+                       torch.from_numpy(w.biases.view(np.int16)).to(dev)) for _ in range(copies)]
+                for M in QMM_M:
+                    xq = torch.from_numpy(synth.make_x(M, K, synth.seed_for(5, M, 9)).view(np.int16)).to(dev)
+                    yq = torch.empty((M, N), dtype=torch.int16, device=dev)
 
-        def launch8(i, ws8=ws8, x8=x8, y8=y8, N=N, K=K):
-            wt, st_, bt = ws8[i % len(ws8)]
-            rc = lib.aq_matmul_bf16_ex(x8.data_ptr(), wt.data_ptr(), st_.data_ptr(), bt.data_ptr(), y8.data_ptr(),
-                                       1, N, K, 64, 8, aq.AQ_KERNEL_AUTO, aq.AQ_FLAG_PDL, cur.cuda_stream)
-            if rc != aq.AQ_OK:
-                raise aq.AqError(rc, "aq_matmul_bf16_ex")
+                    xws = torch.empty(aq.aq_matmul_workspace_bytes(M, K), dtype=torch.uint8, device=dev)
 
-        us = time_calls(launch8, 8)
-        eight_bit[name] = {"N": N, "K": K, "us_per_call": round(us, 3),
-                           "gbs": round(alg_bytes(1, N, K, 8) / (us * 1e-6) / 1e9, 1)}
-        del ws8, base
+                    def qlaunch(i, ws=ws, xq=xq, yq=yq, M=M, N=N, K=K, bits=bits, xws=xws, use_ws=True):
+                        wt, st, bt = ws[i % copies]
+                        if use_ws:   # x converted once into the workspace (aq_matmul_bf16_ws)
+                            rc = lib.aq_matmul_bf16_ws(xq.data_ptr(), wt.data_ptr(), st.data_ptr(), bt.data_ptr(),
+                                                       yq.data_ptr(), M, N, K, 64, bits, xws.data_ptr(), xws.numel(),
+                                                       cur.cuda_stream)
+                        else:
+                            rc = lib.aq_matmul_bf16_ex(xq.data_ptr(), wt.data_ptr(), st.data_ptr(), bt.data_ptr(),
+                                                       yq.data_ptr(), M, N, K, 64, bits, aq.AQ_KERNEL_AUTO, 0,
+                                                       cur.cuda_stream)
+                        if rc != aq.AQ_OK:
+                            raise aq.AqError(rc, "qmm call")
 
-    # ---- prefill-sized tensor-core GEMM (qmm): M in {256, 2048}, (K, N) in {(4096, 14336), (14336, 4096)},
-    # 4-bit codes (the workload) and 8-bit codes
-    qmm = {}
-    for bits in (4, 8):
-        for (K, N, label) in QMM_SHAPES:
-            w = synth.make_weights(N, K, synth.seed_for(5, 0, 0 if N == 14336 else 1), bits=bits)
-            copies = 4   # 4 x 33 MB (4-bit) of distinct weights > L2 between consecutive launches
-            ws = [(torch.from_numpy(w.w_packed.view(np.int32)).to(dev), torch.from_numpy(w.scales.view(np.int16)).to(dev),
-                   torch.from_numpy(w.biases.view(np.int16)).to(dev)) for _ in range(copies)]
-            for M in QMM_M:
-                xq = torch.from_numpy(synth.make_x(M, K, synth.seed_for(5, M, 9)).view(np.int16)).to(dev)
-                yq = torch.empty((M, N), dtype=torch.int16, device=dev)
+                    def time_q(use_ws, reps=10):
+                        for i in range(3):
+                            qlaunch(i, use_ws=use_ws)
+                        torch.cuda.synchronize(dev)
+                        e0.record(cur)
+                        for i in range(reps):
+                            qlaunch(i, use_ws=use_ws)
+                        e1.record(cur)
+                        e1.synchronize()
+                        return e0.elapsed_time(e1) * 1e3 / reps
 
-                xws = torch.empty(aq.aq_matmul_workspace_bytes(M, K), dtype=torch.uint8, device=dev)
+                    us = time_q(True)
+                    us_plain = time_q(False)
+                    tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
+                    key = f"M{M}_K{K}_N{N}" + ("" if bits == 4 else "_8bit")
+                    qmm[key] = {"us_per_call": round(us, 2), "tflops": round(tf, 1),
+                                "frac_of_bf16_burst": round(tf / bf16_peak, 4),
+                                "frac_of_bf16_sustained": round(tf / bf16_sus, 4),
+                                "without_workspace_us": round(us_plain, 2),
+                                "without_workspace_tflops": round(2.0 * M * N * K / (us_plain * 1e-6) / 1e12, 1)}
+                    del xws
+                del ws
 
-                def qlaunch(i, ws=ws, xq=xq, yq=yq, M=M, N=N, K=K, bits=bits, xws=xws, use_ws=True):
-                    wt, st, bt = ws[i % copies]
-                    if use_ws:   # x converted once into the workspace (aq_matmul_bf16_ws)
-                        rc = lib.aq_matmul_bf16_ws(xq.data_ptr(), wt.data_ptr(), st.data_ptr(), bt.data_ptr(),
-                                                   yq.data_ptr(), M, N, K, 64, bits, xws.data_ptr(), xws.numel(),
-                                                   cur.cuda_stream)
-                    else:
-                        rc = lib.aq_matmul_bf16_ex(xq.data_ptr(), wt.data_ptr(), st.data_ptr(), bt.data_ptr(),
-                                                   yq.data_ptr(), M, N, K, 64, bits, aq.AQ_KERNEL_AUTO, 0,
-                                                   cur.cuda_stream)
-                    if rc != aq.AQ_OK:
-                        raise aq.AqError(rc, "qmm call")
+        # ---- NVFP4 weights (E2M1 codes, E4M3 scale per 16, fp32 tensor scale), M = 1, the step's shapes:
+        # 4 device copies of each matrix cycled (0.5625 B per weight, as the affine 4-bit format)
+        nvfp4 = {}
+        for j, (name, N, K) in enumerate(synth.LLAMA8B_LAYER + (synth.LLAMA8B_LM_HEAD,)):
+            wn = synth.make_nvfp4_weights(N, K, synth.seed_for(7, 0, j))
+            base = (torch.from_numpy(wn.w_packed.view(np.int32)).to(dev), torch.from_numpy(wn.scales).to(dev))
+            wsn = [base] + [tuple(t.clone() for t in base) for _ in range(3)]
+            xn = torch.from_numpy(synth.make_x(1, K, synth.seed_for(7, 1, j)).view(np.int16)).to(dev)
+            yn = torch.empty((1, N), dtype=torch.int16, device=dev)
 
-                def time_q(use_ws, reps=10):
-                    for i in range(3):
-                        qlaunch(i, use_ws=use_ws)
-                    torch.cuda.synchronize(dev)
-                    e0.record(cur)
-                    for i in range(reps):
-                        qlaunch(i, use_ws=use_ws)
-                    e1.record(cur)
-                    e1.synchronize()
-                    return e0.elapsed_time(e1) * 1e3 / reps
+            def launchn(i, wsn=wsn, xn=xn, yn=yn, N=N, K=K, g=wn.global_scale):
+                wt, st_ = wsn[i % len(wsn)]
+                rc = lib.aq_matmul_nvfp4_bf16(xn.data_ptr(), wt.data_ptr(), st_.data_ptr(), g, yn.data_ptr(), 1, N, K,
+                                              aq.AQ_FLAG_PDL, cur.cuda_stream)
+                if rc != aq.AQ_OK:
+                    raise aq.AqError(rc, "aq_matmul_nvfp4_bf16")
 
-                us = time_q(True)
-                us_plain = time_q(False)
-                tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
-                key = f"M{M}_K{K}_N{N}" + ("" if bits == 4 else "_8bit")
-                qmm[key] = {"us_per_call": round(us, 2), "tflops": round(tf, 1),
-                            "frac_of_bf16_burst": round(tf / bf16_peak, 4),
-                            "frac_of_bf16_sustained": round(tf / bf16_sus, 4),
-                            "without_workspace_us": round(us_plain, 2),
-                            "without_workspace_tflops": round(2.0 * M * N * K / (us_plain * 1e-6) / 1e12, 1)}
-                del xws
-            del ws
+            us = time_calls(launchn, 8)
+            nvfp4[name] = {"N": N, "K": K, "us_per_call": round(us, 3),
+                           "gbs": round(alg_bytes(1, N, K) / (us * 1e-6) / 1e9, 1)}
+            del wsn, base
 
-    # ---- NVFP4 weights (E2M1 codes, E4M3 scale per 16, fp32 tensor scale), M = 1, the step's shapes:
-    # 4 device copies of each matrix cycled (0.5625 B per weight, as the affine 4-bit format)
-    nvfp4 = {}
-    for j, (name, N, K) in enumerate(synth.LLAMA8B_LAYER + (synth.LLAMA8B_LM_HEAD,)):
-        wn = synth.make_nvfp4_weights(N, K, synth.seed_for(7, 0, j))
-        base = (torch.from_numpy(wn.w_packed.view(np.int32)).to(dev), torch.from_numpy(wn.scales).to(dev))
-        wsn = [base] + [tuple(t.clone() for t in base) for _ in range(3)]
-        xn = torch.from_numpy(synth.make_x(1, K, synth.seed_for(7, 1, j)).view(np.int16)).to(dev)
-        yn = torch.empty((1, N), dtype=torch.int16, device=dev)
+        # ---- MoE prefill (expert-indexed matmul): Mixtral-8x7B-shaped experts, 2048 tokens routed
+        # top-2 over 8 experts (4096 rows), one call = plan + row gather + tensor-core matmul
+        moe = {}
+        T_moe = 2048
+        lhs, rhs = synth.make_routing(T_moe, synth.MIXTRAL_EXPERTS, synth.MIXTRAL_TOP_K, synth.seed_for(6, 0, 9))
+        lt = torch.from_numpy(lhs).to(dev)
+        rt = torch.from_numpy(rhs).to(dev)
+        R_moe = int(lhs.size)
+        for j, (name, N, K) in enumerate(synth.MIXTRAL_EXPERT_MATS):
+            ew = synth.ExpertWeights(synth.MIXTRAL_EXPERTS, N, K, synth.seed_for(6, 0, 16 * j))
+            wt = torch.from_numpy(ew.w_packed.view(np.int32)).to(dev)
+            st = torch.from_numpy(ew.scales.view(np.int16)).to(dev)
+            bt = torch.from_numpy(ew.biases.view(np.int16)).to(dev)
+            xm = torch.from_numpy(synth.make_x(T_moe, K, synth.seed_for(6, 0, 8)).view(np.int16)).to(dev)
+            ym = torch.empty((R_moe, N), dtype=torch.int16, device=dev)
+            nws = aq.aq_gather_qmm_workspace_bytes(R_moe, K, synth.MIXTRAL_EXPERTS)
+            wsm = torch.empty(nws, dtype=torch.uint8, device=dev)
 
-        def launchn(i, wsn=wsn, xn=xn, yn=yn, N=N, K=K, g=wn.global_scale):
-            wt, st_ = wsn[i % len(wsn)]
-            rc = lib.aq_matmul_nvfp4_bf16(xn.data_ptr(), wt.data_ptr(), st_.data_ptr(), g, yn.data_ptr(), 1, N, K,
-                                          aq.AQ_FLAG_PDL, cur.cuda_stream)
-            if rc != aq.AQ_OK:
-                raise aq.AqError(rc, "aq_matmul_nvfp4_bf16")
+            def mlaunch(i, wt=wt, st=st, bt=bt, xm=xm, ym=ym, wsm=wsm, N=N, K=K):
+                rc = lib.aq_gather_qmm_bf16(xm.data_ptr(), wt.data_ptr(), st.data_ptr(), bt.data_ptr(), lt.data_ptr(),
+                                            rt.data_ptr(), ym.data_ptr(), R_moe, T_moe, N, K, synth.MIXTRAL_EXPERTS, 64,
+                                            4, wsm.data_ptr(), wsm.numel(), cur.cuda_stream)
+                if rc != aq.AQ_OK:
+                    raise aq.AqError(rc, "aq_gather_qmm_bf16")
 
-        us = time_calls(launchn, 8)
-        nvfp4[name] = {"N": N, "K": K, "us_per_call": round(us, 3),
-                       "gbs": round(alg_bytes(1, N, K) / (us * 1e-6) / 1e9, 1)}
-        del wsn, base
+            us = time_calls(mlaunch, 4)
+            tf = 2.0 * R_moe * N * K / (us * 1e-6) / 1e12
+            moe[name] = {"tokens": T_moe, "experts": synth.MIXTRAL_EXPERTS, "top_k": synth.MIXTRAL_TOP_K, "rows": R_moe,
+                         "N": N, "K": K, "us_per_call": round(us, 2), "tflops": round(tf, 1),
+                         "frac_of_bf16_burst": round(tf / bf16_peak, 4)}
+            del wt, st, bt, ew, wsm
+        return per_matrix, small_batch, eight_bit, qmm, nvfp4, moe
 
-    # ---- MoE prefill (expert-indexed matmul): Mixtral-8x7B-shaped experts, 2048 tokens routed
-    # top-2 over 8 experts (4096 rows), one call = plan + row gather + tensor-core matmul
-    moe = {}
-    T_moe = 2048
-    lhs, rhs = synth.make_routing(T_moe, synth.MIXTRAL_EXPERTS, synth.MIXTRAL_TOP_K, synth.seed_for(6, 0, 9))
-    lt = torch.from_numpy(lhs).to(dev)
-    rt = torch.from_numpy(rhs).to(dev)
-    R_moe = int(lhs.size)
-    for j, (name, N, K) in enumerate(synth.MIXTRAL_EXPERT_MATS):
-        ew = synth.ExpertWeights(synth.MIXTRAL_EXPERTS, N, K, synth.seed_for(6, 0, 16 * j))
-        wt = torch.from_numpy(ew.w_packed.view(np.int32)).to(dev)
-        st = torch.from_numpy(ew.scales.view(np.int16)).to(dev)
-        bt = torch.from_numpy(ew.biases.view(np.int16)).to(dev)
-        xm = torch.from_numpy(synth.make_x(T_moe, K, synth.seed_for(6, 0, 8)).view(np.int16)).to(dev)
-        ym = torch.empty((R_moe, N), dtype=torch.int16, device=dev)
-        nws = aq.aq_gather_qmm_workspace_bytes(R_moe, K, synth.MIXTRAL_EXPERTS)
-        wsm = torch.empty(nws, dtype=torch.uint8, device=dev)
-
-        def mlaunch(i, wt=wt, st=st, bt=bt, xm=xm, ym=ym, wsm=wsm, N=N, K=K):
-            rc = lib.aq_gather_qmm_bf16(xm.data_ptr(), wt.data_ptr(), st.data_ptr(), bt.data_ptr(), lt.data_ptr(),
-                                        rt.data_ptr(), ym.data_ptr(), R_moe, T_moe, N, K, synth.MIXTRAL_EXPERTS, 64,
-                                        4, wsm.data_ptr(), wsm.numel(), cur.cuda_stream)
-            if rc != aq.AQ_OK:
-                raise aq.AqError(rc, "aq_gather_qmm_bf16")
-
-        us = time_calls(mlaunch, 4)
-        tf = 2.0 * R_moe * N * K / (us * 1e-6) / 1e12
-        moe[name] = {"tokens": T_moe, "experts": synth.MIXTRAL_EXPERTS, "top_k": synth.MIXTRAL_TOP_K, "rows": R_moe,
-                     "N": N, "K": K, "us_per_call": round(us, 2), "tflops": round(tf, 1),
-                     "frac_of_bf16_burst": round(tf / bf16_peak, 4)}
-        del wt, st, bt, ew, wsm
+    if args.step_only:
+        per_matrix = small_batch = eight_bit = qmm = nvfp4 = moe = None
+    else:
+        per_matrix, small_batch, eight_bit, qmm, nvfp4, moe = side_sections()
 
     # ---- CPU baseline: the oracle on two layers of the same workload, host cores
     cpu = None
@@ -699,7 +725,11 @@ def main():
                      "traffic": traffic if args.step_impl == "chain" else None,
                      "kernel": {"chain": "qmv_chain_kernel (the one launch of the step)",
                                 "graph": "qmv_tma_kernel (every launch of the step)"}[args.step_impl],
-                     "peak_source": f"{peak_src} hbm_gbs (copy)"},
+                     "peak_source": f"{peak_src} hbm_gbs (copy)",
+                     "peak_read": round(read_peak, 1),
+                     "frac_read": round(step_bytes / (ms_step * 1e-3) / 1e9 / read_peak, 4),
+                     "peak_read_source": "aq_read_probe on this device: TMA bulk reads of a 4 GiB buffer, "
+                                         "no arithmetic, best of 5 x 10 launches"},
         "e2e": {"value": round(gbs_e2e, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(ms_e2e, 5)},
         "gpu_launches": args.steps * (1 if args.step_impl == "chain" else len(launches)),
@@ -713,6 +743,9 @@ def main():
         "moe_prefill": moe,
         "qmm": qmm,
     }
+    for k in ("per_matrix", "small_batch", "eight_bit", "nvfp4", "moe_prefill", "qmm"):
+        if line[k] is None:
+            del line[k]
     if cpu:
         line["cpu_baseline"] = cpu
     if rank == 0:

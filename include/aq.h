@@ -171,7 +171,7 @@ typedef struct aq_matmul_desc {
     const void *biases;       /* bf16 [N, K/64], device */
     void *y;                  /* bf16 [M, N], device, written */
     int64_t M, N, K;
-    int64_t flags;            /* 0 or AQ_CHAIN_INDEPENDENT */
+    int64_t flags;            /* 0, AQ_CHAIN_INDEPENDENT, AQ_CHAIN_DEBUG_SKIP_COPY (test hook) */
 } aq_matmul_desc;
 
 enum {
@@ -180,7 +180,13 @@ enum {
      * dependency).  It is ordered after whatever the previous matmul waited
      * for, but not after the previous matmul itself, so the two overlap.  A
      * run of matmuls on the same x buffer with this flag loads x once. */
-    AQ_CHAIN_INDEPENDENT = 1
+    AQ_CHAIN_INDEPENDENT = 1,
+    /* Test hook for the failure path of the chain's bounded waits: the first
+     * CTA's producer leaves out the first copy of this matmul's weights, so
+     * waits in the kernel expire (after 20 ms instead of 2 s), a timeout is
+     * recorded in the device status word (read it with
+     * aq_read_device_status()) and the outputs of the run are not valid. */
+    AQ_CHAIN_DEBUG_SKIP_COPY = 0x40000000
 };
 
 /* Filled by aq_chain_prepare; owned by the caller, read by aq_chain_run. */
@@ -340,6 +346,20 @@ const char *aq_last_cuda_error(void);
  * synchronization or copy failed.
  * A debugging call: it synchronizes the host with the stream. */
 aq_status aq_read_device_status(void *stream);
+
+/*
+ * Measurement probe, not an operation of the pages (they have no counterpart;
+ * their roofline is bytes per token over the memory bandwidth, "epic: CUDA
+ * (MLX backend) prefill and decode acceleration program", Diagnosis).  Reads
+ * floor(bytes / 16384) * 16384 bytes of `buf` (device, 16-byte aligned,
+ * bytes >= 16384) once, with the same TMA bulk copies into shared memory that
+ * the weight-streaming kernels use and no arithmetic: one persistent CTA per
+ * SM, twelve 16 KB copies in flight each.  Time it on `stream` to get the
+ * device's read-only streaming rate, the ceiling of a kernel that only reads.
+ * Asynchronous; allocates nothing; writes no memory.  AQ_ERR_INVALID_ARG for a
+ * null or too small buffer, AQ_ERR_ALIGNMENT, AQ_ERR_CUDA.
+ */
+aq_status aq_read_probe(const void *buf, size_t bytes, void *stream);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int aq_version(void);

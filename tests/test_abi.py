@@ -225,3 +225,10 @@ def test_ws_variant_rejects_like_the_plain_call(args):
     ws = aq.aq_matmul_bf16_ws(p["x"], p["w"], p["s"], p["b"], p["y"], p["M"], p["N"], p["K"], p["group_size"],
                               p["bits"], A, 1 << 20, None)
     assert plain != aq.AQ_OK and ws == plain
+
+
+def test_read_probe_validation():
+    """The read probe checks its arguments before any CUDA call."""
+    assert aq.aq_read_probe(None, 1 << 20, None) == aq.AQ_ERR_INVALID_ARG
+    assert aq.aq_read_probe(0x10000, 16383, None) == aq.AQ_ERR_INVALID_ARG
+    assert aq.aq_read_probe(0x10008, 1 << 20, None) == aq.AQ_ERR_ALIGNMENT

@@ -192,3 +192,32 @@ def test_chain_longer_than_the_shared_memory_record_cache(dev):
         _, ref = oracle.matmul(xh, w.w_packed, w.scales, w.biases, 1, w.N, K)
         assert_parity(from_dev_bf16(y), ref, what=f"matmul {i}")
         assert torch.equal(y, aq.matmul(xin, wt, st, bt)), f"matmul {i}"
+
+
+def test_chain_bounded_wait_timeout_reports_status(dev):
+    """A matmul flagged with the chain's test hook loses its first copy in the
+    first CTA: that CTA's wait expires and it stops, the other CTAs' waits for
+    its completion count expire too, the host reads AQ_ERR_TIMEOUT, and a
+    normal run of the same chain right after matches the oracle."""
+    import torch
+    shapes = [(1, 4096, 4096), (1, 1024, 4096), (1, 14336, 4096), (1, 4096, 14336)]
+    mats = [_mat(dev, M, N, K, 80 + i) for i, (M, N, K) in enumerate(shapes)]
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def descs(hook):
+        return (aq.MatmulDesc * len(mats))(*[
+            aq.MatmulDesc(t[0].data_ptr(), t[1].data_ptr(), t[2].data_ptr(), t[3].data_ptr(), t[4].data_ptr(), M, N,
+                          K, aq.AQ_CHAIN_DEBUG_SKIP_COPY if (hook and i == 1) else 0)
+            for i, ((x, w, t), (M, N, K)) in enumerate(zip(mats, shapes))])
+
+    nbytes = aq.aq_chain_workspace_bytes(len(mats))
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    for hook in (True, False):
+        plan = aq.ChainPlan()
+        assert aq.aq_chain_prepare(descs(hook), len(mats), 64, 4, ws.data_ptr(), nbytes, plan) == aq.AQ_OK
+        assert aq.aq_chain_run(plan, stream) == aq.AQ_OK
+        torch.cuda.synchronize()
+        assert aq.aq_read_device_status(stream) == (aq.AQ_ERR_TIMEOUT if hook else aq.AQ_OK)
+    for (x, w, t), (M, N, K) in zip(mats, shapes):
+        _, ref = oracle.matmul(x, w.w_packed, w.scales, w.biases, M, N, K)
+        assert_parity(from_dev_bf16(t[4]), ref, what=f"chain after timeout M={M} N={N} K={K}")

@@ -185,3 +185,21 @@ def test_output_beyond_2_31_elements(dev):
     ye, yb = oracle.matmul_sampled(x, w.w_packed, w.scales, w.biases, M, N, K, im, inn)
     rms = float(np.sqrt(np.mean(ye * ye)))
     assert_parity(got, yb, rms=rms, what=f"qmm sampled M={M} N={N} K={K} (y beyond 2^31 elements)")
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 512, 1024), (256, 512, 4096)])   # one tile; split K over a cluster
+def test_qmm_bounded_wait_timeout_reports_status(dev, M, N, K):
+    """The test hook makes the first CTA's producer leave out its first copy:
+    the converters' bounded wait expires, the kernel records a timeout (the
+    other CTAs of a split-K cluster still meet it at the cluster barriers),
+    the host reads AQ_ERR_TIMEOUT, and a normal call right after is correct."""
+    import torch
+    w = synth.make_weights(N, K, 12)
+    x = synth.make_x(M, K, 12)
+    xt, wt, st, bt = upload(x, w, dev)
+    stream = torch.cuda.current_stream().cuda_stream
+    assert aq.aq_read_device_status(stream) == aq.AQ_OK
+    aq.matmul(xt, wt, st, bt, kernel="qmm", flags=aq.AQ_FLAG_DEBUG_SKIP_COPY)
+    assert aq.aq_read_device_status(stream) == aq.AQ_ERR_TIMEOUT
+    assert aq.aq_read_device_status(stream) == aq.AQ_OK          # cleared by the read
+    check_full(dev, M, N, K, 12)

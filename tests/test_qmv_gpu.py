@@ -277,3 +277,16 @@ def test_eight_bit_rejected_where_unsupported(dev):
     with pytest.raises(aq.AqError):
         aq.matmul(xt[:1].contiguous(), wt, st_off, bt, bits=8)
     torch.cuda.synchronize()
+
+
+def test_read_probe_streams_a_buffer(dev):
+    """The read-only stream probe reads a buffer (a ragged number of chunks per
+    SM, plus a tail shorter than a chunk that it leaves out) and leaves the
+    device status clean."""
+    import torch
+    buf = torch.zeros((64 << 20) + 5 * 16384 + 100, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream().cuda_stream
+    for _ in range(3):
+        assert aq.aq_read_probe(buf.data_ptr(), buf.numel(), stream) == aq.AQ_OK
+    assert aq.aq_read_device_status(stream) == aq.AQ_OK
+    assert int(buf.sum()) == 0
