@@ -144,23 +144,25 @@ aq_status matmul_impl(const void *x, const uint32_t *w_packed, const void *scale
     }
     if (bits == 8) {
         // 8-bit codes have no general decode kernel: the TMA-fed one, in launches
-        // of 8 rows of x
+        // of up to 16 rows of x
         st = AQ_OK;
-        return tma_rows(8, &st) ? st : AQ_ERR_UNSUPPORTED;
+        return tma_rows(kQmvMaxRows, &st) ? st : AQ_ERR_UNSUPPORTED;
     }
-    if (M <= 8 && kernel != AQ_KERNEL_QMM) {
+    if (M <= kQmvMaxRows && kernel != AQ_KERNEL_QMM) {
         a.M = M;
-        // an explicit AQ_KERNEL_QMV takes the TMA-fed kernel wherever it applies
+        // an explicit AQ_KERNEL_QMV takes the TMA-fed kernel wherever it applies; up
+        // to 16 rows of x stream W once
         if (aq::qmv_tma_supported(a) &&
             (kernel == AQ_KERNEL_QMV || a.debug_skip_copy || aq::qmv_tma_preferred(a))) {
             st = AQ_OK;
             if (tma_rows(M, &st)) return st;
         }
     }
-    if (M > 8 && M <= kQmvMaxRows && kernel == AQ_KERNEL_AUTO && !a.debug_skip_copy && many_tiles(N)) {
-        // 9..16 rows over a matrix with many tiles per SM (an lm_head): two launches of
-        // half the rows on the TMA kernel stream W twice but still beat one launch of the
-        // general kernel (128256 x 4096 at M = 16: 2 x 89 us against 233 us)
+    if (M > 8 && M <= kQmvMaxRows && kernel == AQ_KERNEL_AUTO && many_tiles(N)) {
+        // 9..16 rows whose x needs K passes (16 rows of K = 4096: 128 KB), over a matrix
+        // with many tiles per SM (an lm_head): two launches of at most 8 rows, each x in
+        // one pass, beat one launch whose every pass deposits partial sums (128256 x
+        // 4096 at M = 16: 2 x 60 us against 204 us) and the general kernel
         const int64_t rows = (M + 1) / 2;
         st = AQ_OK;
         if (tma_rows(rows, &st)) return st;

@@ -101,6 +101,14 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
+// Bounded wait until *p >= want (GPU scope, acquire); false on timeout or abort.
+__device__ __forceinline__ bool wait_count(const int *p, int want, uint64_t timeout_ns, const volatile int *abort_flag) {
+    const uint64_t dl = global_timer() + timeout_ns;
+    while (ld_acquire_gpu(p) < want) {
+        if (*abort_flag || global_timer() > dl) return false;
+    }
+    return true;
+}
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
 }
@@ -118,19 +126,6 @@ __device__ __forceinline__ void acquire_record_maps(const ChainRec *r) {
     acquire_tensormap(&r->ts);
     acquire_tensormap(&r->tb);
 }
-
-#ifdef AQ_V_TRACE
-// timing trace of a launch: [cta][matmul][6] global-timer stamps (working instrument)
-__device__ unsigned long long *g_chain_trace;
-#define CHAIN_TRACE(ev, jm)                                                                                  \
-    do {                                                                                                     \
-        if (g_chain_trace) g_chain_trace[((size_t)blockIdx.x * count + (jm)) * 6 + (ev)] = global_timer(); \
-    } while (0)
-#else
-#define CHAIN_TRACE(ev, jm) \
-    do {                    \
-    } while (0)
-#endif
 
 // The scalar part of a record (three 16-byte vectors).
 struct RecInfo {
@@ -245,7 +240,6 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
                             ok = false;
                             break;
                         }
-                        if (tile == first && kb == 0) CHAIN_TRACE(0, jm);
                         if ((cur.flags & AQ_CHAIN_DEBUG_SKIP_COPY) && cta == 0 && tile == first && kb == 0) {
                             ++issued;   // test hook: this stage never arrives
                             continue;
@@ -291,14 +285,10 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
                 if (lane == 0) {
                     // the previous group's tiles: its last matmul's tile_base counts the ones before it
                     const int want = prev.tile_base + prev.T;
-                    const uint64_t dl = global_timer() + timeout_ns;
-                    while (ok && ld_acquire_gpu(done + prev.group) < want) {
-                        if (*abort_flag || global_timer() > dl) {
-                            set_abort();
-                            ok = false;
-                        }
+                    if (ok && !wait_count(done + prev.group, want, timeout_ns, abort_flag)) {
+                        set_abort();
+                        ok = false;
                     }
-                    CHAIN_TRACE(1, jm);
                     mbar_arrive(bar_dep);
                 }
                 ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
@@ -306,7 +296,6 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
             const int first = (cta - cur.tile_base % ncta + ncta) % ncta;
             for (int tile = first; tile < cur.T && ok; tile += ncta, ++pending, ++tcount)
                 ok = reduce_tile<ONE_ROW>(tc, tcount, tile, cur.M, cur.N, cur.y, lane, timeout_ns, abort_flag);
-            if (lane == 0 && first < cur.T) CHAIN_TRACE(4, jm);
             const bool group_ends = jm + 1 == count || !(nxt.flags & AQ_CHAIN_INDEPENDENT);
             if (ok && group_ends && pending > 0 && lane == 0) {
                 // every lane's y stores precede this (reduce_tile ends with __syncwarp);
@@ -356,7 +345,6 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
                 const int KB = (K + Gm::kStageCodes - 1) / Gm::kStageCodes;
                 // ---- this warp's slice of x: L2 loads, fp16 fragments, group sums and scale
                 if (new_x && ok) stage_x_warp<BITS, ONE_ROW>(xs, cur.x, M, K, K, warp, lane, inv);
-                if (warp == 0 && lane == 0) CHAIN_TRACE(2, jm);
 
                 ConsumerThread ct;
                 consumer_init<BITS, ONE_ROW>(ct, warp, lane, xs, M, K);
@@ -374,11 +362,9 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
                             consume_stage<BITS, ONE_ROW>(s_base + (uint32_t)(slot * kStageBytes), kb, ct, acc);
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
-                        if (warp == 0 && lane == 0 && tile == first && kb == 0) CHAIN_TRACE(3, jm);
                     }
                     if (!ok) break;
-                    if (warp == 0 && lane == 0 && tile + ncta >= T) CHAIN_TRACE(5, jm);
-                    ok = deposit_tile<ONE_ROW>(tc, acc, tcount, M, warp, lane, mma_row<BITS>(lane), inv, timeout_ns,
+                    ok = deposit_tile<ONE_ROW>(tc, acc, tcount, M, warp, lane, lane >> 2, inv, timeout_ns,
                                                abort_flag);
                     ++tcount;
                 }
@@ -390,15 +376,6 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
 }
 
 // ---------------------------------------------------------------- host side
-#ifdef AQ_V_TRACE
-}  // namespace
-}  // namespace aq
-extern "C" int aq_chain_trace_set(void *p) {
-    return (int)cudaMemcpyToSymbol(aq::g_chain_trace, &p, sizeof p);
-}
-namespace aq {
-namespace {
-#endif
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -557,7 +534,7 @@ cudaError_t chain_run(const aq_chain_plan *plan, uint64_t timeout_ns, int *statu
         g_attr_done[ki][dev].store(1, std::memory_order_release);
     }
     int *done = reinterpret_cast<int *>(static_cast<uint8_t *>(plan->workspace) + records_bytes(count));
-    e = cudaMemsetAsync(done, 0, (size_t)count * sizeof(int), stream);
+    e = cudaMemsetAsync(done, 0, counters_bytes(count), stream);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)sms);   // one CTA per SM, all resident (they wait on one another)

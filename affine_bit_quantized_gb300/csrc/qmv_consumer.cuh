@@ -64,7 +64,8 @@ struct Geo {
 // the same numbers at run time (host and device)
 __host__ __device__ constexpr int stage_codes(int bits) { return bits == 4 ? 2048 : 1024; }
 __host__ __device__ constexpr int stage_groups(int bits) { return stage_codes(bits) / 64; }
-constexpr int kMaxM = 8;                                   // rows of x these kernels take
+constexpr int kMaxM = 8;                                   // rows of x per block of 8 MMA columns
+constexpr int kMaxRows = 16;                               // rows of x with two blocks (single-matmul kernel)
 constexpr int kMaxXBytes = 32768;                          // staging room for x (M * K * 2, K in whole stages)
 constexpr int kXInfoBytes = 96;                            // int row_max[2][8], float inv_scale[8]
 // Row stride of x staged in natural order (the NVFP4 kernel): 2K bytes, plus a
@@ -157,10 +158,11 @@ __device__ __forceinline__ uint4 ldg_cg_v4(const void *p) {
 // own partial sums (write_partials), so warps need not agree on e.  Sets
 // inv[c] = 2^-e of the x row of MMA column 2j + c (j = lane % 4; row 0 when
 // ONE_ROW).  Only the calling warp takes part.  M * KB * (stage codes) * 2
-// <= the region's room, K % 64 == 0.
-template <int BITS, bool ONE_ROW>
+// <= XROOM (the region's room), K % 64 == 0.
+template <int BITS, bool ONE_ROW, int XROOM = kMaxXBytes, int NB = 1>
 __device__ __forceinline__ void stage_x_warp(const XStage &xs, const __nv_bfloat16 *xg, int M_, int K, int ldx,
-                                             int warp, int lane, float (&inv)[2]) {
+                                             int warp, int lane, float (&inv)[2 * NB]) {
+    constexpr int MR = ONE_ROW ? 1 : 8 * NB;   // rows of x staged at most
     using Gm = Geo<BITS>;
     const int M = ONE_ROW ? 1 : M_;
     const int nblk = K / Gm::kWarpCodes;                          // column blocks of K
@@ -171,7 +173,7 @@ __device__ __forceinline__ void stage_x_warp(const XStage &xs, const __nv_bfloat
     const int words = M * wpr;
     const uint32_t xq = xs.xq + (uint32_t)(warp * xs.wq), xsum = xs.xsum + (uint32_t)(warp * xs.ws);
     const int xrb = xw_row_bytes(M, KB, BITS), xsrb = xsw_row_bytes(M, KB, BITS);
-    constexpr int NW = kMaxXBytes / 16 / kConsumerThreads;         // words per lane at most (4)
+    constexpr int NW = XROOM / 16 / kConsumerThreads;              // words per lane at most
     uint4 v[NW];
     int row[NW];
     // all loads first (one L2 round trip), then the row maxima
@@ -187,9 +189,9 @@ __device__ __forceinline__ void stage_x_warp(const XStage &xs, const __nv_bfloat
             v[u] = ldg_cg_v4(xg + (size_t)m * ldx + (size_t)(kb * kConsumerWarps + warp) * Gm::kWarpCodes + iw * 8);
         }
     }
-    int e[ONE_ROW ? 1 : kMaxM];
+    int e[MR];
 #pragma unroll
-    for (int m = 0; m < (ONE_ROW ? 1 : kMaxM); ++m) {
+    for (int m = 0; m < MR; ++m) {
         int mx = 0;
 #pragma unroll
         for (int u = 0; u < NW; ++u) {
@@ -212,7 +214,7 @@ __device__ __forceinline__ void stage_x_warp(const XStage &xs, const __nv_bfloat
         int em = e[0];
         if (!ONE_ROW) {
 #pragma unroll
-            for (int mm = 1; mm < kMaxM; ++mm) em = m == mm ? e[mm] : em;
+            for (int mm = 1; mm < MR; ++mm) em = m == mm ? e[mm] : em;
         }
         const int r = wi - m * wpr, kb = r / WPS, iw = r - kb * WPS;
         if (wi < words) {
@@ -259,15 +261,19 @@ __device__ __forceinline__ void stage_x_warp(const XStage &xs, const __nv_bfloat
         inv[0] = inv[1] = pow2f(-e[0]);
     } else {
         const int j = lane & 3;
-        const int r0 = 2 * j < M ? 2 * j : M - 1, r1 = 2 * j + 1 < M ? 2 * j + 1 : M - 1;
-        int e0 = e[0], e1 = e[0];
 #pragma unroll
-        for (int mm = 1; mm < kMaxM; ++mm) {
-            e0 = r0 == mm ? e[mm] : e0;
-            e1 = r1 == mm ? e[mm] : e1;
+        for (int nb = 0; nb < NB; ++nb) {
+            const int r0 = 8 * nb + 2 * j < M ? 8 * nb + 2 * j : M - 1;
+            const int r1 = 8 * nb + 2 * j + 1 < M ? 8 * nb + 2 * j + 1 : M - 1;
+            int e0 = e[0], e1 = e[0];
+#pragma unroll
+            for (int mm = 1; mm < MR; ++mm) {
+                e0 = r0 == mm ? e[mm] : e0;
+                e1 = r1 == mm ? e[mm] : e1;
+            }
+            inv[2 * nb] = pow2f(-e0);
+            inv[2 * nb + 1] = pow2f(-e1);
         }
-        inv[0] = pow2f(-e0);
-        inv[1] = pow2f(-e1);
     }
     __syncwarp();   // the region is written before any lane's ldmatrix reads it
 }
@@ -278,26 +284,16 @@ struct ConsumerThread {
     uint32_t sb;        // offset in a scale box of row lane/4's scales of groups 2w, 2w+1 (rows +8 at +512)
     uint32_t xq;        // ldmatrix row address of this warp's first quad in stage 0
     uint32_t xs0, xs1;  // (Xs, X') of this warp's first group in stage 0, x rows of columns 2j and 2j+1
+    uint32_t xq1;       // with a second block of 8 columns (x rows 8..15): its ldmatrix row address
+    uint32_t xs2, xs3;  // and its (Xs, X') addresses, x rows 8 + 2j and 8 + 2j + 1
 };
 
 // K: the codes of the staged x (the matmul's K, or one K pass).
-// Tile row (within each group of 8 rows) that MMA row lane/4 stands for.
-#ifdef AQ_V_ROWPERM
-template <int BITS>
-__device__ __forceinline__ int mma_row(int lane) {
-    const int g = lane >> 2;
-    return BITS == 4 ? ((g & 3) << 1) | (g >> 2) : (g >> 1) | ((g & 1) << 2);
-}
-#else
-template <int BITS>
-__device__ __forceinline__ int mma_row(int lane) { return lane >> 2; }
-#endif
-
-template <int BITS, bool ONE_ROW>
+template <int BITS, bool ONE_ROW, int NB = 1>
 __device__ __forceinline__ void consumer_init(ConsumerThread &c, int warp, int lane, const XStage &xs, int M_, int K) {
     const int M = ONE_ROW ? 1 : M_;
     using Gm = Geo<BITS>;
-    const int gid = mma_row<BITS>(lane), j = lane & 3;
+    const int gid = lane >> 2, j = lane & 3;
     // code boxes use the 128-byte swizzle: 16-byte chunk c of box row r sits at chunk c ^ (r % 8)
     if (BITS == 4) {
         // words 2j, 2j+1 of groups 2w, 2w+1: 8 bytes per group
@@ -322,6 +318,13 @@ __device__ __forceinline__ void consumer_init(ConsumerThread &c, int warp, int l
     const int m0 = 2 * j < M ? 2 * j : M - 1, m1 = 2 * j + 1 < M ? 2 * j + 1 : M - 1;
     c.xs0 = xs.xsum + (uint32_t)(warp * xs.ws + m0 * xsrb);
     c.xs1 = xs.xsum + (uint32_t)(warp * xs.ws + m1 * xsrb);
+    if (NB == 2) {
+        const int xr1 = 8 + (lane & 7) < M ? 8 + (lane & 7) : M - 1;
+        c.xq1 = xs.xq + (uint32_t)(warp * xs.wq + xr1 * xw_row_bytes(M, KB, BITS) + (lane >> 3) * 16);
+        const int m2 = 8 + 2 * j < M ? 8 + 2 * j : M - 1, m3 = 8 + 2 * j + 1 < M ? 8 + 2 * j + 1 : M - 1;
+        c.xs2 = xs.xsum + (uint32_t)(warp * xs.ws + m2 * xsrb);
+        c.xs3 = xs.xsum + (uint32_t)(warp * xs.ws + m3 * xsrb);
+    }
 }
 
 // acc += scale * (D - 1024 X') + bias * Xs for one group: D = d[h] (the MMA
@@ -377,42 +380,37 @@ __device__ __forceinline__ void consume_stage(uint32_t st, int kb, const Consume
     const uint32_t xq = c.xq + (uint32_t)kb * (Gm::kGroupsPerWarp * 128);
     const uint32_t xo = (uint32_t)kb * (Gm::kGroupsPerWarp * 8);
     if (BITS == 4) {
+        // every shared-memory load of the stage first, then the arithmetic
+        uint2 wrs[2][4];
+        uint4 Xs[2][2];
+#pragma unroll
+        for (int gl = 0; gl < 2; ++gl) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) wrs[gl][r] = lds64(st + c.code[gl] + 1024 * r);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) Xs[gl][i] = ldsm_x4(xq + gl * 128 + i * 64);
+        }
 #pragma unroll
         for (int gl = 0; gl < 2; ++gl) {
             uint2 wr[4];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) wr[r] = lds64(st + c.code[gl] + 1024 * r);
+            for (int r = 0; r < 4; ++r) wr[r] = wrs[gl][r];
             float d[2][4];
-#ifdef AQ_V_SPLITACC
-            float d2[2][4];
-#endif
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
-                const uint4 X = ldsm_x4(xq + gl * 128 + i * 64);
+                const uint4 X = Xs[gl][i];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const uint32_t wa = i ? wr[2 * h].y : wr[2 * h].x;
                     const uint32_t wb = i ? wr[2 * h + 1].y : wr[2 * h + 1].x;
                     const uint32_t ta = wa >> 8, tb = wb >> 8;
-#ifdef AQ_V_SPLITACC
-                    float (&dd)[4] = i ? d2[h] : d[h];
-                    mma_f16_16816_zc(dd, lo_pair(wa), lo_pair(wb), hi_pair(wa), hi_pair(wb), X.x, X.y);
-                    mma_f16_16816(dd, lo_pair(ta), lo_pair(tb), hi_pair(ta), hi_pair(tb), X.z, X.w);
-#else
                     if (i == 0)
                         mma_f16_16816_zc(d[h], lo_pair(wa), lo_pair(wb), hi_pair(wa), hi_pair(wb), X.x, X.y);
                     else
                         mma_f16_16816(d[h], lo_pair(wa), lo_pair(wb), hi_pair(wa), hi_pair(wb), X.x, X.y);
                     mma_f16_16816(d[h], lo_pair(ta), lo_pair(tb), hi_pair(ta), hi_pair(tb), X.z, X.w);
-#endif
                 }
             }
-#ifdef AQ_V_SPLITACC
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int r = 0; r < 4; ++r) d[h][r] += d2[h][r];
-#endif
             float sc[4], bi[4];
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
@@ -458,6 +456,103 @@ __device__ __forceinline__ void consume_stage(uint32_t st, int kb, const Consume
     }
 }
 
+// consume_stage for 9..16 rows of x: two blocks of 8 MMA columns (x rows 0..7
+// and 8..15).  Each code pair is extracted once and feeds both blocks' MMAs;
+// acc[nb] holds block nb.
+template <int BITS>
+__device__ __forceinline__ void consume_stage2(uint32_t st, int kb, const ConsumerThread &c, float (&acc)[2][2][4]) {
+    using Gm = Geo<BITS>;
+    uint32_t sw[4], bw[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        sw[r] = lds32(st + kCodesBytes + c.sb + 8 * Gm::kSBRowBytes * r);
+        bw[r] = lds32(st + kCodesBytes + kSBRegion + c.sb + 8 * Gm::kSBRowBytes * r);
+    }
+    const uint32_t xo = (uint32_t)kb * (Gm::kGroupsPerWarp * 8);
+    const uint32_t xq[2] = {c.xq + (uint32_t)kb * (Gm::kGroupsPerWarp * 128),
+                            c.xq1 + (uint32_t)kb * (Gm::kGroupsPerWarp * 128)};
+    const uint32_t xsa[2] = {c.xs0 + xo, c.xs2 + xo}, xsb[2] = {c.xs1 + xo, c.xs3 + xo};
+    if (BITS == 4) {
+#pragma unroll
+        for (int gl = 0; gl < 2; ++gl) {
+            uint2 wr[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) wr[r] = lds64(st + c.code[gl] + 1024 * r);
+            float d[2][2][4];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                uint4 X[2];
+#pragma unroll
+                for (int nb = 0; nb < 2; ++nb) X[nb] = ldsm_x4(xq[nb] + gl * 128 + i * 64);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t wa = i ? wr[2 * h].y : wr[2 * h].x;
+                    const uint32_t wb = i ? wr[2 * h + 1].y : wr[2 * h + 1].x;
+                    const uint32_t ta = wa >> 8, tb = wb >> 8;
+                    const uint32_t a0 = lo_pair(wa), a1 = lo_pair(wb), a2 = hi_pair(wa), a3 = hi_pair(wb);
+                    const uint32_t b0 = lo_pair(ta), b1 = lo_pair(tb), b2 = hi_pair(ta), b3 = hi_pair(tb);
+#pragma unroll
+                    for (int nb = 0; nb < 2; ++nb) {
+                        if (i == 0)
+                            mma_f16_16816_zc(d[nb][h], a0, a1, a2, a3, X[nb].x, X[nb].y);
+                        else
+                            mma_f16_16816(d[nb][h], a0, a1, a2, a3, X[nb].x, X[nb].y);
+                        mma_f16_16816(d[nb][h], b0, b1, b2, b3, X[nb].z, X[nb].w);
+                    }
+                }
+            }
+            float sc[4], bi[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                sc[r] = gl ? bf16hi(sw[r]) : bf16lo(sw[r]);
+                bi[r] = gl ? bf16hi(bw[r]) : bf16lo(bw[r]);
+            }
+#pragma unroll
+            for (int nb = 0; nb < 2; ++nb) fold_group<false>(d[nb], sc, bi, xsa[nb] + gl * 8, xsb[nb] + gl * 8, acc[nb]);
+        }
+    } else {
+        uint4 wr[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) wr[r] = lds128(st + c.code[0] + 1024 * r);
+        float d[2][2][4];
+#pragma unroll
+        for (int sp = 0; sp < 2; ++sp) {
+            uint4 X[2];
+#pragma unroll
+            for (int nb = 0; nb < 2; ++nb) X[nb] = ldsm_x4(xq[nb] + sp * 64);
+#pragma unroll
+            for (int ss = 0; ss < 2; ++ss) {
+                const int s = 2 * sp + ss;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint4 &A = wr[2 * h], &B = wr[2 * h + 1];
+                    const uint32_t wa = s == 0 ? A.x : s == 1 ? A.y : s == 2 ? A.z : A.w;
+                    const uint32_t wb = s == 0 ? B.x : s == 1 ? B.y : s == 2 ? B.z : B.w;
+                    const uint32_t a0 = byte_pair(wa), a1 = byte_pair(wb), a2 = byte_pair(wa >> 8),
+                                   a3 = byte_pair(wb >> 8);
+#pragma unroll
+                    for (int nb = 0; nb < 2; ++nb) {
+                        const uint32_t b0 = ss ? X[nb].z : X[nb].x, b1 = ss ? X[nb].w : X[nb].y;
+                        if (s == 0)
+                            mma_f16_16816_zc(d[nb][h], a0, a1, a2, a3, b0, b1);
+                        else
+                            mma_f16_16816(d[nb][h], a0, a1, a2, a3, b0, b1);
+                    }
+                }
+            }
+        }
+        const int odd = threadIdx.x >> 5 & 1;   // the warp's group is the high half of its scale word
+        float sc[4], bi[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            sc[r] = odd ? bf16hi(sw[r]) : bf16lo(sw[r]);
+            bi[r] = odd ? bf16hi(bw[r]) : bf16lo(bw[r]);
+        }
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb) fold_group<false>(d[nb], sc, bi, xsa[nb], xsb[nb], acc[nb]);
+    }
+}
+
 // This warp's partial sums of a tile, times the x scale 2^-e of their column
 // (exact: a power of two; inv[c] for column 2j + c, j = lane % 4), into rw =
 // its [kRows][M] slice; gid: the tile row (mod 8) of this lane's MMA rows;
@@ -500,10 +595,13 @@ __device__ __forceinline__ void write_partials(float *rw, int M, int lane, int g
 // order and stores y.  The consumers never wait for one another here (a
 // buffer is reused only after the reducer has emptied it), and every sum has
 // a fixed order, so results do not depend on timing.
-template <bool ONE_ROW>
-__host__ __device__ constexpr int red_bufs() { return ONE_ROW ? 4 : 2; }
+// (NB = 2, i.e. 9..16 rows of x: one buffer, whose 32 KB would otherwise crowd out x)
+template <bool ONE_ROW, int NB = 1>
+__host__ __device__ constexpr int red_bufs() { return ONE_ROW ? 4 : (NB == 2 ? 1 : 2); }
 // bytes of the partial-sum buffers: float [bufs][kConsumerWarps][kRows][M]
-__host__ __device__ constexpr int red_bytes(int m) { return (m == 1 ? 4 : 2) * kConsumerWarps * kRows * m * 4; }
+__host__ __device__ constexpr int red_bytes(int m) {
+    return (m == 1 ? 4 : (m > 8 ? 1 : 2)) * kConsumerWarps * kRows * m * 4;
+}
 
 struct TileCtx {
     float *red;            // float [bufs][kConsumerWarps][kRows][M]
@@ -528,6 +626,41 @@ __device__ __forceinline__ bool deposit_tile(const TileCtx &t, float (&acc)[2][4
     return true;
 }
 
+// deposit_tile for two blocks of 8 MMA columns (9..16 rows of x): block nb
+// holds x rows 8nb + 2j + c, unscaled by inv[2nb + c].
+__device__ __forceinline__ bool deposit_tile2(const TileCtx &t, float (&acc)[2][2][4], int tcount, int M, int warp,
+                                              int lane, const float (&inv)[4], uint64_t timeout_ns,
+                                              const volatile int *abort_flag) {
+    constexpr int B = red_bufs<false, 2>();
+    const int b = tcount % B;
+    const int n_out = kRows * M;
+    if (tcount >= B && !mbar_wait_for(t.red_empty + 8 * b, (uint32_t)((tcount / B) - 1) & 1u, timeout_ns, abort_flag))
+        return false;
+    float *rw = t.red + (b * kConsumerWarps + warp) * n_out;
+    const int gid = lane >> 2, j = lane & 3;
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+            const int m = 8 * nb + 2 * j + cc;
+            if (m < M) {
+                const float sc = inv[2 * nb + cc];
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int rr = 0; rr < 2; ++rr)
+                        rw[(16 * h + gid + 8 * rr) * M + m] = acc[nb][h][2 * rr + cc] * sc;
+            }
+        }
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) acc[nb][h][0] = acc[nb][h][1] = acc[nb][h][2] = acc[nb][h][3] = 0.f;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(t.red_full + 8 * b);
+    return true;
+}
+
 // Reducer warp, for the tcount-th tile of this CTA (tile index `tile` of a
 // matrix with N rows): adds the (already unscaled) partials in warp order and
 // stores y rows tile*kRows .. (bf16, round to nearest even).
@@ -535,20 +668,22 @@ __device__ __forceinline__ bool deposit_tile(const TileCtx &t, float (&acc)[2][4
 // When K is walked in several passes (pass `pass` of `passes`), the tile's
 // sums of the passes before the last are kept in yacc (float [kRows][M]):
 // assigned by the first pass, added to by the next ones, in pass order.
-template <bool ONE_ROW>
+template <bool ONE_ROW, int NB = 1>
 __device__ __forceinline__ bool reduce_tile(const TileCtx &t, int tcount, int tile, int M, int N,
                                             __nv_bfloat16 *y, int lane, uint64_t timeout_ns,
                                             const volatile int *abort_flag, float *yacc = nullptr, int pass = 0,
-                                            int passes = 1, float yscale = 1.f) {
-    constexpr int B = red_bufs<ONE_ROW>();
+                                            int passes = 1, float yscale = 1.f, int part = 0, int parts = 1) {
+    constexpr int B = red_bufs<ONE_ROW, NB>();
     const int b = tcount % B;
     const int n_out = kRows * M;
+    // this reducer's share of the outputs: rows [part, part + 1) * kRows / parts of the tile
+    const int o0 = part * (kRows / parts) * M, o1 = o0 + (kRows / parts) * M;
     if (!mbar_wait_for(t.red_full + 8 * b, (uint32_t)(tcount / B) & 1u, timeout_ns, abort_flag)) return false;
     const float *rb = t.red + b * kConsumerWarps * n_out;
     if (!ONE_ROW && (M & 3) == 0) {
         // four outputs (one row of W, four rows of x) per lane and step: 16-byte
         // loads and paired adds, the same warp order as below, so the same sums
-        for (int idx = lane * 4; idx < n_out; idx += 128) {
+        for (int idx = o0 + lane * 4; idx < o1; idx += 128) {
             const float4 f0 = *reinterpret_cast<const float4 *>(rb + idx);
             float2 lo = make_float2(f0.x, f0.y), hi = make_float2(f0.z, f0.w);
 #pragma unroll
@@ -580,7 +715,7 @@ __device__ __forceinline__ bool reduce_tile(const TileCtx &t, int tcount, int ti
     }
     if (!ONE_ROW && (M & 1) == 0) {
         // two outputs per lane and step (8-byte loads, paired adds), same order
-        for (int idx = lane * 2; idx < n_out; idx += 64) {
+        for (int idx = o0 + lane * 2; idx < o1; idx += 64) {
             float2 v = *reinterpret_cast<const float2 *>(rb + idx);
 #pragma unroll
             for (int w = 1; w < kConsumerWarps; ++w) v = add2(v, *reinterpret_cast<const float2 *>(rb + w * n_out + idx));
@@ -599,7 +734,7 @@ __device__ __forceinline__ bool reduce_tile(const TileCtx &t, int tcount, int ti
         if (lane == 0) mbar_arrive(t.red_empty + 8 * b);
         return true;
     }
-    for (int idx = lane; idx < n_out; idx += 32) {
+    for (int idx = o0 + lane; idx < o1; idx += 32) {
         const int row = idx / M, m = idx - row * M;
         const int n = tile * kRows + row;
         float v = rb[idx];

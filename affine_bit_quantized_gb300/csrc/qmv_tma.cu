@@ -51,7 +51,8 @@ namespace {
 using namespace dev;
 using namespace qmv;
 
-constexpr int kThreads = (kConsumerWarps + 2) * 32;   // consumers, TMA producer, reducer
+constexpr int kReducers = 2;   // reducer warps, each summing half the rows of every tile
+constexpr int kThreads = (kConsumerWarps + 1 + kReducers) * 32;   // consumers, TMA producer, reducers
 constexpr int kMaxStages = 4;   // ring depth (36 KB stages); 5 measured no faster
 constexpr int kNumBars = 2 * kMaxStages + 8;   // full[S], empty[S], red_full[4], red_empty[4]
 constexpr int kSmemLimit = 232448;               // dynamic shared memory a CTA may use
@@ -68,10 +69,11 @@ struct Layout {
     int total;       // bytes (excluding the 1024 alignment slack)
 };
 // Kp: codes of K per pass; cap: tiles per batch kept in yacc (0 with one pass)
-__host__ __device__ inline Layout make_layout(int M, int Kp, int cap, int bits) {
+// ns: ring depth (4, or 3 to make room for x of up to 64 KB in one pass)
+__host__ __device__ inline Layout make_layout(int M, int Kp, int cap, int bits, int ns = kMaxStages) {
     Layout L;
     const int xb = x_stage_bytes(M, Kp, bits);
-    L.stages = kMaxStages;   // fits beside the largest rest (x of 32 KB, M = 8)
+    L.stages = ns;
     L.xq_off = L.stages * kStageBytes;
     L.wq = xw_region_bytes(xb, M);
     L.xsum_off = L.xq_off + kConsumerWarps * L.wq;
@@ -93,7 +95,9 @@ constexpr int kMaxSmem = kSmemLimit;
 // MULTI, x is staged once (kbp and cap are unused).
 // skip_copy: test hook; the producer leaves out the first stage's copies, so the
 // consumers' bounded wait on it expires.
-template <int BITS, bool ONE_ROW, bool MULTI>
+// NS: ring depth; 3 leaves room for x of up to 64 KB (one pass for, e.g., 8 rows of K = 4096).
+// NB: blocks of 8 MMA columns, 2 for 9..16 rows of x (every code pair feeds both).
+template <int BITS, bool ONE_ROW, bool MULTI, int NS = kMaxStages, int NB = 1>
 __global__ void __launch_bounds__(kThreads, 1)
 qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
                const __grid_constant__ CUtensorMap tm_b, const __nv_bfloat16 *__restrict__ x,
@@ -106,9 +110,10 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
     if (!MULTI) kbp = KB;
     const int P = MULTI ? (KB + kbp - 1) / kbp : 1;                // K passes
     const int Kp = MULTI ? kbp * Gm::kStageCodes : K;
-    const Layout L = make_layout(M, Kp, MULTI ? cap : 0, BITS);
+    const Layout L = make_layout(M, Kp, MULTI ? cap : 0, BITS, NS);
     const uint32_t s_base = smem_addr(smem);
-    constexpr int NS = kMaxStages;   // compile time: a runtime ring modulus measured 8% slower
+    // NS at compile time: a runtime ring modulus measured 8% slower
+    constexpr int kXRoom = NS == kMaxStages ? kMaxXBytes : 2 * kMaxXBytes;
     const XStage xs = {s_base + (uint32_t)L.xq_off, s_base + (uint32_t)L.xsum_off, L.wq, L.ws};
     float *yacc = reinterpret_cast<float *>(smem + L.yacc_off);
     const uint32_t bar_full = s_base + L.bar_off;          // NS barriers (room for kMaxStages)
@@ -132,9 +137,9 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, kConsumerWarps);
         }
-        for (int p = 0; p < red_bufs<ONE_ROW>(); ++p) {
+        for (int p = 0; p < red_bufs<ONE_ROW, NB>(); ++p) {
             mbar_init(tc.red_full + 8 * p, kConsumerWarps);
-            mbar_init(tc.red_empty + 8 * p, 1);
+            mbar_init(tc.red_empty + 8 * p, kReducers);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -207,24 +212,28 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
             }
         }
         __syncwarp();
-    } else if (warp == kConsumerWarps + 1) {
-        // ------------------------------------------------------------ reducer
-        // Adds the sixteen warps' partials of each tile and stores y (the
+    } else if (warp > kConsumerWarps) {
+        // ------------------------------------------------------------ reducers
+        // Add the sixteen warps' partials of each tile and store y (the
         // consumers deposit a tile only after their griddepcontrol.wait, so y
-        // is written after the preceding kernel).
+        // is written after the preceding kernel).  Reducer r takes rows
+        // [r, r + 1) * 32 / kReducers of every tile, and with K passes it
+        // keeps those rows' sums across the passes.
+        const int r = warp - kConsumerWarps - 1;
         int tcount = 0;
         bool ok = true;
         if (!MULTI) {
             for (int t = 0; ok && t < my_tiles; ++t, ++tcount)
-                ok = reduce_tile<ONE_ROW>(tc, tcount, (int)blockIdx.x + t * (int)gridDim.x, M, N, y, lane,
-                                          timeout_ns, abort_flag);
+                ok = reduce_tile<ONE_ROW, NB>(tc, tcount, (int)blockIdx.x + t * (int)gridDim.x, M, N, y, lane,
+                                              timeout_ns, abort_flag, nullptr, 0, 1, 1.f, r, kReducers);
         } else {
             for (int tb = 0; ok && tb < my_tiles; tb += cap) {
                 const int tb_end = tb + cap < my_tiles ? tb + cap : my_tiles;
                 for (int p = 0; ok && p < P; ++p)
                     for (int t = tb; ok && t < tb_end; ++t, ++tcount)
-                        ok = reduce_tile<ONE_ROW>(tc, tcount, (int)blockIdx.x + t * (int)gridDim.x, M, N, y, lane,
-                                                  timeout_ns, abort_flag, yacc + (t - tb) * kRows * M, p, P);
+                        ok = reduce_tile<ONE_ROW, NB>(tc, tcount, (int)blockIdx.x + t * (int)gridDim.x, M, N, y,
+                                                      lane, timeout_ns, abort_flag, yacc + (t - tb) * kRows * M, p, P,
+                                                      1.f, r, kReducers);
             }
         }
         if (!ok && lane == 0 && !*abort_flag) {
@@ -238,8 +247,8 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
         // return at once and the work is skipped.
         griddep_wait();  // x comes from the preceding kernel; the deadline starts after it
         const uint64_t deadline = global_timer() + timeout_ns;
-        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        float inv[2];
+        float acc[NB][2][4] = {};
+        float inv[2 * NB];
         bool ok = !*abort_flag;
         int item = 0, tcount = 0;
         // one tile over stages [kb0, kb1) of the staged slice of x, then its partials to the reducer
@@ -250,18 +259,28 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                     ok = false;
                     break;
                 }
-                if ((kb - kb0) * kConsumerWarps + warp < nblk)
-                    consume_stage<BITS, ONE_ROW>(s_base + (uint32_t)(slot * kStageBytes), kb - kb0, ct, acc);
+                if ((kb - kb0) * kConsumerWarps + warp < nblk) {
+                    if constexpr (NB == 2)
+                        consume_stage2<BITS>(s_base + (uint32_t)(slot * kStageBytes), kb - kb0, ct, acc);
+                    else
+                        consume_stage<BITS, ONE_ROW>(s_base + (uint32_t)(slot * kStageBytes), kb - kb0, ct, acc[0]);
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
             }
-            if (ok) ok = deposit_tile<ONE_ROW>(tc, acc, tcount, M, warp, lane, mma_row<BITS>(lane), inv, timeout_ns, abort_flag);
+            if (ok) {
+                if constexpr (NB == 2)
+                    ok = deposit_tile2(tc, acc, tcount, M, warp, lane, inv, timeout_ns, abort_flag);
+                else
+                    ok = deposit_tile<ONE_ROW>(tc, acc[0], tcount, M, warp, lane, lane >> 2, inv, timeout_ns,
+                                               abort_flag);
+            }
             ++tcount;
         };
         if (!MULTI) {
-            stage_x_warp<BITS, ONE_ROW>(xs, x, M, K, K, warp, lane, inv);
+            stage_x_warp<BITS, ONE_ROW, kXRoom, NB>(xs, x, M, K, K, warp, lane, inv);
             ConsumerThread ct;
-            consumer_init<BITS, ONE_ROW>(ct, warp, lane, xs, M, K);
+            consumer_init<BITS, ONE_ROW, NB>(ct, warp, lane, xs, M, K);
             for (int t = 0; t < my_tiles; ++t) run_tile(ct, 0, KB, K / Gm::kWarpCodes);
         } else {
             for (int tb = 0; tb < my_tiles; tb += cap) {
@@ -270,9 +289,9 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                     const int k0 = p * Kp, Kpass = K - k0 < Kp ? K - k0 : Kp;
                     const int kb0 = p * kbp, kb1 = kb0 + kbp < KB ? kb0 + kbp : KB;
                     // the pass's slice of x, from L2
-                    stage_x_warp<BITS, ONE_ROW>(xs, x + k0, M, Kpass, K, warp, lane, inv);
+                    stage_x_warp<BITS, ONE_ROW, kXRoom, NB>(xs, x + k0, M, Kpass, K, warp, lane, inv);
                     ConsumerThread ct;
-                    consumer_init<BITS, ONE_ROW>(ct, warp, lane, xs, M, Kpass);
+                    consumer_init<BITS, ONE_ROW, NB>(ct, warp, lane, xs, M, Kpass);
                     for (int t = tb; t < tb_end; ++t) run_tile(ct, kb0, kb1, Kpass / Gm::kWarpCodes);
                 }
             }
@@ -314,7 +333,7 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint6
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sms[kMaxDevices];
-std::atomic<int> g_attr_done[8][kMaxDevices];
+std::atomic<int> g_attr_done[32][kMaxDevices];
 
 }  // namespace
 
@@ -337,17 +356,25 @@ bool encode_codes_3d(CUtensorMap *map, const void *base, uint64_t row_bytes, uin
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() { return encode_fn(); }
 
 bool qmv_tma_supported(const MatmulArgs &a) {
-    return (a.bits == 4 || a.bits == 8) && a.M >= 1 && a.M <= kMaxM && a.K % 512 == 0 && encode_fn() != nullptr &&
+    return (a.bits == 4 || a.bits == 8) && a.M >= 1 && a.M <= kMaxRows && a.K % 512 == 0 && encode_fn() != nullptr &&
            (reinterpret_cast<uintptr_t>(a.scales) & 15) == 0 && (reinterpret_cast<uintptr_t>(a.biases) & 15) == 0;
 }
 
 namespace {
 // stages of K per pass: as many whole stages as keep one pass of x within kMaxXBytes
-int stages_per_pass(int M, int bits) { return std::max(1, kMaxXBytes / 2 / M / stage_codes(bits)); }
+// x within kMaxXBytes is staged beside a 4-stage ring; larger x gets twice the
+// room beside a 3-stage ring, in one pass where it fits (8 rows of K = 4096:
+// lm_head 92 -> 60 us against two passes), else in passes of as many whole
+// stages as fit.
+int ring_stages(int M, int K, int bits) { return x_stage_bytes(M, K, bits) <= kMaxXBytes ? kMaxStages : 3; }
+int x_room(int ns) { return ns == kMaxStages ? kMaxXBytes : 2 * kMaxXBytes; }
+int stages_per_pass(int M, int K, int bits) {
+    return std::max(1, x_room(ring_stages(M, K, bits)) / 2 / M / stage_codes(bits));
+}
 }  // namespace
 
 int qmv_tma_passes(const MatmulArgs &a) {
-    const int SC = stage_codes(a.bits), kbp = stages_per_pass((int)a.M, a.bits);
+    const int SC = stage_codes(a.bits), kbp = stages_per_pass((int)a.M, (int)a.K, a.bits);
     const int KB = (int)((a.K + SC - 1) / SC);
     return (KB + kbp - 1) / kbp;
 }
@@ -376,6 +403,11 @@ cudaError_t device_sms(int *dev, int *sms) {
 // 4096 at M = 2: 5.7 us against 6.2 us).  One row always takes the TMA kernel.
 bool qmv_tma_preferred(const MatmulArgs &a) {
     if (a.M == 1) return true;
+    // 9..16 rows: where x fits one pass.  In K passes every pass of every tile
+    // deposits the partial sums of 16 rows through one buffer (x of 16 rows at
+    // K = 4096 is 128 KB): 128256 x 4096 took 204 us, 4096 x 14336 82 us, against
+    // 2 x 60 us as two launches of 8 rows and 28 us on the general kernel.
+    if (a.M > kMaxM) return qmv_tma_passes(a) == 1;
     int dev = 0, sms = 0;
     if (device_sms(&dev, &sms) != cudaSuccess) return true;
     const int T = (int)((a.N + kRows - 1) / kRows);
@@ -388,29 +420,41 @@ cudaError_t launch_qmv_tma(const MatmulArgs &a) {
     if (e != cudaSuccess) return e;
     const int M = (int)a.M, N = (int)a.N, K = (int)a.K;
     const int SC = stage_codes(a.bits);
-    const int kbp = stages_per_pass(M, a.bits);
+    const int kbp = stages_per_pass(M, K, a.bits);
     const int P = qmv_tma_passes(a);
+    const bool ns3 = ring_stages(M, K, a.bits) == 3;
     const int T = (N + kRows - 1) / kRows;
     const int grid = std::min(T, sms);   // persistent, one CTA per SM
     const int tpc = (T + grid - 1) / grid;
     int cap = 0;   // tiles per batch whose sums stay in shared memory across the passes
     if (P > 1) {
-        const int free_bytes = kSmemLimit - 1024 - make_layout(M, kbp * SC, 0, a.bits).total;
+        const int free_bytes = kSmemLimit - 1024 - make_layout(M, kbp * SC, 0, a.bits, ns3 ? 3 : kMaxStages).total;
         cap = std::min(tpc, free_bytes / (kRows * M * 4));
         if (cap < 1) return cudaErrorInvalidConfiguration;
     }
-    const Layout L = make_layout(M, P > 1 ? kbp * SC : K, cap, a.bits);
+    const Layout L = make_layout(M, P > 1 ? kbp * SC : K, cap, a.bits, ns3 ? 3 : kMaxStages);
     const int smem = L.total + 1024;
     if (smem > kSmemLimit) return cudaErrorInvalidConfiguration;
-    const bool one = (M == 1), eight = (a.bits == 8), multi = (P > 1);
+    const bool one = (M == 1), eight = (a.bits == 8), multi = (P > 1), wide = (M > kMaxM);
     decltype(&qmv_tma_kernel<4, true, false>) kern;
-    if (multi)
+    if (wide)
+        kern = eight ? (multi ? (ns3 ? qmv_tma_kernel<8, false, true, 3, 2> : qmv_tma_kernel<8, false, true, 4, 2>)
+                              : (ns3 ? qmv_tma_kernel<8, false, false, 3, 2> : qmv_tma_kernel<8, false, false, 4, 2>))
+                     : (multi ? (ns3 ? qmv_tma_kernel<4, false, true, 3, 2> : qmv_tma_kernel<4, false, true, 4, 2>)
+                              : (ns3 ? qmv_tma_kernel<4, false, false, 3, 2> : qmv_tma_kernel<4, false, false, 4, 2>));
+    else if (ns3 && multi)
+        kern = eight ? (one ? qmv_tma_kernel<8, true, true, 3> : qmv_tma_kernel<8, false, true, 3>)
+                     : (one ? qmv_tma_kernel<4, true, true, 3> : qmv_tma_kernel<4, false, true, 3>);
+    else if (ns3)
+        kern = eight ? (one ? qmv_tma_kernel<8, true, false, 3> : qmv_tma_kernel<8, false, false, 3>)
+                     : (one ? qmv_tma_kernel<4, true, false, 3> : qmv_tma_kernel<4, false, false, 3>);
+    else if (multi)
         kern = eight ? (one ? qmv_tma_kernel<8, true, true> : qmv_tma_kernel<8, false, true>)
                      : (one ? qmv_tma_kernel<4, true, true> : qmv_tma_kernel<4, false, true>);
     else
         kern = eight ? (one ? qmv_tma_kernel<8, true, false> : qmv_tma_kernel<8, false, false>)
                      : (one ? qmv_tma_kernel<4, true, false> : qmv_tma_kernel<4, false, false>);
-    const int ki = 4 * (int)multi + 2 * (int)eight + (int)one;
+    const int ki = 16 * (int)wide + 8 * (int)ns3 + 4 * (int)multi + 2 * (int)eight + (int)one;
     if (!g_attr_done[ki][dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
         if (e != cudaSuccess) return e;

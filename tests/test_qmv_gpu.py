@@ -53,10 +53,11 @@ def test_small_batch_sweep(dev, M, name, N, K):
     check(dev, M, N, K, synth.seed_for(3, M, j))
 
 
-@pytest.mark.parametrize("M,kernel", [(2, "qmv"), (16, "qmv"), (16, "auto"), (12, "auto")])
+@pytest.mark.parametrize("M,kernel", [(2, "qmv"), (16, "qmv"), (16, "auto"), (12, "auto"), (9, "auto")])
 def test_small_batch_lm_head_sampled(dev, M, kernel):
-    """The lm_head shape at small batch; with "auto", 9..16 rows run as two
-    launches of half the rows on the TMA kernel."""
+    """The lm_head shape at small batch.  With "qmv", 9..16 rows run in one
+    launch on the two blocks of MMA columns (in K passes: x of 16 rows of
+    K = 4096 is 128 KB); with "auto", as two launches of at most 8 rows."""
     import torch
     _, N, K = synth.LLAMA8B_LM_HEAD
     w = synth.make_weights(N, K, synth.seed_for(3, M, 7))
@@ -68,6 +69,22 @@ def test_small_batch_lm_head_sampled(dev, M, kernel):
     ye, yb = oracle.matmul_sampled(x, w.w_packed, w.scales, w.biases, M, N, K, im, inn)
     rms = float(np.sqrt(np.mean(ye * ye)))
     assert_parity(got[im, inn], yb, rms=rms, what="lm_head sampled")
+
+
+@pytest.mark.parametrize("M", [9, 10, 11, 12, 13, 14, 15, 16])
+@pytest.mark.parametrize("N,K", [(100, 512), (300, 2048), (67, 4096), (40, 8704)])
+def test_nine_to_sixteen_rows_one_pass(dev, M, N, K):
+    """9..16 rows of x on the weight-streaming kernel's two blocks of MMA
+    columns: ragged N, x in one pass (K <= 2048) and in K passes (K = 4096,
+    8704 with a ragged last stage), element by element against the oracle, on
+    the default choice and on the explicit one."""
+    check(dev, M, N, K, 900 + M + K, kernel="auto")
+    check(dev, M, N, K, 950 + M + K, kernel="qmv")
+
+
+@pytest.mark.parametrize("M,N,K", [(9, 70, 1024), (16, 300, 4096), (12, 33, 5120)])
+def test_nine_to_sixteen_rows_eight_bit(dev, M, N, K):
+    check(dev, M, N, K, 970 + M, bits=8)
 
 
 @pytest.mark.parametrize("M,N,K", [
