@@ -422,7 +422,7 @@ aq_status aq_matmul_nvfp4_bf16(const void *x, const uint32_t *w_packed, const ui
     if (flags & ~(unsigned)AQ_FLAG_PDL) return AQ_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim || K % 16) return AQ_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return AQ_OK;
-    if (M > 8 || K == 0 || K % 256 || M * K > 16384) return AQ_ERR_UNSUPPORTED;
+    if (M > 8 || K == 0 || K % 256 || M * K > 32768) return AQ_ERR_UNSUPPORTED;
     if (!x || !w_packed || !scales_e4m3 || !y) return AQ_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(w_packed, 16) || !aligned(scales_e4m3, 16) || !aligned(y, 2))
         return AQ_ERR_ALIGNMENT;

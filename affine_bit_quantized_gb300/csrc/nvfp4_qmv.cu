@@ -46,7 +46,7 @@ using namespace dev;
 using namespace qmv;
 
 constexpr int kThreads = (kConsumerWarps + 2) * 32;   // consumers, TMA producer, reducer
-constexpr int kNS = 4;                                 // ring depth
+constexpr int kNS = 4;                                 // ring depth (room for the bars)
 constexpr int kCodes = 2048;                           // codes per row and stage (1024 bytes)
 constexpr int kScaleBytes = kRows * (kCodes / 16);     // 4096: one E4M3 byte per 16 codes, 32 rows
 constexpr int kStage = kCodesBytes + kScaleBytes;      // 36864
@@ -56,9 +56,10 @@ constexpr int kSmemLimit = 232448;
 struct Layout {
     int x_off, xinfo_off, red_off, bar_off, total;
 };
-__host__ __device__ inline Layout make_layout(int M, int K) {
+// ns: ring depth, 4 beside x of up to 32 KB, 3 beside x of up to 64 KB
+__host__ __device__ inline Layout make_layout(int M, int K, int ns) {
     Layout L;
-    L.x_off = kNS * kStage;
+    L.x_off = ns * kStage;
     L.xinfo_off = L.x_off + M * x_row_bytes(M, K);
     L.red_off = L.xinfo_off + kXInfoBytes;
     L.bar_off = L.red_off + red_bytes(M);
@@ -100,16 +101,16 @@ __device__ __forceinline__ uint32_t lds16u(uint32_t a) {
 // x [M][K] bf16, bulk-copied to `raw` (rows x_row_bytes apart) -> fp16 in
 // natural k order in place, each row times 2^e (e from its max |x|, as in the
 // affine staging), and inv_scale[m] = 2^-e.
-template <bool ONE_ROW>
+template <bool ONE_ROW, int XROOM>
 __device__ __forceinline__ void stage_x_fp16(uint32_t raw, uint32_t xinfo, int M_, int K) {
     const int M = ONE_ROW ? 1 : M_;
     const int tid = threadIdx.x;
     const int wpr = K / 8, words = M * wpr, xrb = x_row_bytes(M, K);
     int *row_max = reinterpret_cast<int *>(__cvta_shared_to_generic(xinfo));
     float *inv_scale = reinterpret_cast<float *>(__cvta_shared_to_generic(xinfo + 64));
-    uint4 v[kMaxXBytes / 16 / kConsumerThreads];
+    uint4 v[XROOM / 16 / kConsumerThreads];
 #pragma unroll
-    for (int u = 0; u < kMaxXBytes / 16 / kConsumerThreads; ++u) {
+    for (int u = 0; u < XROOM / 16 / kConsumerThreads; ++u) {
         if (u * kConsumerThreads >= words) break;   // uniform over the CTA
         const int wi = u * kConsumerThreads + tid;
         int mx = 0;
@@ -124,7 +125,7 @@ __device__ __forceinline__ void stage_x_fp16(uint32_t raw, uint32_t xinfo, int M
     }
     consumer_sync();
 #pragma unroll
-    for (int u = 0; u < kMaxXBytes / 16 / kConsumerThreads; ++u) {
+    for (int u = 0; u < XROOM / 16 / kConsumerThreads; ++u) {
         if (u * kConsumerThreads >= words) break;
         const int wi = u * kConsumerThreads + tid;
         if (wi < words) {
@@ -185,14 +186,14 @@ __device__ __forceinline__ void consume_stage_nvfp4(uint32_t st, const uint32_t 
     }
 }
 
-template <bool ONE_ROW>
+template <bool ONE_ROW, int NS>
 __global__ void __launch_bounds__(kThreads, 1)
 nvfp4_qmv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
                  const __nv_bfloat16 *__restrict__ x, __nv_bfloat16 *__restrict__ y, int M, int N, int K,
                  float global_scale, unsigned long long timeout_ns, int *status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const Layout L = make_layout(M, K);
+    const Layout L = make_layout(M, K, NS);
     const uint32_t s_base = smem_addr(smem);
     const uint32_t x_s = s_base + (uint32_t)L.x_off;
     const uint32_t xinfo = s_base + (uint32_t)L.xinfo_off;
@@ -214,7 +215,7 @@ nvfp4_qmv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     const int items = my_tiles * KB;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kNS; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, kConsumerWarps);
         }
@@ -235,7 +236,7 @@ nvfp4_qmv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             auto issue = [&](int it) {
-                const int slot = it % kNS, tile = (int)blockIdx.x + (it / KB) * (int)gridDim.x, kb = it % KB;
+                const int slot = it % NS, tile = (int)blockIdx.x + (it / KB) * (int)gridDim.x, kb = it % KB;
                 const uint32_t dst = s_base + slot * kStage, fb = bar_full + 8 * slot;
                 // codes: one box of 8 chunks x 32 rows x 128 bytes; scales: 128 bytes x 32 rows
                 // (parts past the row's end read as zeros and still count)
@@ -245,15 +246,15 @@ nvfp4_qmv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             };
             int issued = 0;
             bool ok = true;
-            for (; issued < items && issued < kNS; ++issued) issue(issued);   // weights first
+            for (; issued < items && issued < NS; ++issued) issue(issued);   // weights first
             griddep_wait();
             const uint64_t deadline = global_timer() + timeout_ns;
             mbar_expect_tx(bar_x, (uint32_t)(M * K * 2));
             for (int m = 0; m < M; ++m)
                 bulk_load(x_s + m * x_row_bytes(M, K), x + (int64_t)m * K, (uint32_t)(K * 2), bar_x);
             for (; issued < items; ++issued) {
-                const int slot = issued % kNS;
-                if (!mbar_wait(bar_empty + 8 * slot, ((issued / kNS) - 1) & 1, deadline, abort_flag)) {
+                const int slot = issued % NS;
+                if (!mbar_wait(bar_empty + 8 * slot, ((issued / NS) - 1) & 1, deadline, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -265,8 +266,8 @@ nvfp4_qmv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                     *abort_flag = 1;
                 }
                 const uint64_t drain = global_timer() + timeout_ns;
-                for (int it = (issued > kNS ? issued - kNS : 0); it < issued; ++it)
-                    while (!mbar_try_wait(bar_full + 8 * (it % kNS), (it / kNS) & 1) && global_timer() < drain) {
+                for (int it = (issued > NS ? issued - NS : 0); it < issued; ++it)
+                    while (!mbar_try_wait(bar_full + 8 * (it % NS), (it / NS) & 1) && global_timer() < drain) {
                     }
                 while (!mbar_try_wait(bar_x, 0) && global_timer() < drain) {
                 }
@@ -296,7 +297,7 @@ nvfp4_qmv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             alive = false;
         };
         if (!mbar_wait(bar_x, 0, deadline, abort_flag)) fail();
-        stage_x_fp16<ONE_ROW>(x_s, xinfo, M, K);
+        stage_x_fp16<ONE_ROW, NS == kNS ? kMaxXBytes : 2 * kMaxXBytes>(x_s, xinfo, M, K);
         const int gid = lane >> 2, t = lane & 3;
         // the lane's 16 bytes of codes in row gid + 8r (128-byte swizzle: unit u of row r at u ^ (r % 8))
         uint32_t code[4];
@@ -316,8 +317,8 @@ nvfp4_qmv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         int item = 0;
         for (int tl = 0; tl < my_tiles; ++tl) {
             for (int kb = 0; ok && kb < KB; ++kb, ++item) {
-                const int slot = item % kNS;
-                if (!mbar_wait_fast(bar_full + 8 * slot, (uint32_t)(item / kNS) & 1u, deadline, abort_flag)) {
+                const int slot = item % NS;
+                if (!mbar_wait_fast(bar_full + 8 * slot, (uint32_t)(item / NS) & 1u, deadline, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -347,7 +348,7 @@ bool encode_scales_2d(CUtensorMap *map, const void *base, uint64_t row_bytes, ui
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sms[kMaxDevices];
-std::atomic<int> g_attr_done[2][kMaxDevices];
+std::atomic<int> g_attr_done[4][kMaxDevices];
 
 }  // namespace
 
@@ -364,13 +365,17 @@ cudaError_t launch_nvfp4_qmv(const Nvfp4Args &a) {
     }
     const int M = (int)a.M, N = (int)a.N, K = (int)a.K;
     const bool one = M == 1;
-    auto kern = one ? nvfp4_qmv_kernel<true> : nvfp4_qmv_kernel<false>;
-    if (!g_attr_done[one][dev].load(std::memory_order_acquire)) {
+    // x beyond 32 KB (up to 64 KB): a 3-stage ring beside it
+    const bool ns3 = (int64_t)M * K * 2 > kMaxXBytes;
+    auto kern = ns3 ? (one ? nvfp4_qmv_kernel<true, 3> : nvfp4_qmv_kernel<false, 3>)
+                    : (one ? nvfp4_qmv_kernel<true, kNS> : nvfp4_qmv_kernel<false, kNS>);
+    const int ki = 2 * (int)ns3 + (int)one;
+    if (!g_attr_done[ki][dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
         if (e != cudaSuccess) return e;
-        g_attr_done[one][dev].store(1, std::memory_order_release);
+        g_attr_done[ki][dev].store(1, std::memory_order_release);
     }
-    const Layout L = make_layout(M, K);
+    const Layout L = make_layout(M, K, ns3 ? 3 : kNS);
     const int smem = L.total + 1024;
     if (smem > kSmemLimit) return cudaErrorInvalidConfiguration;
     CUtensorMap tw, ts;

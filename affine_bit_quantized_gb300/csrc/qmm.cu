@@ -73,11 +73,15 @@ constexpr int kSBBytes = kTileN * kSBGroups * 2;   // 4096 (scales, and again bi
 // MMA's k order, from a conversion pass into the caller's workspace), copied
 // by TMA straight into the operand tile: no raw x stage, which leaves room
 // for a third converted stage.
-template <int BITS, bool XPRE = false>
+// TM: rows of x per CTA.  8-bit codes without x converted once take 128 (their
+// raw x and code stages would not fit beside 256-row operand stages); with x
+// already fp16 there is no raw x stage and two converted stages of 256 rows
+// fit, which doubles the MMA work per converted W tile.
+template <int BITS, bool XPRE = false, int TM = (BITS == 4 ? 256 : 128)>
 struct Cfg {
-    static constexpr int kTileM = BITS == 4 ? 256 : 128;        // rows of x per CTA
+    static constexpr int kTileM = TM;
     static constexpr int kHalves = kTileM / 128;                 // UMMA M=128 accumulators
-    static constexpr int kConvStages = XPRE ? 3 : 2;
+    static constexpr int kConvStages = XPRE ? ((BITS == 8 && TM == 256) ? 2 : 3) : 2;
     static constexpr int kATileBytes = kTileM * 128;             // fp16 x, kTileM rows x 64 k
     static constexpr int kConvStageBytes = kATileBytes + kBTileBytes;
     static constexpr int kRawXBytes = XPRE ? 0 : kTileM * 128;   // bf16 x, same swizzled geometry
@@ -95,14 +99,17 @@ struct Cfg {
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;     // + alignment slack
 };
 static_assert(Cfg<4>::kSmemBytes <= 232448 && Cfg<8>::kSmemBytes <= 232448 && Cfg<4, true>::kSmemBytes <= 232448 &&
-                  Cfg<8, true>::kSmemBytes <= 232448,
+                  Cfg<8, true>::kSmemBytes <= 232448 && Cfg<8, true, 256>::kSmemBytes <= 232448,
               "shared memory per CTA");
 // split-K partials received by a CTA (at most 7 sources x its 32 columns x the tile's rows) fit in
 // the stage memory in front of the barriers
 constexpr int kMaxSplit = 8;
 static_assert((kMaxSplit - 1) * Cfg<4>::kTileM * (kTileN / kMaxSplit) * 4 <= Cfg<4>::kOffBar &&
-                  (kMaxSplit - 1) * Cfg<8>::kTileM * (kTileN / kMaxSplit) * 4 <= Cfg<8>::kOffBar,
+                  (kMaxSplit - 1) * Cfg<8>::kTileM * (kTileN / kMaxSplit) * 4 <= Cfg<8>::kOffBar &&
+                  (kMaxSplit - 1) * Cfg<4, true>::kTileM * (kTileN / kMaxSplit) * 4 <= Cfg<4, true>::kOffBar &&
+                  (kMaxSplit - 1) * Cfg<8, true>::kTileM * (kTileN / kMaxSplit) * 4 <= Cfg<8, true>::kOffBar,
               "split-K receive slots");
+// 256-row 8-bit tiles are taken only without a split
 
 constexpr uint32_t kTmemCols = 512;
 constexpr int kPlanHeaderInts = 32;    // tile count, then the tiles (int4 each) from byte 128
@@ -315,13 +322,13 @@ cudaError_t launch_plain(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaSt
 // W, scales and biases are E matrices stacked along N, and `plan` lists the
 // work tiles {expert, first row, rows} (see gather_plan_kernel); CTA row
 // blockIdx.y takes tile blockIdx.y and exits at once if there is none.
-template <int BITS, bool GROUPED, bool XPRE>
+template <int BITS, bool GROUPED, bool XPRE, int TM = (BITS == 4 ? 256 : 128)>
 __global__ void __launch_bounds__(kThreads, 1)
 qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
            const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_b,
            __nv_bfloat16 *__restrict__ y, int M, int N, int K, unsigned long long timeout_ns, int *status,
            const int *__restrict__ plan, int skip_copy) {
-    using C = Cfg<BITS, XPRE>;
+    using C = Cfg<BITS, XPRE, TM>;
     constexpr int kConvStages = C::kConvStages;
     constexpr int kTileM = C::kTileM, kATileBytes = C::kATileBytes, kConvStageBytes = C::kConvStageBytes;
     constexpr int kRawXBytes = C::kRawXBytes, kRawStageBytes = C::kRawStageBytes;
@@ -750,7 +757,7 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *gaddr, uint
 }
 
 constexpr int kMaxDevices = 64;
-std::atomic<int> g_attr_done[4][kMaxDevices];
+std::atomic<int> g_attr_done[5][kMaxDevices];
 std::atomic<int> g_attr_done_grouped[2][kMaxDevices];
 std::atomic<int> g_sms[kMaxDevices];
 // clusters of 2, 4, 8 CTAs that can be resident at once, per code width (0: not yet asked; -1: none)
@@ -764,62 +771,31 @@ bool qmm_supported(const MatmulArgs &a) {
 }
 
 namespace {
-template <int BITS, bool XPRE>
-cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev) {
-    using C = Cfg<BITS, XPRE>;
-    const int bi = (BITS == 8 ? 1 : 0) + (XPRE ? 2 : 0);
-    if (!g_attr_done[bi][dev].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(qmm_kernel<BITS, false, XPRE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        g_attr_done[bi][dev].store(1, std::memory_order_release);
-    }
-    const int M = (int)a.M, N = (int)a.N, K = (int)a.K, G = K / 64;
-    if (XPRE) {
-        const int64_t vecs = (int64_t)M * K / 8;
-        cudaError_t e = launch_plain(x_to_f16_kernel<BITS>, dim3((unsigned)std::min<int64_t>((vecs + 255) / 256, 4096)),
-                                     dim3(256), a.stream, static_cast<const uint4 *>(a.x), static_cast<uint4 *>(a.xf16),
-                                     vecs);
-        if (e != cudaSuccess) return e;
-    }
-    CUtensorMap tx, tw, ts, tb;
-    if (!encode_2d(&tx, XPRE ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, XPRE ? a.xf16 : a.x, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, kGroup,
-                   C::kTileM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.w, (uint64_t)K * BITS / 32, (uint64_t)N,
-                   (uint64_t)K * BITS / 8, C::kRowWords, kTileN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.scales, (uint64_t)G, (uint64_t)N, (uint64_t)G * 2, kSBGroups,
-                   kTileN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.biases, (uint64_t)G, (uint64_t)N, (uint64_t)G * 2, kSBGroups,
-                   kTileN, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorInvalidValue;
+// K split across a cluster of 2, 4 or 8 CTAs when the output has too few tiles to
+// occupy half the SMs (prefill at M = 256), as many as still fit in one wave.
+// Decided on the tiles of the kernel without the workspace, so that both
+// variants split alike (same summation order, same bits).
+template <int BITS>
+int qmm_split(const MatmulArgs &a, int dev) {
+    using C = Cfg<BITS, false>;
+    const int M = (int)a.M, N = (int)a.N, K = (int)a.K;
     int sms = g_sms[dev].load(std::memory_order_relaxed);
     if (sms == 0) {
-        cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();   // no split; the launch reports the device's state
+            return 1;
+        }
         g_sms[dev].store(sms, std::memory_order_relaxed);
     }
     const int64_t tiles = (int64_t)((N + kTileN - 1) / kTileN) * ((M + C::kTileM - 1) / C::kTileM);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + C::kTileM - 1) / C::kTileM), 1);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = a.stream;
-    cudaLaunchAttribute attr[2];
-    int na = 0;
-    if (a.pdl) {
-        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[na].val.programmaticStreamSerializationAllowed = 1;
-        ++na;
-    }
-    // Too few output tiles to occupy half the SMs (prefill at M = 256): split K
-    // across a cluster of 2, 4 or 8 CTAs, as many as still fit in one wave.
     int split = 1;
     if (2 * tiles <= sms) {
         for (int si = 2; si >= 0 && split == 1; --si) {
             const int S = 2 << si;
             if (S > K / (kGroup * kSBGroups) || tiles * S > sms) continue;
-            // decided on the kernel without the workspace, so that both variants split alike
-            // (same summation order, same bits)
             const int bb = BITS == 8 ? 1 : 0;
             int n = g_max_clusters[bb][si][dev].load(std::memory_order_relaxed);
             if (n == 0) {
@@ -850,6 +826,50 @@ cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev) {
             if (n >= tiles) split = S;
         }
     }
+    return split;
+}
+
+// split: K split across a cluster of this many CTAs (qmm_split)
+template <int BITS, bool XPRE, int TM = (BITS == 4 ? 256 : 128)>
+cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev, int split) {
+    using C = Cfg<BITS, XPRE, TM>;
+    const int bi = TM == 256 && BITS == 8 ? 4 : (BITS == 8 ? 1 : 0) + (XPRE ? 2 : 0);
+    if (!g_attr_done[bi][dev].load(std::memory_order_acquire)) {
+        cudaError_t e = cudaFuncSetAttribute(qmm_kernel<BITS, false, XPRE, TM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        g_attr_done[bi][dev].store(1, std::memory_order_release);
+    }
+    const int M = (int)a.M, N = (int)a.N, K = (int)a.K, G = K / 64;
+    if (XPRE) {
+        const int64_t vecs = (int64_t)M * K / 8;
+        cudaError_t e = launch_plain(x_to_f16_kernel<BITS>, dim3((unsigned)std::min<int64_t>((vecs + 255) / 256, 4096)),
+                                     dim3(256), a.stream, static_cast<const uint4 *>(a.x), static_cast<uint4 *>(a.xf16),
+                                     vecs);
+        if (e != cudaSuccess) return e;
+    }
+    CUtensorMap tx, tw, ts, tb;
+    if (!encode_2d(&tx, XPRE ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, XPRE ? a.xf16 : a.x, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, kGroup,
+                   C::kTileM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.w, (uint64_t)K * BITS / 32, (uint64_t)N,
+                   (uint64_t)K * BITS / 8, C::kRowWords, kTileN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.scales, (uint64_t)G, (uint64_t)N, (uint64_t)G * 2, kSBGroups,
+                   kTileN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.biases, (uint64_t)G, (uint64_t)N, (uint64_t)G * 2, kSBGroups,
+                   kTileN, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + C::kTileM - 1) / C::kTileM), 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (a.pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     if (split > 1) {
         cfg.gridDim.z = (unsigned)split;
         attr[na].id = cudaLaunchAttributeClusterDimension;
@@ -860,7 +880,7 @@ cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev) {
     }
     cfg.attrs = attr;
     cfg.numAttrs = (unsigned)na;
-    return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS, false, XPRE>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(a.y), M,
+    return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS, false, XPRE, TM>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(a.y), M,
                               N, K, (unsigned long long)a.timeout_ns, a.status, (const int *)nullptr,
                               a.debug_skip_copy ? 1 : 0);
 }
@@ -871,8 +891,19 @@ cudaError_t launch_qmm(const MatmulArgs &a) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if (a.xf16) return a.bits == 8 ? launch_qmm_bits<8, true>(a, dev) : launch_qmm_bits<4, true>(a, dev);
-    return a.bits == 8 ? launch_qmm_bits<8, false>(a, dev) : launch_qmm_bits<4, false>(a, dev);
+    if (a.bits == 4) {
+        const int split = qmm_split<4>(a, dev);
+        return a.xf16 ? launch_qmm_bits<4, true>(a, dev, split) : launch_qmm_bits<4, false>(a, dev, split);
+    }
+    const int split = qmm_split<8>(a, dev);
+    if (!a.xf16) return launch_qmm_bits<8, false>(a, dev, split);
+    // x converted once: 256-row tiles where that needs no split and still fills half the
+    // SMs (M = 2048 on 14336 x 4096: 743 -> 1205 TFLOP/s; on 4096 x 14336 one wave of
+    // 128 such tiles against 1.7 waves of 128-row tiles)
+    const int sms = g_sms[dev].load(std::memory_order_relaxed);
+    const int64_t tiles256 = ((a.N + kTileN - 1) / kTileN) * ((a.M + 255) / 256);
+    if (split == 1 && sms > 0 && 2 * tiles256 >= sms) return launch_qmm_bits<8, true, 256>(a, dev, split);
+    return launch_qmm_bits<8, true>(a, dev, split);
 }
 
 // ---------------------------------------------------------------- expert-indexed matmul

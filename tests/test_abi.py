@@ -190,7 +190,7 @@ def test_gather_validation(kw, expect):
     (dict(K=100), aq.AQ_ERR_INVALID_ARG),          # not a multiple of 16
     (dict(K=272), aq.AQ_ERR_UNSUPPORTED),          # not a multiple of 256
     (dict(M=9), aq.AQ_ERR_UNSUPPORTED),
-    (dict(M=2, K=16384), aq.AQ_ERR_UNSUPPORTED),   # x beyond one staging
+    (dict(M=4, K=16384), aq.AQ_ERR_UNSUPPORTED),   # x beyond one staging (64 KB)
     (dict(M=-1), aq.AQ_ERR_INVALID_ARG),
     (dict(flags=1 << 3), aq.AQ_ERR_INVALID_ARG),
     (dict(x=None), aq.AQ_ERR_INVALID_ARG),

@@ -41,6 +41,8 @@ def check(dev, M, N, K, seed):
 @pytest.mark.parametrize("M,N,K", [
     (1, 1, 256), (1, 32, 256), (1, 33, 512), (1, 100, 2048), (1, 300, 2304), (1, 4096, 4096),
     (1, 64, 16384), (2, 77, 4096), (3, 129, 1280), (4, 50, 4096), (8, 64, 2048), (5, 31, 768),
+    # x between 32 and 64 KB: the 3-stage ring beside it
+    (8, 300, 4096), (2, 150, 14336), (1, 70, 32768), (7, 33, 4608), (3, 4096, 8192),
 ])
 def test_nvfp4_shapes(dev, M, N, K):
     check(dev, M, N, K, 900 + M + N + K)
