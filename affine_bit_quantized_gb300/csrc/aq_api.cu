@@ -4,6 +4,7 @@
 // touches the device (the boundary behaviour asked for by the "MLX CUDA
 // Cleanup Plan" page: small wrappers for status handling, no hidden
 // fallbacks, no extra copies or synchronization).
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdio>
@@ -422,7 +423,7 @@ aq_status aq_matmul_nvfp4_bf16(const void *x, const uint32_t *w_packed, const ui
     if (flags & ~(unsigned)AQ_FLAG_PDL) return AQ_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim || K % 16) return AQ_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return AQ_OK;
-    if (M > 8 || K == 0 || K % 256 || M * K > 32768) return AQ_ERR_UNSUPPORTED;
+    if (K == 0 || K % 256 || K > 32768) return AQ_ERR_UNSUPPORTED;
     if (!x || !w_packed || !scales_e4m3 || !y) return AQ_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(w_packed, 16) || !aligned(scales_e4m3, 16) || !aligned(y, 2))
         return AQ_ERR_ALIGNMENT;
@@ -440,7 +441,17 @@ aq_status aq_matmul_nvfp4_bf16(const void *x, const uint32_t *w_packed, const ui
     a.timeout_ns = kTimeoutNs;
     aq_status st = record_cuda(status_ptr(&a.status));
     if (st != AQ_OK) return st;
-    return record_cuda(aq::launch_nvfp4_qmv(a));
+    // launches of up to 8 rows whose x fits the kernel's 64 KB staging room, each
+    // streaming W once
+    const int64_t rows = std::min<int64_t>(8, 32768 / K);
+    for (int64_t m0 = 0; m0 < M; m0 += rows) {
+        a.x = static_cast<const uint16_t *>(x) + m0 * K;
+        a.y = static_cast<uint16_t *>(y) + m0 * N;
+        a.M = (M - m0) < rows ? (M - m0) : rows;
+        st = record_cuda(aq::launch_nvfp4_qmv(a));
+        if (st != AQ_OK) return st;
+    }
+    return AQ_OK;
 }
 
 aq_status aq_read_probe(const void *buf, size_t bytes, void *stream) {

@@ -201,10 +201,11 @@ def run_case(args):
     from affine_bit_quantized_gb300 import _build
 
     M, N, K = (int(v) for v in args.case.split(","))
+    bits = args.bits
     dev = torch.device("cuda", 0)
     _build.build_library()
     lib = aq.load()
-    w = synth.make_weights(N, K, 1)
+    w = synth.make_weights(N, K, 1, bits=bits)
     x = synth.make_x(M, K, 1)
     wbytes = w.nbytes
     copies = max(1, min(64, -(-3 * 129 * 2**20 // wbytes)))
@@ -224,10 +225,10 @@ def run_case(args):
         wt, st, bt = ws[i % copies]
         if args.workspace:
             rc = lib.aq_matmul_bf16_ws(xt.data_ptr(), wt.data_ptr(), st.data_ptr(), bt.data_ptr(), yt.data_ptr(), M,
-                                       N, K, 64, 4, xws.data_ptr(), xws.numel(), stream.cuda_stream)
+                                       N, K, 64, bits, xws.data_ptr(), xws.numel(), stream.cuda_stream)
         else:
             rc = lib.aq_matmul_bf16_ex(xt.data_ptr(), wt.data_ptr(), st.data_ptr(), bt.data_ptr(), yt.data_ptr(), M,
-                                       N, K, 64, 4, kernel, 0, stream.cuda_stream)
+                                       N, K, 64, bits, kernel, 0, stream.cuda_stream)
         if rc != aq.AQ_OK:
             raise aq.AqError(rc, "matmul call")
 
@@ -242,9 +243,9 @@ def run_case(args):
     e1.synchronize()
     us = e0.elapsed_time(e1) * 1e3 / args.steps
     hbm_peak, bf16_peak, _, _ = load_peaks()
-    gbs = alg_bytes(M, N, K) / (us * 1e-6) / 1e9
+    gbs = alg_bytes(M, N, K, bits) / (us * 1e-6) / 1e9
     tflops = 2.0 * M * N * K / (us * 1e-6) / 1e12
-    print(json.dumps({"case": [M, N, K], "kernel": args.kernel, "us_per_call": round(us, 3), "gbs": round(gbs, 1),
+    print(json.dumps({"case": [M, N, K], "bits": bits, "kernel": args.kernel, "us_per_call": round(us, 3), "gbs": round(gbs, 1),
                       "hbm_frac": round(gbs / hbm_peak, 4), "tflops": round(tflops, 2),
                       "bf16_frac": round(tflops / bf16_peak, 4), "weight_copies": copies}), flush=True)
 
@@ -356,6 +357,7 @@ def main():
     ap.add_argument("--case", default=None,
                     help="M,N,K: time one matrix shape instead of the decode step (also the ncu target)")
     ap.add_argument("--kernel", choices=("auto", "qmv", "qmm"), default="auto", help="kernel for --case")
+    ap.add_argument("--bits", type=int, choices=(4, 8), default=4, help="code width for --case")
     ap.add_argument("--nvfp4-case", default=None, help="M,N,K: time one NVFP4 shape (an ncu target)")
     ap.add_argument("--moe-case", default=None, choices=[m[0] for m in synth.MIXTRAL_EXPERT_MATS],
                     help="time one MoE prefill matrix (2048 tokens, top-2 of 8 experts; an ncu target)")

@@ -324,8 +324,9 @@ aq_status aq_gather_qmm_bf16(const void *x, const uint32_t *w_packed, const void
  *                 infinities; S.1111.111 is NaN and propagates)
  *   global_scale  the tensor's fp32 scale (1.0f if it has none)
  *   y             bf16 [M, N], device, written; fp32 accumulation, one rounding
- *   1 <= M <= 8, N >= 1, K a multiple of 256 with M*K <= 32768 (M == 0 or
- *   N == 0: nothing launched).  x, w_packed and scales_e4m3 16-byte aligned,
+ *   M >= 0, N >= 1, K a multiple of 256 up to 32768 (M == 0 or N == 0:
+ *   nothing launched).  Runs as launches of up to min(8, 32768 / K) rows of x,
+ *   each streaming the weights once.  x, w_packed and scales_e4m3 16-byte aligned,
  *   y 2-byte aligned.  Errors: AQ_ERR_INVALID_ARG, AQ_ERR_UNSUPPORTED (sizes
  *   outside these limits), AQ_ERR_ALIGNMENT, AQ_ERR_CUDA.  Asynchronous;
  *   allocates nothing; deterministic.  AQ_FLAG_PDL is accepted in `flags`.

@@ -189,8 +189,7 @@ def test_gather_validation(kw, expect):
 @pytest.mark.parametrize("kw,expect", [
     (dict(K=100), aq.AQ_ERR_INVALID_ARG),          # not a multiple of 16
     (dict(K=272), aq.AQ_ERR_UNSUPPORTED),          # not a multiple of 256
-    (dict(M=9), aq.AQ_ERR_UNSUPPORTED),
-    (dict(M=4, K=16384), aq.AQ_ERR_UNSUPPORTED),   # x beyond one staging (64 KB)
+    (dict(K=32768 + 256), aq.AQ_ERR_UNSUPPORTED),  # one row of x beyond the 64 KB staging room
     (dict(M=-1), aq.AQ_ERR_INVALID_ARG),
     (dict(flags=1 << 3), aq.AQ_ERR_INVALID_ARG),
     (dict(x=None), aq.AQ_ERR_INVALID_ARG),
