@@ -155,7 +155,9 @@ def aq_chain_run(plan, stream) -> int:
 
 def _chain_descs(items, group_size: int, bits: int, independent):
     """Checks (x, w_packed, scales, biases, y) tensors of a chain and returns
-    their aq_matmul_desc array (at least one element)."""
+    their aq_matmul_desc array (at least one element).  group_size 16 is an
+    NVFP4 chain: (x, w_packed, scales_e4m3 uint8 [N, K/16], global_scale
+    float32 [1] on the device, y)."""
     n = len(items)
     if independent is not None and len(independent) != n:
         raise ValueError(f"independent has {len(independent)} flags for {n} matmuls")
@@ -166,7 +168,14 @@ def _chain_descs(items, group_size: int, bits: int, independent):
             raise ValueError(f"chain item {i}: x and w_packed must be 2-D")
         at = f"chain item {i}: "
         _check(at + "x", x, tuple(x.shape), "bf16")
-        _check_weights(w, s, b, (w.shape[0],), x.shape[1], group_size, bits, prefix=at)
+        if group_size == 16:
+            K = x.shape[1]
+            blocks_ok = K % 16 == 0          # other K the library rejects itself
+            _check(at + "w_packed", w, (None, K // 8 if blocks_ok else None), "word")
+            _check(at + "scales_e4m3", s, (w.shape[0], K // 16 if blocks_ok else None), "u8")
+            _check(at + "global_scale", b, (1,), "f32")
+        else:
+            _check_weights(w, s, b, (w.shape[0],), x.shape[1], group_size, bits, prefix=at)
         _check(at + "y", y, (x.shape[0], w.shape[0]), "bf16")
         named += [(at + "x", x), (at + "w_packed", w), (at + "scales", s), (at + "biases", b), (at + "y", y)]
     if n:
@@ -286,6 +295,8 @@ def _kind_ok(t, kind: str) -> bool:
         return t.dtype == torch.int32
     if kind == "u8":
         return t.dtype == torch.uint8
+    if kind == "f32":
+        return t.dtype == torch.float32
     raise AssertionError(kind)
 
 

@@ -2,29 +2,14 @@
 //
 // The "MLX CUDA Cleanup Plan" page (Refactor Plan, Phase 3b) asks for a CUDA
 // NVFP4 qmv for its mode=nvfp4, group_size=16 checkpoint, kept structurally
-// separate from the affine path.  Format (the NVFP4 layout of NVIDIA's model
-// optimizer): FP4 E2M1 codes packed eight per uint32 (lowest nibble = lowest
-// k), one FP8 E4M3 scale per 16 codes along K, one fp32 scale per tensor:
-//
-//     w[n,k] = global * e4m3(scale[n, k/16]) * e2m1(q[n,k])
-//
-// The stream and the tile bookkeeping are those of the affine decode kernel
-// (a TMA producer warp filling a ring of 36 KB stages, sixteen consumer warps,
-// a reducer warp adding their partials in a fixed order); the arithmetic is
-// this format's own:
-//
-//  * e2m1 * e4m3 has at most six significant bits and lies in [2^-10, 2688],
-//    so a code pair converted to fp16 (cvt.rn.f16x2.e2m1x2) times its block
-//    scale (fp16, exact for every finite E4M3 value) is the exact weight in
-//    fp16: no per-group fold, the MMA accumulates across all groups;
-//  * x is staged once per CTA in fp16, each row scaled by a power of two so
-//    that its bf16 values stay exact (the partial sums are scaled back, then
-//    the reducer multiplies by the tensor scale before the one bf16 rounding);
-//  * lane t of a warp holds 32 consecutive codes of each of its four rows (one
-//    16-byte load), i.e. two whole scale groups; MMA step s takes bytes 2s and
-//    2s+1 of those 16, and the x fragment of step s is the four x values at
-//    the same code positions (one 8-byte load), so A and B agree on which k
-//    sits in each MMA slot.
+// separate from the affine path.  The format and the consumer arithmetic are
+// in nvfp4_consumer.cuh (shared with the NVFP4 mode of the chain kernel); the
+// stream and the tile bookkeeping are those of the affine decode kernel (a TMA
+// producer warp filling a ring of 36 KB stages, sixteen consumer warps, a
+// reducer warp adding their partials in a fixed order).  x is bulk-copied
+// once per CTA and converted in place to scaled fp16 in the consumer's order,
+// with one power-of-two scale per row (the partial sums are scaled back, then
+// the reducer multiplies by the tensor scale before the one bf16 rounding).
 //
 // Every mbarrier wait is bounded (global-timer deadline, device status word),
 // as in the affine kernels.
@@ -37,6 +22,7 @@
 
 #include "aq_internal.h"
 #include "aq_ptx.cuh"
+#include "nvfp4_consumer.cuh"
 #include "qmv_consumer.cuh"
 
 namespace aq {
@@ -47,9 +33,8 @@ using namespace qmv;
 
 constexpr int kThreads = (kConsumerWarps + 2) * 32;   // consumers, TMA producer, reducer
 constexpr int kNS = 4;                                 // ring depth (room for the bars)
-constexpr int kCodes = 2048;                           // codes per row and stage (1024 bytes)
-constexpr int kScaleBytes = kRows * (kCodes / 16);     // 4096: one E4M3 byte per 16 codes, 32 rows
-constexpr int kStage = kCodesBytes + kScaleBytes;      // 36864
+constexpr int kCodes = kNvCodes;                       // codes per row and stage (1024 bytes)
+constexpr int kStage = kNvStage;                       // 36864
 constexpr int kNumBars = 2 * kNS + 1 + 8;              // full[4], empty[4], x, red_full[4], red_empty[4]
 constexpr int kSmemLimit = 232448;
 
@@ -67,39 +52,8 @@ __host__ __device__ inline Layout make_layout(int M, int K, int ns) {
     return L;
 }
 
-// fp16x2 of the two E2M1 codes of byte `b` of v (low nibble in the low half)
-template <int B>
-__device__ __forceinline__ uint32_t e2m1_pair(uint32_t v) {
-    uint32_t r;
-    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n cvt.rn.f16x2.e2m1x2 %0, b%2;\n}"
-        : "=r"(r)
-        : "r"(v), "n"(B));
-    return r;
-}
-// fp16x2 of the two E4M3 bytes in the low 16 bits of v (low byte in the low half)
-__device__ __forceinline__ uint32_t e4m3_pair(uint32_t v) {
-    uint32_t r;
-    asm("{\n .reg .b16 h;\n cvt.u16.u32 h, %1;\n cvt.rn.f16x2.e4m3x2 %0, h;\n}" : "=r"(r) : "r"(v));
-    return r;
-}
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t r;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-    return r;
-}
-__device__ __forceinline__ uint32_t lds16u(uint32_t a) {
-    uint16_t v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
-    return v;
-}
-
 // x [M][K] bf16, bulk-copied to `raw` (rows x_row_bytes apart) -> fp16 in
-// natural k order in place, each row times 2^e (e from its max |x|, as in the
+// place, in the staged order of nvfp4_consumer.cuh, each row times 2^e (e from its max |x|, as in the
 // affine staging), and inv_scale[m] = 2^-e.
 template <bool ONE_ROW, int XROOM>
 __device__ __forceinline__ void stage_x_fp16(uint32_t raw, uint32_t xinfo, int M_, int K) {
@@ -132,58 +86,16 @@ __device__ __forceinline__ void stage_x_fp16(uint32_t raw, uint32_t xinfo, int M
             const int m = ONE_ROW ? 0 : wi / wpr, wr = wi - m * wpr;
             const float sc = pow2f(x_scale_exponent(row_max[m]));
             const uint4 a = v[u];
-            uint4 o;
-            o.x = f32x2_to_f16x2(bf16lo(a.x) * sc, bf16hi(a.x) * sc);
-            o.y = f32x2_to_f16x2(bf16lo(a.y) * sc, bf16hi(a.y) * sc);
-            o.z = f32x2_to_f16x2(bf16lo(a.z) * sc, bf16hi(a.z) * sc);
-            o.w = f32x2_to_f16x2(bf16lo(a.w) * sc, bf16hi(a.w) * sc);
-            sts128(raw + (uint32_t)(m * xrb + wr * 16), o);
+            // into the consumer's order within the word's 128-code block (every
+            // word of the block was read before the barrier above)
+            const uint32_t q = raw + (uint32_t)(m * xrb + (wr >> 4) * 256) + nv_x_word_offset(wr & 15);
+            sts64u(q, f32x2_to_f16x2(bf16lo(a.x) * sc, bf16hi(a.x) * sc), f32x2_to_f16x2(bf16lo(a.y) * sc, bf16hi(a.y) * sc));
+            sts64u(q + 32, f32x2_to_f16x2(bf16lo(a.z) * sc, bf16hi(a.z) * sc),
+                   f32x2_to_f16x2(bf16lo(a.w) * sc, bf16hi(a.w) * sc));
         }
     }
     if (tid < M) inv_scale[tid] = pow2f(-x_scale_exponent(row_max[tid]));
     consumer_sync();
-}
-
-// Adds warp `warp`'s block of a stage (32 rows x 128 codes: codes
-// [warp*128, warp*128 + 128) of the stage) to acc.  code: the lane's row
-// offsets; xq: byte address of x[row][stage_k + warp*128 + lane%4 * 32].
-__device__ __forceinline__ void consume_stage_nvfp4(uint32_t st, const uint32_t (&code)[4], uint32_t sb,
-                                                    uint32_t xq, float (&acc)[2][4]) {
-    uint4 cw[4];
-    uint32_t sa2[4], sb2[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        cw[r] = lds128(st + code[r]);
-        // the block scales of the lane's two groups in row gid + 8r, each in both halves
-        const uint32_t s2 = e4m3_pair(lds16u(st + kCodesBytes + sb + 8 * 128 * r));
-        sa2[r] = prmt(s2, s2, 0x1010u);
-        sb2[r] = prmt(s2, s2, 0x3232u);
-    }
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-        const uint2 X = lds64(xq + s * 8);   // x at the lane's codes 4s .. 4s+3
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint4 &R0 = cw[2 * h], &R1 = cw[2 * h + 1];   // rows gid + 16h, gid + 8 + 16h
-            const uint32_t w0 = s < 2 ? R0.x : s < 4 ? R0.y : s < 6 ? R0.z : R0.w;
-            const uint32_t w1 = s < 2 ? R1.x : s < 4 ? R1.y : s < 6 ? R1.z : R1.w;
-            const uint32_t g0 = s < 4 ? sa2[2 * h] : sb2[2 * h];
-            const uint32_t g1 = s < 4 ? sa2[2 * h + 1] : sb2[2 * h + 1];
-            uint32_t a0, a1, a2, a3;
-            if (s & 1) {
-                a0 = hmul2(e2m1_pair<2>(w0), g0);
-                a1 = hmul2(e2m1_pair<2>(w1), g1);
-                a2 = hmul2(e2m1_pair<3>(w0), g0);
-                a3 = hmul2(e2m1_pair<3>(w1), g1);
-            } else {
-                a0 = hmul2(e2m1_pair<0>(w0), g0);
-                a1 = hmul2(e2m1_pair<0>(w1), g1);
-                a2 = hmul2(e2m1_pair<1>(w0), g0);
-                a3 = hmul2(e2m1_pair<1>(w1), g1);
-            }
-            mma_f16_16816(acc[h], a0, a1, a2, a3, X.x, X.y);
-        }
-    }
 }
 
 template <bool ONE_ROW, int NS>
@@ -299,16 +211,11 @@ nvfp4_qmv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         if (!mbar_wait(bar_x, 0, deadline, abort_flag)) fail();
         stage_x_fp16<ONE_ROW, NS == kNS ? kMaxXBytes : 2 * kMaxXBytes>(x_s, xinfo, M, K);
         const int gid = lane >> 2, t = lane & 3;
-        // the lane's 16 bytes of codes in row gid + 8r (128-byte swizzle: unit u of row r at u ^ (r % 8))
-        uint32_t code[4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-            code[r] = (uint32_t)((warp >> 1) * kBoxBytes + (gid + 8 * r) * 128 + (((4 * (warp & 1) + t) ^ gid) << 4));
-        // the lane's two scale bytes (groups warp*8 + 2t, +1) of row gid (128-byte swizzle)
-        const uint32_t sb = (uint32_t)(gid * 128 + (((warp >> 1) ^ gid) << 4) + 8 * (warp & 1) + 2 * t);
+        NvThread ct;
+        nv_consumer_init(ct, warp, lane);
         const int M1 = ONE_ROW ? 1 : M;
         const int xrow = ONE_ROW ? 0 : (gid < M1 ? gid : M1 - 1);    // B column gid holds x row gid
-        const uint32_t xq0 = x_s + (uint32_t)(xrow * x_row_bytes(M1, K) + (warp * 128 + t * 32) * 2);
+        const uint32_t xq0 = x_s + (uint32_t)(xrow * x_row_bytes(M1, K) + warp * 256 + t * 8);
         const int nblk = K / 128;
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         // the row scales of this lane's MMA columns 2t and 2t + 1
@@ -323,8 +230,7 @@ nvfp4_qmv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                     break;
                 }
                 if (kb * kConsumerWarps + warp < nblk)
-                    consume_stage_nvfp4(s_base + (uint32_t)(slot * kStage), code, sb, xq0 + (uint32_t)(kb * kCodes * 2),
-                                        acc);
+                    consume_stage_nvfp4(s_base + (uint32_t)(slot * kStage), ct, xq0 + (uint32_t)(kb * kCodes * 2), acc);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
             }

@@ -38,12 +38,14 @@
 #include "aq.h"
 #include "aq_internal.h"
 #include "aq_ptx.cuh"
+#include "nvfp4_consumer.cuh"
 #include "qmv_consumer.cuh"
 
 namespace aq {
 
 struct ChainRec {                // 128-byte aligned, as CUtensorMap is
-    CUtensorMap tw, ts, tb;       // codes (128-byte swizzle), scales and biases (32-byte swizzle)
+    CUtensorMap tw, ts, tb;       // codes (128-byte swizzle), scales and biases (swizzled boxes);
+                                  // NVFP4: E4M3 scales in ts (tb a copy of it)
     const __nv_bfloat16 *x;
     __nv_bfloat16 *y;
     int M, N, K, tiles;           // tiles = ceil(N / 32)
@@ -51,7 +53,8 @@ struct ChainRec {                // 128-byte aligned, as CUtensorMap is
     int tile_base;                // tiles of the preceding matmuls since the last dependent one
     int bits;                     // code width: 4 or 8
     int group;                    // first matmul of this one's dependency group (its counter)
-    int pad[4];
+    const float *gscale;          // NVFP4: the tensor's fp32 scale (device); else unused
+    int pad[2];
 };
 static_assert(sizeof(ChainRec) % 128 == 0, "records must stay 128-byte aligned");
 static_assert(offsetof(ChainRec, x) % 16 == 0 && offsetof(ChainRec, M) == offsetof(ChainRec, x) + 16 &&
@@ -156,8 +159,11 @@ __device__ __forceinline__ RecInfo load_info(const ChainRec *recs, const uint4 *
     return unpack_info(__ldg(p), __ldg(p + 1), __ldg(p + 2));
 }
 
-// BITS: code width of every matmul of the chain (4 or 8).
-template <int BITS, bool ONE_ROW>
+// BITS: code width of every matmul of the chain (4 or 8); NV: every matmul
+// holds NVFP4 weights (BITS = 4: same stage geometry, E4M3 block scales in
+// place of the scale and bias boxes, no fold, the tensor scale applied by the
+// reducer).
+template <int BITS, bool ONE_ROW, bool NV = false>
 __global__ void __launch_bounds__(kThreads, 1)
 qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_bytes, int max_m,
                  unsigned long long timeout_ns, int *status) {
@@ -247,10 +253,17 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
                         const uint32_t dst = s_base + slot * kStageBytes;
                         const uint32_t fb = bar_full + 8 * slot;
                         // one copy of the stage's codes (chunks past the row's end read as zeros)
-                        mbar_expect_tx(fb, (uint32_t)(kCodesBytes + 2 * kRows * SG * 2));
-                        tma_load_3d(dst, &rec->tw, 0, tile * kRows, kb * kBoxes, fb, pol);
-                        tma_load_2d(dst + kCodesBytes, &rec->ts, kb * SG, tile * kRows, fb, pol);
-                        tma_load_2d(dst + kCodesBytes + kSBRegion, &rec->tb, kb * SG, tile * kRows, fb, pol);
+                        if (NV) {
+                            // and one box of E4M3 scales: 128 bytes x 32 rows
+                            mbar_expect_tx(fb, (uint32_t)kNvStage);
+                            tma_load_3d(dst, &rec->tw, 0, tile * kRows, kb * kBoxes, fb, pol);
+                            tma_load_2d(dst + kCodesBytes, &rec->ts, kb * (kNvCodes / 16), tile * kRows, fb, pol);
+                        } else {
+                            mbar_expect_tx(fb, (uint32_t)(kCodesBytes + 2 * kRows * SG * 2));
+                            tma_load_3d(dst, &rec->tw, 0, tile * kRows, kb * kBoxes, fb, pol);
+                            tma_load_2d(dst + kCodesBytes, &rec->ts, kb * SG, tile * kRows, fb, pol);
+                            tma_load_2d(dst + kCodesBytes + kSBRegion, &rec->tb, kb * SG, tile * kRows, fb, pol);
+                        }
                         ++issued;
                     }
                 }
@@ -294,8 +307,14 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
                 ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
             }
             const int first = (cta - cur.tile_base % ncta + ncta) % ncta;
+            float yscale = 1.f;
+            if (NV && first < cur.T) {
+                const float *gs = recs[jm].gscale;
+                yscale = __ldg(gs);
+            }
             for (int tile = first; tile < cur.T && ok; tile += ncta, ++pending, ++tcount)
-                ok = reduce_tile<ONE_ROW>(tc, tcount, tile, cur.M, cur.N, cur.y, lane, timeout_ns, abort_flag);
+                ok = reduce_tile<ONE_ROW>(tc, tcount, tile, cur.M, cur.N, cur.y, lane, timeout_ns, abort_flag, nullptr,
+                                          0, 1, yscale);
             const bool group_ends = jm + 1 == count || !(nxt.flags & AQ_CHAIN_INDEPENDENT);
             if (ok && group_ends && pending > 0 && lane == 0) {
                 // every lane's y stores precede this (reduce_tile ends with __syncwarp);
@@ -339,7 +358,35 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
             prev_K = K;
             prev_bits = cur.bits;
 
-            {
+            if (NV) {
+                const int nblk = K / 128;
+                const int KB = (K + kNvCodes - 1) / kNvCodes;
+                if (new_x && ok) stage_x_nv_warp<ONE_ROW>(xs, cur.x, M, K, warp, lane, inv);
+                NvThread ct;
+                nv_consumer_init(ct, warp, lane);
+                // the lane's x: row lane/4 (B column lane/4), fragment t = lane % 4
+                const int M1 = ONE_ROW ? 1 : M, xrow = ONE_ROW ? 0 : ((lane >> 2) < M1 ? (lane >> 2) : M1 - 1);
+                const uint32_t xq = xs.xq + (uint32_t)(warp * xs.wq + xrow * xw_row_bytes(M1, KB, 4) + (lane & 3) * 8);
+                const int first = (cta - cur.tile_base % ncta + ncta) % ncta;
+                for (int tile = first; tile < T && ok; tile += ncta) {
+                    for (int kb = 0; kb < KB; ++kb, ++item) {
+                        const int slot = item % NS;
+                        const uint32_t phase = (uint32_t)(item / NS) & 1u;
+                        if (!mbar_wait_for(bar_full + 8 * slot, phase, timeout_ns, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        if (kb * kConsumerWarps + warp < nblk)
+                            consume_stage_nvfp4(s_base + (uint32_t)(slot * kStageBytes), ct, xq + (uint32_t)(kb * 256), acc);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+                    }
+                    if (!ok) break;
+                    ok = deposit_tile<ONE_ROW>(tc, acc, tcount, M, warp, lane, lane >> 2, inv, timeout_ns,
+                                               abort_flag);
+                    ++tcount;
+                }
+            } else {
                 using Gm = Geo<BITS>;
                 const int nblk = K / Gm::kWarpCodes;
                 const int KB = (K + Gm::kStageCodes - 1) / Gm::kStageCodes;
@@ -406,7 +453,7 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint6
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 constexpr int kMaxDevices = 64;
-std::atomic<int> g_attr_done[4][kMaxDevices];
+std::atomic<int> g_attr_done[6][kMaxDevices];
 std::atomic<int> g_sms[kMaxDevices];
 
 size_t records_bytes(int count) { return (size_t)count * sizeof(ChainRec); }
@@ -421,26 +468,37 @@ size_t chain_workspace_bytes(int count) {
 
 namespace {
 
+// The chain's weight format: affine codes of 4 or 8 bits in groups of 64, or
+// NVFP4 (group size 16: E2M1 codes, E4M3 block scales, a tensor scale).
+bool chain_format_ok(int group_size, int bits) {
+    return (group_size == 64 && (bits == 4 || bits == 8)) || (group_size == 16 && bits == 4);
+}
+
 // Validates the descriptors (host only, no CUDA call).
 aq_status chain_validate(const aq_matmul_desc *descs, int count, int group_size, int bits) {
-    if ((bits != 4 && bits != 8) || group_size != 64) return AQ_ERR_UNSUPPORTED;
+    if (!chain_format_ok(group_size, bits)) return AQ_ERR_UNSUPPORTED;
+    const bool nv = group_size == 16;
     for (int i = 0; i < count; ++i) {
         const aq_matmul_desc &d = descs[i];
-        if (d.M < 1 || d.N < 1 || d.K < 1 || d.K % 64) return AQ_ERR_INVALID_ARG;
+        if (d.M < 1 || d.N < 1 || d.K < 1 || d.K % group_size) return AQ_ERR_INVALID_ARG;
         if (d.flags & ~(int64_t)(AQ_CHAIN_INDEPENDENT | AQ_CHAIN_DEBUG_SKIP_COPY)) return AQ_ERR_INVALID_ARG;
         if (!d.x || !d.w_packed || !d.scales || !d.biases || !d.y) return AQ_ERR_INVALID_ARG;
-        if (d.M > 8 || d.K % 512 || d.K > (int64_t)1 << 20 || d.N > (int64_t)1 << 30) return AQ_ERR_UNSUPPORTED;
+        // affine: K in whole 512-code chunks (16-byte rows of scales); NVFP4: 256 (16-byte scale rows)
+        if (d.M > 8 || d.K % (nv ? 256 : 512) || d.K > (int64_t)1 << 20 || d.N > (int64_t)1 << 30)
+            return AQ_ERR_UNSUPPORTED;
         if (x_stage_bytes((int)d.M, (int)d.K, bits) > kMaxXBytes) return AQ_ERR_UNSUPPORTED;
-        if (!aligned(d.x, 16) || !aligned(d.w_packed, 16) || !aligned(d.scales, 16) || !aligned(d.biases, 16) ||
-            !aligned(d.y, 2))
+        if (!aligned(d.x, 16) || !aligned(d.w_packed, 16) || !aligned(d.scales, 16) ||
+            !aligned(d.biases, nv ? 4 : 16) || !aligned(d.y, 2))
             return AQ_ERR_ALIGNMENT;
     }
     return AQ_OK;
 }
 
 // Encodes validated descriptors into host records and fills the plan's sizes.
-aq_status chain_encode(const aq_matmul_desc *descs, int count, int bits, ChainRec *recs, aq_chain_plan *plan) {
+aq_status chain_encode(const aq_matmul_desc *descs, int count, int group_size, int bits, ChainRec *recs,
+                       aq_chain_plan *plan) {
     if (!encode_fn()) return AQ_ERR_UNSUPPORTED;
+    const bool nv = group_size == 16;
     int x_bytes = 16;
     bool one_row = true;
     for (int i = 0; i < count; ++i) {
@@ -453,10 +511,19 @@ aq_status chain_encode(const aq_matmul_desc *descs, int count, int bits, ChainRe
         // 32 for 8-bit)
         const uint32_t sg = (uint32_t)stage_groups(bits);
         const CUtensorMapSwizzle sbs = bits == 8 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
-        if (!encode_codes_3d(&r.tw, d.w_packed, K * bits / 8, N) ||
-            !encode_2d(&r.ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, d.scales, G, N, G * 2, sg, kRows, sbs) ||
-            !encode_2d(&r.tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, d.biases, G, N, G * 2, sg, kRows, sbs))
+        if (nv) {
+            // NVFP4: E4M3 scales [N][K/16] bytes, one 128-byte x 32-row box per stage (128-byte swizzle)
+            if (!encode_codes_3d(&r.tw, d.w_packed, K / 2, N) ||
+                !encode_2d(&r.ts, CU_TENSOR_MAP_DATA_TYPE_UINT8, d.scales, K / 16, N, K / 16, kNvCodes / 16, kRows,
+                           CU_TENSOR_MAP_SWIZZLE_128B))
+                return AQ_ERR_INVALID_ARG;
+            r.tb = r.ts;   // a valid map in the unused slot (the producer acquires all three)
+            r.gscale = static_cast<const float *>(d.biases);
+        } else if (!encode_codes_3d(&r.tw, d.w_packed, K * bits / 8, N) ||
+                   !encode_2d(&r.ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, d.scales, G, N, G * 2, sg, kRows, sbs) ||
+                   !encode_2d(&r.tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, d.biases, G, N, G * 2, sg, kRows, sbs)) {
             return AQ_ERR_INVALID_ARG;
+        }
         r.x = static_cast<const __nv_bfloat16 *>(d.x);
         r.y = static_cast<__nv_bfloat16 *>(d.y);
         r.M = (int)d.M;
@@ -475,6 +542,7 @@ aq_status chain_encode(const aq_matmul_desc *descs, int count, int bits, ChainRe
     plan->x_bytes = (x_bytes + 15) & ~15;
     plan->one_row = one_row ? 1 : 0;
     plan->reserved[0] = bits;   // code width of the chain (selects the kernel)
+    plan->reserved[2] = nv ? 1 : 0;   // NVFP4 weights
     for (int i = 0; i < count; ++i)
         if (descs[i].flags & AQ_CHAIN_DEBUG_SKIP_COPY) plan->reserved[1] = 1;   // the test hook: short waits
     return AQ_OK;
@@ -489,13 +557,13 @@ aq_status chain_prepare(const aq_matmul_desc *descs, int count, int group_size, 
     std::memset(plan, 0, sizeof *plan);
     if (count == 0) return AQ_OK;
     if (!descs || !workspace) return AQ_ERR_INVALID_ARG;
-    if ((bits != 4 && bits != 8) || group_size != 64) return AQ_ERR_UNSUPPORTED;
+    if (!chain_format_ok(group_size, bits)) return AQ_ERR_UNSUPPORTED;
     if (workspace_bytes < chain_workspace_bytes(count)) return AQ_ERR_INVALID_ARG;
     if (!aligned(workspace, 128)) return AQ_ERR_ALIGNMENT;
     aq_status st = chain_validate(descs, count, group_size, bits);  // before any CUDA call
     if (st != AQ_OK) return st;
     std::vector<ChainRec> recs((size_t)count);
-    st = chain_encode(descs, count, bits, recs.data(), plan);
+    st = chain_encode(descs, count, group_size, bits, recs.data(), plan);
     if (st != AQ_OK) return st;
     *err = cudaMemcpy(workspace, recs.data(), records_bytes(count), cudaMemcpyHostToDevice);
     if (*err != cudaSuccess) {
@@ -523,10 +591,11 @@ cudaError_t chain_run(const aq_chain_plan *plan, uint64_t timeout_ns, int *statu
     const ChainLayout L = chain_layout(plan->x_bytes, max_m);
     const int smem = L.total + 1024;
     const bool one = plan->one_row != 0;
-    const bool eight = plan->reserved[0] == 8;
-    auto kern = eight ? (one ? qmv_chain_kernel<8, true> : qmv_chain_kernel<8, false>)
-                      : (one ? qmv_chain_kernel<4, true> : qmv_chain_kernel<4, false>);
-    const int ki = 2 * (int)eight + (int)one;
+    const bool eight = plan->reserved[0] == 8, nv = plan->reserved[2] != 0;
+    auto kern = nv      ? (one ? qmv_chain_kernel<4, true, true> : qmv_chain_kernel<4, false, true>)
+                : eight ? (one ? qmv_chain_kernel<8, true> : qmv_chain_kernel<8, false>)
+                        : (one ? qmv_chain_kernel<4, true> : qmv_chain_kernel<4, false>);
+    const int ki = nv ? 4 + (int)one : 2 * (int)eight + (int)one;
     if (!g_attr_done[ki][dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemLimit);
@@ -604,7 +673,7 @@ aq_status chain_run_static(const aq_matmul_desc *descs, int count, int group_siz
     // (one call's kernel running the other's records).  So the lock covers
     // all three.
     std::lock_guard<std::mutex> lock(g_static_host_mutex);
-    st = chain_encode(descs, count, bits, g_static_host_recs, &plan);
+    st = chain_encode(descs, count, group_size, bits, g_static_host_recs, &plan);
     if (st != AQ_OK) return st;
     // from pageable memory: returns once the records are staged (which may
     // mean waiting for the stream's earlier work), so the host array may be

@@ -161,14 +161,22 @@ aq_status aq_pack_ref(const uint8_t *codes, int64_t N, int64_t K, int bits, uint
  * next matmuls keep streaming.
  *
  * Each descriptor follows aq_matmul_bf16's definition, with the limits of the
- * weight-streaming kernel: 1 <= M <= 8, K a multiple of 512, M*K <= 16384,
- * x, w_packed, scales and biases 16-byte aligned, y 2-byte aligned.
+ * weight-streaming kernel: 1 <= M <= 8, K a multiple of 512, M*K <= 16384
+ * (K rounded up to 2048 codes for 4-bit codes, 1024 for 8-bit), x, w_packed,
+ * scales and biases 16-byte aligned, y 2-byte aligned.
+ *
+ * NVFP4 chains (group_size 16, bits 4): every matmul follows
+ * aq_matmul_nvfp4_bf16's definition; `scales` is then the uint8 [N, K/16]
+ * E4M3 block scales and `biases` the device address of the tensor's fp32
+ * global scale (one float, 4-byte aligned, read by the kernel at run time).
+ * Limits: 1 <= M <= 8, K a multiple of 256, M*K <= 16384 (K rounded up to
+ * 2048), x, w_packed and scales 16-byte aligned.  A chain holds one format.
  */
 typedef struct aq_matmul_desc {
     const void *x;            /* bf16 [M, K], device */
     const uint32_t *w_packed; /* uint32 [N, K/8], device */
-    const void *scales;       /* bf16 [N, K/64], device */
-    const void *biases;       /* bf16 [N, K/64], device */
+    const void *scales;       /* bf16 [N, K/64], device (NVFP4: uint8 E4M3 [N, K/16]) */
+    const void *biases;       /* bf16 [N, K/64], device (NVFP4: const float *, the global scale) */
     void *y;                  /* bf16 [M, N], device, written */
     int64_t M, N, K;
     int64_t flags;            /* 0, AQ_CHAIN_INDEPENDENT, AQ_CHAIN_DEBUG_SKIP_COPY (test hook) */

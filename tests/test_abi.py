@@ -125,6 +125,26 @@ def test_chain_prepare_validation(kw, expect):
     assert aq.aq_chain_prepare(arr, 2, 64, 4, A, nbytes, plan) == expect
 
 
+@pytest.mark.parametrize("kw,expect", [
+    (dict(K=256 + 16), aq.AQ_ERR_UNSUPPORTED),    # not a multiple of 256
+    (dict(K=40), aq.AQ_ERR_INVALID_ARG),          # not a multiple of 16
+    (dict(M=9), aq.AQ_ERR_UNSUPPORTED),
+    (dict(M=2, K=8192 + 256), aq.AQ_ERR_UNSUPPORTED),   # K rounds up to 10240: M*K beyond the staged-x limit
+    (dict(biases=A + 2), aq.AQ_ERR_ALIGNMENT),    # the global scale: 4-byte aligned
+    (dict(scales=A + 8), aq.AQ_ERR_ALIGNMENT),
+    (dict(biases=None), aq.AQ_ERR_INVALID_ARG),
+])
+def test_chain_prepare_validation_nvfp4(kw, expect):
+    """NVFP4 chains (group size 16, 4-bit): K a multiple of 256, scales 16-byte
+    aligned, `biases` the 4-byte aligned address of the global scale."""
+    arr = (aq.MatmulDesc * 2)(_desc(K=1024, biases=A + 4), _desc(**{"K": 1024, **kw}))
+    plan = aq.ChainPlan()
+    nbytes = aq.aq_chain_workspace_bytes(2)
+    assert aq.aq_chain_prepare(arr, 2, 16, 4, A, nbytes, plan) == expect
+    assert aq.aq_chain_prepare(arr, 2, 16, 8, A, nbytes, plan) == aq.AQ_ERR_UNSUPPORTED   # NVFP4 is 4-bit
+    assert aq.aq_chain_prepare(arr, 2, 32, 4, A, nbytes, plan) == aq.AQ_ERR_UNSUPPORTED
+
+
 def test_chain_workspace_and_plan_checks():
     assert aq.aq_chain_workspace_bytes(0) == 0
     assert aq.aq_chain_workspace_bytes(225) == 225 * 512 + 1024

@@ -8,7 +8,7 @@ import affine_bit_quantized_gb300 as aq
 import oracle
 from affine_bit_quantized_gb300 import _build, synth
 
-from ._helpers import assert_parity, from_dev_bf16, to_dev_bf16, upload
+from ._helpers import assert_parity, from_dev_bf16, to_dev_bf16, to_dev_u32, upload
 
 pytestmark = pytest.mark.gpu
 
@@ -221,3 +221,80 @@ def test_chain_bounded_wait_timeout_reports_status(dev):
     for (x, w, t), (M, N, K) in zip(mats, shapes):
         _, ref = oracle.matmul(x, w.w_packed, w.scales, w.biases, M, N, K)
         assert_parity(from_dev_bf16(t[4]), ref, what=f"chain after timeout M={M} N={N} K={K}")
+
+
+# ---------------------------------------------------------------- NVFP4 chains (group size 16)
+
+def _nv_upload(w, dev):
+    import torch
+    wt = to_dev_u32(w.w_packed, dev)
+    st = torch.from_numpy(np.ascontiguousarray(w.scales)).to(dev)
+    gs = torch.tensor([w.global_scale], dtype=torch.float32, device=dev)
+    return wt, st, gs
+
+
+@pytest.mark.parametrize("shapes", [
+    [(1, 64, 256)],
+    [(1, 4096, 4096), (1, 1024, 4096), (1, 14336, 4096), (1, 4096, 14336)],
+    [(1, 17, 1280), (2, 300, 2048), (1, 33, 16384), (4, 50, 2304), (8, 77, 2048), (3, 15, 768)],
+])
+def test_chain_nvfp4_parity(dev, shapes):
+    """A chain of NVFP4 matmuls (E2M1 codes, E4M3 block scales, the tensor
+    scale read from device memory): every output against the NVFP4 oracle, and
+    the same bits as single aq_matmul_nvfp4_bf16 calls."""
+    import torch
+    mats = []
+    for i, (M, N, K) in enumerate(shapes):
+        w = synth.make_nvfp4_weights(N, K, 1500 + i)
+        x = synth.make_x(M, K, 1500 + i)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        mats.append((x, w, (to_dev_bf16(x, dev), *_nv_upload(w, dev), y)))
+    chain = aq.Chain([m[2] for m in mats], group_size=16, bits=4)
+    for m in mats:
+        m[2][4].fill_(float("nan"))
+    chain.run()
+    torch.cuda.synchronize()
+    assert aq.aq_read_device_status(None) == aq.AQ_OK
+    for (x, w, t), (M, N, K) in zip(mats, shapes):
+        _, ref = oracle.nvfp4_matmul(x, w.w_packed, w.scales, w.global_scale, M, N, K)
+        assert_parity(from_dev_bf16(t[4]), ref, what=f"nvfp4 chain M={M} N={N} K={K}")
+        xt, wt, st, gs, y = t
+        assert torch.equal(y, aq.matmul_nvfp4(xt, wt, st, w.global_scale)), f"M={M} N={N} K={K}"
+
+
+def test_chain_nvfp4_dependencies_and_shared_x(dev):
+    """NVFP4 chain with a dependent matmul reading the previous output and
+    independent ones sharing an x (k, v after q; up after gate), two rows of x.
+    Each output matches the oracle on the input it actually read, separate
+    calls bit for bit, and the tensor scale is taken from device memory at run
+    time (changing it changes the next run's outputs)."""
+    import torch
+    M, K = 2, 2048
+    plan = [("q", 2048, K, "x"), ("k", 512, K, "x"), ("v", 512, K, "x"), ("o", 2048, 2048, "q"),
+            ("gate", 1536, 2048, "o"), ("up", 1536, 2048, "o"), ("down", 1000, 1536, "gate")]
+    x0 = to_dev_bf16(synth.make_x(M, K, 1600), dev)
+    items, indep, ws, outs = [], [], [], {"x": x0}
+    for i, (name, N, Kin, src) in enumerate(plan):
+        w = synth.make_nvfp4_weights(N, Kin, 1610 + i)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        items.append((outs[src], *_nv_upload(w, dev), y))
+        indep.append(name in ("k", "v", "up"))
+        outs[name] = y
+        ws.append(w)
+    chain = aq.Chain(items, group_size=16, bits=4, independent=indep)
+    for rep in range(2):
+        for it in items:
+            it[4].fill_(float("nan"))
+        chain.run()
+        torch.cuda.synchronize()
+        assert aq.aq_read_device_status(None) == aq.AQ_OK
+        for i, ((xin, wt, st, gs, y), w) in enumerate(zip(items, ws)):
+            scale = float(gs.item())
+            Kin = w.K
+            xh = from_dev_bf16(xin).reshape(M, Kin)
+            _, ref = oracle.nvfp4_matmul(xh, w.w_packed, w.scales, scale, M, w.N, Kin)
+            assert_parity(from_dev_bf16(y), ref, what=f"{plan[i][0]} (run {rep})")
+            assert torch.equal(y, aq.matmul_nvfp4(xin, wt, st, scale)), plan[i][0]
+        # the second run reads new tensor scales from the same device floats
+        for it in items:
+            it[3].mul_(0.5)
