@@ -87,11 +87,7 @@ aq_status validate(const void *x, const uint32_t *w, const void *s, const void *
     if (!x || !w || !s || !b) return AQ_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(w, 16) || !aligned(s, 2) || !aligned(b, 2) || !aligned(y, 2))
         return AQ_ERR_ALIGNMENT;
-    if (bits == 8) {
-        // 8-bit codes run on the TMA-fed kernels only (decode and tensor-core)
-        if (K % 512) return AQ_ERR_UNSUPPORTED;
-        if (!aligned(s, 16) || !aligned(b, 16)) return AQ_ERR_ALIGNMENT;
-    }
+    if (bits == 8 && (!aligned(s, 16) || !aligned(b, 16))) return AQ_ERR_ALIGNMENT;
     return AQ_OK;
 }
 
@@ -104,6 +100,7 @@ aq_status matmul_impl(const void *x, const uint32_t *w_packed, const void *scale
     if (flags & ~(unsigned)(AQ_FLAG_PDL | AQ_FLAG_DEBUG_SKIP_COPY)) return AQ_ERR_INVALID_ARG;
     aq_status st = validate(x, w_packed, scales, biases, y, M, N, K, group_size, bits);
     if (st != AQ_OK || M == 0 || N == 0) return st;
+    if (kernel == AQ_KERNEL_QMM && K % 512) return AQ_ERR_UNSUPPORTED;   // the tensor-core kernel's K step
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (K == 0) return record_cuda(cudaMemsetAsync(y, 0, (size_t)(M * N) * 2, cs));
 
@@ -144,10 +141,10 @@ aq_status matmul_impl(const void *x, const uint32_t *w_packed, const void *scale
         if (kernel == AQ_KERNEL_QMM || a.debug_skip_copy) return AQ_ERR_UNSUPPORTED;
     }
     if (bits == 8) {
-        // 8-bit codes have no general decode kernel: the TMA-fed one, in launches
-        // of up to 16 rows of x
+        // 8-bit codes: the TMA-fed decode kernel in launches of up to 16 rows of x
+        // wherever it applies (K a multiple of 512); else the general kernel below
         st = AQ_OK;
-        return tma_rows(kQmvMaxRows, &st) ? st : AQ_ERR_UNSUPPORTED;
+        if (tma_rows(kQmvMaxRows, &st)) return st;
     }
     if (M <= kQmvMaxRows && kernel != AQ_KERNEL_QMM) {
         a.M = M;

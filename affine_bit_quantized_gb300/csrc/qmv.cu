@@ -24,15 +24,23 @@
 // per-group sums of x in the same instruction; a tile therefore covers 15
 // weight rows.
 //
+// 8-bit codes (the general path for K that the TMA-fed kernels do not take,
+// i.e. K not a multiple of 512): a code q = 16 h + l does not fit the 8-bit
+// significand of bf16 as 128 + q, so each code pair goes through the MMA twice,
+// as 128 + l and as 128 + h (one OR each), and the fold becomes
+//   y[m,n] = sum_g scale * (D_l + 16 D_h) + (bias - 17 * 128 * scale) * X.
+//
 // Decomposition: one CTA per 15-row tile; its warps split K into chunks of
-// 512 (8 groups), each warp first issuing all loads of its chunk (16 x 8-byte
-// code loads per thread) and only then waiting for the preceding kernel
+// 512 codes (8 groups; 4 groups for 8-bit codes), each warp first issuing all
+// loads of its chunk (16 code loads of 8 bytes per thread for 4-bit codes, 8
+// of 16 bytes for 8-bit) and only then waiting for the preceding kernel
 // (programmatic dependent launch) before reading x.  Partial sums are combined
 // across warps in shared memory in a fixed order, so results are
 // deterministic.
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "aq_internal.h"
 
@@ -40,7 +48,8 @@ namespace aq {
 namespace {
 
 constexpr int kTileRows = 15;             // weight rows per CTA; MMA row 15 carries ones
-constexpr int kChunkGroups = 8;           // groups of 64 codes per warp chunk (512 k)
+template <int BITS>
+__host__ __device__ constexpr int chunk_groups() { return BITS == 4 ? 8 : 4; }   // groups of 64 codes per warp chunk
 constexpr int kMaxWarps = 8;
 constexpr uint32_t kOnes = 0x3F803F80u;   // bf16x2 (1.0, 1.0)
 constexpr uint32_t kMagic = 0x43004300u;  // bf16x2 (128.0, 128.0)
@@ -56,6 +65,13 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t w4, int b) {
     return (__byte_perm(w, w4, sel) & 0x000F000Fu) | kMagic;
 }
 
+// 8-bit codes: bf16x2 (128 + v[2b], 128 + v[2b+1]) of the low nibbles v of
+// bytes 2b and 2b+1 of w (pass w >> 4 for the high nibbles).
+__device__ __forceinline__ uint32_t nibble_pair8(uint32_t w, int b) {
+    const uint32_t sel = (uint32_t)(2 * b) | ((uint32_t)(2 * b + 1) << 8);
+    return (__byte_perm(w, 0u, sel) & 0x000F000Fu) | kMagic;
+}
+
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                uint32_t a3, uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -65,8 +81,9 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// MT = number of 8-column MMA tiles of x rows (1: M <= 8, 2: M <= 16).
-template <int MT>
+// MT = number of 8-column MMA tiles of x rows (1: M <= 8, 2: M <= 16); BITS:
+// code width (4 or 8).
+template <int MT, int BITS>
 __global__ void __launch_bounds__(kMaxWarps * 32)
 qmv_kernel(const __nv_bfloat16 *__restrict__ x, const uint32_t *__restrict__ w,
            const uint16_t *__restrict__ sc, const uint16_t *__restrict__ bi,
@@ -80,7 +97,9 @@ qmv_kernel(const __nv_bfloat16 *__restrict__ x, const uint32_t *__restrict__ w,
     const int j = lane & 3;     // thread in group: k-slot pair
     const int64_t n0 = (int64_t)blockIdx.x * kTileRows;
     const int G = K >> 6;
-    const int64_t words = K >> 3;
+    const int64_t words = (int64_t)K * BITS / 32;   // code words per row
+    constexpr int kChunkGroups = chunk_groups<BITS>();
+    using CodeVec = typename std::conditional<BITS == 4, uint2, uint4>::type;   // a lane's codes of a group
     const bool ones_lane = (gid == 7);  // its second A row is tile row 15: the ones row
     const int64_t r0 = n0 + gid, r1 = n0 + gid + 8;
     const bool v0 = r0 < N;
@@ -97,22 +116,25 @@ qmv_kernel(const __nv_bfloat16 *__restrict__ x, const uint32_t *__restrict__ w,
     const int nchunks = (G + kChunkGroups - 1) / kChunkGroups;
     for (int c = warp; c < nchunks; c += nwarps) {
         const int g0 = c * kChunkGroups;
-        uint2 q0[kChunkGroups], q1[kChunkGroups];
+        CodeVec q0[kChunkGroups], q1[kChunkGroups];
         uint32_t sb0[kChunkGroups], sb1[kChunkGroups];  // scale bits | bias bits << 16
 #pragma unroll
         for (int gi = 0; gi < kChunkGroups; ++gi) {
             const int g = g0 + gi;
             const bool ok = g < G;
-            q0[gi] = make_uint2(0u, 0u);
-            q1[gi] = make_uint2(0u, 0u);
+            q0[gi] = CodeVec{};
+            q1[gi] = CodeVec{};
             sb0[gi] = 0u;
             sb1[gi] = 0u;
+            // the lane's words of the group: 2j, 2j+1 of 8 (4-bit), 4j .. 4j+3 of 16 (8-bit)
+            constexpr int WPG = 2 * BITS;   // words per group
+            constexpr int WPL = WPG / 4;    // words per lane
             if (ok && v0) {
-                q0[gi] = __ldcs(reinterpret_cast<const uint2 *>(w + r0 * words + g * 8 + 2 * j));
+                q0[gi] = __ldcs(reinterpret_cast<const CodeVec *>(w + r0 * words + g * WPG + WPL * j));
                 sb0[gi] = (uint32_t)__ldcs(sc + r0 * G + g) | ((uint32_t)__ldcs(bi + r0 * G + g) << 16);
             }
             if (ok && v1) {
-                q1[gi] = __ldcs(reinterpret_cast<const uint2 *>(w + r1 * words + g * 8 + 2 * j));
+                q1[gi] = __ldcs(reinterpret_cast<const CodeVec *>(w + r1 * words + g * WPG + WPL * j));
                 sb1[gi] = (uint32_t)__ldcs(sc + r1 * G + g) | ((uint32_t)__ldcs(bi + r1 * G + g) << 16);
             }
         }
@@ -127,9 +149,16 @@ qmv_kernel(const __nv_bfloat16 *__restrict__ x, const uint32_t *__restrict__ w,
             for (int t = 0; t < MT; ++t)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) d[t][e] = 0.f;
+            float dh[MT][4];   // 8-bit codes: the high nibbles' products
+#pragma unroll
+            for (int t = 0; t < MT; ++t)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) dh[t][e] = 0.f;
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
-                const int kw = (g * 8 + 2 * j + i) * 8;  // first k of this thread's word
+                // the 8 consecutive k of x this step covers: the lane's word 2j + i
+                // (4-bit), or its words 4j + 2i and 4j + 2i + 1 (8-bit)
+                const int kw = BITS == 4 ? (g * 8 + 2 * j + i) * 8 : g * 64 + 16 * j + 8 * i;
                 uint4 X[MT];
 #pragma unroll
                 for (int t = 0; t < MT; ++t) {
@@ -137,25 +166,59 @@ qmv_kernel(const __nv_bfloat16 *__restrict__ x, const uint32_t *__restrict__ w,
                     X[t] = make_uint4(0u, 0u, 0u, 0u);
                     if (m < M) X[t] = __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)m * K + kw));
                 }
-                const uint32_t wa = i ? q0[gi].y : q0[gi].x;
-                const uint32_t wb = i ? q1[gi].y : q1[gi].x;
-                const uint32_t wa4 = wa >> 4, wb4 = wb >> 4;
+                if constexpr (BITS == 4) {
+                    const uint32_t wa = i ? q0[gi].y : q0[gi].x;
+                    const uint32_t wb = i ? q1[gi].y : q1[gi].x;
+                    const uint32_t wa4 = wa >> 4, wb4 = wb >> 4;
 #pragma unroll
-                for (int s = 0; s < 2; ++s) {
-                    const uint32_t a0 = code_pair(wa, wa4, 2 * s);
-                    const uint32_t a2 = code_pair(wa, wa4, 2 * s + 1);
-                    const uint32_t a1 = ones_lane ? kOnes : code_pair(wb, wb4, 2 * s);
-                    const uint32_t a3 = ones_lane ? kOnes : code_pair(wb, wb4, 2 * s + 1);
+                    for (int s = 0; s < 2; ++s) {
+                        const uint32_t a0 = code_pair(wa, wa4, 2 * s);
+                        const uint32_t a2 = code_pair(wa, wa4, 2 * s + 1);
+                        const uint32_t a1 = ones_lane ? kOnes : code_pair(wb, wb4, 2 * s);
+                        const uint32_t a3 = ones_lane ? kOnes : code_pair(wb, wb4, 2 * s + 1);
 #pragma unroll
-                    for (int t = 0; t < MT; ++t)
-                        mma_bf16_16816(d[t], a0, a1, a2, a3, s ? X[t].z : X[t].x, s ? X[t].w : X[t].y);
+                        for (int t = 0; t < MT; ++t)
+                            mma_bf16_16816(d[t], a0, a1, a2, a3, s ? X[t].z : X[t].x, s ? X[t].w : X[t].y);
+                    }
+                } else {
+#pragma unroll
+                    for (int s = 0; s < 2; ++s) {
+                        // word 4j + 2i + s: codes at k = kw + 4s .. kw + 4s + 3 (slots 2j, 2j+1, 2j+8, 2j+9)
+                        const uint32_t wa = i ? (s ? q0[gi].w : q0[gi].z) : (s ? q0[gi].y : q0[gi].x);
+                        const uint32_t wb = i ? (s ? q1[gi].w : q1[gi].z) : (s ? q1[gi].y : q1[gi].x);
+#pragma unroll
+                        for (int hn = 0; hn < 2; ++hn) {
+                            const uint32_t va = hn ? wa >> 4 : wa, vb = hn ? wb >> 4 : wb;
+                            const uint32_t a0 = nibble_pair8(va, 0);
+                            const uint32_t a2 = nibble_pair8(va, 1);
+                            const uint32_t a1 = ones_lane ? kOnes : nibble_pair8(vb, 0);
+                            const uint32_t a3 = ones_lane ? kOnes : nibble_pair8(vb, 1);
+#pragma unroll
+                            for (int t = 0; t < MT; ++t)
+                                mma_bf16_16816(hn ? dh[t] : d[t], a0, a1, a2, a3, s ? X[t].z : X[t].x,
+                                               s ? X[t].w : X[t].y);
+                        }
+                    }
                 }
             }
-            // fold: acc += scale * D + (bias - 128 * scale) * X
+            if constexpr (BITS == 8) {
+                // D = D_l + 16 D_h; the ones row of D_l alone gives X
+#pragma unroll
+                for (int t = 0; t < MT; ++t) {
+                    d[t][0] = fmaf(16.f, dh[t][0], d[t][0]);
+                    d[t][1] = fmaf(16.f, dh[t][1], d[t][1]);
+                    if (!ones_lane) {
+                        d[t][2] = fmaf(16.f, dh[t][2], d[t][2]);
+                        d[t][3] = fmaf(16.f, dh[t][3], d[t][3]);
+                    }
+                }
+            }
+            // fold: acc += scale * D + (bias - c * scale) * X, c = 128 (4-bit) or 17 * 128 (8-bit)
+            constexpr float kOffset = BITS == 4 ? -128.f : -2176.f;
             const float s0 = bf16_bits_to_float(sb0[gi] & 0xFFFFu);
             const float s1 = bf16_bits_to_float(sb1[gi] & 0xFFFFu);
-            const float p0 = fmaf(-128.f, s0, bf16_bits_to_float(sb0[gi] >> 16));
-            const float p1 = fmaf(-128.f, s1, bf16_bits_to_float(sb1[gi] >> 16));
+            const float p0 = fmaf(kOffset, s0, bf16_bits_to_float(sb0[gi] >> 16));
+            const float p1 = fmaf(kOffset, s1, bf16_bits_to_float(sb1[gi] >> 16));
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
                 const float xs0 = __shfl_sync(0xFFFFFFFFu, d[t][2], 28 + j);
@@ -194,7 +257,8 @@ qmv_kernel(const __nv_bfloat16 *__restrict__ x, const uint32_t *__restrict__ w,
 
 cudaError_t launch_qmv(const MatmulArgs &a) {
     const int G = (int)(a.K / 64);
-    const int nchunks = (G + kChunkGroups - 1) / kChunkGroups;
+    const int cg = a.bits == 8 ? chunk_groups<8>() : chunk_groups<4>();
+    const int nchunks = (G + cg - 1) / cg;
     const int nwarps = std::min(kMaxWarps, nchunks);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((a.N + kTileRows - 1) / kTileRows));
@@ -209,8 +273,9 @@ cudaError_t launch_qmv(const MatmulArgs &a) {
     const auto *x = static_cast<const __nv_bfloat16 *>(a.x);
     auto *y = static_cast<__nv_bfloat16 *>(a.y);
     const int M = (int)a.M, N = (int)a.N, K = (int)a.K;
-    if (a.M <= 8) return cudaLaunchKernelEx(&cfg, qmv_kernel<1>, x, a.w, a.scales, a.biases, y, M, N, K);
-    return cudaLaunchKernelEx(&cfg, qmv_kernel<2>, x, a.w, a.scales, a.biases, y, M, N, K);
+    auto kern = a.bits == 8 ? (a.M <= 8 ? qmv_kernel<1, 8> : qmv_kernel<2, 8>)
+                            : (a.M <= 8 ? qmv_kernel<1, 4> : qmv_kernel<2, 4>);
+    return cudaLaunchKernelEx(&cfg, kern, x, a.w, a.scales, a.biases, y, M, N, K);
 }
 
 }  // namespace aq

@@ -66,14 +66,15 @@ typedef enum aq_status {
  * aq_matmul_bf16 does. */
 typedef enum aq_kernel {
     AQ_KERNEL_AUTO = 0,
-    AQ_KERNEL_QMV = 1, /* weight-streaming decode kernels, any M.  4-bit codes: the TMA-fed
-                          kernel wherever it applies (M <= 8, K % 512 == 0, 16-byte aligned
-                          scales and biases), else the general one in launches of 16 rows of
-                          x.  8-bit codes: the TMA-fed kernel in launches of 8 rows.
-                          AQ_KERNEL_AUTO chooses among these (and the GEMM kernel above 16
-                          rows) by measured speed; for 9..16 rows over a matrix of at least
-                          four 32-row tiles per SM it runs the TMA-fed kernel twice, on half
-                          the rows each. */
+    AQ_KERNEL_QMV = 1, /* weight-streaming decode kernels, any M.  The TMA-fed kernel
+                          wherever it applies (K % 512 == 0, 16-byte aligned scales and
+                          biases; up to 16 rows of x per launch, W streamed once per
+                          launch), else the general one in launches of 16 rows of x (both
+                          code widths).  AQ_KERNEL_AUTO chooses among these (and the GEMM
+                          kernel above 16 rows) by measured speed; for 9..16 rows whose x
+                          needs several K passes, over a matrix of at least four 32-row
+                          tiles per SM, it runs the TMA-fed kernel twice, on half the rows
+                          each. */
     AQ_KERNEL_QMM = 2  /* tensor-core GEMM kernel (tcgen05); any M >= 1 */
 } aq_kernel;
 
@@ -102,10 +103,11 @@ typedef enum aq_kernel {
  *               N == 0 launches nothing and returns AQ_OK; K == 0 writes y = 0.
  *   group_size  64.  Other values return AQ_ERR_UNSUPPORTED.
  *   bits        4 or 8.  Other values return AQ_ERR_UNSUPPORTED.  8-bit codes
- *               run on the TMA-fed kernels only (the decode kernel up to 16
- *               rows of x, the tensor-core kernel above): they need K a
- *               multiple of 512 and 16-byte aligned scales and biases
- *               (AQ_ERR_UNSUPPORTED / AQ_ERR_ALIGNMENT otherwise).
+ *               need 16-byte aligned scales and biases (AQ_ERR_ALIGNMENT
+ *               otherwise).  With K not a multiple of 512 (either width) the
+ *               TMA-fed and tensor-core kernels do not apply and every M runs
+ *               on the general decode kernel, in launches of 16 rows of x that
+ *               each stream W: correct, but slow for large M.
  *   Alignment   x and w_packed 16-byte aligned; scales, biases and y 2-byte
  *               aligned; otherwise AQ_ERR_ALIGNMENT.
  *   Aliasing    y must not overlap any input.

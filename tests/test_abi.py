@@ -36,8 +36,8 @@ def test_status_strings():
 
 @pytest.mark.parametrize("args,expect", [
     (dict(bits=3), aq.AQ_ERR_UNSUPPORTED),
-    (dict(bits=8), aq.AQ_ERR_UNSUPPORTED),           # 8-bit codes need K % 512 == 0 (here K = 128)
-    (dict(bits=8, K=1024, s=A + 2), aq.AQ_ERR_ALIGNMENT),  # ... and 16-byte aligned scales
+    (dict(bits=8, s=A + 2), aq.AQ_ERR_ALIGNMENT),    # 8-bit codes need 16-byte aligned scales
+    (dict(bits=8, K=1024, b=A + 8), aq.AQ_ERR_ALIGNMENT),  # ... and biases
     (dict(group_size=32), aq.AQ_ERR_UNSUPPORTED),
     (dict(group_size=128), aq.AQ_ERR_UNSUPPORTED),
     (dict(K=96), aq.AQ_ERR_INVALID_ARG),

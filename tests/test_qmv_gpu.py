@@ -275,13 +275,45 @@ def test_eight_bit_special_inputs(dev):
     assert np.all((got[3] & 0x7F80) == 0x7F80) and np.all(got[3] & 0x007F)
 
 
+@pytest.mark.parametrize("M,N,K", [
+    (1, 1, 64), (1, 100, 576), (2, 33, 1088), (3, 300, 4160), (8, 64, 14400), (9, 77, 576), (16, 40, 640),
+    (20, 129, 1088), (40, 65, 192),
+])
+def test_eight_bit_general_kernel(dev, M, N, K):
+    """8-bit codes with K not a multiple of 512: the general decode kernel (each
+    code pair through the MMA as its two nibbles), in launches of 16 rows of x
+    for any M, against the oracle; the explicit tensor-core choice is refused."""
+    check(dev, M, N, K, 1700 + M + N + K, bits=8, kernel="auto")
+    check(dev, M, N, K, 1800 + M + N + K, bits=8, kernel="qmv")
+    if M > 16:
+        w = synth.make_weights(N, K, 1, bits=8)
+        xt, wt, st, bt = upload(synth.make_x(M, K, 1), w, dev)
+        with pytest.raises(aq.AqError):
+            aq.matmul(xt, wt, st, bt, bits=8, kernel="qmm")
+
+
+def test_eight_bit_general_kernel_endpoints(dev):
+    """The general kernel's 8-bit fold: a one-hot x over a q = 0 column gives
+    the bias exactly (|bias| well above |scale| / 16 here, so the fold's fp32
+    rounding stays below half a bf16 ulp), and q = 255, 15, 16, 240 (both
+    nibbles, one nibble set) give scale * q + bias within the usual bound."""
+    N, K = 45, 576
+    w = synth.make_weights(N, K, 29, bits=8)
+    codes = oracle.unpack(w.w_packed, N, K, 8)
+    for col, q in ((3, 0), (100, 255), (200, 15), (300, 16), (575, 240)):
+        codes[:, col] = q
+    w.w_packed = oracle.pack(codes, 8)
+    x = np.zeros((5, K), np.uint16)
+    for r, col in enumerate((3, 100, 200, 300, 575)):
+        x[r, col] = 0x3F80
+    got = run(dev, x, w, kernel="qmv")
+    _, ref = oracle.matmul(x, w.w_packed, w.scales, w.biases, 5, N, K, bits=8)
+    assert np.array_equal(got[0], w.biases[:, 0])
+    assert_parity(got, ref, what="8-bit general kernel endpoints")
+
+
 def test_eight_bit_rejected_where_unsupported(dev):
     import torch
-    w = synth.make_weights(8, 576, 1, bits=8)
-    x = synth.make_x(1, 576, 1)
-    xt, wt, st, bt = upload(x, w, dev)
-    with pytest.raises(aq.AqError):
-        aq.matmul(xt, wt, st, bt, bits=8)            # K % 512 != 0: no 8-bit kernel
     w = synth.make_weights(8, 512, 1, bits=8)
     x = synth.make_x(32, 512, 1)
     xt, wt, st, bt = upload(x, w, dev)
