@@ -84,12 +84,20 @@ class DecodeStep:
 
     keep_host: keep the host copies of the weights (``host_weights[i]``, for a
     comparison with the oracle); ``host_layers`` limits that to some layers.
+
+    fmt: "affine4" (4-bit codes, groups of 64, bf16 scales and biases) or
+    "nvfp4" (E2M1 codes, E4M3 scales per 16 codes, one fp32 scale per matrix:
+    the same 0.5625 bytes per weight); a weight tuple is then (codes, E4M3
+    scales, the fp32 scale as a one-element device tensor).
     """
 
     def __init__(self, device, layers: int = synth.LLAMA8B_LAYERS, keep_host: bool = False, host_layers=None,
-                 threads: int | None = None):
+                 threads: int | None = None, fmt: str = "affine4"):
         import torch
 
+        if fmt not in ("affine4", "nvfp4"):
+            raise ValueError(f"unknown weight format {fmt!r}")
+        self.fmt = fmt
         self.device = device
         self.layers = layers
         self.mats = step_matrices(layers)
@@ -108,12 +116,21 @@ class DecodeStep:
 
         def gen(i):
             _, _, _, N, K, seed = self.mats[i]
+            if fmt == "nvfp4":
+                return i, synth.make_nvfp4_weights(N, K, seed)
             return i, synth.make_weights(N, K, seed)
 
+        self.global_scales = [1.0] * len(self.mats)
         for i, w in pool.map(gen, range(len(self.mats))):
-            self.weights[i] = (torch.from_numpy(w.w_packed.view(np.int32)).to(device),
-                               torch.from_numpy(w.scales.view(np.int16)).to(device),
-                               torch.from_numpy(w.biases.view(np.int16)).to(device))
+            if fmt == "nvfp4":
+                self.global_scales[i] = float(w.global_scale)
+                self.weights[i] = (torch.from_numpy(w.w_packed.view(np.int32)).to(device),
+                                   torch.from_numpy(w.scales).to(device),
+                                   torch.tensor([w.global_scale], dtype=torch.float32, device=device))
+            else:
+                self.weights[i] = (torch.from_numpy(w.w_packed.view(np.int32)).to(device),
+                                   torch.from_numpy(w.scales.view(np.int16)).to(device),
+                                   torch.from_numpy(w.biases.view(np.int16)).to(device))
             if keep_host and (host_layers is None or self.mats[i][0] in host_layers):
                 self.host_weights[i] = w
         pool.shutdown()
@@ -129,8 +146,8 @@ class DecodeStep:
         nbytes = aq.aq_chain_workspace_bytes(len(self.launches))
         self.chain_workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
         self.plan = aq.ChainPlan()
-        st = aq.aq_chain_prepare(self.descs, len(self.launches), 64, 4, self.chain_workspace.data_ptr(), nbytes,
-                                 self.plan)
+        st = aq.aq_chain_prepare(self.descs, len(self.launches), 16 if fmt == "nvfp4" else 64, 4,
+                                 self.chain_workspace.data_ptr(), nbytes, self.plan)
         if st != aq.AQ_OK:
             raise aq.AqError(st, "aq_chain_prepare")
 
@@ -154,14 +171,19 @@ class DecodeStep:
             raise aq.AqError(st, "aq_chain_run")
 
     def enqueue(self, stream_handle, sel=None, flags: int = aq.AQ_FLAG_PDL) -> None:
-        """One aq_matmul_bf16_ex launch per matmul (those in ``sel``, or all), in order."""
+        """One launch per matmul (those in ``sel``, or all), in order:
+        aq_matmul_bf16_ex, or aq_matmul_nvfp4_bf16 for NVFP4 weights."""
         lib = aq.load()
         for i, (xp, wp, sp, bp, yp, M, N, K) in enumerate(self.launches):
             if sel is not None and i not in sel:
                 continue
-            st = lib.aq_matmul_bf16_ex(xp, wp, sp, bp, yp, M, N, K, 64, 4, aq.AQ_KERNEL_AUTO, flags, stream_handle)
+            if self.fmt == "nvfp4":
+                st = lib.aq_matmul_nvfp4_bf16(xp, wp, sp, self.global_scales[i], yp, M, N, K, flags, stream_handle)
+            else:
+                st = lib.aq_matmul_bf16_ex(xp, wp, sp, bp, yp, M, N, K, 64, 4, aq.AQ_KERNEL_AUTO, flags,
+                                           stream_handle)
             if st != aq.AQ_OK:
-                raise aq.AqError(st, "aq_matmul_bf16_ex")
+                raise aq.AqError(st, "matmul launch")
 
     def capture_graph(self):
         """The step as a CUDA graph of one launch per matmul: k and v run as

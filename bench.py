@@ -635,6 +635,23 @@ def main():
                            "gbs": round(alg_bytes(1, N, K) / (us * 1e-6) / 1e9, 1)}
             del wsn, base
 
+        # ---- the whole step with NVFP4 weights (same shapes, same 0.5625 bytes per weight, its
+        # own seeds), as one chained launch like the headline step
+        ds_nv = DecodeStep(dev, args.layers, fmt="nvfp4")
+
+        def nv_step():
+            ds_nv.run_chain(cur.cuda_stream)
+
+        for _ in range(3):
+            nv_step()
+        ms_nv = time_steps(nv_step, max(3, min(args.steps, 20)))
+        if aq.aq_read_device_status(cur.cuda_stream) != aq.AQ_OK:
+            raise RuntimeError("a bounded device-side wait expired in the NVFP4 step")
+        nvfp4["step_chain"] = {"layers": args.layers, "ms_per_step": round(ms_nv, 5),
+                               "gbs": round(step_bytes / (ms_nv * 1e-3) / 1e9, 1),
+                               "frac": round(step_bytes / (ms_nv * 1e-3) / 1e9 / hbm_peak, 4)}
+        del ds_nv
+
         # ---- MoE prefill (expert-indexed matmul): Mixtral-8x7B-shaped experts, 2048 tokens routed
         # top-2 over 8 experts (4096 rows), one call = plan + row gather + tensor-core matmul
         moe = {}

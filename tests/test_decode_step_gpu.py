@@ -78,3 +78,34 @@ def test_step_is_repeatable_and_equals_the_graph_of_single_launches(step):
     graph.replay()
     torch.cuda.synchronize(step.device)
     assert torch.equal(step.y, first)
+
+
+def test_nvfp4_step_matches_the_oracle_and_single_launches():
+    """The same step with NVFP4 weights (the benchmark's NVFP4 step line), on
+    4 layers plus lm_head: every output of the chained launch against the
+    NVFP4 oracle, and the same bits as one aq_matmul_nvfp4_bf16 per matmul
+    (captured as a graph)."""
+    import torch
+    import affine_bit_quantized_gb300 as aq
+
+    _build.build_library()
+    dev = torch.device("cuda:0")
+    ds = decode_step.DecodeStep(dev, 4, keep_host=True, fmt="nvfp4")
+    assert ds.count == 4 * 7 + 1
+    stream = torch.cuda.current_stream(dev)
+    ds.y.fill_(0x7FC0)
+    ds.run_chain(stream.cuda_stream)
+    torch.cuda.synchronize(dev)
+    assert aq.aq_read_device_status(stream.cuda_stream) == aq.AQ_OK
+    y = _host_y(ds)
+    for i, (layer, j, name, N, K, seed) in enumerate(ds.mats):
+        w = ds.host_weights[i]
+        _, ref = oracle.nvfp4_matmul(ds.host_x_row(i), w.w_packed, w.scales, w.global_scale, 1, N, K)
+        got = y[ds.y_offsets[i]:ds.y_offsets[i] + N].reshape(1, N)
+        assert_parity(got, ref, what=f"nvfp4 layer {layer} {name}")
+    first = ds.y.clone()
+    graph = ds.capture_graph()
+    ds.y.fill_(0x7FC0)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    assert torch.equal(ds.y, first)
