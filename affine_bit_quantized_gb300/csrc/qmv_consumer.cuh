@@ -364,6 +364,23 @@ __device__ __forceinline__ void fold_group(const float (&d)[2][4], const float (
     }
 }
 
+// fold_group for one row block (rows gid and gid + 8: scales s0, s1 and
+// biases b0, b1), several rows of x: acc += s * (D - 1024 X') + b * Xs.
+__device__ __forceinline__ void fold_rows(const float (&d)[4], float s0, float s1, float b0, float b1, uint32_t xs0,
+                                          uint32_t xs1, float (&acc)[4]) {
+    const uint2 xa = lds64(xs0), xb = lds64(xs1);
+    const float2 xsum = make_float2(__uint_as_float(xa.x), __uint_as_float(xb.x));
+    const float2 xpr = make_float2(__uint_as_float(xa.y), __uint_as_float(xb.y));
+    const float2 t0 = fma2(make_float2(-1024.f, -1024.f), xpr, make_float2(d[0], d[1]));
+    const float2 t1 = fma2(make_float2(-1024.f, -1024.f), xpr, make_float2(d[2], d[3]));
+    const float2 a0 = fma2(make_float2(s0, s0), t0, fma2(make_float2(b0, b0), xsum, make_float2(acc[0], acc[1])));
+    const float2 a1 = fma2(make_float2(s1, s1), t1, fma2(make_float2(b1, b1), xsum, make_float2(acc[2], acc[3])));
+    acc[0] = a0.x;
+    acc[1] = a0.y;
+    acc[2] = a1.x;
+    acc[3] = a1.y;
+}
+
 // Adds the warp's block of stage `st` (32 rows x 128 bytes of codes; stage
 // index kb of the tile) to acc.  acc[h][*] are the MMA accumulator registers
 // of row block h: (row, column) = (gid, 2j), (gid, 2j+1), (gid+8, 2j),
@@ -462,30 +479,29 @@ __device__ __forceinline__ void consume_stage(uint32_t st, int kb, const Consume
 template <int BITS>
 __device__ __forceinline__ void consume_stage2(uint32_t st, int kb, const ConsumerThread &c, float (&acc)[2][2][4]) {
     using Gm = Geo<BITS>;
-    uint32_t sw[4], bw[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        sw[r] = lds32(st + kCodesBytes + c.sb + 8 * Gm::kSBRowBytes * r);
-        bw[r] = lds32(st + kCodesBytes + kSBRegion + c.sb + 8 * Gm::kSBRowBytes * r);
-    }
+    const uint32_t sbase = st + kCodesBytes + c.sb;   // scale word of row gid + 8r at + 8 * kSBRowBytes * r
     const uint32_t xo = (uint32_t)kb * (Gm::kGroupsPerWarp * 8);
     const uint32_t xq[2] = {c.xq + (uint32_t)kb * (Gm::kGroupsPerWarp * 128),
                             c.xq1 + (uint32_t)kb * (Gm::kGroupsPerWarp * 128)};
     const uint32_t xsa[2] = {c.xs0 + xo, c.xs2 + xo}, xsb[2] = {c.xs1 + xo, c.xs3 + xo};
     if (BITS == 4) {
+        // one row block h at a time, so that only its accumulators (two blocks of
+        // columns) are live beside acc: the whole stage's at once spill
 #pragma unroll
         for (int gl = 0; gl < 2; ++gl) {
             uint2 wr[4];
 #pragma unroll
             for (int r = 0; r < 4; ++r) wr[r] = lds64(st + c.code[gl] + 1024 * r);
-            float d[2][2][4];
+            uint4 X[2][2];   // [quad i][column block]
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                uint4 X[2];
+            for (int i = 0; i < 2; ++i)
 #pragma unroll
-                for (int nb = 0; nb < 2; ++nb) X[nb] = ldsm_x4(xq[nb] + gl * 128 + i * 64);
+                for (int nb = 0; nb < 2; ++nb) X[i][nb] = ldsm_x4(xq[nb] + gl * 128 + i * 64);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < 2; ++h) {
+                float d[2][4];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
                     const uint32_t wa = i ? wr[2 * h].y : wr[2 * h].x;
                     const uint32_t wb = i ? wr[2 * h + 1].y : wr[2 * h + 1].x;
                     const uint32_t ta = wa >> 8, tb = wb >> 8;
@@ -494,23 +510,32 @@ __device__ __forceinline__ void consume_stage2(uint32_t st, int kb, const Consum
 #pragma unroll
                     for (int nb = 0; nb < 2; ++nb) {
                         if (i == 0)
-                            mma_f16_16816_zc(d[nb][h], a0, a1, a2, a3, X[nb].x, X[nb].y);
+                            mma_f16_16816_zc(d[nb], a0, a1, a2, a3, X[i][nb].x, X[i][nb].y);
                         else
-                            mma_f16_16816(d[nb][h], a0, a1, a2, a3, X[nb].x, X[nb].y);
-                        mma_f16_16816(d[nb][h], b0, b1, b2, b3, X[nb].z, X[nb].w);
+                            mma_f16_16816(d[nb], a0, a1, a2, a3, X[i][nb].x, X[i][nb].y);
+                        mma_f16_16816(d[nb], b0, b1, b2, b3, X[i][nb].z, X[i][nb].w);
                     }
                 }
-            }
-            float sc[4], bi[4];
+                // this row block's scale and bias words, loaded here rather than
+                // held across the stage
+                const uint32_t s0 = lds32(sbase + 8 * Gm::kSBRowBytes * (2 * h));
+                const uint32_t s1 = lds32(sbase + 8 * Gm::kSBRowBytes * (2 * h + 1));
+                const uint32_t b0 = lds32(sbase + kSBRegion + 8 * Gm::kSBRowBytes * (2 * h));
+                const uint32_t b1 = lds32(sbase + kSBRegion + 8 * Gm::kSBRowBytes * (2 * h + 1));
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                sc[r] = gl ? bf16hi(sw[r]) : bf16lo(sw[r]);
-                bi[r] = gl ? bf16hi(bw[r]) : bf16lo(bw[r]);
+                for (int nb = 0; nb < 2; ++nb)
+                    fold_rows(d[nb], gl ? bf16hi(s0) : bf16lo(s0), gl ? bf16hi(s1) : bf16lo(s1),
+                              gl ? bf16hi(b0) : bf16lo(b0), gl ? bf16hi(b1) : bf16lo(b1), xsa[nb] + gl * 8,
+                              xsb[nb] + gl * 8, acc[nb][h]);
             }
-#pragma unroll
-            for (int nb = 0; nb < 2; ++nb) fold_group<false>(d[nb], sc, bi, xsa[nb] + gl * 8, xsb[nb] + gl * 8, acc[nb]);
         }
     } else {
+        uint32_t sw[4], bw[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            sw[r] = lds32(sbase + 8 * Gm::kSBRowBytes * r);
+            bw[r] = lds32(sbase + kSBRegion + 8 * Gm::kSBRowBytes * r);
+        }
         uint4 wr[4];
 #pragma unroll
         for (int r = 0; r < 4; ++r) wr[r] = lds128(st + c.code[0] + 1024 * r);
