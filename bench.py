@@ -320,7 +320,7 @@ def run_case_other(args):
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for name in ("qmv_chain.cu", "qmv_tma.cu", "qmv_consumer.cuh", "aq_ptx.cuh"):
+    for name in ("qmv_chain.cu", "qmv_tma.cu", "qmv_consumer.cuh", "nvfp4_consumer.cuh", "aq_ptx.cuh"):
         with open(os.path.join(ROOT, "affine_bit_quantized_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
