@@ -490,33 +490,45 @@ def main():
 
     def side_sections():
         """Per-matrix, small-batch, 8-bit, tensor-core, NVFP4 and MoE measurements beside the step."""
-        # ---- per-matrix kernel times (the 32 layer copies of each shape back to back)
-        per_matrix = {}
-        reps = 5
-        for j, (name, N, K) in enumerate(synth.LLAMA8B_LAYER + (synth.LLAMA8B_LM_HEAD,)):
-            sel = {i for i, m in enumerate(mats) if (m[2] == name)}
+        def sh():
+            """The stream the next launch goes to (the capture stream while a graph is captured)."""
+            return torch.cuda.current_stream(dev).cuda_stream
+
+        def graph_us(enqueue_all, n_calls, reps=5):
+            """Device time per call of n_calls launches, captured once as a CUDA graph and
+            replayed: launches with programmatic dependent launch, no host work in between (a
+            Python loop of single calls is bound by the host at these sizes)."""
             for _ in range(2):
-                enqueue(cur.cuda_stream, sel)
+                enqueue_all()
+            torch.cuda.synchronize(dev)
+            cap = torch.cuda.Stream(dev)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                enqueue_all()
+            g.replay()
             torch.cuda.synchronize(dev)
             e0.record(cur)
             for _ in range(reps):
-                enqueue(cur.cuda_stream, sel)
+                g.replay()
             e1.record(cur)
             e1.synchronize()
-            us = e0.elapsed_time(e1) * 1e3 / (reps * len(sel))
-            per_matrix[name] = {"N": N, "K": K, "us_per_call": round(us, 3),
-                                "gbs": round(alg_bytes(1, N, K) / (us * 1e-6) / 1e9, 1)}
+            del g
+            return e0.elapsed_time(e1) * 1e3 / (reps * n_calls)
 
         def time_calls(launch, n_calls, reps=5):
-            for i in range(2 * n_calls):
-                launch(i)
-            torch.cuda.synchronize(dev)
-            e0.record(cur)
-            for i in range(reps * n_calls):
-                launch(i)
-            e1.record(cur)
-            e1.synchronize()
-            return e0.elapsed_time(e1) * 1e3 / (reps * n_calls)
+            def enqueue_all():
+                for i in range(n_calls):
+                    launch(i)
+            return graph_us(enqueue_all, n_calls, reps)
+
+        # ---- per-matrix kernel times (the 32 layer copies of each shape back to back)
+        per_matrix = {}
+        for j, (name, N, K) in enumerate(synth.LLAMA8B_LAYER + (synth.LLAMA8B_LM_HEAD,)):
+            sel = {i for i, m in enumerate(mats) if (m[2] == name)}
+            reps = 5 if len(sel) > 1 else 20
+            us = graph_us(lambda sel=sel: enqueue(sh(), sel), len(sel), reps)
+            per_matrix[name] = {"N": N, "K": K, "us_per_call": round(us, 3),
+                                "gbs": round(alg_bytes(1, N, K) / (us * 1e-6) / 1e9, 1)}
 
         # ---- small batches (the multi-row decode path): M in {2, 4, 8, 16} over the layer shapes
         # and lm_head, on the step's copies (32 distinct weights per layer shape: no L2 reuse; the
@@ -532,7 +544,7 @@ def main():
                 def launch_sb(i, ws=ws, xb=xb, yb=yb, M=M, N=N, K=K):
                     wt, st_, bt = ws[i % len(ws)]
                     rc = lib.aq_matmul_bf16_ex(xb.data_ptr(), wt.data_ptr(), st_.data_ptr(), bt.data_ptr(), yb.data_ptr(),
-                                               M, N, K, 64, 4, aq.AQ_KERNEL_AUTO, aq.AQ_FLAG_PDL, cur.cuda_stream)
+                                               M, N, K, 64, 4, aq.AQ_KERNEL_AUTO, aq.AQ_FLAG_PDL, sh())
                     if rc != aq.AQ_OK:
                         raise aq.AqError(rc, "aq_matmul_bf16_ex")
 
@@ -540,24 +552,28 @@ def main():
                 small_batch[f"M{M}_{name}"] = {"M": M, "N": N, "K": K, "us_per_call": round(us, 3),
                                                "gbs": round(alg_bytes(M, N, K) / (us * 1e-6) / 1e9, 1)}
 
-        # ---- 8-bit codes (same shapes, M = 1): 4 device copies of each weight matrix cycled
+        def copies_for(nbytes):
+            """Distinct device copies of a matrix whose cycle spans at least 3 x L2 (129 MB)."""
+            return max(2, min(128, -(-3 * 129 * 2**20 // nbytes)))
+
+        # ---- 8-bit codes (same shapes, M = 1): device copies of each weight matrix cycled over >= 3 x L2
         eight_bit = {}
         for j, (name, N, K) in enumerate(synth.LLAMA8B_LAYER + (synth.LLAMA8B_LM_HEAD,)):
             w8 = synth.make_weights(N, K, synth.seed_for(6, 0, j), bits=8)
             base = (torch.from_numpy(w8.w_packed.view(np.int32)).to(dev), torch.from_numpy(w8.scales.view(np.int16)).to(dev),
                     torch.from_numpy(w8.biases.view(np.int16)).to(dev))
-            ws8 = [base] + [tuple(t.clone() for t in base) for _ in range(3)]
+            ws8 = [base] + [tuple(t.clone() for t in base) for _ in range(copies_for(N * K * 17 // 16) - 1)]
             x8 = torch.from_numpy(synth.make_x(1, K, synth.seed_for(6, 1, j)).view(np.int16)).to(dev)
             y8 = torch.empty((1, N), dtype=torch.int16, device=dev)
 
             def launch8(i, ws8=ws8, x8=x8, y8=y8, N=N, K=K):
                 wt, st_, bt = ws8[i % len(ws8)]
                 rc = lib.aq_matmul_bf16_ex(x8.data_ptr(), wt.data_ptr(), st_.data_ptr(), bt.data_ptr(), y8.data_ptr(),
-                                           1, N, K, 64, 8, aq.AQ_KERNEL_AUTO, aq.AQ_FLAG_PDL, cur.cuda_stream)
+                                           1, N, K, 64, 8, aq.AQ_KERNEL_AUTO, aq.AQ_FLAG_PDL, sh())
                 if rc != aq.AQ_OK:
                     raise aq.AqError(rc, "aq_matmul_bf16_ex")
 
-            us = time_calls(launch8, 8)
+            us = time_calls(launch8, len(ws8))
             eight_bit[name] = {"N": N, "K": K, "us_per_call": round(us, 3),
                                "gbs": round(alg_bytes(1, N, K, 8) / (us * 1e-6) / 1e9, 1)}
             del ws8, base
@@ -614,23 +630,23 @@ def main():
                 del ws
 
         # ---- NVFP4 weights (E2M1 codes, E4M3 scale per 16, fp32 tensor scale), M = 1, the step's shapes:
-        # 4 device copies of each matrix cycled (0.5625 B per weight, as the affine 4-bit format)
+        # device copies of each matrix cycled over >= 3 x L2 (0.5625 B per weight, as the affine 4-bit format)
         nvfp4 = {}
         for j, (name, N, K) in enumerate(synth.LLAMA8B_LAYER + (synth.LLAMA8B_LM_HEAD,)):
             wn = synth.make_nvfp4_weights(N, K, synth.seed_for(7, 0, j))
             base = (torch.from_numpy(wn.w_packed.view(np.int32)).to(dev), torch.from_numpy(wn.scales).to(dev))
-            wsn = [base] + [tuple(t.clone() for t in base) for _ in range(3)]
+            wsn = [base] + [tuple(t.clone() for t in base) for _ in range(copies_for(N * K * 9 // 16) - 1)]
             xn = torch.from_numpy(synth.make_x(1, K, synth.seed_for(7, 1, j)).view(np.int16)).to(dev)
             yn = torch.empty((1, N), dtype=torch.int16, device=dev)
 
             def launchn(i, wsn=wsn, xn=xn, yn=yn, N=N, K=K, g=wn.global_scale):
                 wt, st_ = wsn[i % len(wsn)]
                 rc = lib.aq_matmul_nvfp4_bf16(xn.data_ptr(), wt.data_ptr(), st_.data_ptr(), g, yn.data_ptr(), 1, N, K,
-                                              aq.AQ_FLAG_PDL, cur.cuda_stream)
+                                              aq.AQ_FLAG_PDL, sh())
                 if rc != aq.AQ_OK:
                     raise aq.AqError(rc, "aq_matmul_nvfp4_bf16")
 
-            us = time_calls(launchn, 8)
+            us = time_calls(launchn, len(wsn))
             nvfp4[name] = {"N": N, "K": K, "us_per_call": round(us, 3),
                            "gbs": round(alg_bytes(1, N, K) / (us * 1e-6) / 1e9, 1)}
             del wsn, base
