@@ -28,6 +28,7 @@ AQ_KERNEL_QMM = 2
 AQ_FLAG_PDL = 1
 AQ_FLAG_DEBUG_SKIP_COPY = 1 << 31
 AQ_CHAIN_INDEPENDENT = 1
+AQ_CHAIN_RELEASE = 2
 AQ_CHAIN_DEBUG_SKIP_COPY = 0x40000000
 
 _lock = threading.Lock()
@@ -153,7 +154,7 @@ def aq_chain_run(plan, stream) -> int:
     return load().aq_chain_run(ctypes.byref(plan), stream)
 
 
-def _chain_descs(items, group_size: int, bits: int, independent):
+def _chain_descs(items, group_size: int, bits: int, independent, release=None):
     """Checks (x, w_packed, scales, biases, y) tensors of a chain and returns
     their aq_matmul_desc array (at least one element).  group_size 16 is an
     NVFP4 chain: (x, w_packed, scales_e4m3 uint8 [N, K/16], global_scale
@@ -161,6 +162,8 @@ def _chain_descs(items, group_size: int, bits: int, independent):
     n = len(items)
     if independent is not None and len(independent) != n:
         raise ValueError(f"independent has {len(independent)} flags for {n} matmuls")
+    if release is not None and release is not True and len(release) != n:
+        raise ValueError(f"release has {len(release)} flags for {n} matmuls")
     arr = (MatmulDesc * max(n, 1))()
     named = []
     for i, (x, w, s, b, y) in enumerate(items):
@@ -182,6 +185,8 @@ def _chain_descs(items, group_size: int, bits: int, independent):
         _placed(items[0][0].device, named)
     for i, (x, w, s, b, y) in enumerate(items):
         flags = AQ_CHAIN_INDEPENDENT if (independent and independent[i]) else 0
+        if release is True or (release is not None and release[i]):
+            flags |= AQ_CHAIN_RELEASE
         arr[i] = MatmulDesc(x.data_ptr(), w.data_ptr(), s.data_ptr(), b.data_ptr(), y.data_ptr(), x.shape[0],
                             w.shape[0], x.shape[1], flags)
     return arr
@@ -193,11 +198,11 @@ class Chain:
     Each y_j is written before matmul j+1 reads its x, so an x may be an
     earlier y.  Holds the device workspace (a torch tensor) and the plan."""
 
-    def __init__(self, items, group_size: int = 64, bits: int = 4, independent=None):
+    def __init__(self, items, group_size: int = 64, bits: int = 4, independent=None, release=None):
         import torch
 
         n = len(items)
-        arr = _chain_descs(items, group_size, bits, independent)
+        arr = _chain_descs(items, group_size, bits, independent, release)
         self.items = items
         nbytes = aq_chain_workspace_bytes(n)
         dev = items[0][0].device if n else torch.device("cuda")
@@ -221,13 +226,14 @@ def aq_chain_run_static(descs, count, group_size, bits, stream) -> int:
     return load().aq_chain_run_static(descs, count, group_size, bits, stream)
 
 
-def chain_run_static(items, group_size: int = 64, bits: int = 4, independent=None, stream=None) -> None:
+def chain_run_static(items, group_size: int = 64, bits: int = 4, independent=None, stream=None,
+                     release=None) -> None:
     """A chain of matmuls over torch CUDA tensors, as Chain(...).run() gives it,
     through the entry point that allocates nothing (aq_chain_run_static; at
     most 256 matmuls).  The tensors are checked as Chain checks them."""
     import torch
 
-    arr = _chain_descs(items, group_size, bits, independent)
+    arr = _chain_descs(items, group_size, bits, independent, release)
     if stream is None:
         stream = torch.cuda.current_stream(items[0][0].device) if items else torch.cuda.current_stream()
     st = aq_chain_run_static(arr, len(items), group_size, bits, stream.cuda_stream)

@@ -49,7 +49,7 @@ struct ChainRec {                // 128-byte aligned, as CUtensorMap is
     const __nv_bfloat16 *x;
     __nv_bfloat16 *y;
     int M, N, K, tiles;           // tiles = ceil(N / 32)
-    int flags;                    // AQ_CHAIN_INDEPENDENT
+    int flags;                    // AQ_CHAIN_INDEPENDENT, and kRecRelease (set by the host)
     int tile_base;                // tiles of the preceding matmuls since the last dependent one
     int bits;                     // code width: 4 or 8
     int group;                    // first matmul of this one's dependency group (its counter)
@@ -57,6 +57,15 @@ struct ChainRec {                // 128-byte aligned, as CUtensorMap is
     int pad[2];
 };
 static_assert(sizeof(ChainRec) % 128 == 0, "records must stay 128-byte aligned");
+
+// Record flag set by the host on the last matmul of a dependency group whose
+// completion must be published with a GPU-scope release (and acquired by the
+// next group's poll): some later matmul of the chain reads or rewrites memory
+// that a matmul up to this group wrote, or rewrites memory one of them read.
+// Without it the group's completion counter is a relaxed atomic: the next
+// group still starts only after every tile of this one is stored, but no
+// memory fence waits for those stores to reach L2 (≈ 0.9 us per group).
+constexpr int kRecRelease = 0x10000000;
 static_assert(offsetof(ChainRec, x) % 16 == 0 && offsetof(ChainRec, M) == offsetof(ChainRec, x) + 16 &&
                   offsetof(ChainRec, flags) == offsetof(ChainRec, x) + 32 &&
                   offsetof(ChainRec, bits) == offsetof(ChainRec, x) + 40 &&
@@ -99,15 +108,25 @@ __host__ __device__ inline ChainLayout chain_layout(int x_bytes, int max_m) {
 __device__ __forceinline__ void red_release_gpu_add(int *p, int v) {
     asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+__device__ __forceinline__ void red_relaxed_gpu_add(int *p, int v) {
+    asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
-// Bounded wait until *p >= want (GPU scope, acquire); false on timeout or abort.
-__device__ __forceinline__ bool wait_count(const int *p, int want, uint64_t timeout_ns, const volatile int *abort_flag) {
+__device__ __forceinline__ int ld_relaxed_gpu(const int *p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+// Bounded wait until *p >= want (GPU scope; acquire when the group was
+// published with a release); false on timeout or abort.
+__device__ __forceinline__ bool wait_count(const int *p, int want, bool acquire, uint64_t timeout_ns,
+                                           const volatile int *abort_flag) {
     const uint64_t dl = global_timer() + timeout_ns;
-    while (ld_acquire_gpu(p) < want) {
+    while ((acquire ? ld_acquire_gpu(p) : ld_relaxed_gpu(p)) < want) {
         if (*abort_flag || global_timer() > dl) return false;
     }
     return true;
@@ -298,7 +317,8 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
                 if (lane == 0) {
                     // the previous group's tiles: its last matmul's tile_base counts the ones before it
                     const int want = prev.tile_base + prev.T;
-                    if (ok && !wait_count(done + prev.group, want, timeout_ns, abort_flag)) {
+                    if (ok && !wait_count(done + prev.group, want, (prev.flags & kRecRelease) != 0, timeout_ns,
+                                          abort_flag)) {
                         set_abort();
                         ok = false;
                     }
@@ -318,8 +338,12 @@ qmv_chain_kernel(const ChainRec *__restrict__ recs, int count, int *done, int x_
             const bool group_ends = jm + 1 == count || !(nxt.flags & AQ_CHAIN_INDEPENDENT);
             if (ok && group_ends && pending > 0 && lane == 0) {
                 // every lane's y stores precede this (reduce_tile ends with __syncwarp);
-                // the release makes them visible at GPU scope before the count
-                red_release_gpu_add(done + cur.group, pending);
+                // where a later matmul touches what this group wrote, the release
+                // makes them visible at GPU scope before the count
+                if (cur.flags & kRecRelease)
+                    red_release_gpu_add(done + cur.group, pending);
+                else
+                    red_relaxed_gpu_add(done + cur.group, pending);
             }
             if (group_ends) pending = 0;
             if (!ok && lane == 0) set_abort();
@@ -481,7 +505,8 @@ aq_status chain_validate(const aq_matmul_desc *descs, int count, int group_size,
     for (int i = 0; i < count; ++i) {
         const aq_matmul_desc &d = descs[i];
         if (d.M < 1 || d.N < 1 || d.K < 1 || d.K % group_size) return AQ_ERR_INVALID_ARG;
-        if (d.flags & ~(int64_t)(AQ_CHAIN_INDEPENDENT | AQ_CHAIN_DEBUG_SKIP_COPY)) return AQ_ERR_INVALID_ARG;
+        if (d.flags & ~(int64_t)(AQ_CHAIN_INDEPENDENT | AQ_CHAIN_RELEASE | AQ_CHAIN_DEBUG_SKIP_COPY))
+            return AQ_ERR_INVALID_ARG;
         if (!d.x || !d.w_packed || !d.scales || !d.biases || !d.y) return AQ_ERR_INVALID_ARG;
         // affine: K in whole 512-code chunks (16-byte rows of scales); NVFP4: 256 (16-byte scale rows)
         if (d.M > 8 || d.K % (nv ? 256 : 512) || d.K > (int64_t)1 << 20 || d.N > (int64_t)1 << 30)
@@ -492,6 +517,73 @@ aq_status chain_validate(const aq_matmul_desc *descs, int count, int group_size,
             return AQ_ERR_ALIGNMENT;
     }
     return AQ_OK;
+}
+
+// Byte ranges a matmul reads (x, codes, scales, biases or the NVFP4 tensor
+// scale) and writes (y).
+struct Footprint {
+    uintptr_t r[4][2];
+    uintptr_t w[2];
+};
+Footprint footprint(const aq_matmul_desc &d, int bits, bool nv) {
+    auto range = [](const void *p, uint64_t n, uintptr_t (&o)[2]) {
+        o[0] = reinterpret_cast<uintptr_t>(p);
+        o[1] = o[0] + n;
+    };
+    const uint64_t M = (uint64_t)d.M, N = (uint64_t)d.N, K = (uint64_t)d.K;
+    Footprint f;
+    range(d.x, M * K * 2, f.r[0]);
+    range(d.w_packed, N * K * (uint64_t)bits / 8, f.r[1]);
+    range(d.scales, nv ? N * K / 16 : N * (K / 64) * 2, f.r[2]);
+    range(d.biases, nv ? 4 : N * (K / 64) * 2, f.r[3]);
+    range(d.y, M * N * 2, f.w);
+    return f;
+}
+bool overlap(const uintptr_t (&a)[2], const uintptr_t (&b)[2]) { return a[0] < b[1] && b[0] < a[1]; }
+// True if matmul k (later) touches what matmul i (earlier) wrote, or writes what
+// i read: a read-after-write, write-after-write or write-after-read hazard
+// that the chain's ordering must also make visible in memory.
+bool hazard(const Footprint &i, const Footprint &k) {
+    if (overlap(i.w, k.w)) return true;
+    for (int a = 0; a < 4; ++a)
+        if (overlap(i.w, k.r[a]) || overlap(i.r[a], k.w)) return true;
+    return false;
+}
+
+// Marks, on the last matmul of each dependency group, whether its completion
+// is published with a release (kRecRelease): where a hazard pair (i, k), i <=
+// the group's last matmul < k, crosses it, or where the caller asks for it
+// (AQ_CHAIN_RELEASE on any of the group's matmuls).  Every group a hazard
+// crosses is marked, so the release / acquire pairs chain from i to k.  The
+// last group's completion is never awaited inside the chain (the kernel's
+// end orders it for later work).  Chains beyond kHazardScanMax matmuls are
+// not scanned: every group is published with a release.
+constexpr int kHazardScanMax = 4096;
+void mark_releases(const aq_matmul_desc *descs, int count, int bits, bool nv, ChainRec *recs) {
+    std::vector<int> cover((size_t)count + 1, 0);   // difference array over matmul positions
+    if (count > kHazardScanMax) {
+        cover[0] = 1;
+    } else {
+        std::vector<Footprint> fp((size_t)count);
+        for (int i = 0; i < count; ++i) fp[(size_t)i] = footprint(descs[i], bits, nv);
+        for (int i = 0; i < count; ++i)
+            for (int k = count - 1; k > i; --k)
+                if (hazard(fp[(size_t)i], fp[(size_t)k])) {
+                    ++cover[(size_t)i];
+                    --cover[(size_t)k];
+                    break;   // the latest k: its span [i, k) contains those of the earlier ones
+                }
+    }
+    int run = 0;
+    bool forced = false;
+    for (int j = 0; j < count; ++j) {
+        run += cover[(size_t)j];
+        forced = forced || (descs[j].flags & AQ_CHAIN_RELEASE) != 0;
+        const bool group_end = j + 1 == count || !(descs[j + 1].flags & AQ_CHAIN_INDEPENDENT);
+        if (!group_end) continue;
+        if (j + 1 < count && (run > 0 || forced)) recs[j].flags |= kRecRelease;
+        forced = false;
+    }
 }
 
 // Encodes validated descriptors into host records and fills the plan's sizes.
@@ -545,6 +637,9 @@ aq_status chain_encode(const aq_matmul_desc *descs, int count, int group_size, i
     plan->reserved[2] = nv ? 1 : 0;   // NVFP4 weights
     for (int i = 0; i < count; ++i)
         if (descs[i].flags & AQ_CHAIN_DEBUG_SKIP_COPY) plan->reserved[1] = 1;   // the test hook: short waits
+    mark_releases(descs, count, bits, nv, recs);
+    for (int i = 0; i < count; ++i)
+        if (recs[i].flags & kRecRelease) ++plan->reserved[3];   // groups published with a release
     return AQ_OK;
 }
 

@@ -164,11 +164,30 @@ class DecodeStep:
         off = x_offset(self.layers, self.mats[i])
         return self.x_host[off:off + self.mats[i][4]].reshape(1, -1)
 
-    def run_chain(self, stream_handle) -> None:
-        """The whole step as one persistent launch (aq_chain_run)."""
-        st = aq.aq_chain_run(self.plan, stream_handle)
+    def run_chain(self, stream_handle, plan=None) -> None:
+        """The whole step as one persistent launch (aq_chain_run), on this
+        step's plan or on ``plan`` (from ``released_plan``)."""
+        st = aq.aq_chain_run(self.plan if plan is None else plan, stream_handle)
         if st != aq.AQ_OK:
             raise aq.AqError(st, "aq_chain_run")
+
+    def released_plan(self):
+        """(plan, workspace) of the same chain with AQ_CHAIN_RELEASE on every
+        matmul: every dependency group's completion published with a GPU-scope
+        release, as if each matmul read the previous group's output."""
+        import torch
+
+        descs = (aq.MatmulDesc * self.count)(*[
+            aq.MatmulDesc(d.x, d.w_packed, d.scales, d.biases, d.y, d.M, d.N, d.K, d.flags | aq.AQ_CHAIN_RELEASE)
+            for d in self.descs])
+        nbytes = aq.aq_chain_workspace_bytes(self.count)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        plan = aq.ChainPlan()
+        st = aq.aq_chain_prepare(descs, self.count, 16 if self.fmt == "nvfp4" else 64, 4, workspace.data_ptr(),
+                                 nbytes, plan)
+        if st != aq.AQ_OK:
+            raise aq.AqError(st, "aq_chain_prepare")
+        return plan, workspace
 
     def enqueue(self, stream_handle, sel=None, flags: int = aq.AQ_FLAG_PDL) -> None:
         """One launch per matmul (those in ``sel``, or all), in order:

@@ -160,7 +160,8 @@ aq_status aq_pack_ref(const uint8_t *codes, int64_t N, int64_t K, int bits, uint
  * single persistent kernel: matmul j reads its x only after every earlier
  * matmul of the chain has written all of its y (so x_j may be an earlier
  * y_i), unless it is flagged AQ_CHAIN_INDEPENDENT, while the weights of the
- * next matmuls keep streaming.
+ * next matmuls keep streaming.  So w_packed, scales and biases must not be
+ * written by any matmul of the chain (they are read ahead of the ordering).
  *
  * Each descriptor follows aq_matmul_bf16's definition, with the limits of the
  * weight-streaming kernel: 1 <= M <= 8, K a multiple of 512, M*K <= 16384
@@ -181,7 +182,7 @@ typedef struct aq_matmul_desc {
     const void *biases;       /* bf16 [N, K/64], device (NVFP4: const float *, the global scale) */
     void *y;                  /* bf16 [M, N], device, written */
     int64_t M, N, K;
-    int64_t flags;            /* 0, AQ_CHAIN_INDEPENDENT, AQ_CHAIN_DEBUG_SKIP_COPY (test hook) */
+    int64_t flags;            /* 0 or AQ_CHAIN_INDEPENDENT | AQ_CHAIN_RELEASE; AQ_CHAIN_DEBUG_SKIP_COPY (test hook) */
 } aq_matmul_desc;
 
 enum {
@@ -191,6 +192,18 @@ enum {
      * for, but not after the previous matmul itself, so the two overlap.  A
      * run of matmuls on the same x buffer with this flag loads x once. */
     AQ_CHAIN_INDEPENDENT = 1,
+    /* Publish the completion of this matmul's dependency group with a
+     * GPU-scope release even where no later matmul of the chain needs it.
+     * aq_chain_prepare releases a group's completion (a memory fence that
+     * waits for the group's y stores to reach L2, about 0.9 us on GB300)
+     * only where a later matmul reads or rewrites memory that a matmul up to
+     * that group wrote, or rewrites memory one of them read (checked on the
+     * byte ranges of every x, w_packed, scales, biases and y); elsewhere the
+     * next group still starts only after every tile of the previous one is
+     * stored, without the fence.  All outputs are visible to work that
+     * follows the launch on the stream either way.  This flag forces the
+     * fence (measurement, or callers with their own reasons). */
+    AQ_CHAIN_RELEASE = 2,
     /* Test hook for the failure path of the chain's bounded waits: the first
      * CTA's producer leaves out the first copy of this matmul's weights, so
      * waits in the kernel expire (after 20 ms instead of 2 s), a timeout is
@@ -205,7 +218,7 @@ typedef struct aq_chain_plan {
     int count;       /* number of matmuls */
     int x_bytes;     /* largest M*K*2 of the chain */
     int one_row;     /* 1 if every matmul has M == 1 */
-    int reserved[5];
+    int reserved[5];  /* internal; reserved[3]: dependency groups whose completion is released */
 } aq_chain_plan;
 
 /* Device workspace bytes a chain of `count` matmuls needs (one 512-byte

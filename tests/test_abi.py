@@ -157,8 +157,11 @@ def test_chain_workspace_and_plan_checks():
     assert aq.aq_chain_run(plan, None) == aq.AQ_OK                                          # empty chain
 
 
-def test_chain_prepare_rejects_unknown_flags():
-    arr = (aq.MatmulDesc * 1)(_desc(flags=2))
+@pytest.mark.parametrize("flags", [4, 0x10000000, 1 << 40])
+def test_chain_prepare_rejects_unknown_flags(flags):
+    # bits other than AQ_CHAIN_INDEPENDENT, AQ_CHAIN_RELEASE and the test hook, the
+    # library's own record bit included
+    arr = (aq.MatmulDesc * 1)(_desc(flags=flags))
     plan = aq.ChainPlan()
     assert aq.aq_chain_prepare(arr, 1, 64, 4, A, aq.aq_chain_workspace_bytes(1), plan) == aq.AQ_ERR_INVALID_ARG
 

@@ -298,3 +298,72 @@ def test_chain_nvfp4_dependencies_and_shared_x(dev):
         # the second run reads new tensor scales from the same device floats
         for it in items:
             it[3].mul_(0.5)
+
+
+# ---------------------------------------------------------------- release only where memory is shared
+
+def _plan_of(dev, items, independent=None, release=None, group_size=64, bits=4):
+    chain = aq.Chain(items, group_size=group_size, bits=bits, independent=independent, release=release)
+    return chain, int(chain.plan.reserved[3])
+
+
+def test_chain_releases_only_where_a_later_matmul_touches_earlier_memory(dev):
+    """aq_chain_prepare publishes a group's completion with a GPU-scope release
+    only where a later matmul reads or rewrites memory written up to that
+    group, or rewrites memory read up to it (the plan reports how many
+    groups); results are the same bits either way, and AQ_CHAIN_RELEASE
+    forces the release on every group."""
+    import torch
+    K = 1024
+    ws = [synth.make_weights(K, K, 1900 + i) for i in range(4)]
+    wdev = [upload(np.zeros((1, K), np.uint16), w, dev)[1:] for w in ws]
+    x = to_dev_bf16(synth.make_x(1, K, 1900), dev)
+    xs = [to_dev_bf16(synth.make_x(1, K, 1901 + i), dev) for i in range(4)]
+    ys = [torch.empty((1, K), dtype=torch.bfloat16, device=dev) for _ in range(4)]
+
+    # separate inputs and outputs (the decode step's layout): ordering only, no release
+    items = [(xs[i], *wdev[i], ys[i]) for i in range(4)]
+    chain, n = _plan_of(dev, items)
+    assert n == 0
+    chain.run()
+    torch.cuda.synchronize()
+    ref = [y.clone() for y in ys]
+    for i in range(4):
+        assert torch.equal(ys[i], aq.matmul(xs[i], *wdev[i])), i
+    # forced: every group but the last (whose completion nothing in the chain awaits)
+    chain_f, n_f = _plan_of(dev, items, release=True)
+    assert n_f == 3
+    for y in ys:
+        y.fill_(float("nan"))
+    chain_f.run()
+    torch.cuda.synchronize()
+    assert all(torch.equal(a, b) for a, b in zip(ys, ref))
+
+    # read after write: matmul 2 reads matmul 0's output -> groups 0 and 1 released
+    items_raw = [(x, *wdev[0], ys[0]), (xs[1], *wdev[1], ys[1]), (ys[0], *wdev[2], ys[2]), (xs[3], *wdev[3], ys[3])]
+    chain_raw, n_raw = _plan_of(dev, items_raw)
+    assert n_raw == 2
+    for _ in range(3):
+        for y in ys:
+            y.fill_(float("nan"))
+        chain_raw.run()
+        torch.cuda.synchronize()
+        y0 = aq.matmul(x, *wdev[0])
+        assert torch.equal(ys[0], y0)
+        assert torch.equal(ys[2], aq.matmul(y0, *wdev[2]))
+    assert aq.aq_read_device_status(None) == aq.AQ_OK
+
+    # write after read: matmul 3 overwrites matmul 1's input -> groups 1 and 2 released
+    xw = xs[1].clone()
+    items_war = [(xs[0], *wdev[0], ys[0]), (xw, *wdev[1], ys[1]), (xs[2], *wdev[2], ys[2]), (xs[3], *wdev[3], xw)]
+    chain_war, n_war = _plan_of(dev, items_war)
+    assert n_war == 2
+    chain_war.run()
+    torch.cuda.synchronize()
+    assert torch.equal(ys[1], aq.matmul(xs[1], *wdev[1]))
+    assert torch.equal(xw, aq.matmul(xs[3], *wdev[3]))
+
+    # independent matmuls: a hazard between groups still marks every group it crosses
+    items_ind = [(x, *wdev[0], ys[0]), (x, *wdev[1], ys[1]), (xs[2], *wdev[2], ys[2]), (ys[1], *wdev[3], ys[3])]
+    _, n_ind = _plan_of(dev, items_ind, independent=[False, True, False, False])
+    assert n_ind == 2          # groups {0, 1} and {2}
