@@ -539,40 +539,62 @@ Footprint footprint(const aq_matmul_desc &d, int bits, bool nv) {
     range(d.y, M * N * 2, f.w);
     return f;
 }
-bool overlap(const uintptr_t (&a)[2], const uintptr_t (&b)[2]) { return a[0] < b[1] && b[0] < a[1]; }
-// True if matmul k (later) touches what matmul i (earlier) wrote, or writes what
-// i read: a read-after-write, write-after-write or write-after-read hazard
-// that the chain's ordering must also make visible in memory.
-bool hazard(const Footprint &i, const Footprint &k) {
-    if (overlap(i.w, k.w)) return true;
-    for (int a = 0; a < 4; ++a)
-        if (overlap(i.w, k.r[a]) || overlap(i.r[a], k.w)) return true;
-    return false;
-}
-
 // Marks, on the last matmul of each dependency group, whether its completion
 // is published with a release (kRecRelease): where a hazard pair (i, k), i <=
 // the group's last matmul < k, crosses it, or where the caller asks for it
 // (AQ_CHAIN_RELEASE on any of the group's matmuls).  Every group a hazard
 // crosses is marked, so the release / acquire pairs chain from i to k.  The
 // last group's completion is never awaited inside the chain (the kernel's
-// end orders it for later work).  Chains beyond kHazardScanMax matmuls are
-// not scanned: every group is published with a release.
-constexpr int kHazardScanMax = 4096;
+// end orders it for later work).
+//
+// The pairs come from one sweep over every byte range of the chain sorted by
+// start (O(n log n) plus the overlapping pairs); past kPairBudget overlapping
+// pairs (chains whose matmuls share much memory) every group is released.
+constexpr long kPairBudget = 1L << 22;
 void mark_releases(const aq_matmul_desc *descs, int count, int bits, bool nv, ChainRec *recs) {
+    struct Span {
+        uintptr_t lo, hi;
+        int mm;
+        bool write;
+    };
+    std::vector<Span> spans;
+    spans.reserve((size_t)count * 5);
+    for (int i = 0; i < count; ++i) {
+        const Footprint f = footprint(descs[i], bits, nv);
+        for (int a = 0; a < 4; ++a)
+            if (f.r[a][1] > f.r[a][0]) spans.push_back({f.r[a][0], f.r[a][1], i, false});
+        if (f.w[1] > f.w[0]) spans.push_back({f.w[0], f.w[1], i, true});
+    }
+    std::sort(spans.begin(), spans.end(), [](const Span &a, const Span &b) { return a.lo < b.lo; });
+    std::vector<int> latest((size_t)count, -1);   // latest k > i with a hazard against matmul i
+    std::vector<int> active;                      // spans still open at the current start
+    long pairs = 0;
+    bool all = false;
+    for (int s = 0; s < (int)spans.size() && !all; ++s) {
+        const Span &cur = spans[(size_t)s];
+        int kept = 0;
+        for (int a : active)
+            if (spans[(size_t)a].hi > cur.lo) active[(size_t)kept++] = a;   // overlaps cur
+        active.resize((size_t)kept);
+        for (int a : active) {
+            const Span &o = spans[(size_t)a];
+            if ((o.write || cur.write) && o.mm != cur.mm) {
+                const int i = std::min(o.mm, cur.mm), k = std::max(o.mm, cur.mm);
+                latest[(size_t)i] = std::max(latest[(size_t)i], k);
+            }
+            if (++pairs > kPairBudget) all = true;
+        }
+        active.push_back(s);
+    }
     std::vector<int> cover((size_t)count + 1, 0);   // difference array over matmul positions
-    if (count > kHazardScanMax) {
+    if (all) {
         cover[0] = 1;
     } else {
-        std::vector<Footprint> fp((size_t)count);
-        for (int i = 0; i < count; ++i) fp[(size_t)i] = footprint(descs[i], bits, nv);
         for (int i = 0; i < count; ++i)
-            for (int k = count - 1; k > i; --k)
-                if (hazard(fp[(size_t)i], fp[(size_t)k])) {
-                    ++cover[(size_t)i];
-                    --cover[(size_t)k];
-                    break;   // the latest k: its span [i, k) contains those of the earlier ones
-                }
+            if (latest[(size_t)i] > i) {
+                ++cover[(size_t)i];
+                --cover[(size_t)latest[(size_t)i]];
+            }
     }
     int run = 0;
     bool forced = false;
