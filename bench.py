@@ -83,7 +83,15 @@ class ClockSampler:
                  "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
-        time.sleep(0.3)
+        # wait (up to 10 s) for the first sample, so that nvidia-smi's start-up is
+        # over before the timed region begins
+        t0 = time.time()
+        while self.proc is not None and time.time() - t0 < 10:
+            self.file.flush()
+            if os.path.getsize(self.file.name) > 0:
+                break
+            time.sleep(0.05)
+        time.sleep(0.25)
 
     def stop(self):
         if self.proc is None:
