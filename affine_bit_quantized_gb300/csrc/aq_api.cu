@@ -55,7 +55,7 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 constexpr int64_t kMaxDim = (int64_t)1 << 30;  // keeps every per-row index inside 32 bits
 constexpr int kQmvMaxRows = 16;                // rows of x per weight-streaming pass
 
-// At least four 32-row tiles per SM of the current device.
+// At least two 32-row tiles per SM of the current device.
 bool many_tiles(int64_t N) {
     constexpr int kDevices = 64;
     static std::atomic<int> sms[kDevices];
@@ -72,7 +72,7 @@ bool many_tiles(int64_t N) {
         }
         sms[dev].store(n, std::memory_order_relaxed);
     }
-    return (N + 31) / 32 >= 4 * (int64_t)n;
+    return (N + 31) / 32 >= 2 * (int64_t)n;
 }
 
 aq_status validate(const void *x, const uint32_t *w, const void *s, const void *b, void *y,
@@ -158,9 +158,10 @@ aq_status matmul_impl(const void *x, const uint32_t *w_packed, const void *scale
     }
     if (M > 8 && M <= kQmvMaxRows && kernel == AQ_KERNEL_AUTO && many_tiles(N)) {
         // 9..16 rows whose x needs K passes (16 rows of K = 4096: 128 KB), over a matrix
-        // with many tiles per SM (an lm_head): two launches of at most 8 rows, each x in
-        // one pass, beat one launch whose every pass deposits partial sums (128256 x
-        // 4096 at M = 16: 2 x 60 us against 204 us) and the general kernel
+        // with at least two tiles per SM: two launches of at most 8 rows, each x in one
+        // pass, beat one launch whose every pass deposits partial sums (128256 x 4096 at
+        // M = 16: 2 x 60 us against 204 us) and the general kernel (14336 x 4096 at
+        // M = 9 / 16: 25.4 / 27.9 us against 27.3 / 29.7 us)
         const int64_t rows = (M + 1) / 2;
         st = AQ_OK;
         if (tma_rows(rows, &st)) return st;

@@ -72,7 +72,7 @@ typedef enum aq_kernel {
                           launch), else the general one in launches of 16 rows of x (both
                           code widths).  AQ_KERNEL_AUTO chooses among these (and the GEMM
                           kernel above 16 rows) by measured speed; for 9..16 rows whose x
-                          needs several K passes, over a matrix of at least four 32-row
+                          needs several K passes, over a matrix of at least two 32-row
                           tiles per SM, it runs the TMA-fed kernel twice, on half the rows
                           each. */
     AQ_KERNEL_QMM = 2  /* tensor-core GEMM kernel (tcgen05); any M >= 1 */
