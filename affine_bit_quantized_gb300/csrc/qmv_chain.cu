@@ -551,55 +551,62 @@ Footprint footprint(const aq_matmul_desc &d, int bits, bool nv) {
 // start (O(n log n) plus the overlapping pairs); past kPairBudget overlapping
 // pairs (chains whose matmuls share much memory) every group is released.
 constexpr long kPairBudget = 1L << 22;
-void mark_releases(const aq_matmul_desc *descs, int count, int bits, bool nv, ChainRec *recs) {
-    struct Span {
-        uintptr_t lo, hi;
-        int mm;
-        bool write;
-    };
-    std::vector<Span> spans;
-    spans.reserve((size_t)count * 5);
+struct Span {
+    uintptr_t lo, hi;
+    int mm;
+    bool write;
+};
+// Working room of mark_releases for `count` matmuls: spans and active hold 5 *
+// count entries, latest count, cover count + 1 (the caller provides it, so that
+// the allocation-free entry point can pass static arrays).
+struct ReleaseScratch {
+    Span *spans;
+    int *active, *latest, *cover;
+};
+void mark_releases(const aq_matmul_desc *descs, int count, int bits, bool nv, ChainRec *recs,
+                   const ReleaseScratch &w) {
+    int ns = 0;
     for (int i = 0; i < count; ++i) {
         const Footprint f = footprint(descs[i], bits, nv);
         for (int a = 0; a < 4; ++a)
-            if (f.r[a][1] > f.r[a][0]) spans.push_back({f.r[a][0], f.r[a][1], i, false});
-        if (f.w[1] > f.w[0]) spans.push_back({f.w[0], f.w[1], i, true});
+            if (f.r[a][1] > f.r[a][0]) w.spans[ns++] = {f.r[a][0], f.r[a][1], i, false};
+        if (f.w[1] > f.w[0]) w.spans[ns++] = {f.w[0], f.w[1], i, true};
     }
-    std::sort(spans.begin(), spans.end(), [](const Span &a, const Span &b) { return a.lo < b.lo; });
-    std::vector<int> latest((size_t)count, -1);   // latest k > i with a hazard against matmul i
-    std::vector<int> active;                      // spans still open at the current start
+    std::sort(w.spans, w.spans + ns, [](const Span &a, const Span &b) { return a.lo < b.lo; });
+    for (int i = 0; i < count; ++i) w.latest[i] = -1;   // latest k > i with a hazard against matmul i
+    int na = 0;                                         // spans still open at the current start
     long pairs = 0;
     bool all = false;
-    for (int s = 0; s < (int)spans.size() && !all; ++s) {
-        const Span &cur = spans[(size_t)s];
+    for (int s = 0; s < ns && !all; ++s) {
+        const Span &cur = w.spans[s];
         int kept = 0;
-        for (int a : active)
-            if (spans[(size_t)a].hi > cur.lo) active[(size_t)kept++] = a;   // overlaps cur
-        active.resize((size_t)kept);
-        for (int a : active) {
-            const Span &o = spans[(size_t)a];
+        for (int a = 0; a < na; ++a)
+            if (w.spans[w.active[a]].hi > cur.lo) w.active[kept++] = w.active[a];   // overlaps cur
+        na = kept;
+        for (int a = 0; a < na; ++a) {
+            const Span &o = w.spans[w.active[a]];
             if ((o.write || cur.write) && o.mm != cur.mm) {
                 const int i = std::min(o.mm, cur.mm), k = std::max(o.mm, cur.mm);
-                latest[(size_t)i] = std::max(latest[(size_t)i], k);
+                w.latest[i] = std::max(w.latest[i], k);
             }
             if (++pairs > kPairBudget) all = true;
         }
-        active.push_back(s);
+        w.active[na++] = s;
     }
-    std::vector<int> cover((size_t)count + 1, 0);   // difference array over matmul positions
+    for (int j = 0; j <= count; ++j) w.cover[j] = 0;   // difference array over matmul positions
     if (all) {
-        cover[0] = 1;
+        w.cover[0] = 1;
     } else {
         for (int i = 0; i < count; ++i)
-            if (latest[(size_t)i] > i) {
-                ++cover[(size_t)i];
-                --cover[(size_t)latest[(size_t)i]];
+            if (w.latest[i] > i) {
+                ++w.cover[i];
+                --w.cover[w.latest[i]];
             }
     }
     int run = 0;
     bool forced = false;
     for (int j = 0; j < count; ++j) {
-        run += cover[(size_t)j];
+        run += w.cover[j];
         forced = forced || (descs[j].flags & AQ_CHAIN_RELEASE) != 0;
         const bool group_end = j + 1 == count || !(descs[j + 1].flags & AQ_CHAIN_INDEPENDENT);
         if (!group_end) continue;
@@ -610,7 +617,7 @@ void mark_releases(const aq_matmul_desc *descs, int count, int bits, bool nv, Ch
 
 // Encodes validated descriptors into host records and fills the plan's sizes.
 aq_status chain_encode(const aq_matmul_desc *descs, int count, int group_size, int bits, ChainRec *recs,
-                       aq_chain_plan *plan) {
+                       aq_chain_plan *plan, const ReleaseScratch &scratch) {
     if (!encode_fn()) return AQ_ERR_UNSUPPORTED;
     const bool nv = group_size == 16;
     int x_bytes = 16;
@@ -659,7 +666,7 @@ aq_status chain_encode(const aq_matmul_desc *descs, int count, int group_size, i
     plan->reserved[2] = nv ? 1 : 0;   // NVFP4 weights
     for (int i = 0; i < count; ++i)
         if (descs[i].flags & AQ_CHAIN_DEBUG_SKIP_COPY) plan->reserved[1] = 1;   // the test hook: short waits
-    mark_releases(descs, count, bits, nv, recs);
+    mark_releases(descs, count, bits, nv, recs, scratch);
     for (int i = 0; i < count; ++i)
         if (recs[i].flags & kRecRelease) ++plan->reserved[3];   // groups published with a release
     return AQ_OK;
@@ -680,7 +687,10 @@ aq_status chain_prepare(const aq_matmul_desc *descs, int count, int group_size, 
     aq_status st = chain_validate(descs, count, group_size, bits);  // before any CUDA call
     if (st != AQ_OK) return st;
     std::vector<ChainRec> recs((size_t)count);
-    st = chain_encode(descs, count, group_size, bits, recs.data(), plan);
+    std::vector<Span> spans((size_t)count * 5);
+    std::vector<int> active((size_t)count * 5), latest((size_t)count), cover((size_t)count + 1);
+    const ReleaseScratch scratch = {spans.data(), active.data(), latest.data(), cover.data()};
+    st = chain_encode(descs, count, group_size, bits, recs.data(), plan, scratch);
     if (st != AQ_OK) return st;
     *err = cudaMemcpy(workspace, recs.data(), records_bytes(count), cudaMemcpyHostToDevice);
     if (*err != cudaSuccess) {
@@ -755,6 +765,8 @@ namespace {
 std::atomic<void *> g_static_scratch_ptr[kMaxDevices];
 std::mutex g_static_host_mutex;
 ChainRec g_static_host_recs[kStaticChainMax];  // host staging of the records (no heap allocation)
+Span g_static_spans[5 * kStaticChainMax];       // and the release marking's working room
+int g_static_active[5 * kStaticChainMax], g_static_latest[kStaticChainMax], g_static_cover[kStaticChainMax + 1];
 }  // namespace
 
 int chain_static_max() { return kStaticChainMax; }
@@ -790,7 +802,8 @@ aq_status chain_run_static(const aq_matmul_desc *descs, int count, int group_siz
     // (one call's kernel running the other's records).  So the lock covers
     // all three.
     std::lock_guard<std::mutex> lock(g_static_host_mutex);
-    st = chain_encode(descs, count, group_size, bits, g_static_host_recs, &plan);
+    const ReleaseScratch marks = {g_static_spans, g_static_active, g_static_latest, g_static_cover};
+    st = chain_encode(descs, count, group_size, bits, g_static_host_recs, &plan, marks);
     if (st != AQ_OK) return st;
     // from pageable memory: returns once the records are staged (which may
     // mean waiting for the stream's earlier work), so the host array may be

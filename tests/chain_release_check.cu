@@ -42,7 +42,9 @@ int main() {
         }
         std::vector<ChainRec> recs((size_t)n);
         for (ChainRec &r : recs) r.flags = 0;
-        mark_releases(d.data(), n, 4, nv, recs.data());
+        std::vector<Span> spans((size_t)n * 5);
+        std::vector<int> active((size_t)n * 5), latest((size_t)n), cover((size_t)n + 1);
+        mark_releases(d.data(), n, 4, nv, recs.data(), {spans.data(), active.data(), latest.data(), cover.data()});
 
         // brute force: a group ending at j (not the last) is released iff it is forced or some
         // matmul i <= j and some matmul k > j share memory with at least one of them writing it
