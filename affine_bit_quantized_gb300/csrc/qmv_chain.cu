@@ -17,9 +17,14 @@
 //    matmuls' weights while the consumers wait for a dependency, because
 //    weights never depend on earlier outputs;
 //  * matmul j reads its x only after every CTA has stored all of its tiles of
-//    matmul j-1 (a completion counter per matmul in the caller's workspace,
-//    release / acquire at GPU scope, bounded wait), which is the same
-//    ordering a chain of stream-ordered launches gives.
+//    matmul j-1 (a completion counter per dependency group in the caller's
+//    workspace, bounded wait), which is the same ordering a chain of
+//    stream-ordered launches gives; the count is published with a GPU-scope
+//    release, and polled with an acquire, where a later matmul reads or
+//    rewrites memory written up to the group (or rewrites memory read up to
+//    it), as the host finds when it encodes the plan;
+//  * matmuls may hold 4- or 8-bit affine codes, or NVFP4 weights (one format
+//    per chain).
 //
 // The plan (one record per matmul: three TMA descriptors plus pointers and
 // sizes) and the counters live in caller-owned device memory.

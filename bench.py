@@ -26,6 +26,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -327,10 +328,15 @@ def run_case_other(args):
 
 
 def kernel_source_hash() -> str:
+    """Hash of the chained kernel's sources with comments and blank space taken
+    out (an edit of a comment leaves the captured traffic valid)."""
     h = hashlib.sha256()
     for name in ("qmv_chain.cu", "qmv_tma.cu", "qmv_consumer.cuh", "nvfp4_consumer.cuh", "aq_ptx.cuh"):
-        with open(os.path.join(ROOT, "affine_bit_quantized_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "affine_bit_quantized_gb300", "csrc", name), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
