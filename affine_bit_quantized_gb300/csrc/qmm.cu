@@ -107,7 +107,9 @@ constexpr int kMaxSplit = 8;
 static_assert((kMaxSplit - 1) * Cfg<4>::kTileM * (kTileN / kMaxSplit) * 4 <= Cfg<4>::kOffBar &&
                   (kMaxSplit - 1) * Cfg<8>::kTileM * (kTileN / kMaxSplit) * 4 <= Cfg<8>::kOffBar &&
                   (kMaxSplit - 1) * Cfg<4, true>::kTileM * (kTileN / kMaxSplit) * 4 <= Cfg<4, true>::kOffBar &&
-                  (kMaxSplit - 1) * Cfg<8, true>::kTileM * (kTileN / kMaxSplit) * 4 <= Cfg<8, true>::kOffBar,
+                  (kMaxSplit - 1) * Cfg<8, true>::kTileM * (kTileN / kMaxSplit) * 4 <= Cfg<8, true>::kOffBar &&
+                  (kMaxSplit - 1) * Cfg<4, false, 128>::kTileM * (kTileN / kMaxSplit) * 4 <= Cfg<4, false, 128>::kOffBar &&
+                  (kMaxSplit - 1) * Cfg<4, true, 128>::kTileM * (kTileN / kMaxSplit) * 4 <= Cfg<4, true, 128>::kOffBar,
               "split-K receive slots");
 // 256-row 8-bit tiles are taken only without a split
 
@@ -757,11 +759,11 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *gaddr, uint
 }
 
 constexpr int kMaxDevices = 64;
-std::atomic<int> g_attr_done[5][kMaxDevices];
+std::atomic<int> g_attr_done[7][kMaxDevices];
 std::atomic<int> g_attr_done_grouped[2][kMaxDevices];
 std::atomic<int> g_sms[kMaxDevices];
 // clusters of 2, 4, 8 CTAs that can be resident at once, per code width (0: not yet asked; -1: none)
-std::atomic<int> g_max_clusters[2][3][kMaxDevices];
+std::atomic<int> g_max_clusters[3][3][kMaxDevices];
 
 }  // namespace
 
@@ -775,9 +777,14 @@ namespace {
 // occupy half the SMs (prefill at M = 256), as many as still fit in one wave.
 // Decided on the tiles of the kernel without the workspace, so that both
 // variants split alike (same summation order, same bits).
-template <int BITS>
+// g_attr_done slot of a kernel instance without the expert index
+template <int BITS, bool XPRE, int TM>
+constexpr int attr_slot() {
+    return (BITS == 8 && TM == 256) ? 4 : (BITS == 4 && TM == 128) ? 5 + (int)XPRE : (BITS == 8 ? 1 : 0) + (XPRE ? 2 : 0);
+}
+template <int BITS, int TM = (BITS == 4 ? 256 : 128)>
 int qmm_split(const MatmulArgs &a, int dev) {
-    using C = Cfg<BITS, false>;
+    using C = Cfg<BITS, false, TM>;
     const int M = (int)a.M, N = (int)a.N, K = (int)a.K;
     int sms = g_sms[dev].load(std::memory_order_relaxed);
     if (sms == 0) {
@@ -796,16 +803,17 @@ int qmm_split(const MatmulArgs &a, int dev) {
         for (int si = 2; si >= 0 && split == 1; --si) {
             const int S = 2 << si;
             if (S > K / (kGroup * kSBGroups) || tiles * S > sms) continue;
-            const int bb = BITS == 8 ? 1 : 0;
+            const int bb = BITS == 8 ? 1 : (TM == 128 ? 2 : 0);
+            constexpr int ab = attr_slot<BITS, false, TM>();
             int n = g_max_clusters[bb][si][dev].load(std::memory_order_relaxed);
             if (n == 0) {
-                using C0 = Cfg<BITS, false>;
-                if (!g_attr_done[bb][dev].load(std::memory_order_acquire)) {
-                    if (cudaFuncSetAttribute(qmm_kernel<BITS, false, false>,
+                using C0 = C;
+                if (!g_attr_done[ab][dev].load(std::memory_order_acquire)) {
+                    if (cudaFuncSetAttribute(qmm_kernel<BITS, false, false, TM>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C0::kSmemBytes) != cudaSuccess)
                         cudaGetLastError();
                     else
-                        g_attr_done[bb][dev].store(1, std::memory_order_release);
+                        g_attr_done[ab][dev].store(1, std::memory_order_release);
                 }
                 cudaLaunchConfig_t q = cfg;
                 q.dynamicSmemBytes = C0::kSmemBytes;
@@ -817,7 +825,7 @@ int qmm_split(const MatmulArgs &a, int dev) {
                 ca.val.clusterDim.z = (unsigned)S;
                 q.attrs = &ca;
                 q.numAttrs = 1;
-                if (cudaOccupancyMaxActiveClusters(&n, qmm_kernel<BITS, false, false>, &q) != cudaSuccess || n < 1) {
+                if (cudaOccupancyMaxActiveClusters(&n, qmm_kernel<BITS, false, false, TM>, &q) != cudaSuccess || n < 1) {
                     cudaGetLastError();   // the query's error is not the caller's
                     n = -1;
                 }
@@ -833,7 +841,7 @@ int qmm_split(const MatmulArgs &a, int dev) {
 template <int BITS, bool XPRE, int TM = (BITS == 4 ? 256 : 128)>
 cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev, int split) {
     using C = Cfg<BITS, XPRE, TM>;
-    const int bi = TM == 256 && BITS == 8 ? 4 : (BITS == 8 ? 1 : 0) + (XPRE ? 2 : 0);
+    constexpr int bi = attr_slot<BITS, XPRE, TM>();
     if (!g_attr_done[bi][dev].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(qmm_kernel<BITS, false, XPRE, TM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
@@ -893,6 +901,16 @@ cudaError_t launch_qmm(const MatmulArgs &a) {
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     if (a.bits == 4) {
         const int split = qmm_split<4>(a, dev);
+        // few 256-row tiles (prefill at M = 256 over 4096 x 14336): 128-row tiles, where
+        // they keep the K split (so that no CTA converts more of W) and still fit one
+        // wave, put more SMs to work; the same choice with and without the workspace
+        // (same summation order, same bits)
+        const int sms = g_sms[dev].load(std::memory_order_relaxed);
+        const int64_t ntiles = (a.N + kTileN - 1) / kTileN;
+        const int64_t tiles256 = ntiles * ((a.M + 255) / 256), tiles128 = ntiles * ((a.M + 127) / 128);
+        if (sms > 0 && 4 * tiles256 * split <= 3 * (int64_t)sms && tiles128 * split <= sms &&
+            qmm_split<4, 128>(a, dev) == split)
+            return a.xf16 ? launch_qmm_bits<4, true, 128>(a, dev, split) : launch_qmm_bits<4, false, 128>(a, dev, split);
         return a.xf16 ? launch_qmm_bits<4, true>(a, dev, split) : launch_qmm_bits<4, false>(a, dev, split);
     }
     const int split = qmm_split<8>(a, dev);
