@@ -227,15 +227,17 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     d |= (uint64_t)2 << 61;                   // 128-byte swizzle
     return d;
 }
-// instruction descriptor: D f32, A f16, B f16, both K-major, M=128, N=256
-constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(kTileN >> 3) << 17) |
-                            ((uint32_t)(128 >> 4) << 24);
+// instruction descriptor: D f32, A f16, B f16, both K-major, M=128, N=tn (256 or 224)
+__host__ __device__ constexpr uint32_t umma_idesc(int tn) {
+    return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(tn >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
 
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate) {
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -329,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
            const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_b,
            __nv_bfloat16 *__restrict__ y, int M, int N, int K, unsigned long long timeout_ns, int *status,
-           const int *__restrict__ plan, int skip_copy) {
+           const int *__restrict__ plan, int skip_copy, int tn) {
     using C = Cfg<BITS, XPRE, TM>;
     constexpr int kConvStages = C::kConvStages;
     constexpr int kTileM = C::kTileM, kATileBytes = C::kATileBytes, kConvStageBytes = C::kConvStageBytes;
@@ -354,7 +356,9 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * kTileN;
+    // tn: rows of W per CTA, kTileN or 224 (a full last wave where 256 would leave SMs
+    // idle; only without a K split); the stage memory is laid out for kTileN
+    const int n0 = blockIdx.x * tn;
     int m0 = blockIdx.y * kTileM;   // first row of x (and of y) of the tile
     int m_end = M;                  // rows from m_end on are not this tile's
     int wrow0 = n0;                 // first row of W (in the stacked experts: expert * N + n0)
@@ -491,7 +495,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                         break;
                     }
                     const uint32_t dst = base + kOffSB + ss * 2 * kSBBytes;
-                    mbar_expect_tx(sb_full(ss), 2 * kSBBytes);
+                    mbar_expect_tx(sb_full(ss), (uint32_t)(2 * tn * kSBGroups * 2));
                     tma_load_2d(dst, &tm_s, g0 + j * kSBGroups, wrow0, sb_full(ss));
                     tma_load_2d(dst + kSBBytes, &tm_b, g0 + j * kSBGroups, wrow0, sb_full(ss));
                     issued_sb = j + 1;
@@ -502,7 +506,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 }
                 const uint32_t dst = base + kOffRaw + rs * kRawStageBytes;
                 if (!(skip_first && i == 0)) {
-                    mbar_expect_tx(raw_full(rs), kRawStageBytes);
+                    mbar_expect_tx(raw_full(rs), (uint32_t)(kRawXBytes + tn * C::kRowWords * 4));
                     if (!XPRE) tma_load_2d(dst, &tm_x, (g0 + i) * kGroup, m0, raw_full(rs));
                     tma_load_2d(dst + kRawXBytes, &tm_w, (g0 + i) * C::kRowWords, wrow0, raw_full(rs));
                 }
@@ -525,6 +529,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
+            const uint32_t idesc = umma_idesc(tn);
             for (int i = 0; i < steps; ++i) {
                 const int cs = i % kConvStages;
                 if (!mbar_wait(conv_full(cs), (i / kConvStages) & 1, deadline, abort_flag) ||
@@ -540,7 +545,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                     const uint64_t bd = sw128_desc(b0 + kk * 32);
 #pragma unroll
                     for (int h = 0; h < C::kHalves; ++h)
-                        umma_f16(tmem + h * kTileN, sw128_desc(a0 + h * (128 * 128) + kk * 32), bd,
+                        umma_f16(tmem + h * kTileN, sw128_desc(a0 + h * (128 * 128) + kk * 32), bd, idesc,
                                  (i > 0 || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(conv_empty(cs));
@@ -582,8 +587,8 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             // becomes 8 fp16 weights at row r, chunk c ^ (r & 7)
             const uint32_t sb = base + kOffSB + ss * 2 * kSBBytes;
             const int g8 = i % kSBGroups;
-            {
-                static_assert(kConvThreads == 2 * kTileN, "two converter threads per W row");
+            static_assert(kConvThreads == 2 * kTileN, "two converter threads per W row");
+            if ((t >> 1) < tn) {   // rows of W past tn are not loaded and not used
                 const int r = t >> 1, hw = t & 1;
                 const __half sh = __float2half_rn(__uint_as_float((uint32_t)lds16(sb + (r * kSBGroups + g8) * 2) << 16));
                 const __half bh =
@@ -640,7 +645,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             tc_fence_after();
             if (nsplit == 1) {
 #pragma unroll 1
-                for (int j = 0; j < kTileN / 32; ++j) {
+                for (int j = 0; j < tn / 32; ++j) {
                     uint32_t r[32];
                     tmem_ld32(tbase + j * 32, r);
                     store_row32(r, m, n0 + j * 32);
@@ -773,15 +778,28 @@ bool qmm_supported(const MatmulArgs &a) {
 }
 
 namespace {
-// K split across a cluster of 2, 4 or 8 CTAs when the output has too few tiles to
-// occupy half the SMs (prefill at M = 256), as many as still fit in one wave.
-// Decided on the tiles of the kernel without the workspace, so that both
-// variants split alike (same summation order, same bits).
+// Rows of W per CTA when K is not split: 224 where that takes no more waves of
+// CTAs than 256 and so lowers the busiest SM's work (M = 2048 over 4096 rows of W:
+// 128 tiles of 256 leave 24 of 152 SMs idle, 152 tiles of 224 fill them).
+int qmm_tile_n(int64_t n_rows, int64_t row_tiles, int sms) {
+    if (sms <= 0) return kTileN;
+    auto cost = [&](int tn) {
+        const int64_t tiles = (n_rows + tn - 1) / tn * row_tiles;
+        return (tiles + sms - 1) / sms * tn;
+    };
+    return cost(224) < cost(kTileN) ? 224 : kTileN;
+}
+
 // g_attr_done slot of a kernel instance without the expert index
 template <int BITS, bool XPRE, int TM>
 constexpr int attr_slot() {
     return (BITS == 8 && TM == 256) ? 4 : (BITS == 4 && TM == 128) ? 5 + (int)XPRE : (BITS == 8 ? 1 : 0) + (XPRE ? 2 : 0);
 }
+// K split across a cluster of 2, 4 or 8 CTAs when the output has too few tiles to
+// occupy half the SMs (prefill at M = 256), as many as still fit in one wave.
+// Decided on the tiles of the kernel without the workspace, so that both
+// variants split alike (same summation order, same bits).  Also records the
+// device's SM count.
 template <int BITS, int TM = (BITS == 4 ? 256 : 128)>
 int qmm_split(const MatmulArgs &a, int dev) {
     using C = Cfg<BITS, false, TM>;
@@ -838,8 +856,9 @@ int qmm_split(const MatmulArgs &a, int dev) {
 }
 
 // split: K split across a cluster of this many CTAs (qmm_split)
+// tn: rows of W per CTA (kTileN, or 224 without a K split; see qmm_tile_n)
 template <int BITS, bool XPRE, int TM = (BITS == 4 ? 256 : 128)>
-cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev, int split) {
+cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev, int split, int tn = kTileN) {
     using C = Cfg<BITS, XPRE, TM>;
     constexpr int bi = attr_slot<BITS, XPRE, TM>();
     if (!g_attr_done[bi][dev].load(std::memory_order_acquire)) {
@@ -860,14 +879,15 @@ cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev, int split) {
     if (!encode_2d(&tx, XPRE ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, XPRE ? a.xf16 : a.x, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, kGroup,
                    C::kTileM, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.w, (uint64_t)K * BITS / 32, (uint64_t)N,
-                   (uint64_t)K * BITS / 8, C::kRowWords, kTileN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                   (uint64_t)K * BITS / 8, C::kRowWords, (uint32_t)tn, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.scales, (uint64_t)G, (uint64_t)N, (uint64_t)G * 2, kSBGroups,
-                   kTileN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                   (uint32_t)tn, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.biases, (uint64_t)G, (uint64_t)N, (uint64_t)G * 2, kSBGroups,
-                   kTileN, CU_TENSOR_MAP_SWIZZLE_NONE))
+                   (uint32_t)tn, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
+    if (split > 1 && tn != kTileN) return cudaErrorInvalidConfiguration;   // the K split owns 256 / split columns
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((M + C::kTileM - 1) / C::kTileM), 1);
+    cfg.gridDim = dim3((unsigned)((N + tn - 1) / tn), (unsigned)((M + C::kTileM - 1) / C::kTileM), 1);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = a.stream;
@@ -890,7 +910,7 @@ cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev, int split) {
     cfg.numAttrs = (unsigned)na;
     return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS, false, XPRE, TM>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(a.y), M,
                               N, K, (unsigned long long)a.timeout_ns, a.status, (const int *)nullptr,
-                              a.debug_skip_copy ? 1 : 0);
+                              a.debug_skip_copy ? 1 : 0, tn);
 }
 }  // namespace
 
@@ -901,27 +921,30 @@ cudaError_t launch_qmm(const MatmulArgs &a) {
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     if (a.bits == 4) {
         const int split = qmm_split<4>(a, dev);
+        const int sms = g_sms[dev].load(std::memory_order_relaxed);
         // few 256-row tiles (prefill at M = 256 over 4096 x 14336): 128-row tiles, where
         // they keep the K split (so that no CTA converts more of W) and still fit one
         // wave, put more SMs to work; the same choice with and without the workspace
         // (same summation order, same bits)
-        const int sms = g_sms[dev].load(std::memory_order_relaxed);
         const int64_t ntiles = (a.N + kTileN - 1) / kTileN;
         const int64_t tiles256 = ntiles * ((a.M + 255) / 256), tiles128 = ntiles * ((a.M + 127) / 128);
         if (sms > 0 && 4 * tiles256 * split <= 3 * (int64_t)sms && tiles128 * split <= sms &&
             qmm_split<4, 128>(a, dev) == split)
             return a.xf16 ? launch_qmm_bits<4, true, 128>(a, dev, split) : launch_qmm_bits<4, false, 128>(a, dev, split);
-        return a.xf16 ? launch_qmm_bits<4, true>(a, dev, split) : launch_qmm_bits<4, false>(a, dev, split);
+        const int tn = split == 1 ? qmm_tile_n(a.N, (a.M + 255) / 256, sms) : kTileN;
+        return a.xf16 ? launch_qmm_bits<4, true>(a, dev, split, tn) : launch_qmm_bits<4, false>(a, dev, split, tn);
     }
     const int split = qmm_split<8>(a, dev);
-    if (!a.xf16) return launch_qmm_bits<8, false>(a, dev, split);
+    const int sms = g_sms[dev].load(std::memory_order_relaxed);
+    const int tn128 = split == 1 ? qmm_tile_n(a.N, (a.M + 127) / 128, sms) : kTileN;
+    if (!a.xf16) return launch_qmm_bits<8, false>(a, dev, split, tn128);
     // x converted once: 256-row tiles where that needs no split and still fills half the
     // SMs (M = 2048 on 14336 x 4096: 743 -> 1205 TFLOP/s; on 4096 x 14336 one wave of
     // 128 such tiles against 1.7 waves of 128-row tiles)
-    const int sms = g_sms[dev].load(std::memory_order_relaxed);
     const int64_t tiles256 = ((a.N + kTileN - 1) / kTileN) * ((a.M + 255) / 256);
-    if (split == 1 && sms > 0 && 2 * tiles256 >= sms) return launch_qmm_bits<8, true, 256>(a, dev, split);
-    return launch_qmm_bits<8, true>(a, dev, split);
+    if (split == 1 && sms > 0 && 2 * tiles256 >= sms)
+        return launch_qmm_bits<8, true, 256>(a, dev, split, qmm_tile_n(a.N, (a.M + 255) / 256, sms));
+    return launch_qmm_bits<8, true>(a, dev, split, tn128);
 }
 
 // ---------------------------------------------------------------- expert-indexed matmul
@@ -998,6 +1021,8 @@ int64_t plan_bytes(int64_t R, int64_t E) { return (kPlanHeaderInts * 4 + 16 * pl
 template <int BITS>
 cudaError_t launch_gather_bits(const GatherArgs &g, int dev, int sms) {
     using C = Cfg<BITS, true>;
+    // rows of W per CTA on the row-tile count without the experts' partial tiles
+    const int tn = qmm_tile_n(g.N, (g.R + C::kTileM - 1) / C::kTileM, sms);
     const int bi = BITS == 8 ? 1 : 0;
     if (!g_attr_done_grouped[bi][dev].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(qmm_kernel<BITS, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1018,20 +1043,20 @@ cudaError_t launch_gather_bits(const GatherArgs &g, int dev, int sms) {
     if (!encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xg, (uint64_t)K, (uint64_t)R, (uint64_t)K * 2, kGroup,
                    C::kTileM, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, g.w, (uint64_t)K * BITS / 32, (uint64_t)E * N,
-                   (uint64_t)K * BITS / 8, C::kRowWords, kTileN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                   (uint64_t)K * BITS / 8, C::kRowWords, (uint32_t)tn, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, g.scales, (uint64_t)G, (uint64_t)E * N, (uint64_t)G * 2,
-                   kSBGroups, kTileN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                   kSBGroups, (uint32_t)tn, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, g.biases, (uint64_t)G, (uint64_t)E * N, (uint64_t)G * 2,
-                   kSBGroups, kTileN, CU_TENSOR_MAP_SWIZZLE_NONE))
+                   kSBGroups, (uint32_t)tn, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     const int64_t max_tiles = (g.R + C::kTileM - 1) / C::kTileM + g.E;
-    cfg.gridDim = dim3((unsigned)((N + kTileN - 1) / kTileN), (unsigned)max_tiles, 1);
+    cfg.gridDim = dim3((unsigned)((N + tn - 1) / tn), (unsigned)max_tiles, 1);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = g.stream;
     return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS, true, true>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(g.y), R, N,
-                              K, (unsigned long long)g.timeout_ns, g.status, (const int *)plan, 0);
+                              K, (unsigned long long)g.timeout_ns, g.status, (const int *)plan, 0, tn);
 }
 
 }  // namespace
