@@ -61,10 +61,7 @@ constexpr int kConvWarps = 16;
 constexpr int kThreads = (2 + kConvWarps) * 32;
 constexpr int kConvThreads = kConvWarps * 32;
 constexpr int kSBGroups = 8;           // groups of scales/biases per TMA box (16 bytes per row)
-constexpr int kRawStages = 2;
 constexpr int kSBStages = 2;
-constexpr int kBTileBytes = kTileN * 128;          // 32768: fp16 W, 256 rows x 64 k
-constexpr int kSBBytes = kTileN * kSBGroups * 2;   // 4096 (scales, and again biases)
 
 // Shared-memory layout for a code width (offsets from a 1024-aligned base).
 // 4-bit codes: 256 rows of x per CTA (two UMMA M=128 halves); 8-bit codes
@@ -77,20 +74,27 @@ constexpr int kSBBytes = kTileN * kSBGroups * 2;   // 4096 (scales, and again bi
 // raw x and code stages would not fit beside 256-row operand stages); with x
 // already fp16 there is no raw x stage and two converted stages of 256 rows
 // fit, which doubles the MMA work per converted W tile.
-template <int BITS, bool XPRE = false, int TM = (BITS == 4 ? 256 : 128)>
+// PAIR (without XPRE): the CTA holds half of the W tile (see qmm_kernel), which
+// leaves room for a third converted stage.
+template <int BITS, bool XPRE = false, int TM = (BITS == 4 ? 256 : 128), bool PAIR = false>
 struct Cfg {
     static constexpr int kTileM = TM;
     static constexpr int kHalves = kTileM / 128;                 // UMMA M=128 accumulators
-    static constexpr int kConvStages = XPRE ? ((BITS == 8 && TM == 256) ? 2 : 3) : 2;
+    static constexpr int kWRows = PAIR ? kTileN / 2 : kTileN;   // rows of W in this CTA's stages
+    static constexpr int kBTileBytes = kWRows * 128;             // fp16 W, kWRows rows x 64 k
+    static constexpr int kSBBytes = kWRows * kSBGroups * 2;      // scales (and again biases) per stage
+    static constexpr int kRawStages = 2;                          // raw code (and bf16 x) stages
+    static constexpr int kConvStages = PAIR ? (TM == 128 ? 4 : 3) : XPRE ? ((BITS == 8 && TM == 256) ? 2 : 3) : 2;
     static constexpr int kATileBytes = kTileM * 128;             // fp16 x, kTileM rows x 64 k
     static constexpr int kConvStageBytes = kATileBytes + kBTileBytes;
     static constexpr int kRawXBytes = XPRE ? 0 : kTileM * 128;   // bf16 x, same swizzled geometry
     static constexpr int kRowWords = kGroup * BITS / 32;         // code words per W row and group
-    static constexpr int kRawCodeBytes = kTileN * kRowWords * 4; // 8192 or 16384
+    static constexpr int kRawCodeBytes = kWRows * kRowWords * 4; // 8192 or 16384 (half in a pair)
     static constexpr int kRawStageBytes = kRawXBytes + kRawCodeBytes;
     // barriers: raw_full[2], raw_empty[2], sb_full[2], sb_empty[2], conv_full[S], conv_empty[S], acc_done,
-    // and with XPRE x_full[S] (the x copy of a converted stage has landed)
-    static constexpr int kNumBars = 2 * kRawStages + 2 * kSBStages + 2 * kConvStages + 1 + (XPRE ? kConvStages : 0);
+    // x_full[S] (with XPRE: the x copy of a converted stage has landed) and peer_full[S] (in a CTA
+    // pair: the other CTA's half of a converted stage is ready)
+    static constexpr int kNumBars = 2 * kRawStages + 2 * kSBStages + 4 * kConvStages + 1;
     static constexpr int kOffConv = 0;
     static constexpr int kOffRaw = kOffConv + kConvStages * kConvStageBytes;
     static constexpr int kOffSB = kOffRaw + kRawStages * kRawStageBytes;
@@ -99,7 +103,8 @@ struct Cfg {
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;     // + alignment slack
 };
 static_assert(Cfg<4>::kSmemBytes <= 232448 && Cfg<8>::kSmemBytes <= 232448 && Cfg<4, true>::kSmemBytes <= 232448 &&
-                  Cfg<8, true>::kSmemBytes <= 232448 && Cfg<8, true, 256>::kSmemBytes <= 232448,
+                  Cfg<8, true>::kSmemBytes <= 232448 && Cfg<8, true, 256>::kSmemBytes <= 232448 &&
+                  Cfg<4, false, 256, true>::kSmemBytes <= 232448 && Cfg<8, false, 128, true>::kSmemBytes <= 232448,
               "shared memory per CTA");
 // split-K partials received by a CTA (at most 7 sources x its 32 columns x the tile's rows) fit in
 // the stage memory in front of the barriers
@@ -150,6 +155,29 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     }
     return true;
 }
+// the same wait at cluster scope: the arrivals come from the other CTA of a pair
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, uint64_t deadline,
+                                                  const volatile int *abort_flag) {
+    while (!mbar_try_wait_cluster(bar, parity)) {
+        if (*abort_flag) return false;
+        if (global_timer() > deadline) return false;
+    }
+    return true;
+}
+// arrive on an mbarrier of another CTA of the cluster (its shared::cluster address)
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
@@ -166,6 +194,11 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
     return v;
 }
 __device__ __forceinline__ uint16_t lds16(uint32_t a) {
@@ -227,9 +260,10 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     d |= (uint64_t)2 << 61;                   // 128-byte swizzle
     return d;
 }
-// instruction descriptor: D f32, A f16, B f16, both K-major, M=128, N=tn (256 or 224)
-__host__ __device__ constexpr uint32_t umma_idesc(int tn) {
-    return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(tn >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+// instruction descriptor: D f32, A f16, B f16, both K-major, M (128, or 256 over a CTA pair),
+// N=tn (256 or 224)
+__host__ __device__ constexpr uint32_t umma_idesc(int tn, int m = 128) {
+    return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(tn >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -243,6 +277,25 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
+}
+// CTA pair (cta_group::2): one MMA of M = 256 rows of x, 128 from each CTA's A tile, over
+// N rows of W of which each CTA holds N/2 in its B tile (the first half in the even CTA);
+// each CTA's accumulators hold its own 128 rows.  Issued by the even CTA only.
+__device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// arrive on the mbarrier at this offset in both CTAs of the pair once the MMAs issued so far are done
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"((uint16_t)3)
+        : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
@@ -326,14 +379,26 @@ cudaError_t launch_plain(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaSt
 // W, scales and biases are E matrices stacked along N, and `plan` lists the
 // work tiles {expert, first row, rows} (see gather_plan_kernel); CTA row
 // blockIdx.y takes tile blockIdx.y and exits at once if there is none.
-template <int BITS, bool GROUPED, bool XPRE, int TM = (BITS == 4 ? 256 : 128)>
+// PAIR: a cluster of two CTAs (blockIdx.x 2j, 2j+1: W tile j, row tiles of x
+// 2 blockIdx.y and 2 blockIdx.y + 1; the pair lies along the cluster's x) shares one tile of
+// tn rows of W: each CTA loads and converts tn/2 of them (the even CTA the
+// first half) and its own TM rows of x, and the even CTA issues the MMAs for
+// both (tcgen05 cta_group::2, M = 256 across the pair), so every W element is
+// converted, stored and read from shared memory once per 2 TM rows of x.  Only
+// without a K split, and only where each CTA converts its own x tiles: there the
+// converters bound the step and the pair takes a quarter of their work away
+// (M = 2048 on 4096 x 14336: 214 -> 201 us); with x converted once the MMAs
+// bound it and the pair's MMAs ran slower than two single-CTA ones.
+template <int BITS, bool GROUPED, bool XPRE, int TM = (BITS == 4 ? 256 : 128), bool PAIR = false>
 __global__ void __launch_bounds__(kThreads, 1)
 qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
            const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_b,
            __nv_bfloat16 *__restrict__ y, int M, int N, int K, unsigned long long timeout_ns, int *status,
            const int *__restrict__ plan, int skip_copy, int tn) {
-    using C = Cfg<BITS, XPRE, TM>;
-    constexpr int kConvStages = C::kConvStages;
+    static_assert(!(PAIR && (GROUPED || XPRE)), "CTA pairs only on the plain matmul without x converted once");
+    using C = Cfg<BITS, XPRE, TM, PAIR>;
+    constexpr int kSBBytes = C::kSBBytes;
+    constexpr int kConvStages = C::kConvStages, kRawStages = C::kRawStages;
     constexpr int kTileM = C::kTileM, kATileBytes = C::kATileBytes, kConvStageBytes = C::kConvStageBytes;
     constexpr int kRawXBytes = C::kRawXBytes, kRawStageBytes = C::kRawStageBytes;
     constexpr int kOffConv = C::kOffConv, kOffRaw = C::kOffRaw, kOffSB = C::kOffSB, kOffMisc = C::kOffMisc;
@@ -351,6 +416,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     auto conv_empty = [&](int s) { return bar0 + 8 * (2 * kRawStages + 2 * kSBStages + kConvStages + s); };
     const uint32_t acc_done = bar0 + 8 * (2 * kRawStages + 2 * kSBStages + 2 * kConvStages);
     auto x_full = [&](int s) { return acc_done + 8 * (1 + s); };
+    auto peer_full = [&](int s) { return acc_done + 8 * (1 + kConvStages + s); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
 
@@ -358,10 +424,13 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     const int lane = threadIdx.x & 31;
     // tn: rows of W per CTA, kTileN or 224 (a full last wave where 256 would leave SMs
     // idle; only without a K split); the stage memory is laid out for kTileN
-    const int n0 = blockIdx.x * tn;
-    int m0 = blockIdx.y * kTileM;   // first row of x (and of y) of the tile
+    // rank in the CTA pair (0: issues the MMAs) and the rows of W this CTA loads and converts
+    const uint32_t prank = PAIR ? cluster_rank() : 0u;
+    const int n0 = (PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x) * tn;
+    int m0 = (PAIR ? 2 * (int)blockIdx.y + (int)prank : (int)blockIdx.y) * kTileM;   // first row of x (and y)
     int m_end = M;                  // rows from m_end on are not this tile's
-    int wrow0 = n0;                 // first row of W (in the stacked experts: expert * N + n0)
+    const int wrows = PAIR ? tn / 2 : tn;
+    int wrow0 = n0 + (int)prank * wrows;   // first of them (in the stacked experts: expert * N + ...)
     if (GROUPED) {
         if ((int)blockIdx.y >= __ldg(plan)) return;   // no tile: nothing set up yet
         const int4 t = __ldg(reinterpret_cast<const int4 *>(plan + kPlanHeaderInts) + blockIdx.y);
@@ -389,6 +458,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         }
         for (int s = 0; s < kConvStages; ++s) {
             if (XPRE) mbar_init(x_full(s), 1);
+            if (PAIR) mbar_init(peer_full(s), 1);
             mbar_init(conv_full(s), kConvWarps);
             mbar_init(conv_empty(s), 1);
         }
@@ -397,13 +467,26 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
-                     "r"(kTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if constexpr (PAIR) {
+            // one warp of each CTA of the pair, together: the same columns in both
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_addr(tmem_slot)),
+                         "r"(kTmemCols)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_addr(tmem_slot)),
+                         "r"(kTmemCols)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    if (PAIR)
+        cluster_sync();   // both CTAs' barriers initialised before either signals the other
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     griddep_launch();
@@ -495,7 +578,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                         break;
                     }
                     const uint32_t dst = base + kOffSB + ss * 2 * kSBBytes;
-                    mbar_expect_tx(sb_full(ss), (uint32_t)(2 * tn * kSBGroups * 2));
+                    mbar_expect_tx(sb_full(ss), (uint32_t)(2 * wrows * kSBGroups * 2));
                     tma_load_2d(dst, &tm_s, g0 + j * kSBGroups, wrow0, sb_full(ss));
                     tma_load_2d(dst + kSBBytes, &tm_b, g0 + j * kSBGroups, wrow0, sb_full(ss));
                     issued_sb = j + 1;
@@ -506,7 +589,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 }
                 const uint32_t dst = base + kOffRaw + rs * kRawStageBytes;
                 if (!(skip_first && i == 0)) {
-                    mbar_expect_tx(raw_full(rs), (uint32_t)(kRawXBytes + tn * C::kRowWords * 4));
+                    mbar_expect_tx(raw_full(rs), (uint32_t)(kRawXBytes + wrows * C::kRowWords * 4));
                     if (!XPRE) tma_load_2d(dst, &tm_x, (g0 + i) * kGroup, m0, raw_full(rs));
                     tma_load_2d(dst + kRawXBytes, &tm_w, (g0 + i) * C::kRowWords, wrow0, raw_full(rs));
                 }
@@ -526,14 +609,27 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             }
             if (!ok) fail();   // the copies issued are drained at the end of the kernel
         }
+    } else if (warp == 1 && PAIR && prank != 0) {
+        // ------------------------------------------------------------ pair: stage readiness to the MMA CTA
+        if (lane == 0) {
+            for (int i = 0; i < steps; ++i) {
+                const int cs = i % kConvStages;
+                if (!mbar_wait(conv_full(cs), (i / kConvStages) & 1, deadline, abort_flag)) {
+                    fail();
+                    break;
+                }
+                mbar_arrive_cluster(map_cta(peer_full(cs), 0));
+            }
+        }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = umma_idesc(tn);
+            const uint32_t idesc = umma_idesc(tn, PAIR ? 256 : 128);
             for (int i = 0; i < steps; ++i) {
                 const int cs = i % kConvStages;
                 if (!mbar_wait(conv_full(cs), (i / kConvStages) & 1, deadline, abort_flag) ||
-                    (XPRE && !mbar_wait(x_full(cs), (i / kConvStages) & 1, deadline, abort_flag))) {
+                    (XPRE && !mbar_wait(x_full(cs), (i / kConvStages) & 1, deadline, abort_flag)) ||
+                    (PAIR && !mbar_wait_cluster(peer_full(cs), (i / kConvStages) & 1, deadline, abort_flag))) {
                     fail();
                     break;
                 }
@@ -544,14 +640,25 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 for (int kk = 0; kk < kGroup / 16; ++kk) {
                     const uint64_t bd = sw128_desc(b0 + kk * 32);
 #pragma unroll
-                    for (int h = 0; h < C::kHalves; ++h)
-                        umma_f16(tmem + h * kTileN, sw128_desc(a0 + h * (128 * 128) + kk * 32), bd, idesc,
-                                 (i > 0 || kk > 0) ? 1u : 0u);
+                    for (int h = 0; h < C::kHalves; ++h) {
+                        if constexpr (PAIR)
+                            umma_f16_pair(tmem + h * kTileN, sw128_desc(a0 + h * (128 * 128) + kk * 32), bd, idesc,
+                                          (i > 0 || kk > 0) ? 1u : 0u);
+                        else
+                            umma_f16(tmem + h * kTileN, sw128_desc(a0 + h * (128 * 128) + kk * 32), bd, idesc,
+                                     (i > 0 || kk > 0) ? 1u : 0u);
+                    }
                 }
-                umma_commit(conv_empty(cs));
+                if constexpr (PAIR)
+                    umma_commit_pair(conv_empty(cs));
+                else
+                    umma_commit(conv_empty(cs));
             }
             // acc_done fires when every MMA issued so far has completed (also on abort)
-            umma_commit(acc_done);
+            if constexpr (PAIR)
+                umma_commit_pair(acc_done);
+            else
+                umma_commit(acc_done);
         }
     } else {
         // ------------------------------------------------------------ converters
@@ -582,27 +689,35 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 const uint32_t off = (uint32_t)((c * kConvThreads + t) * 16);
                 sts128(conv + off, x_chunk_f16<BITS>(lds128(raw + off)));
             }
-            // W: thread t takes half of row r = t / 2 (chunks 4h..4h+3, h = t % 2) and
-            // converts the row's scale and bias once; each chunk of 8 codes
-            // becomes 8 fp16 weights at row r, chunk c ^ (r & 7)
+            // W: thread t takes chunks kCpt*p .. kCpt*p + kCpt-1 of row r = t / kTpr
+            // (p = t % kTpr) and converts the row's scale and bias once; each chunk of
+            // 8 codes becomes 8 fp16 weights at row r, chunk c ^ (r & 7)
             const uint32_t sb = base + kOffSB + ss * 2 * kSBBytes;
             const int g8 = i % kSBGroups;
-            static_assert(kConvThreads == 2 * kTileN, "two converter threads per W row");
-            if ((t >> 1) < tn) {   // rows of W past tn are not loaded and not used
-                const int r = t >> 1, hw = t & 1;
+            constexpr int kTpr = PAIR ? 4 : 2, kCpt = 8 / kTpr;   // threads per row, chunks per thread
+            static_assert(kConvThreads == kTpr * (PAIR ? kTileN / 2 : kTileN), "converter threads per W row");
+            if (t / kTpr < wrows) {   // rows past wrows are not loaded and not used
+                const int r = t / kTpr, hw = t % kTpr;
                 const __half sh = __float2half_rn(__uint_as_float((uint32_t)lds16(sb + (r * kSBGroups + g8) * 2) << 16));
                 const __half bh =
                     __float2half_rn(__uint_as_float((uint32_t)lds16(sb + kSBBytes + (r * kSBGroups + g8) * 2) << 16));
                 const uint32_t s2 = (uint32_t)__half_as_ushort(sh) * 0x00010001u;
                 const uint32_t b2 = (uint32_t)__half_as_ushort(bh) * 0x00010001u;
-                const uint32_t wrow = raw + kRawXBytes + r * (C::kRowWords * 4) + hw * (C::kRowWords * 2);
+                const uint32_t wrow = raw + kRawXBytes + r * (C::kRowWords * 4) + hw * (C::kRowWords * 4 / kTpr);
                 if (BITS == 4) {
                     // word c of the row holds chunk c: pairs (p, p+4) from the word shifted by 4p
-                    const uint4 wv = lds128(wrow);
+                    uint32_t wvs[kCpt];
+                    if constexpr (kCpt == 4) {
+                        const uint4 v = lds128(wrow);
+                        wvs[0] = v.x, wvs[1] = v.y, wvs[2] = v.z, wvs[3] = v.w;
+                    } else {
+                        const uint2 v = lds64(wrow);
+                        wvs[0] = v.x, wvs[1] = v.y;
+                    }
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const uint32_t w = e == 0 ? wv.x : e == 1 ? wv.y : e == 2 ? wv.z : wv.w;
-                        const int c = 4 * hw + e;
+                    for (int e = 0; e < kCpt; ++e) {
+                        const uint32_t w = wvs[e];
+                        const int c = kCpt * hw + e;
                         uint4 o;
                         o.x = dequant_pair(code_pair_f16(w, magic), s2, b2, off2);
                         o.y = dequant_pair(code_pair_f16(w >> 4, magic), s2, b2, off2);
@@ -613,12 +728,12 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 } else {
                     // words 2c, 2c+1 hold chunk c: bytes (0,2) and (1,3) of each word pair up
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
+                    for (int hh = 0; hh < kCpt / 2; ++hh) {
                         const uint4 wv = lds128(wrow + hh * 16);
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
                             const uint32_t wa = e == 0 ? wv.x : wv.z, wb = e == 0 ? wv.y : wv.w;
-                            const int c = 4 * hw + 2 * hh + e;
+                            const int c = kCpt * hw + 2 * hh + e;
                             uint4 o;
                             o.x = dequant_pair(byte_pair_f16(wa, magic), s2, b2, off2);
                             o.y = dequant_pair(byte_pair_f16(wa >> 8, magic), s2, b2, off2);
@@ -728,10 +843,18 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         }
     }
     tc_fence_before();
-    __syncthreads();
+    if (PAIR)
+        cluster_sync();   // neither CTA leaves while the other may still signal it or read its stages
+    else
+        __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+        if constexpr (PAIR)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                         : "memory");
+        else
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                         : "memory");
     }
 }
 
@@ -766,6 +889,7 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *gaddr, uint
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_attr_done[7][kMaxDevices];
 std::atomic<int> g_attr_done_grouped[2][kMaxDevices];
+std::atomic<int> g_attr_done_pair[2][kMaxDevices];   // CTA-pair instances, by code width
 std::atomic<int> g_sms[kMaxDevices];
 // clusters of 2, 4, 8 CTAs that can be resident at once, per code width (0: not yet asked; -1: none)
 std::atomic<int> g_max_clusters[3][3][kMaxDevices];
@@ -788,6 +912,14 @@ int qmm_tile_n(int64_t n_rows, int64_t row_tiles, int sms) {
         return (tiles + sms - 1) / sms * tn;
     };
     return cost(224) < cost(kTileN) ? 224 : kTileN;
+}
+
+// CTA pairs (each W tile converted once per 2 TM rows of x) without a K split and
+// without x converted once, where the row tiles pair up with at most one padding
+// tile in five
+bool qmm_pair(int64_t M, int tm, int split) {
+    const int64_t mtiles = (M + tm - 1) / tm;
+    return split == 1 && mtiles >= 2 && (mtiles % 2 == 0 || mtiles >= 5);
 }
 
 // g_attr_done slot of a kernel instance without the expert index
@@ -857,16 +989,20 @@ int qmm_split(const MatmulArgs &a, int dev) {
 
 // split: K split across a cluster of this many CTAs (qmm_split)
 // tn: rows of W per CTA (kTileN, or 224 without a K split; see qmm_tile_n)
-template <int BITS, bool XPRE, int TM = (BITS == 4 ? 256 : 128)>
+// PAIR: CTA pairs along M sharing each W tile (no K split; see qmm_kernel)
+template <int BITS, bool XPRE, int TM = (BITS == 4 ? 256 : 128), bool PAIR = false>
 cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev, int split, int tn = kTileN) {
-    using C = Cfg<BITS, XPRE, TM>;
-    constexpr int bi = attr_slot<BITS, XPRE, TM>();
-    if (!g_attr_done[bi][dev].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(qmm_kernel<BITS, false, XPRE, TM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::kSmemBytes);
+    using C = Cfg<BITS, XPRE, TM, PAIR>;
+    std::atomic<int> &attr_done =
+        PAIR ? g_attr_done_pair[BITS == 8 ? 1 : 0][dev] : g_attr_done[attr_slot<BITS, XPRE, TM>()][dev];
+    if (!attr_done.load(std::memory_order_acquire)) {
+        cudaError_t e = cudaFuncSetAttribute(qmm_kernel<BITS, false, XPRE, TM, PAIR>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return e;
-        g_attr_done[bi][dev].store(1, std::memory_order_release);
+        attr_done.store(1, std::memory_order_release);
     }
+    if (PAIR && split != 1) return cudaErrorInvalidConfiguration;
+    const uint32_t wbox = (uint32_t)(PAIR ? tn / 2 : tn);   // rows of W one CTA loads
     const int M = (int)a.M, N = (int)a.N, K = (int)a.K, G = K / 64;
     if (XPRE) {
         const int64_t vecs = (int64_t)M * K / 8;
@@ -879,15 +1015,17 @@ cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev, int split, int tn = kT
     if (!encode_2d(&tx, XPRE ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, XPRE ? a.xf16 : a.x, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, kGroup,
                    C::kTileM, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.w, (uint64_t)K * BITS / 32, (uint64_t)N,
-                   (uint64_t)K * BITS / 8, C::kRowWords, (uint32_t)tn, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                   (uint64_t)K * BITS / 8, C::kRowWords, wbox, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.scales, (uint64_t)G, (uint64_t)N, (uint64_t)G * 2, kSBGroups,
-                   (uint32_t)tn, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                   wbox, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.biases, (uint64_t)G, (uint64_t)N, (uint64_t)G * 2, kSBGroups,
-                   (uint32_t)tn, CU_TENSOR_MAP_SWIZZLE_NONE))
+                   wbox, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     if (split > 1 && tn != kTileN) return cudaErrorInvalidConfiguration;   // the K split owns 256 / split columns
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((N + tn - 1) / tn), (unsigned)((M + C::kTileM - 1) / C::kTileM), 1);
+    const int64_t mtiles = (M + C::kTileM - 1) / C::kTileM, ntiles = (N + tn - 1) / tn;
+    cfg.gridDim = PAIR ? dim3((unsigned)(2 * ntiles), (unsigned)((mtiles + 1) / 2), 1)
+                       : dim3((unsigned)ntiles, (unsigned)mtiles, 1);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = a.stream;
@@ -905,10 +1043,16 @@ cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev, int split, int tn = kT
         attr[na].val.clusterDim.y = 1;
         attr[na].val.clusterDim.z = (unsigned)split;
         ++na;
+    } else if (PAIR) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 2;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
     }
     cfg.attrs = attr;
     cfg.numAttrs = (unsigned)na;
-    return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS, false, XPRE, TM>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(a.y), M,
+    return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS, false, XPRE, TM, PAIR>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(a.y), M,
                               N, K, (unsigned long long)a.timeout_ns, a.status, (const int *)nullptr,
                               a.debug_skip_copy ? 1 : 0, tn);
 }
@@ -932,12 +1076,16 @@ cudaError_t launch_qmm(const MatmulArgs &a) {
             qmm_split<4, 128>(a, dev) == split)
             return a.xf16 ? launch_qmm_bits<4, true, 128>(a, dev, split) : launch_qmm_bits<4, false, 128>(a, dev, split);
         const int tn = split == 1 ? qmm_tile_n(a.N, (a.M + 255) / 256, sms) : kTileN;
+        if (!a.xf16 && qmm_pair(a.M, 256, split)) return launch_qmm_bits<4, false, 256, true>(a, dev, split, tn);
         return a.xf16 ? launch_qmm_bits<4, true>(a, dev, split, tn) : launch_qmm_bits<4, false>(a, dev, split, tn);
     }
     const int split = qmm_split<8>(a, dev);
     const int sms = g_sms[dev].load(std::memory_order_relaxed);
     const int tn128 = split == 1 ? qmm_tile_n(a.N, (a.M + 127) / 128, sms) : kTileN;
-    if (!a.xf16) return launch_qmm_bits<8, false>(a, dev, split, tn128);
+    const bool pair128 = qmm_pair(a.M, 128, split);
+    if (!a.xf16)
+        return pair128 ? launch_qmm_bits<8, false, 128, true>(a, dev, split, tn128)
+                       : launch_qmm_bits<8, false>(a, dev, split, tn128);
     // x converted once: 256-row tiles where that needs no split and still fills half the
     // SMs (M = 2048 on 14336 x 4096: 743 -> 1205 TFLOP/s; on 4096 x 14336 one wave of
     // 128 such tiles against 1.7 waves of 128-row tiles)

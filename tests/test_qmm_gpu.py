@@ -141,12 +141,27 @@ def test_qmm_split_k(dev, M, N, K, bits):
 
 
 @pytest.mark.parametrize("M,N,K,bits", [
+    (512, 256, 512, 4), (1100, 300, 512, 4), (2048, 600, 512, 4),    # 256-row tiles; 5 row tiles: one padding CTA
+    (512, 300, 512, 8), (640, 257, 512, 8), (1300, 520, 512, 8),     # 128-row tiles
+])
+def test_qmm_cta_pairs(dev, M, N, K, bits):
+    """Without a K split (K = 512: one block of 8 groups) and with at least two
+    row tiles of x, CTA pairs share each W tile: each converts half of it and
+    one MMA over 256 rows of x spans both.  Every output against the oracle,
+    with ragged M and N and a pair whose second CTA has no rows of x."""
+    check_full(dev, M, N, K, 1500 + M + N, bits=bits)
+
+
+@pytest.mark.parametrize("M,N,K,bits", [
     (17, 64, 512, 4), (300, 700, 2048, 4), (256, 512, 4096, 4), (2048, 1024, 4096, 4),
     (129, 300, 1024, 8), (1000, 257, 4096, 8),
+    (1024, 300, 512, 4), (640, 257, 512, 8), (2048, 4864, 512, 8),   # CTA pairs without the workspace
 ])
 def test_qmm_workspace_path_same_bits(dev, M, N, K, bits):
     """With a workspace, x is converted to fp16 once and copied straight into
-    the MMA tiles: the same bits as without, and the oracle's result class."""
+    the MMA tiles: the same bits as without (also where the call without the
+    workspace runs on CTA pairs and the one with it on single CTAs), and the
+    oracle's result class."""
     import torch
     w = synth.make_weights(N, K, 1400 + M, bits=bits)
     x = synth.make_x(M, K, 1400 + M)
@@ -187,12 +202,15 @@ def test_output_beyond_2_31_elements(dev):
     assert_parity(got, yb, rms=rms, what=f"qmm sampled M={M} N={N} K={K} (y beyond 2^31 elements)")
 
 
-@pytest.mark.parametrize("M,N,K", [(64, 512, 1024), (256, 512, 4096)])   # one tile; split K over a cluster
+@pytest.mark.parametrize("M,N,K", [(64, 512, 1024), (256, 512, 4096),   # one tile; split K over a cluster
+                                   (512, 256, 512)])                     # a CTA pair
 def test_qmm_bounded_wait_timeout_reports_status(dev, M, N, K):
     """The test hook makes the first CTA's producer leave out its first copy:
     the converters' bounded wait expires, the kernel records a timeout (the
-    other CTAs of a split-K cluster still meet it at the cluster barriers),
-    the host reads AQ_ERR_TIMEOUT, and a normal call right after is correct."""
+    other CTAs of a split-K cluster still meet it at the cluster barriers; the
+    other CTA of a pair waits out its own bounded waits for the stages that
+    never get consumed), the host reads AQ_ERR_TIMEOUT, and a normal call
+    right after is correct."""
     import torch
     w = synth.make_weights(N, K, 12)
     x = synth.make_x(M, K, 12)
