@@ -152,6 +152,25 @@ def test_qmm_cta_pairs(dev, M, N, K, bits):
     check_full(dev, M, N, K, 1500 + M + N, bits=bits)
 
 
+@pytest.mark.parametrize("M,N,K,bits", [(256, 256, 512, 4), (256, 512, 4096, 4), (512, 256, 512, 4),
+                                        (512, 300, 512, 8)])   # one CTA; split K; CTA pairs
+def test_qmm_pdl_flag_same_bits(dev, M, N, K, bits):
+    """Programmatic dependent launch beside the cluster launch of a K split or a
+    CTA pair: the same bits as a plain launch, after a preceding kernel that
+    writes x on the same stream."""
+    import torch
+    w = synth.make_weights(N, K, 1600 + M, bits=bits)
+    x = synth.make_x(M, K, 1600 + M)
+    xt, wt, st, bt = upload(x, w, dev)
+    a = aq.matmul(xt, wt, st, bt, kernel="qmm", bits=bits)
+    x2 = torch.zeros_like(xt)
+    x2.copy_(xt)                     # the kernel before the launch writes its x
+    b = aq.matmul(x2, wt, st, bt, kernel="qmm", bits=bits, pdl=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    assert aq.aq_read_device_status(torch.cuda.current_stream().cuda_stream) == aq.AQ_OK
+
+
 @pytest.mark.parametrize("M,N,K,bits", [
     (17, 64, 512, 4), (300, 700, 2048, 4), (256, 512, 4096, 4), (2048, 1024, 4096, 4),
     (129, 300, 1024, 8), (1000, 257, 4096, 8),
