@@ -383,9 +383,13 @@ cudaError_t launch_plain(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaSt
 // W, scales and biases are E matrices stacked along N, and `plan` lists the
 // work tiles {expert, first row, rows} (see gather_plan_kernel); CTA row
 // blockIdx.y takes tile blockIdx.y and exits at once if there is none.
-// PAIR: a cluster of two CTAs (blockIdx.x 2j, 2j+1: W tile j, row tiles of x
-// 2 blockIdx.y and 2 blockIdx.y + 1; the pair lies along the cluster's x) shares one tile of
-// tn rows of W: each CTA loads and converts tn/2 of them (the even CTA the
+// Plain matmul, order of the tiles (mfast): where W is the larger operand, row
+// tiles of x run fastest (blockIdx.x: row tile of x, blockIdx.y: tile of W), so
+// that a wave of CTAs finishes a band of W tiles (each read from DRAM once) while
+// x stays in L2; otherwise W tiles run fastest (blockIdx.x: tile of W).
+// PAIR: a cluster of two CTAs, along the cluster's x (row tiles 2j and 2j + 1 of
+// x: blockIdx.x = 2j + rank with mfast, else blockIdx.x = 2 (W tile) + rank and
+// blockIdx.y = j), shares one tile of tn rows of W: each CTA loads and converts tn/2 of them (the even CTA the
 // first half) and its own TM rows of x, and the even CTA issues the MMAs for
 // both (tcgen05 cta_group::2, M = 256 across the pair), so every W element is
 // converted, stored and read from shared memory once per 2 TM rows of x.  Only
@@ -398,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
            const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_b,
            __nv_bfloat16 *__restrict__ y, int M, int N, int K, unsigned long long timeout_ns, int *status,
-           const int *__restrict__ plan, int skip_copy, int tn) {
+           const int *__restrict__ plan, int skip_copy, int tn, int mfast) {
     static_assert(!(PAIR && (GROUPED || XPRE)), "CTA pairs only on the plain matmul without x converted once");
     using C = Cfg<BITS, XPRE, TM, PAIR>;
     constexpr int kSBBytes = C::kSBBytes;
@@ -430,8 +434,9 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     // idle; only without a K split); the stage memory is laid out for kTileN
     // rank in the CTA pair (0: issues the MMAs) and the rows of W this CTA loads and converts
     const uint32_t prank = PAIR ? cluster_rank() : 0u;
-    const int n0 = (PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x) * tn;
-    int m0 = (PAIR ? 2 * (int)blockIdx.y + (int)prank : (int)blockIdx.y) * kTileM;   // first row of x (and y)
+    const int bx = (int)blockIdx.x, by = (int)blockIdx.y;
+    const int n0 = (GROUPED ? bx : mfast ? by : PAIR ? bx >> 1 : bx) * tn;
+    int m0 = (GROUPED ? 0 : mfast ? bx : PAIR ? 2 * by + (int)prank : by) * kTileM;   // first row of x (and y)
     int m_end = M;                  // rows from m_end on are not this tile's
     const int wrows = PAIR ? tn / 2 : tn;
     int wrow0 = n0 + (int)prank * wrows;   // first of them (in the stacked experts: expert * N + ...)
@@ -1028,8 +1033,12 @@ cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev, int split, int tn = kT
     if (split > 1 && tn != kTileN) return cudaErrorInvalidConfiguration;   // the K split owns 256 / split columns
     cudaLaunchConfig_t cfg = {};
     const int64_t mtiles = (M + C::kTileM - 1) / C::kTileM, ntiles = (N + tn - 1) / tn;
-    cfg.gridDim = PAIR ? dim3((unsigned)(2 * ntiles), (unsigned)((mtiles + 1) / 2), 1)
-                       : dim3((unsigned)ntiles, (unsigned)mtiles, 1);
+    // row tiles of x fastest where W has more bytes than x (see qmm_kernel)
+    const int mfast = (int64_t)N * BITS / 8 > (int64_t)M * 2 ? 1 : 0;
+    const int64_t gx = mfast ? (PAIR ? (mtiles + 1) / 2 * 2 : mtiles) : (PAIR ? 2 * ntiles : ntiles);
+    const int64_t gy = mfast ? ntiles : (PAIR ? (mtiles + 1) / 2 : mtiles);
+    if (gy > 65535) return cudaErrorInvalidConfiguration;
+    cfg.gridDim = dim3((unsigned)gx, (unsigned)gy, 1);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = a.stream;
@@ -1058,7 +1067,7 @@ cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev, int split, int tn = kT
     cfg.numAttrs = (unsigned)na;
     return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS, false, XPRE, TM, PAIR>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(a.y), M,
                               N, K, (unsigned long long)a.timeout_ns, a.status, (const int *)nullptr,
-                              a.debug_skip_copy ? 1 : 0, tn);
+                              a.debug_skip_copy ? 1 : 0, tn, mfast);
 }
 }  // namespace
 
@@ -1208,7 +1217,7 @@ cudaError_t launch_gather_bits(const GatherArgs &g, int dev, int sms) {
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = g.stream;
     return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS, true, true>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(g.y), R, N,
-                              K, (unsigned long long)g.timeout_ns, g.status, (const int *)plan, 0, tn);
+                              K, (unsigned long long)g.timeout_ns, g.status, (const int *)plan, 0, tn, 0);
 }
 
 }  // namespace
