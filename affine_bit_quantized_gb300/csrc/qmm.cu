@@ -1034,7 +1034,7 @@ cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev, int split, int tn = kT
     cudaLaunchConfig_t cfg = {};
     const int64_t mtiles = (M + C::kTileM - 1) / C::kTileM, ntiles = (N + tn - 1) / tn;
     // row tiles of x fastest where W has more bytes than x (see qmm_kernel)
-    const int mfast = (int64_t)N * BITS / 8 > (int64_t)M * 2 ? 1 : 0;
+    const int mfast = (int64_t)N * BITS / 8 > (int64_t)M * 2 && ntiles <= 65535 ? 1 : 0;
     const int64_t gx = mfast ? (PAIR ? (mtiles + 1) / 2 * 2 : mtiles) : (PAIR ? 2 * ntiles : ntiles);
     const int64_t gy = mfast ? ntiles : (PAIR ? (mtiles + 1) / 2 : mtiles);
     if (gy > 65535) return cudaErrorInvalidConfiguration;
