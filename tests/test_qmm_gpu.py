@@ -143,6 +143,7 @@ def test_qmm_split_k(dev, M, N, K, bits):
 @pytest.mark.parametrize("M,N,K,bits", [
     (512, 256, 512, 4), (1100, 300, 512, 4), (2048, 600, 512, 4),    # 256-row tiles; 5 row tiles: one padding CTA
     (512, 300, 512, 8), (640, 257, 512, 8), (1300, 520, 512, 8),     # 128-row tiles
+    (512, 4864, 512, 4), (640, 2600, 512, 8),                        # W the larger operand: row tiles fastest
 ])
 def test_qmm_cta_pairs(dev, M, N, K, bits):
     """Without a K split (K = 512: one block of 8 groups) and with at least two
