@@ -327,6 +327,25 @@ def run_case_other(args):
     print(json.dumps(out), flush=True)
 
 
+def check_side_rates(per_matrix, small_batch, eight_bit, qmm, nvfp4, moe, read_peak, bf16_peak):
+    """A side measurement far above its ceiling timed launches that did no work
+    (a capture that recorded nothing, a call that returned early): refuse to
+    print it.  Bandwidths are held against the measured read ceiling, tensor
+    rates against the bf16 burst peak, each with 50 % to spare."""
+    bad = []
+    for sec in (per_matrix, small_batch, eight_bit, nvfp4):
+        for name, e in (sec or {}).items():
+            if "gbs" in e and e["gbs"] > 1.5 * read_peak:
+                bad.append(f"{name}: {e['gbs']} GB/s")
+    for sec in (qmm, moe):
+        for name, e in (sec or {}).items():
+            for key in ("tflops", "without_workspace_tflops"):
+                if key in e and e[key] > 1.5 * bf16_peak:
+                    bad.append(f"{name}: {e[key]} TFLOP/s")
+    if bad:
+        raise RuntimeError("side measurements above any ceiling (no work timed): " + "; ".join(bad))
+
+
 def kernel_source_hash() -> str:
     """Hash of the chained kernel's sources with comments and blank space taken
     out (an edit of a comment leaves the captured traffic valid)."""
@@ -714,7 +733,7 @@ def main():
             def mlaunch(i, wt=wt, st=st, bt=bt, xm=xm, ym=ym, wsm=wsm, N=N, K=K):
                 rc = lib.aq_gather_qmm_bf16(xm.data_ptr(), wt.data_ptr(), st.data_ptr(), bt.data_ptr(), lt.data_ptr(),
                                             rt.data_ptr(), ym.data_ptr(), R_moe, T_moe, N, K, synth.MIXTRAL_EXPERTS, 64,
-                                            4, wsm.data_ptr(), wsm.numel(), cur.cuda_stream)
+                                            4, wsm.data_ptr(), wsm.numel(), sh())
                 if rc != aq.AQ_OK:
                     raise aq.AqError(rc, "aq_gather_qmm_bf16")
 
@@ -730,6 +749,7 @@ def main():
         per_matrix = small_batch = eight_bit = qmm = nvfp4 = moe = None
     else:
         per_matrix, small_batch, eight_bit, qmm, nvfp4, moe = side_sections()
+        check_side_rates(per_matrix, small_batch, eight_bit, qmm, nvfp4, moe, read_peak, bf16_peak)
 
     # ---- CPU baseline: the oracle on two layers of the same workload, host cores
     cpu = None

@@ -90,3 +90,16 @@ def test_reference_arm_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_side_measurements_above_every_ceiling_are_refused():
+    """A side measurement far above the device's ceilings timed no work (a
+    graph capture that recorded nothing): the benchmark refuses to print it."""
+    ok_moe = {"w1_gate": {"us_per_call": 450.0, "tflops": 1068.7}}
+    bad_moe = {"w1_gate": {"us_per_call": 0.73, "tflops": 659315.1}}
+    per_matrix = {"lm_head": {"us_per_call": 49.4, "gbs": 5985.0}}
+    bench.check_side_rates(per_matrix, None, None, None, None, ok_moe, 7450.0, 1915.6)
+    with pytest.raises(RuntimeError, match="no work timed"):
+        bench.check_side_rates(per_matrix, None, None, None, None, bad_moe, 7450.0, 1915.6)
+    with pytest.raises(RuntimeError, match="lm_head"):
+        bench.check_side_rates({"lm_head": {"gbs": 60000.0}}, None, None, None, None, None, 7450.0, 1915.6)
