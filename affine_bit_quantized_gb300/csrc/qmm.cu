@@ -430,16 +430,16 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // tn: rows of W per CTA, kTileN or 224 (a full last wave where 256 would leave SMs
-    // idle; only without a K split); the stage memory is laid out for kTileN
-    // rank in the CTA pair (0: issues the MMAs) and the rows of W this CTA loads and converts
+    // tn: rows of W per output tile (per CTA, or per CTA pair), kTileN or 224 (a full
+    // last wave where 256 would leave SMs idle; only without a K split); the stage
+    // memory is laid out for kTileN.  prank: rank in the CTA pair (0 issues the MMAs).
     const uint32_t prank = PAIR ? cluster_rank() : 0u;
     const int bx = (int)blockIdx.x, by = (int)blockIdx.y;
     const int n0 = (GROUPED ? bx : mfast ? by : PAIR ? bx >> 1 : bx) * tn;
     int m0 = (GROUPED ? 0 : mfast ? bx : PAIR ? 2 * by + (int)prank : by) * kTileM;   // first row of x (and y)
     int m_end = M;                  // rows from m_end on are not this tile's
-    const int wrows = PAIR ? tn / 2 : tn;
-    int wrow0 = n0 + (int)prank * wrows;   // first of them (in the stacked experts: expert * N + ...)
+    const int wrows = PAIR ? tn / 2 : tn;   // rows of W this CTA loads and converts
+    int wrow0 = n0 + (int)prank * wrows;    // the first of them (in the stacked experts: expert * N + ...)
     if (GROUPED) {
         if ((int)blockIdx.y >= __ldg(plan)) return;   // no tile: nothing set up yet
         const int4 t = __ldg(reinterpret_cast<const int4 *>(plan + kPlanHeaderInts) + blockIdx.y);
