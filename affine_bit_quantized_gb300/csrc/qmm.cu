@@ -84,7 +84,7 @@ struct Cfg {
     static constexpr int kBTileBytes = kWRows * 128;             // fp16 W, kWRows rows x 64 k
     static constexpr int kSBBytes = kWRows * kSBGroups * 2;      // scales (and again biases) per stage
     static constexpr int kRawStages = 2;                          // raw code (and bf16 x) stages
-    static constexpr int kConvStages = PAIR ? (TM == 128 ? 4 : 3) : XPRE ? ((BITS == 8 && TM == 256) ? 2 : 3) : 2;
+    static constexpr int kConvStages = PAIR ? (TM == 128 ? 4 : BITS == 8 ? 2 : 3) : XPRE ? ((BITS == 8 && TM == 256) ? 2 : 3) : 2;
     static constexpr int kATileBytes = kTileM * 128;             // fp16 x, kTileM rows x 64 k
     static constexpr int kConvStageBytes = kATileBytes + kBTileBytes;
     static constexpr int kRawXBytes = XPRE ? 0 : kTileM * 128;   // bf16 x, same swizzled geometry
@@ -104,7 +104,8 @@ struct Cfg {
 };
 static_assert(Cfg<4>::kSmemBytes <= 232448 && Cfg<8>::kSmemBytes <= 232448 && Cfg<4, true>::kSmemBytes <= 232448 &&
                   Cfg<8, true>::kSmemBytes <= 232448 && Cfg<8, true, 256>::kSmemBytes <= 232448 &&
-                  Cfg<4, false, 256, true>::kSmemBytes <= 232448 && Cfg<8, false, 128, true>::kSmemBytes <= 232448,
+                  Cfg<4, false, 256, true>::kSmemBytes <= 232448 && Cfg<8, false, 128, true>::kSmemBytes <= 232448 &&
+                  Cfg<8, false, 256, true>::kSmemBytes <= 232448,
               "shared memory per CTA");
 // split-K partials received by a CTA (at most 7 sources x its 32 columns x the tile's rows) fit in
 // the stage memory in front of the barriers
@@ -898,7 +899,7 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *gaddr, uint
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_attr_done[7][kMaxDevices];
 std::atomic<int> g_attr_done_grouped[2][kMaxDevices];
-std::atomic<int> g_attr_done_pair[2][kMaxDevices];   // CTA-pair instances, by code width
+std::atomic<int> g_attr_done_pair[4][kMaxDevices];   // CTA-pair instances: (8-bit) * 2 + (TM == 256)
 std::atomic<int> g_sms[kMaxDevices];
 // clusters of 2, 4, 8 CTAs that can be resident at once, per code width (0: not yet asked; -1: none)
 std::atomic<int> g_max_clusters[3][3][kMaxDevices];
@@ -1003,7 +1004,8 @@ template <int BITS, bool XPRE, int TM = (BITS == 4 ? 256 : 128), bool PAIR = fal
 cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev, int split, int tn = kTileN) {
     using C = Cfg<BITS, XPRE, TM, PAIR>;
     std::atomic<int> &attr_done =
-        PAIR ? g_attr_done_pair[BITS == 8 ? 1 : 0][dev] : g_attr_done[attr_slot<BITS, XPRE, TM>()][dev];
+        PAIR ? g_attr_done_pair[(BITS == 8 ? 2 : 0) + (TM == 256 ? 1 : 0)][dev]
+             : g_attr_done[attr_slot<BITS, XPRE, TM>()][dev];
     if (!attr_done.load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(qmm_kernel<BITS, false, XPRE, TM, PAIR>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -1096,9 +1098,12 @@ cudaError_t launch_qmm(const MatmulArgs &a) {
     const int sms = g_sms[dev].load(std::memory_order_relaxed);
     const int tn128 = split == 1 ? qmm_tile_n(a.N, (a.M + 127) / 128, sms) : kTileN;
     const bool pair128 = qmm_pair(a.M, 128, split);
-    if (!a.xf16)
+    if (!a.xf16) {
+        if (qmm_pair(a.M, 256, split))
+            return launch_qmm_bits<8, false, 256, true>(a, dev, split, qmm_tile_n(a.N, (a.M + 255) / 256, sms));
         return pair128 ? launch_qmm_bits<8, false, 128, true>(a, dev, split, tn128)
                        : launch_qmm_bits<8, false>(a, dev, split, tn128);
+    }
     // x converted once: 256-row tiles where that needs no split and still fills half the
     // SMs (M = 2048 on 14336 x 4096: 743 -> 1205 TFLOP/s; on 4096 x 14336 one wave of
     // 128 such tiles against 1.7 waves of 128-row tiles)
