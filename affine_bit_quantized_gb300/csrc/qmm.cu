@@ -365,6 +365,7 @@ __device__ __forceinline__ uint4 x_chunk_f16(uint4 v) {
 // otherwise repeat on its raw x tiles.
 template <int BITS>
 __global__ void x_to_f16_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ xf, int64_t vecs) {
+    griddep_launch();   // the tensor-core kernel after it may start its set-up (it waits for xf)
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < vecs; i += (int64_t)gridDim.x * blockDim.x)
         xf[i] = x_chunk_f16<BITS>(__ldg(x + i));
 }
@@ -1046,7 +1047,7 @@ cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev, int split, int tn = kT
     cfg.stream = a.stream;
     cudaLaunchAttribute attr[2];
     int na = 0;
-    if (a.pdl) {
+    if (a.pdl || XPRE) {   // with XPRE the launch before is the conversion of x into the workspace
         attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[na].val.programmaticStreamSerializationAllowed = 1;
         ++na;
@@ -1173,6 +1174,7 @@ gather_plan_kernel(const int *__restrict__ lhs, const int *__restrict__ rhs, int
 template <int BITS>
 __global__ void gather_rows_kernel(const uint4 *__restrict__ x, const int *__restrict__ lhs, uint4 *__restrict__ xg,
                                    int R, int T, int row_vecs) {
+    griddep_launch();   // the expert-indexed matmul after it may start its set-up (it waits for xg)
     const int64_t total = (int64_t)R * row_vecs;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = i / row_vecs, c = i - r * row_vecs;
@@ -1221,6 +1223,13 @@ cudaError_t launch_gather_bits(const GatherArgs &g, int dev, int sms) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = g.stream;
+    // programmatic launch after the row gather: the plan (two launches back) is complete, and
+    // the kernel waits for the gathered rows before it reads them
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS, true, true>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(g.y), R, N,
                               K, (unsigned long long)g.timeout_ns, g.status, (const int *)plan, 0, tn, 0);
 }
