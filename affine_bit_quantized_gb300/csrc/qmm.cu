@@ -442,12 +442,16 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     int m_end = M;                  // rows from m_end on are not this tile's
     const int wrows = PAIR ? tn / 2 : tn;   // rows of W this CTA loads and converts
     int wrow0 = n0 + (int)prank * wrows;    // the first of them (in the stacked experts: expert * N + ...)
+    int halves = C::kHalves;                 // M=128 accumulators in use
     if (GROUPED) {
         if ((int)blockIdx.y >= __ldg(plan)) return;   // no tile: nothing set up yet
         const int4 t = __ldg(reinterpret_cast<const int4 *>(plan + kPlanHeaderInts) + blockIdx.y);
         m0 = t.y;
         m_end = t.y + t.z;
         wrow0 = t.x * N + n0;
+        // an expert's last tile with at most 128 rows (the few rows past a multiple of 256)
+        // runs only the first half's MMAs and epilogue: half the operand reads per step
+        if (t.z <= 128) halves = 1;
     }
     // split K: the gridDim.z CTAs of a cluster each take a contiguous share of
     // the K/512 blocks of 8 groups and add their partial tiles through
@@ -652,6 +656,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                     const uint64_t bd = sw128_desc(b0 + kk * 32);
 #pragma unroll
                     for (int h = 0; h < C::kHalves; ++h) {
+                        if (h >= halves) break;
                         if constexpr (PAIR)
                             umma_f16_pair(tmem + h * kTileN, sw128_desc(a0 + h * (128 * 128) + kk * 32), bd, idesc,
                                           (i > 0 || kk > 0) ? 1u : 0u);
@@ -765,7 +770,8 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         }
         // ------------------------------------------------------------ epilogue
         // warps 2..(1 + 4 x halves) read the accumulators (one per TMEM lane quarter and half)
-        go = warp < kEpiEnd && alive && mbar_wait(acc_done, 0, deadline, abort_flag) && !*abort_flag;
+        const bool epi = warp < kEpiEnd && h < halves;   // this warp's accumulators are in use
+        go = epi && alive && mbar_wait(acc_done, 0, deadline, abort_flag) && !*abort_flag;
         go = __all_sync(0xFFFFFFFFu, go);   // tcgen05.ld below is warp-collective
         if (go) {
             tc_fence_after();
@@ -777,7 +783,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                     store_row32(r, m, n0 + j * 32);
                 }
             }
-        } else if (alive && warp < kEpiEnd) {
+        } else if (alive && epi) {
             fail();
         }
     }
