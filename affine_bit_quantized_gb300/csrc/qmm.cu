@@ -7,9 +7,10 @@
 // the hundreds to thousands the work is a real dense contraction, so here it
 // runs on tcgen05.mma with fp32 accumulators in tensor memory (TMEM):
 //
-//   * CTA tile 256 (rows of x; 128 for 8-bit codes) x 256 (rows of W), K
-//     walked one group of 64 at a time; two 128 x 256 fp32 accumulators fill
-//     the 512 TMEM columns.
+//   * CTA tile 256 (rows of x; 128 for 8-bit codes unless x is converted once
+//     or the CTAs work in pairs) x 256 (rows of W, or 224 where that fills the
+//     last wave), K walked one group of 64 at a time; two 128 x 256 fp32
+//     accumulators fill the 512 TMEM columns.
 //   * warp 0 (one thread) streams raw tiles with TMA: x (bf16, 128-byte
 //     swizzle), the packed codes of the 256 W rows, and every 8 groups the
 //     rows' bf16 scales and biases;
@@ -33,7 +34,9 @@
 //   * after the last group, warps 2..9 read the accumulators with tcgen05.ld,
 //     round to bf16 and store y; with few output tiles, K is split across a
 //     cluster and the partial tiles are added through distributed shared
-//     memory first (see the epilogue).
+//     memory first (see the epilogue);
+//   * where each CTA converts its own x tiles and K is not split, two CTAs of a
+//     cluster share each W tile (tcgen05 cta_group::2, see qmm_kernel).
 //
 // Every mbarrier wait is bounded by a global-timer deadline; on expiry the
 // kernel records a timeout in the device status word, stops issuing work,
