@@ -73,12 +73,17 @@ constexpr int kSBStages = 2;
 // MMA's k order, from a conversion pass into the caller's workspace), copied
 // by TMA straight into the operand tile: no raw x stage, which leaves room
 // for a third converted stage.
-// TM: rows of x per CTA.  8-bit codes without x converted once take 128 (their
-// raw x and code stages would not fit beside 256-row operand stages); with x
-// already fp16 there is no raw x stage and two converted stages of 256 rows
-// fit, which doubles the MMA work per converted W tile.
-// PAIR (without XPRE): the CTA holds half of the W tile (see qmm_kernel), which
-// leaves room for a third converted stage.
+// TM: rows of x per CTA.  kXInConv: x (fp16 with XPRE; bf16 with 8-bit codes on
+// 256-row tiles, which the converters turn into fp16 in place) is copied by TMA
+// straight into the x tile of a converted stage, so there is no raw x stage: the
+// 8-bit 256-row tiles get four converted stages instead of two (M = 2048 without
+// the workspace: 255 -> 202 us).  Otherwise bf16 x comes with the codes in the raw
+// stage, two stages ahead of the converters, and is converted into the converted
+// stage: in the converted stage the copy's latency would sit on the loop from the
+// MMAs back to the converters (4-bit M = 2048 on 14336 x 4096: 186 -> 196 us; 8-bit
+// 128-row pairs at M = 256: 58 -> 65 us).  As many converted stages as fit (at
+// most 4) follow the raw and scale/bias stages.
+// PAIR (without XPRE): the CTA holds half of the W tile (see qmm_kernel).
 template <int BITS, bool XPRE = false, int TM = (BITS == 4 ? 256 : 128), bool PAIR = false>
 struct Cfg {
     static constexpr int kTileM = TM;
@@ -86,17 +91,20 @@ struct Cfg {
     static constexpr int kWRows = PAIR ? kTileN / 2 : kTileN;   // rows of W in this CTA's stages
     static constexpr int kBTileBytes = kWRows * 128;             // fp16 W, kWRows rows x 64 k
     static constexpr int kSBBytes = kWRows * kSBGroups * 2;      // scales (and again biases) per stage
+    static constexpr bool kXInConv = XPRE || (BITS == 8 && TM == 256);
     static constexpr int kRawStages = 2;                          // raw code (and bf16 x) stages
-    static constexpr int kConvStages = PAIR ? (TM == 128 ? 4 : BITS == 8 ? 2 : 3) : XPRE ? ((BITS == 8 && TM == 256) ? 2 : 3) : 2;
-    static constexpr int kATileBytes = kTileM * 128;             // fp16 x, kTileM rows x 64 k
+    static constexpr int kATileBytes = kTileM * 128;             // x, kTileM rows x 64 k (fp16 once converted)
     static constexpr int kConvStageBytes = kATileBytes + kBTileBytes;
-    static constexpr int kRawXBytes = XPRE ? 0 : kTileM * 128;   // bf16 x, same swizzled geometry
+    static constexpr int kRawXBytes = kXInConv ? 0 : kTileM * 128;   // bf16 x, same swizzled geometry
     static constexpr int kRowWords = kGroup * BITS / 32;         // code words per W row and group
     static constexpr int kRawCodeBytes = kWRows * kRowWords * 4; // 8192 or 16384 (half in a pair)
     static constexpr int kRawStageBytes = kRawXBytes + kRawCodeBytes;
+    // the raw, scale/bias stages, room for the barriers and the alignment slack; then the converted stages
+    static constexpr int kFixedBytes = kRawStages * kRawStageBytes + kSBStages * 2 * kSBBytes + 512 + 16 + 1024;
+    static constexpr int kConvStages = (232448 - kFixedBytes) / kConvStageBytes < 4 ? (232448 - kFixedBytes) / kConvStageBytes : 4;
     // barriers: raw_full[2], raw_empty[2], sb_full[2], sb_empty[2], conv_full[S], conv_empty[S], acc_done,
-    // x_full[S] (with XPRE: the x copy of a converted stage has landed) and peer_full[S] (in a CTA
-    // pair: the other CTA's half of a converted stage is ready)
+    // x_full[S] (the x copy of a converted stage has landed) and peer_full[S] (in a CTA pair: the
+    // other CTA's half of a converted stage is ready)
     static constexpr int kNumBars = 2 * kRawStages + 2 * kSBStages + 4 * kConvStages + 1;
     static constexpr int kOffConv = 0;
     static constexpr int kOffRaw = kOffConv + kConvStages * kConvStageBytes;
@@ -108,7 +116,9 @@ struct Cfg {
 static_assert(Cfg<4>::kSmemBytes <= 232448 && Cfg<8>::kSmemBytes <= 232448 && Cfg<4, true>::kSmemBytes <= 232448 &&
                   Cfg<8, true>::kSmemBytes <= 232448 && Cfg<8, true, 256>::kSmemBytes <= 232448 &&
                   Cfg<4, false, 256, true>::kSmemBytes <= 232448 && Cfg<8, false, 128, true>::kSmemBytes <= 232448 &&
-                  Cfg<8, false, 256, true>::kSmemBytes <= 232448,
+                  Cfg<8, false, 256, true>::kSmemBytes <= 232448 && Cfg<4, false, 128>::kSmemBytes <= 232448 &&
+                  Cfg<4, true, 128>::kSmemBytes <= 232448 && Cfg<4>::kConvStages >= 2 && Cfg<8>::kConvStages >= 2 &&
+                  Cfg<8, true, 256>::kConvStages >= 2,
               "shared memory per CTA");
 // split-K partials received by a CTA (at most 7 sources x its 32 columns x the tile's rows) fit in
 // the stage memory in front of the barriers
@@ -414,6 +424,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     constexpr int kConvStages = C::kConvStages, kRawStages = C::kRawStages;
     constexpr int kTileM = C::kTileM, kATileBytes = C::kATileBytes, kConvStageBytes = C::kConvStageBytes;
     constexpr int kRawXBytes = C::kRawXBytes, kRawStageBytes = C::kRawStageBytes;
+    constexpr bool kXInConv = C::kXInConv;
     constexpr int kOffConv = C::kOffConv, kOffRaw = C::kOffRaw, kOffSB = C::kOffSB, kOffMisc = C::kOffMisc;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_addr(smem_raw);
@@ -475,7 +486,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             mbar_init(sb_empty(s), kConvWarps);
         }
         for (int s = 0; s < kConvStages; ++s) {
-            if (XPRE) mbar_init(x_full(s), 1);
+            mbar_init(x_full(s), 1);
             if (PAIR) mbar_init(peer_full(s), 1);
             mbar_init(conv_full(s), kConvWarps);
             mbar_init(conv_empty(s), 1);
@@ -576,7 +587,7 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         for (int j = (issued_sb > kSBStages ? issued_sb - kSBStages : 0); j < issued_sb; ++j)
             while (!mbar_try_wait(sb_full(j % kSBStages), (j / kSBStages) & 1) && global_timer() < drain) {
             }
-        if (XPRE)
+        if (kXInConv)
             for (int i = (issued_conv > kConvStages ? issued_conv - kConvStages : 0); i < issued_conv; ++i)
                 while (!mbar_try_wait(x_full(i % kConvStages), (i / kConvStages) & 1) && global_timer() < drain) {
                 }
@@ -608,12 +619,12 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 const uint32_t dst = base + kOffRaw + rs * kRawStageBytes;
                 if (!(skip_first && i == 0)) {
                     mbar_expect_tx(raw_full(rs), (uint32_t)(kRawXBytes + wrows * C::kRowWords * 4));
-                    if (!XPRE) tma_load_2d(dst, &tm_x, (g0 + i) * kGroup, m0, raw_full(rs));
+                    if (!kXInConv) tma_load_2d(dst, &tm_x, (g0 + i) * kGroup, m0, raw_full(rs));
                     tma_load_2d(dst + kRawXBytes, &tm_w, (g0 + i) * C::kRowWords, wrow0, raw_full(rs));
                 }
                 issued_raw = i + 1;
-                if (XPRE) {
-                    // fp16 x straight into the converted stage, once the MMAs have released it
+                if (kXInConv) {
+                    // x straight into the converted stage, once the MMAs have released it
                     const int cs = i % kConvStages;
                     if (i >= kConvStages &&
                         !mbar_wait(conv_empty(cs), ((i / kConvStages) - 1) & 1, deadline, abort_flag)) {
@@ -700,13 +711,14 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             }
             const uint32_t raw = base + kOffRaw + rs * kRawStageBytes;
             const uint32_t conv = base + kOffConv + cs * kConvStageBytes;
-            // x: bf16 -> fp16, chunk by chunk at the same (swizzled) offsets,
-            // each chunk's k order becoming (0,4,1,5,2,6,3,7) for 4-bit codes
-            // and (0,2,1,3,4,6,5,7) for 8-bit codes (the order the W pairs come in)
+            if (!kXInConv) {
+                // x: bf16 -> fp16 from the raw stage, chunk by chunk at the same (swizzled) offsets,
+                // each chunk's k order becoming (0,4,1,5,2,6,3,7) (the order the W pairs come in)
 #pragma unroll 4
-            for (int c = 0; c < (XPRE ? 0 : C::kRawXBytes / 16 / kConvThreads); ++c) {
-                const uint32_t off = (uint32_t)((c * kConvThreads + t) * 16);
-                sts128(conv + off, x_chunk_f16<BITS>(lds128(raw + off)));
+                for (int c = 0; c < kRawXBytes / 16 / kConvThreads; ++c) {
+                    const uint32_t off = (uint32_t)((c * kConvThreads + t) * 16);
+                    sts128(conv + off, x_chunk_f16<BITS>(lds128(raw + off)));
+                }
             }
             // W: thread t takes chunks kCpt*p .. kCpt*p + kCpt-1 of row r = t / kTpr
             // (p = t % kTpr) and converts the row's scale and bias once; each chunk of
@@ -761,6 +773,25 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                             sts128(conv + kATileBytes + r * 128 + ((c ^ (r & 7)) << 4), o);
                         }
                     }
+                }
+            }
+            if (kXInConv && !XPRE) {
+                // x: the bf16 copy in the stage's x tile becomes fp16 in place, chunk by chunk
+                // at the same (swizzled) offsets, each chunk's k order becoming (0,2,1,3,4,6,5,7)
+                // (the order the 8-bit W pairs come in; only 8-bit codes take this way); W above
+                // did not need it, so its conversion overlapped the copy
+                bool xok = mbar_wait(x_full(cs), (i / kConvStages) & 1, deadline, abort_flag);
+                xok = __all_sync(0xFFFFFFFFu, xok);
+                if (!xok) {
+                    alive = false;
+                    fail();
+                    break;
+                }
+                // the TMA wrote the tile (async proxy); these generic loads follow its completion
+#pragma unroll 4
+                for (int c = 0; c < kATileBytes / 16 / kConvThreads; ++c) {
+                    const uint32_t off = (uint32_t)((c * kConvThreads + t) * 16);
+                    sts128(conv + off, x_chunk_f16<BITS>(lds128(conv + off)));
                 }
             }
             fence_proxy_async();  // make the generic-proxy stores visible to the MMA (async proxy)
