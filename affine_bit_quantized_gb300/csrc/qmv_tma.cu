@@ -397,8 +397,9 @@ cudaError_t device_sms(int *dev, int *sms) {
 // Measured on GB300 against the general kernel (graph-replayed calls, weights
 // not in L2): the TMA kernel wins wherever every SM gets a tile (14336 x 4096:
 // 12.7-20 us against 24-25 us at M = 2..8; the 128256-row matrix: 58-91 us
-// against 179-185 us) and, for M <= 3, down to 64 tiles (4096 x 14336 at M = 2:
-// 17 us against 23 us); with fewer tiles or more rows the general kernel's
+// against 179-185 us) and, for M <= 4, down to 64 tiles (4096 x 14336 at M = 2:
+// 17 us against 23 us; at M = 4: 22.6 us against 27.4 us, while at M = 6 and 8 the
+// general kernel leads, 28 against 33-35 us); with fewer tiles or more rows the general kernel's
 // shorter start wins (4096 x 4096 at M = 8: 8.0 us against 12.8 us; 1024 x
 // 4096 at M = 2: 5.7 us against 6.2 us).  One row always takes the TMA kernel.
 bool qmv_tma_preferred(const MatmulArgs &a) {
@@ -411,7 +412,7 @@ bool qmv_tma_preferred(const MatmulArgs &a) {
     int dev = 0, sms = 0;
     if (device_sms(&dev, &sms) != cudaSuccess) return true;
     const int T = (int)((a.N + kRows - 1) / kRows);
-    return T >= sms || (a.M <= 3 && T >= 64);
+    return T >= sms || (a.M <= 4 && T >= 64);
 }
 
 cudaError_t launch_qmv_tma(const MatmulArgs &a) {
