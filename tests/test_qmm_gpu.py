@@ -222,9 +222,10 @@ def test_output_beyond_2_31_elements(dev):
     assert_parity(got, yb, rms=rms, what=f"qmm sampled M={M} N={N} K={K} (y beyond 2^31 elements)")
 
 
-@pytest.mark.parametrize("M,N,K", [(64, 512, 1024), (256, 512, 4096),   # one tile; split K over a cluster
-                                   (512, 256, 512)])                     # a CTA pair
-def test_qmm_bounded_wait_timeout_reports_status(dev, M, N, K):
+@pytest.mark.parametrize("M,N,K,bits", [(64, 512, 1024, 4), (256, 512, 4096, 4),   # one tile; split K over a cluster
+                                        (512, 256, 512, 4),                        # a CTA pair
+                                        (512, 256, 512, 8)])                       # a pair converting x in its stages
+def test_qmm_bounded_wait_timeout_reports_status(dev, M, N, K, bits):
     """The test hook makes the first CTA's producer leave out its first copy:
     the converters' bounded wait expires, the kernel records a timeout (the
     other CTAs of a split-K cluster still meet it at the cluster barriers; the
@@ -232,12 +233,12 @@ def test_qmm_bounded_wait_timeout_reports_status(dev, M, N, K):
     never get consumed), the host reads AQ_ERR_TIMEOUT, and a normal call
     right after is correct."""
     import torch
-    w = synth.make_weights(N, K, 12)
+    w = synth.make_weights(N, K, 12, bits=bits)
     x = synth.make_x(M, K, 12)
     xt, wt, st, bt = upload(x, w, dev)
     stream = torch.cuda.current_stream().cuda_stream
     assert aq.aq_read_device_status(stream) == aq.AQ_OK
-    aq.matmul(xt, wt, st, bt, kernel="qmm", flags=aq.AQ_FLAG_DEBUG_SKIP_COPY)
+    aq.matmul(xt, wt, st, bt, kernel="qmm", bits=bits, flags=aq.AQ_FLAG_DEBUG_SKIP_COPY)
     assert aq.aq_read_device_status(stream) == aq.AQ_ERR_TIMEOUT
     assert aq.aq_read_device_status(stream) == aq.AQ_OK          # cleared by the read
-    check_full(dev, M, N, K, 12)
+    check_full(dev, M, N, K, 12, bits=bits)
