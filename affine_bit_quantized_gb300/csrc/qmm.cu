@@ -78,7 +78,7 @@ constexpr int kSBStages = 2;
 // straight into the x tile of a converted stage, so there is no raw x stage: the
 // 8-bit 256-row tiles get four converted stages instead of two (M = 2048 without
 // the workspace: 255 -> 202 us).  Otherwise bf16 x comes with the codes in the raw
-// stage, two stages ahead of the converters, and is converted into the converted
+// stage, two to four stages ahead of the converters, and is converted into the converted
 // stage: in the converted stage the copy's latency would sit on the loop from the
 // MMAs back to the converters (4-bit M = 2048 on 14336 x 4096: 186 -> 196 us; 8-bit
 // 128-row pairs at M = 256: 58 -> 65 us).  As many converted stages as fit (at
@@ -92,17 +92,34 @@ struct Cfg {
     static constexpr int kBTileBytes = kWRows * 128;             // fp16 W, kWRows rows x 64 k
     static constexpr int kSBBytes = kWRows * kSBGroups * 2;      // scales (and again biases) per stage
     static constexpr bool kXInConv = XPRE || (BITS == 8 && TM == 256);
-    static constexpr int kRawStages = 2;                          // raw code (and bf16 x) stages
     static constexpr int kATileBytes = kTileM * 128;             // x, kTileM rows x 64 k (fp16 once converted)
     static constexpr int kConvStageBytes = kATileBytes + kBTileBytes;
     static constexpr int kRawXBytes = kXInConv ? 0 : kTileM * 128;   // bf16 x, same swizzled geometry
     static constexpr int kRowWords = kGroup * BITS / 32;         // code words per W row and group
     static constexpr int kRawCodeBytes = kWRows * kRowWords * 4; // 8192 or 16384 (half in a pair)
     static constexpr int kRawStageBytes = kRawXBytes + kRawCodeBytes;
-    // the raw, scale/bias stages, room for the barriers and the alignment slack; then the converted stages
+    // converted stages (at most 4) that fit beside R raw stages, the scale/bias stages, room for
+    // the barriers and the alignment slack
+    static constexpr int conv_fit(int R) {
+        return (232448 - (R * kRawStageBytes + kSBStages * 2 * kSBBytes + 512 + 16 + 1024)) / kConvStageBytes < 4
+                   ? (232448 - (R * kRawStageBytes + kSBStages * 2 * kSBBytes + 512 + 16 + 1024)) / kConvStageBytes
+                   : 4;
+    }
+    // Raw stages: each raw stage's loop is the copy's latency plus its conversion, so the ring's
+    // depth bounds the step rate wherever a step carries little work.  128-row tiles of one CTA
+    // (prefill at M = 256, where the K split leaves each CTA few steps) take 4 raw stages (3 for
+    // 8-bit codes with bf16 x) even where that leaves two converted stages; CTA pairs deepen the
+    // ring (up to 4) only where the converted stages keep their number.  Measured at M = 256:
+    // 4-bit 60.0 -> 58.6 us (59.3 -> 55.6 with x converted once), 8-bit 64.4 -> 59.9 us and
+    // 55.6 -> 48.3 us; 8-bit 256-row pairs at M = 2048: 204.6 -> 194.8 us.  256-row tiles of
+    // one CTA keep two (8-bit with x converted once measured 0.6 % slower with four).
+    static constexpr int kRawStages =
+        (TM == 128 && !PAIR) ? (conv_fit(4) >= 2 ? 4 : 3)
+        : PAIR ? (conv_fit(4) == conv_fit(2) ? 4 : conv_fit(3) == conv_fit(2) ? 3 : 2)
+               : 2;
     static constexpr int kFixedBytes = kRawStages * kRawStageBytes + kSBStages * 2 * kSBBytes + 512 + 16 + 1024;
-    static constexpr int kConvStages = (232448 - kFixedBytes) / kConvStageBytes < 4 ? (232448 - kFixedBytes) / kConvStageBytes : 4;
-    // barriers: raw_full[2], raw_empty[2], sb_full[2], sb_empty[2], conv_full[S], conv_empty[S], acc_done,
+    static constexpr int kConvStages = conv_fit(kRawStages);
+    // barriers: raw_full[R], raw_empty[R], sb_full[2], sb_empty[2], conv_full[S], conv_empty[S], acc_done,
     // x_full[S] (the x copy of a converted stage has landed) and peer_full[S] (in a CTA pair: the
     // other CTA's half of a converted stage is ready)
     static constexpr int kNumBars = 2 * kRawStages + 2 * kSBStages + 4 * kConvStages + 1;
