@@ -224,7 +224,8 @@ def test_output_beyond_2_31_elements(dev):
 
 @pytest.mark.parametrize("M,N,K,bits", [(64, 512, 1024, 4), (256, 512, 4096, 4),   # one tile; split K over a cluster
                                         (512, 256, 512, 4),                        # a CTA pair
-                                        (512, 256, 512, 8)])                       # a pair converting x in its stages
+                                        (512, 256, 512, 8),                        # a pair converting x in its stages
+                                        (256, 512, 4096, 8)])                      # 8-bit, split K, three raw stages
 def test_qmm_bounded_wait_timeout_reports_status(dev, M, N, K, bits):
     """The test hook makes the first CTA's producer leave out its first copy:
     the converters' bounded wait expires, the kernel records a timeout (the
