@@ -140,13 +140,33 @@ aq_status matmul_impl(const void *x, const uint32_t *w_packed, const void *scale
         if (aq::qmm_supported(a)) return record_cuda(aq::launch_qmm(a));
         if (kernel == AQ_KERNEL_QMM || a.debug_skip_copy) return AQ_ERR_UNSUPPORTED;
     }
+    // 9..16 rows of x over a matrix with at least two tiles per SM, where x of all the
+    // rows would need K passes (16 rows of K = 4096: 128 KB): one launch of the TMA-fed
+    // kernel whose CTA pairs take the two halves of the rows (each half's x in one
+    // pass) and walk the same tiles together, so W comes from DRAM about once
+    auto split_launch = [&](aq_status *out) -> bool {
+        if (!(M > 8 && M <= kQmvMaxRows && kernel == AQ_KERNEL_AUTO && many_tiles(N))) return false;
+        a.x = x;
+        a.y = y;
+        a.M = M;
+        if (!aq::qmv_tma_supported(a) || aq::qmv_tma_passes(a) == 1) return false;
+        a.split_rows = true;
+        *out = record_cuda(aq::launch_qmv_tma(a));
+        a.split_rows = false;
+        return true;
+    };
     if (bits == 8) {
         // 8-bit codes: the TMA-fed decode kernel in launches of up to 16 rows of x
         // wherever it applies (K a multiple of 512); else the general kernel below
         st = AQ_OK;
+        if (split_launch(&st)) return st;
         if (tma_rows(kQmvMaxRows, &st)) return st;
     }
     if (M <= kQmvMaxRows && kernel != AQ_KERNEL_QMM) {
+        st = AQ_OK;
+        if (split_launch(&st)) return st;
+        a.x = x;
+        a.y = y;
         a.M = M;
         // an explicit AQ_KERNEL_QMV takes the TMA-fed kernel wherever it applies; up
         // to 16 rows of x stream W once
@@ -155,16 +175,6 @@ aq_status matmul_impl(const void *x, const uint32_t *w_packed, const void *scale
             st = AQ_OK;
             if (tma_rows(M, &st)) return st;
         }
-    }
-    if (M > 8 && M <= kQmvMaxRows && kernel == AQ_KERNEL_AUTO && many_tiles(N)) {
-        // 9..16 rows whose x needs K passes (16 rows of K = 4096: 128 KB), over a matrix
-        // with at least two tiles per SM: two launches of at most 8 rows, each x in one
-        // pass, beat one launch whose every pass deposits partial sums (128256 x 4096 at
-        // M = 16: 2 x 60 us against 204 us) and the general kernel (14336 x 4096 at
-        // M = 9 / 16: 25.4 / 27.9 us against 27.3 / 29.7 us)
-        const int64_t rows = (M + 1) / 2;
-        st = AQ_OK;
-        if (tma_rows(rows, &st)) return st;
     }
     if (a.debug_skip_copy) return AQ_ERR_UNSUPPORTED;  // the general kernel has no copy producer
     // Weight-streaming passes over at most 16 rows of x each.

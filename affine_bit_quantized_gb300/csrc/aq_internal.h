@@ -26,6 +26,7 @@ struct MatmulArgs {
     bool debug_skip_copy;    // test hook: the kernel's producer leaves out one copy
     int bits = 4;            // code width: 4 or 8
     void *xf16 = nullptr;    // tensor-core path: M*K*2 bytes of caller workspace for x converted once
+    bool split_rows = false; // TMA-fed decode kernel: CTA pairs take the two halves of x's rows
 };
 
 // Values of the device status word.

@@ -97,13 +97,27 @@ constexpr int kMaxSmem = kSmemLimit;
 // consumers' bounded wait on it expires.
 // NS: ring depth; 3 leaves room for x of up to 64 KB (one pass for, e.g., 8 rows of K = 4096).
 // NB: blocks of 8 MMA columns, 2 for 9..16 rows of x (every code pair feeds both).
+// split_rows: CTAs 2p and 2p + 1 take rows [0, ceil(M/2)) and [ceil(M/2), M) of x
+// and y and walk the same tiles at the same pace, so that the second copy of a
+// tile mostly finds it in L2 (9..16 rows as two halves of at most 8 in one launch).
 template <int BITS, bool ONE_ROW, bool MULTI, int NS = kMaxStages, int NB = 1>
 __global__ void __launch_bounds__(kThreads, 1)
 qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
                const __grid_constant__ CUtensorMap tm_b, const __nv_bfloat16 *__restrict__ x,
                __nv_bfloat16 *__restrict__ y, int M, int N, int K, int kbp, int cap, unsigned long long timeout_ns,
-               int *status, int skip_copy) {
+               int *status, int skip_copy, int split_rows) {
     using Gm = Geo<BITS>;
+    // the CTA's place among those walking the tiles (a pair counts once with split_rows;
+    // the two-block instances never split, and keep x, y and M as launched)
+    const bool split = NB == 1 && split_rows;
+    const int cta = split ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int ncta = split ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    if (split) {
+        const int half = (int)(blockIdx.x & 1u), m0 = half ? (M + 1) / 2 : 0;
+        x += (size_t)m0 * K;
+        y += (size_t)m0 * N;
+        M = half ? M / 2 : (M + 1) / 2;
+    }
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int KB = (K + Gm::kStageCodes - 1) / Gm::kStageCodes;    // stages per tile
@@ -128,7 +142,7 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int T = (N + kRows - 1) / kRows;
-    const int my_tiles = (int)blockIdx.x < T ? (T - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int my_tiles = cta < T ? (T - 1 - cta) / ncta + 1 : 0;
     const int L_items = my_tiles * KB;
     if (!MULTI) cap = my_tiles > 0 ? my_tiles : 1;   // one batch
 
@@ -171,7 +185,7 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
             };
             auto issue = [&](int it) {
                 const int slot = it % NS;
-                const int tile = (int)blockIdx.x + t * (int)gridDim.x;
+                const int tile = cta + t * ncta;
                 const uint32_t dst = s_base + slot * kStageBytes;
                 const uint32_t fb = bar_full + 8 * slot;
                 if (skip_copy && it == 0) {   // test hook: this stage never arrives
@@ -224,14 +238,14 @@ qmv_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
         bool ok = true;
         if (!MULTI) {
             for (int t = 0; ok && t < my_tiles; ++t, ++tcount)
-                ok = reduce_tile<ONE_ROW, NB>(tc, tcount, (int)blockIdx.x + t * (int)gridDim.x, M, N, y, lane,
+                ok = reduce_tile<ONE_ROW, NB>(tc, tcount, cta + t * ncta, M, N, y, lane,
                                               timeout_ns, abort_flag, nullptr, 0, 1, 1.f, r, kReducers);
         } else {
             for (int tb = 0; ok && tb < my_tiles; tb += cap) {
                 const int tb_end = tb + cap < my_tiles ? tb + cap : my_tiles;
                 for (int p = 0; ok && p < P; ++p)
                     for (int t = tb; ok && t < tb_end; ++t, ++tcount)
-                        ok = reduce_tile<ONE_ROW, NB>(tc, tcount, (int)blockIdx.x + t * (int)gridDim.x, M, N, y,
+                        ok = reduce_tile<ONE_ROW, NB>(tc, tcount, cta + t * ncta, M, N, y,
                                                       lane, timeout_ns, abort_flag, yacc + (t - tb) * kRows * M, p, P,
                                                       1.f, r, kReducers);
             }
@@ -407,7 +421,8 @@ bool qmv_tma_preferred(const MatmulArgs &a) {
     // 9..16 rows: where x fits one pass.  In K passes every pass of every tile
     // deposits the partial sums of 16 rows through one buffer (x of 16 rows at
     // K = 4096 is 128 KB): 128256 x 4096 took 204 us, 4096 x 14336 82 us, against
-    // 2 x 60 us as two launches of 8 rows and 28 us on the general kernel.
+    // 110 us as one launch whose CTA pairs split the rows (taken over at least
+    // two tiles per SM) and 28 us on the general kernel.
     if (a.M > kMaxM) return qmv_tma_passes(a) == 1;
     int dev = 0, sms = 0;
     if (device_sms(&dev, &sms) != cudaSuccess) return true;
@@ -419,14 +434,18 @@ cudaError_t launch_qmv_tma(const MatmulArgs &a) {
     int dev = 0, sms = 0;
     cudaError_t e = device_sms(&dev, &sms);
     if (e != cudaSuccess) return e;
-    const int M = (int)a.M, N = (int)a.N, K = (int)a.K;
+    // M: rows of x per CTA (half of them, rounded up, when CTA pairs split the rows)
+    const int M = a.split_rows ? (int)((a.M + 1) / 2) : (int)a.M, N = (int)a.N, K = (int)a.K;
     const int SC = stage_codes(a.bits);
     const int kbp = stages_per_pass(M, K, a.bits);
-    const int P = qmv_tma_passes(a);
+    const int P = ((K + SC - 1) / SC + kbp - 1) / kbp;
     const bool ns3 = ring_stages(M, K, a.bits) == 3;
     const int T = (N + kRows - 1) / kRows;
-    const int grid = std::min(T, sms);   // persistent, one CTA per SM
-    const int tpc = (T + grid - 1) / grid;
+    // persistent, one CTA per SM (CTA pairs with split rows: as many pairs as fit)
+    const int walkers = a.split_rows ? std::min(T, sms / 2) : std::min(T, sms);
+    if (walkers < 1) return cudaErrorInvalidConfiguration;
+    const int grid = a.split_rows ? 2 * walkers : walkers;
+    const int tpc = (T + walkers - 1) / walkers;
     int cap = 0;   // tiles per batch whose sums stay in shared memory across the passes
     if (P > 1) {
         const int free_bytes = kSmemLimit - 1024 - make_layout(M, kbp * SC, 0, a.bits, ns3 ? 3 : kMaxStages).total;
@@ -485,9 +504,9 @@ cudaError_t launch_qmv_tma(const MatmulArgs &a) {
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, tw, ts, tb, static_cast<const __nv_bfloat16 *>(a.x),
-                              static_cast<__nv_bfloat16 *>(a.y), M, N, K, kbp, std::max(cap, 1),
+                              static_cast<__nv_bfloat16 *>(a.y), (int)a.M, N, K, kbp, std::max(cap, 1),
                               (unsigned long long)a.timeout_ns,
-                              a.status, a.debug_skip_copy ? 1 : 0);
+                              a.status, a.debug_skip_copy ? 1 : 0, a.split_rows ? 1 : 0);
 }
 
 }  // namespace aq

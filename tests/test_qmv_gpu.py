@@ -57,7 +57,8 @@ def test_small_batch_sweep(dev, M, name, N, K):
 def test_small_batch_lm_head_sampled(dev, M, kernel):
     """The lm_head shape at small batch.  With "qmv", 9..16 rows run in one
     launch on the two blocks of MMA columns (in K passes: x of 16 rows of
-    K = 4096 is 128 KB); with "auto", as two launches of at most 8 rows."""
+    K = 4096 is 128 KB); with "auto", in one launch whose CTA pairs take the
+    two halves of the rows."""
     import torch
     _, N, K = synth.LLAMA8B_LM_HEAD
     w = synth.make_weights(N, K, synth.seed_for(3, M, 7))
@@ -80,6 +81,39 @@ def test_nine_to_sixteen_rows_one_pass(dev, M, N, K):
     the default choice and on the explicit one."""
     check(dev, M, N, K, 900 + M + K, kernel="auto")
     check(dev, M, N, K, 950 + M + K, kernel="qmv")
+
+
+@pytest.mark.parametrize("M,N,K,bits", [
+    (9, 9729, 4096, 4),     # halves of 5 and 4 rows; a ragged last tile
+    (13, 10000, 4096, 4),
+    (16, 9760, 4096, 4),    # 305 tiles over 76 pairs
+    (16, 10016, 8192, 4),   # each half's x in two K passes
+    (11, 9728, 4096, 8),
+    (16, 9760, 2048, 8),
+])
+def test_nine_to_sixteen_rows_split_pairs(dev, M, N, K, bits):
+    """9..16 rows over at least two tiles per SM, where x of all the rows
+    would need K passes: the default choice is one launch whose CTA pairs take
+    the two halves of x's rows and walk the same tiles; every output against
+    the oracle."""
+    check(dev, M, N, K, 990 + M + N + bits, kernel="auto", bits=bits)
+
+
+def test_split_pairs_bounded_wait_timeout(dev):
+    """The test hook on the split-rows launch: every CTA of both halves runs its
+    bounded wait out, the host reads AQ_ERR_TIMEOUT, and a normal call right
+    after is correct."""
+    import torch
+    M, N, K = 12, 9728, 4096
+    w = synth.make_weights(N, K, 14)
+    x = synth.make_x(M, K, 14)
+    xt, wt, st, bt = upload(x, w, dev)
+    stream = torch.cuda.current_stream().cuda_stream
+    assert aq.aq_read_device_status(stream) == aq.AQ_OK
+    aq.matmul(xt, wt, st, bt, flags=aq.AQ_FLAG_DEBUG_SKIP_COPY)
+    assert aq.aq_read_device_status(stream) == aq.AQ_ERR_TIMEOUT
+    assert aq.aq_read_device_status(stream) == aq.AQ_OK
+    check(dev, M, N, K, 14, kernel="auto")
 
 
 @pytest.mark.parametrize("M,N,K", [(9, 70, 1024), (16, 300, 4096), (12, 33, 5120)])
