@@ -55,8 +55,9 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 constexpr int64_t kMaxDim = (int64_t)1 << 30;  // keeps every per-row index inside 32 bits
 constexpr int kQmvMaxRows = 16;                // rows of x per weight-streaming pass
 
-// At least two 32-row tiles per SM of the current device.
-bool many_tiles(int64_t N) {
+// At least `per_sm` 32-row tiles per SM of the current device (per_sm = 0: at
+// least 64 tiles).
+bool many_tiles(int64_t N, int per_sm = 2) {
     constexpr int kDevices = 64;
     static std::atomic<int> sms[kDevices];
     int dev = 0;
@@ -72,7 +73,7 @@ bool many_tiles(int64_t N) {
         }
         sms[dev].store(n, std::memory_order_relaxed);
     }
-    return (N + 31) / 32 >= 2 * (int64_t)n;
+    return (N + 31) / 32 >= (per_sm > 0 ? per_sm * (int64_t)n : 64);
 }
 
 aq_status validate(const void *x, const uint32_t *w, const void *s, const void *b, void *y,
@@ -140,16 +141,26 @@ aq_status matmul_impl(const void *x, const uint32_t *w_packed, const void *scale
         if (aq::qmm_supported(a)) return record_cuda(aq::launch_qmm(a));
         if (kernel == AQ_KERNEL_QMM || a.debug_skip_copy) return AQ_ERR_UNSUPPORTED;
     }
-    // 9..16 rows of x over a matrix with at least two tiles per SM, where x of all the
-    // rows would need K passes (16 rows of K = 4096: 128 KB): one launch of the TMA-fed
-    // kernel whose CTA pairs take the two halves of the rows (each half's x in one
-    // pass) and walk the same tiles together, so W comes from DRAM about once
+    // 9..16 rows of x where x of all the rows would need K passes (16 rows of
+    // K = 4096: 128 KB): one launch of the TMA-fed kernel whose CTA pairs take the
+    // two halves of the rows and walk the same tiles together, so W comes from DRAM
+    // about once.  4-bit codes: where each half's x fits one pass, over at least one
+    // tile per SM (14336 x 4096 at M = 16: 33.1 -> 21.7 us against two launches of 8
+    // rows; 4864 x 4096: 18.1 -> 14.6 us against the general kernel, while at 4096 x
+    // 4096 the general kernel leads, 12.5 against 14.6 us); where a half needs passes
+    // too, over at least two tiles per SM.  8-bit codes: always (against the two
+    // column blocks in K passes, 4096 x 4096 at M = 16: 28.6 -> 16.6 us; 1024 x 4096:
+    // 26.9 -> 12.7 us; 4096 x 14336, halves in passes: 87.1 -> 47.3 us).
     auto split_launch = [&](aq_status *out) -> bool {
-        if (!(M > 8 && M <= kQmvMaxRows && kernel == AQ_KERNEL_AUTO && many_tiles(N))) return false;
+        if (!(M > 8 && M <= kQmvMaxRows && kernel == AQ_KERNEL_AUTO)) return false;
         a.x = x;
         a.y = y;
         a.M = M;
         if (!aq::qmv_tma_supported(a) || aq::qmv_tma_passes(a) == 1) return false;
+        a.M = (M + 1) / 2;
+        const bool half_one_pass = aq::qmv_tma_passes(a) == 1;
+        a.M = M;
+        if (!(bits == 8 || (half_one_pass ? many_tiles(N, 1) : many_tiles(N, 2)))) return false;
         a.split_rows = true;
         *out = record_cuda(aq::launch_qmv_tma(a));
         a.split_rows = false;

@@ -90,12 +90,17 @@ def test_nine_to_sixteen_rows_one_pass(dev, M, N, K):
     (16, 10016, 8192, 4),   # each half's x in two K passes
     (11, 9728, 4096, 8),
     (16, 9760, 2048, 8),
+    (16, 4900, 4096, 4),    # 154 tiles: one per SM is enough where each half fits one pass
+    (12, 2048, 4096, 8),    # 8-bit codes: over any number of tiles
+    (16, 4096, 14336, 8),   # each half's x in K passes
+    (12, 1024, 8192, 8),
+    (9, 100, 4096, 8),      # 4 tiles: 4 CTA pairs
 ])
 def test_nine_to_sixteen_rows_split_pairs(dev, M, N, K, bits):
-    """9..16 rows over at least two tiles per SM, where x of all the rows
-    would need K passes: the default choice is one launch whose CTA pairs take
-    the two halves of x's rows and walk the same tiles; every output against
-    the oracle."""
+    """9..16 rows over enough tiles, where x of all the rows would need K
+    passes: the default choice is one launch whose CTA pairs take the two
+    halves of x's rows and walk the same tiles; every output against the
+    oracle."""
     check(dev, M, N, K, 990 + M + N + bits, kernel="auto", bits=bits)
 
 
