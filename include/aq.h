@@ -72,9 +72,10 @@ typedef enum aq_kernel {
                           launch), else the general one in launches of 16 rows of x (both
                           code widths).  AQ_KERNEL_AUTO chooses among these (and the GEMM
                           kernel above 16 rows) by measured speed; for 9..16 rows whose x
-                          needs several K passes, over a matrix of at least two 32-row
-                          tiles per SM, it runs the TMA-fed kernel twice, on half the rows
-                          each. */
+                          needs several K passes (4-bit codes: over at least one 32-row
+                          tile per SM) it runs the TMA-fed kernel once, with pairs of CTAs
+                          that take the two halves of the rows and walk the same tiles of
+                          W together. */
     AQ_KERNEL_QMM = 2  /* tensor-core GEMM kernel (tcgen05); any M >= 1 */
 } aq_kernel;
 
