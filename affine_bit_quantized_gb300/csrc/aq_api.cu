@@ -460,13 +460,15 @@ aq_status aq_matmul_nvfp4_bf16(const void *x, const uint32_t *w_packed, const ui
     a.timeout_ns = kTimeoutNs;
     aq_status st = record_cuda(status_ptr(&a.status));
     if (st != AQ_OK) return st;
-    // launches of up to 8 rows whose x fits the kernel's 64 KB staging room, each
-    // streaming W once
-    const int64_t rows = std::min<int64_t>(8, 32768 / K);
-    for (int64_t m0 = 0; m0 < M; m0 += rows) {
+    // each CTA takes up to 8 rows whose x fits the kernel's 64 KB staging room; one
+    // launch takes up to 8 such row blocks, on groups of CTAs that walk the same
+    // tiles together, so W comes from DRAM about once per launch
+    const int64_t rows = std::min<int64_t>(8, 32768 / K), per_launch = 8 * rows;
+    a.rows = (int)rows;
+    for (int64_t m0 = 0; m0 < M; m0 += per_launch) {
         a.x = static_cast<const uint16_t *>(x) + m0 * K;
         a.y = static_cast<uint16_t *>(y) + m0 * N;
-        a.M = (M - m0) < rows ? (M - m0) : rows;
+        a.M = (M - m0) < per_launch ? (M - m0) : per_launch;
         st = record_cuda(aq::launch_nvfp4_qmv(a));
         if (st != AQ_OK) return st;
     }

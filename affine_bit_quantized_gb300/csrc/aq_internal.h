@@ -88,6 +88,7 @@ struct Nvfp4Args {
     cudaStream_t stream;
     int *status;
     uint64_t timeout_ns;
+    int rows = 0;             // rows of x per CTA: groups of CTAs split M and walk the same tiles (0: M)
 };
 cudaError_t launch_nvfp4_qmv(const Nvfp4Args &a);
 

@@ -98,11 +98,23 @@ __device__ __forceinline__ void stage_x_fp16(uint32_t raw, uint32_t xinfo, int M
     consumer_sync();
 }
 
+// group: CTAs per group (1: each CTA takes all M rows).  With group G > 1, CTA
+// g of each group takes rows [g rows, (g + 1) rows) of x and y, and the G CTAs
+// walk the same tiles at the same pace, so that W mostly comes from DRAM once
+// and from L2 for the others.
 template <bool ONE_ROW, int NS>
 __global__ void __launch_bounds__(kThreads, 1)
 nvfp4_qmv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
                  const __nv_bfloat16 *__restrict__ x, __nv_bfloat16 *__restrict__ y, int M, int N, int K,
-                 float global_scale, unsigned long long timeout_ns, int *status) {
+                 float global_scale, unsigned long long timeout_ns, int *status, int group, int rows) {
+    // the CTA's place among those walking the tiles (a group counts once)
+    const int cta = (int)blockIdx.x / group, ncta = (int)gridDim.x / group;
+    if (group > 1) {
+        const int m0 = ((int)blockIdx.x % group) * rows;
+        x += (size_t)m0 * K;
+        y += (size_t)m0 * N;
+        M = M - m0 < rows ? M - m0 : rows;
+    }
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const Layout L = make_layout(M, K, NS);
@@ -123,7 +135,7 @@ nvfp4_qmv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KB = (K + kCodes - 1) / kCodes;   // stages per tile
     const int T = (N + kRows - 1) / kRows;
-    const int my_tiles = (int)blockIdx.x < T ? (T - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int my_tiles = cta < T ? (T - 1 - cta) / ncta + 1 : 0;
     const int items = my_tiles * KB;
 
     if (threadIdx.x == 0) {
@@ -148,7 +160,7 @@ nvfp4_qmv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             auto issue = [&](int it) {
-                const int slot = it % NS, tile = (int)blockIdx.x + (it / KB) * (int)gridDim.x, kb = it % KB;
+                const int slot = it % NS, tile = cta + (it / KB) * ncta, kb = it % KB;
                 const uint32_t dst = s_base + slot * kStage, fb = bar_full + 8 * slot;
                 // codes: one box of 8 chunks x 32 rows x 128 bytes; scales: 128 bytes x 32 rows
                 // (parts past the row's end read as zeros and still count)
@@ -190,7 +202,7 @@ nvfp4_qmv_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         // ------------------------------------------------------------ reducer
         bool ok = true;
         for (int t = 0; ok && t < my_tiles; ++t)
-            ok = reduce_tile<ONE_ROW>(tc, t, (int)blockIdx.x + t * (int)gridDim.x, M, N, y, lane, timeout_ns,
+            ok = reduce_tile<ONE_ROW>(tc, t, cta + t * ncta, M, N, y, lane, timeout_ns,
                                       abort_flag, nullptr, 0, 1, global_scale);
         if (!ok && lane == 0 && !*abort_flag) {
             atomicExch(status, (int)AQ_DEVICE_STATUS_TIMEOUT);
@@ -269,7 +281,10 @@ cudaError_t launch_nvfp4_qmv(const Nvfp4Args &a) {
         if (e != cudaSuccess) return e;
         g_sms[dev].store(sms, std::memory_order_relaxed);
     }
-    const int M = (int)a.M, N = (int)a.N, K = (int)a.K;
+    // M: rows of x per CTA; G CTAs per group of CTAs walking the same tiles
+    const int M = a.rows > 0 && a.rows < a.M ? a.rows : (int)a.M, N = (int)a.N, K = (int)a.K;
+    const int G = (int)((a.M + M - 1) / M);
+    if (G > sms) return cudaErrorInvalidConfiguration;
     const bool one = M == 1;
     // x beyond 32 KB (up to 64 KB): a 3-stage ring beside it
     const bool ns3 = (int64_t)M * K * 2 > kMaxXBytes;
@@ -290,7 +305,7 @@ cudaError_t launch_nvfp4_qmv(const Nvfp4Args &a) {
         return cudaErrorInvalidValue;
     const int T = (N + kRows - 1) / kRows;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)std::min(T, sms));
+    cfg.gridDim = dim3((unsigned)(G * std::min(T, sms / G)));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = a.stream;
@@ -300,8 +315,8 @@ cudaError_t launch_nvfp4_qmv(const Nvfp4Args &a) {
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, tw, ts, static_cast<const __nv_bfloat16 *>(a.x),
-                              static_cast<__nv_bfloat16 *>(a.y), M, N, K, a.global_scale,
-                              (unsigned long long)a.timeout_ns, a.status);
+                              static_cast<__nv_bfloat16 *>(a.y), (int)a.M, N, K, a.global_scale,
+                              (unsigned long long)a.timeout_ns, a.status, G, M);
 }
 
 }  // namespace aq

@@ -349,8 +349,10 @@ aq_status aq_gather_qmm_bf16(const void *x, const uint32_t *w_packed, const void
  *   global_scale  the tensor's fp32 scale (1.0f if it has none)
  *   y             bf16 [M, N], device, written; fp32 accumulation, one rounding
  *   M >= 0, N >= 1, K a multiple of 256 up to 32768 (M == 0 or N == 0:
- *   nothing launched).  Runs as launches of up to min(8, 32768 / K) rows of x,
- *   each streaming the weights once.  x, w_packed and scales_e4m3 16-byte aligned,
+ *   nothing launched).  Each CTA takes up to r = min(8, 32768 / K) rows of x;
+ *   one launch takes up to 8 r rows on groups of CTAs that split them and walk
+ *   the same tiles of W together (W read from DRAM about once per launch).
+ *   x, w_packed and scales_e4m3 16-byte aligned,
  *   y 2-byte aligned.  Errors: AQ_ERR_INVALID_ARG, AQ_ERR_UNSUPPORTED (sizes
  *   outside these limits), AQ_ERR_ALIGNMENT, AQ_ERR_CUDA.  Asynchronous;
  *   allocates nothing; deterministic.  AQ_FLAG_PDL is accepted in `flags`.

@@ -43,8 +43,10 @@ def check(dev, M, N, K, seed):
     (1, 64, 16384), (2, 77, 4096), (3, 129, 1280), (4, 50, 4096), (8, 64, 2048), (5, 31, 768),
     # x between 32 and 64 KB: the 3-stage ring beside it
     (8, 300, 4096), (2, 150, 14336), (1, 70, 32768), (7, 33, 4608), (3, 4096, 8192),
-    # more rows than one launch takes: launches of up to 8 rows (or fewer, for 64 KB of x)
+    # more rows than one CTA takes (8, or fewer for 64 KB of x): groups of CTAs that split the
+    # rows and walk the same tiles, 8 row blocks per launch
     (16, 200, 4096), (12, 65, 2048), (5, 40, 14336), (9, 128, 32768),
+    (16, 9760, 4096), (11, 3000, 14336), (20, 700, 32768), (70, 500, 4096),
 ])
 def test_nvfp4_shapes(dev, M, N, K):
     check(dev, M, N, K, 900 + M + N + K)
