@@ -1247,7 +1247,24 @@ template <int BITS>
 cudaError_t launch_gather_bits(const GatherArgs &g, int dev, int sms) {
     using C = Cfg<BITS, true>;
     // rows of W per CTA on the row-tile count without the experts' partial tiles
-    const int tn = qmm_tile_n(g.N, (g.R + C::kTileM - 1) / C::kTileM, sms);
+    int tn = qmm_tile_n(g.N, (g.R + C::kTileM - 1) / C::kTileM, sms);
+    // K split across a cluster of 2 (256-row W tiles) where it fills the last wave of
+    // CTAs better, on the expected row-tile count (each expert adds about half a
+    // partial tile) and allowing 7.5 % for the partial sums' exchange: the
+    // Mixtral-shaped down projection (4096 x 14336 experts) has 380 tiles of 224 rows,
+    // a third wave of 76 CTAs, against 640 half-K CTAs in five waves
+    int split = 1;
+    {
+        const int64_t est = (g.R + C::kTileM - 1) / C::kTileM + g.E / 2;
+        const int64_t steps = g.K / kGroup;
+        auto waves = [&](int64_t ctas) { return (ctas + sms - 1) / sms; };
+        const int64_t plain = waves((g.N + tn - 1) / tn * est) * steps * 20;
+        const int64_t halved = waves(2 * ((g.N + kTileN - 1) / kTileN) * est) * (steps / 2) * 43 / 2;
+        if (sms > 0 && g.K % (2 * kGroup * kSBGroups) == 0 && halved < plain) {
+            split = 2;
+            tn = kTileN;
+        }
+    }
     const int bi = BITS == 8 ? 1 : 0;
     if (!g_attr_done_grouped[bi][dev].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(qmm_kernel<BITS, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1276,17 +1293,22 @@ cudaError_t launch_gather_bits(const GatherArgs &g, int dev, int sms) {
         return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     const int64_t max_tiles = (g.R + C::kTileM - 1) / C::kTileM + g.E;
-    cfg.gridDim = dim3((unsigned)((N + tn - 1) / tn), (unsigned)max_tiles, 1);
+    cfg.gridDim = dim3((unsigned)((N + tn - 1) / tn), (unsigned)max_tiles, (unsigned)split);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = g.stream;
     // programmatic launch after the row gather: the plan (two launches back) is complete, and
-    // the kernel waits for the gathered rows before it reads them
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
+    // the kernel waits for the gathered rows before it reads them; with the K split, the two
+    // CTAs of an output tile form a cluster
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = (unsigned)split;
+    cfg.attrs = attr;
+    cfg.numAttrs = split > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS, true, true>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(g.y), R, N,
                               K, (unsigned long long)g.timeout_ns, g.status, (const int *)plan, 0, tn, 0);
 }

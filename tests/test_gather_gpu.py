@@ -107,14 +107,16 @@ def test_gather_bad_indices_reported_and_nothing_written(dev, bad):
     check(dev, T, E, N, K, 2, 14)                               # the context stays usable
 
 
-def test_gather_mixtral_shape_sampled(dev):
-    """Mixtral-8x7B-shaped expert matrices (8 experts, 14336 x 4096), 2048
-    tokens routed top-2: sampled outputs (plus the last row and column)
+@pytest.mark.parametrize("j", [0, 2])
+def test_gather_mixtral_shape_sampled(dev, j):
+    """Mixtral-8x7B-shaped expert matrices (8 experts; 14336 x 4096, and the
+    4096 x 14336 down projection, whose launch splits K across CTA pairs),
+    2048 tokens routed top-2: sampled outputs (plus the last row and column)
     against the oracle."""
-    T, E, (name, N, K), top_k = 2048, synth.MIXTRAL_EXPERTS, synth.MIXTRAL_EXPERT_MATS[0], synth.MIXTRAL_TOP_K
-    ew = synth.ExpertWeights(E, N, K, synth.seed_for(6, 0, 0))
-    x = synth.make_x(T, K, synth.seed_for(6, 0, 8))
-    lhs, rhs = synth.make_routing(T, E, top_k, synth.seed_for(6, 0, 9))
+    T, E, (name, N, K), top_k = 2048, synth.MIXTRAL_EXPERTS, synth.MIXTRAL_EXPERT_MATS[j], synth.MIXTRAL_TOP_K
+    ew = synth.ExpertWeights(E, N, K, synth.seed_for(6, j, 0))
+    x = synth.make_x(T, K, synth.seed_for(6, j, 8))
+    lhs, rhs = synth.make_routing(T, E, top_k, synth.seed_for(6, j, 9))
     got = from_dev_bf16(run(dev, x, ew, lhs, rhs))
     rng = np.random.default_rng(3)
     R = lhs.size
