@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
            const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_b,
            __nv_bfloat16 *__restrict__ y, int M, int N, int K, unsigned long long timeout_ns, int *status,
-           const int *__restrict__ plan, int skip_copy, int tn, int mfast) {
+           const int *__restrict__ plan, int skip_copy, int tn, int mfast, int tile0) {
     static_assert(!(PAIR && (GROUPED || XPRE)), "CTA pairs only on the plain matmul without x converted once");
     using C = Cfg<BITS, XPRE, TM, PAIR>;
     constexpr int kSBBytes = C::kSBBytes;
@@ -475,8 +475,9 @@ qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     int wrow0 = n0 + (int)prank * wrows;    // the first of them (in the stacked experts: expert * N + ...)
     int halves = C::kHalves;                 // M=128 accumulators in use
     if (GROUPED) {
-        if ((int)blockIdx.y >= __ldg(plan)) return;   // no tile: nothing set up yet
-        const int4 t = __ldg(reinterpret_cast<const int4 *>(plan + kPlanHeaderInts) + blockIdx.y);
+        const int ti = (int)blockIdx.y + tile0;   // this launch's tiles start at the plan's tile0
+        if (ti >= __ldg(plan)) return;              // no tile: nothing set up yet
+        const int4 t = __ldg(reinterpret_cast<const int4 *>(plan + kPlanHeaderInts) + ti);
         m0 = t.y;
         m_end = t.y + t.z;
         wrow0 = t.x * N + n0;
@@ -1127,7 +1128,7 @@ cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev, int split, int tn = kT
     cfg.numAttrs = (unsigned)na;
     return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS, false, XPRE, TM, PAIR>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(a.y), M,
                               N, K, (unsigned long long)a.timeout_ns, a.status, (const int *)nullptr,
-                              a.debug_skip_copy ? 1 : 0, tn, mfast);
+                              a.debug_skip_copy ? 1 : 0, tn, mfast, 0);
 }
 }  // namespace
 
@@ -1247,23 +1248,22 @@ template <int BITS>
 cudaError_t launch_gather_bits(const GatherArgs &g, int dev, int sms) {
     using C = Cfg<BITS, true>;
     // rows of W per CTA on the row-tile count without the experts' partial tiles
-    int tn = qmm_tile_n(g.N, (g.R + C::kTileM - 1) / C::kTileM, sms);
-    // K split across a cluster of 2 (256-row W tiles) where it fills the last wave of
-    // CTAs better, on the expected row-tile count (each expert adds about half a
-    // partial tile) and allowing 7.5 % for the partial sums' exchange: the
-    // Mixtral-shaped down projection (4096 x 14336 experts) has 380 tiles of 224 rows,
-    // a third wave of 76 CTAs, against 640 half-K CTAs in five waves
-    int split = 1;
+    const int tn = qmm_tile_n(g.N, (g.R + C::kTileM - 1) / C::kTileM, sms);
+    // Two launches: the row tiles that fill whole waves of CTAs, one CTA per output
+    // tile, then the rest with K split across the two CTAs of a cluster (256-row W
+    // tiles), so the last, partly filled wave takes half as long.  Counted on the
+    // expected row-tile count (each expert adds about half a partial tile); the
+    // plan's actual tiles decide which CTAs run (past the count, a CTA exits at once).
+    // The Mixtral-shaped down projection (4096 x 14336 experts): 16 row tiles x 19 W
+    // tiles of 224 rows in two full waves, then 4 x 16 x 2 half-K CTAs.
+    const int64_t max_tiles = (g.R + C::kTileM - 1) / C::kTileM + g.E;
+    int64_t full = 0;   // row tiles of the first launch
     {
-        const int64_t est = (g.R + C::kTileM - 1) / C::kTileM + g.E / 2;
-        const int64_t steps = g.K / kGroup;
-        auto waves = [&](int64_t ctas) { return (ctas + sms - 1) / sms; };
-        const int64_t plain = waves((g.N + tn - 1) / tn * est) * steps * 20;
-        const int64_t halved = waves(2 * ((g.N + kTileN - 1) / kTileN) * est) * (steps / 2) * 43 / 2;
-        if (sms > 0 && g.K % (2 * kGroup * kSBGroups) == 0 && halved < plain) {
-            split = 2;
-            tn = kTileN;
-        }
+        const int64_t est = std::min<int64_t>((g.R + C::kTileM - 1) / C::kTileM + g.E / 2, max_tiles);
+        const int64_t wt = (g.N + tn - 1) / tn;
+        full = sms > 0 ? (est * wt / sms) * sms / wt : max_tiles;
+        if (g.K % (2 * kGroup * kSBGroups) != 0) full = max_tiles;   // no even K split
+        if (full > max_tiles) full = max_tiles;
     }
     const int bi = BITS == 8 ? 1 : 0;
     if (!g_attr_done_grouped[bi][dev].load(std::memory_order_acquire)) {
@@ -1291,26 +1291,44 @@ cudaError_t launch_gather_bits(const GatherArgs &g, int dev, int sms) {
         !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, g.biases, (uint64_t)G, (uint64_t)E * N, (uint64_t)G * 2,
                    kSBGroups, (uint32_t)tn, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    cudaLaunchConfig_t cfg = {};
-    const int64_t max_tiles = (g.R + C::kTileM - 1) / C::kTileM + g.E;
-    cfg.gridDim = dim3((unsigned)((N + tn - 1) / tn), (unsigned)max_tiles, (unsigned)split);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = C::kSmemBytes;
-    cfg.stream = g.stream;
-    // programmatic launch after the row gather: the plan (two launches back) is complete, and
-    // the kernel waits for the gathered rows before it reads them; with the K split, the two
-    // CTAs of an output tile form a cluster
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = 1;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = (unsigned)split;
-    cfg.attrs = attr;
-    cfg.numAttrs = split > 1 ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS, true, true>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(g.y), R, N,
-                              K, (unsigned long long)g.timeout_ns, g.status, (const int *)plan, 0, tn, 0);
+    // programmatic launches: after the row gather, the plan (two launches back) is
+    // complete and the kernel waits for the gathered rows before it reads them; the
+    // second launch waits for the first in the same way.  With the K split, the two
+    // CTAs of an output tile form a cluster.
+    auto launch_part = [&](int64_t tile0, int64_t rows_tiles, int split, int tn_part,
+                           const CUtensorMap &twp, const CUtensorMap &tsp, const CUtensorMap &tbp) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)((N + tn_part - 1) / tn_part), (unsigned)rows_tiles, (unsigned)split);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = C::kSmemBytes;
+        cfg.stream = g.stream;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 1;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = (unsigned)split;
+        cfg.attrs = attr;
+        cfg.numAttrs = split > 1 ? 2 : 1;
+        return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS, true, true>, tx, twp, tsp, tbp,
+                                  static_cast<__nv_bfloat16 *>(g.y), R, N, K, (unsigned long long)g.timeout_ns,
+                                  g.status, (const int *)plan, 0, tn_part, 0, (int)tile0);
+    };
+    if (full > 0) {
+        e = launch_part(0, full, 1, tn, tw, ts, tb);
+        if (e != cudaSuccess || full == max_tiles) return e;
+    }
+    CUtensorMap tw2 = tw, ts2 = ts, tb2 = tb;   // W boxes of 256 rows for the split launch
+    if (tn != kTileN &&
+        (!encode_2d(&tw2, CU_TENSOR_MAP_DATA_TYPE_UINT32, g.w, (uint64_t)K * BITS / 32, (uint64_t)E * N,
+                    (uint64_t)K * BITS / 8, C::kRowWords, (uint32_t)kTileN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+         !encode_2d(&ts2, CU_TENSOR_MAP_DATA_TYPE_UINT16, g.scales, (uint64_t)G, (uint64_t)E * N, (uint64_t)G * 2,
+                    kSBGroups, (uint32_t)kTileN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+         !encode_2d(&tb2, CU_TENSOR_MAP_DATA_TYPE_UINT16, g.biases, (uint64_t)G, (uint64_t)E * N, (uint64_t)G * 2,
+                    kSBGroups, (uint32_t)kTileN, CU_TENSOR_MAP_SWIZZLE_NONE)))
+        return cudaErrorInvalidValue;
+    return launch_part(full, max_tiles - full, 2, kTileN, tw2, ts2, tb2);
 }
 
 }  // namespace
