@@ -125,3 +125,23 @@ def test_gather_mixtral_shape_sampled(dev, j):
     ye, yb = oracle.gather_matmul_sampled(x, ew.w_packed, ew.scales, ew.biases, lhs, rhs, N, K, ir, inn)
     rms = float(np.sqrt(np.mean(ye * ye)))
     assert_parity(got[ir, inn], yb, rms=rms, what="mixtral gather sampled")
+
+
+def test_gather_whole_waves_then_split_tail_8bit_sampled(dev):
+    """8-bit expert matrices (4096 x 4096, 8 experts, 2048 tokens top-2): the
+    row tiles that fill whole waves run in one launch, the remaining ones with
+    K split across CTA pairs; sampled outputs (plus both ends of the last row
+    tiles) against the oracle."""
+    T, E, N, K, top_k = 2048, 8, 4096, 4096, 2
+    ew = synth.ExpertWeights(E, N, K, 31, bits=8)
+    x = synth.make_x(T, K, 32)
+    lhs, rhs = synth.make_routing(T, E, top_k, 33)
+    got = from_dev_bf16(run(dev, x, ew, lhs, rhs))
+    rng = np.random.default_rng(5)
+    R = lhs.size
+    ir = np.concatenate([rng.integers(0, R, 3000), R - 1 - np.arange(64), [0, R - 1]])
+    inn = np.concatenate([rng.integers(0, N, 3064), [N - 1, 0]])
+    ye, yb = oracle.gather_matmul_sampled(x, ew.w_packed, ew.scales, ew.biases, lhs, rhs, N, K, ir, inn, bits=8)
+    rms = float(np.sqrt(np.mean(ye * ye)))
+    assert aq.aq_read_device_status(None) == aq.AQ_OK
+    assert_parity(got[ir, inn], yb, rms=rms, what="gather 8-bit two launches sampled")
