@@ -117,7 +117,6 @@ struct Cfg {
         (TM == 128 && !PAIR) ? (conv_fit(4) >= 2 ? 4 : 3)
         : PAIR ? (conv_fit(4) == conv_fit(2) ? 4 : conv_fit(3) == conv_fit(2) ? 3 : 2)
                : 2;
-    static constexpr int kFixedBytes = kRawStages * kRawStageBytes + kSBStages * 2 * kSBBytes + 512 + 16 + 1024;
     static constexpr int kConvStages = conv_fit(kRawStages);
     // barriers: raw_full[R], raw_empty[R], sb_full[2], sb_empty[2], conv_full[S], conv_empty[S], acc_done,
     // x_full[S] (the x copy of a converted stage has landed) and peer_full[S] (in a CTA pair: the
