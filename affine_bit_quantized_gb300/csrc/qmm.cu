@@ -84,11 +84,12 @@ constexpr int kSBStages = 2;
 // 128-row pairs at M = 256: 58 -> 65 us).  As many converted stages as fit (at
 // most 4) follow the raw and scale/bias stages.
 // PAIR (without XPRE): the CTA holds half of the W tile (see qmm_kernel).
-template <int BITS, bool XPRE = false, int TM = (BITS == 4 ? 256 : 128), bool PAIR = false>
+// TN: rows of W the stages are laid out for (kTileN, or 224: smaller stages, more of them).
+template <int BITS, bool XPRE = false, int TM = (BITS == 4 ? 256 : 128), bool PAIR = false, int TN = kTileN>
 struct Cfg {
     static constexpr int kTileM = TM;
     static constexpr int kHalves = kTileM / 128;                 // UMMA M=128 accumulators
-    static constexpr int kWRows = PAIR ? kTileN / 2 : kTileN;   // rows of W in this CTA's stages
+    static constexpr int kWRows = PAIR ? TN / 2 : TN;           // rows of W in this CTA's stages
     static constexpr int kBTileBytes = kWRows * 128;             // fp16 W, kWRows rows x 64 k
     static constexpr int kSBBytes = kWRows * kSBGroups * 2;      // scales (and again biases) per stage
     static constexpr bool kXInConv = XPRE || (BITS == 8 && TM == 256);
@@ -133,6 +134,7 @@ static_assert(Cfg<4>::kSmemBytes <= 232448 && Cfg<8>::kSmemBytes <= 232448 && Cf
                   Cfg<8, true>::kSmemBytes <= 232448 && Cfg<8, true, 256>::kSmemBytes <= 232448 &&
                   Cfg<4, false, 256, true>::kSmemBytes <= 232448 && Cfg<8, false, 128, true>::kSmemBytes <= 232448 &&
                   Cfg<8, false, 256, true>::kSmemBytes <= 232448 && Cfg<4, false, 128>::kSmemBytes <= 232448 &&
+                  Cfg<8, true, 256, false, 224>::kSmemBytes <= 232448 &&
                   Cfg<4, true, 128>::kSmemBytes <= 232448 && Cfg<4>::kConvStages >= 2 && Cfg<8>::kConvStages >= 2 &&
                   Cfg<8, true, 256>::kConvStages >= 2,
               "shared memory per CTA");
@@ -428,14 +430,14 @@ cudaError_t launch_plain(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaSt
 // converters bound the step and the pair takes a quarter of their work away
 // (M = 2048 on 4096 x 14336: 214 -> 201 us); with x converted once the MMAs
 // bound it and the pair's MMAs ran slower than two single-CTA ones.
-template <int BITS, bool GROUPED, bool XPRE, int TM = (BITS == 4 ? 256 : 128), bool PAIR = false>
+template <int BITS, bool GROUPED, bool XPRE, int TM = (BITS == 4 ? 256 : 128), bool PAIR = false, int TN = kTileN>
 __global__ void __launch_bounds__(kThreads, 1)
 qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
            const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_b,
            __nv_bfloat16 *__restrict__ y, int M, int N, int K, unsigned long long timeout_ns, int *status,
            const int *__restrict__ plan, int skip_copy, int tn, int mfast, int tile0) {
     static_assert(!(PAIR && (GROUPED || XPRE)), "CTA pairs only on the plain matmul without x converted once");
-    using C = Cfg<BITS, XPRE, TM, PAIR>;
+    using C = Cfg<BITS, XPRE, TM, PAIR, TN>;
     constexpr int kSBBytes = C::kSBBytes;
     constexpr int kConvStages = C::kConvStages, kRawStages = C::kRawStages;
     constexpr int kTileM = C::kTileM, kATileBytes = C::kATileBytes, kConvStageBytes = C::kConvStageBytes;
@@ -1058,14 +1060,17 @@ int qmm_split(const MatmulArgs &a, int dev) {
 // split: K split across a cluster of this many CTAs (qmm_split)
 // tn: rows of W per CTA (kTileN, or 224 without a K split; see qmm_tile_n)
 // PAIR: CTA pairs along M sharing each W tile (no K split; see qmm_kernel)
-template <int BITS, bool XPRE, int TM = (BITS == 4 ? 256 : 128), bool PAIR = false>
+template <int BITS, bool XPRE, int TM = (BITS == 4 ? 256 : 128), bool PAIR = false, int TN = kTileN>
 cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev, int split, int tn = kTileN) {
-    using C = Cfg<BITS, XPRE, TM, PAIR>;
+    using C = Cfg<BITS, XPRE, TM, PAIR, TN>;
+    static std::atomic<int> attr_done_tn[kMaxDevices];   // the instance laid out for 224 rows
     std::atomic<int> &attr_done =
-        PAIR ? g_attr_done_pair[(BITS == 8 ? 2 : 0) + (TM == 256 ? 1 : 0)][dev]
-             : g_attr_done[attr_slot<BITS, XPRE, TM>()][dev];
+        TN != kTileN ? attr_done_tn[dev]
+        : PAIR       ? g_attr_done_pair[(BITS == 8 ? 2 : 0) + (TM == 256 ? 1 : 0)][dev]
+                     : g_attr_done[attr_slot<BITS, XPRE, TM>()][dev];
+    if (TN != kTileN && tn != TN) return cudaErrorInvalidConfiguration;
     if (!attr_done.load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(qmm_kernel<BITS, false, XPRE, TM, PAIR>,
+        cudaError_t e = cudaFuncSetAttribute(qmm_kernel<BITS, false, XPRE, TM, PAIR, TN>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_done.store(1, std::memory_order_release);
@@ -1125,7 +1130,7 @@ cudaError_t launch_qmm_bits(const MatmulArgs &a, int dev, int split, int tn = kT
     }
     cfg.attrs = attr;
     cfg.numAttrs = (unsigned)na;
-    return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS, false, XPRE, TM, PAIR>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(a.y), M,
+    return cudaLaunchKernelEx(&cfg, qmm_kernel<BITS, false, XPRE, TM, PAIR, TN>, tx, tw, ts, tb, static_cast<__nv_bfloat16 *>(a.y), M,
                               N, K, (unsigned long long)a.timeout_ns, a.status, (const int *)nullptr,
                               a.debug_skip_copy ? 1 : 0, tn, mfast, 0);
 }
@@ -1166,8 +1171,14 @@ cudaError_t launch_qmm(const MatmulArgs &a) {
     // SMs (M = 2048 on 14336 x 4096: 743 -> 1205 TFLOP/s; on 4096 x 14336 one wave of
     // 128 such tiles against 1.7 waves of 128-row tiles)
     const int64_t tiles256 = ((a.N + kTileN - 1) / kTileN) * ((a.M + 255) / 256);
-    if (split == 1 && sms > 0 && 2 * tiles256 >= sms)
-        return launch_qmm_bits<8, true, 256>(a, dev, split, qmm_tile_n(a.N, (a.M + 255) / 256, sms));
+    if (split == 1 && sms > 0 && 2 * tiles256 >= sms) {
+        // where 224-row W tiles fill the waves better, stages laid out for 224 rows:
+        // three converted stages fit instead of two (M = 2048 on 4096 x 14336: 191.2 ->
+        // 188.3 us; forcing 224-row tiles on 14336 x 4096 adds a wave, 187 -> 225 us)
+        const int tn = qmm_tile_n(a.N, (a.M + 255) / 256, sms);
+        if (tn == 224) return launch_qmm_bits<8, true, 256, false, 224>(a, dev, split, 224);
+        return launch_qmm_bits<8, true, 256>(a, dev, split, tn);
+    }
     return launch_qmm_bits<8, true>(a, dev, split, tn128);
 }
 
