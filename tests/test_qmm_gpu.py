@@ -176,6 +176,7 @@ def test_qmm_pdl_flag_same_bits(dev, M, N, K, bits):
     (17, 64, 512, 4), (300, 700, 2048, 4), (256, 512, 4096, 4), (2048, 1024, 4096, 4),
     (129, 300, 1024, 8), (1000, 257, 4096, 8),
     (1024, 300, 512, 4), (640, 257, 512, 8), (2048, 4864, 512, 8),   # CTA pairs without the workspace
+    (2048, 4096, 512, 8), (2048, 4096, 14336, 8),   # with it: 224-row tiles, stages laid out for 224 rows
 ])
 def test_qmm_workspace_path_same_bits(dev, M, N, K, bits):
     """With a workspace, x is converted to fp16 once and copied straight into
